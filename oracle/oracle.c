@@ -1,0 +1,483 @@
+/*
+ * oracle.c -- plain, slow CPU oracle for the CSA / HCA attention hot path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the independent definition that the
+ * CUDA library is checked against.  Only the test suite, the smoke entry and
+ * the benchmark's CPU-baseline leg may load it; the product path never does.
+ * It shares no code, header, table or constant generator with the CUDA
+ * sources, and it includes nothing from them.
+ *
+ * Every quantity is computed in fp64 from the exact values of the stored
+ * inputs (bf16 or OCP FP8 E4M3 codes, decoded by the codecs below, which are
+ * written from the format definitions).  Loops follow the method's steps in
+ * order, with no blocking, fusion or reordering; OpenMP only spreads
+ * independent queries / blocks over cores.
+ *
+ * Sources (page title, section):
+ *  - "DeepSeek-V4: Towards Highly Efficient Million-Token Context
+ *    Intelligence" (hyper.ai paper page), Method, CSA paragraph: every m
+ *    tokens compressed into one entry with learnable compression weights and
+ *    positional biases; a Lightning Indexer picks the top-k compressed entries;
+ *    core attention is MQA over shared keys and values.
+ *  - same page, Method, HCA paragraph: m' >> m, no overlapping compression,
+ *    dense attention over all compressed entries; both branches add a
+ *    sliding-window attention branch.
+ *  - same page, Method: FP8 storage for non-RoPE KV, low precision indexer.
+ *  - "DeepSeek-V4" (aiboss88 news page), Technical Principles: indexer score
+ *    then top-k; sliding window and attention sink combined; FP8 range
+ *    extension for the low-precision indexer QK path.
+ *  - elamur.ai summary of the same paper, Summary: CSA "runs DeepSeek Sparse
+ *    Attention" -- read here as the indexer form
+ *    I(t,s) = sum_h w[t][h] * ReLU(q[t][h] . k[s]).
+ *  - same page, References [95] (attention sinks): a per-head sink logit that
+ *    joins the softmax denominator with a zero value vector.
+ *
+ * Readings where the pages are silent are listed in the design notes of the
+ * repository (compression operator, visibility rule, window extent, FP8
+ * scale rule, tie rule); each function below states the one it uses.
+ *
+ * Parity status: every function here is pinned by tests that do not re-type
+ * it (closed forms, library routines on special cases, exhaustive checks);
+ * see tests/test_oracle_pins.py.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORC_OK 0
+#define ORC_ERR_ARG 1
+#define ORC_ERR_RANGE 2
+#define ORC_ERR_NOMEM 3
+
+enum { ORC_BF16 = 0, ORC_FP8_E4M3 = 1 };
+
+int orc_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+/* ------------------------------------------------------------------------ */
+/* Number formats                                                           */
+/* ------------------------------------------------------------------------ */
+
+/* bf16: 1 sign bit, 8 exponent bits (bias 127), 7 stored mantissa bits; the
+ * upper half of an IEEE binary32. */
+double orc_bf16_to_f64(uint16_t bits) {
+  uint32_t u = ((uint32_t)bits) << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+/* Round a double to the nearest bf16, ties to even, in one step (no detour
+ * through binary32, which would round twice).  Results beyond the largest
+ * finite value become infinity, as IEEE round-to-nearest prescribes. */
+uint16_t orc_f64_to_bf16(double x) {
+  if (isnan(x)) return 0x7FC0;
+  uint16_t sign = signbit(x) ? 0x8000 : 0;
+  double a = fabs(x);
+  if (isinf(a)) return sign | 0x7F80;
+  if (a == 0.0) return sign;
+  int e;
+  frexp(a, &e);            /* a in [2^(e-1), 2^e) */
+  int E = e - 1;
+  int q = (E < -126) ? -133 : E - 7; /* exponent of one unit in the last place */
+  double r = rint(ldexp(a, -q));     /* default rounding mode: nearest, ties to even */
+  double v = ldexp(r, q);
+  if (v >= ldexp(1.0, 128)) return sign | 0x7F80;
+  float f = (float)v;                /* exact: v has at most 8 significant bits */
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  return sign | (uint16_t)(u >> 16);
+}
+
+/* OCP FP8 E4M3 ("E4M3FN"): 1 sign bit, 4 exponent bits (bias 7), 3 mantissa
+ * bits, no infinities; S.1111.111 is NaN; largest finite 1.75 * 2^8 = 448;
+ * exponent field 0 holds subnormals m * 2^-9. */
+double orc_e4m3_to_f64(uint8_t c) {
+  int s = c >> 7, E = (c >> 3) & 15, mnt = c & 7;
+  double v;
+  if (E == 15 && mnt == 7) return NAN;
+  if (E == 0)
+    v = ldexp((double)mnt, -9);
+  else
+    v = ldexp(1.0 + mnt / 8.0, E - 7);
+  return s ? -v : v;
+}
+
+/* Nearest E4M3 value, ties to even; magnitudes beyond 448 saturate to 448
+ * (the format has no infinity). */
+uint8_t orc_f64_to_e4m3(double x) {
+  if (isnan(x)) return 0x7F;
+  uint8_t s = signbit(x) ? 0x80 : 0;
+  double a = fabs(x);
+  if (a >= 448.0) return s | 0x7E;
+  if (a == 0.0) return s;
+  int e;
+  frexp(a, &e);
+  int E = e - 1;
+  int q = (E < -6) ? -9 : E - 3;
+  double v = ldexp(rint(ldexp(a, -q)), q);
+  if (v > 448.0) v = 448.0;
+  if (v == 0.0) return s;
+  frexp(v, &e);
+  E = e - 1;
+  if (E < -6) return s | (uint8_t)ldexp(v, 9);         /* subnormal */
+  int mnt = (int)(ldexp(v, -E) * 8.0 - 8.0);            /* (v / 2^E - 1) * 8 */
+  return s | (uint8_t)(((E + 7) << 3) | mnt);
+}
+
+void orc_bf16_decode_array(const uint16_t* in, double* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = orc_bf16_to_f64(in[i]);
+}
+void orc_bf16_encode_array(const double* in, uint16_t* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = orc_f64_to_bf16(in[i]);
+}
+void orc_e4m3_decode_array(const uint8_t* in, double* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = orc_e4m3_to_f64(in[i]);
+}
+void orc_e4m3_encode_array(const double* in, uint8_t* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = orc_f64_to_e4m3(in[i]);
+}
+
+/* Per-row FP8 quantisation of compressed entries.  Reading of the pages'
+ * "FP8 dynamic range" remark: one fp32 scale per entry, scale = amax / 448
+ * (amax = 0 gives scale 1), stored as binary32; each channel is coded as the
+ * nearest E4M3 value of y / scale, using the stored (binary32) scale. */
+void orc_quantize_e4m3_rows(const double* y, int64_t rows, int d, uint8_t* codes,
+                            float* scales) {
+  for (int64_t r = 0; r < rows; ++r) {
+    const double* yr = y + r * d;
+    double amax = 0.0;
+    for (int c = 0; c < d; ++c)
+      if (fabs(yr[c]) > amax) amax = fabs(yr[c]);
+    float sc = (amax > 0.0) ? (float)(amax / 448.0) : 1.0f;
+    scales[r] = sc;
+    for (int c = 0; c < d; ++c) codes[r * d + c] = orc_f64_to_e4m3(yr[c] / (double)sc);
+  }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Step a1: block compression                                               */
+/* ------------------------------------------------------------------------ */
+
+/* Compress blocks [block_begin, block_begin + n_blocks) of every sequence.
+ * Block j covers raw tokens j*m .. j*m+m-1 (non-overlapping).  For each
+ * channel c (the operator is the build's reading of "learnable compression
+ * weights and positional biases"):
+ *     g[i][c] = sum_e W[c][e] * x[j*m+i][e] + pos_bias[i][c]
+ *     a[.][c] = softmax over i of g[.][c]
+ *     y[j][c] = sum_i a[i][c] * x[j*m+i][c]
+ * raw: bf16 [B][raw_bstride] with token rows of d; W: bf16 [d][d] (row =
+ * output channel); pos_bias: fp32 [m][d].  y: fp64 [B][n_blocks][d]. */
+int orc_compress(const uint16_t* raw, int64_t raw_bstride, int B, int d, int m,
+                 int block_begin, int n_blocks, const uint16_t* W, const float* pos_bias,
+                 double* y) {
+  if (!raw || !W || !pos_bias || !y || B < 0 || d <= 0 || m <= 0 || block_begin < 0 ||
+      n_blocks < 0)
+    return ORC_ERR_ARG;
+  if ((int64_t)(block_begin + n_blocks) * m * d > raw_bstride) return ORC_ERR_RANGE;
+  double* Wd = (double*)malloc(sizeof(double) * (size_t)d * d);
+  if (!Wd) return ORC_ERR_NOMEM;
+  orc_bf16_decode_array(W, Wd, (int64_t)d * d);
+  int err = ORC_OK;
+#pragma omp parallel
+  {
+    double* x = (double*)malloc(sizeof(double) * (size_t)m * d);
+    double* g = (double*)malloc(sizeof(double) * (size_t)m);
+    if (!x || !g) {
+#pragma omp atomic write
+      err = ORC_ERR_NOMEM;
+    }
+#pragma omp for collapse(2) schedule(dynamic)
+    for (int b = 0; b < B; ++b) {
+      for (int jj = 0; jj < n_blocks; ++jj) {
+        if (!x || !g) continue;
+        int64_t j = block_begin + jj;
+        const uint16_t* xb = raw + (int64_t)b * raw_bstride + j * m * d;
+        orc_bf16_decode_array(xb, x, (int64_t)m * d);
+        double* yo = y + ((int64_t)b * n_blocks + jj) * d;
+        for (int c = 0; c < d; ++c) {
+          for (int i = 0; i < m; ++i) {
+            double s = 0.0;
+            for (int e = 0; e < d; ++e) s += Wd[(int64_t)c * d + e] * x[(int64_t)i * d + e];
+            g[i] = s + (double)pos_bias[(int64_t)i * d + c];
+          }
+          double gmax = g[0];
+          for (int i = 1; i < m; ++i)
+            if (g[i] > gmax) gmax = g[i];
+          double den = 0.0, num = 0.0;
+          for (int i = 0; i < m; ++i) {
+            double a = exp(g[i] - gmax);
+            den += a;
+            num += a * x[(int64_t)i * d + c];
+          }
+          yo[c] = num / den;
+        }
+      }
+    }
+    free(x);
+    free(g);
+  }
+  free(Wd);
+  return err;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Step a2: Lightning-Indexer scores                                        */
+/* ------------------------------------------------------------------------ */
+
+/* Visible compressed entries for a query at absolute position t (block j is
+ * visible iff it ends at or before t: j*m + m - 1 <= t), capped by the
+ * number of entries present. */
+static int64_t visible(int64_t t, int m, int64_t present) {
+  int64_t nv = (t + 1) / m;
+  return nv < present ? nv : present;
+}
+
+/* I(t,s) = sum_h w[t][h] * ReLU(q[t][h] . k[s]) for s < n_vis(t).
+ * bf16: q, k are bf16 codes.  FP8: q, k are E4M3 codes and
+ *     q[t][h] . k[s] = q_scale[t][h] * k_scale[s] * sum_d q8[d] * k8[d].
+ * q: [B][T][H][dI]; w, q_scale: [B][T][H]; k: [B][k_bstride] rows of dI;
+ * k_scale: [B][ks_bstride].  scores: fp64 [B][T][N_out]; entries at and
+ * beyond n_vis are -inf.  n_vis_out: [B][T]. */
+int orc_indexer_scores(const void* q, const float* q_scale, const float* w, const void* k,
+                       int64_t k_bstride, const float* k_scale, int64_t ks_bstride, int dtype,
+                       const int32_t* q_pos, const int32_t* n_cmp, int B, int T, int H,
+                       int dI, int m, int64_t N_out, double* scores, int32_t* n_vis_out) {
+  if (!q || !w || !k || !q_pos || !n_cmp || !scores || B < 0 || T < 0 || H <= 0 ||
+      dI <= 0 || m <= 0)
+    return ORC_ERR_ARG;
+  if (dtype != ORC_BF16 && dtype != ORC_FP8_E4M3) return ORC_ERR_ARG;
+  if (dtype == ORC_FP8_E4M3 && (!q_scale || !k_scale)) return ORC_ERR_ARG;
+  int err = ORC_OK;
+#pragma omp parallel
+  {
+    double* qv = (double*)malloc(sizeof(double) * (size_t)H * dI);
+    double* kv = (double*)malloc(sizeof(double) * (size_t)dI);
+#pragma omp for collapse(2) schedule(dynamic)
+    for (int b = 0; b < B; ++b) {
+      for (int t = 0; t < T; ++t) {
+        if (!qv || !kv) {
+#pragma omp atomic write
+          err = ORC_ERR_NOMEM;
+          continue;
+        }
+        int64_t bt = (int64_t)b * T + t;
+        int64_t tabs = q_pos[bt];
+        if (tabs < 0 || n_cmp[b] < 0 || n_cmp[b] > N_out) {
+#pragma omp atomic write
+          err = ORC_ERR_RANGE;
+          continue;
+        }
+        int64_t nv = visible(tabs, m, n_cmp[b]);
+        if (n_vis_out) n_vis_out[bt] = (int32_t)nv;
+        for (int h = 0; h < H; ++h)
+          for (int e = 0; e < dI; ++e) {
+            int64_t o = (bt * H + h) * dI + e;
+            qv[h * dI + e] = dtype == ORC_BF16 ? orc_bf16_to_f64(((const uint16_t*)q)[o])
+                                               : orc_e4m3_to_f64(((const uint8_t*)q)[o]);
+          }
+        double* out = scores + bt * N_out;
+        for (int64_t s = 0; s < nv; ++s) {
+          int64_t ko = (int64_t)b * k_bstride + s * dI;
+          for (int e = 0; e < dI; ++e)
+            kv[e] = dtype == ORC_BF16 ? orc_bf16_to_f64(((const uint16_t*)k)[ko + e])
+                                      : orc_e4m3_to_f64(((const uint8_t*)k)[ko + e]);
+          double I = 0.0;
+          for (int h = 0; h < H; ++h) {
+            double dot = 0.0;
+            for (int e = 0; e < dI; ++e) dot += qv[h * dI + e] * kv[e];
+            if (dtype == ORC_FP8_E4M3)
+              dot *= (double)q_scale[bt * H + h] * (double)k_scale[(int64_t)b * ks_bstride + s];
+            I += (double)w[bt * H + h] * (dot > 0.0 ? dot : 0.0);
+          }
+          out[s] = I;
+        }
+        for (int64_t s = nv; s < N_out; ++s) out[s] = -INFINITY;
+      }
+    }
+    free(qv);
+    free(kv);
+  }
+  return err;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Step a3: top-k selection                                                 */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+  double s;
+  int32_t i;
+} scored_t;
+
+/* Higher score first; equal scores: lower index first (the tie rule). */
+static int by_score_then_index(const void* pa, const void* pb) {
+  const scored_t* a = (const scored_t*)pa;
+  const scored_t* b = (const scored_t*)pb;
+  if (a->s > b->s) return -1;
+  if (a->s < b->s) return 1;
+  return (a->i > b->i) - (a->i < b->i);
+}
+static int ascending_i32(const void* pa, const void* pb) {
+  int32_t a = *(const int32_t*)pa, b = *(const int32_t*)pb;
+  return (a > b) - (a < b);
+}
+
+/* For each of Q queries: the min(k, n_vis) best entries by a full sort on
+ * (-score, index), returned in ascending index order and padded with -1. */
+int orc_topk(const double* scores, int64_t stride, const int32_t* n_vis, int64_t Q, int k,
+             int32_t* idx_out) {
+  if (!scores || !n_vis || !idx_out || Q < 0 || k < 0) return ORC_ERR_ARG;
+  int err = ORC_OK;
+#pragma omp parallel for schedule(dynamic)
+  for (int64_t qq = 0; qq < Q; ++qq) {
+    int64_t nv = n_vis[qq];
+    int32_t* out = idx_out + qq * k;
+    if (nv < 0 || nv > stride) {
+#pragma omp atomic write
+      err = ORC_ERR_RANGE;
+      continue;
+    }
+    scored_t* arr = (scored_t*)malloc(sizeof(scored_t) * (size_t)(nv > 0 ? nv : 1));
+    if (!arr) {
+#pragma omp atomic write
+      err = ORC_ERR_NOMEM;
+      continue;
+    }
+    for (int64_t s = 0; s < nv; ++s) {
+      arr[s].s = scores[qq * stride + s];
+      arr[s].i = (int32_t)s;
+    }
+    qsort(arr, (size_t)nv, sizeof(scored_t), by_score_then_index);
+    int64_t take = nv < k ? nv : k;
+    for (int64_t r = 0; r < take; ++r) out[r] = arr[r].i;
+    qsort(out, (size_t)take, sizeof(int32_t), ascending_i32);
+    for (int64_t r = take; r < k; ++r) out[r] = -1;
+    free(arr);
+  }
+  return err;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Steps a4 / a5: attention over compressed entries + window + sink          */
+/* ------------------------------------------------------------------------ */
+
+/* For query qq (sequence qb[qq], absolute position qt[qq]) and each head h,
+ * over the key set
+ *     S = { compressed rows sel[qq][i] for i < n_sel, sel >= 0 }
+ *       u { raw rows p in [max(0, t - window + 1), t] }
+ * (both parts count, even where a compressed entry summarises raw tokens that
+ * are also in the window):
+ *     l_j = scale * q_h . K_j
+ *     M   = max(max_j l_j, sink_h)
+ *     Z   = exp(sink_h - M) + sum_j exp(l_j - M)
+ *     o_h = sum_j exp(l_j - M) * V_j / Z,      lse_h = M + ln Z
+ * The sink term is absent when sink is NULL.  Empty S without a sink gives
+ * o = 0 and lse = -inf.  MQA: one K and one V stream shared by all heads.
+ * q: bf16 [Q][H][D].  k_cmp/v_cmp: bf16 [B][cmp_bstride] rows of D, with
+ * n_cmp_rows valid rows per sequence.  k_raw/v_raw: bf16 [B][raw_bstride]
+ * rows of D, row r holding absolute position raw_base + r, raw_rows rows.
+ * out: fp64 [Q][H][D]; lse: fp64 [Q][H]. */
+int orc_attend(const uint16_t* q, const int32_t* qb, const int32_t* qt, int64_t Q, int H, int D,
+               const uint16_t* k_cmp, const uint16_t* v_cmp, int64_t cmp_bstride,
+               int64_t n_cmp_rows, const int32_t* sel, int64_t sel_stride, int n_sel,
+               const uint16_t* k_raw, const uint16_t* v_raw, int64_t raw_bstride,
+               int64_t raw_base, int64_t raw_rows, int window, const float* sink, double scale,
+               double* out, double* lse) {
+  if (!q || !qb || !qt || !out || !lse || Q < 0 || H <= 0 || D <= 0 || n_sel < 0 ||
+      window < 0)
+    return ORC_ERR_ARG;
+  if (n_sel > 0 && (!sel || !k_cmp || !v_cmp)) return ORC_ERR_ARG;
+  if (window > 0 && (!k_raw || !v_raw)) return ORC_ERR_ARG;
+  int err = ORC_OK;
+  int64_t max_keys = (int64_t)n_sel + window;
+#pragma omp parallel
+  {
+    double* qv = (double*)malloc(sizeof(double) * (size_t)D);
+    const uint16_t** kr = (const uint16_t**)malloc(sizeof(void*) * (size_t)(max_keys + 1));
+    const uint16_t** vr = (const uint16_t**)malloc(sizeof(void*) * (size_t)(max_keys + 1));
+    double* l = (double*)malloc(sizeof(double) * (size_t)(max_keys + 1));
+    double* acc = (double*)malloc(sizeof(double) * (size_t)D);
+#pragma omp for schedule(dynamic)
+    for (int64_t qq = 0; qq < Q; ++qq) {
+      if (!qv || !kr || !vr || !l || !acc) {
+#pragma omp atomic write
+        err = ORC_ERR_NOMEM;
+        continue;
+      }
+      int64_t b = qb[qq], t = qt[qq];
+      int64_t n = 0;
+      int bad = 0;
+      for (int i = 0; i < n_sel; ++i) {
+        int64_t j = sel[qq * sel_stride + i];
+        if (j < 0) continue;
+        if (j >= n_cmp_rows) {
+          bad = 1;
+          break;
+        }
+        kr[n] = k_cmp + b * cmp_bstride + j * D;
+        vr[n] = v_cmp + b * cmp_bstride + j * D;
+        ++n;
+      }
+      int64_t p0 = t - window + 1;
+      if (p0 < 0) p0 = 0;
+      for (int64_t p = p0; window > 0 && p <= t; ++p) {
+        int64_t r = p - raw_base;
+        if (r < 0 || r >= raw_rows) {
+          bad = 1;
+          break;
+        }
+        kr[n] = k_raw + b * raw_bstride + r * D;
+        vr[n] = v_raw + b * raw_bstride + r * D;
+        ++n;
+      }
+      if (bad) {
+#pragma omp atomic write
+        err = ORC_ERR_RANGE;
+        continue;
+      }
+      for (int h = 0; h < H; ++h) {
+        for (int e = 0; e < D; ++e) qv[e] = orc_bf16_to_f64(q[(qq * H + h) * D + e]);
+        double M = -INFINITY;
+        for (int64_t j = 0; j < n; ++j) {
+          double s = 0.0;
+          for (int e = 0; e < D; ++e) s += qv[e] * orc_bf16_to_f64(kr[j][e]);
+          l[j] = scale * s;
+          if (l[j] > M) M = l[j];
+        }
+        double sk = sink ? (double)sink[h] : -INFINITY;
+        if (sink && sk > M) M = sk;
+        double* o = out + (qq * H + h) * D;
+        if (M == -INFINITY) { /* empty set, no sink */
+          for (int e = 0; e < D; ++e) o[e] = 0.0;
+          lse[qq * H + h] = -INFINITY;
+          continue;
+        }
+        double Z = sink ? exp(sk - M) : 0.0;
+        for (int e = 0; e < D; ++e) acc[e] = 0.0;
+        for (int64_t j = 0; j < n; ++j) {
+          double p = exp(l[j] - M);
+          Z += p;
+          for (int e = 0; e < D; ++e) acc[e] += p * orc_bf16_to_f64(vr[j][e]);
+        }
+        for (int e = 0; e < D; ++e) o[e] = acc[e] / Z;
+        lse[qq * H + h] = M + log(Z);
+      }
+    }
+    free(qv);
+    free(kr);
+    free(vr);
+    free(l);
+    free(acc);
+  }
+  return err;
+}
