@@ -1,0 +1,490 @@
+#!/usr/bin/env python
+"""Benchmark of the CSA / HCA hot path on B300 GPUs (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference] [--cpu-seconds S] [--no-cpu-baseline]
+
+A step is one pass of the workload's hot path over one batch of synthetic
+inputs resident in HBM (see synth.WORKLOADS; default: CSA decode at 128K
+context, batch 32).  The step is captured once in a CUDA graph per stage and
+replayed; L2 is flushed (a 2x-L2 write) before every timed step, outside the
+timed events.  ``value`` is whole-job queries/s (tokens/s for prefill) over
+all ranks; ``e2e`` is the same metric through the public Python API with the
+step's inputs copied from pinned host memory and its output copied back
+inside the timed region.  ``roofline`` rates the dominant stage (the indexer
+for CSA decode, the attention for HCA decode and prefill) against the
+measured peaks in MEASURED_PEAKS.json.  ``cpu_baseline`` times the CPU oracle
+on a bounded sample on this host.  ``--impl reference`` times only the CPU
+oracle, as the reference arm.
+
+Under torchrun each rank runs its own batch (weak scaling, no collective in
+the data path); rank 0 prints the line with the max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "CSA/HCA decode queries/s and achieved HBM GB/s vs peak at 128K and 1M context"
+DEFAULT_WORKLOAD = "csa_decode_128k"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+# ---------------------------------------------------------------- workload arithmetic
+
+def units(wl) -> int:
+    """Queries per step: decode = sequences, prefill = new tokens."""
+    return wl.B * wl.T
+
+
+def unit_name(wl) -> str:
+    return "tokens/s" if wl.kind == "csa_prefill" else "queries/s"
+
+
+def n_vis_decode(wl):
+    return [min(n // wl.m, n // wl.m) for n in wl.lens]
+
+
+def algorithmic(wl) -> dict:
+    """Algorithmic bytes (HBM) or FLOPs per stage per step, from the method's
+    own data movement: every byte a stage must read or write at least once."""
+    D, H, W = wl.D, wl.H, wl.W
+    qo = 2 * H * D * 2  # q in + out, bf16
+    if wl.kind == "hca_decode":
+        nb = sum((min(n // wl.m, n // wl.m) + min(W, n)) * 2 * D * 2 for n in wl.lens)
+        return {"attention": {"bytes": nb + wl.B * qo}}
+    if wl.kind == "csa_decode":
+        row = wl.d_I + 4 if wl.idx_fp8 else wl.d_I * 2
+        qrow = (wl.d_I + 4) if wl.idx_fp8 else wl.d_I * 2
+        idx_b = sum(nv * row for nv in n_vis_decode(wl)) + wl.B * (
+            wl.H_I * qrow + wl.H_I * 4 + wl.k * 4)
+        att_b = sum((min(wl.k, n // wl.m) + min(W, n)) * 2 * D * 2 for n in wl.lens) + wl.B * qo
+        st = {"indexer_topk": {"bytes": idx_b}, "attention": {"bytes": att_b}}
+        if wl.stream_compress:
+            per_seq = wl.m * (2 * D * 2 + wl.d_I * 2) + 2 * D * 2 + wl.d_I + 4
+            weights = (2 * D * D + wl.d_I * wl.d_I) * 2 + wl.m * (2 * D + wl.d_I) * 4
+            st["compress"] = {"bytes": wl.B * per_seq + weights}
+        return st
+    # prefill: contraction FLOPs of the indexer and the attention
+    nvis = [min(wl.N_cap, (wl.L + t + 1) // wl.m) for t in range(wl.T)]
+    idx_f = wl.B * sum(nvis) * wl.H_I * wl.d_I * 2
+    att_f = wl.B * wl.T * H * (wl.k + W) * D * 4
+    return {"indexer_topk": {"flops": idx_f}, "attention": {"flops": att_f},
+            "compress": {"flops": 3 * wl.B * wl.T * D * D * 2}}
+
+
+def dominant_stage(wl) -> str:
+    return {"csa_decode": "indexer_topk", "hca_decode": "attention",
+            "csa_prefill": "attention"}[wl.kind]
+
+
+# ---------------------------------------------------------------- environment
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def src_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "sparse_attention_28_b300", "csrc")
+    for n in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, n), "rb") as f:
+            h.update(n.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_record(wl_name: str, stage: str):
+    """DRAM bytes per launch of the stage from the committed ncu summary, or
+    None if absent or taken on other kernel sources."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    rec = d.get(wl_name, {}).get(stage)
+    if not rec or rec.get("src_hash") != src_hash():
+        return None
+    return rec.get("dram_bytes")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- CPU oracle leg
+
+class OracleRunner:
+    """The CPU oracle run on a bounded sample of the workload (``units`` per call)."""
+
+    def __init__(self, wl, inp: dict, n_units: int):
+        import oracle  # the oracle is test infrastructure: only this leg uses it
+        from oracle.feed import oracle_inputs
+        self.o = oracle
+        self.wl = wl
+        self.n = n_units
+        self.arr = oracle_inputs(wl, inp, n_units)
+
+    def __call__(self):
+        o, wl, a = self.o, self.wl, self.arr
+        if wl.kind == "hca_decode":
+            o.hca_decode(a["q"], a["k_cmp"], a["v_cmp"], a["n_cmp"], wl.m, a["k_win"], a["v_win"],
+                         a["seq_len"], wl.W, a["sink"], 1.0, a["raw_base"])
+            return
+        if wl.kind == "csa_decode":
+            if wl.stream_compress:
+                for s in ("k", "v", "idx"):
+                    y = o.compress(a["raw_new_" + s], *a["gate_" + s], wl.m, 0, 1)
+                    if s == "idx" and wl.idx_fp8:
+                        o.quantize_e4m3_rows(y)
+                    else:
+                        o.quantize_bf16(y)
+            sc, nv = o.indexer_scores(a["q_idx"], a["w"], a["k_idx"], a["q_pos"], a["n_cmp"],
+                                      wl.m, o.FP8_E4M3 if wl.idx_fp8 else o.BF16,
+                                      a.get("q_scale"), a.get("k_scale"))
+            idx = o.topk(sc, nv, wl.k)
+            o.csa_decode(a["q"], a["k_cmp"], a["v_cmp"], idx[:, 0, :], a["k_win"], a["v_win"],
+                         a["seq_len"], wl.W, a["sink"], 1.0, a["raw_base"])
+            return
+        # prefill sample: the sampled tokens' blocks, scores, top-k, attention
+        for s in ("k", "v", "idx"):
+            o.quantize_bf16(o.compress(a["raw_new_" + s], *a["gate_" + s], wl.m, 0,
+                                       a["n_blocks"]))
+        sc, nv = o.indexer_scores(a["q_idx"], a["w"], a["k_idx"], a["q_pos"], a["n_cmp"], wl.m)
+        idx = o.topk(sc, nv, wl.k)
+        o.csa_prefill(a["q"], a["k_cmp"], a["v_cmp"], idx, a["k_raw"], a["v_raw"], a["q_pos"],
+                      wl.W, a["sink"], 1.0, a["raw_base"])
+
+
+def oracle_sample_units(wl, cores: int) -> int:
+    if wl.kind == "csa_prefill":
+        return max(8, min(64, 2 * cores))
+    return max(1, min(wl.B, cores))
+
+
+def time_oracle(runner, budget_s: float):
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        runner()
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            return reps * runner.n / el, reps, el
+
+
+# ---------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--seed", type=int, default=0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    wl = synth.WORKLOADS[args.workload]
+    cfg = {"workload": wl.name, "kind": wl.kind, "B": wl.B, "L": wl.L, "T": wl.T, "m": wl.m,
+           "H": wl.H, "D": wl.D, "k": wl.k, "window": wl.W, "H_I": wl.H_I, "d_I": wl.d_I,
+           "indexer_dtype": "e4m3" if wl.idx_fp8 else "bf16",
+           "stream_compress": wl.stream_compress, "parallelism": f"replicas{world}"}
+
+    if args.impl == "reference":
+        return run_reference(args, wl, cfg, world, rank)
+
+    import torch.distributed as dist
+    import sparse_attention_28_b300 as csa
+    from sparse_attention_28_b300.steps import make_step
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    csa.lib()  # fail loudly now if the library is missing
+
+    inp = synth.make_inputs(wl, seed=args.seed + 7919 * rank, device=dev)
+    step = make_step(inp, dev)
+    stages = step.stages()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # one CUDA graph per stage, replayed back to back
+    graphs = []
+    cap = torch.cuda.Stream(device=dev)
+    cap.wait_stream(torch.cuda.current_stream())
+    for name, fn in stages:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            fn()
+        graphs.append((name, g))
+    torch.cuda.synchronize()
+    for _, g in graphs:
+        g.replay()
+    torch.cuda.synchronize()
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    n_st = len(graphs)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_st + 1)]
+           for _ in range(args.steps)]
+
+    sampler = ClockSampler(dev.index)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.25)
+    for i in range(args.steps):
+        flush.zero_()
+        evs[i][0].record(stream)
+        for s, (_, g) in enumerate(graphs):
+            g.replay()
+            evs[i][s + 1].record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    if world > 1:
+        dist.barrier()
+
+    step_ms = [evs[i][0].elapsed_time(evs[i][n_st]) for i in range(args.steps)]
+    stage_ms = {name: statistics.mean(evs[i][s].elapsed_time(evs[i][s + 1])
+                                      for i in range(args.steps))
+                for s, (name, _) in enumerate(graphs)}
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = units(wl) * world * args.steps / (total_ms / 1e3)
+
+    # e2e: public API, inputs from pinned host memory, result back to host
+    e2e = run_e2e(args, wl, step, dev, flush, world, dist)
+
+    # roofline of the dominant stage
+    peaks, peaks_src = load_peaks()
+    alg = algorithmic(wl)
+    dom = dominant_stage(wl)
+    dom_s = stage_ms[dom] / 1e3
+    if "bytes" in alg[dom]:
+        achieved = alg[dom]["bytes"] / dom_s / 1e9
+        peak = float(peaks["hbm_gbs"])
+        roof = {"bound": "hbm", "unit": "GB/s"}
+    else:
+        achieved = alg[dom]["flops"] / dom_s / 1e12
+        peak = float(peaks["bf16_tflops"])
+        roof = {"bound": "tensor", "unit": "TFLOP/s"}
+    roof.update({"achieved": round(achieved, 2), "peak": peak, "frac": round(achieved / peak, 4),
+                 "traffic": traffic_record(wl.name, dom), "stage": dom,
+                 "stage_ms": round(stage_ms[dom], 5), "peak_source": peaks_src + " (burst)"})
+
+    stage_report = {}
+    for name, ms in stage_ms.items():
+        r = {"ms": round(ms, 5)}
+        a = alg.get(name, {})
+        if "bytes" in a:
+            r["GB/s"] = round(a["bytes"] / (ms / 1e3) / 1e9, 1)
+        if "flops" in a:
+            r["TFLOP/s"] = round(a["flops"] / (ms / 1e3) / 1e12, 1)
+        stage_report[name] = r
+    step_bytes = sum(a.get("bytes", 0) for a in alg.values())
+    if step_bytes:
+        stage_report["step_GB/s"] = round(step_bytes / (ms_per_step / 1e3) / 1e9, 1)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args, wl, inp)
+
+    launches = launches_per_step(wl, csa) * args.steps
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": unit_name(wl), "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3-indexer+bf16" if wl.idx_fp8 else "bf16", "data": "synthetic",
+        "config": dict(cfg, l2="flushed before every step (2x L2 write, untimed)",
+                       timing="CUDA graph per stage, CUDA events"),
+        "roofline": roof, "stages": stage_report, "cpu_baseline": cpu, "e2e": e2e,
+        "clocks": clocks, "gpu_launches": launches,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def launches_per_step(wl, csa) -> int:
+    """Kernels of the library launched per step (memsets not counted)."""
+    n = 0
+    q = units(wl)
+    if wl.kind in ("csa_decode", "csa_prefill"):
+        n += 3 * ((q + 255) // 256)  # score, mark, select per chunk of 256 queries
+        n += 1 + (csa.attn_workspace(wl.B, wl.T, wl.H, wl.k + wl.W) > 0)
+        if wl.stream_compress or wl.kind == "csa_prefill":
+            n += 3
+    else:
+        n += 1 + (csa.attn_workspace(wl.B, 1, wl.H, wl.N_cap + wl.W) > 0)
+    return n
+
+
+def run_e2e(args, wl, step, dev, flush, world, dist):
+    """Per step: pinned host -> device copy of the step's inputs, the step via
+    the public API (eager), device -> pinned host copy of its output."""
+    names = {"csa_decode": ["q", "q_idx", "w", "q_scale", "seq_len"],
+             "hca_decode": ["q", "seq_len"],
+             "csa_prefill": ["q", "q_idx", "w", "q_pos"]}[wl.kind]
+    pairs = []
+    for n in names:
+        d = getattr(step, n, None)
+        if d is None:
+            continue
+        h = torch.empty(d.shape, dtype=d.dtype, pin_memory=True)
+        h.copy_(d)
+        pairs.append((h, d))
+    out_h = torch.empty(step.out.shape, dtype=step.out.dtype, pin_memory=True)
+    h2d = sum(h.numel() * h.element_size() for h, _ in pairs)
+    d2h = out_h.numel() * out_h.element_size()
+    stream = torch.cuda.current_stream(dev)
+    times = []
+    for i in range(args.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for h, d in pairs:
+            d.copy_(h, non_blocking=True)
+        out = step()
+        out_h.copy_(out, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1))
+    total = sum(times)
+    if world > 1:
+        t = torch.tensor([total], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total = float(t.item())
+    return {"value": round(units(wl) * world * args.steps / (total / 1e3), 2),
+            "unit": unit_name(wl), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(total / args.steps, 5)}
+
+
+def cpu_baseline(args, wl, inp):
+    import oracle
+    cores = oracle.num_threads()
+    n = oracle_sample_units(wl, cores)
+    runner = OracleRunner(wl, inp, n)
+    value, reps, el = time_oracle(runner, args.cpu_seconds)
+    what = "tokens" if wl.kind == "csa_prefill" else "sequences"
+    return {"value": round(value, 4), "unit": unit_name(wl), "cores": cores, "kind": "oracle",
+            "sample": f"{n} {what} of the workload, full step each, repeated {reps}x "
+                      f"in {el:.1f} s (fp64 C oracle, OpenMP)"}
+
+
+def run_reference(args, wl, cfg, world, rank):
+    """The reference arm: the CPU oracle as it stands, on host cores."""
+    if rank != 0:
+        return
+    import oracle
+    cores = oracle.num_threads()
+    inp = synth.make_inputs(wl, seed=args.seed, device="cpu")
+    n = oracle_sample_units(wl, cores)
+    runner = OracleRunner(wl, inp, n)
+    for _ in range(args.warmup):
+        runner()
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        runner()
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = n * args.steps / total
+    what = "tokens" if wl.kind == "csa_prefill" else "sequences"
+    line = {
+        "metric": METRIC, "value": round(value, 4), "unit": unit_name(wl), "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * total / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic", "config": cfg, "impl": "reference",
+        "cpu_baseline": {"value": round(value, 4), "unit": unit_name(wl), "cores": cores,
+                         "kind": "oracle",
+                         "sample": f"{n} {what} of the workload per step (fp64 C oracle)"},
+        "e2e": {"value": round(value, 4), "unit": unit_name(wl), "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,198 @@
+/*
+ * csa.h -- C ABI of libcsa.so: the CSA / HCA attention hot path on one GPU.
+ *
+ * The method (page "DeepSeek-V4: Towards Highly Efficient Million-Token
+ * Context Intelligence", hyper.ai, Method):
+ *   CSA compresses every m raw KV tokens into one entry, scores the entries
+ *   with a Lightning Indexer, keeps the top-k, and runs MQA attention over
+ *   them (plus a sliding window of raw tokens and an attention sink, aiboss88
+ *   DeepSeek-V4 page, Technical Principles).  HCA compresses by m' >> m
+ *   without overlap and attends densely over every compressed entry, also
+ *   with the window branch.
+ *
+ * Conventions for every call
+ *   - All tensor pointers are DEVICE pointers owned by the caller; nothing is
+ *     allocated, freed or retained by the library.  Scratch memory is passed in
+ *     (`ws`, sized by the *_workspace queries).
+ *   - Tensors are row-major and contiguous inside a sequence; the distance
+ *     between sequences ("bstride") is given in ELEMENTS of the tensor's type.
+ *     bf16 tensors and their bstrides must be 16-byte aligned (bstride a
+ *     multiple of 8 elements); FP8 tensors 16-byte aligned (bstride a multiple
+ *     of 16); fp32 / int32 tensors 4-byte aligned.
+ *   - Each call is asynchronous and stream-ordered on `stream` (a
+ *     cudaStream_t; NULL = legacy default stream).  No call synchronises the
+ *     device or the host.  Calls with disjoint outputs and workspaces may run
+ *     concurrently on different streams.
+ *   - Host-side validation runs first; on any error nothing is launched and a
+ *     non-zero status is returned.
+ *   - `err_word` (optional, device int32) receives bit flags OR-ed in by the
+ *     kernels when they meet an input they cannot honour (they skip it and
+ *     never trap): CSA_EW_BAD_INDEX (a top-k index outside [-1, N_cap)),
+ *     CSA_EW_BAD_POSITION (a position or length outside the cache or < 0).
+ *     The word is never cleared by the library; the caller reads it when it
+ *     chooses.
+ *   - Numbers: bf16 inputs, fp32 accumulation, bf16 outputs rounded to
+ *     nearest even.  FP8 is OCP E4M3 ("e4m3fn") with one fp32 scale per row.
+ */
+#ifndef CSA_H_
+#define CSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define CSA_API __attribute__((visibility("default")))
+#else
+#define CSA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* status codes */
+#define CSA_OK 0
+#define CSA_ERR_INVALID_ARG 1 /* null pointer, bad shape / stride / alignment, k > N_cap ... */
+#define CSA_ERR_UNSUPPORTED 2 /* a size or dtype this build has no kernel for */
+#define CSA_ERR_WORKSPACE 3   /* ws too small (or NULL while needed) */
+#define CSA_ERR_CUDA 4        /* a launch failed; the CUDA error was consumed */
+#define CSA_ERR_TIMEOUT 5     /* reserved for bounded device-side waits */
+
+/* err_word bits */
+#define CSA_EW_BAD_INDEX 1
+#define CSA_EW_BAD_POSITION 2
+
+/* element types */
+#define CSA_BF16 0
+#define CSA_FP8_E4M3 1
+
+/* Human-readable name of a status code (static string, never NULL). */
+CSA_API const char* csa_status_str(int status);
+
+/* Version of this ABI (bumped on any signature change). */
+CSA_API int csa_abi_version(void);
+
+/* ------------------------------------------------------------------------
+ * a1. Block compression (CSA ratio m, HCA ratio m').
+ *
+ * Source: hyper.ai DeepSeek-V4 page, Method -- "compresses every m tokens
+ * into a single entry using learnable compression weights and positional
+ * biases"; HCA: "without overlapping compression".  The operator is this
+ * library's reading of that sentence: for block j of sequence b, channel c,
+ *     g[i][c] = sum_e W[c][e] * x[j*m+i][e] + pos_bias[i][c],  i < m
+ *     y[j][c] = sum_i softmax_i(g[.][c])[i] * x[j*m+i][c]
+ * Blocks [block_begin, block_begin + n_blocks) of every sequence are written.
+ *
+ *   raw       bf16 [B][raw_bstride]: token rows of d; block j reads rows
+ *             j*m .. j*m+m-1.
+ *   W         bf16 [d][d] (row = output channel), pos_bias fp32 [m][d].
+ *   out       out_dtype == CSA_BF16: bf16 [B][out_bstride], row j of d.
+ *             out_dtype == CSA_FP8_E4M3: E4M3 bytes, row j of d, plus
+ *             out_scale fp32 [B][scale_bstride]: scale = max_c |y| / 448
+ *             (1 when all zero), code = nearest-even E4M3 of y / scale,
+ *             saturating at 448.
+ *   d in {64, 128}; 1 <= m <= 256.
+ * ---------------------------------------------------------------------- */
+CSA_API int csa_compress_kv(const void* raw, int64_t raw_bstride, int B, int d, int m,
+                    int block_begin, int n_blocks, const void* W, const float* pos_bias,
+                    void* out, int64_t out_bstride, int out_dtype, float* out_scale,
+                    int64_t scale_bstride, int32_t* err_word, void* stream);
+
+/* ------------------------------------------------------------------------
+ * a2 + a3. Lightning-Indexer scores and exact top-k.
+ *
+ * Sources: hyper.ai DeepSeek-V4 page, Method ("A Lightning Indexer then
+ * selects the top-k compressed KV entries"); aiboss88 page, Technical
+ * Principles (index score, then top-k; FP8 range for the low-precision
+ * indexer QK path); elamur.ai page, Summary ("runs DeepSeek Sparse
+ * Attention") -- read as the score
+ *     I(t,s) = sum_h w[t][h] * ReLU(q[t][h] . k[s]),    s < n_vis(t)
+ *     n_vis(t) = min(n_cmp[b], floor((t + 1) / m))   (block-causal)
+ * FP8: q[t][h] . k[s] = q_scale[t][h] * k_scale[s] * sum_d q8[d] * k8[d].
+ * Selection: the min(k, n_vis) largest scores, ties to the lower index,
+ * written in ascending index order and padded with -1.
+ *
+ *   q_idx     [B][T][H_I][d_I] (bf16, or E4M3 bytes with q_scale fp32
+ *             [B][T][H_I]); w fp32 [B][T][H_I].
+ *   k_idx     [B][k_bstride] rows of d_I (bf16 or E4M3 bytes), with
+ *             k_scale fp32 [B][ks_bstride] for E4M3.
+ *   q_pos     int32 [B][T] absolute positions; n_cmp int32 [B] entries present
+ *             (<= N_cap).
+ *   topk_idx  int32 [B][T][k] out; topk_score fp32 [B][T][k] out (optional,
+ *             the selected entries' scores, -inf in padded slots).
+ *   ws        csa_indexer_topk_workspace(B, T, N_cap, k) bytes.
+ *   H_I == 4, d_I == 64; 1 <= k <= N_cap.
+ * ---------------------------------------------------------------------- */
+CSA_API size_t csa_indexer_topk_workspace(int B, int T, int N_cap, int k);
+CSA_API int csa_indexer_topk(const void* q_idx, const float* q_scale, const float* w,
+                     const void* k_idx, int64_t k_bstride, const float* k_scale,
+                     int64_t ks_bstride, int idx_dtype, const int32_t* q_pos,
+                     const int32_t* n_cmp, int B, int T, int H_I, int d_I, int N_cap, int m,
+                     int k, int32_t* topk_idx, float* topk_score, void* ws, size_t ws_bytes,
+                     int32_t* err_word, void* stream);
+
+/* ------------------------------------------------------------------------
+ * a4 / a5 / a6. Attention over compressed entries + window + sink.
+ *
+ * Sources: hyper.ai DeepSeek-V4 page, Method (MQA core attention with shared
+ * keys and values over the top-k entries; HCA dense over all entries; both
+ * with a sliding-window branch); aiboss88 page, Technical Principles
+ * (sliding window and attention sink); elamur.ai page, References [20]
+ * (flash-decoding: split the keys, merge partial results by log-sum-exp).
+ * For query token t of sequence b and head h, over the key set
+ *     S = {compressed rows selected for t} u {raw rows max(0,t-window+1)..t}
+ *     l_j = softmax_scale * q_h . K_j,  M = max(max_j l_j, sink_h)
+ *     Z   = exp(sink_h - M) + sum_j exp(l_j - M)
+ *     out_h = sum_j exp(l_j - M) V_j / Z,   lse_h = M + ln Z
+ * (no sink term when sink == NULL; empty S without sink gives out = 0,
+ * lse = -inf).  K and V are shared by all H heads (MQA).  They may alias
+ * (k_cmp == v_cmp, k_raw == v_raw).
+ *
+ *   q         bf16 [B][H][D] (decode) or [B][T][H][D] (prefill).
+ *   k_cmp, v_cmp  bf16 [B][cmp_bstride], rows of D; N_cap rows per sequence.
+ *   k_raw, v_raw  bf16 [B][raw_bstride], row p = absolute position p;
+ *             raw_cap rows per sequence.
+ *   seq_len   int32 [B] (decode: t = seq_len - 1, the token's own K/V is
+ *             already in the raw cache); q_pos int32 [B][T] (prefill).
+ *   out       bf16, same shape as q; lse fp32 [B][(T)][H] (optional).
+ *   ws        csa_attn_workspace(B, T, H, n_keys_max) bytes, where n_keys_max
+ *             is the largest key-set size (k + window for CSA; the largest
+ *             n_vis + window for HCA).  Zero bytes may be needed.
+ *   H in {16, 32, 64, 128}; D == 128.
+ * ---------------------------------------------------------------------- */
+CSA_API size_t csa_attn_workspace(int B, int T, int H, int n_keys_max);
+
+/* CSA decode: one query token per sequence; compressed rows = topk_idx[b][.]
+ * (entries < 0 are skipped). */
+CSA_API int csa_sparse_attn_decode(const void* q, const void* k_cmp, const void* v_cmp,
+                           int64_t cmp_bstride, int N_cap, const int32_t* topk_idx, int k,
+                           const void* k_raw, const void* v_raw, int64_t raw_bstride,
+                           int64_t raw_cap, const int32_t* seq_len, int window,
+                           const float* sink, float softmax_scale, int B, int H, int D,
+                           void* out, float* lse, void* ws, size_t ws_bytes, int32_t* err_word,
+                           void* stream);
+
+/* CSA prefill: T query tokens per sequence at positions q_pos; compressed
+ * rows = topk_idx[b][t][.]. */
+CSA_API int csa_sparse_attn_prefill(const void* q, const void* k_cmp, const void* v_cmp,
+                            int64_t cmp_bstride, int N_cap, const int32_t* topk_idx, int k,
+                            const void* k_raw, const void* v_raw, int64_t raw_bstride,
+                            int64_t raw_cap, const int32_t* q_pos, int window,
+                            const float* sink, float softmax_scale, int B, int T, int H, int D,
+                            void* out, float* lse, void* ws, size_t ws_bytes,
+                            int32_t* err_word, void* stream);
+
+/* HCA decode: compressed rows 0 .. n_vis-1 with
+ * n_vis = min(n_cmp[b], floor(seq_len[b] / m_prime)). */
+CSA_API int hca_dense_attn_decode(const void* q, const void* k_cmp, const void* v_cmp,
+                          int64_t cmp_bstride, int N_cap, const int32_t* n_cmp, int m_prime,
+                          const void* k_raw, const void* v_raw, int64_t raw_bstride,
+                          int64_t raw_cap, const int32_t* seq_len, int window,
+                          const float* sink, float softmax_scale, int B, int H, int D,
+                          void* out, float* lse, void* ws, size_t ws_bytes, int32_t* err_word,
+                          void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CSA_H_ */

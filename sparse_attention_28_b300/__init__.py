@@ -1,0 +1,294 @@
+"""CSA / HCA hybrid-attention hot path on one B300 GPU.
+
+A thin ctypes binding over ``libcsa.so`` (C ABI in ``include/csa.h``).  Every
+step of the path runs in the library's CUDA kernels; this module only checks
+tensors, allocates outputs / workspaces with torch on the tensors' device, and
+passes pointers plus the current CUDA stream.  There is no CPU fallback: if
+the library is missing, every call raises.
+
+Calls (same names as the C ABI, without the prefix where it reads better):
+
+* :func:`compress_kv`            -- csa_compress_kv
+* :func:`indexer_topk`           -- csa_indexer_topk
+* :func:`sparse_attn_decode`     -- csa_sparse_attn_decode
+* :func:`sparse_attn_prefill`    -- csa_sparse_attn_prefill
+* :func:`hca_dense_attn_decode`  -- hca_dense_attn_decode
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libcsa.so")
+
+CSA_BF16 = 0
+CSA_FP8_E4M3 = 1
+EW_BAD_INDEX = 1
+EW_BAD_POSITION = 2
+
+# exported symbols of the C ABI (include/csa.h)
+ABI_SYMBOLS = (
+    "csa_status_str", "csa_abi_version", "csa_compress_kv", "csa_indexer_topk_workspace",
+    "csa_indexer_topk", "csa_attn_workspace", "csa_sparse_attn_decode",
+    "csa_sparse_attn_prefill", "hca_dense_attn_decode",
+)
+
+_lock = threading.Lock()
+_lib = None
+
+
+class CsaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {lib().csa_status_str(status).decode()} (status {status})")
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libcsa.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"libcsa.so not found at {LIB_PATH}; build it with "
+                    "`python -m sparse_attention_28_b300._build` (there is no CPU fallback)")
+            L = ctypes.CDLL(LIB_PATH)
+            P, I, I64, F, SZ = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
+                                ctypes.c_size_t)
+            L.csa_status_str.argtypes = [I]
+            L.csa_status_str.restype = ctypes.c_char_p
+            L.csa_abi_version.restype = I
+            L.csa_compress_kv.argtypes = [P, I64, I, I, I, I, I, P, P, P, I64, I, P, I64, P, P]
+            L.csa_compress_kv.restype = I
+            L.csa_indexer_topk_workspace.argtypes = [I, I, I, I]
+            L.csa_indexer_topk_workspace.restype = SZ
+            L.csa_indexer_topk.argtypes = [P, P, P, P, I64, P, I64, I, P, P, I, I, I, I, I, I, I,
+                                           P, P, P, SZ, P, P]
+            L.csa_indexer_topk.restype = I
+            L.csa_attn_workspace.argtypes = [I, I, I, I]
+            L.csa_attn_workspace.restype = SZ
+            L.csa_sparse_attn_decode.argtypes = [P, P, P, I64, I, P, I, P, P, I64, I64, P, I, P,
+                                                 F, I, I, I, P, P, P, SZ, P, P]
+            L.csa_sparse_attn_decode.restype = I
+            L.csa_sparse_attn_prefill.argtypes = [P, P, P, I64, I, P, I, P, P, I64, I64, P, I, P,
+                                                  F, I, I, I, I, P, P, P, SZ, P, P]
+            L.csa_sparse_attn_prefill.restype = I
+            L.hca_dense_attn_decode.argtypes = [P, P, P, I64, I, P, I, P, P, I64, I64, P, I, P, F,
+                                                I, I, I, P, P, P, SZ, P, P]
+            L.hca_dense_attn_decode.restype = I
+            _lib = L
+    return _lib
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise CsaError(status, what)
+
+
+def _need(cond: bool, msg: str):
+    if not cond:
+        raise ValueError(msg)
+
+
+def _cuda(t, name, dtype=None):
+    _need(t is not None and t.is_cuda, f"{name} must be a CUDA tensor")
+    if dtype is not None:
+        _need(t.dtype == dtype, f"{name} must be {dtype}, got {t.dtype}")
+    return t
+
+
+def _bstride(t) -> int:
+    """Elements between sequences of a [B, rows, d] tensor with contiguous rows."""
+    _need(t.dim() == 3 and t.stride(2) == 1 and t.stride(1) == t.shape[2],
+          "tensor rows must be contiguous")
+    return t.stride(0)
+
+
+def _ws(nbytes: int, device, ws):
+    if nbytes == 0:
+        return None, 0
+    if ws is not None:
+        _need(ws.numel() * ws.element_size() >= nbytes, "workspace too small")
+        return ws, ws.numel() * ws.element_size()
+    return torch.empty(nbytes, dtype=torch.uint8, device=device), nbytes
+
+
+# ---------------------------------------------------------------- a1
+
+def compress_kv(raw, W, pos_bias, m: int, block_begin: int, n_blocks: int, out,
+                out_scale=None, err_word=None):
+    """Compress blocks [block_begin, block_begin+n_blocks) of every sequence.
+
+    raw: bf16 [B, L_cap, d]; W: bf16 [d, d]; pos_bias: fp32 [m, d];
+    out: bf16 [B, N_cap, d] or uint8 [B, N_cap, d] (E4M3 codes, then
+    out_scale fp32 [B, N_cap] is required).  Writes in place; returns out.
+    """
+    _cuda(raw, "raw", torch.bfloat16)
+    _cuda(W, "W", torch.bfloat16)
+    _cuda(pos_bias, "pos_bias", torch.float32)
+    _cuda(out, "out")
+    B, _, d = raw.shape
+    fp8 = out.dtype in (torch.uint8, torch.float8_e4m3fn)
+    _need(fp8 or out.dtype == torch.bfloat16, "out must be bf16 or E4M3 bytes")
+    _need(W.is_contiguous() and pos_bias.is_contiguous(), "W, pos_bias must be contiguous")
+    if fp8:
+        _cuda(out_scale, "out_scale", torch.float32)
+        _need(out_scale.dim() == 2 and out_scale.stride(1) == 1, "out_scale [B, N_cap]")
+    st = lib().csa_compress_kv(
+        _p(raw), _bstride(raw), B, d, m, block_begin, n_blocks, _p(W), _p(pos_bias), _p(out),
+        _bstride(out), CSA_FP8_E4M3 if fp8 else CSA_BF16, _p(out_scale) if fp8 else None,
+        out_scale.stride(0) if fp8 else 0, _p(err_word), _stream(raw.device))
+    _check(st, "csa_compress_kv")
+    return out
+
+
+# ---------------------------------------------------------------- a2 + a3
+
+def indexer_topk(q_idx, w, k_idx, q_pos, n_cmp, m: int, k: int, q_scale=None, k_scale=None,
+                 return_scores: bool = False, out=None, ws=None, err_word=None):
+    """Top-k compressed entries per query token by Lightning-Indexer score.
+
+    q_idx: [B, T, 4, 64] bf16 (or uint8 E4M3 codes with q_scale fp32 [B, T, 4]);
+    w: fp32 [B, T, 4]; k_idx: [B, N_cap, 64] bf16 (or uint8 with k_scale fp32
+    [B, N_cap]); q_pos: int32 [B, T]; n_cmp: int32 [B].
+    Returns int32 [B, T, k] (ascending, -1 padded) [, fp32 scores [B, T, k]].
+    """
+    _cuda(q_idx, "q_idx")
+    _cuda(k_idx, "k_idx")
+    _cuda(w, "w", torch.float32)
+    _cuda(q_pos, "q_pos", torch.int32)
+    _cuda(n_cmp, "n_cmp", torch.int32)
+    fp8 = q_idx.dtype in (torch.uint8, torch.float8_e4m3fn)
+    _need(fp8 == (k_idx.dtype in (torch.uint8, torch.float8_e4m3fn)), "q/k dtypes differ")
+    if not fp8:
+        _need(q_idx.dtype == torch.bfloat16 and k_idx.dtype == torch.bfloat16, "bf16 expected")
+    _need(q_idx.is_contiguous() and w.is_contiguous() and q_pos.is_contiguous(),
+          "q_idx, w, q_pos must be contiguous")
+    B, T, H_I, d_I = q_idx.shape
+    N_cap = k_idx.shape[1]
+    dev = q_idx.device
+    if fp8:
+        _cuda(q_scale, "q_scale", torch.float32)
+        _cuda(k_scale, "k_scale", torch.float32)
+        _need(q_scale.is_contiguous() and k_scale.stride(1) == 1, "scale layout")
+    idx = out if out is not None else torch.empty((B, T, k), dtype=torch.int32, device=dev)
+    scores = torch.empty((B, T, k), dtype=torch.float32, device=dev) if return_scores else None
+    nbytes = lib().csa_indexer_topk_workspace(B, T, N_cap, k)
+    wsb, wsn = _ws(nbytes, dev, ws)
+    st = lib().csa_indexer_topk(
+        _p(q_idx), _p(q_scale) if fp8 else None, _p(w), _p(k_idx), _bstride(k_idx),
+        _p(k_scale) if fp8 else None, k_scale.stride(0) if fp8 else 0,
+        CSA_FP8_E4M3 if fp8 else CSA_BF16, _p(q_pos), _p(n_cmp), B, T, H_I, d_I, N_cap, m, k,
+        _p(idx), _p(scores), _p(wsb), wsn, _p(err_word), _stream(dev))
+    _check(st, "csa_indexer_topk")
+    return (idx, scores) if return_scores else idx
+
+
+def indexer_topk_workspace(B: int, T: int, N_cap: int, k: int) -> int:
+    return int(lib().csa_indexer_topk_workspace(B, T, N_cap, k))
+
+
+# ---------------------------------------------------------------- a4 / a5 / a6
+
+def attn_workspace(B: int, T: int, H: int, n_keys_max: int) -> int:
+    return int(lib().csa_attn_workspace(B, T, H, n_keys_max))
+
+
+def _attn_common(q, k_cmp, v_cmp, k_raw, v_raw, sink):
+    _cuda(q, "q", torch.bfloat16)
+    _need(q.is_contiguous(), "q must be contiguous")
+    _cuda(k_cmp, "k_cmp", torch.bfloat16)
+    _cuda(v_cmp, "v_cmp", torch.bfloat16)
+    _need(k_cmp.stride() == v_cmp.stride() and k_cmp.shape == v_cmp.shape,
+          "k_cmp and v_cmp must share shape and strides")
+    if k_raw is not None:
+        _cuda(k_raw, "k_raw", torch.bfloat16)
+        _cuda(v_raw, "v_raw", torch.bfloat16)
+        _need(k_raw.stride() == v_raw.stride() and k_raw.shape == v_raw.shape,
+              "k_raw and v_raw must share shape and strides")
+    if sink is not None:
+        _cuda(sink, "sink", torch.float32)
+
+
+def sparse_attn_decode(q, k_cmp, v_cmp, topk_idx, k_raw, v_raw, seq_len, window: int, sink,
+                       softmax_scale: float = 1.0, return_lse: bool = False, out=None, ws=None,
+                       err_word=None):
+    """CSA decode attention.  q: bf16 [B, H, 128]; k_cmp/v_cmp: bf16 [B, N_cap, 128];
+    topk_idx: int32 [B, k]; k_raw/v_raw: bf16 [B, L_cap, 128]; seq_len: int32 [B];
+    sink: fp32 [H] or None.  Returns bf16 [B, H, 128] [, lse fp32 [B, H]]."""
+    _attn_common(q, k_cmp, v_cmp, k_raw, v_raw, sink)
+    _cuda(topk_idx, "topk_idx", torch.int32)
+    _cuda(seq_len, "seq_len", torch.int32)
+    topk_idx = topk_idx.reshape(q.shape[0], -1)
+    _need(topk_idx.is_contiguous(), "topk_idx must be contiguous")
+    B, H, D = q.shape
+    k = topk_idx.shape[1]
+    dev = q.device
+    o = out if out is not None else torch.empty_like(q)
+    lse = torch.empty((B, H), dtype=torch.float32, device=dev) if return_lse else None
+    wsb, wsn = _ws(attn_workspace(B, 1, H, k + window), dev, ws)
+    st = lib().csa_sparse_attn_decode(
+        _p(q), _p(k_cmp), _p(v_cmp), _bstride(k_cmp), k_cmp.shape[1], _p(topk_idx), k,
+        _p(k_raw), _p(v_raw), _bstride(k_raw) if k_raw is not None else 0,
+        k_raw.shape[1] if k_raw is not None else 0, _p(seq_len), window, _p(sink),
+        softmax_scale, B, H, D, _p(o), _p(lse), _p(wsb), wsn, _p(err_word), _stream(dev))
+    _check(st, "csa_sparse_attn_decode")
+    return (o, lse) if return_lse else o
+
+
+def sparse_attn_prefill(q, k_cmp, v_cmp, topk_idx, k_raw, v_raw, q_pos, window: int, sink,
+                        softmax_scale: float = 1.0, return_lse: bool = False, out=None, ws=None,
+                        err_word=None):
+    """CSA prefill attention.  q: bf16 [B, T, H, 128]; topk_idx: int32 [B, T, k];
+    q_pos: int32 [B, T].  Returns bf16 [B, T, H, 128] [, lse fp32 [B, T, H]]."""
+    _attn_common(q, k_cmp, v_cmp, k_raw, v_raw, sink)
+    _cuda(topk_idx, "topk_idx", torch.int32)
+    _cuda(q_pos, "q_pos", torch.int32)
+    _need(topk_idx.is_contiguous() and q_pos.is_contiguous(), "contiguous index tensors")
+    B, T, H, D = q.shape
+    k = topk_idx.shape[-1]
+    dev = q.device
+    o = out if out is not None else torch.empty_like(q)
+    lse = torch.empty((B, T, H), dtype=torch.float32, device=dev) if return_lse else None
+    wsb, wsn = _ws(attn_workspace(B, T, H, k + window), dev, ws)
+    st = lib().csa_sparse_attn_prefill(
+        _p(q), _p(k_cmp), _p(v_cmp), _bstride(k_cmp), k_cmp.shape[1], _p(topk_idx), k,
+        _p(k_raw), _p(v_raw), _bstride(k_raw) if k_raw is not None else 0,
+        k_raw.shape[1] if k_raw is not None else 0, _p(q_pos), window, _p(sink), softmax_scale,
+        B, T, H, D, _p(o), _p(lse), _p(wsb), wsn, _p(err_word), _stream(dev))
+    _check(st, "csa_sparse_attn_prefill")
+    return (o, lse) if return_lse else o
+
+
+def hca_dense_attn_decode(q, k_cmp, v_cmp, n_cmp, m_prime: int, k_raw, v_raw, seq_len,
+                          window: int, sink, softmax_scale: float = 1.0,
+                          return_lse: bool = False, out=None, ws=None, err_word=None):
+    """HCA decode attention over compressed entries 0 .. n_vis-1 plus the window."""
+    _attn_common(q, k_cmp, v_cmp, k_raw, v_raw, sink)
+    _cuda(n_cmp, "n_cmp", torch.int32)
+    _cuda(seq_len, "seq_len", torch.int32)
+    B, H, D = q.shape
+    N_cap = k_cmp.shape[1]
+    dev = q.device
+    o = out if out is not None else torch.empty_like(q)
+    lse = torch.empty((B, H), dtype=torch.float32, device=dev) if return_lse else None
+    wsb, wsn = _ws(attn_workspace(B, 1, H, N_cap + window), dev, ws)
+    st = lib().hca_dense_attn_decode(
+        _p(q), _p(k_cmp), _p(v_cmp), _bstride(k_cmp), N_cap, _p(n_cmp), m_prime, _p(k_raw),
+        _p(v_raw), _bstride(k_raw) if k_raw is not None else 0,
+        k_raw.shape[1] if k_raw is not None else 0, _p(seq_len), window, _p(sink),
+        softmax_scale, B, H, D, _p(o), _p(lse), _p(wsb), wsn, _p(err_word), _stream(dev))
+    _check(st, "hca_dense_attn_decode")
+    return (o, lse) if return_lse else o

@@ -1,0 +1,302 @@
+// api.cu -- the extern "C" boundary of libcsa.so (declared in include/csa.h).
+// Validates every argument on the host, then launches the kernels on the
+// caller's stream.  Nothing here allocates device memory or synchronises.
+#include <mutex>
+#include <set>
+#include <tuple>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace csa {
+
+cudaError_t ensure_smem_attr(const void* func, int bytes) {
+  static std::mutex mu;
+  static std::set<std::tuple<const void*, int, int>> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.count(std::make_tuple(func, dev, bytes))) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.insert(std::make_tuple(func, dev, bytes));
+  return e;
+}
+
+namespace {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+inline int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return CSA_OK;
+  return CSA_ERR_CUDA;
+}
+
+constexpr int kD = 128;
+
+bool heads_supported(int H) { return H == 16 || H == 32 || H == 64 || H == 128; }
+
+// Shared validation of the attention calls.
+int check_attention_common(const void* q, const void* k_cmp, const void* v_cmp,
+                           int64_t cmp_bstride, int N_cap, const void* k_raw, const void* v_raw,
+                           int64_t raw_bstride, int64_t raw_cap, int window, const float* sink,
+                           int B, int T, int H, int D, const void* out, const float* lse) {
+  if (B < 0 || T < 0 || H <= 0 || D <= 0 || window < 0 || N_cap < 0 || raw_cap < 0)
+    return CSA_ERR_INVALID_ARG;
+  if (D != kD || !heads_supported(H)) return CSA_ERR_UNSUPPORTED;
+  if (B == 0 || T == 0) return CSA_OK;
+  if (!q || !out || !aligned16(q) || !aligned16(out)) return CSA_ERR_INVALID_ARG;
+  if (N_cap > 0) {
+    if (!k_cmp || !v_cmp || !aligned16(k_cmp) || !aligned16(v_cmp)) return CSA_ERR_INVALID_ARG;
+    if (cmp_bstride % 8 != 0 || cmp_bstride < (int64_t)N_cap * D) return CSA_ERR_INVALID_ARG;
+  }
+  if (window > 0) {
+    if (!k_raw || !v_raw || !aligned16(k_raw) || !aligned16(v_raw)) return CSA_ERR_INVALID_ARG;
+    if (raw_bstride % 8 != 0 || raw_bstride < raw_cap * D) return CSA_ERR_INVALID_ARG;
+  }
+  if (sink && !aligned4(sink)) return CSA_ERR_INVALID_ARG;
+  if (lse && !aligned4(lse)) return CSA_ERR_INVALID_ARG;
+  return CSA_OK;
+}
+
+}  // namespace
+}  // namespace csa
+
+using namespace csa;
+
+extern "C" {
+
+const char* csa_status_str(int status) {
+  switch (status) {
+    case CSA_OK: return "CSA_OK";
+    case CSA_ERR_INVALID_ARG: return "CSA_ERR_INVALID_ARG: invalid argument";
+    case CSA_ERR_UNSUPPORTED: return "CSA_ERR_UNSUPPORTED: size or dtype not supported";
+    case CSA_ERR_WORKSPACE: return "CSA_ERR_WORKSPACE: workspace too small";
+    case CSA_ERR_CUDA: return "CSA_ERR_CUDA: CUDA launch failed";
+    case CSA_ERR_TIMEOUT: return "CSA_ERR_TIMEOUT: bounded device wait expired";
+    default: return "unknown status";
+  }
+}
+
+int csa_abi_version(void) { return 1; }
+
+// ---------------------------------------------------------------- a1
+int csa_compress_kv(const void* raw, int64_t raw_bstride, int B, int d, int m, int block_begin,
+                    int n_blocks, const void* W, const float* pos_bias, void* out,
+                    int64_t out_bstride, int out_dtype, float* out_scale, int64_t scale_bstride,
+                    int32_t* err_word, void* stream) {
+  (void)err_word;
+  if (B < 0 || d <= 0 || m <= 0 || block_begin < 0 || n_blocks < 0) return CSA_ERR_INVALID_ARG;
+  if (out_dtype != CSA_BF16 && out_dtype != CSA_FP8_E4M3) return CSA_ERR_UNSUPPORTED;
+  if ((d != 64 && d != 128) || m > 256) return CSA_ERR_UNSUPPORTED;
+  if (B == 0 || n_blocks == 0) return CSA_OK;
+  if (!raw || !W || !pos_bias || !out) return CSA_ERR_INVALID_ARG;
+  if (!aligned16(raw) || !aligned16(W) || !aligned4(pos_bias)) return CSA_ERR_INVALID_ARG;
+  const int64_t end_block = (int64_t)block_begin + n_blocks;
+  if (raw_bstride % 8 != 0 || end_block * m * d > raw_bstride) return CSA_ERR_INVALID_ARG;
+  if (end_block * d > out_bstride) return CSA_ERR_INVALID_ARG;
+  if (out_dtype == CSA_FP8_E4M3) {
+    if (!out_scale || !aligned4(out_scale) || end_block > scale_bstride) return CSA_ERR_INVALID_ARG;
+  }
+  CompressArgs a;
+  a.raw = reinterpret_cast<const bf16*>(raw);
+  a.raw_bstride = raw_bstride;
+  a.B = B;
+  a.d = d;
+  a.m = m;
+  a.block_begin = block_begin;
+  a.n_blocks = n_blocks;
+  a.W = reinterpret_cast<const bf16*>(W);
+  a.pos_bias = pos_bias;
+  a.out = out;
+  a.out_bstride = out_bstride;
+  a.fp8 = out_dtype == CSA_FP8_E4M3;
+  a.out_scale = out_scale;
+  a.scale_bstride = scale_bstride;
+  return cuda_status(launch_compress(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+// ---------------------------------------------------------------- a2 + a3
+size_t csa_indexer_topk_workspace(int B, int T, int N_cap, int k) {
+  (void)k;
+  if (B <= 0 || T <= 0 || N_cap <= 0) return 0;
+  return indexer_topk_workspace_bytes(B * T, N_cap);
+}
+
+int csa_indexer_topk(const void* q_idx, const float* q_scale, const float* w, const void* k_idx,
+                     int64_t k_bstride, const float* k_scale, int64_t ks_bstride, int idx_dtype,
+                     const int32_t* q_pos, const int32_t* n_cmp, int B, int T, int H_I, int d_I,
+                     int N_cap, int m, int k, int32_t* topk_idx, float* topk_score, void* ws,
+                     size_t ws_bytes, int32_t* err_word, void* stream) {
+  if (B < 0 || T < 0 || N_cap < 0 || m <= 0 || k <= 0) return CSA_ERR_INVALID_ARG;
+  if (idx_dtype != CSA_BF16 && idx_dtype != CSA_FP8_E4M3) return CSA_ERR_UNSUPPORTED;
+  if (H_I != 4 || d_I != 64) return CSA_ERR_UNSUPPORTED;
+  if (N_cap > kMaxNcap) return CSA_ERR_UNSUPPORTED;
+  if (B == 0 || T == 0) return CSA_OK;
+  if (N_cap == 0 || k > N_cap) return CSA_ERR_INVALID_ARG;
+  if ((int64_t)B * T > (1 << 30)) return CSA_ERR_UNSUPPORTED;
+  const bool fp8 = idx_dtype == CSA_FP8_E4M3;
+  if (!q_idx || !w || !k_idx || !q_pos || !n_cmp || !topk_idx) return CSA_ERR_INVALID_ARG;
+  if (!aligned16(q_idx) || !aligned16(k_idx) || !aligned4(w) || !aligned4(q_pos) ||
+      !aligned4(n_cmp) || !aligned4(topk_idx))
+    return CSA_ERR_INVALID_ARG;
+  if (topk_score && !aligned4(topk_score)) return CSA_ERR_INVALID_ARG;
+  if (fp8) {
+    if (!q_scale || !k_scale || !aligned4(q_scale) || !aligned4(k_scale))
+      return CSA_ERR_INVALID_ARG;
+    if (k_bstride % 16 != 0 || ks_bstride < N_cap) return CSA_ERR_INVALID_ARG;
+  } else if (k_bstride % 8 != 0) {
+    return CSA_ERR_INVALID_ARG;
+  }
+  if (k_bstride < (int64_t)N_cap * d_I) return CSA_ERR_INVALID_ARG;
+  const size_t need = indexer_topk_workspace_bytes(B * T, N_cap);
+  if (!ws || ws_bytes < need || !aligned16(ws)) return CSA_ERR_WORKSPACE;
+  IndexerArgs a;
+  a.q = q_idx;
+  a.q_scale = q_scale;
+  a.w = w;
+  a.keys = k_idx;
+  a.k_bstride = k_bstride;
+  a.k_scale = k_scale;
+  a.ks_bstride = ks_bstride;
+  a.fp8 = fp8;
+  a.q_pos = q_pos;
+  a.n_cmp = n_cmp;
+  a.T = T;
+  a.n_query = B * T;
+  a.N_cap = N_cap;
+  a.m = m;
+  a.k = k;
+  a.err = err_word;
+  a.topk_idx = topk_idx;
+  a.topk_score = topk_score;
+  return cuda_status(launch_indexer_topk(a, ws, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+// ---------------------------------------------------------------- a4 / a5 / a6
+size_t csa_attn_workspace(int B, int T, int H, int n_keys_max) {
+  if (B <= 0 || T <= 0 || H <= 0 || n_keys_max <= 0) return 0;
+  return attn_workspace_bytes(B * T, H, n_keys_max);
+}
+
+static int run_attention(AttnArgs& a, void* ws, size_t ws_bytes, void* stream) {
+  if (a.n_query == 0) return CSA_OK;
+  const size_t need = attn_workspace_bytes(a.n_query, a.H, a.n_keys_max);
+  if (need > 0 && (!ws || ws_bytes < need || !aligned16(ws))) return CSA_ERR_WORKSPACE;
+  return cuda_status(launch_attention(a, ws, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+static void fill_common(AttnArgs& a, const void* q, const void* k_cmp, const void* v_cmp,
+                        int64_t cmp_bstride, int N_cap, const void* k_raw, const void* v_raw,
+                        int64_t raw_bstride, int64_t raw_cap, int window, const float* sink,
+                        float softmax_scale, int H, void* out, float* lse, int32_t* err_word) {
+  a.q = reinterpret_cast<const bf16*>(q);
+  a.k_cmp = reinterpret_cast<const bf16*>(k_cmp);
+  a.v_cmp = reinterpret_cast<const bf16*>(v_cmp);
+  a.cmp_bstride = cmp_bstride;
+  a.N_cap = N_cap;
+  // with no window, raw pointers may be NULL: point the (never dereferenced)
+  // raw source at the compressed cache so address arithmetic stays defined
+  a.k_raw = reinterpret_cast<const bf16*>(window > 0 ? k_raw : k_cmp);
+  a.v_raw = reinterpret_cast<const bf16*>(window > 0 ? v_raw : v_cmp);
+  a.raw_bstride = window > 0 ? raw_bstride : 0;
+  a.raw_cap = raw_cap;
+  a.window = window;
+  a.sink = sink;
+  a.scale_log2 = softmax_scale * kLog2e;
+  a.H = H;
+  a.out = reinterpret_cast<bf16*>(out);
+  a.lse = lse;
+  a.err = err_word;
+  a.part_o = nullptr;
+  a.part_lse = nullptr;
+  a.n_cmp = nullptr;
+  a.m_prime = 1;
+  a.dense = 0;
+  a.sel = nullptr;
+  a.sel_count = 0;
+  a.sel_stride = 0;
+}
+
+int csa_sparse_attn_decode(const void* q, const void* k_cmp, const void* v_cmp,
+                           int64_t cmp_bstride, int N_cap, const int32_t* topk_idx, int k,
+                           const void* k_raw, const void* v_raw, int64_t raw_bstride,
+                           int64_t raw_cap, const int32_t* seq_len, int window, const float* sink,
+                           float softmax_scale, int B, int H, int D, void* out, float* lse,
+                           void* ws, size_t ws_bytes, int32_t* err_word, void* stream) {
+  int st = check_attention_common(q, k_cmp, v_cmp, cmp_bstride, N_cap, k_raw, v_raw, raw_bstride,
+                                  raw_cap, window, sink, B, 1, H, D, out, lse);
+  if (st != CSA_OK || B == 0) return st;
+  if (k < 0 || (k > 0 && (!topk_idx || !aligned4(topk_idx) || N_cap <= 0))) return CSA_ERR_INVALID_ARG;
+  if (!seq_len || !aligned4(seq_len)) return CSA_ERR_INVALID_ARG;
+  if (k + window <= 0) return CSA_ERR_INVALID_ARG;
+  AttnArgs a;
+  fill_common(a, q, k_cmp, v_cmp, cmp_bstride, N_cap, k_raw, v_raw, raw_bstride, raw_cap, window,
+              sink, softmax_scale, H, out, lse, err_word);
+  a.sel = topk_idx;
+  a.sel_count = k;
+  a.sel_stride = k;
+  a.pos = seq_len;
+  a.pos_is_len = 1;
+  a.T = 1;
+  a.n_query = B;
+  a.n_keys_max = k + window;
+  return run_attention(a, ws, ws_bytes, stream);
+}
+
+int csa_sparse_attn_prefill(const void* q, const void* k_cmp, const void* v_cmp,
+                            int64_t cmp_bstride, int N_cap, const int32_t* topk_idx, int k,
+                            const void* k_raw, const void* v_raw, int64_t raw_bstride,
+                            int64_t raw_cap, const int32_t* q_pos, int window, const float* sink,
+                            float softmax_scale, int B, int T, int H, int D, void* out,
+                            float* lse, void* ws, size_t ws_bytes, int32_t* err_word,
+                            void* stream) {
+  int st = check_attention_common(q, k_cmp, v_cmp, cmp_bstride, N_cap, k_raw, v_raw, raw_bstride,
+                                  raw_cap, window, sink, B, T, H, D, out, lse);
+  if (st != CSA_OK || B == 0 || T == 0) return st;
+  if (k < 0 || (k > 0 && (!topk_idx || !aligned4(topk_idx) || N_cap <= 0))) return CSA_ERR_INVALID_ARG;
+  if (!q_pos || !aligned4(q_pos)) return CSA_ERR_INVALID_ARG;
+  if (k + window <= 0) return CSA_ERR_INVALID_ARG;
+  if ((int64_t)B * T > (1 << 30)) return CSA_ERR_UNSUPPORTED;
+  AttnArgs a;
+  fill_common(a, q, k_cmp, v_cmp, cmp_bstride, N_cap, k_raw, v_raw, raw_bstride, raw_cap, window,
+              sink, softmax_scale, H, out, lse, err_word);
+  a.sel = topk_idx;
+  a.sel_count = k;
+  a.sel_stride = k;
+  a.pos = q_pos;
+  a.pos_is_len = 0;
+  a.T = T;
+  a.n_query = B * T;
+  a.n_keys_max = k + window;
+  return run_attention(a, ws, ws_bytes, stream);
+}
+
+int hca_dense_attn_decode(const void* q, const void* k_cmp, const void* v_cmp,
+                          int64_t cmp_bstride, int N_cap, const int32_t* n_cmp, int m_prime,
+                          const void* k_raw, const void* v_raw, int64_t raw_bstride,
+                          int64_t raw_cap, const int32_t* seq_len, int window, const float* sink,
+                          float softmax_scale, int B, int H, int D, void* out, float* lse,
+                          void* ws, size_t ws_bytes, int32_t* err_word, void* stream) {
+  int st = check_attention_common(q, k_cmp, v_cmp, cmp_bstride, N_cap, k_raw, v_raw, raw_bstride,
+                                  raw_cap, window, sink, B, 1, H, D, out, lse);
+  if (st != CSA_OK || B == 0) return st;
+  if (m_prime <= 0 || !seq_len || !aligned4(seq_len)) return CSA_ERR_INVALID_ARG;
+  if (N_cap > 0 && (!n_cmp || !aligned4(n_cmp))) return CSA_ERR_INVALID_ARG;
+  if (N_cap + window <= 0) return CSA_ERR_INVALID_ARG;
+  AttnArgs a;
+  fill_common(a, q, k_cmp, v_cmp, cmp_bstride, N_cap, k_raw, v_raw, raw_bstride, raw_cap, window,
+              sink, softmax_scale, H, out, lse, err_word);
+  a.dense = 1;
+  a.n_cmp = n_cmp;
+  a.m_prime = m_prime;
+  a.pos = seq_len;
+  a.pos_is_len = 1;
+  a.T = 1;
+  a.n_query = B;
+  a.n_keys_max = N_cap + window;
+  return run_attention(a, ws, ws_bytes, stream);
+}
+
+}  // extern "C"

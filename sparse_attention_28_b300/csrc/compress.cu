@@ -1,0 +1,124 @@
+// compress.cu -- block compression of raw KV / indexer-key rows.
+//
+// Method: hyper.ai DeepSeek-V4 page, Method -- CSA "compresses every m tokens
+// into a single entry using learnable compression weights and positional
+// biases"; HCA consolidates every m' tokens "without overlapping
+// compression".  Operator (this library's reading of that sentence), for
+// block j and channel c:
+//     g[i][c] = sum_e W[c][e] x[j*m+i][e] + pos_bias[i][c]
+//     y[j][c] = sum_i softmax_i(g[.][c])[i] * x[j*m+i][c]
+// Output: bf16 (nearest even), or E4M3 with one fp32 scale per entry,
+// scale = max_c |y| / 448 (1 if all zero), code = nearest-even E4M3 of
+// y / scale, saturating.
+//
+// One CTA per (block, sequence), one thread per output channel.  The block's
+// m raw rows are staged in shared memory as fp32; each thread forms its
+// channel's m gate logits 16 positions at a time (W row from L1, x rows from
+// shared memory as broadcasts) and folds them into an online softmax.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace csa {
+
+namespace {
+
+constexpr int kPosChunk = 16;
+
+template <int D>
+__global__ void __launch_bounds__(D) compress_kernel(CompressArgs a) {
+  extern __shared__ __align__(16) float xs[];  // [m][D]
+  __shared__ float red[D / 32];
+  const int c = threadIdx.x;
+  const int b = blockIdx.y;
+  const int64_t j = (int64_t)a.block_begin + blockIdx.x;
+  const int m = a.m;
+  const bf16* x = a.raw + (int64_t)b * a.raw_bstride + j * m * D;
+  for (int i = c; i < m * D; i += D) xs[i] = __bfloat162float(x[i]);
+  __syncthreads();
+
+  const bf16* wr = a.W + (int64_t)c * D;
+  float mx = -INFINITY, den = 0.f, num = 0.f;
+  for (int i0 = 0; i0 < m; i0 += kPosChunk) {
+    const int n = (m - i0 < kPosChunk) ? m - i0 : kPosChunk;
+    float gl[kPosChunk];
+#pragma unroll
+    for (int ii = 0; ii < kPosChunk; ++ii) gl[ii] = 0.f;
+    for (int e = 0; e < D; e += 8) {
+      const uint4 wv = __ldg(reinterpret_cast<const uint4*>(wr + e));
+      const __nv_bfloat162* w2 = reinterpret_cast<const __nv_bfloat162*>(&wv);
+      float wf[8];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 f = __bfloat1622float2(w2[q]);
+        wf[2 * q] = f.x;
+        wf[2 * q + 1] = f.y;
+      }
+#pragma unroll
+      for (int ii = 0; ii < kPosChunk; ++ii) {
+        if (ii < n) {
+          const float* xr = xs + (i0 + ii) * D + e;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) gl[ii] = fmaf(wf[q], xr[q], gl[ii]);
+        }
+      }
+    }
+#pragma unroll
+    for (int ii = 0; ii < kPosChunk; ++ii) {
+      if (ii < n) {
+        const float gi = gl[ii] + __ldg(a.pos_bias + (int64_t)(i0 + ii) * D + c);
+        const float xv = xs[(i0 + ii) * D + c];
+        if (gi > mx) {
+          const float r = expf(mx - gi);
+          den = den * r + 1.f;
+          num = num * r + xv;
+          mx = gi;
+        } else {
+          const float p = expf(gi - mx);
+          den += p;
+          num += p * xv;
+        }
+      }
+    }
+  }
+  const float y = num / den;
+
+  if (!a.fp8) {
+    bf16* out = reinterpret_cast<bf16*>(a.out) + (int64_t)b * a.out_bstride + j * D;
+    out[c] = __float2bfloat16_rn(y);
+    return;
+  }
+  // E4M3 with a per-entry scale
+  float am = fabsf(y);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, o));
+  if ((c & 31) == 0) red[c >> 5] = am;
+  __syncthreads();
+  float amax = 0.f;
+#pragma unroll
+  for (int w = 0; w < D / 32; ++w) amax = fmaxf(amax, red[w]);
+  const float scale = amax > 0.f ? amax / 448.f : 1.f;
+  uint8_t* out = reinterpret_cast<uint8_t*>(a.out) + (int64_t)b * a.out_bstride + j * D;
+  out[c] = static_cast<uint8_t>(__nv_cvt_float_to_fp8(y / scale, __NV_SATFINITE, __NV_E4M3));
+  if (c == 0) a.out_scale[(int64_t)b * a.scale_bstride + j] = scale;
+}
+
+}  // namespace
+
+cudaError_t launch_compress(const CompressArgs& a, cudaStream_t st) {
+  if (a.n_blocks == 0 || a.B == 0) return cudaSuccess;
+  const int smem = a.m * a.d * (int)sizeof(float);
+  dim3 grid(a.n_blocks, a.B);
+  cudaError_t e;
+  if (a.d == 128) {
+    e = ensure_smem_attr((const void*)compress_kernel<128>, 256 * 128 * 4);
+    if (e != cudaSuccess) return e;
+    compress_kernel<128><<<grid, 128, smem, st>>>(a);
+  } else {
+    e = ensure_smem_attr((const void*)compress_kernel<64>, 256 * 64 * 4);
+    if (e != cudaSuccess) return e;
+    compress_kernel<64><<<grid, 64, smem, st>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace csa

@@ -1,0 +1,102 @@
+// kernels.h -- internal launch interface between the C ABI layer (api.cu)
+// and the kernels.  Not installed; not part of the ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_bf16.h>
+
+namespace csa {
+
+// Sets the dynamic shared-memory limit of a kernel once per device.
+cudaError_t ensure_smem_attr(const void* func, int bytes);
+
+// ---------------------------------------------------------------- attention
+struct AttnArgs {
+  const __nv_bfloat16* q;  // [n_query][H][128]
+  const __nv_bfloat16* k_cmp;
+  const __nv_bfloat16* v_cmp;
+  int64_t cmp_bstride;
+  int N_cap;
+  int dense;           // 1: compressed rows 0 .. n_vis-1 (HCA); 0: rows from sel
+  const int32_t* sel;  // [n_query][sel_stride] compressed rows (sparse)
+  int sel_count;
+  int64_t sel_stride;
+  const int32_t* n_cmp;  // dense: entries present per sequence
+  int m_prime;           // dense: compression ratio for the visibility rule
+  const __nv_bfloat16* k_raw;
+  const __nv_bfloat16* v_raw;
+  int64_t raw_bstride;
+  int64_t raw_cap;
+  const int32_t* pos;  // pos_is_len ? seq_len[B] : q_pos[n_query]
+  int pos_is_len;
+  int T;  // query tokens per sequence (query q belongs to sequence q / T)
+  int window;
+  const float* sink;
+  float scale_log2;  // softmax_scale * log2(e)
+  int H;
+  int n_query;
+  int n_keys_max;
+  // filled by launch_attention
+  int n_split;
+  int keys_per_split;
+  float* part_o;
+  float* part_lse;
+  __nv_bfloat16* out;
+  float* lse;
+  int32_t* err;
+};
+
+void attn_plan(int n_query, int n_keys_max, int* n_split, int* keys_per_split);
+size_t attn_workspace_bytes(int n_query, int H, int n_keys_max);
+cudaError_t launch_attention(AttnArgs a, void* ws, cudaStream_t st);
+
+// ---------------------------------------------------------------- indexer + top-k
+constexpr int kHistBins = 4096;  // top 12 bits of the order-preserving score key
+constexpr int kCandCap = 8192;   // candidates of the threshold bin kept per query
+constexpr int kMaxNcap = 1 << 19;
+
+struct IndexerArgs {
+  const void* q;  // [n_query][4][64] bf16 or E4M3
+  const float* q_scale;
+  const float* w;
+  const void* keys;  // [B][k_bstride] rows of 64 (bf16 or E4M3)
+  int64_t k_bstride;
+  const float* k_scale;
+  int64_t ks_bstride;
+  int fp8;
+  const int32_t* q_pos;
+  const int32_t* n_cmp;
+  int T;
+  int n_query;
+  int N_cap;
+  int m;
+  int k;
+  int32_t* err;
+  // outputs
+  int32_t* topk_idx;
+  float* topk_score;
+};
+
+size_t indexer_topk_workspace_bytes(int n_query, int N_cap);
+cudaError_t launch_indexer_topk(const IndexerArgs& a, void* ws, cudaStream_t st);
+
+// ---------------------------------------------------------------- compression
+struct CompressArgs {
+  const __nv_bfloat16* raw;
+  int64_t raw_bstride;
+  int B, d, m, block_begin, n_blocks;
+  const __nv_bfloat16* W;
+  const float* pos_bias;
+  void* out;
+  int64_t out_bstride;
+  int fp8;
+  float* out_scale;
+  int64_t scale_bstride;
+};
+
+cudaError_t launch_compress(const CompressArgs& a, cudaStream_t st);
+
+}  // namespace csa

@@ -1,0 +1,208 @@
+"""One step of each hot-path workload on resident device buffers.
+
+A step object takes the inputs of a workload (the dict that ``synth``
+returns), lays them out on the GPU once -- caches at full capacity, rows a
+step must not read filled with NaN so that a stray read cannot go unnoticed,
+workspaces and outputs preallocated -- and then runs one step per call:
+
+* CSA decode:  [compress the newest block of K, V and indexer keys]
+  -> indexer top-k -> sparse attention (split-K + merge)
+* HCA decode:  dense attention (split-K + merge)
+* CSA prefill: compress the new blocks -> indexer top-k for every new token
+  -> sparse attention for every new token
+
+Each call only launches library kernels on the current stream (no host
+synchronisation, no allocation), so a step can be captured in a CUDA graph.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import (attn_workspace, compress_kv, hca_dense_attn_decode, indexer_topk,
+               indexer_topk_workspace, sparse_attn_decode, sparse_attn_prefill)
+
+
+def _nan(shape, dtype, device):
+    if dtype in (torch.uint8,):
+        return torch.full(shape, 0x7F, dtype=dtype, device=device)  # E4M3 NaN code
+    return torch.full(shape, float("nan"), dtype=dtype, device=device)
+
+
+class CsaDecodeStep:
+    def __init__(self, inp: dict, device="cuda"):
+        wl = inp["workload"]
+        self.wl = wl
+        dev = torch.device(device)
+        B, W, m, D = wl.B, wl.W, wl.m, wl.D
+        lens = list(wl.lens)
+        L_cap = max(lens)
+        g = lambda k: None if inp.get(k) is None else inp[k].to(dev).clone()
+        self.q, self.sink = g("q"), g("sink")
+        self.seq_len, self.n_cmp = g("seq_len"), g("n_cmp")
+        self.k_cmp, self.v_cmp = g("k_cmp"), g("v_cmp")
+        self.q_idx, self.w, self.k_idx = g("q_idx"), g("w"), g("k_idx")
+        self.q_scale, self.k_scale = g("q_scale"), g("k_scale")
+        self.q_pos = (self.seq_len - 1).view(B, 1).contiguous()
+        # raw caches: only the window rows are defined
+        self.k_raw = _nan((B, L_cap, D), torch.bfloat16, dev)
+        self.v_raw = _nan((B, L_cap, D), torch.bfloat16, dev)
+        kw, vw = g("k_win"), g("v_win")
+        for b, n in enumerate(lens):
+            lo = max(0, n - W)
+            self.k_raw[b, lo:n] = kw[b, W - (n - lo):]
+            self.v_raw[b, lo:n] = vw[b, W - (n - lo):]
+        self.compress = wl.stream_compress
+        if self.compress:
+            self.idx_raw = _nan((B, L_cap, wl.d_I), torch.bfloat16, dev)
+            rn = g("raw_new_idx")
+            for b, n in enumerate(lens):
+                self.idx_raw[b, n - m:n] = rn[b]
+            self.gates = {s: tuple(t.to(dev) for t in inp["gate_" + s]) for s in ("k", "v", "idx")}
+            # the newest entry is produced by the step itself
+            for b, n in enumerate(lens):
+                j = n // m - 1
+                self.k_cmp[b, j] = float("nan")
+                self.v_cmp[b, j] = float("nan")
+                if self.k_scale is not None:
+                    self.k_idx[b, j] = 0x7F
+                    self.k_scale[b, j] = float("nan")
+                else:
+                    self.k_idx[b, j] = float("nan")
+            assert len(set(lens)) == 1, "streaming compression assumes equal lengths"
+            self.new_block = lens[0] // m - 1
+        self.idx = torch.empty((B, 1, wl.k), dtype=torch.int32, device=dev)
+        self.out = torch.empty_like(self.q)
+        self.ws_idx = torch.empty(max(1, indexer_topk_workspace(B, 1, wl.N_cap, wl.k)),
+                                  dtype=torch.uint8, device=dev)
+        self.ws_attn = torch.empty(max(1, attn_workspace(B, 1, wl.H, wl.k + W)),
+                                   dtype=torch.uint8, device=dev)
+
+    def _compress(self):
+        wl, j = self.wl, self.new_block
+        compress_kv(self.k_raw, *self.gates["k"], wl.m, j, 1, self.k_cmp)
+        compress_kv(self.v_raw, *self.gates["v"], wl.m, j, 1, self.v_cmp)
+        compress_kv(self.idx_raw, *self.gates["idx"], wl.m, j, 1, self.k_idx, self.k_scale)
+
+    def _index(self):
+        wl = self.wl
+        indexer_topk(self.q_idx, self.w, self.k_idx, self.q_pos, self.n_cmp, wl.m, wl.k,
+                     q_scale=self.q_scale, k_scale=self.k_scale, out=self.idx, ws=self.ws_idx)
+
+    def _attend(self):
+        wl = self.wl
+        sparse_attn_decode(self.q, self.k_cmp, self.v_cmp, self.idx.view(wl.B, wl.k),
+                           self.k_raw, self.v_raw, self.seq_len, wl.W, self.sink,
+                           out=self.out, ws=self.ws_attn)
+
+    def stages(self):
+        """(name, callable) per stage, in order."""
+        st = [("compress", self._compress)] if self.compress else []
+        return st + [("indexer_topk", self._index), ("attention", self._attend)]
+
+    def __call__(self):
+        for _, fn in self.stages():
+            fn()
+        return self.out
+
+
+class HcaDecodeStep:
+    def __init__(self, inp: dict, device="cuda"):
+        wl = inp["workload"]
+        self.wl = wl
+        dev = torch.device(device)
+        B, W, D = wl.B, wl.W, wl.D
+        lens = list(wl.lens)
+        L_cap = max(lens)
+        g = lambda k: None if inp.get(k) is None else inp[k].to(dev).clone()
+        self.q, self.sink = g("q"), g("sink")
+        self.seq_len, self.n_cmp = g("seq_len"), g("n_cmp")
+        self.k_cmp, self.v_cmp = g("k_cmp"), g("v_cmp")
+        self.k_raw = _nan((B, L_cap, D), torch.bfloat16, dev)
+        self.v_raw = _nan((B, L_cap, D), torch.bfloat16, dev)
+        kw, vw = g("k_win"), g("v_win")
+        for b, n in enumerate(lens):
+            lo = max(0, n - W)
+            self.k_raw[b, lo:n] = kw[b, W - (n - lo):]
+            self.v_raw[b, lo:n] = vw[b, W - (n - lo):]
+        self.out = torch.empty_like(self.q)
+        self.ws_attn = torch.empty(max(1, attn_workspace(B, 1, wl.H, wl.N_cap + W)),
+                                   dtype=torch.uint8, device=dev)
+
+    def _attend(self):
+        wl = self.wl
+        hca_dense_attn_decode(self.q, self.k_cmp, self.v_cmp, self.n_cmp, wl.m, self.k_raw,
+                              self.v_raw, self.seq_len, wl.W, self.sink, out=self.out,
+                              ws=self.ws_attn)
+
+    def stages(self):
+        return [("attention", self._attend)]
+
+    def __call__(self):
+        self._attend()
+        return self.out
+
+
+class CsaPrefillStep:
+    def __init__(self, inp: dict, device="cuda"):
+        wl = inp["workload"]
+        self.wl = wl
+        dev = torch.device(device)
+        B, T, L, W, m, D = wl.B, wl.T, wl.L, wl.W, wl.m, wl.D
+        L_cap = L + T
+        g = lambda k: None if inp.get(k) is None else inp[k].to(dev).clone()
+        self.q, self.sink = g("q"), g("sink")
+        self.q_pos, self.n_cmp = g("q_pos"), g("n_cmp")
+        self.q_idx, self.w = g("q_idx"), g("w")
+        self.k_cmp, self.v_cmp, self.k_idx = g("k_cmp"), g("v_cmp"), g("k_idx")
+        n_old = L // m
+        # new entries are produced by the step
+        self.k_cmp[:, n_old:] = float("nan")
+        self.v_cmp[:, n_old:] = float("nan")
+        self.k_idx[:, n_old:] = float("nan")
+        self.k_raw = _nan((B, L_cap, D), torch.bfloat16, dev)
+        self.v_raw = _nan((B, L_cap, D), torch.bfloat16, dev)
+        self.idx_raw = _nan((B, L_cap, wl.d_I), torch.bfloat16, dev)
+        base = L - (W - 1)
+        self.k_raw[:, base:] = g("raw_k")
+        self.v_raw[:, base:] = g("raw_v")
+        self.idx_raw[:, L:] = g("raw_idx")
+        self.gates = {s: tuple(t.to(dev) for t in inp["gate_" + s]) for s in ("k", "v", "idx")}
+        self.block0, self.n_new = n_old, T // m
+        self.idx = torch.empty((B, T, wl.k), dtype=torch.int32, device=dev)
+        self.out = torch.empty_like(self.q)
+        self.ws_idx = torch.empty(max(1, indexer_topk_workspace(B, T, wl.N_cap, wl.k)),
+                                  dtype=torch.uint8, device=dev)
+        self.ws_attn = torch.empty(max(1, attn_workspace(B, T, wl.H, wl.k + W)),
+                                   dtype=torch.uint8, device=dev)
+
+    def _compress(self):
+        wl = self.wl
+        for raw, dst, gate in ((self.k_raw, self.k_cmp, self.gates["k"]),
+                               (self.v_raw, self.v_cmp, self.gates["v"]),
+                               (self.idx_raw, self.k_idx, self.gates["idx"])):
+            compress_kv(raw, *gate, wl.m, self.block0, self.n_new, dst)
+
+    def _index(self):
+        wl = self.wl
+        indexer_topk(self.q_idx, self.w, self.k_idx, self.q_pos, self.n_cmp, wl.m, wl.k,
+                     out=self.idx, ws=self.ws_idx)
+
+    def _attend(self):
+        wl = self.wl
+        sparse_attn_prefill(self.q, self.k_cmp, self.v_cmp, self.idx, self.k_raw, self.v_raw,
+                            self.q_pos, wl.W, self.sink, out=self.out, ws=self.ws_attn)
+
+    def stages(self):
+        return [("compress", self._compress), ("indexer_topk", self._index),
+                ("attention", self._attend)]
+
+    def __call__(self):
+        for _, fn in self.stages():
+            fn()
+        return self.out
+
+
+def make_step(inp: dict, device="cuda"):
+    kind = inp["workload"].kind
+    return {"csa_decode": CsaDecodeStep, "hca_decode": HcaDecodeStep,
+            "csa_prefill": CsaPrefillStep}[kind](inp, device)

@@ -114,8 +114,10 @@ def make_inputs(wl: Workload, seed: int = 0, device="cpu") -> dict:
     Decode keys: q [B,H,D]; k_cmp, v_cmp [B,N_cap,D]; q_idx [B,1,H_I,d_I];
     w [B,1,H_I]; k_idx [B,N_cap,d_I] (+ q_scale, k_scale for FP8); sink [H];
     seq_len, n_cmp [B]; k_win, v_win [B,W,D] = raw rows L_b-W .. L_b-1.
-    Streaming compression adds raw_new_{k,v,idx} [B,m,*] (the newest block)
-    and gate parameters gate_{k,v,idx} = (W, pos_bias).
+    Streaming compression adds raw_new_idx [B,m,d_I] (raw indexer-key rows of
+    the newest block, whose K/V rows are the last m window rows) and gate
+    parameters gate_{k,v,idx} = (W, pos_bias); the newest compressed entry
+    (index N-1) is left for the step to compute.
     Prefill keys: q [B,T,H,D]; q_idx [B,T,H_I,d_I]; w [B,T,H_I]; q_pos [B,T];
     k_cmp, v_cmp, k_idx with the L/m cached entries (the T/m new ones are left
     for the compression step, zero here); raw_{k,v} [B,W-1+T,D] for positions
@@ -155,8 +157,8 @@ def make_inputs(wl: Workload, seed: int = 0, device="cpu") -> dict:
                 out["k_idx"] = randn((B, N_cap, wl.d_I), seed, 9, dev)
                 out["q_scale"] = out["k_scale"] = None
         if wl.stream_compress:
-            out["raw_new_k"] = randn((B, m, D), seed, 10, dev)
-            out["raw_new_v"] = randn((B, m, D), seed, 11, dev)
+            # the newest block's raw K/V rows are the last m window rows;
+            # its raw indexer-key rows have no other source
             out["raw_new_idx"] = randn((B, m, wl.d_I), seed, 12, dev)
             out["gate_k"] = gate(D, 20)
             out["gate_v"] = gate(D, 22)

@@ -1,0 +1,102 @@
+"""Shared test plumbing: tensor <-> numpy views, raw-cache placement, and the
+parity criteria.  No step of the method is computed here."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+# Parity bars for bf16 inputs with fp32 accumulation (attention outputs).
+ATTN_MAX_ABS = 2e-2
+ATTN_REL_L2 = 5e-3
+LSE_ABS = 1e-3
+NEAR_TIE_REL = 1e-6
+
+
+def u16(t: torch.Tensor) -> np.ndarray:
+    """bf16 tensor -> numpy uint16 bit patterns (CPU copy)."""
+    return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def u8(t: torch.Tensor) -> np.ndarray:
+    return t.detach().contiguous().cpu().view(torch.uint8).numpy()
+
+
+def f64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def poisoned(shape, dtype=torch.bfloat16, device="cuda"):
+    """A tensor filled with NaN: any stray read shows up in the outputs."""
+    return torch.full(shape, float("nan"), dtype=dtype, device=device)
+
+
+def place_window(win: torch.Tensor, lens, L_cap: int, device="cuda") -> torch.Tensor:
+    """Raw cache [B, L_cap, D], NaN everywhere except rows len-W .. len-1 of
+    sequence b, which hold win[b] (rows before position 0 are dropped)."""
+    B, W, D = win.shape
+    raw = poisoned((B, L_cap, D), device=device)
+    for b, n in enumerate(lens):
+        lo = max(0, n - W)
+        raw[b, lo:n] = win[b, W - (n - lo):].to(device)
+    return raw
+
+
+def window_arrays(win: torch.Tensor, lens):
+    """The oracle's view of place_window: rows for positions base .. base+R-1
+    of every sequence, with base = min over b of (len_b - W) clipped at 0.
+    Returns (uint16 [B, R, D], base)."""
+    B, W, D = win.shape
+    base = max(0, min(lens) - W)
+    R = max(lens) - base
+    arr = np.zeros((B, R, D), np.uint16)
+    w = u16(win)
+    for b, n in enumerate(lens):
+        lo = max(0, n - W)
+        arr[b, lo - base:n - base] = w[b, W - (n - lo):]
+    return arr, base
+
+
+def check_attention(out_gpu, out_ref, lse_gpu=None, lse_ref=None, what=""):
+    """Attention parity: max-abs <= 2e-2, relative L2 <= 5e-3, lse within 1e-3."""
+    o = f64(out_gpu).reshape(-1)
+    r = np.asarray(out_ref, np.float64).reshape(-1)
+    assert np.all(np.isfinite(o)), f"{what}: non-finite output (stray read?)"
+    max_abs = np.max(np.abs(o - r)) if o.size else 0.0
+    rel_l2 = np.linalg.norm(o - r) / max(np.linalg.norm(r), 1e-30)
+    assert max_abs <= ATTN_MAX_ABS, f"{what}: max-abs {max_abs:.3e}"
+    assert rel_l2 <= ATTN_REL_L2, f"{what}: rel-L2 {rel_l2:.3e}"
+    if lse_gpu is not None:
+        lg = f64(lse_gpu).reshape(-1)
+        lr = np.asarray(lse_ref, np.float64).reshape(-1)
+        fin = np.isfinite(lr)
+        np.testing.assert_array_equal(np.isfinite(lg), fin, err_msg=f"{what}: lse finiteness")
+        if fin.any():
+            d = np.max(np.abs(lg[fin] - lr[fin]))
+            assert d <= LSE_ABS, f"{what}: lse max-abs {d:.3e}"
+    return max_abs, rel_l2
+
+
+def check_topk(idx_gpu, idx_ref, scores_ref, n_vis, k: int, what=""):
+    """Top-k parity: identical index sets except near-ties (an index in the
+    symmetric difference must have an oracle score within 1e-6 relative of the
+    oracle's k-th score); ascending order; -1 padding exactly where expected."""
+    g = np.asarray(idx_gpu).reshape(-1, k)
+    r = np.asarray(idx_ref).reshape(-1, k)
+    s = np.asarray(scores_ref, np.float64).reshape(g.shape[0], -1)
+    nv = np.asarray(n_vis).reshape(-1)
+    mismatched = 0
+    for qq in range(g.shape[0]):
+        take = min(k, int(nv[qq]))
+        gq, rq = g[qq], r[qq]
+        assert np.all(gq[take:] == -1), f"{what}: query {qq} padding"
+        gs = gq[:take]
+        assert np.all(np.diff(gs) > 0), f"{what}: query {qq} not ascending"
+        assert np.all((gs >= 0) & (gs < nv[qq])), f"{what}: query {qq} index range"
+        diff = set(gs.tolist()) ^ set(rq[:take].tolist())
+        if diff:
+            kth = np.sort(s[qq, : nv[qq]])[::-1][take - 1]
+            for i in diff:
+                assert abs(s[qq, i] - kth) <= NEAR_TIE_REL * abs(kth), (
+                    f"{what}: query {qq} index {i} score {s[qq, i]!r} vs k-th {kth!r}")
+            mismatched += 1
+    return mismatched

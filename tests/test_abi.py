@@ -1,0 +1,113 @@
+"""The C-ABI library on the host (no GPU needed): it loads, exports every
+symbol include/csa.h declares, and rejects bad arguments before launching
+anything."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import sparse_attention_28_b300 as csa
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "csa.h")
+FAKE = ctypes.c_void_p(0x10000)  # aligned, never dereferenced: validation fails first
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b((?:csa|hca)_\w+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol():
+    names = declared_functions()
+    assert len(names) >= 9
+    L = csa.lib()
+    for n in names:
+        assert hasattr(L, n), f"libcsa.so does not export {n}"
+    assert set(names) == set(csa.ABI_SYMBOLS)
+
+
+def test_status_strings():
+    L = csa.lib()
+    for code in range(6):
+        assert L.csa_status_str(code).startswith(b"CSA_")
+    assert L.csa_status_str(99) == b"unknown status"
+    assert L.csa_abi_version() == 1
+
+
+def _decode(**over):
+    args = dict(q=FAKE, k_cmp=FAKE, v_cmp=FAKE, cmp_bstride=1024 * 128, N_cap=1024,
+                topk_idx=FAKE, k=64, k_raw=FAKE, v_raw=FAKE, raw_bstride=4096 * 128,
+                raw_cap=4096, seq_len=FAKE, window=128, sink=None, scale=1.0, B=2, H=64, D=128,
+                out=FAKE, lse=None, ws=FAKE, ws_bytes=1, err=None, stream=None)
+    args.update(over)
+    return csa.lib().csa_sparse_attn_decode(*args.values())
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(q=None), 1), (dict(out=None), 1), (dict(D=64), 2), (dict(H=48), 2), (dict(B=-1), 1),
+    (dict(window=-1), 1), (dict(cmp_bstride=1000), 1), (dict(k_raw=None), 1),
+    (dict(raw_bstride=100), 1), (dict(q=ctypes.c_void_p(0x10002)), 1), (dict(k=-3), 1),
+    (dict(topk_idx=None), 1), (dict(seq_len=None), 1), (dict(ws=None), 3),
+    (dict(ws_bytes=0), 3),
+])
+def test_sparse_decode_rejects(over, status):
+    assert _decode(**over) == status
+
+
+def test_zero_batch_is_a_no_op():
+    assert _decode(B=0, q=None, out=None) == 0
+
+
+def test_indexer_rejects():
+    L = csa.lib()
+
+    def call(**over):
+        a = dict(q=FAKE, qs=None, w=FAKE, kk=FAKE, kbs=4096 * 64, ks=None, ksbs=0, dt=0,
+                 pos=FAKE, ncmp=FAKE, B=2, T=1, HI=4, dI=64, N=4096, m=4, k=256, idx=FAKE,
+                 sc=None, ws=FAKE, wsb=1, err=None, st=None)
+        a.update(over)
+        return L.csa_indexer_topk(*a.values())
+
+    assert call(HI=8) == 2 and call(dI=128) == 2 and call(dt=7) == 2
+    assert call(k=5000) == 1 and call(k=0) == 1 and call(q=None) == 1
+    assert call(dt=1) == 1  # FP8 without scales
+    assert call(kbs=100) == 1
+    assert call(N=1 << 20) == 2
+    assert call() == 3  # workspace too small
+    assert L.csa_indexer_topk_workspace(2, 1, 4096, 256) > 2 * 4096 * 4
+
+
+def test_compress_rejects():
+    L = csa.lib()
+
+    def call(**over):
+        a = dict(raw=FAKE, rbs=64 * 128, B=2, d=128, m=4, b0=0, nb=16, W=FAKE, pb=FAKE, out=FAKE,
+                 obs=16 * 128, dt=0, sc=None, sbs=0, err=None, st=None)
+        a.update(over)
+        return L.csa_compress_kv(*a.values())
+
+    assert call(d=96) == 2 and call(m=300) == 2 and call(dt=5) == 2
+    assert call(nb=17) == 1  # reads past the raw rows
+    assert call(obs=15 * 128) == 1
+    assert call(dt=1) == 1  # FP8 output needs a scale array
+    assert call(W=None) == 1
+    assert call(B=0) == 0 and call(nb=0) == 0
+
+
+def test_attention_workspace_plan():
+    L = csa.lib()
+    # long key sets split over many CTAs -> partials; many queries -> one split
+    assert L.csa_attn_workspace(32, 1, 64, 1152) > 0
+    assert L.csa_attn_workspace(1, 4096, 64, 2176) == 0
+    assert L.csa_attn_workspace(16, 1, 64, 8320) == L.csa_attn_workspace(16, 1, 64, 8320)
+
+
+def test_binding_rejects_cpu_tensors():
+    import torch
+    q = torch.zeros(2, 64, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        csa.sparse_attn_decode(q, q, q, torch.zeros(2, 4, dtype=torch.int32), q, q,
+                               torch.zeros(2, dtype=torch.int32), 128, None)

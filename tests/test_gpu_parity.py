@@ -1,0 +1,383 @@
+"""CUDA path vs the CPU oracle, element by element, on seeded inputs at sizes
+the oracle finishes in seconds: several tiles, several splits, ragged tails,
+edge cases.  All calls go through the C ABI (via the thin binding)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sparse_attention_28_b300 as csa
+import synth
+from _util import (check_attention, check_topk, f64, place_window, poisoned, u8, u16,
+                   window_arrays)
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def rnd(shape, tid, scale=1.0, dtype=torch.bfloat16, seed=11):
+    return synth.randn(shape, seed, tid, "cpu", scale=scale, dtype=dtype)
+
+
+# ---------------------------------------------------------------- a1 compression
+
+def e4m3_half_step(v):
+    a = np.abs(v)
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -6)))
+    return 2.0 ** (e - 4)
+
+
+@pytest.mark.parametrize("d,m,fp8", [(128, 4, False), (64, 4, False), (128, 1, False),
+                                     (128, 128, False), (64, 4, True), (128, 4, True),
+                                     (64, 256, True), (128, 7, False)])
+def test_compress_parity(cuda_device, d, m, fp8):
+    B, bb, nb = 3, 2, 5
+    N_cap = bb + nb + 2
+    L = N_cap * m
+    raw = rnd((B, L, d), 1)
+    W = rnd((d, d), 2, 1 / math.sqrt(d))
+    pb = rnd((m, d), 3, dtype=torch.float32)
+    if fp8:
+        out = torch.full((B, N_cap, d), 0x7F, dtype=torch.uint8, device=DEV)
+        sc = torch.full((B, N_cap), float("nan"), device=DEV)
+    else:
+        out = poisoned((B, N_cap, d))
+        sc = None
+    csa.compress_kv(raw.to(DEV), W.to(DEV), pb.to(DEV), m, bb, nb, out, sc)
+    torch.cuda.synchronize()
+    y = oracle.compress(u16(raw), u16(W), pb.numpy(), m, bb, nb)
+    if not fp8:
+        g = f64(out[:, bb:bb + nb])
+        ulp = 2.0 ** (np.floor(np.log2(np.abs(y))) - 7)
+        assert np.all(np.abs(g - y) <= ulp), "more than 1 bf16 ulp from the exact value"
+        exact = np.mean(u16(out[:, bb:bb + nb]) == oracle.quantize_bf16(y))
+        assert exact > 0.99
+        assert torch.isnan(out[:, :bb]).all() and torch.isnan(out[:, bb + nb:]).all()
+        return
+    codes_ref, sc_ref = oracle.quantize_e4m3_rows(y)
+    gs = sc[:, bb:bb + nb].cpu().numpy().astype(np.float64)
+    np.testing.assert_allclose(gs, sc_ref, rtol=1e-6)
+    dec = oracle.e4m3_decode(u8(out[:, bb:bb + nb]))
+    exact_v = y / gs[..., None]
+    assert np.all(np.abs(dec - exact_v) <= e4m3_half_step(exact_v) * (1 + 1e-5) + 1e-12)
+    assert np.mean(u8(out[:, bb:bb + nb]) == codes_ref) > 0.99
+    assert (out[:, :bb] == 0x7F).all() and (out[:, bb + nb:] == 0x7F).all()
+
+
+# ---------------------------------------------------------------- a2 + a3 indexer top-k
+
+def _indexer_case(B, T, N_cap, n_cmp, q_pos, fp8, seed=5):
+    if fp8:
+        qi, qs = synth.randn_fp8_rows((B, T, 4, 64), seed, 1)
+        ki, ks = synth.randn_fp8_rows((B, N_cap, 64), seed, 2)
+    else:
+        qi, qs = synth.randn((B, T, 4, 64), seed, 1), None
+        ki, ks = synth.randn((B, N_cap, 64), seed, 2), None
+    w = synth.randn((B, T, 4), seed, 3, dtype=torch.float32)
+    # entries beyond n_cmp must never be read: poison them
+    for b in range(B):
+        if fp8:
+            ki[b, n_cmp[b]:] = 0x7F
+        else:
+            ki[b, n_cmp[b]:] = float("nan")
+    return qi, qs, ki, ks, w, torch.tensor(q_pos, dtype=torch.int32), torch.tensor(
+        n_cmp, dtype=torch.int32)
+
+
+def _run_indexer(qi, qs, ki, ks, w, qp, nc, m, k):
+    idx, sc = csa.indexer_topk(qi.to(DEV), w.to(DEV), ki.to(DEV), qp.to(DEV), nc.to(DEV), m, k,
+                               q_scale=None if qs is None else qs.to(DEV),
+                               k_scale=None if ks is None else ks.to(DEV), return_scores=True)
+    torch.cuda.synchronize()
+    return idx.cpu().numpy(), sc.cpu().numpy()
+
+
+def _oracle_indexer(qi, qs, ki, ks, w, qp, nc, m, k, fp8):
+    conv = u8 if fp8 else u16
+    s, nv = oracle.indexer_scores(conv(qi), w.numpy(), conv(ki), qp.numpy(), nc.numpy(), m,
+                                  oracle.FP8_E4M3 if fp8 else oracle.BF16,
+                                  None if qs is None else qs.numpy(),
+                                  None if ks is None else ks.numpy())
+    return s, nv, oracle.topk(s, nv, k)
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+@pytest.mark.parametrize("T", [1, 5])
+def test_indexer_topk_parity(cuda_device, fp8, T):
+    B, N_cap, m, k = 3, 3000, 4, 200
+    n_cmp = [3000, 2100, 150]
+    base = [12003, 8401, 601]
+    q_pos = [[base[b] - 37 * (T - 1 - t) for t in range(T)] for b in range(B)]
+    case = _indexer_case(B, T, N_cap, n_cmp, q_pos, fp8)
+    idx, sc = _run_indexer(*case, m, k)
+    s, nv, ref = _oracle_indexer(*case, m, k, fp8)
+    check_topk(idx, ref, s, nv, k, "indexer")
+    # reported scores agree with the oracle's
+    for b in range(B):
+        for t in range(T):
+            take = min(k, nv[b, t])
+            got = sc[b, t, :take].astype(np.float64)
+            want = s[b, t, idx[b, t, :take]]
+            np.testing.assert_allclose(got, want, rtol=2e-5, atol=2e-4)
+            assert np.all(np.isneginf(sc[b, t, take:]))
+
+
+def test_topk_ties_take_lowest_indices(cuda_device):
+    # identical keys: every score ties, so the k lowest indices win; 20000
+    # entries in one histogram bin overflow the candidate list (slow path)
+    B, N_cap, m, k = 2, 20000, 4, 300
+    qi = synth.randn((B, 1, 4, 64), 3, 1)
+    ki = synth.randn((1, 1, 64), 3, 2).expand(B, N_cap, 64).contiguous()
+    w = torch.ones((B, 1, 4))
+    w[1] = -1.0  # second query: all scores equal and <= 0
+    qp = torch.tensor([[N_cap * m - 1], [N_cap * m - 1]], dtype=torch.int32)
+    nc = torch.tensor([N_cap, N_cap], dtype=torch.int32)
+    idx, _ = _run_indexer(qi, None, ki, None, w, qp, nc, m, k)
+    np.testing.assert_array_equal(idx[:, 0], np.tile(np.arange(k), (B, 1)))
+
+
+def test_topk_dense_threshold_bin_slow_path(cuda_device):
+    # a one-hot query makes the score the key's first channel; those take 16
+    # bf16 values in [1, 1.125): one histogram bin holds all 12000 entries
+    B, N_cap, m, k = 2, 12000, 4, 777
+    qi = torch.zeros((B, 1, 4, 64), dtype=torch.bfloat16)
+    qi[:, :, 0, 0] = 1.0
+    g = torch.Generator().manual_seed(9)
+    ki = synth.randn((B, N_cap, 64), 4, 2)
+    ki[:, :, 0] = (1.0 + torch.randint(0, 16, (B, N_cap), generator=g) / 128.0).to(torch.bfloat16)
+    w = torch.tensor([1.0, 0.0, 0.0, 0.0]).repeat(B, 1, 1)
+    qp = torch.tensor([[N_cap * m - 1], [N_cap * m - 3]], dtype=torch.int32)
+    nc = torch.tensor([N_cap, N_cap], dtype=torch.int32)
+    case = (qi, None, ki, None, w, qp, nc)
+    idx, _ = _run_indexer(*case, m, k)
+    s, nv, ref = _oracle_indexer(*case, m, k, False)
+    np.testing.assert_array_equal(idx, ref)  # exact: ties resolved by index
+
+
+def test_topk_zero_scores_and_short_lists(cuda_device):
+    # n_vis below k (every visible entry, -1 padded), n_vis == 0, and a query
+    # whose scores are mostly exactly zero (negative dot products)
+    B, N_cap, m, k = 4, 600, 4, 64
+    case = list(_indexer_case(B, 1, N_cap, [600, 600, 10, 600], [[2399], [3], [2399], [2399]],
+                              False))
+    case[2][:, :, :] = case[2].abs()  # positive keys ...
+    case[0][3] = -case[0][3].abs()  # ... and a negative query: every score of query 3 is 0
+    idx, _ = _run_indexer(*case, m, k)
+    s, nv, ref = _oracle_indexer(*case, m, k, False)
+    assert nv.ravel().tolist() == [600, 1, 10, 600]
+    check_topk(idx, ref, s, nv, k, "short lists")
+    np.testing.assert_array_equal(idx[1, 0], [0] + [-1] * (k - 1))
+    np.testing.assert_array_equal(idx[3, 0], np.arange(k))
+
+
+# ---------------------------------------------------------------- a4 / a5 attention
+
+def _attn_inputs(B, H, N_cap, lens, seed=21, W=128):
+    q = synth.randn((B, H, 128), seed, 1, scale=1 / math.sqrt(128))
+    kc, vc = synth.randn((B, N_cap, 128), seed, 2), synth.randn((B, N_cap, 128), seed, 3)
+    kw, vw = synth.randn((B, W, 128), seed, 4), synth.randn((B, W, 128), seed, 5)
+    sink = synth.randn((H,), seed, 6, dtype=torch.float32)
+    return q, kc, vc, kw, vw, sink
+
+
+def _random_topk(B, k, n_vis, seed=3):
+    g = np.random.default_rng(seed)
+    sel = np.full((B, k), -1, np.int32)
+    for b in range(B):
+        take = min(k, n_vis[b])
+        sel[b, :take] = np.sort(g.choice(n_vis[b], take, replace=False))
+    return sel
+
+
+@pytest.mark.parametrize("H", [16, 64, 128])
+@pytest.mark.parametrize("with_sink", [True, False])
+def test_sparse_decode_parity(cuda_device, H, with_sink):
+    B, N_cap, k, W = 3, 300, 48, 128
+    lens = [700, 129, 37]
+    q, kc, vc, kw, vw, sink = _attn_inputs(B, H, N_cap, lens)
+    sink = sink if with_sink else None
+    n_vis = [min(N_cap, n // 4) for n in lens]
+    sel = _random_topk(B, k, n_vis)
+    kc_d = kc.to(DEV)
+    vc_d = vc.to(DEV)
+    for b in range(B):  # entries beyond n_vis are never selected: poison them
+        kc_d[b, n_vis[b]:] = float("nan")
+        vc_d[b, n_vis[b]:] = float("nan")
+    out, lse = csa.sparse_attn_decode(
+        q.to(DEV), kc_d, vc_d, torch.from_numpy(sel).to(DEV), place_window(kw, lens, 800),
+        place_window(vw, lens, 800), torch.tensor(lens, dtype=torch.int32, device=DEV), W,
+        None if sink is None else sink.to(DEV), return_lse=True)
+    torch.cuda.synchronize()
+    kr, base = window_arrays(kw, lens)
+    vr, _ = window_arrays(vw, lens)
+    ro, rl = oracle.csa_decode(u16(q), u16(kc), u16(vc), sel, kr, vr, np.array(lens), W,
+                               None if sink is None else sink.numpy(), 1.0, base)
+    check_attention(out, ro, lse, rl, f"csa decode H={H}")
+
+
+def test_sparse_decode_many_splits_multi_tile(cuda_device):
+    # 40 queries x 640 keys: 8 splits of 128 keys (two 64-key tiles each)
+    B, H, N_cap, k, W = 40, 64, 900, 512, 128
+    lens = [3600 - 37 * b for b in range(B)]
+    q, kc, vc, kw, vw, sink = _attn_inputs(B, H, N_cap, lens, seed=33)
+    n_vis = [min(N_cap, n // 4) for n in lens]
+    sel = _random_topk(B, k, n_vis, seed=8)
+    out, lse = csa.sparse_attn_decode(
+        q.to(DEV), kc.to(DEV), vc.to(DEV), torch.from_numpy(sel).to(DEV),
+        place_window(kw, lens, 3600), place_window(vw, lens, 3600),
+        torch.tensor(lens, dtype=torch.int32, device=DEV), W, sink.to(DEV), return_lse=True)
+    torch.cuda.synchronize()
+    kr, base = window_arrays(kw, lens)
+    vr, _ = window_arrays(vw, lens)
+    ro, rl = oracle.csa_decode(u16(q), u16(kc), u16(vc), sel, kr, vr, np.array(lens), W,
+                               sink.numpy(), 1.0, base)
+    check_attention(out, ro, lse, rl, "csa decode splits")
+
+
+def test_decode_window_only_and_compressed_only(cuda_device):
+    B, H, N_cap, k = 2, 64, 100, 32
+    lens = [400, 90]
+    q, kc, vc, kw, vw, sink = _attn_inputs(B, H, N_cap, lens, seed=44)
+    n_vis = [min(N_cap, n // 4) for n in lens]
+    sel = _random_topk(B, k, n_vis, seed=1)
+    L = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    kr, base = window_arrays(kw, lens)
+    vr, _ = window_arrays(vw, lens)
+    # compressed entries only (window 0, no raw cache)
+    out = csa.sparse_attn_decode(q.to(DEV), kc.to(DEV), vc.to(DEV),
+                                 torch.from_numpy(sel).to(DEV), None, None, L, 0, sink.to(DEV))
+    ro, _ = oracle.csa_decode(u16(q), u16(kc), u16(vc), sel, None, None, np.array(lens), 0,
+                              sink.numpy(), 1.0)
+    check_attention(out, ro, what="compressed only")
+    # window only (every top-k slot is padding)
+    pad = np.full_like(sel, -1)
+    out = csa.sparse_attn_decode(q.to(DEV), kc.to(DEV), vc.to(DEV),
+                                 torch.from_numpy(pad).to(DEV), place_window(kw, lens, 400),
+                                 place_window(vw, lens, 400), L, 128, sink.to(DEV))
+    ro, _ = oracle.csa_decode(u16(q), u16(kc), u16(vc), pad, kr, vr, np.array(lens), 128,
+                              sink.numpy(), 1.0, base)
+    check_attention(out, ro, what="window only")
+
+
+@pytest.mark.parametrize("window", [128, 0])
+def test_hca_decode_parity(cuda_device, window):
+    B, H, m = 4, 64, 8
+    lens = [1000, 517, 64, 5]
+    N_cap = 130
+    n_cmp = [125, 64, 8, 0]
+    q, kc, vc, kw, vw, sink = _attn_inputs(B, H, N_cap, lens, seed=55)
+    kc_d, vc_d = kc.to(DEV), vc.to(DEV)
+    for b in range(B):
+        nv = min(n_cmp[b], lens[b] // m)
+        kc_d[b, nv:] = float("nan")
+        vc_d[b, nv:] = float("nan")
+    out, lse = csa.hca_dense_attn_decode(
+        q.to(DEV), kc_d, vc_d, torch.tensor(n_cmp, dtype=torch.int32, device=DEV), m,
+        place_window(kw, lens, 1000) if window else None,
+        place_window(vw, lens, 1000) if window else None,
+        torch.tensor(lens, dtype=torch.int32, device=DEV), window, sink.to(DEV), return_lse=True)
+    torch.cuda.synchronize()
+    kr, base = window_arrays(kw, lens)
+    vr, _ = window_arrays(vw, lens)
+    ro, rl = oracle.hca_decode(u16(q), u16(kc), u16(vc), np.array(n_cmp), m,
+                               kr if window else None, vr if window else None, np.array(lens),
+                               window, sink.numpy(), 1.0, base)
+    check_attention(out, ro, lse, rl, f"hca window={window}")
+    if window == 0:  # sequence 3 sees nothing: output 0, lse = sink
+        assert torch.all(out[3] == 0)
+        np.testing.assert_allclose(lse[3].cpu().numpy(), sink.numpy(), rtol=1e-6)
+
+
+def test_prefill_parity(cuda_device):
+    B, T, H, N_cap, k, W, m = 2, 37, 64, 140, 48, 128, 4
+    q_pos = np.array([[500 + t for t in range(T)], [100 + 3 * t for t in range(T)]], np.int32)
+    L_cap = 700
+    q = synth.randn((B, T, H, 128), 61, 1, scale=1 / math.sqrt(128))
+    kc, vc = synth.randn((B, N_cap, 128), 61, 2), synth.randn((B, N_cap, 128), 61, 3)
+    kr, vr = synth.randn((B, L_cap, 128), 61, 4), synth.randn((B, L_cap, 128), 61, 5)
+    sink = synth.randn((H,), 61, 6, dtype=torch.float32)
+    n_vis = np.minimum(N_cap, (q_pos + 1) // m)
+    g = np.random.default_rng(4)
+    sel = np.full((B, T, k), -1, np.int32)
+    for b in range(B):
+        for t in range(T):
+            take = min(k, n_vis[b, t])
+            sel[b, t, :take] = np.sort(g.choice(n_vis[b, t], take, replace=False))
+    kr_d, vr_d = kr.to(DEV), vr.to(DEV)
+    kr_d[:, 611:] = float("nan")  # beyond the last query position
+    vr_d[:, 611:] = float("nan")
+    out, lse = csa.sparse_attn_prefill(
+        q.to(DEV), kc.to(DEV), vc.to(DEV), torch.from_numpy(sel).to(DEV), kr_d, vr_d,
+        torch.from_numpy(q_pos).to(DEV), W, sink.to(DEV), return_lse=True)
+    torch.cuda.synchronize()
+    ro, rl = oracle.csa_prefill(u16(q), u16(kc), u16(vc), sel, u16(kr), u16(vr), q_pos, W,
+                                sink.numpy(), 1.0)
+    check_attention(out, ro, lse, rl, "prefill")
+
+
+def test_softmax_scale_is_applied(cuda_device):
+    B, H, N_cap, k = 2, 32, 64, 16
+    lens = [256, 256]
+    q, kc, vc, kw, vw, sink = _attn_inputs(B, H, N_cap, lens, seed=77)
+    q = (q.float() * math.sqrt(128)).to(torch.bfloat16)  # unscaled query
+    sel = _random_topk(B, k, [64, 64], seed=2)
+    L = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    out = csa.sparse_attn_decode(q.to(DEV), kc.to(DEV), vc.to(DEV),
+                                 torch.from_numpy(sel).to(DEV), place_window(kw, lens, 256),
+                                 place_window(vw, lens, 256), L, 128, sink.to(DEV),
+                                 softmax_scale=1 / math.sqrt(128))
+    kr, base = window_arrays(kw, lens)
+    vr, _ = window_arrays(vw, lens)
+    ro, _ = oracle.csa_decode(u16(q), u16(kc), u16(vc), sel, kr, vr, np.array(lens), 128,
+                              sink.numpy(), 1 / math.sqrt(128), base)
+    check_attention(out, ro, what="softmax scale")
+
+
+# ---------------------------------------------------------------- errors, determinism
+
+def test_bad_indices_and_positions_set_the_error_word(cuda_device):
+    B, H, N_cap, k = 2, 64, 64, 8
+    lens = [200, 200]
+    q, kc, vc, kw, vw, sink = _attn_inputs(B, H, N_cap, lens, seed=88)
+    sel = _random_topk(B, k, [50, 50], seed=3)
+    bad = sel.copy()
+    bad[0, 2] = N_cap + 5  # out of range: skipped and flagged
+    bad[1, 3] = -7
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    L = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    kr_d, vr_d = place_window(kw, lens, 256), place_window(vw, lens, 256)
+    out = csa.sparse_attn_decode(q.to(DEV), kc.to(DEV), vc.to(DEV),
+                                 torch.from_numpy(bad).to(DEV), kr_d, vr_d, L, 128,
+                                 sink.to(DEV), err_word=err)
+    torch.cuda.synchronize()
+    assert err.item() & csa.EW_BAD_INDEX
+    assert torch.isfinite(out.float()).all()
+    # the flagged entries are skipped, exactly as if they were padding
+    skip = bad.copy()
+    skip[0, 2] = -1
+    skip[1, 3] = -1
+    kr, base = window_arrays(kw, lens)
+    vr, _ = window_arrays(vw, lens)
+    ro, _ = oracle.csa_decode(u16(q), u16(kc), u16(vc), skip, kr, vr, np.array(lens), 128,
+                              sink.numpy(), 1.0, base)
+    check_attention(out, ro, what="skipped bad indices")
+    # a length beyond the raw cache: flagged, window dropped, no fault
+    err.zero_()
+    L2 = torch.tensor([200, 900], dtype=torch.int32, device=DEV)
+    csa.sparse_attn_decode(q.to(DEV), kc.to(DEV), vc.to(DEV), torch.from_numpy(sel).to(DEV),
+                           kr_d, vr_d, L2, 128, sink.to(DEV), err_word=err)
+    torch.cuda.synchronize()
+    assert err.item() & csa.EW_BAD_POSITION
+
+
+def test_determinism_bitwise(cuda_device):
+    wl = synth.Workload("det", "csa_decode", B=4, L=16384, m=4, H=64, k=512)
+    from sparse_attention_28_b300.steps import make_step
+    step = make_step(synth.make_inputs(wl, seed=3, device=DEV), DEV)
+    a = step().clone()
+    ia = step.idx.clone()
+    b = step().clone()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert torch.equal(ia, step.idx)
