@@ -7,7 +7,8 @@
 A step is one pass of the workload's hot path over one batch of synthetic
 inputs resident in HBM (see synth.WORKLOADS; default: CSA decode at 128K
 context, batch 32).  The step is captured once in a CUDA graph per stage and
-replayed; L2 is flushed (a 2x-L2 write) before every timed step, outside the
+replayed; L2 is flushed (a 2x-L2 write, then a 2x-L2 read) before every timed
+step, outside the
 timed events.  ``value`` is whole-job queries/s (tokens/s for prefill) over
 all ranks; ``e2e`` is the same metric through the public Python API with the
 step's inputs copied from pinned host memory and its output copied back
@@ -176,6 +177,20 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
+class L2Flush:
+    """Evicts L2 between timed steps: writes one 2x-L2 buffer, then reads a
+    second one, so that L2 ends up holding clean unrelated lines (a write-only
+    flush would leave dirty lines whose write-back lands in the timed step)."""
+
+    def __init__(self, l2_bytes: int, dev):
+        self.w = torch.empty(2 * l2_bytes, dtype=torch.uint8, device=dev)
+        self.r = torch.ones(2 * l2_bytes // 4, dtype=torch.int32, device=dev)
+
+    def __call__(self):
+        self.w.zero_()
+        self.sink = self.r.sum()
+
+
 # ---------------------------------------------------------------- CPU oracle leg
 
 class OracleRunner:
@@ -297,7 +312,7 @@ def main():
     torch.cuda.synchronize()
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    flush = L2Flush(l2, dev)
     stream = torch.cuda.current_stream(dev)
     n_st = len(graphs)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_st + 1)]
@@ -310,7 +325,7 @@ def main():
     sampler.start()
     time.sleep(0.25)
     for i in range(args.steps):
-        flush.zero_()
+        flush()
         evs[i][0].record(stream)
         for s, (_, g) in enumerate(graphs):
             g.replay()
@@ -375,7 +390,7 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "e4m3-indexer+bf16" if wl.idx_fp8 else "bf16", "data": "synthetic",
-        "config": dict(cfg, l2="flushed before every step (2x L2 write, untimed)",
+        "config": dict(cfg, l2="flushed before every step (2x L2 write + 2x L2 read, untimed)",
                        timing="CUDA graph per stage, CUDA events"),
         "roofline": roof, "stages": stage_report, "cpu_baseline": cpu, "e2e": e2e,
         "clocks": clocks, "gpu_launches": launches,
@@ -420,7 +435,7 @@ def run_e2e(args, wl, step, dev, flush, world, dist):
     stream = torch.cuda.current_stream(dev)
     times = []
     for i in range(args.steps):
-        flush.zero_()
+        flush()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for h, d in pairs:

@@ -79,9 +79,12 @@ __global__ void __launch_bounds__(NW * 32) attn_partial_kernel(AttnArgs a) {
   const int b = qid / a.T;
 
   // ---- the query's key set
-  int64_t t = a.pos_is_len ? (int64_t)__ldg(a.pos + b) - 1 : (int64_t)__ldg(a.pos + qid);
-  bool t_ok = t >= 0 && t < a.raw_cap;
-  if (!t_ok && tid == 0) flag_error(a.err, CSA_EW_BAD_POSITION);
+  const int64_t t = a.pos_is_len ? (int64_t)__ldg(a.pos + b) - 1 : (int64_t)__ldg(a.pos + qid);
+  // the window part needs the position inside the raw cache; visibility of
+  // compressed entries only needs t >= 0
+  const bool win_ok = a.window > 0 && t >= 0 && t < a.raw_cap;
+  if (tid == 0 && (t < 0 || (a.window > 0 && t >= a.raw_cap)))
+    flag_error(a.err, CSA_EW_BAD_POSITION);
   int n_c;
   if (!a.dense) {
     n_c = a.sel_count;
@@ -91,12 +94,12 @@ __global__ void __launch_bounds__(NW * 32) attn_partial_kernel(AttnArgs a) {
       if (tid == 0) flag_error(a.err, CSA_EW_BAD_POSITION);
       present = present < 0 ? 0 : a.N_cap;
     }
-    int64_t nv = t_ok ? (t + 1) / a.m_prime : 0;
+    const int64_t nv = t >= 0 ? (t + 1) / a.m_prime : 0;
     n_c = (int)(nv < present ? nv : present);
   }
   int64_t win_lo = t - a.window + 1;
   if (win_lo < 0) win_lo = 0;
-  const int n_w = (t_ok && a.window > 0) ? (int)(t - win_lo + 1) : 0;
+  const int n_w = win_ok ? (int)(t - win_lo + 1) : 0;
   const int n_keys = n_c + n_w;
   const int k_begin = split * a.keys_per_split;
   int k_end = k_begin + a.keys_per_split;

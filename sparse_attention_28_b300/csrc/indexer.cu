@@ -36,6 +36,7 @@ constexpr int kChunk = 2048;       // entries per score CTA
 constexpr int kUnroll = 4;         // 16-entry groups in flight per warp
 constexpr int kMarkThreads = 256;
 constexpr int kMarkSlice = 8192;   // entries per mark CTA
+constexpr int kMarkUnroll = 8;     // 32-entry words per warp per run
 constexpr int kSelThreads = 512;
 constexpr int kQueryChunk = 256;   // queries per pass (bounds the workspace)
 constexpr int kHdrWords = kHistBins + 32;  // hist[4096], cand counter, pad
@@ -284,21 +285,33 @@ __global__ void __launch_bounds__(kMarkThreads) topk_mark_kernel(IndexerArgs a, 
   uint2* cand = L.cand + (int64_t)lq * kCandCap;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t s1 = (s0 + kMarkSlice < nv) ? s0 + kMarkSlice : nv;
-  for (int64_t base = s0 + warp * 32; base < s1; base += kMarkThreads) {
-    const int64_t i = base + lane;
-    const bool in = i < s1;
-    const uint32_t key = in ? score_key(scores[i]) : 0u;
-    const uint32_t bin = key >> 20;
-    const unsigned above = __ballot_sync(0xFFFFFFFFu, in && bin > bstar);
-    const unsigned at = __ballot_sync(0xFFFFFFFFu, in && bin == bstar);
-    if (lane == 0) bm[base >> 5] = above;
-    if (at) {
-      int slot0 = 0;
-      if (lane == 0) slot0 = atomicAdd(counter, __popc(at));
-      slot0 = __shfl_sync(0xFFFFFFFFu, slot0, 0);
-      if ((at >> lane) & 1u) {
-        const int slot = slot0 + __popc(at & ((1u << lane) - 1u));
-        if (slot < kCandCap) cand[slot] = make_uint2(key, (uint32_t)i);
+  // each warp takes runs of kMarkUnroll * 32 consecutive entries; all loads of
+  // a run are issued before any is used
+  for (int64_t run = s0 + (int64_t)warp * kMarkUnroll * 32; run < s1;
+       run += (int64_t)kMarkThreads * kMarkUnroll) {
+    uint32_t key[kMarkUnroll];
+#pragma unroll
+    for (int u = 0; u < kMarkUnroll; ++u) {
+      const int64_t i = run + u * 32 + lane;
+      key[u] = i < s1 ? score_key(scores[i]) : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < kMarkUnroll; ++u) {
+      const int64_t base = run + u * 32;
+      if (base >= s1) break;
+      const bool in = base + lane < s1;
+      const uint32_t bin = key[u] >> 20;
+      const unsigned above = __ballot_sync(0xFFFFFFFFu, in && bin > bstar);
+      const unsigned at = __ballot_sync(0xFFFFFFFFu, in && bin == bstar);
+      if (lane == 0) bm[base >> 5] = above;
+      if (at) {
+        int slot0 = 0;
+        if (lane == 0) slot0 = atomicAdd(counter, __popc(at));
+        slot0 = __shfl_sync(0xFFFFFFFFu, slot0, 0);
+        if ((at >> lane) & 1u) {
+          const int slot = slot0 + __popc(at & ((1u << lane) - 1u));
+          if (slot < kCandCap) cand[slot] = make_uint2(key[u], (uint32_t)(base + lane));
+        }
       }
     }
   }

@@ -12,6 +12,20 @@ LSE_ABS = 1e-3
 NEAR_TIE_REL = 1e-6
 
 
+# Compressed entries: one bf16 ulp of the exact value (rounding) plus the
+# fp32 evaluation error of the gate logits and the weighted sum.  With
+# |x| <~ 6, d = 128, and fp32 sums the absolute error stays below ~1e-6, which
+# matters only where y is tiny (cancellation) and its ulp smaller than that.
+COMPRESS_ABS = 2.0 ** -19
+
+
+def bf16_bound(y):
+    """Allowed |gpu - y| for a bf16 compressed entry with exact value y."""
+    a = np.abs(np.asarray(y, np.float64))
+    ulp = 2.0 ** (np.floor(np.log2(np.maximum(a, 2.0 ** -126))) - 7)
+    return ulp + COMPRESS_ABS
+
+
 def u16(t: torch.Tensor) -> np.ndarray:
     """bf16 tensor -> numpy uint16 bit patterns (CPU copy)."""
     return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)

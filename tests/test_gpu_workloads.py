@@ -8,7 +8,7 @@ import torch
 import oracle
 import sparse_attention_28_b300 as csa
 import synth
-from _util import check_attention, check_topk, f64, u8, u16
+from _util import bf16_bound, check_attention, check_topk, f64, u8, u16
 from oracle.feed import fill_new_entries, idx_dtype, oracle_inputs
 from sparse_attention_28_b300.steps import make_step
 
@@ -27,8 +27,7 @@ def _run(name):
 
 def _check_bf16_entries(gpu, y, what):
     g = f64(gpu)
-    ulp = 2.0 ** (np.floor(np.log2(np.abs(y))) - 7)
-    assert np.all(np.abs(g - y) <= ulp), f"{what}: more than 1 bf16 ulp from the exact value"
+    assert np.all(np.abs(g - y) <= bf16_bound(y)), f"{what}: beyond 1 bf16 ulp + fp32 error"
 
 
 def _check_decode(name, seqs):
