@@ -28,7 +28,8 @@
  *   - `err_word` (optional, device int32) receives bit flags OR-ed in by the
  *     kernels when they meet an input they cannot honour (they skip it and
  *     never trap): CSA_EW_BAD_INDEX (a top-k index outside [-1, N_cap)),
- *     CSA_EW_BAD_POSITION (a position or length outside the cache or < 0).
+ *     CSA_EW_BAD_POSITION (a position or length outside the cache or < 0),
+ *     CSA_EW_TIMEOUT (an internal pipeline wait expired; outputs invalid).
  *     The word is never cleared by the library; the caller reads it when it
  *     chooses.
  *   - Numbers: bf16 inputs, fp32 accumulation, bf16 outputs rounded to
@@ -61,6 +62,7 @@ extern "C" {
 /* err_word bits */
 #define CSA_EW_BAD_INDEX 1
 #define CSA_EW_BAD_POSITION 2
+#define CSA_EW_TIMEOUT 4 /* a bounded device-side wait gave up (should never happen) */
 
 /* element types */
 #define CSA_BF16 0
@@ -83,8 +85,9 @@ CSA_API int csa_abi_version(void);
  *     y[j][c] = sum_i softmax_i(g[.][c])[i] * x[j*m+i][c]
  * Blocks [block_begin, block_begin + n_blocks) of every sequence are written.
  *
- *   raw       bf16 [B][raw_bstride]: token rows of d; block j reads rows
- *             j*m .. j*m+m-1.
+ *   raw       bf16 [B][raw_bstride]: token rows of d, a ring of raw_cap rows:
+ *             position p is row p mod raw_cap; block j reads positions
+ *             j*m .. j*m+m-1 (raw_cap >= m).
  *   W         bf16 [d][d] (row = output channel), pos_bias fp32 [m][d].
  *   out       out_dtype == CSA_BF16: bf16 [B][out_bstride], row j of d.
  *             out_dtype == CSA_FP8_E4M3: E4M3 bytes, row j of d, plus
@@ -93,8 +96,8 @@ CSA_API int csa_abi_version(void);
  *             saturating at 448.
  *   d in {64, 128}; 1 <= m <= 256.
  * ---------------------------------------------------------------------- */
-CSA_API int csa_compress_kv(const void* raw, int64_t raw_bstride, int B, int d, int m,
-                    int block_begin, int n_blocks, const void* W, const float* pos_bias,
+CSA_API int csa_compress_kv(const void* raw, int64_t raw_bstride, int64_t raw_cap, int B, int d,
+                    int m, int block_begin, int n_blocks, const void* W, const float* pos_bias,
                     void* out, int64_t out_bstride, int out_dtype, float* out_scale,
                     int64_t scale_bstride, int32_t* err_word, void* stream);
 
@@ -149,15 +152,21 @@ CSA_API int csa_indexer_topk(const void* q_idx, const float* q_scale, const floa
  * (k_cmp == v_cmp, k_raw == v_raw).
  *
  *   q         bf16 [B][H][D] (decode) or [B][T][H][D] (prefill).
- *   k_cmp, v_cmp  bf16 [B][cmp_bstride], rows of D; N_cap rows per sequence.
- *   k_raw, v_raw  bf16 [B][raw_bstride], row p = absolute position p;
- *             raw_cap rows per sequence.
+ *   k_cmp, v_cmp  bf16 [B][cmp_bstride], rows of D; N_cap rows per sequence;
+ *             cmp_bstride a multiple of D (the caches are read as one 2-D
+ *             array of 256-byte rows).
+ *   k_raw, v_raw  bf16 [B][raw_bstride]: a ring of raw_cap rows per
+ *             sequence, position p at row p mod raw_cap (raw_cap >= window;
+ *             a cache at full length is the case raw_cap > every position);
+ *             raw_bstride a multiple of D.
  *   seq_len   int32 [B] (decode: t = seq_len - 1, the token's own K/V is
  *             already in the raw cache); q_pos int32 [B][T] (prefill).
  *   out       bf16, same shape as q; lse fp32 [B][(T)][H] (optional).
  *   ws        csa_attn_workspace(B, T, H, n_keys_max) bytes, where n_keys_max
  *             is the largest key-set size (k + window for CSA; the largest
- *             n_vis + window for HCA).  Zero bytes may be needed.
+ *             n_vis + window for HCA).  This build needs none (it returns 0:
+ *             the key splits of a query run as one thread-block cluster and
+ *             merge through distributed shared memory); ws may be NULL.
  *   H in {16, 32, 64, 128}; D == 128.
  * ---------------------------------------------------------------------- */
 CSA_API size_t csa_attn_workspace(int B, int T, int H, int n_keys_max);

@@ -62,7 +62,8 @@ def lib() -> ctypes.CDLL:
             L.csa_status_str.argtypes = [I]
             L.csa_status_str.restype = ctypes.c_char_p
             L.csa_abi_version.restype = I
-            L.csa_compress_kv.argtypes = [P, I64, I, I, I, I, I, P, P, P, I64, I, P, I64, P, P]
+            L.csa_compress_kv.argtypes = [P, I64, I64, I, I, I, I, I, P, P, P, I64, I, P, I64, P,
+                                          P]
             L.csa_compress_kv.restype = I
             L.csa_indexer_topk_workspace.argtypes = [I, I, I, I]
             L.csa_indexer_topk_workspace.restype = SZ
@@ -131,7 +132,8 @@ def compress_kv(raw, W, pos_bias, m: int, block_begin: int, n_blocks: int, out,
                 out_scale=None, err_word=None):
     """Compress blocks [block_begin, block_begin+n_blocks) of every sequence.
 
-    raw: bf16 [B, L_cap, d]; W: bf16 [d, d]; pos_bias: fp32 [m, d];
+    raw: bf16 [B, R, d], a ring of R rows (position p at row p mod R; a
+    full-length cache is R > every position); W: bf16 [d, d]; pos_bias: fp32 [m, d];
     out: bf16 [B, N_cap, d] or uint8 [B, N_cap, d] (E4M3 codes, then
     out_scale fp32 [B, N_cap] is required).  Writes in place; returns out.
     """
@@ -147,7 +149,8 @@ def compress_kv(raw, W, pos_bias, m: int, block_begin: int, n_blocks: int, out,
         _cuda(out_scale, "out_scale", torch.float32)
         _need(out_scale.dim() == 2 and out_scale.stride(1) == 1, "out_scale [B, N_cap]")
     st = lib().csa_compress_kv(
-        _p(raw), _bstride(raw), B, d, m, block_begin, n_blocks, _p(W), _p(pos_bias), _p(out),
+        _p(raw), _bstride(raw), raw.shape[1], B, d, m, block_begin, n_blocks, _p(W), _p(pos_bias),
+        _p(out),
         _bstride(out), CSA_FP8_E4M3 if fp8 else CSA_BF16, _p(out_scale) if fp8 else None,
         out_scale.stride(0) if fp8 else 0, _p(err_word), _stream(raw.device))
     _check(st, "csa_compress_kv")
@@ -226,7 +229,8 @@ def sparse_attn_decode(q, k_cmp, v_cmp, topk_idx, k_raw, v_raw, seq_len, window:
                        softmax_scale: float = 1.0, return_lse: bool = False, out=None, ws=None,
                        err_word=None):
     """CSA decode attention.  q: bf16 [B, H, 128]; k_cmp/v_cmp: bf16 [B, N_cap, 128];
-    topk_idx: int32 [B, k]; k_raw/v_raw: bf16 [B, L_cap, 128]; seq_len: int32 [B];
+    topk_idx: int32 [B, k]; k_raw/v_raw: bf16 [B, R, 128], a ring of R rows
+    (position p at row p mod R, R >= window); seq_len: int32 [B];
     sink: fp32 [H] or None.  Returns bf16 [B, H, 128] [, lse fp32 [B, H]]."""
     _attn_common(q, k_cmp, v_cmp, k_raw, v_raw, sink)
     _cuda(topk_idx, "topk_idx", torch.int32)

@@ -47,14 +47,19 @@ int check_attention_common(const void* q, const void* k_cmp, const void* v_cmp,
   if (D != kD || !heads_supported(H)) return CSA_ERR_UNSUPPORTED;
   if (B == 0 || T == 0) return CSA_OK;
   if (!q || !out || !aligned16(q) || !aligned16(out)) return CSA_ERR_INVALID_ARG;
+  // caches are read as 2-D views of 256-byte rows spanning all sequences
   if (N_cap > 0) {
     if (!k_cmp || !v_cmp || !aligned16(k_cmp) || !aligned16(v_cmp)) return CSA_ERR_INVALID_ARG;
-    if (cmp_bstride % 8 != 0 || cmp_bstride < (int64_t)N_cap * D) return CSA_ERR_INVALID_ARG;
+    if (cmp_bstride % D != 0 || cmp_bstride < (int64_t)N_cap * D) return CSA_ERR_INVALID_ARG;
+    if ((B - 1) * (cmp_bstride / D) + N_cap >= (int64_t(1) << 31)) return CSA_ERR_UNSUPPORTED;
   }
   if (window > 0) {
     if (!k_raw || !v_raw || !aligned16(k_raw) || !aligned16(v_raw)) return CSA_ERR_INVALID_ARG;
-    if (raw_bstride % 8 != 0 || raw_bstride < raw_cap * D) return CSA_ERR_INVALID_ARG;
+    if (raw_cap < window || raw_bstride % D != 0 || raw_bstride < raw_cap * D)
+      return CSA_ERR_INVALID_ARG;
+    if ((B - 1) * (raw_bstride / D) + raw_cap >= (int64_t(1) << 31) - 2) return CSA_ERR_UNSUPPORTED;
   }
+  if ((int64_t)B * T * H >= (int64_t(1) << 31)) return CSA_ERR_UNSUPPORTED;
   if (sink && !aligned4(sink)) return CSA_ERR_INVALID_ARG;
   if (lse && !aligned4(lse)) return CSA_ERR_INVALID_ARG;
   return CSA_OK;
@@ -82,8 +87,8 @@ const char* csa_status_str(int status) {
 int csa_abi_version(void) { return 1; }
 
 // ---------------------------------------------------------------- a1
-int csa_compress_kv(const void* raw, int64_t raw_bstride, int B, int d, int m, int block_begin,
-                    int n_blocks, const void* W, const float* pos_bias, void* out,
+int csa_compress_kv(const void* raw, int64_t raw_bstride, int64_t raw_cap, int B, int d, int m,
+                    int block_begin, int n_blocks, const void* W, const float* pos_bias, void* out,
                     int64_t out_bstride, int out_dtype, float* out_scale, int64_t scale_bstride,
                     int32_t* err_word, void* stream) {
   (void)err_word;
@@ -94,7 +99,7 @@ int csa_compress_kv(const void* raw, int64_t raw_bstride, int B, int d, int m, i
   if (!raw || !W || !pos_bias || !out) return CSA_ERR_INVALID_ARG;
   if (!aligned16(raw) || !aligned16(W) || !aligned4(pos_bias)) return CSA_ERR_INVALID_ARG;
   const int64_t end_block = (int64_t)block_begin + n_blocks;
-  if (raw_bstride % 8 != 0 || end_block * m * d > raw_bstride) return CSA_ERR_INVALID_ARG;
+  if (raw_cap < m || raw_bstride % 8 != 0 || raw_cap * d > raw_bstride) return CSA_ERR_INVALID_ARG;
   if (end_block * d > out_bstride) return CSA_ERR_INVALID_ARG;
   if (out_dtype == CSA_FP8_E4M3) {
     if (!out_scale || !aligned4(out_scale) || end_block > scale_bstride) return CSA_ERR_INVALID_ARG;
@@ -102,6 +107,7 @@ int csa_compress_kv(const void* raw, int64_t raw_bstride, int B, int d, int m, i
   CompressArgs a;
   a.raw = reinterpret_cast<const bf16*>(raw);
   a.raw_bstride = raw_bstride;
+  a.raw_cap = raw_cap;
   a.B = B;
   a.d = d;
   a.m = m;
@@ -240,6 +246,7 @@ int csa_sparse_attn_decode(const void* q, const void* k_cmp, const void* v_cmp,
   a.pos = seq_len;
   a.pos_is_len = 1;
   a.T = 1;
+  a.n_batch = B;
   a.n_query = B;
   a.n_keys_max = k + window;
   return run_attention(a, ws, ws_bytes, stream);
@@ -268,6 +275,7 @@ int csa_sparse_attn_prefill(const void* q, const void* k_cmp, const void* v_cmp,
   a.pos = q_pos;
   a.pos_is_len = 0;
   a.T = T;
+  a.n_batch = B;
   a.n_query = B * T;
   a.n_keys_max = k + window;
   return run_attention(a, ws, ws_bytes, stream);
@@ -294,6 +302,7 @@ int hca_dense_attn_decode(const void* q, const void* k_cmp, const void* v_cmp,
   a.pos = seq_len;
   a.pos_is_len = 1;
   a.T = 1;
+  a.n_batch = B;
   a.n_query = B;
   a.n_keys_max = N_cap + window;
   return run_attention(a, ws, ws_bytes, stream);

@@ -1,97 +1,202 @@
 // attn.cu -- MQA attention over a gathered key set (compressed entries chosen
-// by top-k or all visible ones, plus the raw sliding window), with an
-// attention-sink logit; split over keys, merged by log-sum-exp.
+// by top-k, or all visible ones, plus the raw sliding window) with an
+// attention-sink logit, on the fifth-generation tensor cores (tcgen05/TMEM);
+// the keys of one query are split across a thread-block cluster and the
+// partial results merged through distributed shared memory.
 //
 // Method: hyper.ai DeepSeek-V4 page, Method (MQA core attention over the
 // top-k compressed entries; HCA dense over all entries; sliding-window
 // branch); aiboss88 DeepSeek-V4 page, Technical Principles (window + attention
 // sink); elamur.ai page, References [20] (flash-decoding: split the key range
-// over many CTAs, merge the partial softmax results by their log-sum-exp).
+// over many CTAs, merge the partial softmax results by log-sum-exp).
 //
-// Design (B300): all H heads of one query token share every K/V row (MQA), so
-// the H x D query block is the M side of a tensor-core contraction and each
-// gathered 256-byte K/V row is read from HBM once per (query, split).  A CTA
-// owns one (query, key split); warp w owns heads 16w..16w+15.  K/V rows are
-// gathered by 16-byte cp.async into an XOR-swizzled, double-buffered shared
-// tile of 64 keys; S = Q K^T and O += P V use m16n8k16 bf16 MMAs with fp32
-// accumulators; the online softmax runs in the base-2 domain.
+// One CTA owns one (query token, key split); the splits of a query form one
+// cluster.  All H heads share each K/V row (MQA), so the H x 128 query block is
+// the M side of the contractions (M = 64 for H <= 64, else 128) and every
+// gathered 256-byte K/V row is read from memory once.  Key slots: compressed
+// entries [0, n_c), padding to a multiple of 4, then the window.
+// Warp roles:
+//   warp 0       one thread issues tcgen05.mma and commits; owns TMEM
+//   loader warps (1-3, and 8-11 when M = 64): per 64-key tile, one row lookup
+//                per key, then either one TMA box per (tensor, K-block) when
+//                the 64 rows are contiguous, or 16-byte cp.async row gathers
+//                from every loader thread, into a ring of SW128 stages
+//                (skipped slots are zero-filled)
+//   warps 4-7    softmax on the 16-lane TMEM layout (four threads share a row,
+//                all 32 lanes busy): base-2 online softmax with lazy
+//                rescaling (O in TMEM is rescaled only when a row's running
+//                max grows by more than 2^8); P (bf16) to shared memory
+// Per 64-key tile: S = Q K^T as 8 MMAs of M x 64 x 16 into one of two TMEM
+// buffers; O += P V as 4 MMAs of M x 128 x 16 into a TMEM accumulator.
+// Every mbarrier wait is bounded; on timeout the CTA records CSA_EW_TIMEOUT in
+// the error word, still reaches every barrier, and frees its TMEM.
 #include "common.cuh"
 #include "kernels.h"
+#include "tc.cuh"
+#include "tma.cuh"
 
 namespace csa {
 
 namespace {
 
-constexpr int kTileKeys = 64;
 constexpr int kD = 128;
-constexpr int kRowBytes = kD * 2;                   // 256
-constexpr int kTileBytes = kTileKeys * kRowBytes;   // 16 KB
-constexpr int kStageBytes = 2 * kTileBytes;         // K + V
+constexpr int kTile = 64;  // keys per tile / stage
+constexpr int kStageBytes = 32768;  // K: 2 K-blocks x [64 x 128 B]; V: 2 blocks
+constexpr int kSoftWarp0 = 4;
+constexpr int kSoftThreads = 128;
+constexpr int kMaxCluster = 16;
+constexpr uint32_t kWaitLimit = 1u << 24;
 
-// Virtual key slot v of a query -> (pointer to K row, pointer to V row), or
-// invalid.  Slots [0, n_c) are compressed entries, [n_c, n_c + n_w) the raw
-// window rows win_lo .. t.
-struct KeySource {
-  const bf16* kc;
-  const bf16* vc;
-  const bf16* kr;
-  const bf16* vr;
-  const int32_t* sel;  // nullptr: dense (slot v -> entry v)
-  int n_c;
+// TMEM columns
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kSCol = 0;    // S buffer b at column 64 * b
+constexpr uint32_t kOCol = 128;  // O accumulator
+
+template <int M>
+struct Cfg {
+  static constexpr int kThreads = M == 64 ? 384 : 256;
+  static constexpr int kLoadThreads = M == 64 ? 224 : 96;  // warps 1-3 (+ 8-11)
+  static constexpr int kStages = M == 64 ? 6 : 5;
+  static constexpr int kQBytes = M * 256;    // 2 K-blocks x [M x 128 B]
+  static constexpr int kPBytes = M * 128;    // one K-block of 64 keys per buffer
+  static constexpr int kQOff = 0;
+  static constexpr int kKVOff = kQBytes;
+  static constexpr int kPOff = kKVOff + kStages * kStageBytes;
+  static constexpr int kMetaOff = kPOff + 2 * kPBytes;  // stages x 64 row codes
+  static constexpr int kBarOff = kMetaOff + kStages * kTile * 4;
+  static constexpr int kSmemBytes = kBarOff + 512 + 1024;  // + alignment slack
+  // after the main loop: partial O rows (fp32) in stages 0-1, lse + merge
+  // weights in the P buffers
+  static constexpr int kPartOff = kKVOff;
+  static constexpr int kPartLseOff = kPOff;
+  static constexpr int kWgtOff = kPOff + 512;
+  static_assert(kSmemBytes <= 232448, "shared memory");
+  static_assert(2 * kStageBytes >= M * 512, "partial O fits in two stages");
+  static_assert(2 * kPBytes >= 512 + 4 * 64 * kMaxCluster, "merge scratch fits in P");
+};
+
+struct Bars {
+  uint64_t kv_full[6];
+  uint64_t kv_empty[6];
+  uint64_t meta_full[6];  // validity bits of the stage's tile published
+  uint64_t s_full[2];
+  uint64_t s_free[2];
+  uint64_t p_full[2];
+  uint64_t p_free[2];
+  uint64_t q_full;
+  uint32_t tmem_slot;
+  int timed_out;
+  uint32_t valid[6][2];
+  uint32_t dense[6][2];  // per loader warp 0/1: its 32 rows continue row 0's run
+};
+
+// Tensor maps: the query block, and boxes of 64 rows that load a whole tile
+// of contiguous compressed entries.
+struct Maps {
+  CUtensorMap q, kc, vc;
+};
+
+// Slot -> row code: r >= 0 is row r of the 2-D row view of the compressed
+// caches, -1 a skipped slot, -(r + 2) row r of the raw (window) caches.  Row
+// counts below 2^31 - 2 are checked on the host.
+
+struct KeySet {
+  const int32_t* sel;  // nullptr: dense
+  int n_c, n_c4;
   int n_cap;
-  int64_t win_lo;
-  int32_t* err;
+  int64_t cmp_row0;  // b * cmp rows per sequence
+  int64_t raw_row0;  // b * raw rows per sequence
+  int64_t win_row0;  // ring row of the window's first position
+  int64_t raw_cap;
+  int k_end;
 
-  __device__ __forceinline__ bool row(int v, int64_t& off, bool& raw) const {
+  __device__ __forceinline__ int32_t code(int v, int32_t* err) const {
+    if (v >= k_end) return -1;
     if (v < n_c) {
       int64_t e = v;
       if (sel) {
-        int32_t s = __ldg(sel + v);
-        if (s < 0) {
+        const int32_t s = __ldg(sel + v);
+        if (s < 0 || s >= n_cap) {
           if (s != -1) flag_error(err, CSA_EW_BAD_INDEX);
-          return false;
-        }
-        if (s >= n_cap) {
-          flag_error(err, CSA_EW_BAD_INDEX);
-          return false;
+          return -1;
         }
         e = s;
       }
-      off = e * kD;
-      raw = false;
-      return true;
+      return (int32_t)(cmp_row0 + e);
     }
-    off = (win_lo + (v - n_c)) * kD;
-    raw = true;
-    return true;
+    if (v < n_c4) return -1;  // padding
+    int64_t r = win_row0 + (v - n_c4);
+    if (r >= raw_cap) r -= raw_cap;
+    return (int32_t)(-(raw_row0 + r) - 2);
   }
 };
 
-template <int NW>
-__global__ void __launch_bounds__(NW * 32) attn_partial_kernel(AttnArgs a) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  constexpr int NT = NW * 32;
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5, lane = tid & 31;
-  const int g = lane >> 2, c = lane & 3;
-  const int qid = blockIdx.y;
-  const int split = blockIdx.x;
-  const int b = qid / a.T;
+__device__ __forceinline__ bool wait_or_flag(uint64_t* bar, uint32_t parity, Bars* bars,
+                                             int32_t* err) {
+  if (tc::mbar_wait(bar, parity, kWaitLimit)) return true;
+  atomicExch(&bars->timed_out, 1);
+  flag_error(err, CSA_EW_TIMEOUT);
+  return false;
+}
 
-  // ---- the query's key set
+// AND of a predicate over the loader threads (named barrier 1).
+template <int NL>
+__device__ __forceinline__ bool loaders_all(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.and.pred p, 1, %2, q;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)v), "n"(NL)
+      : "memory");
+  return r != 0;
+}
+template <int NL>
+__device__ __forceinline__ void loaders_sync() {
+  asm volatile("bar.sync 1, %0;\n" ::"n"(NL) : "memory");
+}
+
+template <int M>
+struct RowMap {  // softmax-thread view of the 16-lane TMEM layout
+  static constexpr int NG = M / 64;  // 16-lane groups per warp quadrant
+  __device__ __forceinline__ static int row(int qd, int g, int r8) {
+    return M == 64 ? qd * 16 + r8 : qd * 32 + g * 16 + r8;
+  }
+  __device__ __forceinline__ static uint32_t lane_field(int qd, int g) {
+    return (uint32_t)((qd * 32 + g * 16) << 16);
+  }
+};
+
+template <int M>
+__global__ void __launch_bounds__(Cfg<M>::kThreads, 1)
+    attn_tc_kernel(AttnArgs a, const __grid_constant__ Maps maps) {
+  using C = Cfg<M>;
+  constexpr int kStages = C::kStages;
+  constexpr int NL = C::kLoadThreads;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* sm = smem_raw + ((1024 - (raw_addr & 1023)) & 1023);
+  const uint32_t sbase = smem_u32(sm);
+  Bars* bars = reinterpret_cast<Bars*>(sm + C::kBarOff);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ns = a.n_split;
+  const int qid = blockIdx.x / ns, split = blockIdx.x % ns;
+  const int b = qid / a.T;
+  const int H = a.H;
+  const bool is_loader = (warp >= 1 && warp <= 3) || (M == 64 && warp >= 8);
+  const int lt = warp <= 3 ? tid - 32 : tid - 160;  // loader index (loader warps only)
+
+  // ---- the query's key set and this split's range
   const int64_t t = a.pos_is_len ? (int64_t)__ldg(a.pos + b) - 1 : (int64_t)__ldg(a.pos + qid);
-  // the window part needs the position inside the raw cache; visibility of
-  // compressed entries only needs t >= 0
-  const bool win_ok = a.window > 0 && t >= 0 && t < a.raw_cap;
-  if (tid == 0 && (t < 0 || (a.window > 0 && t >= a.raw_cap)))
-    flag_error(a.err, CSA_EW_BAD_POSITION);
+  if (tid == 0 && split == 0 && t < 0) flag_error(a.err, CSA_EW_BAD_POSITION);
   int n_c;
   if (!a.dense) {
     n_c = a.sel_count;
   } else {
     int64_t present = a.n_cmp ? (int64_t)__ldg(a.n_cmp + b) : 0;
     if (present < 0 || present > a.N_cap) {
-      if (tid == 0) flag_error(a.err, CSA_EW_BAD_POSITION);
+      if (tid == 0 && split == 0) flag_error(a.err, CSA_EW_BAD_POSITION);
       present = present < 0 ? 0 : a.N_cap;
     }
     const int64_t nv = t >= 0 ? (t + 1) / a.m_prime : 0;
@@ -99,332 +204,552 @@ __global__ void __launch_bounds__(NW * 32) attn_partial_kernel(AttnArgs a) {
   }
   int64_t win_lo = t - a.window + 1;
   if (win_lo < 0) win_lo = 0;
-  const int n_w = win_ok ? (int)(t - win_lo + 1) : 0;
-  const int n_keys = n_c + n_w;
+  const int n_w = (a.window > 0 && t >= 0) ? (int)(t - win_lo + 1) : 0;
+  const int n_c4 = n_w > 0 ? (n_c + 3) & ~3 : n_c;
+  const int n_keys = n_c4 + n_w;
   const int k_begin = split * a.keys_per_split;
   int k_end = k_begin + a.keys_per_split;
   if (k_end > n_keys) k_end = n_keys;
-  const int n_tiles = k_end > k_begin ? (k_end - k_begin + kTileKeys - 1) / kTileKeys : 0;
+  const int n_tiles = k_end > k_begin ? (k_end - k_begin + kTile - 1) / kTile : 0;
 
-  KeySource src;
-  src.kc = a.k_cmp + (int64_t)b * a.cmp_bstride;
-  src.vc = a.v_cmp + (int64_t)b * a.cmp_bstride;
-  src.kr = a.k_raw + (int64_t)b * a.raw_bstride;
-  src.vr = a.v_raw + (int64_t)b * a.raw_bstride;
-  src.sel = a.dense ? nullptr : a.sel + (int64_t)qid * a.sel_stride;
-  src.n_c = n_c;
-  src.n_cap = a.N_cap;
-  src.win_lo = win_lo;
-  src.err = a.err;
-
-  uint32_t* valid_mask = reinterpret_cast<uint32_t*>(smem + 2 * kStageBytes);  // [2][2]
-  const uint32_t smem_base = smem_u32(smem);
-
-  // Loader: chunk ci = tid + i*NT covers row ci/16, 16-byte column ci%16;
-  // 16 consecutive threads copy one 256-byte row.
-  auto load_tile = [&](int stage, int tile) {
-    const int v0 = k_begin + tile * kTileKeys;
-    const uint32_t kbase = smem_base + stage * kStageBytes;
-    const uint32_t vbase = kbase + kTileBytes;
-#pragma unroll
-    for (int i = 0; i < (kTileKeys * 16) / NT; ++i) {
-      const int ci = tid + i * NT;
-      const int r = ci >> 4, col = ci & 15;
-      const int v = v0 + r;
-      int64_t off = 0;
-      bool raw = false;
-      bool ok = v < k_end && src.row(v, off, raw);
-      // zero-fill copies read nothing; their source is any valid address
-      const bf16* kp = ok ? (raw ? src.kr : src.kc) + off + col * 8 : a.q;
-      const bf16* vp = ok ? (raw ? src.vr : src.vc) + off + col * 8 : a.q;
-      const uint32_t so = r * kRowBytes + ((col ^ (r & 7)) << 4);
-      cp_async16(kbase + so, kp, ok ? 16 : 0);
-      cp_async16(vbase + so, vp, ok ? 16 : 0);
+  // ---- set-up: barriers, TMEM, zero Q rows >= H (the MMA reads M rows)
+  if (warp == 0) {
+    tc::tmem_alloc(&bars->tmem_slot, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  if (tid == 32) {
+    for (int s = 0; s < kStages; ++s) {
+      tc::mbar_init(&bars->kv_full[s], NL + 1);
+      tc::mbar_init(&bars->kv_empty[s], 1);
+      tc::mbar_init(&bars->meta_full[s], 1);
     }
-    // validity words for rows 0..31 and 32..63 (warp w handles word w, w+NW, ..)
-    for (int wd = warp; wd < 2; wd += NW) {
-      const int v = v0 + wd * 32 + lane;
-      int64_t off;
-      bool raw;
-      const bool ok = v < k_end && src.row(v, off, raw);
-      const unsigned bal = __ballot_sync(0xFFFFFFFFu, ok);
-      if (lane == 0) valid_mask[stage * 2 + wd] = bal;
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&bars->s_full[i], 1);
+      tc::mbar_init(&bars->s_free[i], kSoftThreads);
+      tc::mbar_init(&bars->p_full[i], kSoftThreads);
+      tc::mbar_init(&bars->p_free[i], 1);
     }
-  };
+    tc::mbar_init(&bars->q_full, 1);
+    bars->timed_out = 0;
+    tc::fence_mbar_init();
+  }
+  for (int idx = tid; idx < (M - H) * 16; idx += C::kThreads) {
+    const int r = H + (idx >> 4), c16 = idx & 15;
+    *reinterpret_cast<uint4*>(sm + C::kQOff + (c16 >> 3) * (M * 128) +
+                              tc::sw128_offset(r, c16 & 7)) = make_uint4(0, 0, 0, 0);
+  }
+  tc::fence_proxy_async_smem();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = bars->tmem_slot;
 
-  // ---- Q fragments for this warp's 16 heads (rows g and g+8), 8 k-steps
-  uint32_t qa[8][4];
-  {
-    const int h0 = warp * 16 + g;
-    const uint32_t* q0 = reinterpret_cast<const uint32_t*>(a.q + ((int64_t)qid * a.H + h0) * kD);
-    const uint32_t* q1 = q0 + 8 * kD / 2;
+  if (n_tiles > 0 && warp == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t id_s = tc::idesc_bf16(M, kTile, false, false);
+      const uint32_t id_o = tc::idesc_bf16(M, kD, false, true);
+      auto issue_pv = [&](int i) -> bool {
+        const int st = i % kStages, pb = i & 1;
+        if (!wait_or_flag(&bars->p_full[pb], (i >> 1) & 1, bars, a.err)) return false;
+        tc::fence_after_sync();
+        const uint32_t p_addr = sbase + C::kPOff + pb * C::kPBytes;
+        const uint32_t v_addr = sbase + C::kKVOff + st * kStageBytes + 16384;
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      qa[kk][0] = __ldg(q0 + kk * 8 + c);
-      qa[kk][1] = __ldg(q1 + kk * 8 + c);
-      qa[kk][2] = __ldg(q0 + kk * 8 + 4 + c);
-      qa[kk][3] = __ldg(q1 + kk * 8 + 4 + c);
+        for (int s = 0; s < kTile / 16; ++s) {
+          const uint64_t ad = tc::desc_sw128(p_addr + s * 32, 16, 1024);
+          const uint64_t bd = tc::desc_sw128(v_addr + s * 2048, kTile * 128, 1024);
+          tc::mma_ss(tmem + kOCol, ad, bd, id_o, (i > 0 || s > 0) ? 1u : 0u);
+        }
+        tc::mma_commit(&bars->p_free[pb]);
+        tc::mma_commit(&bars->kv_empty[st]);
+        return true;
+      };
+      bool ok = wait_or_flag(&bars->q_full, 0, bars, a.err);
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        const int st = j % kStages, sb = j & 1;
+        ok = wait_or_flag(&bars->kv_full[st], (j / kStages) & 1, bars, a.err);
+        if (ok && j >= 2) ok = wait_or_flag(&bars->s_free[sb], ((j - 2) >> 1) & 1, bars, a.err);
+        if (!ok) break;
+        tc::fence_after_sync();
+        const uint32_t k_addr = sbase + C::kKVOff + st * kStageBytes;
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint64_t ad =
+              tc::desc_sw128(sbase + C::kQOff + (kk >> 2) * (M * 128) + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = tc::desc_sw128(k_addr + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
+          tc::mma_ss(tmem + kSCol + sb * kTile, ad, bd, id_s, kk > 0 ? 1u : 0u);
+        }
+        tc::mma_commit(&bars->s_full[sb]);
+        if (j >= 1) ok = issue_pv(j - 1);
+      }
+      if (ok) ok = issue_pv(n_tiles - 1);
+      // drain: the last commit covers every MMA this thread issued
+      if (ok) wait_or_flag(&bars->kv_empty[(n_tiles - 1) % kStages],
+                           ((n_tiles - 1) / kStages) & 1, bars, a.err);
+    }
+    __syncwarp();
+  } else if (n_tiles > 0 && is_loader) {
+    // ------------------------------------------------------------ loaders
+    KeySet ks;
+    ks.sel = a.dense ? nullptr : a.sel + (int64_t)qid * a.sel_stride;
+    ks.n_c = n_c;
+    ks.n_c4 = n_c4;
+    ks.n_cap = a.N_cap;
+    ks.cmp_row0 = (int64_t)b * (a.cmp_bstride / kD);
+    ks.raw_row0 = (int64_t)b * (a.raw_bstride / kD);
+    ks.raw_cap = a.raw_cap > 0 ? a.raw_cap : 1;
+    ks.win_row0 = win_lo % ks.raw_cap;
+    ks.k_end = k_end;
+    const bf16* kc = a.k_cmp;
+    const bf16* vc = a.v_cmp;
+    const bf16* kr = a.k_raw;
+    const bf16* vr = a.v_raw;
+    if (lt == 0) {
+      tma::expect_tx(&bars->q_full, 2 * H * 128);
+      tma::load_box(sbase + C::kQOff, &maps.q, 0, qid * H, &bars->q_full);
+      tma::load_box(sbase + C::kQOff + M * 128, &maps.q, 64, qid * H, &bars->q_full);
+    }
+    int32_t* codes = reinterpret_cast<int32_t*>(sm + C::kMetaOff);
+    // row code of this thread's row (lt < 64) for the next tile, looked up
+    // while the current tile is issued; base = the tile's first row code
+    int32_t next = lt < kTile ? ks.code(k_begin + lt, a.err) : -1;
+    int32_t next_base = ks.code(k_begin, nullptr);
+    int issued = 0;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int st = j % kStages;
+      bool go = true;
+      if (lt == 0 && j >= kStages)
+        go = wait_or_flag(&bars->kv_empty[st], ((j / kStages) - 1) & 1, bars, a.err);
+      go = go && !*(volatile int*)&bars->timed_out;
+      // every loader thread takes the same branch: named barrier 1 below
+      if (!loaders_all<NL>(go)) break;
+      const int32_t base = next_base;
+      if (lt < kTile) {
+        codes[st * kTile + lt] = next;
+        const unsigned vb = __ballot_sync(0xFFFFFFFFu, next != -1);
+        const bool cons = base >= 0 && next == base + lt;
+        const unsigned cb = __ballot_sync(0xFFFFFFFFu, cons);
+        if ((lt & 31) == 0) {
+          bars->valid[st][lt >> 5] = vb;
+          bars->dense[st][lt >> 5] = cb;
+        }
+      }
+      loaders_sync<NL>();
+      const bool dense = (bars->dense[st][0] & bars->dense[st][1]) == 0xFFFFFFFFu;
+      if (lt == 0) tc::mbar_arrive(&bars->meta_full[st]);
+      const uint32_t kdst = sbase + C::kKVOff + st * kStageBytes;
+      if (dense) {
+        if (lt == 0) {
+          tma::expect_tx(&bars->kv_full[st], kStageBytes);  // the extra arrival
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            tma::load_box(kdst + (i >> 1) * 16384 + (i & 1) * 8192, (i >> 1) ? &maps.vc : &maps.kc,
+                          (i & 1) * 64, (int)base, &bars->kv_full[st]);
+        }
+        tc::mbar_arrive(&bars->kv_full[st]);
+      } else {
+        if (lt == 0) tc::mbar_arrive(&bars->kv_full[st]);  // the extra arrival
+        for (int ci = lt; ci < kTile * 16; ci += NL) {
+          const int r = ci >> 4, c16 = ci & 15;
+          const int32_t cd = codes[st * kTile + r];
+          const bool ok = cd != -1;
+          const bool raw = cd < -1;
+          const int64_t off = (int64_t)(raw ? -(cd + 2) : cd) * kD + c16 * 8;
+          const bf16* kp = ok ? (raw ? kr : kc) + off : a.q;
+          const bf16* vp = ok ? (raw ? vr : vc) + off : a.q;
+          const uint32_t so = (c16 >> 3) * 8192 + tc::sw128_offset(r, c16 & 7);
+          cp_async16(kdst + so, kp, ok ? 16 : 0);
+          cp_async16(kdst + 16384 + so, vp, ok ? 16 : 0);
+        }
+        tc::cp_async_mbar_arrive(&bars->kv_full[st]);
+      }
+      issued = j + 1;
+      if (j + 1 < n_tiles) {
+        const int v0 = k_begin + (j + 1) * kTile;
+        if (lt < kTile) next = ks.code(v0 + lt, a.err);
+        next_base = ks.code(v0, nullptr);
+      }
+    }
+    asm volatile("cp.async.wait_all;\n" ::: "memory");
+    // bulk copies still in flight after a timeout land before the CTA exits
+    if (lt == 0) {
+      tc::mbar_wait(&bars->q_full, 0, kWaitLimit);
+      for (int i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
+        tc::mbar_wait(&bars->kv_full[i % kStages], (i / kStages) & 1, kWaitLimit);
+    }
+  } else if (warp >= kSoftWarp0 && warp < kSoftWarp0 + 4) {
+    // ------------------------------------------------------------ softmax
+    using RM = RowMap<M>;
+    constexpr int NG = RM::NG;
+    const int qd = warp & 3;
+    const int r8 = lane >> 2, c4 = lane & 3;
+    float m_ref[NG][2], l_sum[NG][2];
+#pragma unroll
+    for (int g = 0; g < NG; ++g) {
+      m_ref[g][0] = m_ref[g][1] = -INFINITY;
+      l_sum[g][0] = l_sum[g][1] = 0.f;
+    }
+    for (int j = 0; j < n_tiles; ++j) {
+      const int sb = j & 1, st = j % kStages;
+      // waits are made warp-uniform: tcgen05.ld/st below are warp-collective
+      if (!__all_sync(0xFFFFFFFFu,
+                      wait_or_flag(&bars->meta_full[st], (j / kStages) & 1, bars, a.err)))
+        break;
+      const uint32_t vm0 = bars->valid[st][0], vm1 = bars->valid[st][1];
+      if (!__all_sync(0xFFFFFFFFu, wait_or_flag(&bars->s_full[sb], (j >> 1) & 1, bars, a.err)))
+        break;
+      tc::fence_after_sync();
+      // sr[g][q*16 + u*4 + k]: k = 0,1 -> row A cols 32q + 8u + 2c4 (+1);
+      //                        k = 2,3 -> row B, same columns
+      uint32_t sr[NG][32];
+#pragma unroll
+      for (int g = 0; g < NG; ++g)
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+          tc::tmem_ld16x256_x4(tmem + RM::lane_field(qd, g) + kSCol + sb * kTile + q * 32,
+                               &sr[g][q * 16]);
+      tc::tmem_ld_wait();
+      tc::fence_before_sync();
+      tc::mbar_arrive(&bars->s_free[sb]);
+
+      bool need_rescale = false;
+      float mt[NG][2];
+#pragma unroll
+      for (int g = 0; g < NG; ++g) {
+        mt[g][0] = mt[g][1] = -INFINITY;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const uint32_t vm = q ? vm1 : vm0;
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int bit = 8 * u + 2 * c4 + (k & 1);
+              const int i = q * 16 + u * 4 + k;
+              const float x =
+                  ((vm >> bit) & 1u) ? __uint_as_float(sr[g][i]) * a.scale_log2 : -INFINITY;
+              sr[g][i] = __float_as_uint(x);
+              mt[g][k >> 1] = fmaxf(mt[g][k >> 1], x);
+            }
+        }
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          mt[g][h2] = fmaxf(mt[g][h2], __shfl_xor_sync(0xFFFFFFFFu, mt[g][h2], 1));
+          mt[g][h2] = fmaxf(mt[g][h2], __shfl_xor_sync(0xFFFFFFFFu, mt[g][h2], 2));
+          need_rescale |= mt[g][h2] > m_ref[g][h2] + 8.f && m_ref[g][h2] != -INFINITY;
+        }
+      }
+      // lazy rescaling: a row's reference max moves only when the tile max
+      // exceeds it by more than 2^8 (or on its first finite tile)
+      if (__any_sync(0xFFFFFFFFu, need_rescale)) {
+        // O holds sum p*v relative to m_ref: wait for the P.V of tile j-1
+        if (!__all_sync(0xFFFFFFFFu, wait_or_flag(&bars->p_free[(j - 1) & 1],
+                                                  ((j - 1) >> 1) & 1, bars, a.err)))
+          break;
+        tc::fence_after_sync();
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+          float f[2];
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const bool grow = mt[g][h2] > m_ref[g][h2] + 8.f && m_ref[g][h2] != -INFINITY;
+            f[h2] = grow ? exp2f(m_ref[g][h2] - mt[g][h2]) : 1.f;
+            l_sum[g][h2] *= f[h2];
+          }
+#pragma unroll 1
+          for (int q = 0; q < 4; ++q) {
+            uint32_t o[16];
+            const uint32_t ta = tmem + RM::lane_field(qd, g) + kOCol + q * 32;
+            tc::tmem_ld16x256_x4(ta, o);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              o[i] = __float_as_uint(__uint_as_float(o[i]) * f[(i & 3) >> 1]);
+            tc::tmem_st16x256_x4(ta, o);
+          }
+        }
+        tc::tmem_st_wait();
+      }
+#pragma unroll
+      for (int g = 0; g < NG; ++g)
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2)
+          if (mt[g][h2] > m_ref[g][h2] + 8.f) m_ref[g][h2] = mt[g][h2];
+      // P buffer sb was last read by the P.V of tile j-2
+      if (j >= 2 && !__all_sync(0xFFFFFFFFu, wait_or_flag(&bars->p_free[sb], ((j - 2) >> 1) & 1,
+                                                         bars, a.err)))
+        break;
+      uint8_t* pbuf = sm + C::kPOff + sb * C::kPBytes;
+#pragma unroll
+      for (int g = 0; g < NG; ++g) {
+        const float mA = m_ref[g][0] == -INFINITY ? 0.f : m_ref[g][0];
+        const float mB = m_ref[g][1] == -INFINITY ? 0.f : m_ref[g][1];
+        const int rowA = RM::row(qd, g, r8), rowB = rowA + 8;
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int i = q * 16 + u * 4;
+            const float p0 = exp2f(__uint_as_float(sr[g][i]) - mA);
+            const float p1 = exp2f(__uint_as_float(sr[g][i + 1]) - mA);
+            const float p2 = exp2f(__uint_as_float(sr[g][i + 2]) - mB);
+            const float p3 = exp2f(__uint_as_float(sr[g][i + 3]) - mB);
+            l_sum[g][0] += p0 + p1;
+            l_sum[g][1] += p2 + p3;
+            // key 32q + 8u + 2c4: 16-byte chunk 4q + u, byte 4c4
+            *reinterpret_cast<uint32_t*>(pbuf + tc::sw128_offset(rowA, 4 * q + u) + 4 * c4) =
+                pack_bf16x2(p0, p1);
+            *reinterpret_cast<uint32_t*>(pbuf + tc::sw128_offset(rowB, 4 * q + u) + 4 * c4) =
+                pack_bf16x2(p2, p3);
+          }
+      }
+      tc::fence_proxy_async_smem();
+      tc::fence_before_sync();
+      tc::mbar_arrive(&bars->p_full[sb]);
+    }
+    // ---- epilogue: O rows after the last P.V, normalised
+    bool have_o = n_tiles > 0 && !*(volatile int*)&bars->timed_out;
+    if (__any_sync(0xFFFFFFFFu, have_o))
+      have_o = wait_or_flag(&bars->p_free[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1, bars,
+                            a.err);
+    have_o = __all_sync(0xFFFFFFFFu, have_o);
+    tc::fence_after_sync();
+#pragma unroll
+    for (int g = 0; g < NG; ++g) {
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        l_sum[g][h2] += __shfl_xor_sync(0xFFFFFFFFu, l_sum[g][h2], 1);
+        l_sum[g][h2] += __shfl_xor_sync(0xFFFFFFFFu, l_sum[g][h2], 2);
+      }
+      const int rowA = RM::row(qd, g, r8);
+      float fac[2], lse_r[2];
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const int h = rowA + 8 * h2;
+        const bool any = have_o && l_sum[g][h2] > 0.f;
+        if (ns > 1) {
+          fac[h2] = any ? 1.f / l_sum[g][h2] : 0.f;
+          lse_r[h2] = any ? (m_ref[g][h2] + log2f(l_sum[g][h2])) * kLn2 : -INFINITY;
+        } else {
+          const float sk = (a.sink && h < H) ? __ldg(a.sink + h) * kLog2e : -INFINITY;
+          float Mx = any ? m_ref[g][h2] : -INFINITY;
+          if (a.sink) Mx = fmaxf(Mx, sk);
+          fac[h2] = 0.f;
+          lse_r[h2] = -INFINITY;
+          if (Mx != -INFINITY) {
+            const float w = any ? exp2f(m_ref[g][h2] - Mx) : 0.f;
+            const float Z = l_sum[g][h2] * w + (a.sink ? exp2f(sk - Mx) : 0.f);
+            fac[h2] = w / Z;
+            lse_r[h2] = (Mx + log2f(Z)) * kLn2;
+          }
+        }
+      }
+#pragma unroll 1
+      for (int q = 0; q < 4; ++q) {
+        uint32_t o[16];
+        if (have_o) {
+          tc::tmem_ld16x256_x4(tmem + RM::lane_field(qd, g) + kOCol + q * 32, o);
+          tc::tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) o[i] = 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int col = 32 * q + 8 * u + 2 * c4;
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const int h = rowA + 8 * h2;
+            if (h >= H) continue;
+            const float v0 = __uint_as_float(o[u * 4 + 2 * h2]) * fac[h2];
+            const float v1 = __uint_as_float(o[u * 4 + 2 * h2 + 1]) * fac[h2];
+            if (ns > 1)
+              *reinterpret_cast<float2*>(sm + C::kPartOff + h * 512 + col * 4) =
+                  make_float2(v0, v1);
+            else
+              *reinterpret_cast<uint32_t*>(a.out + ((int64_t)qid * H + h) * kD + col) =
+                  pack_bf16x2(v0, v1);
+          }
+        }
+      }
+      if (c4 == 0) {
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const int h = rowA + 8 * h2;
+          if (h >= H) continue;
+          if (ns > 1)
+            reinterpret_cast<float*>(sm + C::kPartLseOff)[h] = lse_r[h2];
+          else if (a.lse)
+            a.lse[(int64_t)qid * H + h] = lse_r[h2];
+        }
+      }
     }
   }
 
-  float acc[16][4];
-#pragma unroll
-  for (int j = 0; j < 16; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-  float m0 = -INFINITY, m1 = -INFINITY;  // running max (log2 domain), rows g, g+8
-  float l0 = 0.f, l1 = 0.f;              // per-thread partial sums
-
-  if (n_tiles > 0) {
-    load_tile(0, 0);
-    cp_async_commit();
+  // ---- teardown: every role is done with TMEM
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
   }
-  for (int tile = 0; tile < n_tiles; ++tile) {
-    const int stage = tile & 1;
-    if (tile + 1 < n_tiles) {
-      load_tile(stage ^ 1, tile + 1);
-      cp_async_commit();
-      cp_async_wait<1>();
+  if (ns <= 1) return;
+
+  // ---- split merge inside the cluster: CTA `split` combines heads
+  // [split*hp, split*hp + hp) from every CTA's shared memory
+  tc::cluster_sync();
+  const int hp = (H + ns - 1) / ns;
+  const int h0 = split * hp;
+  const int nh = H - h0 < hp ? (H - h0 > 0 ? H - h0 : 0) : hp;
+  float* wgt = reinterpret_cast<float*>(sm + C::kWgtOff);  // [nh][ns]
+  for (int i = tid; i < nh * ns; i += C::kThreads) {
+    const int hl = i / ns, s = i % ns;
+    wgt[i] = tc::ld_cluster_f32(tc::map_shared(sbase + C::kPartLseOff + (h0 + hl) * 4, s));
+  }
+  __syncthreads();
+  for (int hl = tid; hl < nh; hl += C::kThreads) {
+    const int h = h0 + hl;
+    float Mx = a.sink ? __ldg(a.sink + h) : -INFINITY;
+    for (int s = 0; s < ns; ++s) Mx = fmaxf(Mx, wgt[hl * ns + s]);
+    float lse = -INFINITY;
+    if (Mx != -INFINITY) {
+      float Z = a.sink ? expf(__ldg(a.sink + h) - Mx) : 0.f;
+      for (int s = 0; s < ns; ++s) {
+        const float ls = wgt[hl * ns + s];
+        const float w = ls == -INFINITY ? 0.f : expf(ls - Mx);
+        wgt[hl * ns + s] = w;
+        Z += w;
+      }
+      const float inv = 1.f / Z;
+      for (int s = 0; s < ns; ++s) wgt[hl * ns + s] *= inv;
+      lse = Mx + logf(Z);
     } else {
-      cp_async_wait<0>();
+      for (int s = 0; s < ns; ++s) wgt[hl * ns + s] = 0.f;
     }
-    __syncthreads();
-
-    const uint32_t kbase = smem_base + stage * kStageBytes;
-    const uint32_t vbase = kbase + kTileBytes;
-    const uint32_t vm0 = valid_mask[stage * 2], vm1 = valid_mask[stage * 2 + 1];
-
-    // ---- S = Q K^T for 16 heads x 64 keys
-    float s[8][4];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
-    const int mi = lane >> 3, ri = lane & 7;
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-#pragma unroll
-      for (int jp = 0; jp < 4; ++jp) {
-        const int key = jp * 16 + ri + ((mi >> 1) << 3);
-        const int chunk = kk * 2 + (mi & 1);
-        uint32_t b0, b1, b2, b3;
-        ldmatrix_x4(kbase + key * kRowBytes + ((chunk ^ (key & 7)) << 4), b0, b1, b2, b3);
-        mma_bf16_16816(s[2 * jp], qa[kk], b0, b1);
-        mma_bf16_16816(s[2 * jp + 1], qa[kk], b2, b3);
-      }
-    }
-
-    // ---- mask, online softmax (base 2)
-    float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int slot = j * 8 + 2 * c + e;
-        const bool ok = ((slot < 32 ? vm0 >> slot : vm1 >> (slot - 32)) & 1u) != 0;
-        s[j][e] = ok ? s[j][e] * a.scale_log2 : -INFINITY;
-        s[j][2 + e] = ok ? s[j][2 + e] * a.scale_log2 : -INFINITY;
-        mx0 = fmaxf(mx0, s[j][e]);
-        mx1 = fmaxf(mx1, s[j][2 + e]);
-      }
-    }
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, 1));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, 2));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 1));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 2));
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    const float use0 = mn0 == -INFINITY ? 0.f : mn0;
-    const float use1 = mn1 == -INFINITY ? 0.f : mn1;
-    const float corr0 = exp2f(m0 - use0), corr1 = exp2f(m1 - use1);
-    m0 = mn0;
-    m1 = mn1;
-    l0 *= corr0;
-    l1 *= corr1;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      acc[j][0] *= corr0;
-      acc[j][1] *= corr0;
-      acc[j][2] *= corr1;
-      acc[j][3] *= corr1;
-    }
-    uint32_t pa[4][4];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float p0 = exp2f(s[j][0] - use0), p1 = exp2f(s[j][1] - use0);
-      const float p2 = exp2f(s[j][2] - use1), p3 = exp2f(s[j][3] - use1);
-      l0 += p0 + p1;
-      l1 += p2 + p3;
-      pa[j >> 1][(j & 1) * 2 + 0] = pack_bf16x2(p0, p1);
-      pa[j >> 1][(j & 1) * 2 + 1] = pack_bf16x2(p2, p3);
-    }
-
-    // ---- O += P V  (P: 16 heads x 64 keys, V: 64 keys x 128 dims)
-#pragma unroll
-    for (int kk2 = 0; kk2 < 4; ++kk2) {
-#pragma unroll
-      for (int np = 0; np < 8; ++np) {
-        const int key = kk2 * 16 + ri + ((mi & 1) << 3);
-        const int chunk = np * 2 + (mi >> 1);
-        uint32_t b0, b1, b2, b3;
-        ldmatrix_x4_trans(vbase + key * kRowBytes + ((chunk ^ (key & 7)) << 4), b0, b1, b2, b3);
-        mma_bf16_16816(acc[2 * np], pa[kk2], b0, b1);
-        mma_bf16_16816(acc[2 * np + 1], pa[kk2], b2, b3);
-      }
-    }
-    __syncthreads();  // the stage is overwritten by the load two tiles ahead
+    if (a.lse) a.lse[(int64_t)qid * H + h] = lse;
   }
-
-  // ---- finish: row sums across the 4 threads of a row group
-  l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, 1);
-  l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, 2);
-  l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, 1);
-  l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, 2);
-
-  const int h_lo = warp * 16 + g, h_hi = h_lo + 8;
-  if (a.n_split > 1) {
-    // partial result of this split: normalised o and its lse (natural log)
-    const int64_t base = ((int64_t)qid * a.n_split + split) * a.H;
-    const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
-    float* o0 = a.part_o + (base + h_lo) * kD;
-    float* o1 = a.part_o + (base + h_hi) * kD;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      *reinterpret_cast<float2*>(o0 + j * 8 + 2 * c) = make_float2(acc[j][0] * inv0, acc[j][1] * inv0);
-      *reinterpret_cast<float2*>(o1 + j * 8 + 2 * c) = make_float2(acc[j][2] * inv1, acc[j][3] * inv1);
+  __syncthreads();
+  for (int it = tid; it < nh * 32; it += C::kThreads) {
+    const int hl = it >> 5, d4 = it & 31, h = h0 + hl;
+    const uint32_t src = sbase + C::kPartOff + h * 512 + d4 * 16;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int s = 0; s < ns; ++s) {
+      const float w = wgt[hl * ns + s];
+      const float4 v = tc::ld_cluster_f32x4(tc::map_shared(src, s));
+      acc.x += w * v.x;
+      acc.y += w * v.y;
+      acc.z += w * v.z;
+      acc.w += w * v.w;
     }
-    if (c == 0) {
-      a.part_lse[base + h_lo] = l0 > 0.f ? (m0 + log2f(l0)) * kLn2 : -INFINITY;
-      a.part_lse[base + h_hi] = l1 > 0.f ? (m1 + log2f(l1)) * kLn2 : -INFINITY;
-    }
-    return;
+    reinterpret_cast<uint2*>(a.out + ((int64_t)qid * H + h) * kD)[d4] =
+        make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
   }
-  // single split: fold in the sink and write the final output
-  float M0 = m0, M1 = m1;
-  float sk0 = -INFINITY, sk1 = -INFINITY;
-  if (a.sink) {
-    sk0 = __ldg(a.sink + h_lo) * kLog2e;
-    sk1 = __ldg(a.sink + h_hi) * kLog2e;
-    M0 = fmaxf(M0, sk0);
-    M1 = fmaxf(M1, sk1);
-  }
-  float f0 = 0.f, f1 = 0.f, lse0 = -INFINITY, lse1 = -INFINITY;
-  if (M0 != -INFINITY) {
-    const float w = l0 > 0.f ? exp2f(m0 - M0) : 0.f;
-    const float Z = l0 * w + (a.sink ? exp2f(sk0 - M0) : 0.f);
-    f0 = w / Z;
-    lse0 = (M0 + log2f(Z)) * kLn2;
-  }
-  if (M1 != -INFINITY) {
-    const float w = l1 > 0.f ? exp2f(m1 - M1) : 0.f;
-    const float Z = l1 * w + (a.sink ? exp2f(sk1 - M1) : 0.f);
-    f1 = w / Z;
-    lse1 = (M1 + log2f(Z)) * kLn2;
-  }
-  uint32_t* out0 = reinterpret_cast<uint32_t*>(a.out + ((int64_t)qid * a.H + h_lo) * kD);
-  uint32_t* out1 = reinterpret_cast<uint32_t*>(a.out + ((int64_t)qid * a.H + h_hi) * kD);
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    out0[j * 4 + c] = pack_bf16x2(acc[j][0] * f0, acc[j][1] * f0);
-    out1[j * 4 + c] = pack_bf16x2(acc[j][2] * f1, acc[j][3] * f1);
-  }
-  if (a.lse && c == 0) {
-    a.lse[(int64_t)qid * a.H + h_lo] = lse0;
-    a.lse[(int64_t)qid * a.H + h_hi] = lse1;
-  }
+  // no CTA leaves while another may still read its shared memory
+  tc::cluster_sync();
 }
 
-// One warp per (query, head): merge the n_split partials with the sink.
-__global__ void __launch_bounds__(256) attn_merge_kernel(AttnArgs a) {
-  const int warp_global = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  const int total = a.n_query * a.H;
-  if (warp_global >= total) return;
-  const int qid = warp_global / a.H, h = warp_global % a.H;
-  const int64_t base = (int64_t)qid * a.n_split * a.H + h;
-  float M = a.sink ? __ldg(a.sink + h) : -INFINITY;
-  for (int s = 0; s < a.n_split; ++s) M = fmaxf(M, a.part_lse[base + (int64_t)s * a.H]);
-  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-  float lse = -INFINITY;
-  if (M != -INFINITY) {
-    float Z = a.sink ? expf(__ldg(a.sink + h) - M) : 0.f;
-    for (int s = 0; s < a.n_split; ++s) {
-      const float ls = a.part_lse[base + (int64_t)s * a.H];
-      if (ls == -INFINITY) continue;
-      const float w = expf(ls - M);
-      Z += w;
-      const float4 v =
-          reinterpret_cast<const float4*>(a.part_o + (base + (int64_t)s * a.H) * kD)[lane];
-      o.x += w * v.x;
-      o.y += w * v.y;
-      o.z += w * v.z;
-      o.w += w * v.w;
-    }
-    const float inv = 1.f / Z;
-    o.x *= inv;
-    o.y *= inv;
-    o.z *= inv;
-    o.w *= inv;
-    lse = M + logf(Z);
-  }
-  uint2 packed = make_uint2(pack_bf16x2(o.x, o.y), pack_bf16x2(o.z, o.w));
-  reinterpret_cast<uint2*>(a.out + ((int64_t)qid * a.H + h) * kD)[lane] = packed;
-  if (a.lse && lane == 0) a.lse[(int64_t)qid * a.H + h] = lse;
+template <int M>
+cudaLaunchConfig_t launch_cfg(int n_split, int n_query, cudaStream_t st,
+                              cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)n_split * (unsigned)n_query);
+  cfg.blockDim = dim3(Cfg<M>::kThreads);
+  cfg.dynamicSmemBytes = Cfg<M>::kSmemBytes;
+  cfg.stream = st;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)n_split;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = n_split > 1 ? 1 : 0;
+  return cfg;
 }
 
-template <int NW>
-cudaError_t launch_partial(const AttnArgs& a, cudaStream_t st) {
-  const int smem = 2 * kStageBytes + 16;
-  cudaError_t e = ensure_smem_attr((const void*)attn_partial_kernel<NW>, smem);
+// Clusters of size n the device keeps resident at once (cached per device).
+template <int M>
+int active_clusters(int n) {
+  static int cache[16][kMaxCluster + 1];
+  static bool init = false;
+  if (n <= 1) return 1 << 20;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev >= 16) return 0;
+  if (!init) {
+    for (auto& row : cache)
+      for (int& v : row) v = -1;
+    init = true;
+  }
+  int& c = cache[dev][n];
+  if (c < 0) {
+    if (n > 8)
+      cudaFuncSetAttribute(attn_tc_kernel<M>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    ensure_smem_attr((const void*)attn_tc_kernel<M>, Cfg<M>::kSmemBytes);
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = launch_cfg<M>(n, 1, nullptr, attr);
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, attn_tc_kernel<M>, &cfg) != cudaSuccess)
+      clusters = 0;
+    cudaGetLastError();
+    c = clusters;
+  }
+  return c;
+}
+
+template <int M>
+cudaError_t launch_tc(AttnArgs a, const Maps& maps, cudaStream_t st) {
+  cudaError_t e = ensure_smem_attr((const void*)attn_tc_kernel<M>, Cfg<M>::kSmemBytes);
   if (e != cudaSuccess) return e;
-  dim3 grid(a.n_split, a.n_query);
-  attn_partial_kernel<NW><<<grid, NW * 32, smem, st>>>(a);
-  return cudaGetLastError();
+  // Pick the split count: at most one cluster of splits per query, every
+  // cluster resident at once (one wave), about one CTA per SM in total.
+  int ns = 1, kps = 0;
+  for (int cap = kMaxCluster; cap >= 1; --cap) {
+    attn_plan(a.n_query, a.n_keys_max, cap, &ns, &kps);
+    if (ns <= 1 || (long)active_clusters<M>(ns) >= (long)a.n_query) break;
+  }
+  a.n_split = ns;
+  a.keys_per_split = kps;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = launch_cfg<M>(ns, a.n_query, st, attr);
+  return cudaLaunchKernelEx(&cfg, attn_tc_kernel<M>, a, maps);
 }
 
 }  // namespace
 
-void attn_plan(int n_query, int n_keys_max, int* n_split, int* keys_per_split) {
-  int max_split = (n_keys_max + kTileKeys - 1) / kTileKeys;
-  if (max_split < 1) max_split = 1;
-  const int target = 2 * kNumSMs;
-  int ns = (target + n_query - 1) / n_query;
-  if (ns > max_split) ns = max_split;
+// Split plan: the splits of a query run as one cluster of at most
+// max_cluster CTAs; about one CTA per SM in total.  Splits hold a multiple of
+// 4 key slots; the key count includes up to 3 padding slots after the
+// compressed entries.
+void attn_plan(int n_query, int n_keys_max, int max_cluster, int* n_split, int* keys_per_split) {
+  n_keys_max += 3;
+  int ns = kNumSMs / (n_query > 0 ? n_query : 1);
+  const int max_tiles = (n_keys_max + kTile - 1) / kTile;
+  if (ns > max_tiles) ns = max_tiles;
+  if (ns > max_cluster) ns = max_cluster;
   if (ns < 1) ns = 1;
   int kps = (n_keys_max + ns - 1) / ns;
-  kps = ((kps + kTileKeys - 1) / kTileKeys) * kTileKeys;
-  if (kps < kTileKeys) kps = kTileKeys;
+  kps = (kps + 3) & ~3;
   ns = (n_keys_max + kps - 1) / kps;
   if (ns < 1) ns = 1;
   *n_split = ns;
   *keys_per_split = kps;
 }
 
-size_t attn_workspace_bytes(int n_query, int H, int n_keys_max) {
-  int ns, kps;
-  attn_plan(n_query, n_keys_max, &ns, &kps);
-  if (ns <= 1) return 0;
-  const size_t parts = (size_t)n_query * ns * H;
-  return parts * kD * sizeof(float) + parts * sizeof(float) + 256;
-}
+size_t attn_workspace_bytes(int, int, int) { return 0; }
 
-cudaError_t launch_attention(AttnArgs a, void* ws, cudaStream_t st) {
-  int ns, kps;
-  attn_plan(a.n_query, a.n_keys_max, &ns, &kps);
-  a.n_split = ns;
-  a.keys_per_split = kps;
-  if (ns > 1) {
-    const size_t parts = (size_t)a.n_query * ns * a.H;
-    a.part_o = reinterpret_cast<float*>(ws);
-    a.part_lse = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + parts * kD * sizeof(float));
-  }
-  cudaError_t e;
-  switch (a.H) {
-    case 16: e = launch_partial<1>(a, st); break;
-    case 32: e = launch_partial<2>(a, st); break;
-    case 64: e = launch_partial<4>(a, st); break;
-    case 128: e = launch_partial<8>(a, st); break;
-    default: return cudaErrorInvalidValue;
-  }
-  if (e != cudaSuccess || ns <= 1) return e;
-  const int warps = a.n_query * a.H;
-  attn_merge_kernel<<<(warps * 32 + 255) / 256, 256, 0, st>>>(a);
-  return cudaGetLastError();
+cudaError_t launch_attention(AttnArgs a, void*, cudaStream_t st) {
+  // 2-D row views (rows of 128 elements) of the query block and the compressed caches
+  Maps maps;
+  const void* dummy = a.q;
+  cudaError_t e = tma::encode_rows128(&maps.q, a.q, (uint64_t)a.n_query * a.H, (uint32_t)a.H);
+  if (e != cudaSuccess) return e;
+  const bool has_c = a.k_cmp && a.N_cap > 0;
+  const uint64_t crow = has_c ? (uint64_t)(a.n_batch - 1) * (a.cmp_bstride / kD) + a.N_cap : 1;
+  e = tma::encode_rows128(&maps.kc, has_c ? a.k_cmp : dummy, crow, kTile);
+  if (e == cudaSuccess) e = tma::encode_rows128(&maps.vc, has_c ? a.v_cmp : dummy, crow, kTile);
+  if (e != cudaSuccess) return e;
+  if (a.H <= 64) return launch_tc<64>(a, maps, st);
+  return launch_tc<128>(a, maps, st);
 }
 
 }  // namespace csa

@@ -266,16 +266,20 @@ __device__ void find_threshold_bin(const int32_t* hist, int k, int* scratch, int
 }
 
 // ------------------------------------------------------------------ mark
-// grid (slices, queries): bitmap bits for keys above the threshold bin,
-// candidate list for keys in it.
+// grid (slices, queries): bitmap bits for keys above the threshold bin; the
+// keys in it are gathered in shared memory and appended to the query's
+// candidate list with one global atomic per CTA.
 __global__ void __launch_bounds__(kMarkThreads) topk_mark_kernel(IndexerArgs a, int q0,
                                                                  WsLayout L) {
+  extern __shared__ __align__(16) uint2 lcand[];  // [kMarkSlice]
   __shared__ int scratch[32];
   __shared__ int res[3];
+  __shared__ int n_local, g_base;
   const int qid = q0 + blockIdx.y, lq = blockIdx.y;
   const int64_t nv = visible_entries(a, qid, nullptr, false);
   const int64_t s0 = (int64_t)blockIdx.x * kMarkSlice;
   if (nv <= a.k || s0 >= nv) return;
+  if (threadIdx.x == 0) n_local = 0;
   const int32_t* hist = L.hdr + (int64_t)lq * kHdrWords;
   find_threshold_bin<kMarkThreads>(hist, a.k, scratch, res);
   const uint32_t bstar = (uint32_t)res[0];
@@ -306,20 +310,48 @@ __global__ void __launch_bounds__(kMarkThreads) topk_mark_kernel(IndexerArgs a, 
       if (lane == 0) bm[base >> 5] = above;
       if (at) {
         int slot0 = 0;
-        if (lane == 0) slot0 = atomicAdd(counter, __popc(at));
+        if (lane == 0) slot0 = atomicAdd(&n_local, __popc(at));
         slot0 = __shfl_sync(0xFFFFFFFFu, slot0, 0);
-        if ((at >> lane) & 1u) {
-          const int slot = slot0 + __popc(at & ((1u << lane) - 1u));
-          if (slot < kCandCap) cand[slot] = make_uint2(key[u], (uint32_t)(base + lane));
-        }
+        if ((at >> lane) & 1u)
+          lcand[slot0 + __popc(at & ((1u << lane) - 1u))] = make_uint2(key[u], (uint32_t)(base + lane));
       }
+    }
+  }
+  __syncthreads();
+  const int n = n_local;
+  if (n == 0) return;
+  if (threadIdx.x == 0) g_base = atomicAdd(counter, n);
+  __syncthreads();
+  const int gb = g_base;
+  for (int i = threadIdx.x; i < n; i += kMarkThreads)
+    if (gb + i < kCandCap) cand[gb + i] = lcand[i];
+}
+
+// ------------------------------------------------------------------ select
+// One CTA per query.  Dynamic shared memory: bitmap[nw] | eqmap[nw] | hist[1024].
+// The exact k-th key inside the threshold bin comes from two 10-bit radix
+// passes over the bin's candidate list (or, if it overflowed, over all
+// scores); ties at that key go to the lowest indices.
+constexpr int kSelUnroll = 8;
+
+template <bool FromCand>
+__device__ __forceinline__ void radix_pass(const uint2* cand, const float* scores, int64_t n,
+                                           uint32_t pmask, uint32_t prefix, int shift, int* h) {
+  for (int64_t i0 = threadIdx.x; i0 < n; i0 += (int64_t)kSelThreads * kSelUnroll) {
+    uint32_t key[kSelUnroll];
+#pragma unroll
+    for (int u = 0; u < kSelUnroll; ++u) {
+      const int64_t i = i0 + (int64_t)u * kSelThreads;
+      key[u] = i < n ? (FromCand ? __ldcg(&cand[i].x) : score_key(__ldcg(scores + i))) : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < kSelUnroll; ++u) {
+      const int64_t i = i0 + (int64_t)u * kSelThreads;
+      if (i < n && (key[u] & pmask) == prefix) atomicAdd(&h[(key[u] >> shift) & 1023], 1);
     }
   }
 }
 
-// ------------------------------------------------------------------ select
-// One CTA per query.  Dynamic shared memory: bitmap[nw] | eqmap[nw] |
-// cand[kCandCap] (uint2) | hist scratch [1024].
 __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(IndexerArgs a, int q0,
                                                                   WsLayout L) {
   extern __shared__ __align__(16) uint8_t sm[];
@@ -345,8 +377,7 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(IndexerArgs a,
   const int nw = (int)((nv + 31) / 32);
   uint32_t* bitmap = reinterpret_cast<uint32_t*>(sm);
   uint32_t* eqmap = bitmap + L.bm_stride;
-  uint2* cand = reinterpret_cast<uint2*>(eqmap + L.bm_stride);
-  int* h = reinterpret_cast<int*>(cand + kCandCap);
+  int* h = reinterpret_cast<int*>(eqmap + L.bm_stride);
 
   const int32_t* hist = L.hdr + (int64_t)lq * kHdrWords;
   find_threshold_bin<kSelThreads>(hist, a.k, scratch, res);
@@ -359,32 +390,21 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(IndexerArgs a,
     eqmap[i] = 0u;
   }
   const bool fast = c_bin <= kCandCap && n_cand_written == c_bin;
+  const uint2* cand = L.cand + (int64_t)lq * kCandCap;
   int need = a.k - c_above;  // to take from the threshold bin, >= 1
 
   // ---- exact key within the bin: two 10-bit radix passes (bits 19..10, 9..0)
   uint32_t prefix = bstar << 20;
-  int n_in = c_bin;
-  if (fast)
-    for (int i = tid; i < n_in; i += kSelThreads) cand[i] = L.cand[(int64_t)lq * kCandCap + i];
-  __syncthreads();
   for (int pass = 0; pass < 2; ++pass) {
     const int shift = pass == 0 ? 10 : 0;
     const uint32_t pmask = pass == 0 ? 0xFFF00000u : 0xFFFFFC00u;
     for (int i = tid; i < 1024; i += kSelThreads) h[i] = 0;
     __syncthreads();
-    if (fast) {
-      for (int i = tid; i < n_in; i += kSelThreads) {
-        const uint32_t key = cand[i].x;
-        if ((key & pmask) == prefix) atomicAdd(&h[(key >> shift) & 1023], 1);
-      }
-    } else {
-      for (int64_t i = tid; i < nv; i += kSelThreads) {
-        const uint32_t key = score_key(scores[i]);
-        if ((key & pmask) == prefix) atomicAdd(&h[(key >> shift) & 1023], 1);
-      }
-    }
+    if (fast)
+      radix_pass<true>(cand, scores, c_bin, pmask, prefix, shift, h);
+    else
+      radix_pass<false>(cand, scores, nv, pmask, prefix, shift, h);
     __syncthreads();
-    // find the bin holding the need-th largest key among those matching prefix
     {
       constexpr int per = 1024 / kSelThreads;
       const int hi = 1024 - tid * per;
@@ -420,17 +440,26 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(IndexerArgs a,
 
   // ---- mark the threshold-bin entries: above kstar -> bitmap, equal -> eqmap
   if (fast) {
-    for (int i = tid; i < n_in; i += kSelThreads) {
-      const uint2 ce = cand[i];
+    for (int i = tid; i < c_bin; i += kSelThreads) {
+      const uint2 ce = __ldcg(&cand[i]);
       if (ce.x > kstar) atomicOr(&bitmap[ce.y >> 5], 1u << (ce.y & 31));
       else if (ce.x == kstar) atomicOr(&eqmap[ce.y >> 5], 1u << (ce.y & 31));
     }
   } else {
-    for (int64_t i = tid; i < nv; i += kSelThreads) {
-      const uint32_t key = score_key(scores[i]);
-      if ((key >> 20) != bstar) continue;
-      if (key > kstar) atomicOr(&bitmap[i >> 5], 1u << (i & 31));
-      else if (key == kstar) atomicOr(&eqmap[i >> 5], 1u << (i & 31));
+    for (int64_t i0 = tid; i0 < nv; i0 += (int64_t)kSelThreads * kSelUnroll) {
+      uint32_t key[kSelUnroll];
+#pragma unroll
+      for (int u = 0; u < kSelUnroll; ++u) {
+        const int64_t i = i0 + (int64_t)u * kSelThreads;
+        key[u] = i < nv ? score_key(__ldcg(scores + i)) : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < kSelUnroll; ++u) {
+        const int64_t i = i0 + (int64_t)u * kSelThreads;
+        if (i >= nv || (key[u] >> 20) != bstar) continue;
+        if (key[u] > kstar) atomicOr(&bitmap[i >> 5], 1u << (i & 31));
+        else if (key[u] == kstar) atomicOr(&eqmap[i >> 5], 1u << (i & 31));
+      }
     }
   }
   __syncthreads();
@@ -477,9 +506,7 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(IndexerArgs a,
   }
 }
 
-int select_smem_bytes(int n_cap) {
-  return 2 * bitmap_words(n_cap) * 4 + kCandCap * 8 + 1024 * 4;
-}
+int select_smem_bytes(int n_cap) { return 2 * bitmap_words(n_cap) * 4 + 1024 * 4; }
 
 }  // namespace
 
@@ -497,6 +524,8 @@ cudaError_t launch_indexer_topk(const IndexerArgs& a, void* ws, cudaStream_t st)
   const int sel_smem = select_smem_bytes(a.N_cap);
   cudaError_t e = ensure_smem_attr((const void*)topk_select_kernel, select_smem_bytes(kMaxNcap));
   if (e != cudaSuccess) return e;
+  e = ensure_smem_attr((const void*)topk_mark_kernel, kMarkSlice * sizeof(uint2));
+  if (e != cudaSuccess) return e;
   for (int q0 = 0; q0 < a.n_query; q0 += kQueryChunk) {
     const int qc = (a.n_query - q0 < kQueryChunk) ? a.n_query - q0 : kQueryChunk;
     e = cudaMemsetAsync(L.hdr, 0, (size_t)qc * kHdrWords * sizeof(int32_t), st);
@@ -509,7 +538,7 @@ cudaError_t launch_indexer_topk(const IndexerArgs& a, void* ws, cudaStream_t st)
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     dim3 g2((a.N_cap + kMarkSlice - 1) / kMarkSlice, qc);
-    topk_mark_kernel<<<g2, kMarkThreads, 0, st>>>(a, q0, L);
+    topk_mark_kernel<<<g2, kMarkThreads, kMarkSlice * sizeof(uint2), st>>>(a, q0, L);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     topk_select_kernel<<<qc, kSelThreads, sel_smem, st>>>(a, q0, L);

@@ -29,7 +29,7 @@ struct AttnArgs {
   const __nv_bfloat16* k_raw;
   const __nv_bfloat16* v_raw;
   int64_t raw_bstride;
-  int64_t raw_cap;
+  int64_t raw_cap;  // ring of raw_cap rows: position p at row p % raw_cap
   const int32_t* pos;  // pos_is_len ? seq_len[B] : q_pos[n_query]
   int pos_is_len;
   int T;  // query tokens per sequence (query q belongs to sequence q / T)
@@ -37,6 +37,7 @@ struct AttnArgs {
   const float* sink;
   float scale_log2;  // softmax_scale * log2(e)
   int H;
+  int n_batch;  // sequences (rows of the caches' 2-D views span all of them)
   int n_query;
   int n_keys_max;
   // filled by launch_attention
@@ -44,18 +45,19 @@ struct AttnArgs {
   int keys_per_split;
   float* part_o;
   float* part_lse;
+  int* counters;  // [n_query] split arrivals (zeroed per call)
   __nv_bfloat16* out;
   float* lse;
   int32_t* err;
 };
 
-void attn_plan(int n_query, int n_keys_max, int* n_split, int* keys_per_split);
-size_t attn_workspace_bytes(int n_query, int H, int n_keys_max);
+void attn_plan(int n_query, int n_keys_max, int max_cluster, int* n_split, int* keys_per_split);
+size_t attn_workspace_bytes(int n_query, int H, int n_keys_max);  // 0: splits merge on chip
 cudaError_t launch_attention(AttnArgs a, void* ws, cudaStream_t st);
 
 // ---------------------------------------------------------------- indexer + top-k
 constexpr int kHistBins = 4096;  // top 12 bits of the order-preserving score key
-constexpr int kCandCap = 8192;   // candidates of the threshold bin kept per query
+constexpr int kCandCap = 32768;  // candidates of the threshold bin kept per query
 constexpr int kMaxNcap = 1 << 19;
 
 struct IndexerArgs {
@@ -87,6 +89,7 @@ cudaError_t launch_indexer_topk(const IndexerArgs& a, void* ws, cudaStream_t st)
 struct CompressArgs {
   const __nv_bfloat16* raw;
   int64_t raw_bstride;
+  int64_t raw_cap;  // ring of raw_cap rows: position p at row p % raw_cap
   int B, d, m, block_begin, n_blocks;
   const __nv_bfloat16* W;
   const float* pos_bias;

@@ -1,9 +1,11 @@
 """One step of each hot-path workload on resident device buffers.
 
 A step object takes the inputs of a workload (the dict that ``synth``
-returns), lays them out on the GPU once -- caches at full capacity, rows a
-step must not read filled with NaN so that a stray read cannot go unnoticed,
-workspaces and outputs preallocated -- and then runs one step per call:
+returns), lays them out on the GPU once -- compressed caches at full
+capacity, raw caches as rings of only the rows a step can read (the window;
+position p at row p mod R), every row a step must not read filled with NaN so
+that a stray read cannot go unnoticed, workspaces and outputs preallocated --
+and then runs one step per call:
 
 * CSA decode:  [compress the newest block of K, V and indexer keys]
   -> indexer top-k -> sparse attention (split-K + merge)
@@ -22,6 +24,13 @@ from . import (attn_workspace, compress_kv, hca_dense_attn_decode, indexer_topk,
                indexer_topk_workspace, sparse_attn_decode, sparse_attn_prefill)
 
 
+def _ring_put(cache, b, positions, rows):
+    """Store rows for absolute positions into a ring cache (row = p mod R)."""
+    R = cache.shape[1]
+    idx = torch.as_tensor(positions, device=cache.device) % R
+    cache[b, idx] = rows
+
+
 def _nan(shape, dtype, device):
     if dtype in (torch.uint8,):
         return torch.full(shape, 0x7F, dtype=dtype, device=device)  # E4M3 NaN code
@@ -35,7 +44,6 @@ class CsaDecodeStep:
         dev = torch.device(device)
         B, W, m, D = wl.B, wl.W, wl.m, wl.D
         lens = list(wl.lens)
-        L_cap = max(lens)
         g = lambda k: None if inp.get(k) is None else inp[k].to(dev).clone()
         self.q, self.sink = g("q"), g("sink")
         self.seq_len, self.n_cmp = g("seq_len"), g("n_cmp")
@@ -43,20 +51,20 @@ class CsaDecodeStep:
         self.q_idx, self.w, self.k_idx = g("q_idx"), g("w"), g("k_idx")
         self.q_scale, self.k_scale = g("q_scale"), g("k_scale")
         self.q_pos = (self.seq_len - 1).view(B, 1).contiguous()
-        # raw caches: only the window rows are defined
-        self.k_raw = _nan((B, L_cap, D), torch.bfloat16, dev)
-        self.v_raw = _nan((B, L_cap, D), torch.bfloat16, dev)
+        # raw caches: rings of W rows holding the window
+        self.k_raw = _nan((B, W, D), torch.bfloat16, dev)
+        self.v_raw = _nan((B, W, D), torch.bfloat16, dev)
         kw, vw = g("k_win"), g("v_win")
         for b, n in enumerate(lens):
             lo = max(0, n - W)
-            self.k_raw[b, lo:n] = kw[b, W - (n - lo):]
-            self.v_raw[b, lo:n] = vw[b, W - (n - lo):]
+            _ring_put(self.k_raw, b, range(lo, n), kw[b, W - (n - lo):])
+            _ring_put(self.v_raw, b, range(lo, n), vw[b, W - (n - lo):])
         self.compress = wl.stream_compress
         if self.compress:
-            self.idx_raw = _nan((B, L_cap, wl.d_I), torch.bfloat16, dev)
+            self.idx_raw = _nan((B, W, wl.d_I), torch.bfloat16, dev)
             rn = g("raw_new_idx")
             for b, n in enumerate(lens):
-                self.idx_raw[b, n - m:n] = rn[b]
+                _ring_put(self.idx_raw, b, range(n - m, n), rn[b])
             self.gates = {s: tuple(t.to(dev) for t in inp["gate_" + s]) for s in ("k", "v", "idx")}
             # the newest entry is produced by the step itself
             for b, n in enumerate(lens):
@@ -112,18 +120,17 @@ class HcaDecodeStep:
         dev = torch.device(device)
         B, W, D = wl.B, wl.W, wl.D
         lens = list(wl.lens)
-        L_cap = max(lens)
         g = lambda k: None if inp.get(k) is None else inp[k].to(dev).clone()
         self.q, self.sink = g("q"), g("sink")
         self.seq_len, self.n_cmp = g("seq_len"), g("n_cmp")
         self.k_cmp, self.v_cmp = g("k_cmp"), g("v_cmp")
-        self.k_raw = _nan((B, L_cap, D), torch.bfloat16, dev)
-        self.v_raw = _nan((B, L_cap, D), torch.bfloat16, dev)
+        self.k_raw = _nan((B, W, D), torch.bfloat16, dev)
+        self.v_raw = _nan((B, W, D), torch.bfloat16, dev)
         kw, vw = g("k_win"), g("v_win")
         for b, n in enumerate(lens):
             lo = max(0, n - W)
-            self.k_raw[b, lo:n] = kw[b, W - (n - lo):]
-            self.v_raw[b, lo:n] = vw[b, W - (n - lo):]
+            _ring_put(self.k_raw, b, range(lo, n), kw[b, W - (n - lo):])
+            _ring_put(self.v_raw, b, range(lo, n), vw[b, W - (n - lo):])
         self.out = torch.empty_like(self.q)
         self.ws_attn = torch.empty(max(1, attn_workspace(B, 1, wl.H, wl.N_cap + W)),
                                    dtype=torch.uint8, device=dev)
@@ -148,7 +155,7 @@ class CsaPrefillStep:
         self.wl = wl
         dev = torch.device(device)
         B, T, L, W, m, D = wl.B, wl.T, wl.L, wl.W, wl.m, wl.D
-        L_cap = L + T
+        R = W - 1 + T  # ring rows: positions L-W+1 .. L+T-1
         g = lambda k: None if inp.get(k) is None else inp[k].to(dev).clone()
         self.q, self.sink = g("q"), g("sink")
         self.q_pos, self.n_cmp = g("q_pos"), g("n_cmp")
@@ -159,13 +166,15 @@ class CsaPrefillStep:
         self.k_cmp[:, n_old:] = float("nan")
         self.v_cmp[:, n_old:] = float("nan")
         self.k_idx[:, n_old:] = float("nan")
-        self.k_raw = _nan((B, L_cap, D), torch.bfloat16, dev)
-        self.v_raw = _nan((B, L_cap, D), torch.bfloat16, dev)
-        self.idx_raw = _nan((B, L_cap, wl.d_I), torch.bfloat16, dev)
+        self.k_raw = _nan((B, R, D), torch.bfloat16, dev)
+        self.v_raw = _nan((B, R, D), torch.bfloat16, dev)
+        self.idx_raw = _nan((B, R, wl.d_I), torch.bfloat16, dev)
         base = L - (W - 1)
-        self.k_raw[:, base:] = g("raw_k")
-        self.v_raw[:, base:] = g("raw_v")
-        self.idx_raw[:, L:] = g("raw_idx")
+        rk, rv, ri = g("raw_k"), g("raw_v"), g("raw_idx")
+        for b in range(B):
+            _ring_put(self.k_raw, b, range(base, L + T), rk[b])
+            _ring_put(self.v_raw, b, range(base, L + T), rv[b])
+            _ring_put(self.idx_raw, b, range(L, L + T), ri[b])
         self.gates = {s: tuple(t.to(dev) for t in inp["gate_" + s]) for s in ("k", "v", "idx")}
         self.block0, self.n_new = n_old, T // m
         self.idx = torch.empty((B, T, wl.k), dtype=torch.int32, device=dev)

@@ -49,9 +49,8 @@ def _decode(**over):
 @pytest.mark.parametrize("over,status", [
     (dict(q=None), 1), (dict(out=None), 1), (dict(D=64), 2), (dict(H=48), 2), (dict(B=-1), 1),
     (dict(window=-1), 1), (dict(cmp_bstride=1000), 1), (dict(k_raw=None), 1),
-    (dict(raw_bstride=100), 1), (dict(q=ctypes.c_void_p(0x10002)), 1), (dict(k=-3), 1),
-    (dict(topk_idx=None), 1), (dict(seq_len=None), 1), (dict(ws=None), 3),
-    (dict(ws_bytes=0), 3),
+    (dict(raw_bstride=100), 1), (dict(raw_cap=100), 1), (dict(q=ctypes.c_void_p(0x10002)), 1), (dict(k=-3), 1),
+    (dict(topk_idx=None), 1), (dict(seq_len=None), 1),
 ])
 def test_sparse_decode_rejects(over, status):
     assert _decode(**over) == status
@@ -84,25 +83,25 @@ def test_compress_rejects():
     L = csa.lib()
 
     def call(**over):
-        a = dict(raw=FAKE, rbs=64 * 128, B=2, d=128, m=4, b0=0, nb=16, W=FAKE, pb=FAKE, out=FAKE,
-                 obs=16 * 128, dt=0, sc=None, sbs=0, err=None, st=None)
+        a = dict(raw=FAKE, rbs=64 * 128, rcap=64, B=2, d=128, m=4, b0=0, nb=16, W=FAKE, pb=FAKE,
+                 out=FAKE, obs=16 * 128, dt=0, sc=None, sbs=0, err=None, st=None)
         a.update(over)
         return L.csa_compress_kv(*a.values())
 
     assert call(d=96) == 2 and call(m=300) == 2 and call(dt=5) == 2
-    assert call(nb=17) == 1  # reads past the raw rows
+    assert call(rcap=3) == 1  # a ring shorter than one block
+    assert call(rcap=65) == 1  # ring rows beyond the sequence stride
     assert call(obs=15 * 128) == 1
     assert call(dt=1) == 1  # FP8 output needs a scale array
     assert call(W=None) == 1
     assert call(B=0) == 0 and call(nb=0) == 0
 
 
-def test_attention_workspace_plan():
+def test_attention_needs_no_workspace():
+    # key splits merge through distributed shared memory inside a cluster
     L = csa.lib()
-    # long key sets split over many CTAs -> partials; many queries -> one split
-    assert L.csa_attn_workspace(32, 1, 64, 1152) > 0
-    assert L.csa_attn_workspace(1, 4096, 64, 2176) == 0
-    assert L.csa_attn_workspace(16, 1, 64, 8320) == L.csa_attn_workspace(16, 1, 64, 8320)
+    for args in ((32, 1, 64, 1152), (1, 4096, 64, 2176), (16, 1, 64, 8320), (8, 1, 128, 2176)):
+        assert L.csa_attn_workspace(*args) == 0
 
 
 def test_binding_rejects_cpu_tensors():

@@ -362,13 +362,16 @@ def test_bad_indices_and_positions_set_the_error_word(cuda_device):
     ro, _ = oracle.csa_decode(u16(q), u16(kc), u16(vc), skip, kr, vr, np.array(lens), 128,
                               sink.numpy(), 1.0, base)
     check_attention(out, ro, what="skipped bad indices")
-    # a length beyond the raw cache: flagged, window dropped, no fault
+    # an empty sequence (length 0, position -1): flagged, its window dropped,
+    # no fault; only the compressed entries and the sink remain
     err.zero_()
-    L2 = torch.tensor([200, 900], dtype=torch.int32, device=DEV)
-    csa.sparse_attn_decode(q.to(DEV), kc.to(DEV), vc.to(DEV), torch.from_numpy(sel).to(DEV),
-                           kr_d, vr_d, L2, 128, sink.to(DEV), err_word=err)
+    L2 = torch.tensor([200, 0], dtype=torch.int32, device=DEV)
+    out2 = csa.sparse_attn_decode(q.to(DEV), kc.to(DEV), vc.to(DEV),
+                                  torch.from_numpy(sel).to(DEV), kr_d, vr_d, L2, 128,
+                                  sink.to(DEV), err_word=err)
     torch.cuda.synchronize()
     assert err.item() & csa.EW_BAD_POSITION
+    assert torch.isfinite(out2.float()).all()
 
 
 def test_determinism_bitwise(cuda_device):
@@ -380,3 +383,27 @@ def test_determinism_bitwise(cuda_device):
     b = step().clone()
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
     assert torch.equal(ia, step.idx)
+
+
+def test_decode_with_window_ring_cache(cuda_device):
+    # raw caches as rings of exactly W rows: position p lives at row p mod W
+    B, H, N_cap, k, W = 3, 64, 200, 40, 128
+    lens = [5000, 777, 90]
+    q, kc, vc, kw, vw, sink = _attn_inputs(B, H, N_cap, lens, seed=99)
+    n_vis = [min(N_cap, n // 4) for n in lens]
+    sel = _random_topk(B, k, n_vis, seed=5)
+    kr_ring, vr_ring = poisoned((B, W, 128)), poisoned((B, W, 128))
+    for b, n in enumerate(lens):
+        lo = max(0, n - W)
+        rows = torch.arange(lo, n) % W
+        kr_ring[b, rows] = kw[b, W - (n - lo):].to(DEV)
+        vr_ring[b, rows] = vw[b, W - (n - lo):].to(DEV)
+    out, lse = csa.sparse_attn_decode(
+        q.to(DEV), kc.to(DEV), vc.to(DEV), torch.from_numpy(sel).to(DEV), kr_ring, vr_ring,
+        torch.tensor(lens, dtype=torch.int32, device=DEV), W, sink.to(DEV), return_lse=True)
+    torch.cuda.synchronize()
+    kr, base = window_arrays(kw, lens)
+    vr, _ = window_arrays(vw, lens)
+    ro, rl = oracle.csa_decode(u16(q), u16(kc), u16(vc), sel, kr, vr, np.array(lens), W,
+                               sink.numpy(), 1.0, base)
+    check_attention(out, ro, lse, rl, "ring cache")
