@@ -12,9 +12,9 @@ step, outside the
 timed events.  ``value`` is whole-job queries/s (tokens/s for prefill) over
 all ranks; ``e2e`` is the same metric through the public Python API with the
 step's inputs copied from pinned host memory and its output copied back
-inside the timed region.  ``roofline`` rates the dominant stage (the indexer
-for CSA decode, the attention for HCA decode and prefill) against the
-measured peaks in MEASURED_PEAKS.json.  ``cpu_baseline`` times the CPU oracle
+inside the timed region.  ``roofline`` rates the dominant stage (the one that
+takes the most time per step) against the measured peaks in
+MEASURED_PEAKS.json.  ``cpu_baseline`` times the CPU oracle
 on a bounded sample on this host.  ``--impl reference`` times only the CPU
 oracle, as the reference arm.
 
@@ -90,9 +90,28 @@ def algorithmic(wl) -> dict:
             "compress": {"flops": 3 * wl.B * wl.T * D * D * 2}}
 
 
-def dominant_stage(wl) -> str:
-    return {"csa_decode": "indexer_topk", "hca_decode": "attention",
-            "csa_prefill": "attention"}[wl.kind]
+def dominant_stage(stage_ms: dict, alg: dict) -> str:
+    """The stage that takes the most time per step (among those with an
+    algorithmic byte or FLOP count)."""
+    return max((n for n in stage_ms if n in alg), key=lambda n: stage_ms[n])
+
+
+# ---------------------------------------------------------------- ranks
+
+def max_over_ranks(x: float, world: int, dist=None, device="cpu") -> float:
+    """The maximum of a per-rank number over all ranks (the slowest rank's
+    time decides the whole job's throughput)."""
+    if world <= 1:
+        return float(x)
+    t = torch.tensor([float(x)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(units_per_rank: int, world: int, steps: int, total_ms: float) -> float:
+    """Whole-job throughput: the units every rank processed over the slowest
+    rank's time."""
+    return units_per_rank * world * steps / (total_ms / 1e3)
 
 
 # ---------------------------------------------------------------- environment
@@ -339,13 +358,9 @@ def main():
     stage_ms = {name: statistics.mean(evs[i][s].elapsed_time(evs[i][s + 1])
                                       for i in range(args.steps))
                 for s, (name, _) in enumerate(graphs)}
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), world, dist, dev)
     ms_per_step = total_ms / args.steps
-    value = units(wl) * world * args.steps / (total_ms / 1e3)
+    value = job_value(units(wl), world, args.steps, total_ms)
 
     # e2e: public API, inputs from pinned host memory, result back to host
     e2e = run_e2e(args, wl, step, dev, flush, world, dist)
@@ -353,7 +368,7 @@ def main():
     # roofline of the dominant stage
     peaks, peaks_src = load_peaks()
     alg = algorithmic(wl)
-    dom = dominant_stage(wl)
+    dom = dominant_stage(stage_ms, alg)
     dom_s = stage_ms[dom] / 1e3
     if "bytes" in alg[dom]:
         achieved = alg[dom]["bytes"] / dom_s / 1e9
@@ -417,7 +432,8 @@ def launches_per_step(wl, csa) -> int:
 
 def run_e2e(args, wl, step, dev, flush, world, dist):
     """Per step: pinned host -> device copy of the step's inputs, the step via
-    the public API (eager), device -> pinned host copy of its output."""
+    the public API (the whole step replayed as one CUDA graph, as a serving
+    loop runs it), device -> pinned host copy of its output."""
     names = {"csa_decode": ["q", "q_idx", "w", "q_scale", "seq_len"],
              "hca_decode": ["q", "seq_len"],
              "csa_prefill": ["q", "q_idx", "w", "q_pos"]}[wl.kind]
@@ -433,24 +449,22 @@ def run_e2e(args, wl, step, dev, flush, world, dist):
     h2d = sum(h.numel() * h.element_size() for h, _ in pairs)
     d2h = out_h.numel() * out_h.element_size()
     stream = torch.cuda.current_stream(dev)
+    run = step.graphed()
     times = []
     for i in range(args.steps):
         flush()
+        torch.cuda.synchronize(dev)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for h, d in pairs:
             d.copy_(h, non_blocking=True)
-        out = step()
+        out = run()
         out_h.copy_(out, non_blocking=True)
         e1.record(stream)
         e1.synchronize()
         times.append(e0.elapsed_time(e1))
-    total = sum(times)
-    if world > 1:
-        t = torch.tensor([total], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total = float(t.item())
-    return {"value": round(units(wl) * world * args.steps / (total / 1e3), 2),
+    total = max_over_ranks(sum(times), world, dist, dev)
+    return {"value": round(job_value(units(wl), world, args.steps, total), 2),
             "unit": unit_name(wl), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": round(total / args.steps, 5)}
 

@@ -37,7 +37,38 @@ def _nan(shape, dtype, device):
     return torch.full(shape, float("nan"), dtype=dtype, device=device)
 
 
-class CsaDecodeStep:
+class _Step:
+    """Shared by the step classes: ``stages()`` lists (name, callable) in
+    order and ``out`` is the output tensor."""
+
+    def __call__(self):
+        for _, fn in self.stages():
+            fn()
+        return self.out
+
+    def graphed(self):
+        """Capture one whole step in a CUDA graph (after an eager warm-up
+        call) and return a callable that replays it on the current stream and
+        returns ``out``.  The graph reads the step's own device tensors when it
+        replays, so new inputs are copied into them first."""
+        dev = self.out.device
+        self()
+        torch.cuda.synchronize(dev)
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.graph(graph, stream=side):
+            self()
+        torch.cuda.synchronize(dev)
+
+        def replay():
+            graph.replay()
+            return self.out
+        self._graph = graph  # keep the graph alive with the step
+        return replay
+
+
+class CsaDecodeStep(_Step):
     def __init__(self, inp: dict, device="cuda"):
         wl = inp["workload"]
         self.wl = wl
@@ -107,13 +138,8 @@ class CsaDecodeStep:
         st = [("compress", self._compress)] if self.compress else []
         return st + [("indexer_topk", self._index), ("attention", self._attend)]
 
-    def __call__(self):
-        for _, fn in self.stages():
-            fn()
-        return self.out
 
-
-class HcaDecodeStep:
+class HcaDecodeStep(_Step):
     def __init__(self, inp: dict, device="cuda"):
         wl = inp["workload"]
         self.wl = wl
@@ -144,12 +170,8 @@ class HcaDecodeStep:
     def stages(self):
         return [("attention", self._attend)]
 
-    def __call__(self):
-        self._attend()
-        return self.out
 
-
-class CsaPrefillStep:
+class CsaPrefillStep(_Step):
     def __init__(self, inp: dict, device="cuda"):
         wl = inp["workload"]
         self.wl = wl
@@ -204,11 +226,6 @@ class CsaPrefillStep:
     def stages(self):
         return [("compress", self._compress), ("indexer_topk", self._index),
                 ("attention", self._attend)]
-
-    def __call__(self):
-        for _, fn in self.stages():
-            fn()
-        return self.out
 
 
 def make_step(inp: dict, device="cuda"):
