@@ -135,6 +135,44 @@ CSA_API int csa_indexer_topk(const void* q_idx, const float* q_scale, const floa
                      int32_t* err_word, void* stream);
 
 /* ------------------------------------------------------------------------
+ * a3, without caller scratch.  An integration variant: the DeepSeek-V4 pages
+ * have no counterpart to it; it computes exactly what csa_indexer_topk does.
+ *
+ * For callers that cannot allocate device memory at the point of the call:
+ * a decode loop that reserved its HBM up front and must not call the device
+ * allocator (which can synchronise the device) inside the step, or a host
+ * runtime that has no device allocator of its own to hand out scratch.  The
+ * scratch is a fixed array of CSA_INDEXER_STATIC_SCRATCH_BYTES in the
+ * library's own device memory (one per device), so the call allocates
+ * nothing: no cudaMalloc / cudaFree, no allocating library routine.
+ *
+ * Arguments, layouts, ownership and results are those of csa_indexer_topk,
+ * without ws / ws_bytes.
+ *   Limit: csa_indexer_topk_workspace(B, T, N_cap, k) must not exceed
+ *   CSA_INDEXER_STATIC_SCRATCH_BYTES (16 MiB: e.g. 32 queries over 32768
+ *   compressed entries, or 8 over 262144); a larger problem returns
+ *   CSA_ERR_WORKSPACE before anything runs.
+ *   Set-up: the first call on a device (the device current on the calling
+ *   thread) looks up the array's device address (cudaGetSymbolAddress) and
+ *   caches it; that lookup can load the library's kernels, so make the first
+ *   call per device before any stream capture.  A failed lookup returns
+ *   CSA_ERR_CUDA.
+ *   Zeroing: nothing in the array has to start at zero; each call clears the
+ *   counters it uses (an asynchronous memset on `stream`) before its kernels.
+ *   Overlap: all calls on one device share the one array.  Calls ordered on
+ *   one stream are safe; two calls that can run at the same time (different
+ *   streams without an event between them, or several host threads) race on
+ *   the scratch and give undefined results.
+ * ---------------------------------------------------------------------- */
+#define CSA_INDEXER_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
+CSA_API int csa_indexer_topk_static(const void* q_idx, const float* q_scale, const float* w,
+                                    const void* k_idx, int64_t k_bstride, const float* k_scale,
+                                    int64_t ks_bstride, int idx_dtype, const int32_t* q_pos,
+                                    const int32_t* n_cmp, int B, int T, int H_I, int d_I,
+                                    int N_cap, int m, int k, int32_t* topk_idx,
+                                    float* topk_score, int32_t* err_word, void* stream);
+
+/* ------------------------------------------------------------------------
  * a4 / a5 / a6. Attention over compressed entries + window + sink.
  *
  * Sources: hyper.ai DeepSeek-V4 page, Method (MQA core attention with shared

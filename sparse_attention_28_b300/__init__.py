@@ -34,8 +34,11 @@ EW_BAD_POSITION = 2
 ABI_SYMBOLS = (
     "csa_status_str", "csa_abi_version", "csa_compress_kv", "csa_indexer_topk_workspace",
     "csa_indexer_topk", "csa_attn_workspace", "csa_sparse_attn_decode",
-    "csa_sparse_attn_prefill", "hca_dense_attn_decode",
+    "csa_sparse_attn_prefill", "hca_dense_attn_decode", "csa_indexer_topk_static",
 )
+
+# capacity of the library-owned scratch behind indexer_topk_static (bytes)
+INDEXER_STATIC_SCRATCH_BYTES = 16 << 20
 
 _lock = threading.Lock()
 _lib = None
@@ -70,6 +73,9 @@ def lib() -> ctypes.CDLL:
             L.csa_indexer_topk.argtypes = [P, P, P, P, I64, P, I64, I, P, P, I, I, I, I, I, I, I,
                                            P, P, P, SZ, P, P]
             L.csa_indexer_topk.restype = I
+            L.csa_indexer_topk_static.argtypes = [P, P, P, P, I64, P, I64, I, P, P, I, I, I, I,
+                                                  I, I, I, P, P, P, P]
+            L.csa_indexer_topk_static.restype = I
             L.csa_attn_workspace.argtypes = [I, I, I, I]
             L.csa_attn_workspace.restype = SZ
             L.csa_sparse_attn_decode.argtypes = [P, P, P, I64, I, P, I, P, P, I64, I64, P, I, P,
@@ -196,6 +202,42 @@ def indexer_topk(q_idx, w, k_idx, q_pos, n_cmp, m: int, k: int, q_scale=None, k_
         CSA_FP8_E4M3 if fp8 else CSA_BF16, _p(q_pos), _p(n_cmp), B, T, H_I, d_I, N_cap, m, k,
         _p(idx), _p(scores), _p(wsb), wsn, _p(err_word), _stream(dev))
     _check(st, "csa_indexer_topk")
+    return (idx, scores) if return_scores else idx
+
+
+def indexer_topk_static(q_idx, w, k_idx, q_pos, n_cmp, m: int, k: int, q_scale=None,
+                        k_scale=None, return_scores: bool = False, out=None, err_word=None):
+    """indexer_topk with the library's fixed scratch instead of a caller
+    workspace: the C call allocates no device memory (the output tensors here
+    are still allocated by torch unless `out` is given).  Problems whose
+    workspace would exceed INDEXER_STATIC_SCRATCH_BYTES are refused.  Calls
+    that may run at the same time share the scratch and race."""
+    _cuda(q_idx, "q_idx")
+    _cuda(k_idx, "k_idx")
+    _cuda(w, "w", torch.float32)
+    _cuda(q_pos, "q_pos", torch.int32)
+    _cuda(n_cmp, "n_cmp", torch.int32)
+    fp8 = q_idx.dtype in (torch.uint8, torch.float8_e4m3fn)
+    _need(fp8 == (k_idx.dtype in (torch.uint8, torch.float8_e4m3fn)), "q/k dtypes differ")
+    if not fp8:
+        _need(q_idx.dtype == torch.bfloat16 and k_idx.dtype == torch.bfloat16, "bf16 expected")
+    _need(q_idx.is_contiguous() and w.is_contiguous() and q_pos.is_contiguous(),
+          "q_idx, w, q_pos must be contiguous")
+    B, T, H_I, d_I = q_idx.shape
+    N_cap = k_idx.shape[1]
+    dev = q_idx.device
+    if fp8:
+        _cuda(q_scale, "q_scale", torch.float32)
+        _cuda(k_scale, "k_scale", torch.float32)
+        _need(q_scale.is_contiguous() and k_scale.stride(1) == 1, "scale layout")
+    idx = out if out is not None else torch.empty((B, T, k), dtype=torch.int32, device=dev)
+    scores = torch.empty((B, T, k), dtype=torch.float32, device=dev) if return_scores else None
+    st = lib().csa_indexer_topk_static(
+        _p(q_idx), _p(q_scale) if fp8 else None, _p(w), _p(k_idx), _bstride(k_idx),
+        _p(k_scale) if fp8 else None, k_scale.stride(0) if fp8 else 0,
+        CSA_FP8_E4M3 if fp8 else CSA_BF16, _p(q_pos), _p(n_cmp), B, T, H_I, d_I, N_cap, m, k,
+        _p(idx), _p(scores), _p(err_word), _stream(dev))
+    _check(st, "csa_indexer_topk_static")
     return (idx, scores) if return_scores else idx
 
 

@@ -110,3 +110,15 @@ def test_binding_rejects_cpu_tensors():
     with pytest.raises(ValueError):
         csa.sparse_attn_decode(q, q, q, torch.zeros(2, 4, dtype=torch.int32), q, q,
                                torch.zeros(2, dtype=torch.int32), 128, None)
+
+
+def test_static_indexer_refuses_beyond_its_scratch():
+    # 256 queries over 2^19 entries need far more than the fixed scratch; the
+    # refusal comes before any CUDA call, so it needs no GPU
+    L = csa.lib()
+    need = L.csa_indexer_topk_workspace(256, 1, 1 << 19, 64)
+    assert need > csa.INDEXER_STATIC_SCRATCH_BYTES
+    assert L.csa_indexer_topk_workspace(32, 1, 32768, 1024) <= csa.INDEXER_STATIC_SCRATCH_BYTES
+    st = L.csa_indexer_topk_static(FAKE, None, FAKE, FAKE, (1 << 19) * 64, None, 0, 0, FAKE, FAKE,
+                                   256, 1, 4, 64, 1 << 19, 4, 64, FAKE, None, None, None)
+    assert st == 3
