@@ -15,21 +15,28 @@
 // the M side of the contractions (M = 64 for H <= 64, else 128) and every
 // gathered 256-byte K/V row is read from memory once.  Key slots: compressed
 // entries [0, n_c), padding to a multiple of 4, then the window.
-// Warp roles:
-//   warp 0       one thread issues tcgen05.mma and commits; owns TMEM
-//   loader warps (1-3, and 8-11 when M = 64): per 64-key tile, one row lookup
-//                per key, then either one TMA box per (tensor, K-block) when
-//                the 64 rows are contiguous, or 16-byte cp.async row gathers
-//                from every loader thread, into a ring of SW128 stages
-//                (skipped slots are zero-filled)
-//   warps 4-7    softmax on the 16-lane TMEM layout (four threads share a row,
-//                all 32 lanes busy): base-2 online softmax with lazy
-//                rescaling (O in TMEM is rescaled only when a row's running
-//                max grows by more than 2^8); P (bf16) to shared memory
-// Per 64-key tile: S = Q K^T as 8 MMAs of M x 64 x 16 into one of two TMEM
-// buffers; O += P V as 4 MMAs of M x 128 x 16 into a TMEM accumulator.
-// Every mbarrier wait is bounded; on timeout the CTA records CSA_EW_TIMEOUT in
-// the error word, still reaches every barrier, and frees its TMEM.
+//
+// Keys move in 64-key stages and are contracted in 128-key tiles (two
+// consecutive stages).  Shared memory holds four regions (K dims 0-63, K dims
+// 64-127, V dims 0-63, V dims 64-127), each a ring of stages of 64 rows x 128
+// bytes in the 128-byte swizzled layout, so that the rows of a stage pair are
+// contiguous and one MMA descriptor spans 128 keys.
+// Warp roles (384 threads):
+//   warp 0       one thread issues S = Q K^T (8 MMAs of M x 128 x 16) into one
+//                of two TMEM buffers; the warp owns the TMEM allocation
+//   warp 1       one thread issues O += P V (8 MMAs of M x 128 x 16)
+//   warps 2-3, 8-11  loaders: per stage, one row lookup per key, then one TMA
+//                box per region when the 64 rows are contiguous, or 16-byte
+//                cp.async row gathers (skipped slots zero-filled)
+//   warps 4-7    softmax on the 16-lane TMEM layout: base-2 online softmax
+//                with lazy rescaling (O in TMEM is rescaled only when a row's
+//                running max grows by more than 2^8); P (bf16) to shared
+//                memory.  The exponentials of tile t are computed while the
+//                P V of tile t-1 still runs.
+// Separate S and P V issuers keep the tensor pipe fed while either one waits
+// on a barrier.  Every mbarrier wait is bounded; on timeout the CTA records
+// CSA_EW_TIMEOUT in the error word, still reaches every barrier, and frees its
+// TMEM.
 #include "common.cuh"
 #include "kernels.h"
 #include "tc.cuh"
@@ -40,57 +47,69 @@ namespace csa {
 namespace {
 
 constexpr int kD = 128;
-constexpr int kTile = 64;  // keys per tile / stage
-constexpr int kStageBytes = 32768;  // K: 2 K-blocks x [64 x 128 B]; V: 2 blocks
+constexpr int kStageKeys = 64;   // keys per stage (one row lookup per loader lane)
+constexpr int kTileKeys = 128;   // keys per MMA tile (two stages)
+constexpr int kBlk = 8192;       // bytes of one stage in one region (64 rows x 128 B)
+constexpr int kThreads = 384;
+constexpr int kLoadThreads = 192;  // warps 2-3 and 8-11
 constexpr int kSoftWarp0 = 4;
 constexpr int kSoftThreads = 128;
 constexpr int kMaxCluster = 16;
 constexpr uint32_t kWaitLimit = 1u << 24;
+constexpr int kPrefetch = 4;  // stages of top-k entries looked up ahead by the loaders
 
 // TMEM columns
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kSCol = 0;    // S buffer b at column 64 * b
-constexpr uint32_t kOCol = 128;  // O accumulator
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSCol = 0;    // S buffer b at column 128 * b
+constexpr uint32_t kOCol = 256;  // O accumulator
 
 template <int M>
 struct Cfg {
-  static constexpr int kThreads = M == 64 ? 384 : 256;
-  static constexpr int kLoadThreads = M == 64 ? 224 : 96;  // warps 1-3 (+ 8-11)
-  static constexpr int kStages = M == 64 ? 6 : 5;
-  static constexpr int kQBytes = M * 256;    // 2 K-blocks x [M x 128 B]
-  static constexpr int kPBytes = M * 128;    // one K-block of 64 keys per buffer
+  static constexpr int kStages = M == 64 ? 6 : 4;  // 64-key stages, even
+  static constexpr int kPairs = kStages / 2;
+  static constexpr int kRegion = kStages * kBlk;
+  static constexpr int kQBytes = M * 256;  // 2 K-blocks x [M x 128 B]
+  static constexpr int kPBytes = M * 256;  // 2 K-blocks (keys 0-63, 64-127) x [M x 128 B]
   static constexpr int kQOff = 0;
-  static constexpr int kKVOff = kQBytes;
-  static constexpr int kPOff = kKVOff + kStages * kStageBytes;
-  static constexpr int kMetaOff = kPOff + 2 * kPBytes;  // stages x 64 row codes
-  static constexpr int kBarOff = kMetaOff + kStages * kTile * 4;
+  static constexpr int kK0 = kQBytes;
+  static constexpr int kK1 = kK0 + kRegion;
+  static constexpr int kV0 = kK1 + kRegion;
+  static constexpr int kV1 = kV0 + kRegion;
+  static constexpr int kPOff = kV1 + kRegion;
+  static constexpr int kMetaOff = kPOff + kPBytes;  // stages x 64 row codes
+  static constexpr int kBarOff = kMetaOff + kStages * kStageKeys * 4;
   static constexpr int kSmemBytes = kBarOff + 512 + 1024;  // + alignment slack
-  // after the main loop: partial O rows (fp32) in stages 0-1, lse + merge
-  // weights in the P buffers
-  static constexpr int kPartOff = kKVOff;
-  static constexpr int kPartLseOff = kPOff;
-  static constexpr int kWgtOff = kPOff + 512;
+  // after the main loop: own partial O rows (fp32) over the K regions, rows
+  // received from the cluster over the V regions (and P); lse values and
+  // merge weights over Q
+  static constexpr int kPartOff = kK0;
+  static constexpr int kRecvOff = kV0;              // [ns][hp][128] fp32
+  static constexpr int kPartLseOff = kQOff;         // [H]
+  static constexpr int kRecvLseOff = kQOff + 1024;  // [ns][hp]
+  static constexpr int kWgtOff = kQOff + 2048;      // [hp][ns]
   static_assert(kSmemBytes <= 232448, "shared memory");
-  static_assert(2 * kStageBytes >= M * 512, "partial O fits in two stages");
-  static_assert(2 * kPBytes >= 512 + 4 * 64 * kMaxCluster, "merge scratch fits in P");
+  static_assert(2 * kRegion >= M * 512, "partial O fits over the K regions");
+  static_assert(2 * kRegion + kPBytes >= (M + kMaxCluster) * 512, "received rows fit");
+  static_assert(kQBytes >= 3072, "merge scratch fits over Q");
 };
 
 struct Bars {
-  uint64_t kv_full[6];
-  uint64_t kv_empty[6];
-  uint64_t meta_full[6];  // validity bits of the stage's tile published
+  uint64_t kv_full[3];     // per stage pair: both stages landed (one arrival per loader thread
+                           // per stage, plus the TMA bytes)
+  uint64_t pair_empty[3];  // per stage pair: the P V that read it has completed
+  uint64_t meta_full[3];   // per stage pair: validity bits published
   uint64_t s_full[2];
   uint64_t s_free[2];
-  uint64_t p_full[2];
-  uint64_t p_free[2];
+  uint64_t p_full;
+  uint64_t p_free;
   uint64_t q_full;
   uint32_t tmem_slot;
   int timed_out;
   uint32_t valid[6][2];
-  uint32_t dense[6][2];  // per loader warp 0/1: its 32 rows continue row 0's run
+  uint32_t dense[6][2];  // per loader warp 0/1: its 32 rows continue its lane 0's row
 };
 
-// Tensor maps: the query block, and boxes of 64 rows that load a whole tile
+// Tensor maps: the query block, and boxes of 64 rows that load a whole stage
 // of contiguous compressed entries.
 struct Maps {
   CUtensorMap q, kc, vc;
@@ -99,9 +118,9 @@ struct Maps {
 // Slot -> row code: r >= 0 is row r of the 2-D row view of the compressed
 // caches, -1 a skipped slot, -(r + 2) row r of the raw (window) caches.  Row
 // counts below 2^31 - 2 are checked on the host.
-
 struct KeySet {
   const int32_t* sel;  // nullptr: dense
+  const int32_t* src;  // list read by fetch(): sel, or any valid int32 when there is none
   int n_c, n_c4;
   int n_cap;
   int64_t cmp_row0;  // b * cmp rows per sequence
@@ -110,12 +129,17 @@ struct KeySet {
   int64_t raw_cap;
   int k_end;
 
-  __device__ __forceinline__ int32_t code(int v, int32_t* err) const {
+  // The top-k entry behind slot v (meaningless for slots that have none).
+  // The value is only consumed by code(), stages later, so the load latency
+  // overlaps the stages in between; the address always stays in the list.
+  __device__ __forceinline__ int32_t fetch(int v) const {
+    return __ldg(src + (sel ? (v < n_c ? v : n_c - 1) : 0));
+  }
+  __device__ __forceinline__ int32_t code(int v, int32_t s, int32_t* err) const {
     if (v >= k_end) return -1;
     if (v < n_c) {
       int64_t e = v;
       if (sel) {
-        const int32_t s = __ldg(sel + v);
         if (s < 0 || s >= n_cap) {
           if (s != -1) flag_error(err, CSA_EW_BAD_INDEX);
           return -1;
@@ -140,20 +164,18 @@ __device__ __forceinline__ bool wait_or_flag(uint64_t* bar, uint32_t parity, Bar
 }
 
 // AND of a predicate over the loader threads (named barrier 1).
-template <int NL>
 __device__ __forceinline__ bool loaders_all(bool v) {
   uint32_t r;
   asm volatile(
       "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.and.pred p, 1, %2, q;\n"
       " selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(r)
-      : "r"((uint32_t)v), "n"(NL)
+      : "r"((uint32_t)v), "n"(kLoadThreads)
       : "memory");
   return r != 0;
 }
-template <int NL>
 __device__ __forceinline__ void loaders_sync() {
-  asm volatile("bar.sync 1, %0;\n" ::"n"(NL) : "memory");
+  asm volatile("bar.sync 1, %0;\n" ::"n"(kLoadThreads) : "memory");
 }
 
 template <int M>
@@ -168,11 +190,12 @@ struct RowMap {  // softmax-thread view of the 16-lane TMEM layout
 };
 
 template <int M>
-__global__ void __launch_bounds__(Cfg<M>::kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(AttnArgs a, const __grid_constant__ Maps maps) {
   using C = Cfg<M>;
   constexpr int kStages = C::kStages;
-  constexpr int NL = C::kLoadThreads;
+  constexpr int kPairs = C::kPairs;
+  constexpr int NL = kLoadThreads;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* sm = smem_raw + ((1024 - (raw_addr & 1023)) & 1023);
@@ -184,8 +207,8 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, 1)
   const int qid = blockIdx.x / ns, split = blockIdx.x % ns;
   const int b = qid / a.T;
   const int H = a.H;
-  const bool is_loader = (warp >= 1 && warp <= 3) || (M == 64 && warp >= 8);
-  const int lt = warp <= 3 ? tid - 32 : tid - 160;  // loader index (loader warps only)
+  const bool is_loader = warp == 2 || warp == 3 || warp >= 8;
+  const int lt = warp <= 3 ? tid - 64 : tid - 192;  // loader index (loader warps only)
 
   // ---- the query's key set and this split's range
   const int64_t t = a.pos_is_len ? (int64_t)__ldg(a.pos + b) - 1 : (int64_t)__ldg(a.pos + qid);
@@ -210,30 +233,36 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, 1)
   const int k_begin = split * a.keys_per_split;
   int k_end = k_begin + a.keys_per_split;
   if (k_end > n_keys) k_end = n_keys;
-  const int n_tiles = k_end > k_begin ? (k_end - k_begin + kTile - 1) / kTile : 0;
+  const int n_tiles = k_end > k_begin ? (k_end - k_begin + kTileKeys - 1) / kTileKeys : 0;
+  const int n_stages = 2 * n_tiles;
 
-  // ---- set-up: barriers, TMEM, zero Q rows >= H (the MMA reads M rows)
+  // ---- set-up: barriers, TMEM, the query block, zero Q rows >= H
   if (warp == 0) {
     tc::tmem_alloc(&bars->tmem_slot, kTmemCols);
     tc::tmem_relinquish();
   }
   if (tid == 32) {
-    for (int s = 0; s < kStages; ++s) {
-      tc::mbar_init(&bars->kv_full[s], NL + 1);
-      tc::mbar_init(&bars->kv_empty[s], 1);
-      tc::mbar_init(&bars->meta_full[s], 1);
+    for (int p = 0; p < kPairs; ++p) {
+      tc::mbar_init(&bars->kv_full[p], 2 * kLoadThreads);
+      tc::mbar_init(&bars->pair_empty[p], 1);
+      tc::mbar_init(&bars->meta_full[p], 1);
     }
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&bars->s_full[i], 1);
-      tc::mbar_init(&bars->s_free[i], kSoftThreads);
-      tc::mbar_init(&bars->p_full[i], kSoftThreads);
-      tc::mbar_init(&bars->p_free[i], 1);
+      tc::mbar_init(&bars->s_free[i], kSoftThreads / 32);  // one arrival per softmax warp
     }
+    tc::mbar_init(&bars->p_full, kSoftThreads / 32);
+    tc::mbar_init(&bars->p_free, 1);
     tc::mbar_init(&bars->q_full, 1);
     bars->timed_out = 0;
     tc::fence_mbar_init();
+    if (n_tiles > 0) {  // H rows of 256 bytes as two K-blocks
+      tma::expect_tx(&bars->q_full, 2 * H * 128);
+      tma::load_box(sbase + C::kQOff, &maps.q, 0, qid * H, &bars->q_full);
+      tma::load_box(sbase + C::kQOff + M * 128, &maps.q, 64, qid * H, &bars->q_full);
+    }
   }
-  for (int idx = tid; idx < (M - H) * 16; idx += C::kThreads) {
+  for (int idx = tid; idx < (M - H) * 16; idx += kThreads) {
     const int r = H + (idx >> 4), c16 = idx & 15;
     *reinterpret_cast<uint4*>(sm + C::kQOff + (c16 >> 3) * (M * 128) +
                               tc::sw128_offset(r, c16 & 7)) = make_uint4(0, 0, 0, 0);
@@ -245,54 +274,61 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, 1)
   const uint32_t tmem = bars->tmem_slot;
 
   if (n_tiles > 0 && warp == 0) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ S issuer
     if (lane == 0) {
-      const uint32_t id_s = tc::idesc_bf16(M, kTile, false, false);
-      const uint32_t id_o = tc::idesc_bf16(M, kD, false, true);
-      auto issue_pv = [&](int i) -> bool {
-        const int st = i % kStages, pb = i & 1;
-        if (!wait_or_flag(&bars->p_full[pb], (i >> 1) & 1, bars, a.err)) return false;
-        tc::fence_after_sync();
-        const uint32_t p_addr = sbase + C::kPOff + pb * C::kPBytes;
-        const uint32_t v_addr = sbase + C::kKVOff + st * kStageBytes + 16384;
-#pragma unroll
-        for (int s = 0; s < kTile / 16; ++s) {
-          const uint64_t ad = tc::desc_sw128(p_addr + s * 32, 16, 1024);
-          const uint64_t bd = tc::desc_sw128(v_addr + s * 2048, kTile * 128, 1024);
-          tc::mma_ss(tmem + kOCol, ad, bd, id_o, (i > 0 || s > 0) ? 1u : 0u);
-        }
-        tc::mma_commit(&bars->p_free[pb]);
-        tc::mma_commit(&bars->kv_empty[st]);
-        return true;
-      };
+      const uint32_t id_s = tc::idesc_bf16(M, kTileKeys, false, false);
       bool ok = wait_or_flag(&bars->q_full, 0, bars, a.err);
       for (int j = 0; j < n_tiles && ok; ++j) {
-        const int st = j % kStages, sb = j & 1;
-        ok = wait_or_flag(&bars->kv_full[st], (j / kStages) & 1, bars, a.err);
+        const int pr = j % kPairs, sb = j & 1;
+        ok = wait_or_flag(&bars->kv_full[pr], (j / kPairs) & 1, bars, a.err);
         if (ok && j >= 2) ok = wait_or_flag(&bars->s_free[sb], ((j - 2) >> 1) & 1, bars, a.err);
         if (!ok) break;
         tc::fence_after_sync();
-        const uint32_t k_addr = sbase + C::kKVOff + st * kStageBytes;
+        const uint32_t k0 = sbase + C::kK0 + pr * 2 * kBlk;
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint64_t ad =
               tc::desc_sw128(sbase + C::kQOff + (kk >> 2) * (M * 128) + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = tc::desc_sw128(k_addr + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
-          tc::mma_ss(tmem + kSCol + sb * kTile, ad, bd, id_s, kk > 0 ? 1u : 0u);
+          const uint64_t bd =
+              tc::desc_sw128(k0 + (kk >> 2) * C::kRegion + (kk & 3) * 32, 16, 1024);
+          tc::mma_ss(tmem + kSCol + sb * kTileKeys, ad, bd, id_s, kk > 0 ? 1u : 0u);
         }
         tc::mma_commit(&bars->s_full[sb]);
-        if (j >= 1) ok = issue_pv(j - 1);
       }
-      if (ok) ok = issue_pv(n_tiles - 1);
+    }
+    __syncwarp();
+  } else if (n_tiles > 0 && warp == 1) {
+    // ------------------------------------------------------------ P V issuer
+    if (lane == 0) {
+      const uint32_t id_o = tc::idesc_bf16(M, kD, false, true);
+      bool ok = true;
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        const int pr = j % kPairs;
+        ok = wait_or_flag(&bars->p_full, j & 1, bars, a.err);
+        if (!ok) break;
+        tc::fence_after_sync();
+        const uint32_t v0 = sbase + C::kV0 + pr * 2 * kBlk;
+#pragma unroll
+        for (int s = 0; s < kTileKeys / 16; ++s) {
+          const uint64_t ad =
+              tc::desc_sw128(sbase + C::kPOff + (s >> 2) * (M * 128) + (s & 3) * 32, 16, 1024);
+          const uint64_t bd = tc::desc_sw128(v0 + s * 2048, C::kRegion, 1024);
+          tc::mma_ss(tmem + kOCol, ad, bd, id_o, (j > 0 || s > 0) ? 1u : 0u);
+        }
+        tc::mma_commit(&bars->p_free);
+        tc::mma_commit(&bars->pair_empty[pr]);
+      }
       // drain: the last commit covers every MMA this thread issued
-      if (ok) wait_or_flag(&bars->kv_empty[(n_tiles - 1) % kStages],
-                           ((n_tiles - 1) / kStages) & 1, bars, a.err);
+      if (ok)
+        wait_or_flag(&bars->pair_empty[(n_tiles - 1) % kPairs], ((n_tiles - 1) / kPairs) & 1,
+                     bars, a.err);
     }
     __syncwarp();
   } else if (n_tiles > 0 && is_loader) {
     // ------------------------------------------------------------ loaders
     KeySet ks;
-    ks.sel = a.dense ? nullptr : a.sel + (int64_t)qid * a.sel_stride;
+    ks.sel = (a.dense || n_c == 0) ? nullptr : a.sel + (int64_t)qid * a.sel_stride;
+    ks.src = ks.sel ? ks.sel : a.pos;
     ks.n_c = n_c;
     ks.n_c4 = n_c4;
     ks.n_cap = a.N_cap;
@@ -305,78 +341,81 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, 1)
     const bf16* vc = a.v_cmp;
     const bf16* kr = a.k_raw;
     const bf16* vr = a.v_raw;
-    if (lt == 0) {
-      tma::expect_tx(&bars->q_full, 2 * H * 128);
-      tma::load_box(sbase + C::kQOff, &maps.q, 0, qid * H, &bars->q_full);
-      tma::load_box(sbase + C::kQOff + M * 128, &maps.q, 64, qid * H, &bars->q_full);
-    }
     int32_t* codes = reinterpret_cast<int32_t*>(sm + C::kMetaOff);
-    // row code of this thread's row (lt < 64) for the next tile, looked up
-    // while the current tile is issued; base = the tile's first row code
-    int32_t next = lt < kTile ? ks.code(k_begin + lt, a.err) : -1;
-    int32_t next_base = ks.code(k_begin, nullptr);
+    // top-k entries of this thread's slot (lt < 64) for the next kPrefetch
+    // stages: pf[i] belongs to stage j + i
+    int32_t pf[kPrefetch];
+#pragma unroll
+    for (int i = 0; i < kPrefetch; ++i)
+      pf[i] = lt < kStageKeys ? ks.fetch(k_begin + i * kStageKeys + lt) : 0;
+    // Every loader thread gives one arrival per stage on its pair's kv_full:
+    // for a gathered stage once its own copies have landed (cp.async
+    // mbarrier tracking, the loader does not block), for a TMA stage at issue
+    // (thread 0's arrival carries the transaction count).
     int issued = 0;
-    for (int j = 0; j < n_tiles; ++j) {
-      const int st = j % kStages;
+    for (int j = 0; j < n_stages; ++j) {
+      const int st = j % kStages, pr = (j >> 1) % kPairs;
       bool go = true;
-      if (lt == 0 && j >= kStages)
-        go = wait_or_flag(&bars->kv_empty[st], ((j / kStages) - 1) & 1, bars, a.err);
+      if (lt == 0 && j >= kStages && (j & 1) == 0)
+        go = wait_or_flag(&bars->pair_empty[pr], ((j >> 1) / kPairs - 1) & 1, bars, a.err);
       go = go && !*(volatile int*)&bars->timed_out;
       // every loader thread takes the same branch: named barrier 1 below
-      if (!loaders_all<NL>(go)) break;
-      const int32_t base = next_base;
-      if (lt < kTile) {
-        codes[st * kTile + lt] = next;
-        const unsigned vb = __ballot_sync(0xFFFFFFFFu, next != -1);
-        const bool cons = base >= 0 && next == base + lt;
-        const unsigned cb = __ballot_sync(0xFFFFFFFFu, cons);
+      if (!loaders_all(go)) break;
+      if (lt < kStageKeys) {
+        const int32_t cd = ks.code(k_begin + j * kStageKeys + lt, pf[0], a.err);
+        codes[st * kStageKeys + lt] = cd;
+        // contiguous compressed rows within this warp's 32 slots
+        const int32_t w0 = __shfl_sync(0xFFFFFFFFu, cd, 0);
+        const unsigned vb = __ballot_sync(0xFFFFFFFFu, cd != -1);
+        const unsigned cb = __ballot_sync(0xFFFFFFFFu, w0 >= 0 && cd == w0 + (lt & 31));
         if ((lt & 31) == 0) {
           bars->valid[st][lt >> 5] = vb;
           bars->dense[st][lt >> 5] = cb;
         }
       }
-      loaders_sync<NL>();
-      const bool dense = (bars->dense[st][0] & bars->dense[st][1]) == 0xFFFFFFFFu;
-      if (lt == 0) tc::mbar_arrive(&bars->meta_full[st]);
-      const uint32_t kdst = sbase + C::kKVOff + st * kStageBytes;
+#pragma unroll
+      for (int i = 0; i + 1 < kPrefetch; ++i) pf[i] = pf[i + 1];
+      if (lt < kStageKeys)
+        pf[kPrefetch - 1] = ks.fetch(k_begin + (j + kPrefetch) * kStageKeys + lt);
+      loaders_sync();
+      const int32_t base = codes[st * kStageKeys];
+      const bool dense = (bars->dense[st][0] & bars->dense[st][1]) == 0xFFFFFFFFu &&
+                         codes[st * kStageKeys + 32] == base + 32;
+      if (lt == 0 && (j & 1)) tc::mbar_arrive(&bars->meta_full[pr]);  // both stages' bits
+      const uint32_t off = st * kBlk;
       if (dense) {
         if (lt == 0) {
-          tma::expect_tx(&bars->kv_full[st], kStageBytes);  // the extra arrival
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            tma::load_box(kdst + (i >> 1) * 16384 + (i & 1) * 8192, (i >> 1) ? &maps.vc : &maps.kc,
-                          (i & 1) * 64, (int)base, &bars->kv_full[st]);
+          tma::expect_tx(&bars->kv_full[pr], 4 * kBlk);
+          tma::load_box(sbase + C::kK0 + off, &maps.kc, 0, (int)base, &bars->kv_full[pr]);
+          tma::load_box(sbase + C::kK1 + off, &maps.kc, 64, (int)base, &bars->kv_full[pr]);
+          tma::load_box(sbase + C::kV0 + off, &maps.vc, 0, (int)base, &bars->kv_full[pr]);
+          tma::load_box(sbase + C::kV1 + off, &maps.vc, 64, (int)base, &bars->kv_full[pr]);
+        } else {
+          tc::mbar_arrive(&bars->kv_full[pr]);
         }
-        tc::mbar_arrive(&bars->kv_full[st]);
       } else {
-        if (lt == 0) tc::mbar_arrive(&bars->kv_full[st]);  // the extra arrival
-        for (int ci = lt; ci < kTile * 16; ci += NL) {
+        for (int ci = lt; ci < kStageKeys * 16; ci += NL) {
           const int r = ci >> 4, c16 = ci & 15;
-          const int32_t cd = codes[st * kTile + r];
+          const int32_t cd = codes[st * kStageKeys + r];
           const bool ok = cd != -1;
           const bool raw = cd < -1;
-          const int64_t off = (int64_t)(raw ? -(cd + 2) : cd) * kD + c16 * 8;
-          const bf16* kp = ok ? (raw ? kr : kc) + off : a.q;
-          const bf16* vp = ok ? (raw ? vr : vc) + off : a.q;
-          const uint32_t so = (c16 >> 3) * 8192 + tc::sw128_offset(r, c16 & 7);
-          cp_async16(kdst + so, kp, ok ? 16 : 0);
-          cp_async16(kdst + 16384 + so, vp, ok ? 16 : 0);
+          const int64_t goff = (int64_t)(raw ? -(cd + 2) : cd) * kD + c16 * 8;
+          const bf16* kp = ok ? (raw ? kr : kc) + goff : a.q;
+          const bf16* vp = ok ? (raw ? vr : vc) + goff : a.q;
+          const uint32_t so = off + ((c16 >> 3) ? C::kRegion : 0) + tc::sw128_offset(r, c16 & 7);
+          cp_async16(sbase + C::kK0 + so, kp, ok ? 16 : 0);
+          cp_async16(sbase + C::kV0 + so, vp, ok ? 16 : 0);
         }
-        tc::cp_async_mbar_arrive(&bars->kv_full[st]);
+        tc::cp_async_mbar_arrive(&bars->kv_full[pr]);
       }
       issued = j + 1;
-      if (j + 1 < n_tiles) {
-        const int v0 = k_begin + (j + 1) * kTile;
-        if (lt < kTile) next = ks.code(v0 + lt, a.err);
-        next_base = ks.code(v0, nullptr);
-      }
     }
     asm volatile("cp.async.wait_all;\n" ::: "memory");
-    // bulk copies still in flight after a timeout land before the CTA exits
     if (lt == 0) {
+      // bulk copies still in flight after a timeout land before the CTA exits
       tc::mbar_wait(&bars->q_full, 0, kWaitLimit);
-      for (int i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
-        tc::mbar_wait(&bars->kv_full[i % kStages], (i / kStages) & 1, kWaitLimit);
+      for (int i = issued > kStages ? issued - kStages : 0; i < issued; i += 2)
+        tc::mbar_wait(&bars->kv_full[(i >> 1) % kPairs], ((i >> 1) / kPairs) & 1, kWaitLimit);
     }
   } else if (warp >= kSoftWarp0 && warp < kSoftWarp0 + 4) {
     // ------------------------------------------------------------ softmax
@@ -390,37 +429,38 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, 1)
       m_ref[g][0] = m_ref[g][1] = -INFINITY;
       l_sum[g][0] = l_sum[g][1] = 0.f;
     }
+    uint8_t* pbuf = sm + C::kPOff;
     for (int j = 0; j < n_tiles; ++j) {
-      const int sb = j & 1, st = j % kStages;
+      const int sb = j & 1, pr = j % kPairs;
       // waits are made warp-uniform: tcgen05.ld/st below are warp-collective
       if (!__all_sync(0xFFFFFFFFu,
-                      wait_or_flag(&bars->meta_full[st], (j / kStages) & 1, bars, a.err)))
+                      wait_or_flag(&bars->meta_full[pr], (j / kPairs) & 1, bars, a.err)))
         break;
-      const uint32_t vm0 = bars->valid[st][0], vm1 = bars->valid[st][1];
+      const int st0 = (2 * j) % kStages;
+      const uint32_t vm[4] = {bars->valid[st0][0], bars->valid[st0][1], bars->valid[st0 + 1][0],
+                              bars->valid[st0 + 1][1]};
       if (!__all_sync(0xFFFFFFFFu, wait_or_flag(&bars->s_full[sb], (j >> 1) & 1, bars, a.err)))
         break;
       tc::fence_after_sync();
-      // sr[g][q*16 + u*4 + k]: k = 0,1 -> row A cols 32q + 8u + 2c4 (+1);
-      //                        k = 2,3 -> row B, same columns
-      uint32_t sr[NG][32];
-#pragma unroll
-      for (int g = 0; g < NG; ++g)
-#pragma unroll
-        for (int q = 0; q < 2; ++q)
-          tc::tmem_ld16x256_x4(tmem + RM::lane_field(qd, g) + kSCol + sb * kTile + q * 32,
-                               &sr[g][q * 16]);
-      tc::tmem_ld_wait();
-      tc::fence_before_sync();
-      tc::mbar_arrive(&bars->s_free[sb]);
-
-      bool need_rescale = false;
-      float mt[NG][2];
-#pragma unroll
+      bool stop = false;
+#pragma unroll 1
       for (int g = 0; g < NG; ++g) {
-        mt[g][0] = mt[g][1] = -INFINITY;
+        // sr[q*16 + u*4 + k]: k = 0,1 -> row A cols 32q + 8u + 2c4 (+1);
+        //                     k = 2,3 -> row B, same columns
+        uint32_t sr[64];
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const uint32_t vm = q ? vm1 : vm0;
+        for (int q = 0; q < 4; ++q)
+          tc::tmem_ld16x256_x4(tmem + RM::lane_field(qd, g) + kSCol + sb * kTileKeys + q * 32,
+                               &sr[q * 16]);
+        tc::tmem_ld_wait();
+        if (g == NG - 1) {
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&bars->s_free[sb]);
+        }
+        float mt[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
 #pragma unroll
           for (int u = 0; u < 4; ++u)
 #pragma unroll
@@ -428,35 +468,49 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, 1)
               const int bit = 8 * u + 2 * c4 + (k & 1);
               const int i = q * 16 + u * 4 + k;
               const float x =
-                  ((vm >> bit) & 1u) ? __uint_as_float(sr[g][i]) * a.scale_log2 : -INFINITY;
-              sr[g][i] = __float_as_uint(x);
-              mt[g][k >> 1] = fmaxf(mt[g][k >> 1], x);
+                  ((vm[q] >> bit) & 1u) ? __uint_as_float(sr[i]) * a.scale_log2 : -INFINITY;
+              sr[i] = __float_as_uint(x);
+              mt[k >> 1] = fmaxf(mt[k >> 1], x);
             }
-        }
+        // lazy rescaling: a row's reference max moves only when the tile max
+        // exceeds it by more than 2^8 (or on its first finite tile)
+        float f[2];
+        bool grow_any = false;
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
-          mt[g][h2] = fmaxf(mt[g][h2], __shfl_xor_sync(0xFFFFFFFFu, mt[g][h2], 1));
-          mt[g][h2] = fmaxf(mt[g][h2], __shfl_xor_sync(0xFFFFFFFFu, mt[g][h2], 2));
-          need_rescale |= mt[g][h2] > m_ref[g][h2] + 8.f && m_ref[g][h2] != -INFINITY;
+          mt[h2] = fmaxf(mt[h2], __shfl_xor_sync(0xFFFFFFFFu, mt[h2], 1));
+          mt[h2] = fmaxf(mt[h2], __shfl_xor_sync(0xFFFFFFFFu, mt[h2], 2));
+          const bool move = mt[h2] > m_ref[g][h2] + 8.f;
+          const bool grow = move && m_ref[g][h2] != -INFINITY;
+          f[h2] = grow ? ex2_approx(m_ref[g][h2] - mt[h2]) : 1.f;
+          grow_any |= grow;
+          if (move) m_ref[g][h2] = mt[h2];
+          l_sum[g][h2] *= f[h2];
         }
-      }
-      // lazy rescaling: a row's reference max moves only when the tile max
-      // exceeds it by more than 2^8 (or on its first finite tile)
-      if (__any_sync(0xFFFFFFFFu, need_rescale)) {
-        // O holds sum p*v relative to m_ref: wait for the P.V of tile j-1
-        if (!__all_sync(0xFFFFFFFFu, wait_or_flag(&bars->p_free[(j - 1) & 1],
-                                                  ((j - 1) >> 1) & 1, bars, a.err)))
-          break;
-        tc::fence_after_sync();
+        // exponentials (relative to the new reference) while P V of tile j-1 runs
+        const float mA = m_ref[g][0] == -INFINITY ? 0.f : m_ref[g][0];
+        const float mB = m_ref[g][1] == -INFINITY ? 0.f : m_ref[g][1];
+        uint32_t pk[32];
 #pragma unroll
-        for (int g = 0; g < NG; ++g) {
-          float f[2];
-#pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) {
-            const bool grow = mt[g][h2] > m_ref[g][h2] + 8.f && m_ref[g][h2] != -INFINITY;
-            f[h2] = grow ? exp2f(m_ref[g][h2] - mt[g][h2]) : 1.f;
-            l_sum[g][h2] *= f[h2];
+        for (int i = 0; i < 16; ++i) {
+          const float p0 = ex2_approx(__uint_as_float(sr[4 * i]) - mA);
+          const float p1 = ex2_approx(__uint_as_float(sr[4 * i + 1]) - mA);
+          const float p2 = ex2_approx(__uint_as_float(sr[4 * i + 2]) - mB);
+          const float p3 = ex2_approx(__uint_as_float(sr[4 * i + 3]) - mB);
+          l_sum[g][0] += p0 + p1;
+          l_sum[g][1] += p2 + p3;
+          pk[2 * i] = pack_bf16x2(p0, p1);
+          pk[2 * i + 1] = pack_bf16x2(p2, p3);
+        }
+        // the P buffer and O are free once P V of tile j-1 has completed
+        if (g == 0 && j >= 1) {
+          if (!__all_sync(0xFFFFFFFFu, wait_or_flag(&bars->p_free, (j - 1) & 1, bars, a.err))) {
+            stop = true;
+            break;
           }
+          tc::fence_after_sync();
+        }
+        if (__any_sync(0xFFFFFFFFu, grow_any)) {
 #pragma unroll 1
           for (int q = 0; q < 4; ++q) {
             uint32_t o[16];
@@ -468,51 +522,31 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, 1)
               o[i] = __float_as_uint(__uint_as_float(o[i]) * f[(i & 3) >> 1]);
             tc::tmem_st16x256_x4(ta, o);
           }
+          tc::tmem_st_wait();
         }
-        tc::tmem_st_wait();
-      }
-#pragma unroll
-      for (int g = 0; g < NG; ++g)
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2)
-          if (mt[g][h2] > m_ref[g][h2] + 8.f) m_ref[g][h2] = mt[g][h2];
-      // P buffer sb was last read by the P.V of tile j-2
-      if (j >= 2 && !__all_sync(0xFFFFFFFFu, wait_or_flag(&bars->p_free[sb], ((j - 2) >> 1) & 1,
-                                                         bars, a.err)))
-        break;
-      uint8_t* pbuf = sm + C::kPOff + sb * C::kPBytes;
-#pragma unroll
-      for (int g = 0; g < NG; ++g) {
-        const float mA = m_ref[g][0] == -INFINITY ? 0.f : m_ref[g][0];
-        const float mB = m_ref[g][1] == -INFINITY ? 0.f : m_ref[g][1];
         const int rowA = RM::row(qd, g, r8), rowB = rowA + 8;
 #pragma unroll
-        for (int q = 0; q < 2; ++q)
+        for (int q = 0; q < 4; ++q)
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const int i = q * 16 + u * 4;
-            const float p0 = exp2f(__uint_as_float(sr[g][i]) - mA);
-            const float p1 = exp2f(__uint_as_float(sr[g][i + 1]) - mA);
-            const float p2 = exp2f(__uint_as_float(sr[g][i + 2]) - mB);
-            const float p3 = exp2f(__uint_as_float(sr[g][i + 3]) - mB);
-            l_sum[g][0] += p0 + p1;
-            l_sum[g][1] += p2 + p3;
-            // key 32q + 8u + 2c4: 16-byte chunk 4q + u, byte 4c4
-            *reinterpret_cast<uint32_t*>(pbuf + tc::sw128_offset(rowA, 4 * q + u) + 4 * c4) =
-                pack_bf16x2(p0, p1);
-            *reinterpret_cast<uint32_t*>(pbuf + tc::sw128_offset(rowB, 4 * q + u) + 4 * c4) =
-                pack_bf16x2(p2, p3);
+            // key 32q + 8u + 2c4: K-block q/2, 16-byte chunk 4(q%2) + u, byte 4c4
+            uint8_t* blk = pbuf + (q >> 1) * (M * 128) + 4 * c4;
+            *reinterpret_cast<uint32_t*>(blk + tc::sw128_offset(rowA, 4 * (q & 1) + u)) =
+                pk[2 * (q * 4 + u)];
+            *reinterpret_cast<uint32_t*>(blk + tc::sw128_offset(rowB, 4 * (q & 1) + u)) =
+                pk[2 * (q * 4 + u) + 1];
           }
       }
+      if (stop) break;
       tc::fence_proxy_async_smem();
       tc::fence_before_sync();
-      tc::mbar_arrive(&bars->p_full[sb]);
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&bars->p_full);
     }
-    // ---- epilogue: O rows after the last P.V, normalised
+    // ---- epilogue: O rows after the last P V, normalised
     bool have_o = n_tiles > 0 && !*(volatile int*)&bars->timed_out;
     if (__any_sync(0xFFFFFFFFu, have_o))
-      have_o = wait_or_flag(&bars->p_free[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1, bars,
-                            a.err);
+      have_o = wait_or_flag(&bars->p_free, (n_tiles - 1) & 1, bars, a.err);
     have_o = __all_sync(0xFFFFFFFFu, have_o);
     tc::fence_after_sync();
 #pragma unroll
@@ -596,27 +630,42 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, 1)
   }
   if (ns <= 1) return;
 
-  // ---- split merge inside the cluster: CTA `split` combines heads
-  // [split*hp, split*hp + hp) from every CTA's shared memory
+  // ---- split merge inside the cluster.  CTA `split` combines heads
+  // [split*hp, split*hp + hp).  After the first cluster barrier no CTA uses
+  // its stages again, so every CTA pushes its partial rows and lse values for
+  // those heads into the owner's shared memory (remote stores, no round
+  // trips); after the second barrier each CTA combines its heads locally.
   tc::cluster_sync();
   const int hp = (H + ns - 1) / ns;
+  {
+    const float* part = reinterpret_cast<const float*>(sm + C::kPartOff);
+    const float* part_lse = reinterpret_cast<const float*>(sm + C::kPartLseOff);
+    for (int it = tid; it < H * 32; it += kThreads) {
+      const int h = it >> 5, d4 = it & 31;
+      const int owner = h / hp, slot = split * hp + (h - owner * hp);
+      const float4 v = *reinterpret_cast<const float4*>(part + h * kD + d4 * 4);
+      tc::st_cluster_f32x4(tc::map_shared(sbase + C::kRecvOff + slot * 512 + d4 * 16, owner), v);
+    }
+    for (int h = tid; h < H; h += kThreads) {
+      const int owner = h / hp, slot = split * hp + (h - owner * hp);
+      tc::st_cluster_f32(tc::map_shared(sbase + C::kRecvLseOff + slot * 4, owner), part_lse[h]);
+    }
+  }
+  tc::cluster_sync();
   const int h0 = split * hp;
   const int nh = H - h0 < hp ? (H - h0 > 0 ? H - h0 : 0) : hp;
-  float* wgt = reinterpret_cast<float*>(sm + C::kWgtOff);  // [nh][ns]
-  for (int i = tid; i < nh * ns; i += C::kThreads) {
-    const int hl = i / ns, s = i % ns;
-    wgt[i] = tc::ld_cluster_f32(tc::map_shared(sbase + C::kPartLseOff + (h0 + hl) * 4, s));
-  }
-  __syncthreads();
-  for (int hl = tid; hl < nh; hl += C::kThreads) {
+  const float* rlse = reinterpret_cast<const float*>(sm + C::kRecvLseOff);  // [ns][hp]
+  const float* rrow = reinterpret_cast<const float*>(sm + C::kRecvOff);     // [ns][hp][128]
+  float* wgt = reinterpret_cast<float*>(sm + C::kWgtOff);                  // [nh][ns]
+  for (int hl = tid; hl < nh; hl += kThreads) {
     const int h = h0 + hl;
     float Mx = a.sink ? __ldg(a.sink + h) : -INFINITY;
-    for (int s = 0; s < ns; ++s) Mx = fmaxf(Mx, wgt[hl * ns + s]);
+    for (int s = 0; s < ns; ++s) Mx = fmaxf(Mx, rlse[s * hp + hl]);
     float lse = -INFINITY;
     if (Mx != -INFINITY) {
       float Z = a.sink ? expf(__ldg(a.sink + h) - Mx) : 0.f;
       for (int s = 0; s < ns; ++s) {
-        const float ls = wgt[hl * ns + s];
+        const float ls = rlse[s * hp + hl];
         const float w = ls == -INFINITY ? 0.f : expf(ls - Mx);
         wgt[hl * ns + s] = w;
         Z += w;
@@ -630,14 +679,12 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, 1)
     if (a.lse) a.lse[(int64_t)qid * H + h] = lse;
   }
   __syncthreads();
-  for (int it = tid; it < nh * 32; it += C::kThreads) {
+  for (int it = tid; it < nh * 32; it += kThreads) {
     const int hl = it >> 5, d4 = it & 31, h = h0 + hl;
-    const uint32_t src = sbase + C::kPartOff + h * 512 + d4 * 16;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
     for (int s = 0; s < ns; ++s) {
       const float w = wgt[hl * ns + s];
-      const float4 v = tc::ld_cluster_f32x4(tc::map_shared(src, s));
+      const float4 v = *reinterpret_cast<const float4*>(rrow + (s * hp + hl) * kD + d4 * 4);
       acc.x += w * v.x;
       acc.y += w * v.y;
       acc.z += w * v.z;
@@ -646,8 +693,6 @@ __global__ void __launch_bounds__(Cfg<M>::kThreads, 1)
     reinterpret_cast<uint2*>(a.out + ((int64_t)qid * H + h) * kD)[d4] =
         make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
   }
-  // no CTA leaves while another may still read its shared memory
-  tc::cluster_sync();
 }
 
 template <int M>
@@ -655,7 +700,7 @@ cudaLaunchConfig_t launch_cfg(int n_split, int n_query, cudaStream_t st,
                               cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)n_split * (unsigned)n_query);
-  cfg.blockDim = dim3(Cfg<M>::kThreads);
+  cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = Cfg<M>::kSmemBytes;
   cfg.stream = st;
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -718,17 +763,17 @@ cudaError_t launch_tc(AttnArgs a, const Maps& maps, cudaStream_t st) {
 
 // Split plan: the splits of a query run as one cluster of at most
 // max_cluster CTAs; about one CTA per SM in total.  Splits hold a multiple of
-// 4 key slots; the key count includes up to 3 padding slots after the
-// compressed entries.
+// 64 key slots (one stage); the key count includes up to 3 padding slots
+// after the compressed entries.
 void attn_plan(int n_query, int n_keys_max, int max_cluster, int* n_split, int* keys_per_split) {
   n_keys_max += 3;
   int ns = kNumSMs / (n_query > 0 ? n_query : 1);
-  const int max_tiles = (n_keys_max + kTile - 1) / kTile;
+  const int max_tiles = (n_keys_max + kTileKeys - 1) / kTileKeys;
   if (ns > max_tiles) ns = max_tiles;
   if (ns > max_cluster) ns = max_cluster;
   if (ns < 1) ns = 1;
   int kps = (n_keys_max + ns - 1) / ns;
-  kps = (kps + 3) & ~3;
+  kps = (kps + kStageKeys - 1) / kStageKeys * kStageKeys;
   ns = (n_keys_max + kps - 1) / kps;
   if (ns < 1) ns = 1;
   *n_split = ns;
@@ -745,8 +790,8 @@ cudaError_t launch_attention(AttnArgs a, void*, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   const bool has_c = a.k_cmp && a.N_cap > 0;
   const uint64_t crow = has_c ? (uint64_t)(a.n_batch - 1) * (a.cmp_bstride / kD) + a.N_cap : 1;
-  e = tma::encode_rows128(&maps.kc, has_c ? a.k_cmp : dummy, crow, kTile);
-  if (e == cudaSuccess) e = tma::encode_rows128(&maps.vc, has_c ? a.v_cmp : dummy, crow, kTile);
+  e = tma::encode_rows128(&maps.kc, has_c ? a.k_cmp : dummy, crow, kStageKeys);
+  if (e == cudaSuccess) e = tma::encode_rows128(&maps.vc, has_c ? a.v_cmp : dummy, crow, kStageKeys);
   if (e != cudaSuccess) return e;
   if (a.H <= 64) return launch_tc<64>(a, maps, st);
   return launch_tc<128>(a, maps, st);

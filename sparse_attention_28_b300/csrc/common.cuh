@@ -90,6 +90,13 @@ __device__ __forceinline__ uint32_t score_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// 2^x by the special-function unit (PTX ex2.approx.ftz: relative error about
+// 2^-22, subnormal results flushed to zero, 2^-inf = +0).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
 __device__ __forceinline__ int lane_id() { return threadIdx.x & 31; }
 
 }  // namespace csa
