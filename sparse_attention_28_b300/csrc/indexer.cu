@@ -7,23 +7,29 @@
 // DeepSeek Sparse Attention"), read as
 //     I(t,s) = sum_h w[t][h] * ReLU(q[t][h] . k[s]),  s < n_vis(t).
 //
-// Pipeline per call (queries processed in chunks that keep the score buffer
-// near L2 size):
-//   1. memset of the per-query histogram + candidate counter,
-//   2. score kernel: streams the compressed indexer keys once (the dominant
-//      HBM traffic), computes the 4-head scores with m16n8k16 tensor-core
-//      MMAs (entries on M, heads on N), writes fp32 scores and a 4096-bin
-//      histogram of the top 12 bits of each score's order-preserving key,
-//   3. mark kernel (several CTAs per query): from the histogram finds the
-//      threshold bin B*; sets a bitmap bit for every entry above B* and
-//      appends the entries of bin B* to a candidate list,
-//   4. select kernel (one CTA per query): exact k-th key among the
-//      candidates (ties to the lower index), then writes the selected entries
-//      in ascending index order from the bitmap.
+// Per call (queries in chunks that bound the workspace):
+//   1. memset of the per-query score histograms,
+//   2. score kernel, one CTA per (2048-entry chunk, query): streams the
+//      compressed indexer keys once (the dominant HBM traffic), computes the
+//      4-head scores with tensor-core MMAs (entries on M, heads on N), writes
+//      fp32 scores and adds a 4096-bin histogram of the top 12 bits of each
+//      score's order-preserving key to the query's histogram,
+//   3. select kernel, one thread-block cluster of up to 16 CTAs per query,
+//      each holding a slice of 8, 16 or 32 entries per thread of the scores
+//      in shared memory (one bulk copy): every CTA finds the threshold bin B*
+//      (the bin of the k-th largest key) from the histogram, then two radix
+//      levels over the B* keys (bits 19..10, 9..0) -- counts pushed into
+//      every cluster CTA with remote atomics, one cluster barrier per level
+//      -- give the exact k-th key k*; one more exchange of the per-CTA counts
+//      of keys above k* and equal to k* gives each CTA its output offset and
+//      how many ties at k* it takes (lowest indices first); each thread then
+//      writes the indices of its consecutive entries in order.
 // Bins, keys and the tie rule give the same set as a full sort on
 // (-score, index).
 #include "common.cuh"
 #include "kernels.h"
+#include "tc.cuh"
+#include "tma.cuh"
 
 namespace csa {
 
@@ -31,39 +37,31 @@ namespace {
 
 constexpr int kDI = 64;
 constexpr int kHI = 4;
-constexpr int kScoreThreads = 256;
-constexpr int kChunk = 2048;       // entries per score CTA
-constexpr int kUnroll = 4;         // 16-entry groups in flight per warp
-constexpr int kMarkThreads = 256;
-constexpr int kMarkSlice = 8192;   // entries per mark CTA
-constexpr int kMarkUnroll = 8;     // 32-entry words per warp per run
-constexpr int kSelThreads = 512;
-constexpr int kQueryChunk = 256;   // queries per pass (bounds the workspace)
-constexpr int kHdrWords = kHistBins + 32;  // hist[4096], cand counter, pad
+constexpr int kThreads = 256;     // score kernel
+constexpr int kChunk = 2048;      // entries per score CTA
+constexpr int kUnroll = 4;        // 16-entry groups in flight per warp
+constexpr int kQueryChunk = 256;  // queries per launch (bounds the workspace)
+constexpr int kHdrWords = kHistBins + 32;
+constexpr int kSelThreads = 1024;
+constexpr int kMaxCluster = 16;  // select CTAs per query
+static_assert(kMaxNcap <= kMaxCluster * kSelThreads * 32, "select cluster");
 
 struct WsLayout {
-  float* scores;      // [QC][N_cap]
-  int32_t* hdr;       // [QC][kHdrWords]
-  uint32_t* bitmap;   // [QC][bm_stride]
-  uint2* cand;        // [QC][kCandCap] (key, index)
-  int bm_stride;
+  float* scores;  // [QC][stride]
+  int32_t* hdr;   // [QC][kHdrWords]: score histogram
+  int stride;     // N_cap rounded up to 32 entries (128-byte aligned rows)
 };
 
-__host__ __device__ inline int bitmap_words(int n_cap) { return ((n_cap + 31) / 32 + 3) & ~3; }
-
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+int score_stride(int n_cap) { return (n_cap + 31) & ~31; }
 
 WsLayout carve(void* ws, int qc, int n_cap) {
   WsLayout L;
   uint8_t* p = reinterpret_cast<uint8_t*>(ws);
+  L.stride = score_stride(n_cap);
   L.scores = reinterpret_cast<float*>(p);
-  p += align256((size_t)qc * n_cap * sizeof(float));
+  p += align256((size_t)qc * L.stride * sizeof(float));
   L.hdr = reinterpret_cast<int32_t*>(p);
-  p += align256((size_t)qc * kHdrWords * sizeof(int32_t));
-  L.bm_stride = bitmap_words(n_cap);
-  L.bitmap = reinterpret_cast<uint32_t*>(p);
-  p += align256((size_t)qc * L.bm_stride * sizeof(uint32_t));
-  L.cand = reinterpret_cast<uint2*>(p);
   return L;
 }
 
@@ -79,134 +77,6 @@ __device__ __forceinline__ int64_t visible_entries(const IndexerArgs& a, int qid
   }
   const int64_t nv = (t + 1) / a.m;
   return nv < present ? nv : present;
-}
-
-// ------------------------------------------------------------------ scores
-// Fragment mapping (m16n8k16, A = 16 entries x 16 dims, B = 16 dims x 8
-// heads, heads 4..7 are zero).  The contraction order over the 64 dims is
-// free, so each thread loads whole 16-byte vectors of a key row and the query
-// fragments use the same permutation:
-//   bf16: thread (g, c) holds row bytes [16c,16c+16) and [64+16c, 64+16c+16);
-//         k-step s takes word s of each vector.
-//   E4M3: thread (g, c) holds row bytes [16c, 16c+16) converted to 8 f16x2
-//         words (exact); k-step s takes words s and 4+s.
-template <bool FP8>
-__global__ void __launch_bounds__(kScoreThreads) indexer_score_kernel(IndexerArgs a, int q0,
-                                                                     WsLayout L) {
-  __shared__ int hist_s[kHistBins];
-  const int qid = q0 + blockIdx.y;
-  const int lq = blockIdx.y;
-  const int64_t nv = visible_entries(a, qid, a.err, blockIdx.x == 0 && threadIdx.x == 0);
-  const int64_t e0 = (int64_t)blockIdx.x * kChunk;
-  if (e0 >= nv) return;
-  const int64_t e1 = (e0 + kChunk < nv) ? e0 + kChunk : nv;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g = lane >> 2, c = lane & 3;
-  for (int i = tid; i < kHistBins; i += kScoreThreads) hist_s[i] = 0;
-
-  // query fragments (heads g < 4) and head weights (heads 2c, 2c+1 for c < 2)
-  uint32_t qb0[4] = {0, 0, 0, 0}, qb1[4] = {0, 0, 0, 0};
-  float w0 = 0.f, w1 = 0.f;
-  if (g < kHI) {
-    if (FP8) {
-      const uint8_t* qr = reinterpret_cast<const uint8_t*>(a.q) + ((int64_t)qid * kHI + g) * kDI;
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(qr + 16 * c));
-      const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        const uint32_t lo = e4m3x2_to_f16x2((uint16_t)(wv[s >> 1] >> ((s & 1) * 16)));
-        const uint32_t hi = e4m3x2_to_f16x2((uint16_t)(wv[2 + (s >> 1)] >> ((s & 1) * 16)));
-        qb0[s] = lo;
-        qb1[s] = hi;
-      }
-    } else {
-      const bf16* qr = reinterpret_cast<const bf16*>(a.q) + ((int64_t)qid * kHI + g) * kDI;
-      const uint4 v0 = __ldg(reinterpret_cast<const uint4*>(qr + 8 * c));
-      const uint4 v1 = __ldg(reinterpret_cast<const uint4*>(qr + 32 + 8 * c));
-      qb0[0] = v0.x; qb0[1] = v0.y; qb0[2] = v0.z; qb0[3] = v0.w;
-      qb1[0] = v1.x; qb1[1] = v1.y; qb1[2] = v1.z; qb1[3] = v1.w;
-    }
-  }
-  if (c < 2) {
-    w0 = __ldg(a.w + (int64_t)qid * kHI + 2 * c);
-    w1 = __ldg(a.w + (int64_t)qid * kHI + 2 * c + 1);
-    if (FP8) {
-      w0 *= __ldg(a.q_scale + (int64_t)qid * kHI + 2 * c);
-      w1 *= __ldg(a.q_scale + (int64_t)qid * kHI + 2 * c + 1);
-    }
-  }
-  __syncthreads();
-
-  const int b = qid / a.T;
-  float* scores = L.scores + (int64_t)lq * a.N_cap;
-  const int n_groups = (int)((e1 - e0 + 15) / 16);
-  for (int gb = warp * kUnroll; gb < n_groups; gb += (kScoreThreads / 32) * kUnroll) {
-    uint4 ra[kUnroll][2], rb[kUnroll][2];  // rows g and g+8 of each group
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int64_t ea = e0 + (int64_t)(gb + u) * 16 + g, eb = ea + 8;
-      if (FP8) {
-        const uint8_t* kb = reinterpret_cast<const uint8_t*>(a.keys) + (int64_t)b * a.k_bstride;
-        ra[u][0] = ea < e1 ? __ldg(reinterpret_cast<const uint4*>(kb + ea * kDI + 16 * c))
-                           : make_uint4(0, 0, 0, 0);
-        rb[u][0] = eb < e1 ? __ldg(reinterpret_cast<const uint4*>(kb + eb * kDI + 16 * c))
-                           : make_uint4(0, 0, 0, 0);
-      } else {
-        const bf16* kb = reinterpret_cast<const bf16*>(a.keys) + (int64_t)b * a.k_bstride;
-        const uint4 z = make_uint4(0, 0, 0, 0);
-        ra[u][0] = ea < e1 ? __ldg(reinterpret_cast<const uint4*>(kb + ea * kDI + 8 * c)) : z;
-        ra[u][1] = ea < e1 ? __ldg(reinterpret_cast<const uint4*>(kb + ea * kDI + 32 + 8 * c)) : z;
-        rb[u][0] = eb < e1 ? __ldg(reinterpret_cast<const uint4*>(kb + eb * kDI + 8 * c)) : z;
-        rb[u][1] = eb < e1 ? __ldg(reinterpret_cast<const uint4*>(kb + eb * kDI + 32 + 8 * c)) : z;
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      if (gb + u >= n_groups) break;
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      if (FP8) {
-        const uint32_t xa[4] = {ra[u][0].x, ra[u][0].y, ra[u][0].z, ra[u][0].w};
-        const uint32_t xb[4] = {rb[u][0].x, rb[u][0].y, rb[u][0].z, rb[u][0].w};
-#pragma unroll
-        for (int s = 0; s < 4; ++s) {
-          uint32_t af[4];
-          af[0] = e4m3x2_to_f16x2((uint16_t)(xa[s >> 1] >> ((s & 1) * 16)));
-          af[1] = e4m3x2_to_f16x2((uint16_t)(xb[s >> 1] >> ((s & 1) * 16)));
-          af[2] = e4m3x2_to_f16x2((uint16_t)(xa[2 + (s >> 1)] >> ((s & 1) * 16)));
-          af[3] = e4m3x2_to_f16x2((uint16_t)(xb[2 + (s >> 1)] >> ((s & 1) * 16)));
-          mma_f16_16816(acc, af, qb0[s], qb1[s]);
-        }
-      } else {
-        const uint32_t xa0[4] = {ra[u][0].x, ra[u][0].y, ra[u][0].z, ra[u][0].w};
-        const uint32_t xa1[4] = {ra[u][1].x, ra[u][1].y, ra[u][1].z, ra[u][1].w};
-        const uint32_t xb0[4] = {rb[u][0].x, rb[u][0].y, rb[u][0].z, rb[u][0].w};
-        const uint32_t xb1[4] = {rb[u][1].x, rb[u][1].y, rb[u][1].z, rb[u][1].w};
-#pragma unroll
-        for (int s = 0; s < 4; ++s) {
-          const uint32_t af[4] = {xa0[s], xb0[s], xa1[s], xb1[s]};
-          mma_bf16_16816(acc, af, qb0[s], qb1[s]);
-        }
-      }
-      // epilogue: weighted ReLU over heads 2c, 2c+1, then over the 4 heads
-      float sa = w0 * fmaxf(acc[0], 0.f) + w1 * fmaxf(acc[1], 0.f);
-      float sb = w0 * fmaxf(acc[2], 0.f) + w1 * fmaxf(acc[3], 0.f);
-      sa += __shfl_xor_sync(0xFFFFFFFFu, sa, 1);
-      sb += __shfl_xor_sync(0xFFFFFFFFu, sb, 1);
-      const int64_t e = e0 + (int64_t)(gb + u) * 16 + g + (c == 1 ? 8 : 0);
-      float sc = c == 1 ? sb : sa;
-      if (c < 2 && e < e1) {
-        if (FP8) sc *= __ldg(a.k_scale + (int64_t)b * a.ks_bstride + e);
-        scores[e] = sc;
-        atomicAdd(&hist_s[score_key(sc) >> 20], 1);
-      }
-    }
-  }
-  __syncthreads();
-  int32_t* hist = L.hdr + (int64_t)lq * kHdrWords;
-  for (int i = tid; i < kHistBins; i += kScoreThreads) {
-    const int v = hist_s[i];
-    if (v) atomicAdd(hist + i, v);
-  }
 }
 
 // ------------------------------------------------------------------ block helpers
@@ -237,312 +107,390 @@ __device__ __forceinline__ int block_excl_scan(int v, int* scratch, int* total) 
   return before + x - v;
 }
 
-// Threshold bin: the highest bin B such that the count of keys in bins > B
-// is < k <= count in bins >= B.  Returns B, the count above it, its count.
-template <int NT>
-__device__ void find_threshold_bin(const int32_t* hist, int k, int* scratch, int* res) {
-  constexpr int per = kHistBins / NT;
-  const int tid = threadIdx.x;
-  // thread tid owns bins [kHistBins - (tid+1)*per, kHistBins - tid*per): high bins first
-  const int hi = kHistBins - tid * per;
+// Thread t of NT holds `cnt` = the count of its bins; bins are split evenly
+// and thread 0 owns the highest ones (`bins` = the thread's bins, highest
+// first).  res[0] = the bin holding the need-th largest key, res[1] = the
+// count in the bins above it.
+template <int NT, int PER>
+__device__ void bin_from_top(const int (&bins)[PER], int first_bin, int need, int* scratch,
+                             int* res) {
   int local = 0;
-  for (int i = 1; i <= per; ++i) local += hist[hi - i];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) local += bins[i];
   int total;
-  const int before = block_excl_scan<NT>(local, scratch, &total);  // count in higher bins
-  if (before < k && before + local >= k) {
+  const int before = block_excl_scan<NT>(local, scratch, &total);
+  if (before < need && before + local >= need) {
     int run = before;
-    for (int i = 1; i <= per; ++i) {
-      const int bin = hi - i, cnt = hist[bin];
-      if (run + cnt >= k) {
-        res[0] = bin;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      if (run + bins[i] >= need) {
+        res[0] = first_bin - i;
         res[1] = run;
-        res[2] = cnt;
         break;
       }
-      run += cnt;
+      run += bins[i];
     }
   }
   __syncthreads();
 }
 
-// ------------------------------------------------------------------ mark
-// grid (slices, queries): bitmap bits for keys above the threshold bin; the
-// keys in it are gathered in shared memory and appended to the query's
-// candidate list with one global atomic per CTA.
-__global__ void __launch_bounds__(kMarkThreads) topk_mark_kernel(IndexerArgs a, int q0,
-                                                                 WsLayout L) {
-  extern __shared__ __align__(16) uint2 lcand[];  // [kMarkSlice]
-  __shared__ int scratch[32];
-  __shared__ int res[3];
-  __shared__ int n_local, g_base;
-  const int qid = q0 + blockIdx.y, lq = blockIdx.y;
-  const int64_t nv = visible_entries(a, qid, nullptr, false);
-  const int64_t s0 = (int64_t)blockIdx.x * kMarkSlice;
-  if (nv <= a.k || s0 >= nv) return;
-  if (threadIdx.x == 0) n_local = 0;
-  const int32_t* hist = L.hdr + (int64_t)lq * kHdrWords;
-  find_threshold_bin<kMarkThreads>(hist, a.k, scratch, res);
-  const uint32_t bstar = (uint32_t)res[0];
-  const float* scores = L.scores + (int64_t)lq * a.N_cap;
-  uint32_t* bm = L.bitmap + (int64_t)lq * L.bm_stride;
-  int32_t* counter = L.hdr + (int64_t)lq * kHdrWords + kHistBins;
-  uint2* cand = L.cand + (int64_t)lq * kCandCap;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t s1 = (s0 + kMarkSlice < nv) ? s0 + kMarkSlice : nv;
-  // each warp takes runs of kMarkUnroll * 32 consecutive entries; all loads of
-  // a run are issued before any is used
-  for (int64_t run = s0 + (int64_t)warp * kMarkUnroll * 32; run < s1;
-       run += (int64_t)kMarkThreads * kMarkUnroll) {
-    uint32_t key[kMarkUnroll];
+// ------------------------------------------------------------------ scores
+// Fragment mapping: 16 entries on M, heads on N (heads 4..7 zero).  The
+// contraction order over the 64 dims is free, so each thread loads whole
+// 16-byte vectors of a key row and the query fragments use the same
+// permutation:
+//   bf16 (m16n8k16): thread (g, c) holds row bytes [16c,16c+16) and
+//         [64+16c, 64+16c+16); k-step s takes word s of each vector.
+//   E4M3 (m16n8k32, products exact in fp32): thread (g, c) holds row bytes
+//         [16c, 16c+16); k-step s takes words 2s and 2s+1.
+template <bool FP8>
+__global__ void __launch_bounds__(kThreads) indexer_score_kernel(IndexerArgs a, int q0,
+                                                                WsLayout L) {
+  __shared__ int hist_s[kHistBins];
+  const int lq = blockIdx.y, qid = q0 + lq;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, c = lane & 3;
+  const int64_t nv = visible_entries(a, qid, a.err, blockIdx.x == 0 && tid == 0);
+  const int64_t e0 = (int64_t)blockIdx.x * kChunk;
+  if (e0 >= nv) return;
+  const int64_t e1 = (e0 + kChunk < nv) ? e0 + kChunk : nv;
+  for (int i = tid; i < kHistBins; i += kThreads) hist_s[i] = 0;
+
+  // query fragments (heads g < 4) and head weights (heads 2c, 2c+1 for c < 2)
+  uint32_t qb0[4] = {0, 0, 0, 0}, qb1[4] = {0, 0, 0, 0};
+  float w0 = 0.f, w1 = 0.f;
+  if (g < kHI) {
+    if (FP8) {
+      const uint8_t* qr = reinterpret_cast<const uint8_t*>(a.q) + ((int64_t)qid * kHI + g) * kDI;
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(qr + 16 * c));
+      qb0[0] = v.x; qb0[1] = v.y; qb0[2] = v.z; qb0[3] = v.w;
+    } else {
+      const bf16* qr = reinterpret_cast<const bf16*>(a.q) + ((int64_t)qid * kHI + g) * kDI;
+      const uint4 v0 = __ldg(reinterpret_cast<const uint4*>(qr + 8 * c));
+      const uint4 v1 = __ldg(reinterpret_cast<const uint4*>(qr + 32 + 8 * c));
+      qb0[0] = v0.x; qb0[1] = v0.y; qb0[2] = v0.z; qb0[3] = v0.w;
+      qb1[0] = v1.x; qb1[1] = v1.y; qb1[2] = v1.z; qb1[3] = v1.w;
+    }
+  }
+  if (c < 2) {
+    w0 = __ldg(a.w + (int64_t)qid * kHI + 2 * c);
+    w1 = __ldg(a.w + (int64_t)qid * kHI + 2 * c + 1);
+    if (FP8) {
+      w0 *= __ldg(a.q_scale + (int64_t)qid * kHI + 2 * c);
+      w1 *= __ldg(a.q_scale + (int64_t)qid * kHI + 2 * c + 1);
+    }
+  }
+  __syncthreads();
+
+  const int b = qid / a.T;
+  float* scores = L.scores + (int64_t)lq * L.stride;
+  const int n_groups = (int)((e1 - e0 + 15) / 16);
+  for (int gb = warp * kUnroll; gb < n_groups; gb += (kThreads / 32) * kUnroll) {
+    uint4 ra[kUnroll][2], rb[kUnroll][2];  // rows g and g+8 of each group
+    float ks[kUnroll];                      // E4M3: scale of the entry this thread scores
 #pragma unroll
-    for (int u = 0; u < kMarkUnroll; ++u) {
-      const int64_t i = run + u * 32 + lane;
-      key[u] = i < s1 ? score_key(scores[i]) : 0u;
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t ea = e0 + (int64_t)(gb + u) * 16 + g, eb = ea + 8;
+      if (FP8) {
+        const int64_t es = c == 1 ? eb : ea;
+        ks[u] = (c < 2 && es < e1) ? __ldg(a.k_scale + (int64_t)b * a.ks_bstride + es) : 0.f;
+        const uint8_t* kb = reinterpret_cast<const uint8_t*>(a.keys) + (int64_t)b * a.k_bstride;
+        ra[u][0] = ea < e1 ? __ldg(reinterpret_cast<const uint4*>(kb + ea * kDI + 16 * c))
+                           : make_uint4(0, 0, 0, 0);
+        rb[u][0] = eb < e1 ? __ldg(reinterpret_cast<const uint4*>(kb + eb * kDI + 16 * c))
+                           : make_uint4(0, 0, 0, 0);
+      } else {
+        const bf16* kb = reinterpret_cast<const bf16*>(a.keys) + (int64_t)b * a.k_bstride;
+        const uint4 z = make_uint4(0, 0, 0, 0);
+        ra[u][0] = ea < e1 ? __ldg(reinterpret_cast<const uint4*>(kb + ea * kDI + 8 * c)) : z;
+        ra[u][1] = ea < e1 ? __ldg(reinterpret_cast<const uint4*>(kb + ea * kDI + 32 + 8 * c)) : z;
+        rb[u][0] = eb < e1 ? __ldg(reinterpret_cast<const uint4*>(kb + eb * kDI + 8 * c)) : z;
+        rb[u][1] = eb < e1 ? __ldg(reinterpret_cast<const uint4*>(kb + eb * kDI + 32 + 8 * c)) : z;
+      }
     }
 #pragma unroll
-    for (int u = 0; u < kMarkUnroll; ++u) {
-      const int64_t base = run + u * 32;
-      if (base >= s1) break;
-      const bool in = base + lane < s1;
-      const uint32_t bin = key[u] >> 20;
-      const unsigned above = __ballot_sync(0xFFFFFFFFu, in && bin > bstar);
-      const unsigned at = __ballot_sync(0xFFFFFFFFu, in && bin == bstar);
-      if (lane == 0) bm[base >> 5] = above;
-      if (at) {
-        int slot0 = 0;
-        if (lane == 0) slot0 = atomicAdd(&n_local, __popc(at));
-        slot0 = __shfl_sync(0xFFFFFFFFu, slot0, 0);
-        if ((at >> lane) & 1u)
-          lcand[slot0 + __popc(at & ((1u << lane) - 1u))] = make_uint2(key[u], (uint32_t)(base + lane));
+    for (int u = 0; u < kUnroll; ++u) {
+      if (gb + u >= n_groups) break;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      if (FP8) {
+        const uint32_t a0[4] = {ra[u][0].x, rb[u][0].x, ra[u][0].y, rb[u][0].y};
+        const uint32_t a1[4] = {ra[u][0].z, rb[u][0].z, ra[u][0].w, rb[u][0].w};
+        mma_e4m3_16832(acc, a0, qb0[0], qb0[1]);
+        mma_e4m3_16832(acc, a1, qb0[2], qb0[3]);
+      } else {
+        const uint32_t xa0[4] = {ra[u][0].x, ra[u][0].y, ra[u][0].z, ra[u][0].w};
+        const uint32_t xa1[4] = {ra[u][1].x, ra[u][1].y, ra[u][1].z, ra[u][1].w};
+        const uint32_t xb0[4] = {rb[u][0].x, rb[u][0].y, rb[u][0].z, rb[u][0].w};
+        const uint32_t xb1[4] = {rb[u][1].x, rb[u][1].y, rb[u][1].z, rb[u][1].w};
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+          const uint32_t af[4] = {xa0[s], xb0[s], xa1[s], xb1[s]};
+          mma_bf16_16816(acc, af, qb0[s], qb1[s]);
+        }
+      }
+      // epilogue: weighted ReLU over heads 2c, 2c+1, then over the 4 heads
+      float sa = w0 * fmaxf(acc[0], 0.f) + w1 * fmaxf(acc[1], 0.f);
+      float sb = w0 * fmaxf(acc[2], 0.f) + w1 * fmaxf(acc[3], 0.f);
+      sa += __shfl_xor_sync(0xFFFFFFFFu, sa, 1);
+      sb += __shfl_xor_sync(0xFFFFFFFFu, sb, 1);
+      const int64_t e = e0 + (int64_t)(gb + u) * 16 + g + (c == 1 ? 8 : 0);
+      float sc = c == 1 ? sb : sa;
+      if (c < 2 && e < e1) {
+        if (FP8) sc *= ks[u];
+        scores[e] = sc;
+        atomicAdd(&hist_s[score_key(sc) >> 20], 1);
       }
     }
   }
   __syncthreads();
-  const int n = n_local;
-  if (n == 0) return;
-  if (threadIdx.x == 0) g_base = atomicAdd(counter, n);
-  __syncthreads();
-  const int gb = g_base;
-  for (int i = threadIdx.x; i < n; i += kMarkThreads)
-    if (gb + i < kCandCap) cand[gb + i] = lcand[i];
+  int32_t* hdr = L.hdr + (int64_t)lq * kHdrWords;
+  for (int i = tid; i < kHistBins; i += kThreads) {
+    const int v = hist_s[i];
+    if (v) atomicAdd(hdr + i, v);
+  }
 }
 
 // ------------------------------------------------------------------ select
-// One CTA per query.  Dynamic shared memory: bitmap[nw] | eqmap[nw] | hist[1024].
-// The exact k-th key inside the threshold bin comes from two 10-bit radix
-// passes over the bin's candidate list (or, if it overflowed, over all
-// scores); ties at that key go to the lowest indices.
-constexpr int kSelUnroll = 8;
-
-template <bool FromCand>
-__device__ __forceinline__ void radix_pass(const uint2* cand, const float* scores, int64_t n,
-                                           uint32_t pmask, uint32_t prefix, int shift, int* h) {
-  for (int64_t i0 = threadIdx.x; i0 < n; i0 += (int64_t)kSelThreads * kSelUnroll) {
-    uint32_t key[kSelUnroll];
-#pragma unroll
-    for (int u = 0; u < kSelUnroll; ++u) {
-      const int64_t i = i0 + (int64_t)u * kSelThreads;
-      key[u] = i < n ? (FromCand ? __ldcg(&cand[i].x) : score_key(__ldcg(scores + i))) : 0u;
-    }
-#pragma unroll
-    for (int u = 0; u < kSelUnroll; ++u) {
-      const int64_t i = i0 + (int64_t)u * kSelThreads;
-      if (i < n && (key[u] & pmask) == prefix) atomicAdd(&h[(key[u] >> shift) & 1023], 1);
-    }
-  }
+struct SelShared {
+  uint64_t bar;
+  int scratch[32];
+  int res[3];
+  uint32_t t2[1024];          // cluster totals, key bits 19..10 of the B* keys
+  uint32_t t3[1024];          // key bits 9..0 under the chosen 19..10 bin
+  uint32_t loc[1024];         // this CTA's counts of the current level
+  uint32_t above[kMaxCluster];  // per CTA of the cluster: keys above k*
+  uint32_t equal[kMaxCluster];  // and equal to k*
+};
+constexpr int sel_smem_bytes(int per_thread) {
+  return (int)((sizeof(SelShared) + 127) / 128 * 128) + kSelThreads * per_thread * 4;
 }
 
-__global__ void __launch_bounds__(kSelThreads) topk_select_kernel(IndexerArgs a, int q0,
-                                                                  WsLayout L) {
-  extern __shared__ __align__(16) uint8_t sm[];
-  __shared__ int scratch[32];
-  __shared__ int res[3];
-  __shared__ uint32_t sel_key;
-  __shared__ int sel_need;
-  const int qid = q0 + blockIdx.x, lq = blockIdx.x;
+// this CTA's counts of one level, added into `tot` of every CTA in the cluster
+__device__ __forceinline__ void push_level(const uint32_t* loc, uint32_t* tot, int cs) {
+  const uint32_t v = loc[threadIdx.x];
+  if (!v) return;
+  const uint32_t la = smem_u32(&tot[threadIdx.x]);
+  for (int q = 0; q < cs; ++q) tc::red_cluster_add_u32(tc::map_shared(la, q), v);
+}
+
+// grid (C, queries), cluster (C, 1, 1); CTA r holds the E*1024 entries from
+// r*E*1024.  Thread t owns the E consecutive entries [E t, E t + E) of the
+// slice, read as 16-byte vectors in a rotated order; bit b of its masks is
+// entry E t + b.
+template <int E>
+__global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(IndexerArgs a, int q0,
+                                                                     WsLayout L) {
+  constexpr int V = E / 4;             // 16-byte vectors per thread
+  constexpr int kSlice = kSelThreads * E;
+  extern __shared__ __align__(128) uint8_t sel_smem[];
+  SelShared* sh = reinterpret_cast<SelShared*>(sel_smem);
+  float* sc = reinterpret_cast<float*>(sel_smem + (sizeof(SelShared) + 127) / 128 * 128);
   const int tid = threadIdx.x;
+  const int cs = gridDim.x, r = blockIdx.x;
+  const int lq = blockIdx.y, qid = q0 + lq;
   const int64_t nv = visible_entries(a, qid, nullptr, false);
   int32_t* out = a.topk_idx + (int64_t)qid * a.k;
   float* out_s = a.topk_score ? a.topk_score + (int64_t)qid * a.k : nullptr;
-  const float* scores = L.scores + (int64_t)lq * a.N_cap;
+  const float* scores = L.scores + (int64_t)lq * L.stride;
+  const int64_t s0 = (int64_t)r * kSlice;
+  const int n_slice = nv > s0 ? (int)(nv - s0 < kSlice ? nv - s0 : kSlice) : 0;
 
-  if (nv <= a.k) {  // every visible entry is selected
-    for (int64_t r = tid; r < a.k; r += kSelThreads) {
-      out[r] = r < nv ? (int32_t)r : -1;
-      if (out_s) out_s[r] = r < nv ? scores[r] : -INFINITY;
+  if (nv <= a.k) {  // every visible entry is selected (the same branch in every CTA)
+    for (int64_t i = s0 + tid; i < s0 + kSlice && i < a.k; i += kSelThreads) {
+      out[i] = i < nv ? (int32_t)i : -1;
+      if (out_s) out_s[i] = i < nv ? scores[i] : -INFINITY;
     }
     return;
   }
-
-  const int nw = (int)((nv + 31) / 32);
-  uint32_t* bitmap = reinterpret_cast<uint32_t*>(sm);
-  uint32_t* eqmap = bitmap + L.bm_stride;
-  int* h = reinterpret_cast<int*>(eqmap + L.bm_stride);
-
-  const int32_t* hist = L.hdr + (int64_t)lq * kHdrWords;
-  find_threshold_bin<kSelThreads>(hist, a.k, scratch, res);
-  const uint32_t bstar = (uint32_t)res[0];
-  const int c_above = res[1], c_bin = res[2];
-  const int n_cand_written = hist[kHistBins];
-  const uint32_t* bm_g = L.bitmap + (int64_t)lq * L.bm_stride;
-  for (int i = tid; i < nw; i += kSelThreads) {
-    bitmap[i] = bm_g[i];
-    eqmap[i] = 0u;
-  }
-  const bool fast = c_bin <= kCandCap && n_cand_written == c_bin;
-  const uint2* cand = L.cand + (int64_t)lq * kCandCap;
-  int need = a.k - c_above;  // to take from the threshold bin, >= 1
-
-  // ---- exact key within the bin: two 10-bit radix passes (bits 19..10, 9..0)
-  uint32_t prefix = bstar << 20;
-  for (int pass = 0; pass < 2; ++pass) {
-    const int shift = pass == 0 ? 10 : 0;
-    const uint32_t pmask = pass == 0 ? 0xFFF00000u : 0xFFFFFC00u;
-    for (int i = tid; i < 1024; i += kSelThreads) h[i] = 0;
-    __syncthreads();
-    if (fast)
-      radix_pass<true>(cand, scores, c_bin, pmask, prefix, shift, h);
-    else
-      radix_pass<false>(cand, scores, nv, pmask, prefix, shift, h);
-    __syncthreads();
-    {
-      constexpr int per = 1024 / kSelThreads;
-      const int hi = 1024 - tid * per;
-      int local = 0;
-      for (int i = 1; i <= per; ++i) local += h[hi - i];
-      int total;
-      const int before = block_excl_scan<kSelThreads>(local, scratch, &total);
-      if (before < need && before + local >= need) {
-        int run = before;
-        for (int i = 1; i <= per; ++i) {
-          const int bin = hi - i, cnt = h[bin];
-          if (run + cnt >= need) {
-            res[0] = bin;
-            res[1] = run;
-            break;
-          }
-          run += cnt;
-        }
-      }
-      __syncthreads();
-      prefix |= (uint32_t)res[0] << shift;
-      need -= res[1];
-      __syncthreads();
-    }
-  }
+  // the slice's scores: one bulk copy of whole 16-byte chunks, the tail below
+  const int bulk = (n_slice * 4) & ~15;
   if (tid == 0) {
-    sel_key = prefix;
-    sel_need = need;  // how many entries with key == sel_key to take (lowest indices)
+    tc::mbar_init(&sh->bar, 1);
+    tc::fence_mbar_init();
+    if (bulk > 0) {
+      tma::expect_tx(&sh->bar, (uint32_t)bulk);
+      tma::bulk_load(smem_u32(sc), scores + s0, (uint32_t)bulk, &sh->bar);
+    } else {
+      tc::mbar_arrive(&sh->bar);
+    }
   }
+  for (int i = tid; i < 1024; i += kSelThreads) {
+    sh->t2[i] = 0u;
+    sh->t3[i] = 0u;
+    sh->loc[i] = 0u;
+  }
+  for (int i = bulk / 4 + tid; i < n_slice; i += kSelThreads) sc[i] = scores[s0 + i];
   __syncthreads();
-  const uint32_t kstar = sel_key;
-  const int need_eq = sel_need;
+  tc::cluster_arrive();  // the totals are zeroed before any CTA adds into them
 
-  // ---- mark the threshold-bin entries: above kstar -> bitmap, equal -> eqmap
-  if (fast) {
-    for (int i = tid; i < c_bin; i += kSelThreads) {
-      const uint2 ce = __ldcg(&cand[i]);
-      if (ce.x > kstar) atomicOr(&bitmap[ce.y >> 5], 1u << (ce.y & 31));
-      else if (ce.x == kstar) atomicOr(&eqmap[ce.y >> 5], 1u << (ce.y & 31));
-    }
-  } else {
-    for (int64_t i0 = tid; i0 < nv; i0 += (int64_t)kSelThreads * kSelUnroll) {
-      uint32_t key[kSelUnroll];
-#pragma unroll
-      for (int u = 0; u < kSelUnroll; ++u) {
-        const int64_t i = i0 + (int64_t)u * kSelThreads;
-        key[u] = i < nv ? score_key(__ldcg(scores + i)) : 0u;
-      }
-#pragma unroll
-      for (int u = 0; u < kSelUnroll; ++u) {
-        const int64_t i = i0 + (int64_t)u * kSelThreads;
-        if (i >= nv || (key[u] >> 20) != bstar) continue;
-        if (key[u] > kstar) atomicOr(&bitmap[i >> 5], 1u << (i & 31));
-        else if (key[u] == kstar) atomicOr(&eqmap[i >> 5], 1u << (i & 31));
-      }
-    }
+  // ---- threshold bin B* from the query's 4096-bin histogram
+  const int32_t* hist = L.hdr + (int64_t)lq * kHdrWords;
+  {
+    const int4 v = __ldcg(reinterpret_cast<const int4*>(hist) + (kHistBins / 4 - 1 - tid));
+    const int bins[4] = {v.w, v.z, v.y, v.x};  // highest first
+    bin_from_top<kSelThreads, 4>(bins, kHistBins - 1 - 4 * tid, a.k, sh->scratch, sh->res);
   }
+  const uint32_t bstar = (uint32_t)sh->res[0];
+  int need = a.k - sh->res[1];
+  if (!tc::mbar_wait(&sh->bar, 0, 1u << 24) && tid == 0) flag_error(a.err, CSA_EW_TIMEOUT);
+
+  // this thread's keys (key 0, below every score, past the slice) and the
+  // entry bit of each register slot
+  uint32_t kk[E];
+  int bitpos[V];
+#pragma unroll
+  for (int q = 0; q < V; ++q) {
+    const int vq = (q + tid) % V;  // rotated vector order: fewer bank conflicts
+    bitpos[q] = 4 * vq;
+    const float4 f = reinterpret_cast<const float4*>(sc)[tid * V + vq];
+    const int e = E * tid + 4 * vq;
+    kk[4 * q + 0] = e + 0 < n_slice ? score_key(f.x) : 0u;
+    kk[4 * q + 1] = e + 1 < n_slice ? score_key(f.y) : 0u;
+    kk[4 * q + 2] = e + 2 < n_slice ? score_key(f.z) : 0u;
+    kk[4 * q + 3] = e + 3 < n_slice ? score_key(f.w) : 0u;
+  }
+  // (a valid key is never 0: the score_key of any finite float is positive)
+
+  // ---- level 2: key bits 19..10 of the B* keys
+#pragma unroll
+  for (int i = 0; i < E; ++i)
+    if (kk[i] && (kk[i] >> 20) == bstar) atomicAdd(&sh->loc[(kk[i] >> 10) & 1023], 1u);
+  __syncthreads();
+  tc::cluster_wait();
+  push_level(sh->loc, sh->t2, cs);
+  tc::cluster_sync();
+  {
+    const int bins[1] = {(int)sh->t2[1023 - tid]};
+    bin_from_top<kSelThreads, 1>(bins, 1023 - tid, need, sh->scratch, sh->res);
+  }
+  const uint32_t p2 = (bstar << 10) | (uint32_t)sh->res[0];
+  need -= sh->res[1];
+  sh->loc[tid] = 0u;
   __syncthreads();
 
-  // ---- ordered emission: thread tid owns words [tid*R, tid*R + R)
-  const int R = (nw + kSelThreads - 1) / kSelThreads;
-  const int w0 = tid * R, w1 = (w0 + R < nw) ? w0 + R : nw;
-  int eqc = 0;
-  for (int w = w0; w < w1; ++w) eqc += __popc(eqmap[w]);
-  int total;
-  int eq_run = block_excl_scan<kSelThreads>(eqc, scratch, &total);
-  int selc = 0;
-  for (int w = w0; w < w1; ++w) {
-    uint32_t e = eqmap[w];
-    uint32_t take = 0;
-    while (e && eq_run < need_eq) {
-      const uint32_t low = e & (~e + 1u);
-      take |= low;
-      e ^= low;
-      ++eq_run;
-    }
-    const uint32_t fin = bitmap[w] | take;
-    bitmap[w] = fin;
-    selc += __popc(fin);
+  // ---- level 3: key bits 9..0 under (B*, level-2 bin)
+#pragma unroll
+  for (int i = 0; i < E; ++i)
+    if (kk[i] && (kk[i] >> 10) == p2) atomicAdd(&sh->loc[kk[i] & 1023], 1u);
+  __syncthreads();
+  push_level(sh->loc, sh->t3, cs);
+  tc::cluster_sync();
+  {
+    const int bins[1] = {(int)sh->t3[1023 - tid]};
+    bin_from_top<kSelThreads, 1>(bins, 1023 - tid, need, sh->scratch, sh->res);
   }
-  int pos = block_excl_scan<kSelThreads>(selc, scratch, &total);
-  for (int w = w0; w < w1; ++w) {
-    uint32_t fin = bitmap[w];
-    while (fin) {
-      const int bit = __ffs(fin) - 1;
-      fin &= fin - 1;
-      const int64_t i = (int64_t)w * 32 + bit;
-      if (pos < a.k) {
-        out[pos] = (int32_t)i;
-        if (out_s) out_s[pos] = scores[i];
-      }
-      ++pos;
+  const uint32_t kstar = (p2 << 10) | (uint32_t)sh->res[0];
+  const int need_eq = need - sh->res[1];  // entries equal to k* to take, lowest index first
+
+  // ---- keys above / equal to k*; counts in index order by block scans
+  uint32_t above_bits = 0u, eq_bits = 0u;
+#pragma unroll
+  for (int q = 0; q < V; ++q)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint32_t k1 = kk[4 * q + c];
+      above_bits |= (uint32_t)(k1 && k1 > kstar) << (bitpos[q] + c);
+      eq_bits |= (uint32_t)(k1 && k1 == kstar) << (bitpos[q] + c);
     }
+  int tot_above, tot_eq;
+  const int above_before = block_excl_scan<kSelThreads>(__popc(above_bits), sh->scratch, &tot_above);
+  const int eq_before = block_excl_scan<kSelThreads>(__popc(eq_bits), sh->scratch, &tot_eq);
+  if (tid < cs) {
+    tc::st_cluster_u32(tc::map_shared(smem_u32(&sh->above[r]), tid), (uint32_t)tot_above);
+    tc::st_cluster_u32(tc::map_shared(smem_u32(&sh->equal[r]), tid), (uint32_t)tot_eq);
   }
-  if (tid == 0 && total != a.k) flag_error(a.err, CSA_EW_BAD_INDEX);  // internal invariant
-  for (int r = total + tid; r < a.k; r += kSelThreads) {
-    out[r] = -1;
-    if (out_s) out_s[r] = -INFINITY;
+  tc::cluster_sync();
+  // ties go to the lowest indices: the lower ranks' equal keys come first
+  int off = 0, eq_lower = 0;
+  for (int q = 0; q < r; ++q) {
+    const int take_q = min(max(need_eq - eq_lower, 0), (int)sh->equal[q]);
+    off += (int)sh->above[q] + take_q;
+    eq_lower += (int)sh->equal[q];
+  }
+  const int take_cta = min(max(need_eq - eq_lower, 0), tot_eq);
+  if (r == cs - 1 && tid == 0 && off + tot_above + take_cta != a.k)
+    flag_error(a.err, CSA_EW_BAD_INDEX);  // internal invariant
+  // this thread's ties taken: the lowest ones, up to what the CTA takes
+  int take = min(max(take_cta - eq_before, 0), __popc(eq_bits));
+  uint32_t sel = above_bits;
+  for (uint32_t e = eq_bits; e && take > 0; --take) {
+    const uint32_t low = e & (~e + 1u);
+    sel |= low;
+    e ^= low;
+  }
+  int pos = off + above_before + min(max(take_cta, 0), eq_before);
+  while (sel) {
+    const int b = __ffs(sel) - 1;
+    sel &= sel - 1;
+    if (pos < a.k) {
+      const int e = E * tid + b;
+      out[pos] = (int32_t)(s0 + e);
+      if (out_s) out_s[pos] = sc[e];
+    }
+    ++pos;
   }
 }
-
-int select_smem_bytes(int n_cap) { return 2 * bitmap_words(n_cap) * 4 + 1024 * 4; }
 
 }  // namespace
 
 size_t indexer_topk_workspace_bytes(int n_query, int N_cap) {
   const int qc = n_query < kQueryChunk ? n_query : kQueryChunk;
-  return align256((size_t)qc * N_cap * sizeof(float)) +
-         align256((size_t)qc * kHdrWords * sizeof(int32_t)) +
-         align256((size_t)qc * bitmap_words(N_cap) * sizeof(uint32_t)) +
-         align256((size_t)qc * kCandCap * sizeof(uint2));
+  return align256((size_t)qc * score_stride(N_cap) * sizeof(float)) +
+         align256((size_t)qc * kHdrWords * sizeof(int32_t));
 }
 
 cudaError_t launch_indexer_topk(const IndexerArgs& a, void* ws, cudaStream_t st) {
   const int qc_max = a.n_query < kQueryChunk ? a.n_query : kQueryChunk;
   WsLayout L = carve(ws, qc_max, a.N_cap);
-  const int sel_smem = select_smem_bytes(a.N_cap);
-  cudaError_t e = ensure_smem_attr((const void*)topk_select_kernel, select_smem_bytes(kMaxNcap));
-  if (e != cudaSuccess) return e;
-  e = ensure_smem_attr((const void*)topk_mark_kernel, kMarkSlice * sizeof(uint2));
-  if (e != cudaSuccess) return e;
+  // entries per select thread: the smallest of 8, 16, 32 with at most
+  // kMaxCluster CTAs per query
+  const int per = a.N_cap <= kMaxCluster * kSelThreads * 8    ? 8
+                  : a.N_cap <= kMaxCluster * kSelThreads * 16 ? 16
+                                                              : 32;
+  const int cs = (a.N_cap + kSelThreads * per - 1) / (kSelThreads * per);
+  const void* sel_fn = per == 8    ? (const void*)topk_select_kernel<8>
+                       : per == 16 ? (const void*)topk_select_kernel<16>
+                                   : (const void*)topk_select_kernel<32>;
+  {
+    static bool attrs[3] = {false, false, false};
+    const int ix = per == 8 ? 0 : (per == 16 ? 1 : 2);
+    if (!attrs[ix]) {
+      cudaError_t e = ensure_smem_attr(sel_fn, sel_smem_bytes(per));
+      if (e != cudaSuccess) return e;
+      e = cudaFuncSetAttribute(sel_fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+      attrs[ix] = true;
+    }
+  }
   for (int q0 = 0; q0 < a.n_query; q0 += kQueryChunk) {
     const int qc = (a.n_query - q0 < kQueryChunk) ? a.n_query - q0 : kQueryChunk;
-    e = cudaMemsetAsync(L.hdr, 0, (size_t)qc * kHdrWords * sizeof(int32_t), st);
+    cudaError_t e = cudaMemsetAsync(L.hdr, 0, (size_t)qc * kHdrWords * sizeof(int32_t), st);
     if (e != cudaSuccess) return e;
     dim3 g1((a.N_cap + kChunk - 1) / kChunk, qc);
     if (a.fp8)
-      indexer_score_kernel<true><<<g1, kScoreThreads, 0, st>>>(a, q0, L);
+      indexer_score_kernel<true><<<g1, kThreads, 0, st>>>(a, q0, L);
     else
-      indexer_score_kernel<false><<<g1, kScoreThreads, 0, st>>>(a, q0, L);
+      indexer_score_kernel<false><<<g1, kThreads, 0, st>>>(a, q0, L);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    dim3 g2((a.N_cap + kMarkSlice - 1) / kMarkSlice, qc);
-    topk_mark_kernel<<<g2, kMarkThreads, kMarkSlice * sizeof(uint2), st>>>(a, q0, L);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    topk_select_kernel<<<qc, kSelThreads, sel_smem, st>>>(a, q0, L);
-    e = cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)cs, (unsigned)qc);
+    cfg.blockDim = dim3(kSelThreads);
+    cfg.dynamicSmemBytes = sel_smem_bytes(per);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (per == 8)
+      e = cudaLaunchKernelEx(&cfg, topk_select_kernel<8>, a, q0, L);
+    else if (per == 16)
+      e = cudaLaunchKernelEx(&cfg, topk_select_kernel<16>, a, q0, L);
+    else
+      e = cudaLaunchKernelEx(&cfg, topk_select_kernel<32>, a, q0, L);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

@@ -57,7 +57,6 @@ cudaError_t launch_attention(AttnArgs a, void* ws, cudaStream_t st);
 
 // ---------------------------------------------------------------- indexer + top-k
 constexpr int kHistBins = 4096;  // top 12 bits of the order-preserving score key
-constexpr int kCandCap = 32768;  // candidates of the threshold bin kept per query
 constexpr int kMaxNcap = 1 << 19;
 
 struct IndexerArgs {

@@ -34,6 +34,17 @@ __device__ __forceinline__ void load_box(uint32_t dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// contiguous bytes (a multiple of 16, both addresses 16-byte aligned)
+// global -> shared, completion through the mbarrier's transaction count
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::
+          "r"(dst),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // four rows (each 64 columns from col) -> four consecutive 128-byte rows at dst
 __device__ __forceinline__ void gather4(uint32_t dst, const CUtensorMap* map, int col, int r0,
                                         int r1, int r2, int r3, uint64_t* bar) {

@@ -103,7 +103,7 @@ def _oracle_indexer(qi, qs, ki, ks, w, qp, nc, m, k, fp8):
 
 
 @pytest.mark.parametrize("fp8", [False, True])
-@pytest.mark.parametrize("T", [1, 5])
+@pytest.mark.parametrize("T", [1, 5, 12])  # up to 8 tokens per sequence: fused path
 def test_indexer_topk_parity(cuda_device, fp8, T):
     B, N_cap, m, k = 3, 3000, 4, 200
     n_cmp = [3000, 2100, 150]
@@ -123,10 +123,13 @@ def test_indexer_topk_parity(cuda_device, fp8, T):
             assert np.all(np.isneginf(sc[b, t, take:]))
 
 
-def test_topk_ties_take_lowest_indices(cuda_device):
-    # identical keys: every score ties, so the k lowest indices win; 20000
-    # entries in one histogram bin overflow the candidate list (slow path)
-    B, N_cap, m, k = 2, 20000, 4, 300
+@pytest.mark.parametrize("N_cap,k", [(20000, 300), (200000, 5000)])
+def test_topk_ties_take_lowest_indices(cuda_device, N_cap, k):
+    # identical keys: every score ties, so the k lowest indices win, and they
+    # come from the lowest-ranked CTAs of the select cluster; at 200000
+    # entries one CTA's slice holds more threshold-bin entries than it keeps
+    # in shared memory (the passes re-read the scores)
+    B, m = 2, 4
     qi = synth.randn((B, 1, 4, 64), 3, 1)
     ki = synth.randn((1, 1, 64), 3, 2).expand(B, N_cap, 64).contiguous()
     w = torch.ones((B, 1, 4))
