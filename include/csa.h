@@ -149,16 +149,17 @@ CSA_API int csa_indexer_topk(const void* q_idx, const float* q_scale, const floa
  * Arguments, layouts, ownership and results are those of csa_indexer_topk,
  * without ws / ws_bytes.
  *   Limit: csa_indexer_topk_workspace(B, T, N_cap, k) must not exceed
- *   CSA_INDEXER_STATIC_SCRATCH_BYTES (16 MiB: e.g. 32 queries over 32768
- *   compressed entries, or 8 over 262144); a larger problem returns
- *   CSA_ERR_WORKSPACE before anything runs.
+ *   CSA_INDEXER_STATIC_SCRATCH_BYTES (16 MiB).  The workspace is one fp32
+ *   score per compressed entry for up to 256 queries at a time, so this covers
+ *   any number of queries over 16384 entries, 32 queries over 131072, or 8 over
+ *   524288; a larger problem returns CSA_ERR_WORKSPACE before anything runs.
  *   Set-up: the first call on a device (the device current on the calling
  *   thread) looks up the array's device address (cudaGetSymbolAddress) and
  *   caches it; that lookup can load the library's kernels, so make the first
  *   call per device before any stream capture.  A failed lookup returns
  *   CSA_ERR_CUDA.
- *   Zeroing: nothing in the array has to start at zero; each call clears the
- *   counters it uses (an asynchronous memset on `stream`) before its kernels.
+ *   Zeroing: nothing in the array has to start at zero; each call writes
+ *   every score it later reads, before reading it, on `stream`.
  *   Overlap: all calls on one device share the one array.  Calls ordered on
  *   one stream are safe; two calls that can run at the same time (different
  *   streams without an event between them, or several host threads) race on

@@ -11,11 +11,11 @@
 // scale = max_c |y| / 448 (1 if all zero), code = nearest-even E4M3 of
 // y / scale, saturating.
 //
-// One CTA per (block, sequence), one thread per output channel.  W (bf16,
-// rows padded by 16 bytes so that 8 consecutive rows cover all banks) and the
-// block's m raw rows (fp32) are staged in shared memory with coalesced loads;
-// each thread forms its channel's m gate logits 16 positions at a time (its
-// W row from shared memory, x rows as broadcasts) and folds them into an
+// One CTA per (block, sequence), one thread per output channel.  The
+// block's m raw rows (fp32) are staged in shared memory; each thread reads
+// its own W row straight from global memory (all of it in flight at once:
+// no other thread uses it) and forms its channel's m gate logits 16
+// positions at a time (x rows as shared-memory broadcasts), folded into an
 // online softmax.
 #include "common.cuh"
 #include "kernels.h"
@@ -27,27 +27,18 @@ namespace {
 constexpr int kPosChunk = 16;
 
 template <int D>
-constexpr int w_stride_bytes() { return D * 2 + 16; }
-
-template <int D>
 __global__ void __launch_bounds__(D) compress_kernel(CompressArgs a) {
-  extern __shared__ __align__(16) uint8_t csm[];
-  uint8_t* ws = csm;                                                  // [D][D + 8] bf16
-  float* xs = reinterpret_cast<float*>(csm + D * w_stride_bytes<D>());  // [m][D]
+  extern __shared__ __align__(16) float xs[];  // [m][D]
   __shared__ float red[D / 32];
-  {
-    constexpr int chunks = D * D / 8;  // 16-byte pieces of W
-#pragma unroll 4
-    for (int i = threadIdx.x; i < chunks; i += D) {
-      const int r = i / (D / 8), c8 = i % (D / 8);
-      *reinterpret_cast<uint4*>(ws + r * w_stride_bytes<D>() + c8 * 16) =
-          __ldg(reinterpret_cast<const uint4*>(a.W) + i);
-    }
-  }
   const int c = threadIdx.x;
   const int b = blockIdx.y;
   const int64_t j = (int64_t)a.block_begin + blockIdx.x;
   const int m = a.m;
+  // this channel's W row: D bf16 as D/8 16-byte vectors
+  uint4 wrow[D / 8];
+#pragma unroll
+  for (int e8 = 0; e8 < D / 8; ++e8)
+    wrow[e8] = __ldg(reinterpret_cast<const uint4*>(a.W + (int64_t)c * D) + e8);
   const bf16* xb = a.raw + (int64_t)b * a.raw_bstride;
   const int64_t r0 = (j * m) % a.raw_cap;  // ring row of the block's first token
   for (int i = 0; i < m; ++i) {
@@ -57,16 +48,15 @@ __global__ void __launch_bounds__(D) compress_kernel(CompressArgs a) {
   }
   __syncthreads();
 
-  const uint8_t* wr = ws + c * w_stride_bytes<D>();
   float mx = -INFINITY, den = 0.f, num = 0.f;
   for (int i0 = 0; i0 < m; i0 += kPosChunk) {
     const int n = (m - i0 < kPosChunk) ? m - i0 : kPosChunk;
     float gl[kPosChunk];
 #pragma unroll
     for (int ii = 0; ii < kPosChunk; ++ii) gl[ii] = 0.f;
-    for (int e = 0; e < D; e += 8) {
-      const uint4 wv = *reinterpret_cast<const uint4*>(wr + e * 2);
-      const __nv_bfloat162* w2 = reinterpret_cast<const __nv_bfloat162*>(&wv);
+#pragma unroll
+    for (int e8 = 0; e8 < D / 8; ++e8) {
+      const __nv_bfloat162* w2 = reinterpret_cast<const __nv_bfloat162*>(&wrow[e8]);
       float wf[8];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -77,7 +67,7 @@ __global__ void __launch_bounds__(D) compress_kernel(CompressArgs a) {
 #pragma unroll
       for (int ii = 0; ii < kPosChunk; ++ii) {
         if (ii < n) {
-          const float* xr = xs + (i0 + ii) * D + e;
+          const float* xr = xs + (i0 + ii) * D + e8 * 8;
 #pragma unroll
           for (int q = 0; q < 8; ++q) gl[ii] = fmaf(wf[q], xr[q], gl[ii]);
         }
@@ -130,16 +120,13 @@ cudaError_t launch_compress(const CompressArgs& a, cudaStream_t st) {
   dim3 grid(a.n_blocks, a.B);
   cudaError_t e;
   if (a.d == 128) {
-    const int smem = 128 * w_stride_bytes<128>() + a.m * 128 * 4;
-    e = ensure_smem_attr((const void*)compress_kernel<128>,
-                         128 * w_stride_bytes<128>() + 256 * 128 * 4);
+    e = ensure_smem_attr((const void*)compress_kernel<128>, 256 * 128 * 4);
     if (e != cudaSuccess) return e;
-    compress_kernel<128><<<grid, 128, smem, st>>>(a);
+    compress_kernel<128><<<grid, 128, a.m * 128 * 4, st>>>(a);
   } else {
-    const int smem = 64 * w_stride_bytes<64>() + a.m * 64 * 4;
-    e = ensure_smem_attr((const void*)compress_kernel<64>, 64 * w_stride_bytes<64>() + 256 * 64 * 4);
+    e = ensure_smem_attr((const void*)compress_kernel<64>, 256 * 64 * 4);
     if (e != cudaSuccess) return e;
-    compress_kernel<64><<<grid, 64, smem, st>>>(a);
+    compress_kernel<64><<<grid, 64, a.m * 64 * 4, st>>>(a);
   }
   return cudaGetLastError();
 }

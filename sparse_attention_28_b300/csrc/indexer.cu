@@ -8,19 +8,19 @@
 //     I(t,s) = sum_h w[t][h] * ReLU(q[t][h] . k[s]),  s < n_vis(t).
 //
 // Per call (queries in chunks that bound the workspace):
-//   1. memset of the per-query score histograms,
-//   2. score kernel, one CTA per (2048-entry chunk, query): streams the
-//      compressed indexer keys once (the dominant HBM traffic), computes the
-//      4-head scores with tensor-core MMAs (entries on M, heads on N), writes
-//      fp32 scores and adds a 4096-bin histogram of the top 12 bits of each
-//      score's order-preserving key to the query's histogram,
-//   3. select kernel, one thread-block cluster of up to 16 CTAs per query,
+//   1. scores: for a few tokens per sequence (decode) a kernel with one CTA
+//      per (2048-entry chunk, query) streams the compressed indexer keys once
+//      (the dominant HBM traffic) and computes the 4-head scores with
+//      tensor-core MMAs (entries on M, heads on N); for many tokens per
+//      sequence (prefill) the scores are one tcgen05 GEMM (indexer_gemm.cu);
+//      either way fp32 scores land in the workspace,
+//   2. select kernel, one thread-block cluster of up to 16 CTAs per query,
 //      each holding a slice of 8, 16 or 32 entries per thread of the scores
-//      in shared memory (one bulk copy): every CTA finds the threshold bin B*
-//      (the bin of the k-th largest key) from the histogram, then two radix
-//      levels over the B* keys (bits 19..10, 9..0) -- counts pushed into
-//      every cluster CTA with remote atomics, one cluster barrier per level
-//      -- give the exact k-th key k*; one more exchange of the per-CTA counts
+//      in shared memory (one bulk copy): three radix levels over the
+//      order-preserving score keys (bits 31..20, then 19..10 and 9..0 of the
+//      keys in the chosen bins) -- counts pushed into every cluster CTA with
+//      remote atomics, one cluster barrier per level -- give the exact k-th
+//      key k*; one more exchange of the per-CTA counts
 //      of keys above k* and equal to k* gives each CTA its output offset and
 //      how many ties at k* it takes (lowest indices first); each thread then
 //      writes the indices of its consecutive entries in order.
@@ -39,29 +39,25 @@ constexpr int kDI = 64;
 constexpr int kHI = 4;
 constexpr int kThreads = 256;     // score kernel
 constexpr int kChunk = 2048;      // entries per score CTA
-constexpr int kUnroll = 4;        // 16-entry groups in flight per warp
+constexpr int kUnrollBf16 = 4;    // 16-entry groups in flight per warp (bf16 keys)
+constexpr int kUnrollFp8 = 8;     // (E4M3 keys: half the bytes per row)
 constexpr int kQueryChunk = 256;  // queries per launch (bounds the workspace)
-constexpr int kHdrWords = kHistBins + 32;
 constexpr int kSelThreads = 1024;
 constexpr int kMaxCluster = 16;  // select CTAs per query
 static_assert(kMaxNcap <= kMaxCluster * kSelThreads * 32, "select cluster");
 
 struct WsLayout {
   float* scores;  // [QC][stride]
-  int32_t* hdr;   // [QC][kHdrWords]: score histogram
   int stride;     // N_cap rounded up to 32 entries (128-byte aligned rows)
 };
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 int score_stride(int n_cap) { return (n_cap + 31) & ~31; }
 
-WsLayout carve(void* ws, int qc, int n_cap) {
+WsLayout carve(void* ws, int n_cap) {
   WsLayout L;
-  uint8_t* p = reinterpret_cast<uint8_t*>(ws);
   L.stride = score_stride(n_cap);
-  L.scores = reinterpret_cast<float*>(p);
-  p += align256((size_t)qc * L.stride * sizeof(float));
-  L.hdr = reinterpret_cast<int32_t*>(p);
+  L.scores = reinterpret_cast<float*>(ws);
   return L;
 }
 
@@ -146,7 +142,6 @@ __device__ void bin_from_top(const int (&bins)[PER], int first_bin, int need, in
 template <bool FP8>
 __global__ void __launch_bounds__(kThreads) indexer_score_kernel(IndexerArgs a, int q0,
                                                                 WsLayout L) {
-  __shared__ int hist_s[kHistBins];
   const int lq = blockIdx.y, qid = q0 + lq;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, c = lane & 3;
@@ -154,7 +149,6 @@ __global__ void __launch_bounds__(kThreads) indexer_score_kernel(IndexerArgs a, 
   const int64_t e0 = (int64_t)blockIdx.x * kChunk;
   if (e0 >= nv) return;
   const int64_t e1 = (e0 + kChunk < nv) ? e0 + kChunk : nv;
-  for (int i = tid; i < kHistBins; i += kThreads) hist_s[i] = 0;
 
   // query fragments (heads g < 4) and head weights (heads 2c, 2c+1 for c < 2)
   uint32_t qb0[4] = {0, 0, 0, 0}, qb1[4] = {0, 0, 0, 0};
@@ -184,6 +178,7 @@ __global__ void __launch_bounds__(kThreads) indexer_score_kernel(IndexerArgs a, 
 
   const int b = qid / a.T;
   float* scores = L.scores + (int64_t)lq * L.stride;
+  constexpr int kUnroll = FP8 ? kUnrollFp8 : kUnrollBf16;
   const int n_groups = (int)((e1 - e0 + 15) / 16);
   for (int gb = warp * kUnroll; gb < n_groups; gb += (kThreads / 32) * kUnroll) {
     uint4 ra[kUnroll][2], rb[kUnroll][2];  // rows g and g+8 of each group
@@ -238,15 +233,8 @@ __global__ void __launch_bounds__(kThreads) indexer_score_kernel(IndexerArgs a, 
       if (c < 2 && e < e1) {
         if (FP8) sc *= ks[u];
         scores[e] = sc;
-        atomicAdd(&hist_s[score_key(sc) >> 20], 1);
       }
     }
-  }
-  __syncthreads();
-  int32_t* hdr = L.hdr + (int64_t)lq * kHdrWords;
-  for (int i = tid; i < kHistBins; i += kThreads) {
-    const int v = hist_s[i];
-    if (v) atomicAdd(hdr + i, v);
   }
 }
 
@@ -255,9 +243,10 @@ struct SelShared {
   uint64_t bar;
   int scratch[32];
   int res[3];
-  uint32_t t2[1024];          // cluster totals, key bits 19..10 of the B* keys
+  uint32_t t1[kHistBins];     // cluster totals, key bits 31..20
+  uint32_t t2[1024];          // key bits 19..10 of the keys in the chosen bin
   uint32_t t3[1024];          // key bits 9..0 under the chosen 19..10 bin
-  uint32_t loc[1024];         // this CTA's counts of the current level
+  uint32_t loc[kHistBins];    // this CTA's counts of the current level
   uint32_t above[kMaxCluster];  // per CTA of the cluster: keys above k*
   uint32_t equal[kMaxCluster];  // and equal to k*
 };
@@ -266,11 +255,13 @@ constexpr int sel_smem_bytes(int per_thread) {
 }
 
 // this CTA's counts of one level, added into `tot` of every CTA in the cluster
-__device__ __forceinline__ void push_level(const uint32_t* loc, uint32_t* tot, int cs) {
-  const uint32_t v = loc[threadIdx.x];
-  if (!v) return;
-  const uint32_t la = smem_u32(&tot[threadIdx.x]);
-  for (int q = 0; q < cs; ++q) tc::red_cluster_add_u32(tc::map_shared(la, q), v);
+__device__ __forceinline__ void push_level(const uint32_t* loc, uint32_t* tot, int nb, int cs) {
+  for (int bin = threadIdx.x; bin < nb; bin += kSelThreads) {
+    const uint32_t v = loc[bin];
+    if (!v) continue;
+    const uint32_t la = smem_u32(&tot[bin]);
+    for (int q = 0; q < cs; ++q) tc::red_cluster_add_u32(tc::map_shared(la, q), v);
+  }
 }
 
 // grid (C, queries), cluster (C, 1, 1); CTA r holds the E*1024 entries from
@@ -314,24 +305,18 @@ __global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(IndexerArgs
       tc::mbar_arrive(&sh->bar);
     }
   }
-  for (int i = tid; i < 1024; i += kSelThreads) {
-    sh->t2[i] = 0u;
-    sh->t3[i] = 0u;
+  for (int i = tid; i < kHistBins; i += kSelThreads) {
+    sh->t1[i] = 0u;
     sh->loc[i] = 0u;
+    if (i < 1024) {
+      sh->t2[i] = 0u;
+      sh->t3[i] = 0u;
+    }
   }
   for (int i = bulk / 4 + tid; i < n_slice; i += kSelThreads) sc[i] = scores[s0 + i];
   __syncthreads();
   tc::cluster_arrive();  // the totals are zeroed before any CTA adds into them
 
-  // ---- threshold bin B* from the query's 4096-bin histogram
-  const int32_t* hist = L.hdr + (int64_t)lq * kHdrWords;
-  {
-    const int4 v = __ldcg(reinterpret_cast<const int4*>(hist) + (kHistBins / 4 - 1 - tid));
-    const int bins[4] = {v.w, v.z, v.y, v.x};  // highest first
-    bin_from_top<kSelThreads, 4>(bins, kHistBins - 1 - 4 * tid, a.k, sh->scratch, sh->res);
-  }
-  const uint32_t bstar = (uint32_t)sh->res[0];
-  int need = a.k - sh->res[1];
   if (!tc::mbar_wait(&sh->bar, 0, 1u << 24) && tid == 0) flag_error(a.err, CSA_EW_TIMEOUT);
 
   // this thread's keys (key 0, below every score, past the slice) and the
@@ -351,13 +336,36 @@ __global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(IndexerArgs
   }
   // (a valid key is never 0: the score_key of any finite float is positive)
 
+  // ---- level 1: key bits 31..20 (lanes that hit the same bin add once)
+#pragma unroll
+  for (int i = 0; i < E; ++i) {
+    const unsigned act = __ballot_sync(0xFFFFFFFFu, kk[i] != 0u);
+    if (kk[i]) {
+      const uint32_t bin = kk[i] >> 20;
+      const unsigned same = __match_any_sync(act, bin);
+      if ((tid & 31) == __ffs(same) - 1) atomicAdd(&sh->loc[bin], (uint32_t)__popc(same));
+    }
+  }
+  __syncthreads();
+  tc::cluster_wait();
+  push_level(sh->loc, sh->t1, kHistBins, cs);
+  tc::cluster_sync();
+  {
+    const int bins[4] = {(int)sh->t1[kHistBins - 1 - 4 * tid], (int)sh->t1[kHistBins - 2 - 4 * tid],
+                         (int)sh->t1[kHistBins - 3 - 4 * tid], (int)sh->t1[kHistBins - 4 - 4 * tid]};
+    bin_from_top<kSelThreads, 4>(bins, kHistBins - 1 - 4 * tid, a.k, sh->scratch, sh->res);
+  }
+  const uint32_t bstar = (uint32_t)sh->res[0];
+  int need = a.k - sh->res[1];
+  sh->loc[tid] = 0u;  // levels 2 and 3 use the first 1024 counters
+  __syncthreads();
+
   // ---- level 2: key bits 19..10 of the B* keys
 #pragma unroll
   for (int i = 0; i < E; ++i)
     if (kk[i] && (kk[i] >> 20) == bstar) atomicAdd(&sh->loc[(kk[i] >> 10) & 1023], 1u);
   __syncthreads();
-  tc::cluster_wait();
-  push_level(sh->loc, sh->t2, cs);
+  push_level(sh->loc, sh->t2, 1024, cs);
   tc::cluster_sync();
   {
     const int bins[1] = {(int)sh->t2[1023 - tid]};
@@ -373,7 +381,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(IndexerArgs
   for (int i = 0; i < E; ++i)
     if (kk[i] && (kk[i] >> 10) == p2) atomicAdd(&sh->loc[kk[i] & 1023], 1u);
   __syncthreads();
-  push_level(sh->loc, sh->t3, cs);
+  push_level(sh->loc, sh->t3, 1024, cs);
   tc::cluster_sync();
   {
     const int bins[1] = {(int)sh->t3[1023 - tid]};
@@ -435,13 +443,11 @@ __global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(IndexerArgs
 
 size_t indexer_topk_workspace_bytes(int n_query, int N_cap) {
   const int qc = n_query < kQueryChunk ? n_query : kQueryChunk;
-  return align256((size_t)qc * score_stride(N_cap) * sizeof(float)) +
-         align256((size_t)qc * kHdrWords * sizeof(int32_t));
+  return align256((size_t)qc * score_stride(N_cap) * sizeof(float));
 }
 
 cudaError_t launch_indexer_topk(const IndexerArgs& a, void* ws, cudaStream_t st) {
-  const int qc_max = a.n_query < kQueryChunk ? a.n_query : kQueryChunk;
-  WsLayout L = carve(ws, qc_max, a.N_cap);
+  WsLayout L = carve(ws, a.N_cap);
   // entries per select thread: the smallest of 8, 16, 32 with at most
   // kMaxCluster CTAs per query
   const int per = a.N_cap <= kMaxCluster * kSelThreads * 8    ? 8
@@ -462,16 +468,21 @@ cudaError_t launch_indexer_topk(const IndexerArgs& a, void* ws, cudaStream_t st)
       attrs[ix] = true;
     }
   }
+  // many tokens per sequence: scores as one tensor-core GEMM per chunk
+  const bool gemm = a.T > 8 && indexer_gemm_applies(a);
   for (int q0 = 0; q0 < a.n_query; q0 += kQueryChunk) {
     const int qc = (a.n_query - q0 < kQueryChunk) ? a.n_query - q0 : kQueryChunk;
-    cudaError_t e = cudaMemsetAsync(L.hdr, 0, (size_t)qc * kHdrWords * sizeof(int32_t), st);
-    if (e != cudaSuccess) return e;
-    dim3 g1((a.N_cap + kChunk - 1) / kChunk, qc);
-    if (a.fp8)
-      indexer_score_kernel<true><<<g1, kThreads, 0, st>>>(a, q0, L);
-    else
-      indexer_score_kernel<false><<<g1, kThreads, 0, st>>>(a, q0, L);
-    e = cudaGetLastError();
+    cudaError_t e;
+    if (gemm) {
+      e = launch_indexer_gemm(a, q0, qc, L.scores, L.stride, st);
+    } else {
+      dim3 g1((a.N_cap + kChunk - 1) / kChunk, qc);
+      if (a.fp8)
+        indexer_score_kernel<true><<<g1, kThreads, 0, st>>>(a, q0, L);
+      else
+        indexer_score_kernel<false><<<g1, kThreads, 0, st>>>(a, q0, L);
+      e = cudaGetLastError();
+    }
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)cs, (unsigned)qc);

@@ -83,6 +83,11 @@ struct IndexerArgs {
 
 size_t indexer_topk_workspace_bytes(int n_query, int N_cap);
 cudaError_t launch_indexer_topk(const IndexerArgs& a, void* ws, cudaStream_t st);
+// tensor-core scorer for many bf16 query tokens per sequence (T a multiple of
+// 64): scores of queries [q0, q0 + qc) into scores[(q - q0) * stride + entry]
+bool indexer_gemm_applies(const IndexerArgs& a);
+cudaError_t launch_indexer_gemm(const IndexerArgs& a, int q0, int qc, float* scores, int stride,
+                                cudaStream_t st);
 
 // ---------------------------------------------------------------- compression
 struct CompressArgs {

@@ -13,6 +13,11 @@ std::once_flag g_once;
 }  // namespace
 
 cudaError_t encode_rows128(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows) {
+  return encode_rows(map, base, 128, rows, box_rows);
+}
+
+cudaError_t encode_rows(CUtensorMap* map, const void* base, uint32_t row_elems, uint64_t rows,
+                        uint32_t box_rows) {
   std::call_once(g_once, [] {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -23,8 +28,8 @@ cudaError_t encode_rows128(CUtensorMap* map, const void* base, uint64_t rows, ui
   });
   if (!g_encode) return cudaErrorNotSupported;
   if (rows == 0) rows = 1;
-  const cuuint64_t dims[2] = {128, rows};
-  const cuuint64_t strides[1] = {256};
+  const cuuint64_t dims[2] = {row_elems, rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)row_elems * 2};
   const cuuint32_t box[2] = {64, box_rows};
   const cuuint32_t es[2] = {1, 1};
   const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),

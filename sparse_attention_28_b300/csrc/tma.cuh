@@ -17,6 +17,9 @@ namespace tma {
 // 64 columns x box_rows rows, 128-byte swizzle (the SW128 shared layout),
 // out-of-range rows read as zeros.
 cudaError_t encode_rows128(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows);
+// The same over rows of row_elems bf16 (a multiple of 64; 16-byte aligned rows).
+cudaError_t encode_rows(CUtensorMap* map, const void* base, uint32_t row_elems, uint64_t rows,
+                        uint32_t box_rows);
 
 __device__ __forceinline__ void expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)),

@@ -37,6 +37,23 @@ def _nan(shape, dtype, device):
     return torch.full(shape, float("nan"), dtype=dtype, device=device)
 
 
+def _overlapped(step, side_fn, main_fns, join_fn):
+    """side_fn on a side stream while main_fns run on the current stream;
+    join_fn after both.  Stream-ordered, so it can be captured in a graph."""
+    cur = torch.cuda.current_stream(step.out.device)
+    side = getattr(step, "_side", None)
+    if side is None:
+        side = step._side = torch.cuda.Stream(device=step.out.device)
+    side.wait_stream(cur)
+    with torch.cuda.stream(side):
+        side_fn()
+    for fn in main_fns:
+        fn()
+    cur.wait_stream(side)
+    join_fn()
+    return step.out
+
+
 class _Step:
     """Shared by the step classes: ``stages()`` lists (name, callable) in
     order and ``out`` is the output tensor."""
@@ -116,11 +133,26 @@ class CsaDecodeStep(_Step):
         self.ws_attn = torch.empty(max(1, attn_workspace(B, 1, wl.H, wl.k + W)),
                                    dtype=torch.uint8, device=dev)
 
-    def _compress(self):
+    def _compress_kv(self):
         wl, j = self.wl, self.new_block
         compress_kv(self.k_raw, *self.gates["k"], wl.m, j, 1, self.k_cmp)
         compress_kv(self.v_raw, *self.gates["v"], wl.m, j, 1, self.v_cmp)
+
+    def _compress_idx(self):
+        wl, j = self.wl, self.new_block
         compress_kv(self.idx_raw, *self.gates["idx"], wl.m, j, 1, self.k_idx, self.k_scale)
+
+    def _compress(self):
+        self._compress_kv()
+        self._compress_idx()
+
+    def __call__(self):
+        if not self.compress:
+            return super().__call__()
+        # the K/V entries are first needed by the attention: compress them on
+        # a side stream while the indexer runs
+        return _overlapped(self, self._compress_kv, [self._compress_idx, self._index],
+                           self._attend)
 
     def _index(self):
         wl = self.wl
@@ -206,12 +238,23 @@ class CsaPrefillStep(_Step):
         self.ws_attn = torch.empty(max(1, attn_workspace(B, T, wl.H, wl.k + W)),
                                    dtype=torch.uint8, device=dev)
 
-    def _compress(self):
+    def _compress_kv(self):
         wl = self.wl
         for raw, dst, gate in ((self.k_raw, self.k_cmp, self.gates["k"]),
-                               (self.v_raw, self.v_cmp, self.gates["v"]),
-                               (self.idx_raw, self.k_idx, self.gates["idx"])):
+                               (self.v_raw, self.v_cmp, self.gates["v"])):
             compress_kv(raw, *gate, wl.m, self.block0, self.n_new, dst)
+
+    def _compress_idx(self):
+        wl = self.wl
+        compress_kv(self.idx_raw, *self.gates["idx"], wl.m, self.block0, self.n_new, self.k_idx)
+
+    def _compress(self):
+        self._compress_kv()
+        self._compress_idx()
+
+    def __call__(self):
+        return _overlapped(self, self._compress_kv, [self._compress_idx, self._index],
+                           self._attend)
 
     def _index(self):
         wl = self.wl

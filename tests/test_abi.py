@@ -76,7 +76,7 @@ def test_indexer_rejects():
     assert call(kbs=100) == 1
     assert call(N=1 << 20) == 2
     assert call() == 3  # workspace too small
-    assert L.csa_indexer_topk_workspace(2, 1, 4096, 256) > 2 * 4096 * 4
+    assert L.csa_indexer_topk_workspace(2, 1, 4096, 256) >= 2 * 4096 * 4  # one fp32 score per entry
 
 
 def test_compress_rejects():

@@ -123,6 +123,30 @@ def test_indexer_topk_parity(cuda_device, fp8, T):
             assert np.all(np.isneginf(sc[b, t, take:]))
 
 
+@pytest.mark.parametrize("B,T,N_cap,k", [(2, 64, 3000, 200), (2, 320, 3000, 256),
+                                         (1, 256, 40000, 2048)])
+def test_indexer_topk_parity_many_tokens(cuda_device, B, T, N_cap, k):
+    # whole 64-token blocks of one sequence (chunked prefill): the scores come
+    # from the tensor-core scorer; 320 tokens cross a 256-query chunk, 40000
+    # entries give each CTA several key tiles (ring and TMEM buffers wrap)
+    m = 4
+    n_cmp = [N_cap, N_cap * 2 // 5 + 7][:B]
+    q_pos = [[(n_cmp[b] * m + 2) * (t + 1) // T - 1 for t in range(T)] for b in range(B)]
+    q_pos[0][0] = 1  # sees no entry
+    case = _indexer_case(B, T, N_cap, n_cmp, q_pos, False)
+    idx, sc = _run_indexer(*case, m, k)
+    s, nv, ref = _oracle_indexer(*case, m, k, False)
+    assert nv[0, 0] == 0 and (nv < k).any() and (nv > k).any()
+    check_topk(idx, ref, s, nv, k, "indexer, many tokens")
+    for b in range(B):
+        for t in range(T):
+            take = min(k, nv[b, t])
+            got = sc[b, t, :take].astype(np.float64)
+            want = s[b, t, idx[b, t, :take]]
+            np.testing.assert_allclose(got, want, rtol=2e-5, atol=2e-4)
+            assert np.all(np.isneginf(sc[b, t, take:]))
+
+
 @pytest.mark.parametrize("N_cap,k", [(20000, 300), (200000, 5000)])
 def test_topk_ties_take_lowest_indices(cuda_device, N_cap, k):
     # identical keys: every score ties, so the k lowest indices win, and they

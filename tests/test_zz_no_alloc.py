@@ -55,12 +55,8 @@ def test_static_scratch_matches_workspace_entry_twice(cuda_device):
 
 @pytest.mark.gpu
 def test_static_scratch_refuses_oversized_problem(cuda_device):
-    inp = _case(1, 1, 64, 4, False, 13)
-    inp["q_idx"] = inp["q_idx"].expand(64, 1, 4, 64).contiguous()
-    inp["w"] = inp["w"].expand(64, 1, 4).contiguous()
-    inp["q_pos"] = inp["q_pos"].expand(64, 1).contiguous()
-    inp["n_cmp"] = inp["n_cmp"].expand(64).contiguous()
-    big = torch.zeros((64, 65536, 64), dtype=torch.bfloat16, device=DEV)
-    inp["k_idx"] = big
+    # 64 tokens of one sequence over 131072 entries: 32 MiB of scores
+    inp = _case(1, 64, 131072, 4, False, 13)
+    assert csa.indexer_topk_workspace(1, 64, 131072, 64) > csa.INDEXER_STATIC_SCRATCH_BYTES
     with pytest.raises(csa.CsaError):
         csa.indexer_topk_static(**inp, k=64)
