@@ -273,6 +273,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(IndexerArgs
                                                                      WsLayout L) {
   constexpr int V = E / 4;             // 16-byte vectors per thread
   constexpr int kSlice = kSelThreads * E;
+  constexpr int kCopies = 8;           // bulk copies the slice is split into
   extern __shared__ __align__(128) uint8_t sel_smem[];
   SelShared* sh = reinterpret_cast<SelShared*>(sel_smem);
   float* sc = reinterpret_cast<float*>(sel_smem + (sizeof(SelShared) + 127) / 128 * 128);
@@ -298,12 +299,18 @@ __global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(IndexerArgs
   if (tid == 0) {
     tc::mbar_init(&sh->bar, 1);
     tc::fence_mbar_init();
-    if (bulk > 0) {
+    if (bulk > 0)
       tma::expect_tx(&sh->bar, (uint32_t)bulk);
-      tma::bulk_load(smem_u32(sc), scores + s0, (uint32_t)bulk, &sh->bar);
-    } else {
+    else
       tc::mbar_arrive(&sh->bar);
-    }
+  }
+  __syncthreads();
+  if (tid < kCopies && bulk > 0) {  // a few copies in flight at once
+    const int piece = ((bulk / kCopies) + 15) & ~15;
+    const int b0 = tid * piece, b1 = min(bulk, b0 + piece);
+    if (b1 > b0)
+      tma::bulk_load(smem_u32(sc) + b0, reinterpret_cast<const uint8_t*>(scores + s0) + b0,
+                     (uint32_t)(b1 - b0), &sh->bar);
   }
   for (int i = tid; i < kHistBins; i += kSelThreads) {
     sh->t1[i] = 0u;
@@ -336,16 +343,10 @@ __global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(IndexerArgs
   }
   // (a valid key is never 0: the score_key of any finite float is positive)
 
-  // ---- level 1: key bits 31..20 (lanes that hit the same bin add once)
+  // ---- level 1: key bits 31..20
 #pragma unroll
-  for (int i = 0; i < E; ++i) {
-    const unsigned act = __ballot_sync(0xFFFFFFFFu, kk[i] != 0u);
-    if (kk[i]) {
-      const uint32_t bin = kk[i] >> 20;
-      const unsigned same = __match_any_sync(act, bin);
-      if ((tid & 31) == __ffs(same) - 1) atomicAdd(&sh->loc[bin], (uint32_t)__popc(same));
-    }
-  }
+  for (int i = 0; i < E; ++i)
+    if (kk[i]) atomicAdd(&sh->loc[kk[i] >> 20], 1u);
   __syncthreads();
   tc::cluster_wait();
   push_level(sh->loc, sh->t1, kHistBins, cs);
@@ -448,11 +449,11 @@ size_t indexer_topk_workspace_bytes(int n_query, int N_cap) {
 
 cudaError_t launch_indexer_topk(const IndexerArgs& a, void* ws, cudaStream_t st) {
   WsLayout L = carve(ws, a.N_cap);
-  // entries per select thread: the smallest of 8, 16, 32 with at most
-  // kMaxCluster CTAs per query
-  const int per = a.N_cap <= kMaxCluster * kSelThreads * 8    ? 8
-                  : a.N_cap <= kMaxCluster * kSelThreads * 16 ? 16
-                                                              : 32;
+  // entries per select thread: the fewest of 8, 16, 32 that need at most 8
+  // CTAs per query (clusters of 8 still fit two to a GPC), else 32
+  const int per = a.N_cap <= 8 * kSelThreads * 8    ? 8
+                  : a.N_cap <= 8 * kSelThreads * 16 ? 16
+                                                    : 32;
   const int cs = (a.N_cap + kSelThreads * per - 1) / (kSelThreads * per);
   const void* sel_fn = per == 8    ? (const void*)topk_select_kernel<8>
                        : per == 16 ? (const void*)topk_select_kernel<16>
