@@ -135,6 +135,21 @@ CSA_API int csa_indexer_topk(const void* q_idx, const float* q_scale, const floa
                      int32_t* err_word, void* stream);
 
 /* ------------------------------------------------------------------------
+ * a2 alone: the Lightning-Indexer scores I(t,s) of csa_indexer_topk (same
+ * sources, reading and arguments), written out instead of selected from.
+ *
+ *   scores    fp32 [B*T][ld] out: row b*T + t holds I(t,s) at column s for
+ *             s < n_vis(t); columns from n_vis(t) on are unspecified (they may
+ *             be written).  ld >= N_cap.
+ *   No workspace.  Errors: as csa_indexer_topk (k is not an argument here).
+ * ---------------------------------------------------------------------- */
+CSA_API int csa_indexer_scores(const void* q_idx, const float* q_scale, const float* w,
+                               const void* k_idx, int64_t k_bstride, const float* k_scale,
+                               int64_t ks_bstride, int idx_dtype, const int32_t* q_pos,
+                               const int32_t* n_cmp, int B, int T, int H_I, int d_I, int N_cap,
+                               int m, float* scores, int64_t ld, int32_t* err_word, void* stream);
+
+/* ------------------------------------------------------------------------
  * a3, without caller scratch.  An integration variant: the DeepSeek-V4 pages
  * have no counterpart to it; it computes exactly what csa_indexer_topk does.
  *

@@ -9,6 +9,7 @@ the library is missing, every call raises.
 Calls (same names as the C ABI, without the prefix where it reads better):
 
 * :func:`compress_kv`            -- csa_compress_kv
+* :func:`indexer_scores`         -- csa_indexer_scores
 * :func:`indexer_topk`           -- csa_indexer_topk
 * :func:`sparse_attn_decode`     -- csa_sparse_attn_decode
 * :func:`sparse_attn_prefill`    -- csa_sparse_attn_prefill
@@ -35,6 +36,7 @@ ABI_SYMBOLS = (
     "csa_status_str", "csa_abi_version", "csa_compress_kv", "csa_indexer_topk_workspace",
     "csa_indexer_topk", "csa_attn_workspace", "csa_sparse_attn_decode",
     "csa_sparse_attn_prefill", "hca_dense_attn_decode", "csa_indexer_topk_static",
+    "csa_indexer_scores",
 )
 
 # capacity of the library-owned scratch behind indexer_topk_static (bytes)
@@ -76,6 +78,9 @@ def lib() -> ctypes.CDLL:
             L.csa_indexer_topk_static.argtypes = [P, P, P, P, I64, P, I64, I, P, P, I, I, I, I,
                                                   I, I, I, P, P, P, P]
             L.csa_indexer_topk_static.restype = I
+            L.csa_indexer_scores.argtypes = [P, P, P, P, I64, P, I64, I, P, P, I, I, I, I, I, I,
+                                             P, I64, P, P]
+            L.csa_indexer_scores.restype = I
             L.csa_attn_workspace.argtypes = [I, I, I, I]
             L.csa_attn_workspace.restype = SZ
             L.csa_sparse_attn_decode.argtypes = [P, P, P, I64, I, P, I, P, P, I64, I64, P, I, P,
@@ -164,6 +169,44 @@ def compress_kv(raw, W, pos_bias, m: int, block_begin: int, n_blocks: int, out,
 
 
 # ---------------------------------------------------------------- a2 + a3
+
+def indexer_scores(q_idx, w, k_idx, q_pos, n_cmp, m: int, q_scale=None, k_scale=None, out=None,
+                   err_word=None):
+    """Lightning-Indexer scores I(t, s) for every query token (no selection).
+
+    Arguments as :func:`indexer_topk`.  Returns fp32 [B, T, N_cap]; column s of
+    token t is defined for s < n_vis(t) only (the rest is unspecified).
+    """
+    _cuda(q_idx, "q_idx")
+    _cuda(k_idx, "k_idx")
+    _cuda(w, "w", torch.float32)
+    _cuda(q_pos, "q_pos", torch.int32)
+    _cuda(n_cmp, "n_cmp", torch.int32)
+    fp8 = q_idx.dtype in (torch.uint8, torch.float8_e4m3fn)
+    _need(fp8 == (k_idx.dtype in (torch.uint8, torch.float8_e4m3fn)), "q/k dtypes differ")
+    if not fp8:
+        _need(q_idx.dtype == torch.bfloat16 and k_idx.dtype == torch.bfloat16, "bf16 expected")
+    _need(q_idx.is_contiguous() and w.is_contiguous() and q_pos.is_contiguous(),
+          "q_idx, w, q_pos must be contiguous")
+    B, T, H_I, d_I = q_idx.shape
+    N_cap = k_idx.shape[1]
+    if fp8:
+        _cuda(q_scale, "q_scale", torch.float32)
+        _cuda(k_scale, "k_scale", torch.float32)
+        _need(q_scale.is_contiguous() and k_scale.stride(1) == 1, "scale layout")
+    sc = out if out is not None else torch.empty((B, T, N_cap), dtype=torch.float32,
+                                                 device=q_idx.device)
+    _need(sc.dtype == torch.float32 and sc.shape[:2] == (B, T) and sc.shape[2] >= N_cap
+          and sc.stride(2) == 1 and sc.stride(1) == sc.shape[2]
+          and sc.stride(0) == T * sc.shape[2], "out: contiguous fp32 [B, T, >= N_cap]")
+    st = lib().csa_indexer_scores(
+        _p(q_idx), _p(q_scale) if fp8 else None, _p(w), _p(k_idx), _bstride(k_idx),
+        _p(k_scale) if fp8 else None, k_scale.stride(0) if fp8 else 0,
+        CSA_FP8_E4M3 if fp8 else CSA_BF16, _p(q_pos), _p(n_cmp), B, T, H_I, d_I, N_cap, m,
+        _p(sc), sc.shape[2], _p(err_word), _stream(q_idx.device))
+    _check(st, "csa_indexer_scores")
+    return sc
+
 
 def indexer_topk(q_idx, w, k_idx, q_pos, n_cmp, m: int, k: int, q_scale=None, k_scale=None,
                  return_scores: bool = False, out=None, ws=None, err_word=None):

@@ -130,25 +130,25 @@ size_t csa_indexer_topk_workspace(int B, int T, int N_cap, int k) {
   return indexer_topk_workspace_bytes(B * T, N_cap);
 }
 
-int csa_indexer_topk(const void* q_idx, const float* q_scale, const float* w, const void* k_idx,
-                     int64_t k_bstride, const float* k_scale, int64_t ks_bstride, int idx_dtype,
-                     const int32_t* q_pos, const int32_t* n_cmp, int B, int T, int H_I, int d_I,
-                     int N_cap, int m, int k, int32_t* topk_idx, float* topk_score, void* ws,
-                     size_t ws_bytes, int32_t* err_word, void* stream) {
-  if (B < 0 || T < 0 || N_cap < 0 || m <= 0 || k <= 0) return CSA_ERR_INVALID_ARG;
+namespace {
+
+// checks shared by the indexer calls (status, or -1 when the call may go on)
+int indexer_checks(const void* q_idx, const float* q_scale, const float* w, const void* k_idx,
+                   int64_t k_bstride, const float* k_scale, int64_t ks_bstride, int idx_dtype,
+                   const int32_t* q_pos, const int32_t* n_cmp, int B, int T, int H_I, int d_I,
+                   int N_cap, int m) {
+  if (B < 0 || T < 0 || N_cap < 0 || m <= 0) return CSA_ERR_INVALID_ARG;
   if (idx_dtype != CSA_BF16 && idx_dtype != CSA_FP8_E4M3) return CSA_ERR_UNSUPPORTED;
   if (H_I != 4 || d_I != 64) return CSA_ERR_UNSUPPORTED;
   if (N_cap > kMaxNcap) return CSA_ERR_UNSUPPORTED;
   if (B == 0 || T == 0) return CSA_OK;
-  if (N_cap == 0 || k > N_cap) return CSA_ERR_INVALID_ARG;
+  if (N_cap == 0) return CSA_ERR_INVALID_ARG;
   if ((int64_t)B * T > (1 << 30)) return CSA_ERR_UNSUPPORTED;
-  const bool fp8 = idx_dtype == CSA_FP8_E4M3;
-  if (!q_idx || !w || !k_idx || !q_pos || !n_cmp || !topk_idx) return CSA_ERR_INVALID_ARG;
+  if (!q_idx || !w || !k_idx || !q_pos || !n_cmp) return CSA_ERR_INVALID_ARG;
   if (!aligned16(q_idx) || !aligned16(k_idx) || !aligned4(w) || !aligned4(q_pos) ||
-      !aligned4(n_cmp) || !aligned4(topk_idx))
+      !aligned4(n_cmp))
     return CSA_ERR_INVALID_ARG;
-  if (topk_score && !aligned4(topk_score)) return CSA_ERR_INVALID_ARG;
-  if (fp8) {
+  if (idx_dtype == CSA_FP8_E4M3) {
     if (!q_scale || !k_scale || !aligned4(q_scale) || !aligned4(k_scale))
       return CSA_ERR_INVALID_ARG;
     if (k_bstride % 16 != 0 || ks_bstride < N_cap) return CSA_ERR_INVALID_ARG;
@@ -156,9 +156,15 @@ int csa_indexer_topk(const void* q_idx, const float* q_scale, const float* w, co
     return CSA_ERR_INVALID_ARG;
   }
   if (k_bstride < (int64_t)N_cap * d_I) return CSA_ERR_INVALID_ARG;
-  const size_t need = indexer_topk_workspace_bytes(B * T, N_cap);
-  if (!ws || ws_bytes < need || !aligned16(ws)) return CSA_ERR_WORKSPACE;
-  IndexerArgs a;
+  return -1;
+}
+
+IndexerArgs indexer_args(const void* q_idx, const float* q_scale, const float* w,
+                         const void* k_idx, int64_t k_bstride, const float* k_scale,
+                         int64_t ks_bstride, int idx_dtype, const int32_t* q_pos,
+                         const int32_t* n_cmp, int B, int T, int N_cap, int m, int k,
+                         int32_t* err_word) {
+  IndexerArgs a = {};
   a.q = q_idx;
   a.q_scale = q_scale;
   a.w = w;
@@ -166,7 +172,7 @@ int csa_indexer_topk(const void* q_idx, const float* q_scale, const float* w, co
   a.k_bstride = k_bstride;
   a.k_scale = k_scale;
   a.ks_bstride = ks_bstride;
-  a.fp8 = fp8;
+  a.fp8 = idx_dtype == CSA_FP8_E4M3;
   a.q_pos = q_pos;
   a.n_cmp = n_cmp;
   a.T = T;
@@ -175,6 +181,42 @@ int csa_indexer_topk(const void* q_idx, const float* q_scale, const float* w, co
   a.m = m;
   a.k = k;
   a.err = err_word;
+  return a;
+}
+
+}  // namespace
+
+int csa_indexer_scores(const void* q_idx, const float* q_scale, const float* w, const void* k_idx,
+                       int64_t k_bstride, const float* k_scale, int64_t ks_bstride, int idx_dtype,
+                       const int32_t* q_pos, const int32_t* n_cmp, int B, int T, int H_I, int d_I,
+                       int N_cap, int m, float* scores, int64_t ld, int32_t* err_word,
+                       void* stream) {
+  const int c = indexer_checks(q_idx, q_scale, w, k_idx, k_bstride, k_scale, ks_bstride, idx_dtype,
+                               q_pos, n_cmp, B, T, H_I, d_I, N_cap, m);
+  if (c >= 0) return c;
+  if (!scores || !aligned4(scores) || ld < N_cap || ld > INT32_MAX) return CSA_ERR_INVALID_ARG;
+  IndexerArgs a = indexer_args(q_idx, q_scale, w, k_idx, k_bstride, k_scale, ks_bstride, idx_dtype,
+                               q_pos, n_cmp, B, T, N_cap, m, 1, err_word);
+  return cuda_status(
+      launch_indexer_scores(a, scores, (int)ld, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int csa_indexer_topk(const void* q_idx, const float* q_scale, const float* w, const void* k_idx,
+                     int64_t k_bstride, const float* k_scale, int64_t ks_bstride, int idx_dtype,
+                     const int32_t* q_pos, const int32_t* n_cmp, int B, int T, int H_I, int d_I,
+                     int N_cap, int m, int k, int32_t* topk_idx, float* topk_score, void* ws,
+                     size_t ws_bytes, int32_t* err_word, void* stream) {
+  if (k <= 0) return CSA_ERR_INVALID_ARG;
+  const int c = indexer_checks(q_idx, q_scale, w, k_idx, k_bstride, k_scale, ks_bstride, idx_dtype,
+                               q_pos, n_cmp, B, T, H_I, d_I, N_cap, m);
+  if (c >= 0) return c;
+  if (k > N_cap) return CSA_ERR_INVALID_ARG;
+  if (!topk_idx || !aligned4(topk_idx)) return CSA_ERR_INVALID_ARG;
+  if (topk_score && !aligned4(topk_score)) return CSA_ERR_INVALID_ARG;
+  const size_t need = indexer_topk_workspace_bytes(B * T, N_cap);
+  if (!ws || ws_bytes < need || !aligned16(ws)) return CSA_ERR_WORKSPACE;
+  IndexerArgs a = indexer_args(q_idx, q_scale, w, k_idx, k_bstride, k_scale, ks_bstride, idx_dtype,
+                               q_pos, n_cmp, B, T, N_cap, m, k, err_word);
   a.topk_idx = topk_idx;
   a.topk_score = topk_score;
   return cuda_status(launch_indexer_topk(a, ws, reinterpret_cast<cudaStream_t>(stream)));

@@ -447,6 +447,36 @@ size_t indexer_topk_workspace_bytes(int n_query, int N_cap) {
   return align256((size_t)qc * score_stride(N_cap) * sizeof(float));
 }
 
+namespace {
+
+// scores of queries [q0, q0 + qc) into L (row of query q0 + i at i * stride):
+// for many tokens per sequence one tensor-core GEMM, else the streaming kernel
+cudaError_t launch_scores(const IndexerArgs& a, int q0, int qc, const WsLayout& L,
+                          cudaStream_t st) {
+  if (a.T > 8 && indexer_gemm_applies(a))
+    return launch_indexer_gemm(a, q0, qc, L.scores, L.stride, st);
+  dim3 g1((a.N_cap + kChunk - 1) / kChunk, qc);
+  if (a.fp8)
+    indexer_score_kernel<true><<<g1, kThreads, 0, st>>>(a, q0, L);
+  else
+    indexer_score_kernel<false><<<g1, kThreads, 0, st>>>(a, q0, L);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_indexer_scores(const IndexerArgs& a, float* scores, int ld, cudaStream_t st) {
+  for (int q0 = 0; q0 < a.n_query; q0 += kQueryChunk) {
+    const int qc = (a.n_query - q0 < kQueryChunk) ? a.n_query - q0 : kQueryChunk;
+    WsLayout L;
+    L.scores = scores + (int64_t)q0 * ld;
+    L.stride = ld;
+    const cudaError_t e = launch_scores(a, q0, qc, L, st);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
 cudaError_t launch_indexer_topk(const IndexerArgs& a, void* ws, cudaStream_t st) {
   WsLayout L = carve(ws, a.N_cap);
   // entries per select thread: the fewest of 8, 16, 32 that need at most 8
@@ -469,21 +499,9 @@ cudaError_t launch_indexer_topk(const IndexerArgs& a, void* ws, cudaStream_t st)
       attrs[ix] = true;
     }
   }
-  // many tokens per sequence: scores as one tensor-core GEMM per chunk
-  const bool gemm = a.T > 8 && indexer_gemm_applies(a);
   for (int q0 = 0; q0 < a.n_query; q0 += kQueryChunk) {
     const int qc = (a.n_query - q0 < kQueryChunk) ? a.n_query - q0 : kQueryChunk;
-    cudaError_t e;
-    if (gemm) {
-      e = launch_indexer_gemm(a, q0, qc, L.scores, L.stride, st);
-    } else {
-      dim3 g1((a.N_cap + kChunk - 1) / kChunk, qc);
-      if (a.fp8)
-        indexer_score_kernel<true><<<g1, kThreads, 0, st>>>(a, q0, L);
-      else
-        indexer_score_kernel<false><<<g1, kThreads, 0, st>>>(a, q0, L);
-      e = cudaGetLastError();
-    }
+    cudaError_t e = launch_scores(a, q0, qc, L, st);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)cs, (unsigned)qc);

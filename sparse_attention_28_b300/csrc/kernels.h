@@ -83,6 +83,8 @@ struct IndexerArgs {
 
 size_t indexer_topk_workspace_bytes(int n_query, int N_cap);
 cudaError_t launch_indexer_topk(const IndexerArgs& a, void* ws, cudaStream_t st);
+// the scores alone: query q's row at scores + q * ld (entries < n_vis)
+cudaError_t launch_indexer_scores(const IndexerArgs& a, float* scores, int ld, cudaStream_t st);
 // tensor-core scorer for many bf16 query tokens per sequence (T a multiple of
 // 64): scores of queries [q0, q0 + qc) into scores[(q - q0) * stride + entry]
 bool indexer_gemm_applies(const IndexerArgs& a);

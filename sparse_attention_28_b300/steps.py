@@ -20,8 +20,8 @@ from __future__ import annotations
 
 import torch
 
-from . import (attn_workspace, compress_kv, hca_dense_attn_decode, indexer_topk,
-               indexer_topk_workspace, sparse_attn_decode, sparse_attn_prefill)
+from . import (attn_workspace, compress_kv, hca_dense_attn_decode, indexer_scores,
+               indexer_topk, indexer_topk_workspace, sparse_attn_decode, sparse_attn_prefill)
 
 
 def _ring_put(cache, b, positions, rows):
@@ -170,6 +170,19 @@ class CsaDecodeStep(_Step):
         st = [("compress", self._compress)] if self.compress else []
         return st + [("indexer_topk", self._index), ("attention", self._attend)]
 
+    def kernel_probe(self):
+        """The step's dominant kernel launched alone on the step's buffers:
+        the indexer's scoring (a2), as (name, callable)."""
+        wl = self.wl
+        if not hasattr(self, "_scores"):
+            self._scores = torch.empty((wl.B, 1, self.k_idx.shape[1]), dtype=torch.float32,
+                                       device=self.out.device)
+
+        def run():
+            indexer_scores(self.q_idx, self.w, self.k_idx, self.q_pos, self.n_cmp, wl.m,
+                           q_scale=self.q_scale, k_scale=self.k_scale, out=self._scores)
+        return "indexer_score", run
+
 
 class HcaDecodeStep(_Step):
     def __init__(self, inp: dict, device="cuda"):
@@ -201,6 +214,10 @@ class HcaDecodeStep(_Step):
 
     def stages(self):
         return [("attention", self._attend)]
+
+    def kernel_probe(self):
+        """The step's one kernel: the dense attention, as (name, callable)."""
+        return "attention", self._attend
 
 
 class CsaPrefillStep(_Step):
@@ -269,6 +286,11 @@ class CsaPrefillStep(_Step):
     def stages(self):
         return [("compress", self._compress), ("indexer_topk", self._index),
                 ("attention", self._attend)]
+
+    def kernel_probe(self):
+        """The step's longest single kernel: the sparse attention of every new
+        token (one launch), as (name, callable)."""
+        return "attention", self._attend
 
 
 def make_step(inp: dict, device="cuda"):

@@ -79,6 +79,22 @@ def test_indexer_rejects():
     assert L.csa_indexer_topk_workspace(2, 1, 4096, 256) >= 2 * 4096 * 4  # one fp32 score per entry
 
 
+def test_indexer_scores_rejects():
+    L = csa.lib()
+
+    def call(**over):
+        a = dict(q=FAKE, qs=None, w=FAKE, kk=FAKE, kbs=4096 * 64, ks=None, ksbs=0, dt=0,
+                 pos=FAKE, ncmp=FAKE, B=2, T=1, HI=4, dI=64, N=4096, m=4, sc=FAKE, ld=4096,
+                 err=None, st=None)
+        a.update(over)
+        return L.csa_indexer_scores(*a.values())
+
+    assert call(HI=8) == 2 and call(dt=7) == 2 and call(N=1 << 20) == 2
+    assert call(sc=None) == 1 and call(ld=4095) == 1 and call(m=0) == 1
+    assert call(dt=1) == 1  # FP8 without scales
+    assert call(B=0, q=None, sc=None) == 0  # nothing to do
+
+
 def test_compress_rejects():
     L = csa.lib()
 

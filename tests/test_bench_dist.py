@@ -58,13 +58,22 @@ def test_single_rank_needs_no_process_group():
     assert bench.job_value(16, 1, 4, 2.0) == pytest.approx(16 * 4 / 2e-3)
 
 
-def test_dominant_stage_is_the_slowest_counted_one():
+def test_kernel_algorithmic_bytes():
+    # the scoring kernel of a 128K-context decode batch: 32 queries over 32768
+    # visible entries, each a 128-byte bf16 key row read and a 4-byte score
+    # written, plus 4 heads x (128-byte query row + 4-byte weight) per query
     sys.path.insert(0, ROOT)
     import bench
-    alg = {"indexer_topk": {"bytes": 1}, "attention": {"bytes": 1}}
-    assert bench.dominant_stage({"indexer_topk": 5.0, "attention": 1.5}, alg) == "indexer_topk"
-    assert bench.dominant_stage({"indexer_topk": 1.0, "attention": 1.5, "x": 9.0},
-                                alg) == "attention"
+    import synth
+    wl = synth.WORKLOADS["csa_decode_128k"]
+    assert bench.kernel_algorithmic(wl, "indexer_score") == {
+        "bytes": 32 * 32768 * (128 + 4) + 32 * 4 * (128 + 4)}
+    # E4M3 keys: 64 code bytes + a 4-byte scale per row
+    wl8 = synth.WORKLOADS["csa_decode_1m_fp8"]
+    assert bench.kernel_algorithmic(wl8, "indexer_score") == {
+        "bytes": 8 * 262144 * (68 + 4) + 8 * 4 * (68 + 4)}
+    hca = synth.WORKLOADS["hca_decode_1m"]
+    assert bench.kernel_algorithmic(hca, "attention") == bench.algorithmic(hca)["attention"]
 
 
 def test_reference_arm_under_torchrun_prints_once_from_rank_0():

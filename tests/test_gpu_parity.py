@@ -123,6 +123,33 @@ def test_indexer_topk_parity(cuda_device, fp8, T):
             assert np.all(np.isneginf(sc[b, t, take:]))
 
 
+@pytest.mark.parametrize("fp8,T", [(False, 1), (True, 1), (False, 3), (True, 5),
+                                    (False, 64), (False, 128)])
+def test_indexer_scores_parity(cuda_device, fp8, T):
+    # the a2 scores alone, element by element on the visible entries; T = 64
+    # and 128 take the tensor-core scorer (whole 64-token blocks)
+    B, N_cap, m = 2, 2500, 4
+    n_cmp = [2500, 1303]
+    q_pos = [[(n_cmp[b] * m + 1) * (t + 1) // T - 1 for t in range(T)] for b in range(B)]
+    qi, qs, ki, ks, w, qp, nc = _indexer_case(B, T, N_cap, n_cmp, q_pos, fp8, seed=17)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    got = csa.indexer_scores(qi.to(DEV), w.to(DEV), ki.to(DEV), qp.to(DEV), nc.to(DEV), m,
+                             q_scale=None if qs is None else qs.to(DEV),
+                             k_scale=None if ks is None else ks.to(DEV), err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    got = got.cpu().numpy().astype(np.float64)
+    conv = u8 if fp8 else u16
+    want, nv = oracle.indexer_scores(conv(qi), w.numpy(), conv(ki), qp.numpy(), nc.numpy(), m,
+                                     oracle.FP8_E4M3 if fp8 else oracle.BF16,
+                                     None if qs is None else qs.numpy(),
+                                     None if ks is None else ks.numpy())
+    for b in range(B):
+        for t in range(T):
+            n = int(nv[b, t])
+            np.testing.assert_allclose(got[b, t, :n], want[b, t, :n], rtol=2e-5, atol=2e-4)
+
+
 @pytest.mark.parametrize("B,T,N_cap,k", [(2, 64, 3000, 200), (2, 320, 3000, 256),
                                          (1, 256, 40000, 2048)])
 def test_indexer_topk_parity_many_tokens(cuda_device, B, T, N_cap, k):
