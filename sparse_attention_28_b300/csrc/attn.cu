@@ -196,6 +196,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kStages = C::kStages;
   constexpr int kPairs = C::kPairs;
   constexpr int NL = kLoadThreads;
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* sm = smem_raw + ((1024 - (raw_addr & 1023)) & 1023);
@@ -695,20 +697,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// attr: room for two attributes (cluster shape; programmatic launch if pdl)
 template <int M>
 cudaLaunchConfig_t launch_cfg(int n_split, int n_query, cudaStream_t st,
-                              cudaLaunchAttribute* attr) {
+                              cudaLaunchAttribute* attr, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)n_split * (unsigned)n_query);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = Cfg<M>::kSmemBytes;
   cfg.stream = st;
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)n_split;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  unsigned n = 0;
+  if (n_split > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = (unsigned)n_split;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  if (pdl) set_pdl(attr[n++]);
   cfg.attrs = attr;
-  cfg.numAttrs = n_split > 1 ? 1 : 0;
+  cfg.numAttrs = n;
   return cfg;
 }
 
@@ -731,7 +739,7 @@ int active_clusters(int n) {
       cudaFuncSetAttribute(attn_tc_kernel<M>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     ensure_smem_attr((const void*)attn_tc_kernel<M>, Cfg<M>::kSmemBytes);
     cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = launch_cfg<M>(n, 1, nullptr, attr);
+    cudaLaunchConfig_t cfg = launch_cfg<M>(n, 1, nullptr, attr, false);
     int clusters = 0;
     if (cudaOccupancyMaxActiveClusters(&clusters, attn_tc_kernel<M>, &cfg) != cudaSuccess)
       clusters = 0;
@@ -754,8 +762,8 @@ cudaError_t launch_tc(AttnArgs a, const Maps& maps, cudaStream_t st) {
   }
   a.n_split = ns;
   a.keys_per_split = kps;
-  cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = launch_cfg<M>(ns, a.n_query, st, attr);
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = launch_cfg<M>(ns, a.n_query, st, attr, true);
   return cudaLaunchKernelEx(&cfg, attn_tc_kernel<M>, a, maps);
 }
 

@@ -107,6 +107,36 @@ __device__ __forceinline__ uint32_t score_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// Programmatic dependent launch.  Every kernel of the library is launched
+// with the programmatic-serialization attribute (set_pdl), so its CTAs may be
+// scheduled while the previous kernel on the stream is still finishing; each
+// kernel first lets its own dependents be scheduled (pdl_trigger) and then
+// waits for the previous grid's completion and memory (pdl_wait) before it
+// touches global memory or tensor memory.  Whatever the previous kernel is,
+// nothing is read before it has finished.
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+inline void set_pdl(cudaLaunchAttribute& at) {
+  at.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at.val.programmaticStreamSerializationAllowed = 1;
+}
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  set_pdl(at[0]);
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 // 2^x by the special-function unit (PTX ex2.approx.ftz: relative error about
 // 2^-22, subnormal results flushed to zero, 2^-inf = +0).
 __device__ __forceinline__ float ex2_approx(float x) {

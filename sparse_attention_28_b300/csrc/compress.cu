@@ -28,6 +28,8 @@ constexpr int kPosChunk = 16;
 
 template <int D>
 __global__ void __launch_bounds__(D) compress_kernel(CompressArgs a) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ __align__(16) float xs[];  // [m][D]
   __shared__ float red[D / 32];
   const int c = threadIdx.x;
@@ -122,13 +124,13 @@ cudaError_t launch_compress(const CompressArgs& a, cudaStream_t st) {
   if (a.d == 128) {
     e = ensure_smem_attr((const void*)compress_kernel<128>, 256 * 128 * 4);
     if (e != cudaSuccess) return e;
-    compress_kernel<128><<<grid, 128, a.m * 128 * 4, st>>>(a);
+    e = launch_pdl(compress_kernel<128>, grid, dim3(128), a.m * 128 * 4, st, a);
   } else {
     e = ensure_smem_attr((const void*)compress_kernel<64>, 256 * 64 * 4);
     if (e != cudaSuccess) return e;
-    compress_kernel<64><<<grid, 64, a.m * 64 * 4, st>>>(a);
+    e = launch_pdl(compress_kernel<64>, grid, dim3(64), a.m * 64 * 4, st, a);
   }
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace csa

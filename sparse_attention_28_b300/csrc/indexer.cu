@@ -142,6 +142,8 @@ __device__ void bin_from_top(const int (&bins)[PER], int first_bin, int need, in
 template <bool FP8>
 __global__ void __launch_bounds__(kThreads) indexer_score_kernel(IndexerArgs a, int q0,
                                                                 WsLayout L) {
+  pdl_trigger();
+  pdl_wait();
   const int lq = blockIdx.y, qid = q0 + lq;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, c = lane & 3;
@@ -276,6 +278,8 @@ __global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(IndexerArgs
   constexpr int kCopies = 8;           // bulk copies the slice is split into
   extern __shared__ __align__(128) uint8_t sel_smem[];
   SelShared* sh = reinterpret_cast<SelShared*>(sel_smem);
+  pdl_trigger();
+  pdl_wait();
   float* sc = reinterpret_cast<float*>(sel_smem + (sizeof(SelShared) + 127) / 128 * 128);
   const int tid = threadIdx.x;
   const int cs = gridDim.x, r = blockIdx.x;
@@ -456,11 +460,8 @@ cudaError_t launch_scores(const IndexerArgs& a, int q0, int qc, const WsLayout& 
   if (a.T > 8 && indexer_gemm_applies(a))
     return launch_indexer_gemm(a, q0, qc, L.scores, L.stride, st);
   dim3 g1((a.N_cap + kChunk - 1) / kChunk, qc);
-  if (a.fp8)
-    indexer_score_kernel<true><<<g1, kThreads, 0, st>>>(a, q0, L);
-  else
-    indexer_score_kernel<false><<<g1, kThreads, 0, st>>>(a, q0, L);
-  return cudaGetLastError();
+  if (a.fp8) return launch_pdl(indexer_score_kernel<true>, g1, dim3(kThreads), 0, st, a, q0, L);
+  return launch_pdl(indexer_score_kernel<false>, g1, dim3(kThreads), 0, st, a, q0, L);
 }
 
 }  // namespace
@@ -508,13 +509,14 @@ cudaError_t launch_indexer_topk(const IndexerArgs& a, void* ws, cudaStream_t st)
     cfg.blockDim = dim3(kSelThreads);
     cfg.dynamicSmemBytes = sel_smem_bytes(per);
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)cs;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    set_pdl(attr[1]);
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     if (per == 8)
       e = cudaLaunchKernelEx(&cfg, topk_select_kernel<8>, a, q0, L);
     else if (per == 16)

@@ -60,6 +60,8 @@ struct GemmMaps {
 __global__ void __launch_bounds__(kGThreads, 1)
     indexer_gemm_kernel(IndexerArgs a, int q0, float* scores, int stride,
                         const __grid_constant__ GemmMaps maps) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ uint8_t gsm_raw[];
   uint8_t* sm = gsm_raw + ((1024 - (smem_u32(gsm_raw) & 1023)) & 1023);
   const uint32_t sbase = smem_u32(sm);
@@ -229,9 +231,8 @@ cudaError_t launch_indexer_gemm(const IndexerArgs& a, int q0, int qc, float* sco
   const int max_tiles = (a.N_cap + kGM - 1) / kGM;
   splits = splits > max_tiles ? max_tiles : splits;
   splits = splits < 1 ? 1 : splits;
-  indexer_gemm_kernel<<<dim3(splits, n_blocks), kGThreads, kGSmem, st>>>(a, q0, scores, stride,
-                                                                        maps);
-  return cudaGetLastError();
+  return launch_pdl(indexer_gemm_kernel, dim3(splits, n_blocks), dim3(kGThreads), kGSmem, st, a, q0,
+                    scores, stride, maps);
 }
 
 }  // namespace csa

@@ -63,11 +63,15 @@ class _Step:
             fn()
         return self.out
 
-    def graphed(self):
+    def graphed(self, h2d=(), d2h=None):
         """Capture one whole step in a CUDA graph (after an eager warm-up
         call) and return a callable that replays it on the current stream and
         returns ``out``.  The graph reads the step's own device tensors when it
-        replays, so new inputs are copied into them first."""
+        replays, so new inputs are copied into them first: ``h2d`` lists
+        (pinned host tensor, device tensor) pairs copied in at the start of
+        the graph and ``d2h`` a pinned host tensor that ``out`` is copied to
+        at its end, so that one replay is one submission for the whole
+        host -> device -> host round trip."""
         dev = self.out.device
         self()
         torch.cuda.synchronize(dev)
@@ -75,7 +79,11 @@ class _Step:
         side = torch.cuda.Stream(device=dev)
         side.wait_stream(torch.cuda.current_stream(dev))
         with torch.cuda.graph(graph, stream=side):
+            for h, d in h2d:
+                d.copy_(h, non_blocking=True)
             self()
+            if d2h is not None:
+                d2h.copy_(self.out, non_blocking=True)
         torch.cuda.synchronize(dev)
 
         def replay():
