@@ -139,19 +139,11 @@ __device__ void bin_from_top(const int (&bins)[PER], int first_bin, int need, in
 //         [64+16c, 64+16c+16); k-step s takes word s of each vector.
 //   E4M3 (m16n8k32, products exact in fp32): thread (g, c) holds row bytes
 //         [16c, 16c+16); k-step s takes words 2s and 2s+1.
+// Scores of entries [e0, e1) of query qid into scores[e]: each warp takes
+// 16-entry groups, kUnroll groups in flight.
 template <bool FP8>
-__global__ void __launch_bounds__(kThreads) indexer_score_kernel(IndexerArgs a, int q0,
-                                                                WsLayout L) {
-  pdl_trigger();
-  pdl_wait();
-  const int lq = blockIdx.y, qid = q0 + lq;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g = lane >> 2, c = lane & 3;
-  const int64_t nv = visible_entries(a, qid, a.err, blockIdx.x == 0 && tid == 0);
-  const int64_t e0 = (int64_t)blockIdx.x * kChunk;
-  if (e0 >= nv) return;
-  const int64_t e1 = (e0 + kChunk < nv) ? e0 + kChunk : nv;
-
+__device__ __forceinline__ void score_range(const IndexerArgs& a, int qid, int64_t e0, int64_t e1,
+                                            float* scores, int warp, int g, int c) {
   // query fragments (heads g < 4) and head weights (heads 2c, 2c+1 for c < 2)
   uint32_t qb0[4] = {0, 0, 0, 0}, qb1[4] = {0, 0, 0, 0};
   float w0 = 0.f, w1 = 0.f;
@@ -176,10 +168,8 @@ __global__ void __launch_bounds__(kThreads) indexer_score_kernel(IndexerArgs a, 
       w1 *= __ldg(a.q_scale + (int64_t)qid * kHI + 2 * c + 1);
     }
   }
-  __syncthreads();
 
   const int b = qid / a.T;
-  float* scores = L.scores + (int64_t)lq * L.stride;
   constexpr int kUnroll = FP8 ? kUnrollFp8 : kUnrollBf16;
   const int n_groups = (int)((e1 - e0 + 15) / 16);
   for (int gb = warp * kUnroll; gb < n_groups; gb += (kThreads / 32) * kUnroll) {
@@ -237,6 +227,49 @@ __global__ void __launch_bounds__(kThreads) indexer_score_kernel(IndexerArgs a, 
         scores[e] = sc;
       }
     }
+  }
+}
+
+// One wave of CTAs; the 16-entry groups of all queries of the chunk,
+// concatenated in query order, are split into equal contiguous ranges, one
+// per CTA.  A CTA walks its range query by query (loading that query's
+// fragments and weights), so that every CTA streams the same number of key
+// bytes whatever the queries' visible counts.
+template <bool FP8>
+__global__ void __launch_bounds__(kThreads) indexer_score_kernel(IndexerArgs a, int q0, int qc,
+                                                                WsLayout L) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ int gp[kQueryChunk + 1];  // group prefix over the chunk's queries
+  __shared__ int nvs[kQueryChunk];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, c = lane & 3;
+  {
+    int nv = 0;
+    if (tid < qc) {
+      nv = (int)visible_entries(a, q0 + tid, a.err, blockIdx.x == 0);
+      nvs[tid] = nv;
+    }
+    int tot;
+    const int before = block_excl_scan<kThreads>((nv + 15) >> 4, reinterpret_cast<int*>(gp + 1),
+                                                 &tot);
+    if (tid < qc) gp[tid] = before;  // (the scan's scratch, gp[1..32], is read before this)
+    __syncthreads();
+    if (tid == 0) gp[qc] = tot;
+    __syncthreads();
+  }
+  const int G = gp[qc];
+  const int g_lo = (int)((int64_t)blockIdx.x * G / gridDim.x);
+  const int g_hi = (int)((int64_t)(blockIdx.x + 1) * G / gridDim.x);
+  int lq = 0;
+  while (lq < qc && gp[lq + 1] <= g_lo) ++lq;
+  for (; lq < qc && gp[lq] < g_hi; ++lq) {
+    const int qid = q0 + lq;
+    const int s_lo = max(g_lo, gp[lq]) - gp[lq], s_hi = min(g_hi, gp[lq + 1]) - gp[lq];
+    if (s_hi <= s_lo) continue;
+    const int64_t e0 = (int64_t)s_lo * 16;
+    const int64_t e1 = min((int64_t)s_hi * 16, (int64_t)nvs[lq]);
+    score_range<FP8>(a, qid, e0, e1, L.scores + (int64_t)lq * L.stride, warp, g, c);
   }
 }
 
@@ -459,9 +492,14 @@ cudaError_t launch_scores(const IndexerArgs& a, int q0, int qc, const WsLayout& 
                           cudaStream_t st) {
   if (a.T > 8 && indexer_gemm_applies(a))
     return launch_indexer_gemm(a, q0, qc, L.scores, L.stride, st);
-  dim3 g1((a.N_cap + kChunk - 1) / kChunk, qc);
-  if (a.fp8) return launch_pdl(indexer_score_kernel<true>, g1, dim3(kThreads), 0, st, a, q0, L);
-  return launch_pdl(indexer_score_kernel<false>, g1, dim3(kThreads), 0, st, a, q0, L);
+  // one wave (two CTAs per SM), fewer when there is little work: at least
+  // kChunk entries' worth of groups per CTA on average
+  const int64_t groups = (int64_t)qc * ((a.N_cap + 15) / 16);
+  int64_t n_cta = (groups * 16 + kChunk - 1) / kChunk;
+  if (n_cta > 2 * kNumSMs) n_cta = 2 * kNumSMs;
+  const dim3 g1((unsigned)(n_cta > 0 ? n_cta : 1));
+  if (a.fp8) return launch_pdl(indexer_score_kernel<true>, g1, dim3(kThreads), 0, st, a, q0, qc, L);
+  return launch_pdl(indexer_score_kernel<false>, g1, dim3(kThreads), 0, st, a, q0, qc, L);
 }
 
 }  // namespace
