@@ -216,11 +216,16 @@ CSA_API int csa_indexer_topk_static(const void* q_idx, const float* q_scale, con
  *   seq_len   int32 [B] (decode: t = seq_len - 1, the token's own K/V is
  *             already in the raw cache); q_pos int32 [B][T] (prefill).
  *   out       bf16, same shape as q; lse fp32 [B][(T)][H] (optional).
- *   ws        csa_attn_workspace(B, T, H, n_keys_max) bytes, where n_keys_max
- *             is the largest key-set size (k + window for CSA; the largest
- *             n_vis + window for HCA).  This build needs none (it returns 0:
- *             the key splits of a query run as one thread-block cluster and
- *             merge through distributed shared memory); ws may be NULL.
+ *   ws        optional: csa_attn_workspace(B, T, H, n_keys_max) bytes (16-byte
+ *             aligned), where n_keys_max is the largest key-set size (k +
+ *             window for CSA; the largest n_vis + window for HCA).  Without it
+ *             (NULL, or fewer bytes) the key splits of a query run as one
+ *             thread-block cluster and merge through distributed shared
+ *             memory.  With it, when clusters that large cannot all be
+ *             resident at once (few queries, many keys), the keys are split
+ *             further without a cluster and the partial results merged by a
+ *             second kernel through this buffer.  Either way the result is
+ *             the same combination; a misaligned ws returns CSA_ERR_WORKSPACE.
  *   H in {16, 32, 64, 128}; D == 128.
  * ---------------------------------------------------------------------- */
 CSA_API size_t csa_attn_workspace(int B, int T, int H, int n_keys_max);

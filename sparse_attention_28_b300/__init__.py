@@ -129,7 +129,9 @@ def _bstride(t) -> int:
 
 
 def _ws(nbytes: int, device, ws):
-    if nbytes == 0:
+    """Workspace for a call: `ws` itself, a new buffer when it is None, or no
+    workspace when it is False (attention only: splits then merge on chip)."""
+    if nbytes == 0 or ws is False:
         return None, 0
     if ws is not None:
         _need(ws.numel() * ws.element_size() >= nbytes, "workspace too small")

@@ -230,9 +230,12 @@ size_t csa_attn_workspace(int B, int T, int H, int n_keys_max) {
 
 static int run_attention(AttnArgs& a, void* ws, size_t ws_bytes, void* stream) {
   if (a.n_query == 0) return CSA_OK;
+  // the workspace is optional: without it (or if it is too small) the key
+  // splits of a query always merge inside a cluster
   const size_t need = attn_workspace_bytes(a.n_query, a.H, a.n_keys_max);
-  if (need > 0 && (!ws || ws_bytes < need || !aligned16(ws))) return CSA_ERR_WORKSPACE;
-  return cuda_status(launch_attention(a, ws, reinterpret_cast<cudaStream_t>(stream)));
+  if (ws && !aligned16(ws)) return CSA_ERR_WORKSPACE;
+  void* use = (need > 0 && ws && ws_bytes >= need) ? ws : nullptr;
+  return cuda_status(launch_attention(a, use, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 static void fill_common(AttnArgs& a, const void* q, const void* k_cmp, const void* v_cmp,

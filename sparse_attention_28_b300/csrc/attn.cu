@@ -600,7 +600,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (h >= H) continue;
             const float v0 = __uint_as_float(o[u * 4 + 2 * h2]) * fac[h2];
             const float v1 = __uint_as_float(o[u * 4 + 2 * h2 + 1]) * fac[h2];
-            if (ns > 1)
+            if (ns > 1 && a.part_o)
+              *reinterpret_cast<float2*>(a.part_o + (((int64_t)qid * ns + split) * H + h) * kD +
+                                         col) = make_float2(v0, v1);
+            else if (ns > 1)
               *reinterpret_cast<float2*>(sm + C::kPartOff + h * 512 + col * 4) =
                   make_float2(v0, v1);
             else
@@ -614,7 +617,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int h2 = 0; h2 < 2; ++h2) {
           const int h = rowA + 8 * h2;
           if (h >= H) continue;
-          if (ns > 1)
+          if (ns > 1 && a.part_lse)
+            a.part_lse[((int64_t)qid * ns + split) * H + h] = lse_r[h2];
+          else if (ns > 1)
             reinterpret_cast<float*>(sm + C::kPartLseOff)[h] = lse_r[h2];
           else if (a.lse)
             a.lse[(int64_t)qid * H + h] = lse_r[h2];
@@ -630,7 +635,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, kTmemCols);
   }
-  if (ns <= 1) return;
+  if (ns <= 1 || a.part_o) return;  // one split, or partials merged by attn_merge_kernel
 
   // ---- split merge inside the cluster.  CTA `split` combines heads
   // [split*hp, split*hp + hp).  After the first cluster barrier no CTA uses
@@ -697,17 +702,60 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Split merge through global memory (a6), for splits run without a cluster:
+// grid (queries, ceil(H / 4)), warp w of CTA (q, y) merges head 4y + w.  The
+// same combination as the cluster merge: weights exp(lse_s - M) / Z over the
+// splits, the sink's exp(sink - M) in Z only.
+__global__ void __launch_bounds__(128) attn_merge_kernel(AttnArgs a) {
+  pdl_trigger();
+  pdl_wait();
+  const int qid = blockIdx.x, lane = threadIdx.x & 31;
+  const int h = blockIdx.y * 4 + (threadIdx.x >> 5);
+  const int ns = a.n_split, H = a.H;
+  if (h >= H) return;
+  const float* lse_p = a.part_lse + (int64_t)qid * ns * H + h;  // split s at s * H
+  float Mx = a.sink ? __ldg(a.sink + h) : -INFINITY;
+  for (int s = lane; s < ns; s += 32) Mx = fmaxf(Mx, lse_p[(int64_t)s * H]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) Mx = fmaxf(Mx, __shfl_xor_sync(0xFFFFFFFFu, Mx, o));
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float lse = -INFINITY;
+  if (Mx != -INFINITY) {
+    float Z = a.sink ? expf(__ldg(a.sink + h) - Mx) : 0.f;
+    for (int s = 0; s < ns; ++s) {
+      const float ls = lse_p[(int64_t)s * H];
+      const float w = ls == -INFINITY ? 0.f : expf(ls - Mx);
+      Z += w;
+      const float4 v = reinterpret_cast<const float4*>(
+          a.part_o + (((int64_t)qid * ns + s) * H + h) * kD)[lane];
+      acc.x += w * v.x;
+      acc.y += w * v.y;
+      acc.z += w * v.z;
+      acc.w += w * v.w;
+    }
+    const float inv = 1.f / Z;
+    acc.x *= inv;
+    acc.y *= inv;
+    acc.z *= inv;
+    acc.w *= inv;
+    lse = Mx + logf(Z);
+  }
+  reinterpret_cast<uint2*>(a.out + ((int64_t)qid * H + h) * kD)[lane] =
+      make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+  if (lane == 0 && a.lse) a.lse[(int64_t)qid * H + h] = lse;
+}
+
 // attr: room for two attributes (cluster shape; programmatic launch if pdl)
 template <int M>
 cudaLaunchConfig_t launch_cfg(int n_split, int n_query, cudaStream_t st,
-                              cudaLaunchAttribute* attr, bool pdl) {
+                              cudaLaunchAttribute* attr, bool pdl, bool cluster = true) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)n_split * (unsigned)n_query);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = Cfg<M>::kSmemBytes;
   cfg.stream = st;
   unsigned n = 0;
-  if (n_split > 1) {
+  if (n_split > 1 && cluster) {
     attr[n].id = cudaLaunchAttributeClusterDimension;
     attr[n].val.clusterDim.x = (unsigned)n_split;
     attr[n].val.clusterDim.y = 1;
@@ -750,7 +798,7 @@ int active_clusters(int n) {
 }
 
 template <int M>
-cudaError_t launch_tc(AttnArgs a, const Maps& maps, cudaStream_t st) {
+cudaError_t launch_tc(AttnArgs a, const Maps& maps, void* ws, cudaStream_t st) {
   cudaError_t e = ensure_smem_attr((const void*)attn_tc_kernel<M>, Cfg<M>::kSmemBytes);
   if (e != cudaSuccess) return e;
   // Pick the split count: at most one cluster of splits per query, every
@@ -760,11 +808,31 @@ cudaError_t launch_tc(AttnArgs a, const Maps& maps, cudaStream_t st) {
     attn_plan(a.n_query, a.n_keys_max, cap, &ns, &kps);
     if (ns <= 1 || (long)active_clusters<M>(ns) >= (long)a.n_query) break;
   }
+  // Where clusters that large cannot all be resident and a workspace is
+  // given, run more splits without a cluster and merge them in a second
+  // kernel (partials through L2) instead.
+  bool free_splits = false;
+  if (ws && a.n_query * ns < (kNumSMs * 4) / 5) {
+    int ns_f = 1, kps_f = 0;
+    attn_plan(a.n_query, a.n_keys_max, kNumSMs, &ns_f, &kps_f);
+    if (ns_f * 5 > ns * 6) {
+      ns = ns_f;
+      kps = kps_f;
+      free_splits = true;
+    }
+  }
   a.n_split = ns;
   a.keys_per_split = kps;
+  if (free_splits) {
+    a.part_o = reinterpret_cast<float*>(ws);
+    a.part_lse = a.part_o + (int64_t)a.n_query * ns * a.H * kD;
+  }
   cudaLaunchAttribute attr[2];
-  cudaLaunchConfig_t cfg = launch_cfg<M>(ns, a.n_query, st, attr, true);
-  return cudaLaunchKernelEx(&cfg, attn_tc_kernel<M>, a, maps);
+  cudaLaunchConfig_t cfg = launch_cfg<M>(ns, a.n_query, st, attr, true, !free_splits);
+  e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<M>, a, maps);
+  if (e != cudaSuccess || !free_splits) return e;
+  return launch_pdl(attn_merge_kernel, dim3((unsigned)a.n_query, (unsigned)((a.H + 3) / 4)),
+                    dim3(128), 0, st, a);
 }
 
 }  // namespace
@@ -788,9 +856,17 @@ void attn_plan(int n_query, int n_keys_max, int max_cluster, int* n_split, int* 
   *keys_per_split = kps;
 }
 
-size_t attn_workspace_bytes(int, int, int) { return 0; }
+// Workspace for splits without a cluster (partial rows and lse values of
+// every split of every query); 0 when a query would get a single split.
+size_t attn_workspace_bytes(int n_query, int H, int n_keys_max) {
+  int ns = 1, kps = 0;
+  attn_plan(n_query, n_keys_max, kNumSMs, &ns, &kps);
+  if (ns <= 1) return 0;
+  const size_t bytes = (size_t)n_query * ns * H * (kD + 1) * sizeof(float);
+  return (bytes + 255) & ~size_t(255);
+}
 
-cudaError_t launch_attention(AttnArgs a, void*, cudaStream_t st) {
+cudaError_t launch_attention(AttnArgs a, void* ws, cudaStream_t st) {
   // 2-D row views (rows of 128 elements) of the query block and the compressed caches
   Maps maps;
   const void* dummy = a.q;
@@ -801,8 +877,8 @@ cudaError_t launch_attention(AttnArgs a, void*, cudaStream_t st) {
   e = tma::encode_rows128(&maps.kc, has_c ? a.k_cmp : dummy, crow, kStageKeys);
   if (e == cudaSuccess) e = tma::encode_rows128(&maps.vc, has_c ? a.v_cmp : dummy, crow, kStageKeys);
   if (e != cudaSuccess) return e;
-  if (a.H <= 64) return launch_tc<64>(a, maps, st);
-  return launch_tc<128>(a, maps, st);
+  if (a.H <= 64) return launch_tc<64>(a, maps, ws, st);
+  return launch_tc<128>(a, maps, ws, st);
 }
 
 }  // namespace csa

@@ -113,11 +113,21 @@ def test_compress_rejects():
     assert call(B=0) == 0 and call(nb=0) == 0
 
 
-def test_attention_needs_no_workspace():
-    # key splits merge through distributed shared memory inside a cluster
+def test_attention_workspace_only_for_split_queries():
+    # partial rows + lse (129 fp32 per head) for every split of every query
+    # when a query can get several splits (fewer queries than SMs / 2); none
+    # when each query gets one split
     L = csa.lib()
-    for args in ((32, 1, 64, 1152), (1, 4096, 64, 2176), (16, 1, 64, 8320), (8, 1, 128, 2176)):
-        assert L.csa_attn_workspace(*args) == 0
+
+    def ws(n_query, ns, H):
+        b = n_query * ns * H * 129 * 4
+        return (b + 255) // 256 * 256
+
+    assert L.csa_attn_workspace(32, 1, 64, 1152) == ws(32, 4, 64)     # 148 // 32 splits
+    assert L.csa_attn_workspace(16, 1, 64, 8320) == ws(16, 9, 64)
+    assert L.csa_attn_workspace(8, 1, 128, 2176) == ws(8, 18, 128)    # 18 tiles of keys
+    assert L.csa_attn_workspace(1, 4096, 64, 2176) == 0                # one split per query
+    assert L.csa_attn_workspace(100, 1, 64, 1152) == 0
 
 
 def test_binding_rejects_cpu_tensors():

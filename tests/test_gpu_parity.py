@@ -289,6 +289,45 @@ def test_sparse_decode_many_splits_multi_tile(cuda_device):
     check_attention(out, ro, lse, rl, "csa decode splits")
 
 
+@pytest.mark.parametrize("ws", [None, False])
+def test_many_keys_few_queries_split_modes(cuda_device, ws):
+    # 25 tiles of keys for each of 1-2 queries: clusters of 16 splits would
+    # leave most SMs idle, so with a workspace (ws=None: the binding sizes one)
+    # the keys are split 25 ways without a cluster and merged by a second
+    # kernel; ws=False forces the in-cluster merge.  Both against the oracle.
+    H, m = 64, 8
+    lens = [24000, 23001]
+    N_cap = 3000
+    n_cmp = [3000, 2875]
+    q, kc, vc, kw, vw, sink = _attn_inputs(2, H, N_cap, lens, seed=61)
+    out, lse = csa.hca_dense_attn_decode(
+        q.to(DEV), kc.to(DEV), vc.to(DEV), torch.tensor(n_cmp, dtype=torch.int32, device=DEV), m,
+        place_window(kw, lens, 24000), place_window(vw, lens, 24000),
+        torch.tensor(lens, dtype=torch.int32, device=DEV), 128, sink.to(DEV), return_lse=True,
+        ws=ws)
+    torch.cuda.synchronize()
+    kr, base = window_arrays(kw, lens)
+    vr, _ = window_arrays(vw, lens)
+    ro, rl = oracle.hca_decode(u16(q), u16(kc), u16(vc), np.array(n_cmp), m, kr, vr,
+                               np.array(lens), 128, sink.numpy(), 1.0, base)
+    check_attention(out, ro, lse, rl, f"hca many keys ws={ws}")
+    # one CSA query with 3000 selected entries (+128 window)
+    lens1 = [16004]
+    q1, kc1, vc1, kw1, vw1, sink1 = _attn_inputs(1, H, 4001, lens1, seed=62)
+    sel = _random_topk(1, 3000, [4001], seed=9)
+    out1, lse1 = csa.sparse_attn_decode(
+        q1.to(DEV), kc1.to(DEV), vc1.to(DEV), torch.from_numpy(sel).to(DEV),
+        place_window(kw1, lens1, 16004), place_window(vw1, lens1, 16004),
+        torch.tensor(lens1, dtype=torch.int32, device=DEV), 128, sink1.to(DEV), return_lse=True,
+        ws=ws)
+    torch.cuda.synchronize()
+    kr1, base1 = window_arrays(kw1, lens1)
+    vr1, _ = window_arrays(vw1, lens1)
+    ro1, rl1 = oracle.csa_decode(u16(q1), u16(kc1), u16(vc1), sel, kr1, vr1, np.array(lens1),
+                                 128, sink1.numpy(), 1.0, base1)
+    check_attention(out1, ro1, lse1, rl1, f"csa 3000 entries ws={ws}")
+
+
 def test_decode_window_only_and_compressed_only(cuda_device):
     B, H, N_cap, k = 2, 64, 100, 32
     lens = [400, 90]
