@@ -79,6 +79,8 @@ def _load():
             lib.orc_quantize_e4m3_rows.restype = None
             lib.orc_compress.argtypes = [P, L, I, I, I, I, I, P, P, P]
             lib.orc_compress.restype = I
+            lib.orc_compress_span.argtypes = [P, L, I, I, I, I, I, I, P, P, P]
+            lib.orc_compress_span.restype = I
             lib.orc_indexer_scores.argtypes = [P, P, P, P, L, P, L, I, P, P, I, I, I, I, I, L,
                                                P, P]
             lib.orc_indexer_scores.restype = I
@@ -162,18 +164,23 @@ def quantize_e4m3_rows(y):
 # --------------------------------------------------------------------------
 
 def compress(raw, W, pos_bias, m: int, block_begin: int, n_blocks: int) -> np.ndarray:
-    """a1 in fp64.  raw: uint16 [B, L, d]; W: uint16 [d, d]; pos_bias: f32 [m, d].
+    """a1 in fp64.  raw: uint16 [B, L, d]; W: uint16 [d, d]; pos_bias: f32 [span, d].
 
-    Returns fp64 [B, n_blocks, d] for blocks [block_begin, block_begin+n_blocks).
+    Block j (stride m) is compressed from the span = pos_bias.shape[0] raw
+    tokens ending at its last token, j*m + m - span .. j*m + m - 1 (the
+    non-negative ones): span = m is the non-overlapping operator, span > m
+    overlapping compression.  Returns fp64 [B, n_blocks, d] for blocks
+    [block_begin, block_begin+n_blocks).
     """
     raw = _c(raw, np.uint16)
     W = _c(W, np.uint16)
     pos_bias = _c(pos_bias, np.float32)
     B, L, d = raw.shape
-    assert W.shape == (d, d) and pos_bias.shape == (m, d)
+    span = pos_bias.shape[0]
+    assert W.shape == (d, d) and pos_bias.shape == (span, d) and span >= m
     y = np.empty((B, n_blocks, d), np.float64)
-    rc = _load().orc_compress(_ptr(raw), L * d, B, d, m, block_begin, n_blocks, _ptr(W),
-                              _ptr(pos_bias), _ptr(y))
+    rc = _load().orc_compress_span(_ptr(raw), L * d, B, d, m, span, block_begin, n_blocks,
+                                   _ptr(W), _ptr(pos_bias), _ptr(y))
     _check(rc, "compress")
     return y
 

@@ -169,19 +169,23 @@ void orc_quantize_e4m3_rows(const double* y, int64_t rows, int d, uint8_t* codes
 /* ------------------------------------------------------------------------ */
 
 /* Compress blocks [block_begin, block_begin + n_blocks) of every sequence.
- * Block j covers raw tokens j*m .. j*m+m-1 (non-overlapping).  For each
- * channel c (the operator is the build's reading of "learnable compression
- * weights and positional biases"):
- *     g[i][c] = sum_e W[c][e] * x[j*m+i][e] + pos_bias[i][c]
- *     a[.][c] = softmax over i of g[.][c]
- *     y[j][c] = sum_i a[i][c] * x[j*m+i][c]
+ * Block j (stride m) is compressed from the `span` raw tokens that end at its
+ * last token, positions P(j) = { j*m + m - span + i : 0 <= i < span } minus the
+ * negative ones (span = m: the non-overlapping blocks j*m .. j*m+m-1; span > m:
+ * overlapping compression, the reading of the HCA paragraph's "without
+ * overlapping compression" as setting HCA apart from CSA).  For each channel c
+ * (the operator is the build's reading of "learnable compression weights and
+ * positional biases"), over the positions p = j*m + m - span + i in P(j):
+ *     g[i][c] = sum_e W[c][e] * x[p][e] + pos_bias[i][c]
+ *     a[.][c] = softmax over those i of g[.][c]
+ *     y[j][c] = sum_i a[i][c] * x[p][c]
  * raw: bf16 [B][raw_bstride] with token rows of d; W: bf16 [d][d] (row =
- * output channel); pos_bias: fp32 [m][d].  y: fp64 [B][n_blocks][d]. */
-int orc_compress(const uint16_t* raw, int64_t raw_bstride, int B, int d, int m,
-                 int block_begin, int n_blocks, const uint16_t* W, const float* pos_bias,
-                 double* y) {
-  if (!raw || !W || !pos_bias || !y || B < 0 || d <= 0 || m <= 0 || block_begin < 0 ||
-      n_blocks < 0)
+ * output channel); pos_bias: fp32 [span][d].  y: fp64 [B][n_blocks][d]. */
+int orc_compress_span(const uint16_t* raw, int64_t raw_bstride, int B, int d, int m, int span,
+                      int block_begin, int n_blocks, const uint16_t* W, const float* pos_bias,
+                      double* y) {
+  if (!raw || !W || !pos_bias || !y || B < 0 || d <= 0 || m <= 0 || span < m ||
+      block_begin < 0 || n_blocks < 0)
     return ORC_ERR_ARG;
   if ((int64_t)(block_begin + n_blocks) * m * d > raw_bstride) return ORC_ERR_RANGE;
   double* Wd = (double*)malloc(sizeof(double) * (size_t)d * d);
@@ -190,8 +194,8 @@ int orc_compress(const uint16_t* raw, int64_t raw_bstride, int B, int d, int m,
   int err = ORC_OK;
 #pragma omp parallel
   {
-    double* x = (double*)malloc(sizeof(double) * (size_t)m * d);
-    double* g = (double*)malloc(sizeof(double) * (size_t)m);
+    double* x = (double*)malloc(sizeof(double) * (size_t)span * d);
+    double* g = (double*)malloc(sizeof(double) * (size_t)span);
     if (!x || !g) {
 #pragma omp atomic write
       err = ORC_ERR_NOMEM;
@@ -200,24 +204,27 @@ int orc_compress(const uint16_t* raw, int64_t raw_bstride, int B, int d, int m,
     for (int b = 0; b < B; ++b) {
       for (int jj = 0; jj < n_blocks; ++jj) {
         if (!x || !g) continue;
-        int64_t j = block_begin + jj;
-        const uint16_t* xb = raw + (int64_t)b * raw_bstride + j * m * d;
-        orc_bf16_decode_array(xb, x, (int64_t)m * d);
+        const int64_t j = block_begin + jj;
+        const int64_t p0 = j * m + m - span;  /* position of bias row 0 */
+        const int i0 = p0 < 0 ? (int)(-p0) : 0; /* first bias row with a token */
+        const int n = span - i0;
+        const uint16_t* xb = raw + (int64_t)b * raw_bstride + (p0 + i0) * d;
+        orc_bf16_decode_array(xb, x, (int64_t)n * d);
         double* yo = y + ((int64_t)b * n_blocks + jj) * d;
         for (int c = 0; c < d; ++c) {
-          for (int i = 0; i < m; ++i) {
+          for (int k = 0; k < n; ++k) {
             double s = 0.0;
-            for (int e = 0; e < d; ++e) s += Wd[(int64_t)c * d + e] * x[(int64_t)i * d + e];
-            g[i] = s + (double)pos_bias[(int64_t)i * d + c];
+            for (int e = 0; e < d; ++e) s += Wd[(int64_t)c * d + e] * x[(int64_t)k * d + e];
+            g[k] = s + (double)pos_bias[(int64_t)(i0 + k) * d + c];
           }
           double gmax = g[0];
-          for (int i = 1; i < m; ++i)
-            if (g[i] > gmax) gmax = g[i];
+          for (int k = 1; k < n; ++k)
+            if (g[k] > gmax) gmax = g[k];
           double den = 0.0, num = 0.0;
-          for (int i = 0; i < m; ++i) {
-            double a = exp(g[i] - gmax);
+          for (int k = 0; k < n; ++k) {
+            double a = exp(g[k] - gmax);
             den += a;
-            num += a * x[(int64_t)i * d + c];
+            num += a * x[(int64_t)k * d + c];
           }
           yo[c] = num / den;
         }
@@ -228,6 +235,13 @@ int orc_compress(const uint16_t* raw, int64_t raw_bstride, int B, int d, int m,
   }
   free(Wd);
   return err;
+}
+
+/* The non-overlapping blocks: span = m (pos_bias [m][d]). */
+int orc_compress(const uint16_t* raw, int64_t raw_bstride, int B, int d, int m,
+                 int block_begin, int n_blocks, const uint16_t* W, const float* pos_bias,
+                 double* y) {
+  return orc_compress_span(raw, raw_bstride, B, d, m, m, block_begin, n_blocks, W, pos_bias, y);
 }
 
 /* ------------------------------------------------------------------------ */

@@ -10,16 +10,20 @@
 
 namespace csa {
 
-cudaError_t ensure_smem_attr(const void* func, int bytes) {
+// Function attributes are per device: set once per (function, device, size),
+// under a lock (the library may be called from several host threads).
+cudaError_t ensure_smem_attr(const void* func, int bytes, bool big_clusters) {
   static std::mutex mu;
-  static std::set<std::tuple<const void*, int, int>> done;
+  static std::set<std::tuple<const void*, int, int, bool>> done;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(mu);
-  if (done.count(std::make_tuple(func, dev, bytes))) return cudaSuccess;
+  if (done.count(std::make_tuple(func, dev, bytes, big_clusters))) return cudaSuccess;
   e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess) done.insert(std::make_tuple(func, dev, bytes));
+  if (e == cudaSuccess && big_clusters)
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e == cudaSuccess) done.insert(std::make_tuple(func, dev, bytes, big_clusters));
   return e;
 }
 

@@ -37,6 +37,8 @@
 // on a barrier.  Every mbarrier wait is bounded; on timeout the CTA records
 // CSA_EW_TIMEOUT in the error word, still reaches every barrier, and frees its
 // TMEM.
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "tc.cuh"
@@ -771,11 +773,13 @@ cudaLaunchConfig_t launch_cfg(int n_split, int n_query, cudaStream_t st,
 // Clusters of size n the device keeps resident at once (cached per device).
 template <int M>
 int active_clusters(int n) {
+  static std::mutex mu;  // callers may be on several host threads
   static int cache[16][kMaxCluster + 1];
   static bool init = false;
   if (n <= 1) return 1 << 20;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev >= 16) return 0;
+  std::lock_guard<std::mutex> lock(mu);
   if (!init) {
     for (auto& row : cache)
       for (int& v : row) v = -1;
@@ -783,9 +787,7 @@ int active_clusters(int n) {
   }
   int& c = cache[dev][n];
   if (c < 0) {
-    if (n > 8)
-      cudaFuncSetAttribute(attn_tc_kernel<M>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    ensure_smem_attr((const void*)attn_tc_kernel<M>, Cfg<M>::kSmemBytes);
+    ensure_smem_attr((const void*)attn_tc_kernel<M>, Cfg<M>::kSmemBytes, true);
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = launch_cfg<M>(n, 1, nullptr, attr, false);
     int clusters = 0;
@@ -799,7 +801,7 @@ int active_clusters(int n) {
 
 template <int M>
 cudaError_t launch_tc(AttnArgs a, const Maps& maps, void* ws, cudaStream_t st) {
-  cudaError_t e = ensure_smem_attr((const void*)attn_tc_kernel<M>, Cfg<M>::kSmemBytes);
+  cudaError_t e = ensure_smem_attr((const void*)attn_tc_kernel<M>, Cfg<M>::kSmemBytes, true);
   if (e != cudaSuccess) return e;
   // Pick the split count: at most one cluster of splits per query, every
   // cluster resident at once (one wave), about one CTA per SM in total.

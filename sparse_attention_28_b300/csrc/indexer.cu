@@ -528,15 +528,8 @@ cudaError_t launch_indexer_topk(const IndexerArgs& a, void* ws, cudaStream_t st)
                        : per == 16 ? (const void*)topk_select_kernel<16>
                                    : (const void*)topk_select_kernel<32>;
   {
-    static bool attrs[3] = {false, false, false};
-    const int ix = per == 8 ? 0 : (per == 16 ? 1 : 2);
-    if (!attrs[ix]) {
-      cudaError_t e = ensure_smem_attr(sel_fn, sel_smem_bytes(per));
-      if (e != cudaSuccess) return e;
-      e = cudaFuncSetAttribute(sel_fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-      if (e != cudaSuccess) return e;
-      attrs[ix] = true;
-    }
+    const cudaError_t e = ensure_smem_attr(sel_fn, sel_smem_bytes(per), true);
+    if (e != cudaSuccess) return e;
   }
   for (int q0 = 0; q0 < a.n_query; q0 += kQueryChunk) {
     const int qc = (a.n_query - q0 < kQueryChunk) ? a.n_query - q0 : kQueryChunk;

@@ -11,7 +11,9 @@
 namespace csa {
 
 // Sets the dynamic shared-memory limit of a kernel once per device.
-cudaError_t ensure_smem_attr(const void* func, int bytes);
+// sets the dynamic shared memory limit (and, with big_clusters, permission
+// for clusters above 8 CTAs) once per function and device; thread-safe
+cudaError_t ensure_smem_attr(const void* func, int bytes, bool big_clusters = false);
 
 // ---------------------------------------------------------------- attention
 struct AttnArgs {

@@ -16,8 +16,9 @@ RNG = np.random.default_rng(1234)
 
 
 def _golden(name):
+    e = math.e
     consts = {"ln3": math.log(3), "ln4": math.log(4), "ln5": math.log(5),
-              "2/(e+1)": 2 / (math.e + 1)}
+              "2/(e+1)": 2 / (e + 1), "(e+9e^3)/(e+3e^3)": (e + 9 * e**3) / (e + 3 * e**3)}
     out = {}
     for line in open(os.path.join(GOLDEN, name)):
         line = line.strip()
@@ -125,6 +126,55 @@ def test_compress_zero_gate_is_block_mean():
     x = bits_to_f64(raw)
     ref = x[:, 4:28].reshape(B, 6, m, d).mean(axis=2)
     np.testing.assert_allclose(y, ref, rtol=1e-14, atol=1e-15)
+
+
+def test_compress_overlap_hand_example():
+    g = _golden("compress_overlap_hand.txt")
+    raw = bf16_bits(g["x"]).reshape(1, 2, 1)
+    bias = g["pos_bias"].astype(np.float32).reshape(2, 1)
+    for key, w in (("y_W0", 0.0), ("y_W1", 1.0)):
+        y = oracle.compress(raw, bf16_bits(np.array([[w]])), bias, m=1, block_begin=0,
+                            n_blocks=2)
+        np.testing.assert_allclose(y[0, :, 0], g[key], rtol=1e-7)
+
+
+def test_compress_overlap_zero_gate_is_span_mean_clipped_at_zero():
+    # m = 4, span = 10: block j averages positions max(0, 4j-6) .. 4j+3
+    B, L, d, m, span = 2, 32, 8, 4, 10
+    raw = _rand_bf16((B, L, d))
+    y = oracle.compress(raw, np.zeros((d, d), np.uint16), np.zeros((span, d), np.float32), m,
+                        0, 8)
+    x = bits_to_f64(raw)
+    for j in range(8):
+        lo, hi = max(0, 4 * j - 6), 4 * j + 4
+        np.testing.assert_allclose(y[:, j], x[:, lo:hi].mean(axis=1), rtol=1e-14, atol=1e-15)
+
+
+def test_compress_overlap_one_hot_bias_reaches_into_the_previous_block():
+    # bias row i belongs to position j*m + m - span + i: rows below span - m
+    # pick tokens of the previous block
+    B, d, m, span = 2, 8, 4, 8
+    raw = _rand_bf16((B, 4 * m, d))
+    pick = RNG.integers(0, span, d)
+    bias = np.zeros((span, d), np.float32)
+    bias[pick, np.arange(d)] = 1e4
+    y = oracle.compress(raw, _rand_bf16((d, d), 0.3), bias, m, 1, 3)
+    x = bits_to_f64(raw)
+    for jj, j in enumerate(range(1, 4)):
+        pos = j * m + m - span + pick
+        np.testing.assert_array_equal(y[:, jj], x[:, pos, np.arange(d)])
+
+
+def test_compress_overlap_is_convex_over_its_span():
+    B, d, m, span = 3, 16, 4, 12
+    raw = _rand_bf16((B, 40, d), 2.0)
+    bias = RNG.standard_normal((span, d)).astype(np.float32) * 3
+    y = oracle.compress(raw, _rand_bf16((d, d), 0.5), bias, m, 0, 10)
+    x = bits_to_f64(raw)
+    for j in range(10):
+        win = x[:, max(0, j * m + m - span):j * m + m]
+        assert np.all(y[:, j] >= win.min(axis=1) - 1e-12)
+        assert np.all(y[:, j] <= win.max(axis=1) + 1e-12)
 
 
 def test_compress_m1_is_identity():
