@@ -87,8 +87,12 @@ def algorithmic(wl) -> dict:
     nvis = [min(wl.N_cap, (wl.L + t + 1) // wl.m) for t in range(wl.T)]
     idx_f = wl.B * sum(nvis) * wl.H_I * wl.d_I * 2
     att_f = wl.B * wl.T * H * (wl.k + W) * D * 4
+    # compression: each of the T/m new blocks evaluates span gate logits per
+    # channel, a d x d contraction per token of its span, for K, V (d = D)
+    # and the indexer keys (d = d_I)
+    cmp_f = wl.B * (wl.T // wl.m) * wl.cspan * (2 * D * D + wl.d_I * wl.d_I) * 2
     return {"indexer_topk": {"flops": idx_f}, "attention": {"flops": att_f},
-            "compress": {"flops": 3 * wl.B * wl.T * D * D * 2}}
+            "compress": {"flops": cmp_f}}
 
 
 def kernel_algorithmic(wl, name: str) -> dict:
@@ -254,7 +258,7 @@ class OracleRunner:
             return
         # prefill sample: the sampled tokens' blocks, scores, top-k, attention
         for s in ("k", "v", "idx"):
-            o.quantize_bf16(o.compress(a["raw_new_" + s], *a["gate_" + s], wl.m, 0,
+            o.quantize_bf16(o.compress(a["raw_new_" + s], *a["gate_" + s], wl.m, a["block0"],
                                        a["n_blocks"]))
         sc, nv = o.indexer_scores(a["q_idx"], a["w"], a["k_idx"], a["q_pos"], a["n_cmp"], wl.m)
         idx = o.topk(sc, nv, wl.k)
@@ -300,6 +304,7 @@ def main():
     local = int(os.environ.get("LOCAL_RANK", "0"))
     wl = synth.WORKLOADS[args.workload]
     cfg = {"workload": wl.name, "kind": wl.kind, "B": wl.B, "L": wl.L, "T": wl.T, "m": wl.m,
+           "span": wl.cspan,
            "H": wl.H, "D": wl.D, "k": wl.k, "window": wl.W, "H_I": wl.H_I, "d_I": wl.d_I,
            "indexer_dtype": "e4m3" if wl.idx_fp8 else "bf16",
            "stream_compress": wl.stream_compress, "parallelism": f"replicas{world}"}

@@ -102,6 +102,25 @@ CSA_API int csa_compress_kv(const void* raw, int64_t raw_bstride, int64_t raw_ca
                     int64_t scale_bstride, int32_t* err_word, void* stream);
 
 /* ------------------------------------------------------------------------
+ * a1 with overlapping blocks.  The hyper.ai DeepSeek-V4 page (Method, HCA
+ * paragraph) says HCA compresses "without overlapping compression", which
+ * this library reads as: CSA's blocks may overlap.  Block j keeps its stride
+ * m, its position in the output and its visibility rule (it ends at token
+ * j*m + m - 1), but is compressed from the `span` raw tokens ending there:
+ *     p_i = j*m + m - span + i,  0 <= i < span,  negative positions left out
+ *     g[i][c] = sum_e W[c][e] x[p_i][e] + pos_bias[i][c];  softmax over i
+ *     y[j][c] = sum_i a[i][c] x[p_i][c]
+ * Arguments as csa_compress_kv, plus span (m <= span <= 256) with
+ * pos_bias fp32 [span][d] (row i belongs to position p_i).  The raw ring
+ * must hold the span: raw_cap >= span.  span == m is csa_compress_kv.
+ * ---------------------------------------------------------------------- */
+CSA_API int csa_compress_kv_span(const void* raw, int64_t raw_bstride, int64_t raw_cap, int B,
+                                 int d, int m, int span, int block_begin, int n_blocks,
+                                 const void* W, const float* pos_bias, void* out,
+                                 int64_t out_bstride, int out_dtype, float* out_scale,
+                                 int64_t scale_bstride, int32_t* err_word, void* stream);
+
+/* ------------------------------------------------------------------------
  * a2 + a3. Lightning-Indexer scores and exact top-k.
  *
  * Sources: hyper.ai DeepSeek-V4 page, Method ("A Lightning Indexer then

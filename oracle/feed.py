@@ -95,10 +95,15 @@ def oracle_inputs(wl, inp: dict, n_units: int, seqs=None, tokens=None) -> dict:
     a["raw_base"] = int(inp["raw_base"])
     nb = max(1, len(toks) // wl.m)
     a["n_blocks"] = nb
+    # rows of the new blocks, plus the span - m older rows the first one reads
+    # (a whole number of blocks here: block_begin = pre / m)
+    pre = wl.cspan - wl.m
+    assert pre % wl.m == 0
+    a["block0"] = pre // wl.m
     first = wl.W - 1  # raw_k row of the first new token
-    a["raw_new_k"] = a["k_raw"][:, first:first + nb * wl.m]
-    a["raw_new_v"] = a["v_raw"][:, first:first + nb * wl.m]
-    a["raw_new_idx"] = u16(inp["raw_idx"][:, : nb * wl.m])
+    a["raw_new_k"] = a["k_raw"][:, first - pre:first + nb * wl.m]
+    a["raw_new_v"] = a["v_raw"][:, first - pre:first + nb * wl.m]
+    a["raw_new_idx"] = u16(inp["raw_idx"][:, : pre + nb * wl.m])
     for s in ("k", "v", "idx"):
         Wg, pb = inp["gate_" + s]
         a["gate_" + s] = (u16(Wg), f32(pb))
@@ -131,10 +136,12 @@ def fill_new_entries(wl, inp: dict, a: dict) -> dict:
     if wl.kind == "csa_prefill":
         n_old, n_new = wl.L // m, wl.T // m
         first = wl.W - 1
-        raws = {"k": a["k_raw"][:, first:first + wl.T], "v": a["v_raw"][:, first:first + wl.T],
-                "idx": u16(inp["raw_idx"])}
+        pre = wl.cspan - m  # older rows the first new block's span reads
+        assert pre % m == 0
+        raws = {"k": a["k_raw"][:, first - pre:first + wl.T],
+                "v": a["v_raw"][:, first - pre:first + wl.T], "idx": u16(inp["raw_idx"])}
         for s, dst in (("k", "k_cmp"), ("v", "v_cmp"), ("idx", "k_idx")):
-            y = compress(raws[s], *a["gate_" + s], m, 0, n_new)
+            y = compress(raws[s], *a["gate_" + s], m, pre // m, n_new)
             a[dst] = a[dst].copy()
             a[dst][:, n_old:n_old + n_new] = quantize_bf16(y)
             res[s] = y

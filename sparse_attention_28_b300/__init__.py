@@ -8,7 +8,7 @@ the library is missing, every call raises.
 
 Calls (same names as the C ABI, without the prefix where it reads better):
 
-* :func:`compress_kv`            -- csa_compress_kv
+* :func:`compress_kv`            -- csa_compress_kv (csa_compress_kv_span for overlap)
 * :func:`indexer_scores`         -- csa_indexer_scores
 * :func:`indexer_topk`           -- csa_indexer_topk
 * :func:`sparse_attn_decode`     -- csa_sparse_attn_decode
@@ -36,7 +36,7 @@ ABI_SYMBOLS = (
     "csa_status_str", "csa_abi_version", "csa_compress_kv", "csa_indexer_topk_workspace",
     "csa_indexer_topk", "csa_attn_workspace", "csa_sparse_attn_decode",
     "csa_sparse_attn_prefill", "hca_dense_attn_decode", "csa_indexer_topk_static",
-    "csa_indexer_scores",
+    "csa_indexer_scores", "csa_compress_kv_span",
 )
 
 # capacity of the library-owned scratch behind indexer_topk_static (bytes)
@@ -70,6 +70,9 @@ def lib() -> ctypes.CDLL:
             L.csa_compress_kv.argtypes = [P, I64, I64, I, I, I, I, I, P, P, P, I64, I, P, I64, P,
                                           P]
             L.csa_compress_kv.restype = I
+            L.csa_compress_kv_span.argtypes = [P, I64, I64, I, I, I, I, I, I, P, P, P, I64, I, P,
+                                               I64, P, P]
+            L.csa_compress_kv_span.restype = I
             L.csa_indexer_topk_workspace.argtypes = [I, I, I, I]
             L.csa_indexer_topk_workspace.restype = SZ
             L.csa_indexer_topk.argtypes = [P, P, P, P, I64, P, I64, I, P, P, I, I, I, I, I, I, I,
@@ -146,9 +149,12 @@ def compress_kv(raw, W, pos_bias, m: int, block_begin: int, n_blocks: int, out,
     """Compress blocks [block_begin, block_begin+n_blocks) of every sequence.
 
     raw: bf16 [B, R, d], a ring of R rows (position p at row p mod R; a
-    full-length cache is R > every position); W: bf16 [d, d]; pos_bias: fp32 [m, d];
-    out: bf16 [B, N_cap, d] or uint8 [B, N_cap, d] (E4M3 codes, then
-    out_scale fp32 [B, N_cap] is required).  Writes in place; returns out.
+    full-length cache is R > every position); W: bf16 [d, d]; pos_bias: fp32
+    [span, d] with span >= m: block j is compressed from the span raw tokens
+    ending at its last token (span == m: non-overlapping blocks, span > m:
+    overlapping compression); out: bf16 [B, N_cap, d] or uint8 [B, N_cap, d]
+    (E4M3 codes, then out_scale fp32 [B, N_cap] is required).  Writes in
+    place; returns out.
     """
     _cuda(raw, "raw", torch.bfloat16)
     _cuda(W, "W", torch.bfloat16)
@@ -161,12 +167,19 @@ def compress_kv(raw, W, pos_bias, m: int, block_begin: int, n_blocks: int, out,
     if fp8:
         _cuda(out_scale, "out_scale", torch.float32)
         _need(out_scale.dim() == 2 and out_scale.stride(1) == 1, "out_scale [B, N_cap]")
-    st = lib().csa_compress_kv(
-        _p(raw), _bstride(raw), raw.shape[1], B, d, m, block_begin, n_blocks, _p(W), _p(pos_bias),
-        _p(out),
-        _bstride(out), CSA_FP8_E4M3 if fp8 else CSA_BF16, _p(out_scale) if fp8 else None,
-        out_scale.stride(0) if fp8 else 0, _p(err_word), _stream(raw.device))
-    _check(st, "csa_compress_kv")
+    _need(pos_bias.dim() == 2 and pos_bias.shape[1] == d, "pos_bias [span, d]")
+    span = pos_bias.shape[0]
+    common = (_p(W), _p(pos_bias), _p(out), _bstride(out), CSA_FP8_E4M3 if fp8 else CSA_BF16,
+              _p(out_scale) if fp8 else None, out_scale.stride(0) if fp8 else 0,
+              _p(err_word), _stream(raw.device))
+    if span == m:
+        st = lib().csa_compress_kv(_p(raw), _bstride(raw), raw.shape[1], B, d, m, block_begin,
+                                   n_blocks, *common)
+        _check(st, "csa_compress_kv")
+    else:
+        st = lib().csa_compress_kv_span(_p(raw), _bstride(raw), raw.shape[1], B, d, m, span,
+                                        block_begin, n_blocks, *common)
+        _check(st, "csa_compress_kv_span")
     return out
 
 

@@ -91,19 +91,22 @@ const char* csa_status_str(int status) {
 int csa_abi_version(void) { return 1; }
 
 // ---------------------------------------------------------------- a1
-int csa_compress_kv(const void* raw, int64_t raw_bstride, int64_t raw_cap, int B, int d, int m,
-                    int block_begin, int n_blocks, const void* W, const float* pos_bias, void* out,
-                    int64_t out_bstride, int out_dtype, float* out_scale, int64_t scale_bstride,
-                    int32_t* err_word, void* stream) {
+int csa_compress_kv_span(const void* raw, int64_t raw_bstride, int64_t raw_cap, int B, int d,
+                         int m, int span, int block_begin, int n_blocks, const void* W,
+                         const float* pos_bias, void* out, int64_t out_bstride, int out_dtype,
+                         float* out_scale, int64_t scale_bstride, int32_t* err_word,
+                         void* stream) {
   (void)err_word;
-  if (B < 0 || d <= 0 || m <= 0 || block_begin < 0 || n_blocks < 0) return CSA_ERR_INVALID_ARG;
+  if (B < 0 || d <= 0 || m <= 0 || span < m || block_begin < 0 || n_blocks < 0)
+    return CSA_ERR_INVALID_ARG;
   if (out_dtype != CSA_BF16 && out_dtype != CSA_FP8_E4M3) return CSA_ERR_UNSUPPORTED;
-  if ((d != 64 && d != 128) || m > 256) return CSA_ERR_UNSUPPORTED;
+  if ((d != 64 && d != 128) || span > 256) return CSA_ERR_UNSUPPORTED;
   if (B == 0 || n_blocks == 0) return CSA_OK;
   if (!raw || !W || !pos_bias || !out) return CSA_ERR_INVALID_ARG;
   if (!aligned16(raw) || !aligned16(W) || !aligned4(pos_bias)) return CSA_ERR_INVALID_ARG;
   const int64_t end_block = (int64_t)block_begin + n_blocks;
-  if (raw_cap < m || raw_bstride % 8 != 0 || raw_cap * d > raw_bstride) return CSA_ERR_INVALID_ARG;
+  if (raw_cap < span || raw_bstride % 8 != 0 || raw_cap * d > raw_bstride)
+    return CSA_ERR_INVALID_ARG;
   if (end_block * d > out_bstride) return CSA_ERR_INVALID_ARG;
   if (out_dtype == CSA_FP8_E4M3) {
     if (!out_scale || !aligned4(out_scale) || end_block > scale_bstride) return CSA_ERR_INVALID_ARG;
@@ -115,6 +118,7 @@ int csa_compress_kv(const void* raw, int64_t raw_bstride, int64_t raw_cap, int B
   a.B = B;
   a.d = d;
   a.m = m;
+  a.span = span;
   a.block_begin = block_begin;
   a.n_blocks = n_blocks;
   a.W = reinterpret_cast<const bf16*>(W);
@@ -125,6 +129,15 @@ int csa_compress_kv(const void* raw, int64_t raw_bstride, int64_t raw_cap, int B
   a.out_scale = out_scale;
   a.scale_bstride = scale_bstride;
   return cuda_status(launch_compress(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int csa_compress_kv(const void* raw, int64_t raw_bstride, int64_t raw_cap, int B, int d, int m,
+                    int block_begin, int n_blocks, const void* W, const float* pos_bias, void* out,
+                    int64_t out_bstride, int out_dtype, float* out_scale, int64_t scale_bstride,
+                    int32_t* err_word, void* stream) {
+  return csa_compress_kv_span(raw, raw_bstride, raw_cap, B, d, m, m, block_begin, n_blocks, W,
+                              pos_bias, out, out_bstride, out_dtype, out_scale, scale_bstride,
+                              err_word, stream);
 }
 
 // ---------------------------------------------------------------- a2 + a3

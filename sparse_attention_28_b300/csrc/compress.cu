@@ -3,18 +3,20 @@
 // Method: hyper.ai DeepSeek-V4 page, Method -- CSA "compresses every m tokens
 // into a single entry using learnable compression weights and positional
 // biases"; HCA consolidates every m' tokens "without overlapping
-// compression".  Operator (this library's reading of that sentence), for
-// block j and channel c:
-//     g[i][c] = sum_e W[c][e] x[j*m+i][e] + pos_bias[i][c]
-//     y[j][c] = sum_i softmax_i(g[.][c])[i] * x[j*m+i][c]
-// Output: bf16 (nearest even), or E4M3 with one fp32 scale per entry,
-// scale = max_c |y| / 448 (1 if all zero), code = nearest-even E4M3 of
-// y / scale, saturating.
+// compression" (read as: CSA's blocks may overlap).  Operator (this
+// library's reading of those sentences): block j (stride m) is compressed
+// from the span >= m raw tokens ending at its last token, positions
+// p_i = j*m + m - span + i (the non-negative ones); for channel c
+//     g[i][c] = sum_e W[c][e] x[p_i][e] + pos_bias[i][c]
+//     y[j][c] = sum_i softmax_i(g[.][c])[i] * x[p_i][c]
+// span = m is the non-overlapping operator.  Output: bf16 (nearest even), or
+// E4M3 with one fp32 scale per entry, scale = max_c |y| / 448 (1 if all
+// zero), code = nearest-even E4M3 of y / scale, saturating.
 //
 // One CTA per (block, sequence), one thread per output channel.  The
-// block's m raw rows (fp32) are staged in shared memory; each thread reads
-// its own W row straight from global memory (all of it in flight at once:
-// no other thread uses it) and forms its channel's m gate logits 16
+// block's span raw rows (fp32) are staged in shared memory; each thread
+// reads its own W row straight from global memory (all of it in flight at
+// once: no other thread uses it) and forms its channel's gate logits 16
 // positions at a time (x rows as shared-memory broadcasts), folded into an
 // online softmax.
 #include "common.cuh"
@@ -30,7 +32,7 @@ template <int D>
 __global__ void __launch_bounds__(D) compress_kernel(CompressArgs a) {
   pdl_trigger();
   pdl_wait();
-  extern __shared__ __align__(16) float xs[];  // [m][D]
+  extern __shared__ __align__(16) float xs[];  // [span][D]
   __shared__ float red[D / 32];
   const int c = threadIdx.x;
   const int b = blockIdx.y;
@@ -42,17 +44,23 @@ __global__ void __launch_bounds__(D) compress_kernel(CompressArgs a) {
   for (int e8 = 0; e8 < D / 8; ++e8)
     wrow[e8] = __ldg(reinterpret_cast<const uint4*>(a.W + (int64_t)c * D) + e8);
   const bf16* xb = a.raw + (int64_t)b * a.raw_bstride;
-  const int64_t r0 = (j * m) % a.raw_cap;  // ring row of the block's first token
-  for (int i = 0; i < m; ++i) {
-    int64_t r = r0 + i;
+  // the span's tokens: bias row i belongs to position j*m + m - span + i; rows
+  // of negative positions are left out (k counts the rows that remain)
+  const int64_t p0 = j * m + m - a.span;
+  const int i_off = p0 < 0 ? (int)(-p0) : 0;
+  const int np = a.span - i_off;
+  const int64_t r0 = (p0 + i_off) % a.raw_cap;  // ring row of the first token
+  for (int k = 0; k < np; ++k) {
+    int64_t r = r0 + k;
     if (r >= a.raw_cap) r -= a.raw_cap;
-    xs[i * D + c] = __bfloat162float(xb[r * D + c]);
+    xs[k * D + c] = __bfloat162float(xb[r * D + c]);
   }
   __syncthreads();
+  const float* bias = a.pos_bias + (int64_t)i_off * D;
 
   float mx = -INFINITY, den = 0.f, num = 0.f;
-  for (int i0 = 0; i0 < m; i0 += kPosChunk) {
-    const int n = (m - i0 < kPosChunk) ? m - i0 : kPosChunk;
+  for (int i0 = 0; i0 < np; i0 += kPosChunk) {
+    const int n = (np - i0 < kPosChunk) ? np - i0 : kPosChunk;
     float gl[kPosChunk];
 #pragma unroll
     for (int ii = 0; ii < kPosChunk; ++ii) gl[ii] = 0.f;
@@ -78,7 +86,7 @@ __global__ void __launch_bounds__(D) compress_kernel(CompressArgs a) {
 #pragma unroll
     for (int ii = 0; ii < kPosChunk; ++ii) {
       if (ii < n) {
-        const float gi = gl[ii] + __ldg(a.pos_bias + (int64_t)(i0 + ii) * D + c);
+        const float gi = gl[ii] + __ldg(bias + (int64_t)(i0 + ii) * D + c);
         const float xv = xs[(i0 + ii) * D + c];
         if (gi > mx) {
           const float r = expf(mx - gi);
@@ -124,11 +132,11 @@ cudaError_t launch_compress(const CompressArgs& a, cudaStream_t st) {
   if (a.d == 128) {
     e = ensure_smem_attr((const void*)compress_kernel<128>, 256 * 128 * 4);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(compress_kernel<128>, grid, dim3(128), a.m * 128 * 4, st, a);
+    e = launch_pdl(compress_kernel<128>, grid, dim3(128), a.span * 128 * 4, st, a);
   } else {
     e = ensure_smem_attr((const void*)compress_kernel<64>, 256 * 64 * 4);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(compress_kernel<64>, grid, dim3(64), a.m * 64 * 4, st, a);
+    e = launch_pdl(compress_kernel<64>, grid, dim3(64), a.span * 64 * 4, st, a);
   }
   return e;
 }

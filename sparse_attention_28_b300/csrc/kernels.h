@@ -99,6 +99,7 @@ struct CompressArgs {
   int64_t raw_bstride;
   int64_t raw_cap;  // ring of raw_cap rows: position p at row p % raw_cap
   int B, d, m, block_begin, n_blocks;
+  int span;  // raw tokens per block, ending at its last token (span >= m; m: no overlap)
   const __nv_bfloat16* W;
   const float* pos_bias;
   void* out;

@@ -250,10 +250,12 @@ class CsaPrefillStep(_Step):
         self.idx_raw = _nan((B, R, wl.d_I), torch.bfloat16, dev)
         base = L - (W - 1)
         rk, rv, ri = g("raw_k"), g("raw_v"), g("raw_idx")
+        pre = wl.cspan - m  # rows before the first new block that its span reads
+        assert pre <= W - 1, "the ring holds the window, so at most W-1 older rows"
         for b in range(B):
             _ring_put(self.k_raw, b, range(base, L + T), rk[b])
             _ring_put(self.v_raw, b, range(base, L + T), rv[b])
-            _ring_put(self.idx_raw, b, range(L, L + T), ri[b])
+            _ring_put(self.idx_raw, b, range(L - pre, L + T), ri[b])
         self.gates = {s: tuple(t.to(dev) for t in inp["gate_" + s]) for s in ("k", "v", "idx")}
         self.block0, self.n_new = n_old, T // m
         self.idx = torch.empty((B, T, wl.k), dtype=torch.int32, device=dev)

@@ -56,6 +56,12 @@ class Workload:
     d_I: int = D_IDX
     sink: bool = True
     seq_lens: Optional[tuple] = None  # ragged decode lengths (default: all L)
+    span: int = 0            # raw tokens per compressed block (0: m, no overlap)
+
+    @property
+    def cspan(self) -> int:
+        """Tokens each compressed block is formed from (>= m; m: no overlap)."""
+        return self.span or self.m
 
     @property
     def N_cap(self) -> int:
@@ -80,6 +86,10 @@ WORKLOADS = {
                                k=2048, T=4096),
     "csa_decode_1m_fp8": Workload("csa_decode_1m_fp8", "csa_decode", B=8, L=1048576, m=4,
                                   H=64, k=2048, idx_fp8=True, stream_compress=True),
+    # overlapping compression: each block formed from 2m tokens (its own and
+    # the previous block's)
+    "csa_prefill_4k_overlap": Workload("csa_prefill_4k_overlap", "csa_prefill", B=1, L=262144,
+                                       m=4, H=64, k=2048, T=4096, span=8),
 }
 
 
@@ -121,7 +131,8 @@ def make_inputs(wl: Workload, seed: int = 0, device="cpu") -> dict:
     Prefill keys: q [B,T,H,D]; q_idx [B,T,H_I,d_I]; w [B,T,H_I]; q_pos [B,T];
     k_cmp, v_cmp, k_idx with the L/m cached entries (the T/m new ones are left
     for the compression step, zero here); raw_{k,v} [B,W-1+T,D] for positions
-    L-W+1 .. L+T-1; raw_idx [B,T,d_I] for positions L .. L+T-1; gates.
+    L-W+1 .. L+T-1; raw_idx [B,span-m+T,d_I] for positions idx_base = L-(span-m)
+    .. L+T-1 (span = m without overlap); gates (pos_bias [span, d]).
     """
     B, H, D, W, m = wl.B, wl.H, wl.D, wl.W, wl.m
     dev = device
@@ -135,7 +146,7 @@ def make_inputs(wl: Workload, seed: int = 0, device="cpu") -> dict:
 
     def gate(d, tid):
         return (randn((d, d), seed, tid, dev, scale=1.0 / math.sqrt(d)),
-                randn((m, d), seed, tid + 1, dev, dtype=torch.float32))
+                randn((wl.cspan, d), seed, tid + 1, dev, dtype=torch.float32))
 
     if wl.kind in ("csa_decode", "hca_decode"):
         lens = torch.tensor(wl.lens, dtype=torch.int32)
@@ -157,6 +168,7 @@ def make_inputs(wl: Workload, seed: int = 0, device="cpu") -> dict:
                 out["k_idx"] = randn((B, N_cap, wl.d_I), seed, 9, dev)
                 out["q_scale"] = out["k_scale"] = None
         if wl.stream_compress:
+            assert wl.cspan == m, "streaming compression: non-overlapping blocks"
             # the newest block's raw K/V rows are the last m window rows;
             # its raw indexer-key rows have no other source
             out["raw_new_idx"] = randn((B, m, wl.d_I), seed, 12, dev)
@@ -180,7 +192,9 @@ def make_inputs(wl: Workload, seed: int = 0, device="cpu") -> dict:
     out["k_cmp"], out["v_cmp"], out["k_idx"] = k_cmp, v_cmp, k_idx
     out["raw_k"] = randn((B, W - 1 + T, D), seed, 5, dev)
     out["raw_v"] = randn((B, W - 1 + T, D), seed, 6, dev)
-    out["raw_idx"] = randn((B, T, wl.d_I), seed, 12, dev)
+    pre = wl.cspan - m  # indexer-key rows before the first new block that its span reads
+    out["raw_idx"] = randn((B, pre + T, wl.d_I), seed, 12, dev)
+    out["idx_base"] = L - pre
     out["raw_base"] = L - (W - 1)
     out["q_idx"] = randn((B, T, wl.H_I, wl.d_I), seed, 8, dev)
     out["w"] = randn((B, T, wl.H_I), seed, 7, dev, dtype=torch.float32)

@@ -113,6 +113,21 @@ def test_compress_rejects():
     assert call(B=0) == 0 and call(nb=0) == 0
 
 
+def test_compress_span_rejects():
+    L = csa.lib()
+
+    def call(**over):
+        a = dict(raw=FAKE, rbs=64 * 128, rcap=64, B=2, d=128, m=4, span=8, b0=0, nb=16, W=FAKE,
+                 pb=FAKE, out=FAKE, obs=16 * 128, dt=0, sc=None, sbs=0, err=None, st=None)
+        a.update(over)
+        return L.csa_compress_kv_span(*a.values())
+
+    assert call(span=3) == 1          # shorter than the stride
+    assert call(span=257) == 2        # more rows than the kernel stages
+    assert call(rcap=7) == 1          # the ring must hold the whole span
+    assert call(B=0, raw=None) == 0
+
+
 def test_attention_workspace_only_for_split_queries():
     # partial rows + lse (129 fp32 per head) for every split of every query
     # when a query can get several splits (fewer queries than SMs / 2); none

@@ -76,6 +76,22 @@ def test_kernel_algorithmic_bytes():
     assert bench.kernel_algorithmic(hca, "attention") == bench.algorithmic(hca)["attention"]
 
 
+def test_oracle_sample_of_overlapping_prefill():
+    # the CPU baseline's bounded sample of the overlap workload: its blocks
+    # read span - m older rows (whole blocks), which the sample includes
+    sys.path.insert(0, ROOT)
+    import bench
+    import synth
+    wl = synth.WORKLOADS["csa_prefill_4k_overlap"]
+    assert wl.cspan == 2 * wl.m
+    inp = synth.make_inputs(wl, seed=0, device="cpu")
+    assert inp["raw_idx"].shape[1] == wl.T + wl.m and inp["idx_base"] == wl.L - wl.m
+    assert inp["gate_k"][1].shape == (wl.cspan, wl.D)
+    run = bench.OracleRunner(wl, inp, 8)
+    assert run.arr["block0"] == 1 and run.arr["raw_new_k"].shape[1] == wl.m * (1 + 2)
+    run()
+
+
 def test_reference_arm_under_torchrun_prints_once_from_rank_0():
     port = _free_port()
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",

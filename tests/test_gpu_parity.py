@@ -65,6 +65,46 @@ def test_compress_parity(cuda_device, d, m, fp8):
     assert (out[:, :bb] == 0x7F).all() and (out[:, bb + nb:] == 0x7F).all()
 
 
+@pytest.mark.parametrize("d,m,span,fp8,ring", [(128, 4, 8, False, False), (64, 4, 12, True, False),
+                                                (128, 4, 16, True, True), (128, 1, 5, False, True)])
+def test_compress_overlap_parity(cuda_device, d, m, span, fp8, ring):
+    # blocks 0 .. 6: the first ones reach below position 0 (left out); ring:
+    # the raw rows sit in a ring just long enough for the blocks' spans
+    B, bb, nb = 3, 0, 7
+    N_cap = nb + 1
+    L = N_cap * m
+    raw = rnd((B, L, d), 11)
+    W = rnd((d, d), 12, 1 / math.sqrt(d))
+    pb = rnd((span, d), 13, dtype=torch.float32)
+    if ring:
+        R = nb * m + span - m + 1
+        src = torch.full((B, R, d), float("nan"), dtype=torch.bfloat16)
+        for p in range(max(0, bb * m + m - span), (bb + nb) * m):
+            src[:, p % R] = raw[:, p]
+    else:
+        src = raw
+    if fp8:
+        out = torch.full((B, N_cap, d), 0x7F, dtype=torch.uint8, device=DEV)
+        sc = torch.full((B, N_cap), float("nan"), device=DEV)
+    else:
+        out = poisoned((B, N_cap, d))
+        sc = None
+    csa.compress_kv(src.to(DEV), W.to(DEV), pb.to(DEV), m, bb, nb, out, sc)
+    torch.cuda.synchronize()
+    y = oracle.compress(u16(raw), u16(W), pb.numpy(), m, bb, nb)
+    if not fp8:
+        g = f64(out[:, bb:bb + nb])
+        assert np.all(np.abs(g - y) <= bf16_bound(y)), "beyond 1 bf16 ulp + fp32 error"
+        assert torch.isnan(out[:, bb + nb:]).all()
+        return
+    codes_ref, sc_ref = oracle.quantize_e4m3_rows(y)
+    gs = sc[:, bb:bb + nb].cpu().numpy().astype(np.float64)
+    np.testing.assert_allclose(gs, sc_ref, rtol=1e-6)
+    dec = oracle.e4m3_decode(u8(out[:, bb:bb + nb]))
+    exact_v = y / gs[..., None]
+    assert np.all(np.abs(dec - exact_v) <= e4m3_half_step(exact_v) * (1 + 1e-5) + 1e-12)
+
+
 # ---------------------------------------------------------------- a2 + a3 indexer top-k
 
 def _indexer_case(B, T, N_cap, n_cmp, q_pos, fp8, seed=5):

@@ -84,8 +84,10 @@ def test_csa_decode_1m_fp8_streaming(cuda_device):
     _check_decode("csa_decode_1m_fp8", [0, 7])
 
 
-def test_csa_prefill_4k(cuda_device):
-    wl, inp, step, out = _run("csa_prefill_4k")
+@pytest.mark.parametrize("name", ["csa_prefill_4k", "csa_prefill_4k_overlap"])
+def test_csa_prefill_4k(cuda_device, name):
+    # the overlap variant forms every new block from 2m raw tokens
+    wl, inp, step, out = _run(name)
     toks = [0, 1, 2, 3, 4, 1023, 2048, 4093, 4094, 4095]
     a = oracle_inputs(wl, inp, 0, tokens=toks)
     y = fill_new_entries(wl, inp, a)
