@@ -304,7 +304,7 @@ def main():
     local = int(os.environ.get("LOCAL_RANK", "0"))
     wl = synth.WORKLOADS[args.workload]
     cfg = {"workload": wl.name, "kind": wl.kind, "B": wl.B, "L": wl.L, "T": wl.T, "m": wl.m,
-           "span": wl.cspan,
+           "span": wl.cspan, "batch_invariant_keys_per_split": wl.batch_invariant,
            "H": wl.H, "D": wl.D, "k": wl.k, "window": wl.W, "H_I": wl.H_I, "d_I": wl.d_I,
            "indexer_dtype": "e4m3" if wl.idx_fp8 else "bf16",
            "stream_compress": wl.stream_compress, "parallelism": f"replicas{world}"}

@@ -169,6 +169,34 @@ CSA_API int csa_indexer_scores(const void* q_idx, const float* q_scale, const fl
                                int m, float* scores, int64_t ld, int32_t* err_word, void* stream);
 
 /* ------------------------------------------------------------------------
+ * a4 + a6, batch-invariant.  The elamur.ai DeepSeek-V4 page (Key points,
+ * infrastructure) and the myWiki DeepSeek-V4 notes (Infrastructure
+ * Highlights) list batch-invariant, deterministic kernels for bitwise
+ * reproducibility.  csa_sparse_attn_prefill splits each query's keys
+ * according to how many queries share the call, so the fp32 summation order
+ * of a query's result changes with B and T.  This call fixes the split by the
+ * key count alone: ranges of keys_per_split slots (rounded up to 64), at most
+ * 16 of them (one thread-block cluster per query), merged in split order.  A
+ * query's output and lse are then bitwise the same whatever else is in the
+ * batch, and from run to run.
+ *
+ * Arguments as csa_sparse_attn_prefill (T query tokens per sequence at
+ * q_pos, so T = 1 is decode with q_pos = seq_len - 1, and T = 2 a two-token
+ * multi-token-prediction step), without a workspace, plus keys_per_split
+ * > 0 with ceil((k + window + 3) / round64(keys_per_split)) <= 16, else
+ * CSA_ERR_INVALID_ARG.  The clusters need not all be resident at once (a
+ * large batch may run in several waves).
+ * ---------------------------------------------------------------------- */
+CSA_API int csa_sparse_attn_batch_invariant(const void* q, const void* k_cmp, const void* v_cmp,
+                                            int64_t cmp_bstride, int N_cap,
+                                            const int32_t* topk_idx, int k, const void* k_raw,
+                                            const void* v_raw, int64_t raw_bstride,
+                                            int64_t raw_cap, const int32_t* q_pos, int window,
+                                            const float* sink, float softmax_scale, int B, int T,
+                                            int H, int D, void* out, float* lse,
+                                            int keys_per_split, int32_t* err_word, void* stream);
+
+/* ------------------------------------------------------------------------
  * a3, without caller scratch.  An integration variant: the DeepSeek-V4 pages
  * have no counterpart to it; it computes exactly what csa_indexer_topk does.
  *

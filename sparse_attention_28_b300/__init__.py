@@ -13,6 +13,7 @@ Calls (same names as the C ABI, without the prefix where it reads better):
 * :func:`indexer_topk`           -- csa_indexer_topk
 * :func:`sparse_attn_decode`     -- csa_sparse_attn_decode
 * :func:`sparse_attn_prefill`    -- csa_sparse_attn_prefill
+* :func:`sparse_attn_batch_invariant` -- csa_sparse_attn_batch_invariant
 * :func:`hca_dense_attn_decode`  -- hca_dense_attn_decode
 """
 from __future__ import annotations
@@ -36,7 +37,7 @@ ABI_SYMBOLS = (
     "csa_status_str", "csa_abi_version", "csa_compress_kv", "csa_indexer_topk_workspace",
     "csa_indexer_topk", "csa_attn_workspace", "csa_sparse_attn_decode",
     "csa_sparse_attn_prefill", "hca_dense_attn_decode", "csa_indexer_topk_static",
-    "csa_indexer_scores", "csa_compress_kv_span",
+    "csa_indexer_scores", "csa_compress_kv_span", "csa_sparse_attn_batch_invariant",
 )
 
 # capacity of the library-owned scratch behind indexer_topk_static (bytes)
@@ -92,6 +93,9 @@ def lib() -> ctypes.CDLL:
             L.csa_sparse_attn_prefill.argtypes = [P, P, P, I64, I, P, I, P, P, I64, I64, P, I, P,
                                                   F, I, I, I, I, P, P, P, SZ, P, P]
             L.csa_sparse_attn_prefill.restype = I
+            L.csa_sparse_attn_batch_invariant.argtypes = [P, P, P, I64, I, P, I, P, P, I64, I64,
+                                                          P, I, P, F, I, I, I, I, P, P, I, P, P]
+            L.csa_sparse_attn_batch_invariant.restype = I
             L.hca_dense_attn_decode.argtypes = [P, P, P, I64, I, P, I, P, P, I64, I64, P, I, P, F,
                                                 I, I, I, P, P, P, SZ, P, P]
             L.hca_dense_attn_decode.restype = I
@@ -373,6 +377,31 @@ def sparse_attn_prefill(q, k_cmp, v_cmp, topk_idx, k_raw, v_raw, q_pos, window: 
         k_raw.shape[1] if k_raw is not None else 0, _p(q_pos), window, _p(sink), softmax_scale,
         B, T, H, D, _p(o), _p(lse), _p(wsb), wsn, _p(err_word), _stream(dev))
     _check(st, "csa_sparse_attn_prefill")
+    return (o, lse) if return_lse else o
+
+
+def sparse_attn_batch_invariant(q, k_cmp, v_cmp, topk_idx, k_raw, v_raw, q_pos, window: int,
+                                sink, keys_per_split: int = 256, softmax_scale: float = 1.0,
+                                return_lse: bool = False, out=None, err_word=None):
+    """CSA attention whose result for a query does not depend on the rest of
+    the batch (bitwise): keys split in fixed ranges of keys_per_split slots.
+    Shapes as :func:`sparse_attn_prefill` (T = 1: decode at q_pos = seq_len - 1;
+    T = 2: a two-token step)."""
+    _attn_common(q, k_cmp, v_cmp, k_raw, v_raw, sink)
+    _cuda(topk_idx, "topk_idx", torch.int32)
+    _cuda(q_pos, "q_pos", torch.int32)
+    _need(topk_idx.is_contiguous() and q_pos.is_contiguous(), "contiguous index tensors")
+    B, T, H, D = q.shape
+    k = topk_idx.shape[-1]
+    dev = q.device
+    o = out if out is not None else torch.empty_like(q)
+    lse = torch.empty((B, T, H), dtype=torch.float32, device=dev) if return_lse else None
+    st = lib().csa_sparse_attn_batch_invariant(
+        _p(q), _p(k_cmp), _p(v_cmp), _bstride(k_cmp), k_cmp.shape[1], _p(topk_idx), k,
+        _p(k_raw), _p(v_raw), _bstride(k_raw) if k_raw is not None else 0,
+        k_raw.shape[1] if k_raw is not None else 0, _p(q_pos), window, _p(sink), softmax_scale,
+        B, T, H, D, _p(o), _p(lse), keys_per_split, _p(err_word), _stream(dev))
+    _check(st, "csa_sparse_attn_batch_invariant")
     return (o, lse) if return_lse else o
 
 

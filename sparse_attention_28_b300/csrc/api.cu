@@ -279,6 +279,7 @@ static void fill_common(AttnArgs& a, const void* q, const void* k_cmp, const voi
   a.err = err_word;
   a.part_o = nullptr;
   a.part_lse = nullptr;
+  a.fixed_kps = 0;
   a.n_cmp = nullptr;
   a.m_prime = 1;
   a.dense = 0;
@@ -341,6 +342,40 @@ int csa_sparse_attn_prefill(const void* q, const void* k_cmp, const void* v_cmp,
   a.n_query = B * T;
   a.n_keys_max = k + window;
   return run_attention(a, ws, ws_bytes, stream);
+}
+
+int csa_sparse_attn_batch_invariant(const void* q, const void* k_cmp, const void* v_cmp,
+                                    int64_t cmp_bstride, int N_cap, const int32_t* topk_idx,
+                                    int k, const void* k_raw, const void* v_raw,
+                                    int64_t raw_bstride, int64_t raw_cap, const int32_t* q_pos,
+                                    int window, const float* sink, float softmax_scale, int B,
+                                    int T, int H, int D, void* out, float* lse,
+                                    int keys_per_split, int32_t* err_word, void* stream) {
+  int st = check_attention_common(q, k_cmp, v_cmp, cmp_bstride, N_cap, k_raw, v_raw, raw_bstride,
+                                  raw_cap, window, sink, B, T, H, D, out, lse);
+  if (st != CSA_OK || B == 0 || T == 0) return st;
+  if (k < 0 || (k > 0 && (!topk_idx || !aligned4(topk_idx) || N_cap <= 0))) return CSA_ERR_INVALID_ARG;
+  if (!q_pos || !aligned4(q_pos)) return CSA_ERR_INVALID_ARG;
+  if (k + window <= 0) return CSA_ERR_INVALID_ARG;
+  if ((int64_t)B * T > (1 << 30)) return CSA_ERR_UNSUPPORTED;
+  // at most 16 splits (one cluster) of keys_per_split slots, rounded up to 64
+  if (keys_per_split <= 0 || keys_per_split > (1 << 24)) return CSA_ERR_INVALID_ARG;
+  const int64_t kps = ((int64_t)keys_per_split + 63) / 64 * 64;
+  if ((k + window + 3 + kps - 1) / kps > 16) return CSA_ERR_INVALID_ARG;
+  AttnArgs a;
+  fill_common(a, q, k_cmp, v_cmp, cmp_bstride, N_cap, k_raw, v_raw, raw_bstride, raw_cap, window,
+              sink, softmax_scale, H, out, lse, err_word);
+  a.sel = topk_idx;
+  a.sel_count = k;
+  a.sel_stride = k;
+  a.pos = q_pos;
+  a.pos_is_len = 0;
+  a.T = T;
+  a.n_batch = B;
+  a.n_query = B * T;
+  a.n_keys_max = k + window;
+  a.fixed_kps = keys_per_split;
+  return cuda_status(launch_attention(a, nullptr, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int hca_dense_attn_decode(const void* q, const void* k_cmp, const void* v_cmp,

@@ -806,9 +806,18 @@ cudaError_t launch_tc(AttnArgs a, const Maps& maps, void* ws, cudaStream_t st) {
   // Pick the split count: at most one cluster of splits per query, every
   // cluster resident at once (one wave), about one CTA per SM in total.
   int ns = 1, kps = 0;
-  for (int cap = kMaxCluster; cap >= 1; --cap) {
-    attn_plan(a.n_query, a.n_keys_max, cap, &ns, &kps);
-    if (ns <= 1 || (long)active_clusters<M>(ns) >= (long)a.n_query) break;
+  if (a.fixed_kps > 0) {
+    // batch-invariant: the split depends on the key count only, so a query's
+    // partials and their merge order do not depend on the other queries
+    kps = (a.fixed_kps + kStageKeys - 1) / kStageKeys * kStageKeys;
+    ns = (a.n_keys_max + 3 + kps - 1) / kps;
+    if (ns > kMaxCluster) return cudaErrorInvalidValue;  // checked on the host first
+    ws = nullptr;
+  } else {
+    for (int cap = kMaxCluster; cap >= 1; --cap) {
+      attn_plan(a.n_query, a.n_keys_max, cap, &ns, &kps);
+      if (ns <= 1 || (long)active_clusters<M>(ns) >= (long)a.n_query) break;
+    }
   }
   // Where clusters that large cannot all be resident and a workspace is
   // given, run more splits without a cluster and merge them in a second

@@ -42,6 +42,7 @@ struct AttnArgs {
   int n_batch;  // sequences (rows of the caches' 2-D views span all of them)
   int n_query;
   int n_keys_max;
+  int fixed_kps;  // > 0: every query's keys split into ranges of this many slots
   // filled by launch_attention
   int n_split;
   int keys_per_split;

@@ -21,7 +21,8 @@ from __future__ import annotations
 import torch
 
 from . import (attn_workspace, compress_kv, hca_dense_attn_decode, indexer_scores,
-               indexer_topk, indexer_topk_workspace, sparse_attn_decode, sparse_attn_prefill)
+               indexer_topk, indexer_topk_workspace, sparse_attn_batch_invariant,
+               sparse_attn_decode, sparse_attn_prefill)
 
 
 def _ring_put(cache, b, positions, rows):
@@ -169,6 +170,14 @@ class CsaDecodeStep(_Step):
 
     def _attend(self):
         wl = self.wl
+        if wl.batch_invariant:
+            # fixed key splits: each sequence's result is independent of the batch
+            B, H, D = self.q.shape
+            sparse_attn_batch_invariant(self.q.view(B, 1, H, D), self.k_cmp, self.v_cmp, self.idx,
+                                        self.k_raw, self.v_raw, self.q_pos, wl.W, self.sink,
+                                        keys_per_split=wl.batch_invariant,
+                                        out=self.out.view(B, 1, H, D))
+            return
         sparse_attn_decode(self.q, self.k_cmp, self.v_cmp, self.idx.view(wl.B, wl.k),
                            self.k_raw, self.v_raw, self.seq_len, wl.W, self.sink,
                            out=self.out, ws=self.ws_attn)

@@ -57,6 +57,7 @@ class Workload:
     sink: bool = True
     seq_lens: Optional[tuple] = None  # ragged decode lengths (default: all L)
     span: int = 0            # raw tokens per compressed block (0: m, no overlap)
+    batch_invariant: int = 0  # > 0: decode attention with fixed key splits of this size
 
     @property
     def cspan(self) -> int:
@@ -86,6 +87,9 @@ WORKLOADS = {
                                k=2048, T=4096),
     "csa_decode_1m_fp8": Workload("csa_decode_1m_fp8", "csa_decode", B=8, L=1048576, m=4,
                                   H=64, k=2048, idx_fp8=True, stream_compress=True),
+    # the 128K decode with batch-invariant attention (fixed 320-key splits)
+    "csa_decode_128k_bi": Workload("csa_decode_128k_bi", "csa_decode", B=32, L=131072, m=4,
+                                   H=64, k=1024, batch_invariant=320),
     # overlapping compression: each block formed from 2m tokens (its own and
     # the previous block's)
     "csa_prefill_4k_overlap": Workload("csa_prefill_4k_overlap", "csa_prefill", B=1, L=262144,

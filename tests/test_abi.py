@@ -128,6 +128,23 @@ def test_compress_span_rejects():
     assert call(B=0, raw=None) == 0
 
 
+def test_batch_invariant_rejects():
+    L = csa.lib()
+
+    def call(**over):
+        a = dict(q=FAKE, kc=FAKE, vc=FAKE, cbs=1024 * 128, N=1024, idx=FAKE, k=512, kr=FAKE,
+                 vr=FAKE, rbs=4096 * 128, rcap=4096, pos=FAKE, W=128, sink=None, scale=1.0, B=2,
+                 T=2, H=64, D=128, out=FAKE, lse=None, kps=256, err=None, st=None)
+        a.update(over)
+        return L.csa_sparse_attn_batch_invariant(*a.values())
+
+    assert call(kps=0) == 1
+    assert call(kps=32, k=1024) == 1   # 1155 slots in ranges of 64: 19 splits (> 16)
+    assert call(kps=64, k=1000) == 1   # 1131 slots: 18 splits
+    assert call(pos=None) == 1
+    assert call(B=0, q=None) == 0
+
+
 def test_attention_workspace_only_for_split_queries():
     # partial rows + lse (129 fp32 per head) for every split of every query
     # when a query can get several splits (fewer queries than SMs / 2); none

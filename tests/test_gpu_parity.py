@@ -449,6 +449,66 @@ def test_prefill_parity(cuda_device):
     check_attention(out, ro, lse, rl, "prefill")
 
 
+def _bi_case(B, T, seed, N_cap=1500, k=1024, L_cap=6100, m=4):
+    q = synth.randn((B, T, 64, 128), seed, 1, scale=1 / math.sqrt(128))
+    kc, vc = synth.randn((B, N_cap, 128), seed, 2), synth.randn((B, N_cap, 128), seed, 3)
+    kr, vr = synth.randn((B, L_cap, 128), seed, 4), synth.randn((B, L_cap, 128), seed, 5)
+    sink = synth.randn((64,), seed, 6, dtype=torch.float32)
+    g = np.random.default_rng(seed)
+    q_pos = np.stack([6000 - 3 * b + np.arange(T) for b in range(B)]).astype(np.int32)
+    n_vis = np.minimum(N_cap, (q_pos + 1) // m)
+    sel = np.full((B, T, k), -1, np.int32)
+    for b in range(B):
+        for t in range(T):
+            take = min(k, n_vis[b, t])
+            sel[b, t, :take] = np.sort(g.choice(n_vis[b, t], take, replace=False))
+    return q, kc, vc, kr, vr, sink, q_pos, sel
+
+
+def _bi_run(case, kps, rows=None):
+    q, kc, vc, kr, vr, sink, q_pos, sel = case
+    if rows is not None:  # a sub-batch of the same sequences
+        q, kc, vc, kr, vr = q[rows], kc[rows], vc[rows], kr[rows], vr[rows]
+        q_pos, sel = q_pos[rows], sel[rows]
+    out, lse = csa.sparse_attn_batch_invariant(
+        q.to(DEV), kc.to(DEV), vc.to(DEV), torch.from_numpy(np.ascontiguousarray(sel)).to(DEV),
+        kr.to(DEV), vr.to(DEV), torch.from_numpy(np.ascontiguousarray(q_pos)).to(DEV), 128,
+        sink.to(DEV), keys_per_split=kps, return_lse=True)
+    torch.cuda.synchronize()
+    return out.cpu(), lse.cpu()
+
+
+@pytest.mark.parametrize("T", [1, 2])  # decode, and a two-token (multi-token) step
+def test_batch_invariant_attention_parity(cuda_device, T):
+    case = _bi_case(3, T, 71)
+    out, lse = _bi_run(case, 256)
+    q, kc, vc, kr, vr, sink, q_pos, sel = case
+    ro, rl = oracle.csa_prefill(u16(q), u16(kc), u16(vc), sel, u16(kr), u16(vr), q_pos, 128,
+                                sink.numpy(), 1.0)
+    check_attention(out, ro, lse, rl, f"batch-invariant T={T}")
+
+
+def test_batch_invariant_attention_is_bitwise_independent_of_the_batch(cuda_device):
+    # the same sequences alone, in a batch of 24, and a token alone vs in a
+    # two-token step: bitwise equal outputs and lse
+    big = _bi_case(24, 2, 72)
+    out_b, lse_b = _bi_run(big, 320)
+    for rows in ([5], [0, 17], list(range(24))[::-1][:9]):
+        out_s, lse_s = _bi_run(big, 320, rows)
+        assert torch.equal(out_s, out_b[rows]) and torch.equal(lse_s, lse_b[rows])
+    q, kc, vc, kr, vr, sink, q_pos, sel = big
+    one = (q[:, 1:], kc, vc, kr, vr, sink, q_pos[:, 1:], sel[:, 1:])
+    out_1, lse_1 = _bi_run(one, 320)
+    assert torch.equal(out_1[:, 0], out_b[:, 1]) and torch.equal(lse_1[:, 0], lse_b[:, 1])
+    # the automatic plan (split count from the batch) agrees within rounding
+    out_a, lse_a = csa.sparse_attn_prefill(
+        q.to(DEV), kc.to(DEV), vc.to(DEV), torch.from_numpy(sel).to(DEV), kr.to(DEV),
+        vr.to(DEV), torch.from_numpy(q_pos).to(DEV), 128, sink.to(DEV), return_lse=True)
+    torch.cuda.synchronize()
+    assert (out_a.cpu().float() - out_b.float()).abs().max().item() < 2e-2
+    assert (lse_a.cpu() - lse_b).abs().max().item() < 1e-3
+
+
 def test_softmax_scale_is_applied(cuda_device):
     B, H, N_cap, k = 2, 32, 64, 16
     lens = [256, 256]

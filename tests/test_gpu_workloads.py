@@ -107,6 +107,11 @@ def test_csa_prefill_4k(cuda_device, name):
     check_attention(out[:, [toks[i] for i in same]], ro[:, same], what="prefill step")
 
 
+def test_csa_decode_128k_batch_invariant(cuda_device):
+    # the same step with fixed 320-key attention splits
+    _check_decode("csa_decode_128k_bi", [0, 13, 31])
+
+
 def test_decode_step_is_deterministic(cuda_device):
     wl, inp, step, out = _run("csa_decode_128k")
     idx = step.idx.clone()
