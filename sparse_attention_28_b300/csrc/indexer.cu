@@ -42,7 +42,7 @@ constexpr int kChunk = 2048;      // entries per score CTA
 constexpr int kUnrollBf16 = 4;    // 16-entry groups in flight per warp (bf16 keys)
 constexpr int kUnrollFp8 = 8;     // (E4M3 keys: half the bytes per row)
 constexpr int kQueryChunk = 256;  // queries per launch (bounds the workspace)
-constexpr int kSelThreads = 1024;
+constexpr int kSelThreads = 1024;  // select CTA size for few queries (512 for many)
 constexpr int kMaxCluster = 16;  // select CTAs per query
 static_assert(kMaxNcap <= kMaxCluster * kSelThreads * 32, "select cluster");
 
@@ -285,13 +285,14 @@ struct SelShared {
   uint32_t above[kMaxCluster];  // per CTA of the cluster: keys above k*
   uint32_t equal[kMaxCluster];  // and equal to k*
 };
-constexpr int sel_smem_bytes(int per_thread) {
-  return (int)((sizeof(SelShared) + 127) / 128 * 128) + kSelThreads * per_thread * 4;
+constexpr int sel_smem_bytes(int threads, int per_thread) {
+  return (int)((sizeof(SelShared) + 127) / 128 * 128) + threads * per_thread * 4;
 }
 
 // this CTA's counts of one level, added into `tot` of every CTA in the cluster
+template <int NT>
 __device__ __forceinline__ void push_level(const uint32_t* loc, uint32_t* tot, int nb, int cs) {
-  for (int bin = threadIdx.x; bin < nb; bin += kSelThreads) {
+  for (int bin = threadIdx.x; bin < nb; bin += NT) {
     const uint32_t v = loc[bin];
     if (!v) continue;
     const uint32_t la = smem_u32(&tot[bin]);
@@ -303,11 +304,13 @@ __device__ __forceinline__ void push_level(const uint32_t* loc, uint32_t* tot, i
 // r*E*1024.  Thread t owns the E consecutive entries [E t, E t + E) of the
 // slice, read as 16-byte vectors in a rotated order; bit b of its masks is
 // entry E t + b.
-template <int E>
-__global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(IndexerArgs a, int q0,
-                                                                     WsLayout L) {
+template <int NT, int E>
+__global__ void __launch_bounds__(NT, 1024 / NT) topk_select_kernel(IndexerArgs a, int q0,
+                                                                    WsLayout L) {
+  constexpr int PER1 = kHistBins / NT;  // level-1 bins per thread
+  constexpr int PER2 = 1024 / NT;       // level-2 / 3 bins per thread
   constexpr int V = E / 4;             // 16-byte vectors per thread
-  constexpr int kSlice = kSelThreads * E;
+  constexpr int kSlice = NT * E;
   constexpr int kCopies = 8;           // bulk copies the slice is split into
   extern __shared__ __align__(128) uint8_t sel_smem[];
   SelShared* sh = reinterpret_cast<SelShared*>(sel_smem);
@@ -325,7 +328,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(IndexerArgs
   const int n_slice = nv > s0 ? (int)(nv - s0 < kSlice ? nv - s0 : kSlice) : 0;
 
   if (nv <= a.k) {  // every visible entry is selected (the same branch in every CTA)
-    for (int64_t i = s0 + tid; i < s0 + kSlice && i < a.k; i += kSelThreads) {
+    for (int64_t i = s0 + tid; i < s0 + kSlice && i < a.k; i += NT) {
       out[i] = i < nv ? (int32_t)i : -1;
       if (out_s) out_s[i] = i < nv ? scores[i] : -INFINITY;
     }
@@ -349,7 +352,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(IndexerArgs
       tma::bulk_load(smem_u32(sc) + b0, reinterpret_cast<const uint8_t*>(scores + s0) + b0,
                      (uint32_t)(b1 - b0), &sh->bar);
   }
-  for (int i = tid; i < kHistBins; i += kSelThreads) {
+  for (int i = tid; i < kHistBins; i += NT) {
     sh->t1[i] = 0u;
     sh->loc[i] = 0u;
     if (i < 1024) {
@@ -357,7 +360,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(IndexerArgs
       sh->t3[i] = 0u;
     }
   }
-  for (int i = bulk / 4 + tid; i < n_slice; i += kSelThreads) sc[i] = scores[s0 + i];
+  for (int i = bulk / 4 + tid; i < n_slice; i += NT) sc[i] = scores[s0 + i];
   __syncthreads();
   tc::cluster_arrive();  // the totals are zeroed before any CTA adds into them
 
@@ -386,16 +389,17 @@ __global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(IndexerArgs
     if (kk[i]) atomicAdd(&sh->loc[kk[i] >> 20], 1u);
   __syncthreads();
   tc::cluster_wait();
-  push_level(sh->loc, sh->t1, kHistBins, cs);
+  push_level<NT>(sh->loc, sh->t1, kHistBins, cs);
   tc::cluster_sync();
   {
-    const int bins[4] = {(int)sh->t1[kHistBins - 1 - 4 * tid], (int)sh->t1[kHistBins - 2 - 4 * tid],
-                         (int)sh->t1[kHistBins - 3 - 4 * tid], (int)sh->t1[kHistBins - 4 - 4 * tid]};
-    bin_from_top<kSelThreads, 4>(bins, kHistBins - 1 - 4 * tid, a.k, sh->scratch, sh->res);
+    int bins[PER1];
+#pragma unroll
+    for (int i = 0; i < PER1; ++i) bins[i] = (int)sh->t1[kHistBins - 1 - PER1 * tid - i];
+    bin_from_top<NT, PER1>(bins, kHistBins - 1 - PER1 * tid, a.k, sh->scratch, sh->res);
   }
   const uint32_t bstar = (uint32_t)sh->res[0];
   int need = a.k - sh->res[1];
-  sh->loc[tid] = 0u;  // levels 2 and 3 use the first 1024 counters
+  for (int i = tid; i < 1024; i += NT) sh->loc[i] = 0u;  // levels 2 and 3 use 1024 counters
   __syncthreads();
 
   // ---- level 2: key bits 19..10 of the B* keys
@@ -403,15 +407,17 @@ __global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(IndexerArgs
   for (int i = 0; i < E; ++i)
     if (kk[i] && (kk[i] >> 20) == bstar) atomicAdd(&sh->loc[(kk[i] >> 10) & 1023], 1u);
   __syncthreads();
-  push_level(sh->loc, sh->t2, 1024, cs);
+  push_level<NT>(sh->loc, sh->t2, 1024, cs);
   tc::cluster_sync();
   {
-    const int bins[1] = {(int)sh->t2[1023 - tid]};
-    bin_from_top<kSelThreads, 1>(bins, 1023 - tid, need, sh->scratch, sh->res);
+    int bins[PER2];
+#pragma unroll
+    for (int i = 0; i < PER2; ++i) bins[i] = (int)sh->t2[1023 - PER2 * tid - i];
+    bin_from_top<NT, PER2>(bins, 1023 - PER2 * tid, need, sh->scratch, sh->res);
   }
   const uint32_t p2 = (bstar << 10) | (uint32_t)sh->res[0];
   need -= sh->res[1];
-  sh->loc[tid] = 0u;
+  for (int i = tid; i < 1024; i += NT) sh->loc[i] = 0u;
   __syncthreads();
 
   // ---- level 3: key bits 9..0 under (B*, level-2 bin)
@@ -419,11 +425,13 @@ __global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(IndexerArgs
   for (int i = 0; i < E; ++i)
     if (kk[i] && (kk[i] >> 10) == p2) atomicAdd(&sh->loc[kk[i] & 1023], 1u);
   __syncthreads();
-  push_level(sh->loc, sh->t3, 1024, cs);
+  push_level<NT>(sh->loc, sh->t3, 1024, cs);
   tc::cluster_sync();
   {
-    const int bins[1] = {(int)sh->t3[1023 - tid]};
-    bin_from_top<kSelThreads, 1>(bins, 1023 - tid, need, sh->scratch, sh->res);
+    int bins[PER2];
+#pragma unroll
+    for (int i = 0; i < PER2; ++i) bins[i] = (int)sh->t3[1023 - PER2 * tid - i];
+    bin_from_top<NT, PER2>(bins, 1023 - PER2 * tid, need, sh->scratch, sh->res);
   }
   const uint32_t kstar = (p2 << 10) | (uint32_t)sh->res[0];
   const int need_eq = need - sh->res[1];  // entries equal to k* to take, lowest index first
@@ -439,8 +447,8 @@ __global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(IndexerArgs
       eq_bits |= (uint32_t)(k1 && k1 == kstar) << (bitpos[q] + c);
     }
   int tot_above, tot_eq;
-  const int above_before = block_excl_scan<kSelThreads>(__popc(above_bits), sh->scratch, &tot_above);
-  const int eq_before = block_excl_scan<kSelThreads>(__popc(eq_bits), sh->scratch, &tot_eq);
+  const int above_before = block_excl_scan<NT>(__popc(above_bits), sh->scratch, &tot_above);
+  const int eq_before = block_excl_scan<NT>(__popc(eq_bits), sh->scratch, &tot_eq);
   if (tid < cs) {
     tc::st_cluster_u32(tc::map_shared(smem_u32(&sh->above[r]), tid), (uint32_t)tot_above);
     tc::st_cluster_u32(tc::map_shared(smem_u32(&sh->equal[r]), tid), (uint32_t)tot_eq);
@@ -516,19 +524,44 @@ cudaError_t launch_indexer_scores(const IndexerArgs& a, float* scores, int ld, c
   return cudaSuccess;
 }
 
+namespace {
+
+// Select launch shape: CTAs of NT threads with E entries per thread, cs per
+// query (one cluster).
+struct SelPlan {
+  int nt, per, cs;
+  const void* fn;
+};
+
+SelPlan select_plan(int n_query, int n_cap) {
+  // few queries: 1024-thread CTAs, the fewest entries per thread (8, 16, 32)
+  // that need at most 8 CTAs per query (clusters of 8 still fit two to a GPC)
+  SelPlan p;
+  p.nt = 1024;
+  p.per = n_cap <= 8 * 1024 * 8 ? 8 : n_cap <= 8 * 1024 * 16 ? 16 : 32;
+  p.cs = (n_cap + 1024 * p.per - 1) / (1024 * p.per);
+  // many queries (several waves of CTAs, each latency-bound): 512-thread
+  // CTAs, two per SM, so that one CTA's barriers overlap another's work
+  const int64_t ctas = (int64_t)(n_query < kQueryChunk ? n_query : kQueryChunk) * p.cs;
+  if (ctas > 2 * kNumSMs && n_cap <= 8 * 512 * 32) {
+    p.nt = 512;
+    p.per = 32;
+    p.cs = (n_cap + 512 * 32 - 1) / (512 * 32);
+  }
+  p.fn = p.nt == 512   ? (const void*)topk_select_kernel<512, 32>
+         : p.per == 8  ? (const void*)topk_select_kernel<1024, 8>
+         : p.per == 16 ? (const void*)topk_select_kernel<1024, 16>
+                       : (const void*)topk_select_kernel<1024, 32>;
+  return p;
+}
+
+}  // namespace
+
 cudaError_t launch_indexer_topk(const IndexerArgs& a, void* ws, cudaStream_t st) {
   WsLayout L = carve(ws, a.N_cap);
-  // entries per select thread: the fewest of 8, 16, 32 that need at most 8
-  // CTAs per query (clusters of 8 still fit two to a GPC), else 32
-  const int per = a.N_cap <= 8 * kSelThreads * 8    ? 8
-                  : a.N_cap <= 8 * kSelThreads * 16 ? 16
-                                                    : 32;
-  const int cs = (a.N_cap + kSelThreads * per - 1) / (kSelThreads * per);
-  const void* sel_fn = per == 8    ? (const void*)topk_select_kernel<8>
-                       : per == 16 ? (const void*)topk_select_kernel<16>
-                                   : (const void*)topk_select_kernel<32>;
+  const SelPlan p = select_plan(a.n_query, a.N_cap);
   {
-    const cudaError_t e = ensure_smem_attr(sel_fn, sel_smem_bytes(per), true);
+    const cudaError_t e = ensure_smem_attr(p.fn, sel_smem_bytes(p.nt, p.per), true);
     if (e != cudaSuccess) return e;
   }
   for (int q0 = 0; q0 < a.n_query; q0 += kQueryChunk) {
@@ -536,24 +569,26 @@ cudaError_t launch_indexer_topk(const IndexerArgs& a, void* ws, cudaStream_t st)
     cudaError_t e = launch_scores(a, q0, qc, L, st);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)cs, (unsigned)qc);
-    cfg.blockDim = dim3(kSelThreads);
-    cfg.dynamicSmemBytes = sel_smem_bytes(per);
+    cfg.gridDim = dim3((unsigned)p.cs, (unsigned)qc);
+    cfg.blockDim = dim3((unsigned)p.nt);
+    cfg.dynamicSmemBytes = sel_smem_bytes(p.nt, p.per);
     cfg.stream = st;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)cs;
+    attr[0].val.clusterDim.x = (unsigned)p.cs;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     set_pdl(attr[1]);
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    if (per == 8)
-      e = cudaLaunchKernelEx(&cfg, topk_select_kernel<8>, a, q0, L);
-    else if (per == 16)
-      e = cudaLaunchKernelEx(&cfg, topk_select_kernel<16>, a, q0, L);
+    if (p.nt == 512)
+      e = cudaLaunchKernelEx(&cfg, topk_select_kernel<512, 32>, a, q0, L);
+    else if (p.per == 8)
+      e = cudaLaunchKernelEx(&cfg, topk_select_kernel<1024, 8>, a, q0, L);
+    else if (p.per == 16)
+      e = cudaLaunchKernelEx(&cfg, topk_select_kernel<1024, 16>, a, q0, L);
     else
-      e = cudaLaunchKernelEx(&cfg, topk_select_kernel<32>, a, q0, L);
+      e = cudaLaunchKernelEx(&cfg, topk_select_kernel<1024, 32>, a, q0, L);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

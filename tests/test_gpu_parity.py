@@ -231,6 +231,22 @@ def test_topk_ties_take_lowest_indices(cuda_device, N_cap, k):
     np.testing.assert_array_equal(idx[:, 0], np.tile(np.arange(k), (B, 1)))
 
 
+def test_topk_ties_many_queries(cuda_device):
+    # 512 tokens of one sequence (several waves of select CTAs: the 512-thread
+    # shape) over 20000 identical keys: every visible score ties, so each
+    # token keeps the k lowest visible indices
+    T, N_cap, m, k = 512, 20000, 4, 700
+    qi = synth.randn((1, T, 4, 64), 5, 1)
+    ki = synth.randn((1, 1, 64), 5, 2).expand(1, N_cap, 64).contiguous()
+    w = torch.ones((1, T, 4))
+    qp = torch.tensor([[N_cap * m - 1 - 37 * (T - 1 - t) for t in range(T)]], dtype=torch.int32)
+    nc = torch.tensor([N_cap], dtype=torch.int32)
+    idx, _ = _run_indexer(qi, None, ki, None, w, qp, nc, m, k)
+    nv = np.minimum(N_cap, (qp.numpy() + 1) // m)
+    want = np.stack([np.where(np.arange(k) < nv[0, t], np.arange(k), -1) for t in range(T)])
+    np.testing.assert_array_equal(idx[0], want)
+
+
 def test_topk_dense_threshold_bin_slow_path(cuda_device):
     # a one-hot query makes the score the key's first channel; those take 16
     # bf16 values in [1, 1.125): one histogram bin holds all 12000 entries
