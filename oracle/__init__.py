@@ -37,6 +37,7 @@ _lib = None
 
 BF16 = 0
 FP8_E4M3 = 1
+FP4_E2M1 = 2
 
 
 def build(force: bool = False) -> str:
@@ -71,12 +72,21 @@ def _load():
             lib.orc_f64_to_e4m3.restype = ctypes.c_uint8
             lib.orc_e4m3_to_f64.argtypes = [ctypes.c_uint8]
             lib.orc_e4m3_to_f64.restype = D
+            lib.orc_f64_to_e2m1.argtypes = [D]
+            lib.orc_f64_to_e2m1.restype = ctypes.c_uint8
+            lib.orc_e2m1_to_f64.argtypes = [ctypes.c_uint8]
+            lib.orc_e2m1_to_f64.restype = D
             for f in ("orc_bf16_decode_array", "orc_bf16_encode_array",
-                      "orc_e4m3_decode_array", "orc_e4m3_encode_array"):
+                      "orc_e4m3_decode_array", "orc_e4m3_encode_array",
+                      "orc_e2m1_decode_array"):
                 getattr(lib, f).argtypes = [P, P, L]
                 getattr(lib, f).restype = None
             lib.orc_quantize_e4m3_rows.argtypes = [P, L, I, P, P]
             lib.orc_quantize_e4m3_rows.restype = None
+            lib.orc_quantize_fp4_rows.argtypes = [P, L, I, P, P]
+            lib.orc_quantize_fp4_rows.restype = None
+            lib.orc_fp4_dequantize_rows.argtypes = [P, P, L, I, P]
+            lib.orc_fp4_dequantize_rows.restype = None
             lib.orc_compress.argtypes = [P, L, I, I, I, I, I, P, P, P]
             lib.orc_compress.restype = I
             lib.orc_compress_span.argtypes = [P, L, I, I, I, I, I, I, P, P, P]
@@ -143,6 +153,46 @@ def e4m3_encode(x) -> np.ndarray:
     return out
 
 
+def e2m1_decode(codes) -> np.ndarray:
+    """Values of FP4 E2M1 codes (one code per uint8, low 4 bits)."""
+    codes = _c(codes, np.uint8)
+    out = np.empty(codes.shape, np.float64)
+    _load().orc_e2m1_decode_array(_ptr(codes), _ptr(out), codes.size)
+    return out
+
+
+def e2m1_encode(x) -> np.ndarray:
+    """Nearest E2M1 codes (ties to even, saturating at 6), one per uint8."""
+    x = np.asarray(x, np.float64)
+    f = _load().orc_f64_to_e2m1
+    return np.array([f(float(v)) for v in x.ravel()], np.uint8).reshape(x.shape)
+
+
+def quantize_fp4_rows(y):
+    """FP4 storage of indexer vectors: per 16 channels one E4M3 scale (nearest
+    to amax / 6), E2M1 codes of y / scale packed two per byte (channel 2i in
+    the low nibble).  Returns (codes uint8 [..., d/2], scales uint8 [..., d/16])."""
+    y = _c(y, np.float64)
+    d = y.shape[-1]
+    assert d % 16 == 0
+    rows = y.size // d
+    codes = np.zeros(y.shape[:-1] + (d // 2,), np.uint8)
+    scales = np.empty(y.shape[:-1] + (d // 16,), np.uint8)
+    _load().orc_quantize_fp4_rows(_ptr(y), rows, d, _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def fp4_dequantize(codes, scales) -> np.ndarray:
+    """Values of FP4-stored vectors (layout of quantize_fp4_rows)."""
+    codes = _c(codes, np.uint8)
+    scales = _c(scales, np.uint8)
+    d = codes.shape[-1] * 2
+    rows = codes.size // (d // 2)
+    out = np.empty(codes.shape[:-1] + (d,), np.float64)
+    _load().orc_fp4_dequantize_rows(_ptr(codes), _ptr(scales), rows, d, _ptr(out))
+    return out
+
+
 def quantize_bf16(y) -> np.ndarray:
     """bf16 storage of a1's output: nearest bf16, ties to even."""
     return bf16_encode(y)
@@ -195,6 +245,8 @@ def indexer_scores(q, w, k, q_pos, n_cmp, m: int, dtype: int = BF16, q_scale=Non
 
     q: [B, T, H, dI] (uint16 bf16 bits, or uint8 E4M3 codes); w: f32 [B, T, H];
     k: [B, N, dI] same format as q; q_scale: f32 [B, T, H]; k_scale: f32 [B, N];
+    FP4: q [B, T, H, dI/2] and k [B, N, dI/2] packed E2M1 codes, q_scale
+    uint8 [B, T, H, dI/16] and k_scale uint8 [B, N, dI/16] E4M3 block scales.
     q_pos: int32 [B, T] absolute positions; n_cmp: int32 [B] entries present.
     Returns (scores fp64 [B, T, N] with -inf beyond n_vis, n_vis int32 [B, T]).
     """
@@ -204,9 +256,12 @@ def indexer_scores(q, w, k, q_pos, n_cmp, m: int, dtype: int = BF16, q_scale=Non
     w = _c(w, np.float32)
     q_pos = _c(q_pos, np.int32)
     n_cmp = _c(n_cmp, np.int32)
-    q_scale = _c(q_scale, np.float32)
-    k_scale = _c(k_scale, np.float32)
+    sc_t = np.uint8 if dtype == FP4_E2M1 else np.float32
+    q_scale = _c(q_scale, sc_t)
+    k_scale = _c(k_scale, sc_t)
     B, T, H, dI = q.shape
+    if dtype == FP4_E2M1:
+        dI *= 2
     N = k.shape[1]
     scores = np.empty((B, T, N), np.float64)
     n_vis = np.empty((B, T), np.int32)

@@ -53,7 +53,7 @@
 #define ORC_ERR_RANGE 2
 #define ORC_ERR_NOMEM 3
 
-enum { ORC_BF16 = 0, ORC_FP8_E4M3 = 1 };
+enum { ORC_BF16 = 0, ORC_FP8_E4M3 = 1, ORC_FP4_E2M1 = 2 };
 
 int orc_num_threads(void) {
 #ifdef _OPENMP
@@ -164,6 +164,78 @@ void orc_quantize_e4m3_rows(const double* y, int64_t rows, int d, uint8_t* codes
   }
 }
 
+/* OCP FP4 E2M1: 1 sign bit, 2 exponent bits (bias 1), 1 mantissa bit, no
+ * infinities or NaN; exponent field 0 holds the subnormal m * 0.5.  The
+ * magnitudes are 0, 0.5, 1, 1.5, 2, 3, 4, 6. */
+double orc_e2m1_to_f64(uint8_t c) {
+  int s = (c >> 3) & 1, E = (c >> 1) & 3, mnt = c & 1;
+  double v = E == 0 ? 0.5 * mnt : ldexp(1.0 + 0.5 * mnt, E - 1);
+  return s ? -v : v;
+}
+
+/* Nearest E2M1 value, ties to the even code (mantissa bit 0); magnitudes
+ * beyond 6 saturate to 6. */
+uint8_t orc_f64_to_e2m1(double x) {
+  uint8_t s = signbit(x) ? 8 : 0;
+  double a = fabs(x);
+  if (isnan(x)) return 7;
+  int best = 0;
+  double bd = INFINITY;
+  for (int c = 0; c < 8; ++c) {
+    double d = fabs(a - orc_e2m1_to_f64((uint8_t)c));
+    if (d < bd || (d == bd && (c & 1) == 0)) {
+      bd = d;
+      best = c;
+    }
+  }
+  return s | (uint8_t)best;
+}
+
+void orc_e2m1_decode_array(const uint8_t* in, double* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = orc_e2m1_to_f64(in[i]);
+}
+
+/* FP4 storage of indexer vectors.  Reading of the pages' FP4 indexer QK path
+ * whose "dynamic range" is "extended with FP8": per block of 16 consecutive
+ * channels one E4M3 scale, the nearest E4M3 value of amax / 6 (amax = 0
+ * gives scale 1; a positive amax whose scale would round to 0 gets the
+ * smallest positive E4M3 value, 2^-9); each channel is the nearest E2M1 value
+ * of y / scale (ties to even, saturating at 6), using the decoded scale.
+ * codes: rows of d/2 bytes, channel 2i in the low nibble of byte i;
+ * scales: rows of d/16 E4M3 bytes.  d a multiple of 16. */
+void orc_quantize_fp4_rows(const double* y, int64_t rows, int d, uint8_t* codes,
+                           uint8_t* scales) {
+  for (int64_t r = 0; r < rows; ++r) {
+    const double* yr = y + r * d;
+    for (int b = 0; b < d / 16; ++b) {
+      double amax = 0.0;
+      for (int c = 16 * b; c < 16 * b + 16; ++c)
+        if (fabs(yr[c]) > amax) amax = fabs(yr[c]);
+      uint8_t sc = amax > 0.0 ? orc_f64_to_e4m3(amax / 6.0) : orc_f64_to_e4m3(1.0);
+      if (orc_e4m3_to_f64(sc) == 0.0) sc = 1;
+      scales[r * (d / 16) + b] = sc;
+      const double scv = orc_e4m3_to_f64(sc);
+      for (int c = 16 * b; c < 16 * b + 16; ++c) {
+        const uint8_t q = orc_f64_to_e2m1(yr[c] / scv);
+        uint8_t* byte = codes + r * (d / 2) + c / 2;
+        *byte = (c & 1) ? (uint8_t)((*byte & 0x0F) | (q << 4)) : (uint8_t)((*byte & 0xF0) | q);
+      }
+    }
+  }
+}
+
+/* Values of FP4-stored vectors: rows of d channels from packed codes and
+ * block scales (layout of orc_quantize_fp4_rows). */
+void orc_fp4_dequantize_rows(const uint8_t* codes, const uint8_t* scales, int64_t rows, int d,
+                             double* out) {
+  for (int64_t r = 0; r < rows; ++r)
+    for (int c = 0; c < d; ++c) {
+      const uint8_t byte = codes[r * (d / 2) + c / 2];
+      const uint8_t q = (c & 1) ? (byte >> 4) : (byte & 0x0F);
+      out[r * d + c] = orc_e2m1_to_f64(q) * orc_e4m3_to_f64(scales[r * (d / 16) + c / 16]);
+    }
+}
+
 /* ------------------------------------------------------------------------ */
 /* Step a1: block compression                                               */
 /* ------------------------------------------------------------------------ */
@@ -259,6 +331,11 @@ static int64_t visible(int64_t t, int m, int64_t present) {
 /* I(t,s) = sum_h w[t][h] * ReLU(q[t][h] . k[s]) for s < n_vis(t).
  * bf16: q, k are bf16 codes.  FP8: q, k are E4M3 codes and
  *     q[t][h] . k[s] = q_scale[t][h] * k_scale[s] * sum_d q8[d] * k8[d].
+ * FP4: q, k are packed E2M1 codes (rows of dI/2 bytes) with E4M3 block
+ *     scales (q_scale, k_scale then point to bytes: [B][T][H][dI/16] and
+ *     [B][ks_bstride][dI/16]); the dot product is over the values
+ *     code * block scale (orc_fp4_dequantize_rows).  k_bstride counts
+ *     channels (elements) in every format.
  * q: [B][T][H][dI]; w, q_scale: [B][T][H]; k: [B][k_bstride] rows of dI;
  * k_scale: [B][ks_bstride].  scores: fp64 [B][T][N_out]; entries at and
  * beyond n_vis are -inf.  n_vis_out: [B][T]. */
@@ -269,8 +346,9 @@ int orc_indexer_scores(const void* q, const float* q_scale, const float* w, cons
   if (!q || !w || !k || !q_pos || !n_cmp || !scores || B < 0 || T < 0 || H <= 0 ||
       dI <= 0 || m <= 0)
     return ORC_ERR_ARG;
-  if (dtype != ORC_BF16 && dtype != ORC_FP8_E4M3) return ORC_ERR_ARG;
-  if (dtype == ORC_FP8_E4M3 && (!q_scale || !k_scale)) return ORC_ERR_ARG;
+  if (dtype != ORC_BF16 && dtype != ORC_FP8_E4M3 && dtype != ORC_FP4_E2M1) return ORC_ERR_ARG;
+  if (dtype != ORC_BF16 && (!q_scale || !k_scale)) return ORC_ERR_ARG;
+  if (dtype == ORC_FP4_E2M1 && (dI % 16 != 0 || k_bstride % 2 != 0)) return ORC_ERR_ARG;
   int err = ORC_OK;
 #pragma omp parallel
   {
@@ -293,18 +371,28 @@ int orc_indexer_scores(const void* q, const float* q_scale, const float* w, cons
         }
         int64_t nv = visible(tabs, m, n_cmp[b]);
         if (n_vis_out) n_vis_out[bt] = (int32_t)nv;
-        for (int h = 0; h < H; ++h)
-          for (int e = 0; e < dI; ++e) {
-            int64_t o = (bt * H + h) * dI + e;
-            qv[h * dI + e] = dtype == ORC_BF16 ? orc_bf16_to_f64(((const uint16_t*)q)[o])
-                                               : orc_e4m3_to_f64(((const uint8_t*)q)[o]);
-          }
+        if (dtype == ORC_FP4_E2M1)
+          orc_fp4_dequantize_rows((const uint8_t*)q + bt * H * (dI / 2),
+                                  (const uint8_t*)q_scale + bt * H * (dI / 16), H, dI, qv);
+        else
+          for (int h = 0; h < H; ++h)
+            for (int e = 0; e < dI; ++e) {
+              int64_t o = (bt * H + h) * dI + e;
+              qv[h * dI + e] = dtype == ORC_BF16 ? orc_bf16_to_f64(((const uint16_t*)q)[o])
+                                                 : orc_e4m3_to_f64(((const uint8_t*)q)[o]);
+            }
         double* out = scores + bt * N_out;
         for (int64_t s = 0; s < nv; ++s) {
           int64_t ko = (int64_t)b * k_bstride + s * dI;
-          for (int e = 0; e < dI; ++e)
-            kv[e] = dtype == ORC_BF16 ? orc_bf16_to_f64(((const uint16_t*)k)[ko + e])
-                                      : orc_e4m3_to_f64(((const uint8_t*)k)[ko + e]);
+          if (dtype == ORC_FP4_E2M1)
+            orc_fp4_dequantize_rows((const uint8_t*)k + ko / 2,
+                                    (const uint8_t*)k_scale +
+                                        ((int64_t)b * ks_bstride + s) * (dI / 16),
+                                    1, dI, kv);
+          else
+            for (int e = 0; e < dI; ++e)
+              kv[e] = dtype == ORC_BF16 ? orc_bf16_to_f64(((const uint16_t*)k)[ko + e])
+                                        : orc_e4m3_to_f64(((const uint8_t*)k)[ko + e]);
           double I = 0.0;
           for (int h = 0; h < H; ++h) {
             double dot = 0.0;

@@ -177,6 +177,91 @@ def test_compress_overlap_is_convex_over_its_span():
         assert np.all(y[:, j] <= win.max(axis=1) + 1e-12)
 
 
+# ---------------------------------------------------------------- FP4 (E2M1)
+
+def test_e2m1_values_are_the_format_definition():
+    g = _golden("indexer_fp4_hand.txt")
+    mags = g["e2m1_magnitudes"]
+    vals = oracle.e2m1_decode(np.arange(16, dtype=np.uint8))
+    np.testing.assert_array_equal(vals[:8], mags)
+    np.testing.assert_array_equal(vals[8:], -mags)
+    assert np.signbit(vals[8])  # code 8 is -0
+
+
+def test_e2m1_encode_nearest_ties_to_even_saturating():
+    # midpoints go to the code with mantissa bit 0; beyond 6 saturates
+    x = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 6.5, 100.0, 0.26, 4.99, -0.75, -5.0]
+    want = [0.0, 1.0, 1.0, 2.0, 2.0, 4.0, 4.0, 6.0, 6.0, 0.5, 4.0, -1.0, -4.0]
+    np.testing.assert_array_equal(oracle.e2m1_decode(oracle.e2m1_encode(x)), want)
+    codes = np.arange(16, dtype=np.uint8)
+    np.testing.assert_array_equal(oracle.e2m1_encode(oracle.e2m1_decode(codes)), codes)
+
+
+def test_fp4_block_quantization_scale_rule_and_error_bound():
+    y = RNG.standard_normal((7, 64)) * np.exp(RNG.uniform(-6, 6, (7, 1)))
+    y[3, 16:32] = 0.0  # an all-zero block: scale 1, codes 0
+    codes, scales = oracle.quantize_fp4_rows(y)
+    sc = oracle.e4m3_decode(scales)
+    amax = np.abs(y.reshape(7, 4, 16)).max(axis=2)
+    want = np.where(amax > 0, oracle.e4m3_decode(oracle.e4m3_encode(amax / 6)), 1.0)
+    np.testing.assert_array_equal(sc, want)
+    assert sc[3, 1] == 1.0 and not codes[3, 8:16].any()
+    d = oracle.fp4_dequantize(codes, scales)
+    r = np.abs(y) / np.repeat(sc, 16, axis=1)  # magnitude in units of the scale
+    half = np.where(r < 2, 0.25, np.where(r < 4, 0.5, 1.0)) * np.repeat(sc, 16, axis=1)
+    over = np.maximum(np.abs(y) - 6 * np.repeat(sc, 16, axis=1), 0)
+    assert np.all(np.abs(d - y) <= np.maximum(half, over) * (1 + 1e-12))
+
+
+def test_fp4_exact_values_round_trip():
+    # values = E2M1 value x a power-of-two scale whose block amax is 6 x scale
+    # are stored exactly
+    mags = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6])
+    v = RNG.choice(np.concatenate([mags, -mags]), (5, 64))
+    v[:, ::16] = 6.0
+    y = v * np.repeat(2.0 ** RNG.integers(-5, 6, (5, 4)), 16, axis=1)
+    codes, scales = oracle.quantize_fp4_rows(y)
+    np.testing.assert_array_equal(oracle.fp4_dequantize(codes, scales), y)
+
+
+def _fp4_pack(vals_codes):
+    c = np.asarray(vals_codes, np.uint8)
+    return (c[..., 0::2] | (c[..., 1::2] << 4)).astype(np.uint8)
+
+
+def test_indexer_scores_fp4_hand_example():
+    g = _golden("indexer_fp4_hand.txt")
+    qc = np.zeros((1, 1, 4, 64), np.uint8)
+    qc[0, 0, 0, 0], qc[0, 0, 0, 17] = 0x2, 0xB
+    qs = np.full((1, 1, 4, 4), 0x38, np.uint8)  # E4M3 1.0
+    qs[0, 0, 0, 0], qs[0, 0, 0, 1] = 0x40, 0x30  # 2.0, 0.5
+    kc = np.zeros((1, 1, 64), np.uint8)
+    kc[0, 0, 0], kc[0, 0, 17] = 0x3, 0x6
+    ks = np.full((1, 1, 4), 0x38, np.uint8)
+    ks[0, 0, 0] = 0x40
+    w = np.array([[[0.5, 1, 1, 1]]], np.float32)
+    sc, nv = oracle.indexer_scores(_fp4_pack(qc), w, _fp4_pack(kc), np.array([[7]], np.int32),
+                                   np.array([1], np.int32), 4, oracle.FP4_E2M1, qs, ks)
+    assert nv[0, 0] == 1 and sc[0, 0, 0] == g["I"]
+
+
+def test_indexer_scores_fp4_is_the_dot_of_the_stored_values():
+    B, T, N, m = 2, 3, 50, 4
+    qc, qs = oracle.quantize_fp4_rows(RNG.standard_normal((B, T, 4, 64)))
+    kc, ks = oracle.quantize_fp4_rows(RNG.standard_normal((B, N, 64)) * 3)
+    w = RNG.standard_normal((B, T, 4)).astype(np.float32)
+    qp = np.full((B, T), 4 * N - 1, np.int32)
+    sc, nv = oracle.indexer_scores(qc, w, kc, qp, np.array([N, N - 7], np.int32), m,
+                                   oracle.FP4_E2M1, qs, ks)
+    qv, kv = oracle.fp4_dequantize(qc, qs), oracle.fp4_dequantize(kc, ks)
+    dots = np.einsum("bthd,bnd->bthn", qv, kv)
+    want = np.einsum("bth,bthn->btn", w.astype(np.float64), np.maximum(dots, 0))
+    for b in range(B):
+        np.testing.assert_allclose(sc[b, :, :nv[b, 0]], want[b, :, :nv[b, 0]], rtol=1e-13,
+                                   atol=1e-12)
+    assert nv[1, 0] == N - 7 and np.all(np.isneginf(sc[1, :, N - 7:]))
+
+
 def test_compress_m1_is_identity():
     raw = _rand_bf16((2, 9, 8))
     W = _rand_bf16((8, 8))
