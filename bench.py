@@ -63,6 +63,16 @@ def n_vis_decode(wl):
     return [min(n // wl.m, n // wl.m) for n in wl.lens]
 
 
+def idx_row_bytes(wl) -> int:
+    """Bytes of one indexer key or query-head vector: bf16 codes; E4M3 codes +
+    an fp32 scale; FP4 codes (two per byte) + one E4M3 scale per 16 channels."""
+    if wl.idx_fp4:
+        return wl.d_I // 2 + wl.d_I // 16
+    if wl.idx_fp8:
+        return wl.d_I + 4
+    return wl.d_I * 2
+
+
 def algorithmic(wl) -> dict:
     """Algorithmic bytes (HBM) or FLOPs per stage per step, from the method's
     own data movement: every byte a stage must read or write at least once."""
@@ -72,14 +82,13 @@ def algorithmic(wl) -> dict:
         nb = sum((min(n // wl.m, n // wl.m) + min(W, n)) * 2 * D * 2 for n in wl.lens)
         return {"attention": {"bytes": nb + wl.B * qo}}
     if wl.kind == "csa_decode":
-        row = wl.d_I + 4 if wl.idx_fp8 else wl.d_I * 2
-        qrow = (wl.d_I + 4) if wl.idx_fp8 else wl.d_I * 2
+        row, qrow = idx_row_bytes(wl), idx_row_bytes(wl)
         idx_b = sum(nv * row for nv in n_vis_decode(wl)) + wl.B * (
             wl.H_I * qrow + wl.H_I * 4 + wl.k * 4)
         att_b = sum((min(wl.k, n // wl.m) + min(W, n)) * 2 * D * 2 for n in wl.lens) + wl.B * qo
         st = {"indexer_topk": {"bytes": idx_b}, "attention": {"bytes": att_b}}
         if wl.stream_compress:
-            per_seq = wl.m * (2 * D * 2 + wl.d_I * 2) + 2 * D * 2 + wl.d_I + 4
+            per_seq = wl.m * (2 * D * 2 + wl.d_I * 2) + 2 * D * 2 + idx_row_bytes(wl)
             weights = (2 * D * D + wl.d_I * wl.d_I) * 2 + wl.m * (2 * D + wl.d_I) * 4
             st["compress"] = {"bytes": wl.B * per_seq + weights}
         return st
@@ -101,8 +110,7 @@ def kernel_algorithmic(wl, name: str) -> dict:
     row once plus the query and weights and writes one fp32 score per visible
     entry; the attention kernels are their whole stage."""
     if name == "indexer_score":
-        row = wl.d_I + 4 if wl.idx_fp8 else wl.d_I * 2
-        qrow = (wl.d_I + 4) if wl.idx_fp8 else wl.d_I * 2
+        row, qrow = idx_row_bytes(wl), idx_row_bytes(wl)
         nv = sum(n_vis_decode(wl))
         return {"bytes": nv * (row + 4) + wl.B * wl.H_I * (qrow + 4)}
     return algorithmic(wl)[name]
@@ -229,8 +237,9 @@ class OracleRunner:
 
     def __init__(self, wl, inp: dict, n_units: int):
         import oracle  # the oracle is test infrastructure: only this leg uses it
-        from oracle.feed import oracle_inputs
+        from oracle.feed import idx_dtype, oracle_inputs
         self.o = oracle
+        self.idx_dtype = idx_dtype(wl)
         self.wl = wl
         self.n = n_units
         self.arr = oracle_inputs(wl, inp, n_units)
@@ -245,12 +254,14 @@ class OracleRunner:
             if wl.stream_compress:
                 for s in ("k", "v", "idx"):
                     y = o.compress(a["raw_new_" + s], *a["gate_" + s], wl.m, 0, 1)
-                    if s == "idx" and wl.idx_fp8:
+                    if s == "idx" and wl.idx_fp4:
+                        o.quantize_fp4_rows(y)
+                    elif s == "idx" and wl.idx_fp8:
                         o.quantize_e4m3_rows(y)
                     else:
                         o.quantize_bf16(y)
             sc, nv = o.indexer_scores(a["q_idx"], a["w"], a["k_idx"], a["q_pos"], a["n_cmp"],
-                                      wl.m, o.FP8_E4M3 if wl.idx_fp8 else o.BF16,
+                                      wl.m, self.idx_dtype,
                                       a.get("q_scale"), a.get("k_scale"))
             idx = o.topk(sc, nv, wl.k)
             o.csa_decode(a["q"], a["k_cmp"], a["v_cmp"], idx[:, 0, :], a["k_win"], a["v_win"],
@@ -306,7 +317,7 @@ def main():
     cfg = {"workload": wl.name, "kind": wl.kind, "B": wl.B, "L": wl.L, "T": wl.T, "m": wl.m,
            "span": wl.cspan, "batch_invariant_keys_per_split": wl.batch_invariant,
            "H": wl.H, "D": wl.D, "k": wl.k, "window": wl.W, "H_I": wl.H_I, "d_I": wl.d_I,
-           "indexer_dtype": "e4m3" if wl.idx_fp8 else "bf16",
+           "indexer_dtype": "e2m1" if wl.idx_fp4 else "e4m3" if wl.idx_fp8 else "bf16",
            "stream_compress": wl.stream_compress, "parallelism": f"replicas{world}"}
 
     if args.impl == "reference":
@@ -446,7 +457,8 @@ def main():
         "metric": METRIC, "value": round(value, 2), "unit": unit_name(wl), "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "e4m3-indexer+bf16" if wl.idx_fp8 else "bf16", "data": "synthetic",
+        "dtype": ("e2m1-indexer+bf16" if wl.idx_fp4 else "e4m3-indexer+bf16" if wl.idx_fp8
+                  else "bf16"), "data": "synthetic",
         "config": dict(cfg, l2="flushed before every step (2x L2 write + 2x L2 read, untimed)",
                        timing="whole step as one CUDA graph, CUDA events; stages timed separately"),
         "roofline": roof, "stages": stage_report, "cpu_baseline": cpu, "e2e": e2e,

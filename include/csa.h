@@ -67,6 +67,11 @@ extern "C" {
 /* element types */
 #define CSA_BF16 0
 #define CSA_FP8_E4M3 1
+/* OCP FP4 E2M1 codes, two per byte (channel 2i in the low nibble), with one
+ * E4M3 scale byte per 16 channels (value = code value * block scale): the
+ * pages' FP4 indexer path, its dynamic range extended with FP8.  Indexer
+ * vectors only (d_I = 64: 32 code bytes and 4 scale bytes per vector). */
+#define CSA_FP4_E2M1 2
 
 /* Human-readable name of a status code (static string, never NULL). */
 CSA_API const char* csa_status_str(int status);
@@ -90,6 +95,12 @@ CSA_API int csa_abi_version(void);
  *             j*m .. j*m+m-1 (raw_cap >= m).
  *   W         bf16 [d][d] (row = output channel), pos_bias fp32 [m][d].
  *   out       out_dtype == CSA_BF16: bf16 [B][out_bstride], row j of d.
+ *             out_dtype == CSA_FP4_E2M1: bytes, row j of d/2 (out_bstride
+ *             counts channels: a multiple of 32), plus out_scale pointing to
+ *             E4M3 bytes [B][scale_bstride][d/16]: per block of 16 channels
+ *             the nearest E4M3 value of amax / 6 (1 if all zero; at least
+ *             2^-9), codes the nearest E2M1 value of y / scale (ties to
+ *             even, saturating at 6).
  *             out_dtype == CSA_FP8_E4M3: E4M3 bytes, row j of d, plus
  *             out_scale fp32 [B][scale_bstride]: scale = max_c |y| / 448
  *             (1 when all zero), code = nearest-even E4M3 of y / scale,
@@ -131,6 +142,10 @@ CSA_API int csa_compress_kv_span(const void* raw, int64_t raw_bstride, int64_t r
  *     I(t,s) = sum_h w[t][h] * ReLU(q[t][h] . k[s]),    s < n_vis(t)
  *     n_vis(t) = min(n_cmp[b], floor((t + 1) / m))   (block-causal)
  * FP8: q[t][h] . k[s] = q_scale[t][h] * k_scale[s] * sum_d q8[d] * k8[d].
+ * FP4 (idx_dtype CSA_FP4_E2M1): q_idx [B][T][H_I][d_I/2] and k_idx rows of
+ * d_I/2 bytes (k_bstride still counts channels: a multiple of 32); q_scale
+ * and k_scale then point to E4M3 block-scale bytes, [B][T][H_I][d_I/16] and
+ * [B][ks_bstride][d_I/16]; the dot product is over code * scale values.
  * Selection: the min(k, n_vis) largest scores, ties to the lower index,
  * written in ascending index order and padded with -1.
  *

@@ -10,7 +10,8 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from . import BF16, FP8_E4M3, compress, quantize_bf16, quantize_e4m3_rows
+from . import (BF16, FP4_E2M1, FP8_E4M3, compress, quantize_bf16, quantize_e4m3_rows,
+               quantize_fp4_rows)
 
 
 def u16(t: torch.Tensor) -> np.ndarray:
@@ -64,7 +65,10 @@ def oracle_inputs(wl, inp: dict, n_units: int, seqs=None, tokens=None) -> dict:
         if wl.kind == "csa_decode":
             a["q_pos"] = (a["seq_len"] - 1).reshape(-1, 1).astype(np.int32)
             a["w"] = f32(inp["w"][ix])
-            if wl.idx_fp8:
+            if wl.idx_fp4:
+                a["q_idx"], a["k_idx"] = u8(inp["q_idx"][ix]), u8(inp["k_idx"][ix])
+                a["q_scale"], a["k_scale"] = u8(inp["q_scale"][ix]), u8(inp["k_scale"][ix])
+            elif wl.idx_fp8:
                 a["q_idx"], a["k_idx"] = u8(inp["q_idx"][ix]), u8(inp["k_idx"][ix])
                 a["q_scale"], a["k_scale"] = f32(inp["q_scale"][ix]), f32(inp["k_scale"][ix])
             else:
@@ -126,7 +130,11 @@ def fill_new_entries(wl, inp: dict, a: dict) -> dict:
         y = compress(a["raw_new_idx"], *a["gate_idx"], m, 0, 1)
         res["idx"] = y
         a["k_idx"] = a["k_idx"].copy()
-        if wl.idx_fp8:
+        if wl.idx_fp4:
+            codes, scales = quantize_fp4_rows(y)
+            a["k_scale"] = a["k_scale"].copy()
+            a["k_idx"][:, j], a["k_scale"][:, j] = codes[:, 0], scales[:, 0]
+        elif wl.idx_fp8:
             codes, scales = quantize_e4m3_rows(y)
             a["k_scale"] = a["k_scale"].copy()
             a["k_idx"][:, j], a["k_scale"][:, j] = codes[:, 0], scales[:, 0]
@@ -149,4 +157,4 @@ def fill_new_entries(wl, inp: dict, a: dict) -> dict:
 
 
 def idx_dtype(wl):
-    return FP8_E4M3 if wl.idx_fp8 else BF16
+    return FP4_E2M1 if wl.idx_fp4 else FP8_E4M3 if wl.idx_fp8 else BF16

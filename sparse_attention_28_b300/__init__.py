@@ -29,6 +29,7 @@ LIB_PATH = os.path.join(_HERE, "libcsa.so")
 
 CSA_BF16 = 0
 CSA_FP8_E4M3 = 1
+CSA_FP4_E2M1 = 2
 EW_BAD_INDEX = 1
 EW_BAD_POSITION = 2
 
@@ -157,24 +158,34 @@ def compress_kv(raw, W, pos_bias, m: int, block_begin: int, n_blocks: int, out,
     [span, d] with span >= m: block j is compressed from the span raw tokens
     ending at its last token (span == m: non-overlapping blocks, span > m:
     overlapping compression); out: bf16 [B, N_cap, d] or uint8 [B, N_cap, d]
-    (E4M3 codes, then out_scale fp32 [B, N_cap] is required).  Writes in
-    place; returns out.
+    (E4M3 codes, then out_scale fp32 [B, N_cap] is required) or uint8
+    [B, N_cap, d/2] (FP4: two E2M1 codes per byte, then out_scale uint8
+    [B, N_cap, d/16] receives the E4M3 block scales).  Writes in place;
+    returns out.
     """
     _cuda(raw, "raw", torch.bfloat16)
     _cuda(W, "W", torch.bfloat16)
     _cuda(pos_bias, "pos_bias", torch.float32)
     _cuda(out, "out")
     B, _, d = raw.shape
-    fp8 = out.dtype in (torch.uint8, torch.float8_e4m3fn)
-    _need(fp8 or out.dtype == torch.bfloat16, "out must be bf16 or E4M3 bytes")
+    coded = out.dtype in (torch.uint8, torch.float8_e4m3fn)
+    _need(coded or out.dtype == torch.bfloat16, "out must be bf16, E4M3 or FP4 bytes")
+    fp4 = coded and out.shape[-1] * 2 == d  # two E2M1 codes per byte
     _need(W.is_contiguous() and pos_bias.is_contiguous(), "W, pos_bias must be contiguous")
-    if fp8:
+    if fp4:
+        _cuda(out_scale, "out_scale", torch.uint8)
+        _need(out_scale.dim() == 3 and out_scale.shape[2] == d // 16 and out_scale.stride(2) == 1
+              and out_scale.stride(1) == d // 16, "FP4 out_scale: uint8 [B, N_cap, d/16]")
+        dtype, obs, sbs = CSA_FP4_E2M1, 2 * _bstride(out), out_scale.stride(0) // (d // 16)
+    elif coded:
         _cuda(out_scale, "out_scale", torch.float32)
         _need(out_scale.dim() == 2 and out_scale.stride(1) == 1, "out_scale [B, N_cap]")
+        dtype, obs, sbs = CSA_FP8_E4M3, _bstride(out), out_scale.stride(0)
+    else:
+        dtype, obs, sbs = CSA_BF16, _bstride(out), 0
     _need(pos_bias.dim() == 2 and pos_bias.shape[1] == d, "pos_bias [span, d]")
     span = pos_bias.shape[0]
-    common = (_p(W), _p(pos_bias), _p(out), _bstride(out), CSA_FP8_E4M3 if fp8 else CSA_BF16,
-              _p(out_scale) if fp8 else None, out_scale.stride(0) if fp8 else 0,
+    common = (_p(W), _p(pos_bias), _p(out), obs, dtype, _p(out_scale) if coded else None, sbs,
               _p(err_word), _stream(raw.device))
     if span == m:
         st = lib().csa_compress_kv(_p(raw), _bstride(raw), raw.shape[1], B, d, m, block_begin,
@@ -189,6 +200,50 @@ def compress_kv(raw, W, pos_bias, m: int, block_begin: int, n_blocks: int, out,
 
 # ---------------------------------------------------------------- a2 + a3
 
+def _indexer_common(q_idx, w, k_idx, q_pos, n_cmp, m, q_scale, k_scale):
+    """Checks and the shared leading C arguments of the indexer calls.
+
+    bf16: q_idx [B, T, 4, 64], k_idx [B, N_cap, 64] bf16.  E4M3: the same as
+    uint8 codes with q_scale fp32 [B, T, 4], k_scale fp32 [B, N_cap].  FP4:
+    q_idx [B, T, 4, 32], k_idx [B, N_cap, 32] uint8 (two E2M1 codes per byte)
+    with q_scale uint8 [B, T, 4, 4], k_scale uint8 [B, N_cap, 4] (E4M3 scale
+    per 16 channels)."""
+    _cuda(q_idx, "q_idx")
+    _cuda(k_idx, "k_idx")
+    _cuda(w, "w", torch.float32)
+    _cuda(q_pos, "q_pos", torch.int32)
+    _cuda(n_cmp, "n_cmp", torch.int32)
+    coded = q_idx.dtype in (torch.uint8, torch.float8_e4m3fn)
+    _need(coded == (k_idx.dtype in (torch.uint8, torch.float8_e4m3fn)), "q/k dtypes differ")
+    if not coded:
+        _need(q_idx.dtype == torch.bfloat16 and k_idx.dtype == torch.bfloat16, "bf16 expected")
+    fp4 = coded and q_scale is not None and q_scale.dtype == torch.uint8
+    _need(q_idx.is_contiguous() and w.is_contiguous() and q_pos.is_contiguous(),
+          "q_idx, w, q_pos must be contiguous")
+    B, T, H_I, d_I = q_idx.shape
+    N_cap = k_idx.shape[1]
+    if coded:
+        _cuda(q_scale, "q_scale")
+        _cuda(k_scale, "k_scale")
+        _need(q_scale.is_contiguous(), "q_scale layout")
+    if fp4:
+        d_I *= 2
+        _need(k_scale.dtype == torch.uint8 and k_scale.dim() == 3 and k_scale.shape[2] == d_I // 16
+              and k_scale.stride(2) == 1 and k_scale.stride(1) == k_scale.shape[2],
+              "FP4 k_scale: uint8 [B, N_cap, d_I/16]")
+        dtype, kbs, ksbs = CSA_FP4_E2M1, 2 * _bstride(k_idx), k_scale.stride(0) // (d_I // 16)
+    elif coded:
+        _need(q_scale.dtype == torch.float32 and k_scale.dtype == torch.float32
+              and k_scale.stride(1) == 1, "E4M3 scales: fp32")
+        dtype, kbs, ksbs = CSA_FP8_E4M3, _bstride(k_idx), k_scale.stride(0)
+    else:
+        dtype, kbs, ksbs = CSA_BF16, _bstride(k_idx), 0
+    args = (_p(q_idx), _p(q_scale) if coded else None, _p(w), _p(k_idx), kbs,
+            _p(k_scale) if coded else None, ksbs, dtype, _p(q_pos), _p(n_cmp), B, T, H_I, d_I,
+            N_cap, m)
+    return args, (B, T, N_cap)
+
+
 def indexer_scores(q_idx, w, k_idx, q_pos, n_cmp, m: int, q_scale=None, k_scale=None, out=None,
                    err_word=None):
     """Lightning-Indexer scores I(t, s) for every query token (no selection).
@@ -196,33 +251,14 @@ def indexer_scores(q_idx, w, k_idx, q_pos, n_cmp, m: int, q_scale=None, k_scale=
     Arguments as :func:`indexer_topk`.  Returns fp32 [B, T, N_cap]; column s of
     token t is defined for s < n_vis(t) only (the rest is unspecified).
     """
-    _cuda(q_idx, "q_idx")
-    _cuda(k_idx, "k_idx")
-    _cuda(w, "w", torch.float32)
-    _cuda(q_pos, "q_pos", torch.int32)
-    _cuda(n_cmp, "n_cmp", torch.int32)
-    fp8 = q_idx.dtype in (torch.uint8, torch.float8_e4m3fn)
-    _need(fp8 == (k_idx.dtype in (torch.uint8, torch.float8_e4m3fn)), "q/k dtypes differ")
-    if not fp8:
-        _need(q_idx.dtype == torch.bfloat16 and k_idx.dtype == torch.bfloat16, "bf16 expected")
-    _need(q_idx.is_contiguous() and w.is_contiguous() and q_pos.is_contiguous(),
-          "q_idx, w, q_pos must be contiguous")
-    B, T, H_I, d_I = q_idx.shape
-    N_cap = k_idx.shape[1]
-    if fp8:
-        _cuda(q_scale, "q_scale", torch.float32)
-        _cuda(k_scale, "k_scale", torch.float32)
-        _need(q_scale.is_contiguous() and k_scale.stride(1) == 1, "scale layout")
+    args, (B, T, N_cap) = _indexer_common(q_idx, w, k_idx, q_pos, n_cmp, m, q_scale, k_scale)
     sc = out if out is not None else torch.empty((B, T, N_cap), dtype=torch.float32,
                                                  device=q_idx.device)
     _need(sc.dtype == torch.float32 and sc.shape[:2] == (B, T) and sc.shape[2] >= N_cap
           and sc.stride(2) == 1 and sc.stride(1) == sc.shape[2]
           and sc.stride(0) == T * sc.shape[2], "out: contiguous fp32 [B, T, >= N_cap]")
-    st = lib().csa_indexer_scores(
-        _p(q_idx), _p(q_scale) if fp8 else None, _p(w), _p(k_idx), _bstride(k_idx),
-        _p(k_scale) if fp8 else None, k_scale.stride(0) if fp8 else 0,
-        CSA_FP8_E4M3 if fp8 else CSA_BF16, _p(q_pos), _p(n_cmp), B, T, H_I, d_I, N_cap, m,
-        _p(sc), sc.shape[2], _p(err_word), _stream(q_idx.device))
+    st = lib().csa_indexer_scores(*args, _p(sc), sc.shape[2], _p(err_word),
+                                  _stream(q_idx.device))
     _check(st, "csa_indexer_scores")
     return sc
 
@@ -231,38 +267,21 @@ def indexer_topk(q_idx, w, k_idx, q_pos, n_cmp, m: int, k: int, q_scale=None, k_
                  return_scores: bool = False, out=None, ws=None, err_word=None):
     """Top-k compressed entries per query token by Lightning-Indexer score.
 
-    q_idx: [B, T, 4, 64] bf16 (or uint8 E4M3 codes with q_scale fp32 [B, T, 4]);
+    q_idx: [B, T, 4, 64] bf16 (or uint8 E4M3 codes with q_scale fp32 [B, T, 4];
+    or uint8 [B, T, 4, 32] FP4 codes with q_scale uint8 [B, T, 4, 4]);
     w: fp32 [B, T, 4]; k_idx: [B, N_cap, 64] bf16 (or uint8 with k_scale fp32
-    [B, N_cap]); q_pos: int32 [B, T]; n_cmp: int32 [B].
+    [B, N_cap]; or uint8 [B, N_cap, 32] FP4 codes with k_scale uint8
+    [B, N_cap, 4]); q_pos: int32 [B, T]; n_cmp: int32 [B].
     Returns int32 [B, T, k] (ascending, -1 padded) [, fp32 scores [B, T, k]].
     """
-    _cuda(q_idx, "q_idx")
-    _cuda(k_idx, "k_idx")
-    _cuda(w, "w", torch.float32)
-    _cuda(q_pos, "q_pos", torch.int32)
-    _cuda(n_cmp, "n_cmp", torch.int32)
-    fp8 = q_idx.dtype in (torch.uint8, torch.float8_e4m3fn)
-    _need(fp8 == (k_idx.dtype in (torch.uint8, torch.float8_e4m3fn)), "q/k dtypes differ")
-    if not fp8:
-        _need(q_idx.dtype == torch.bfloat16 and k_idx.dtype == torch.bfloat16, "bf16 expected")
-    _need(q_idx.is_contiguous() and w.is_contiguous() and q_pos.is_contiguous(),
-          "q_idx, w, q_pos must be contiguous")
-    B, T, H_I, d_I = q_idx.shape
-    N_cap = k_idx.shape[1]
+    args, (B, T, N_cap) = _indexer_common(q_idx, w, k_idx, q_pos, n_cmp, m, q_scale, k_scale)
     dev = q_idx.device
-    if fp8:
-        _cuda(q_scale, "q_scale", torch.float32)
-        _cuda(k_scale, "k_scale", torch.float32)
-        _need(q_scale.is_contiguous() and k_scale.stride(1) == 1, "scale layout")
     idx = out if out is not None else torch.empty((B, T, k), dtype=torch.int32, device=dev)
     scores = torch.empty((B, T, k), dtype=torch.float32, device=dev) if return_scores else None
     nbytes = lib().csa_indexer_topk_workspace(B, T, N_cap, k)
     wsb, wsn = _ws(nbytes, dev, ws)
-    st = lib().csa_indexer_topk(
-        _p(q_idx), _p(q_scale) if fp8 else None, _p(w), _p(k_idx), _bstride(k_idx),
-        _p(k_scale) if fp8 else None, k_scale.stride(0) if fp8 else 0,
-        CSA_FP8_E4M3 if fp8 else CSA_BF16, _p(q_pos), _p(n_cmp), B, T, H_I, d_I, N_cap, m, k,
-        _p(idx), _p(scores), _p(wsb), wsn, _p(err_word), _stream(dev))
+    st = lib().csa_indexer_topk(*args, k, _p(idx), _p(scores), _p(wsb), wsn, _p(err_word),
+                                _stream(dev))
     _check(st, "csa_indexer_topk")
     return (idx, scores) if return_scores else idx
 
@@ -274,31 +293,11 @@ def indexer_topk_static(q_idx, w, k_idx, q_pos, n_cmp, m: int, k: int, q_scale=N
     are still allocated by torch unless `out` is given).  Problems whose
     workspace would exceed INDEXER_STATIC_SCRATCH_BYTES are refused.  Calls
     that may run at the same time share the scratch and race."""
-    _cuda(q_idx, "q_idx")
-    _cuda(k_idx, "k_idx")
-    _cuda(w, "w", torch.float32)
-    _cuda(q_pos, "q_pos", torch.int32)
-    _cuda(n_cmp, "n_cmp", torch.int32)
-    fp8 = q_idx.dtype in (torch.uint8, torch.float8_e4m3fn)
-    _need(fp8 == (k_idx.dtype in (torch.uint8, torch.float8_e4m3fn)), "q/k dtypes differ")
-    if not fp8:
-        _need(q_idx.dtype == torch.bfloat16 and k_idx.dtype == torch.bfloat16, "bf16 expected")
-    _need(q_idx.is_contiguous() and w.is_contiguous() and q_pos.is_contiguous(),
-          "q_idx, w, q_pos must be contiguous")
-    B, T, H_I, d_I = q_idx.shape
-    N_cap = k_idx.shape[1]
+    args, (B, T, N_cap) = _indexer_common(q_idx, w, k_idx, q_pos, n_cmp, m, q_scale, k_scale)
     dev = q_idx.device
-    if fp8:
-        _cuda(q_scale, "q_scale", torch.float32)
-        _cuda(k_scale, "k_scale", torch.float32)
-        _need(q_scale.is_contiguous() and k_scale.stride(1) == 1, "scale layout")
     idx = out if out is not None else torch.empty((B, T, k), dtype=torch.int32, device=dev)
     scores = torch.empty((B, T, k), dtype=torch.float32, device=dev) if return_scores else None
-    st = lib().csa_indexer_topk_static(
-        _p(q_idx), _p(q_scale) if fp8 else None, _p(w), _p(k_idx), _bstride(k_idx),
-        _p(k_scale) if fp8 else None, k_scale.stride(0) if fp8 else 0,
-        CSA_FP8_E4M3 if fp8 else CSA_BF16, _p(q_pos), _p(n_cmp), B, T, H_I, d_I, N_cap, m, k,
-        _p(idx), _p(scores), _p(err_word), _stream(dev))
+    st = lib().csa_indexer_topk_static(*args, k, _p(idx), _p(scores), _p(err_word), _stream(dev))
     _check(st, "csa_indexer_topk_static")
     return (idx, scores) if return_scores else idx
 

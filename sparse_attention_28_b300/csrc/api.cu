@@ -99,7 +99,8 @@ int csa_compress_kv_span(const void* raw, int64_t raw_bstride, int64_t raw_cap, 
   (void)err_word;
   if (B < 0 || d <= 0 || m <= 0 || span < m || block_begin < 0 || n_blocks < 0)
     return CSA_ERR_INVALID_ARG;
-  if (out_dtype != CSA_BF16 && out_dtype != CSA_FP8_E4M3) return CSA_ERR_UNSUPPORTED;
+  if (out_dtype != CSA_BF16 && out_dtype != CSA_FP8_E4M3 && out_dtype != CSA_FP4_E2M1)
+    return CSA_ERR_UNSUPPORTED;
   if ((d != 64 && d != 128) || span > 256) return CSA_ERR_UNSUPPORTED;
   if (B == 0 || n_blocks == 0) return CSA_OK;
   if (!raw || !W || !pos_bias || !out) return CSA_ERR_INVALID_ARG;
@@ -108,9 +109,10 @@ int csa_compress_kv_span(const void* raw, int64_t raw_bstride, int64_t raw_cap, 
   if (raw_cap < span || raw_bstride % 8 != 0 || raw_cap * d > raw_bstride)
     return CSA_ERR_INVALID_ARG;
   if (end_block * d > out_bstride) return CSA_ERR_INVALID_ARG;
-  if (out_dtype == CSA_FP8_E4M3) {
+  if (out_dtype != CSA_BF16) {
     if (!out_scale || !aligned4(out_scale) || end_block > scale_bstride) return CSA_ERR_INVALID_ARG;
   }
+  if (out_dtype == CSA_FP4_E2M1 && out_bstride % 32 != 0) return CSA_ERR_INVALID_ARG;
   CompressArgs a;
   a.raw = reinterpret_cast<const bf16*>(raw);
   a.raw_bstride = raw_bstride;
@@ -126,6 +128,7 @@ int csa_compress_kv_span(const void* raw, int64_t raw_bstride, int64_t raw_cap, 
   a.out = out;
   a.out_bstride = out_bstride;
   a.fp8 = out_dtype == CSA_FP8_E4M3;
+  a.fp4 = out_dtype == CSA_FP4_E2M1;
   a.out_scale = out_scale;
   a.scale_bstride = scale_bstride;
   return cuda_status(launch_compress(a, reinterpret_cast<cudaStream_t>(stream)));
@@ -155,7 +158,8 @@ int indexer_checks(const void* q_idx, const float* q_scale, const float* w, cons
                    const int32_t* q_pos, const int32_t* n_cmp, int B, int T, int H_I, int d_I,
                    int N_cap, int m) {
   if (B < 0 || T < 0 || N_cap < 0 || m <= 0) return CSA_ERR_INVALID_ARG;
-  if (idx_dtype != CSA_BF16 && idx_dtype != CSA_FP8_E4M3) return CSA_ERR_UNSUPPORTED;
+  if (idx_dtype != CSA_BF16 && idx_dtype != CSA_FP8_E4M3 && idx_dtype != CSA_FP4_E2M1)
+    return CSA_ERR_UNSUPPORTED;
   if (H_I != 4 || d_I != 64) return CSA_ERR_UNSUPPORTED;
   if (N_cap > kMaxNcap) return CSA_ERR_UNSUPPORTED;
   if (B == 0 || T == 0) return CSA_OK;
@@ -169,6 +173,11 @@ int indexer_checks(const void* q_idx, const float* q_scale, const float* w, cons
     if (!q_scale || !k_scale || !aligned4(q_scale) || !aligned4(k_scale))
       return CSA_ERR_INVALID_ARG;
     if (k_bstride % 16 != 0 || ks_bstride < N_cap) return CSA_ERR_INVALID_ARG;
+  } else if (idx_dtype == CSA_FP4_E2M1) {
+    // codes: 32 bytes per entry; scales: 4 E4M3 bytes per entry / query head
+    if (!q_scale || !k_scale || !aligned4(q_scale) || !aligned4(k_scale))
+      return CSA_ERR_INVALID_ARG;
+    if (k_bstride % 32 != 0 || ks_bstride < N_cap) return CSA_ERR_INVALID_ARG;
   } else if (k_bstride % 8 != 0) {
     return CSA_ERR_INVALID_ARG;
   }
@@ -190,6 +199,7 @@ IndexerArgs indexer_args(const void* q_idx, const float* q_scale, const float* w
   a.k_scale = k_scale;
   a.ks_bstride = ks_bstride;
   a.fp8 = idx_dtype == CSA_FP8_E4M3;
+  a.fp4 = idx_dtype == CSA_FP4_E2M1;
   a.q_pos = q_pos;
   a.n_cmp = n_cmp;
   a.T = T;

@@ -6,6 +6,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
+#include <cuda_fp4.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -66,6 +67,20 @@ __device__ __forceinline__ void mma_bf16_16816(float* d, const uint32_t* a, uint
       "{%8,%9}, {%0,%1,%2,%3};\n"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// An E4M3 scale byte (low 8 bits of x) as an f16 pair (exact: E4M3 values
+// are f16 values).
+__device__ __forceinline__ __half2 e4m3_half2(uint32_t x) {
+  const __half_raw r = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)(x & 0xFFu), __NV_E4M3);
+  const __half h(r);
+  return __halves2half2(h, h);
+}
+// Two E2M1 codes (low byte of x: low nibble first) times an f16 pair of
+// scales, packed as an f16 pair; exact when the products stay in range.
+__device__ __forceinline__ uint32_t fp4x2_scaled(uint32_t x, __half2 s) {
+  const __half2_raw r = __nv_cvt_fp4x2_to_halfraw2((__nv_fp4x2_storage_t)(x & 0xFFu), __NV_E2M1);
+  const __half2 v = __hmul2(__half2(r), s);
+  return *reinterpret_cast<const uint32_t*>(&v);
 }
 // Same with f16 inputs (used for E4M3 data, which converts to f16 exactly).
 __device__ __forceinline__ void mma_f16_16816(float* d, const uint32_t* a, uint32_t b0,

@@ -103,6 +103,29 @@ __global__ void __launch_bounds__(D) compress_kernel(CompressArgs a) {
   }
   const float y = num / den;
 
+  if (a.fp4) {
+    // FP4: per 16 channels one E4M3 scale, the nearest to amax / 6 (1 if the
+    // block is zero, at least the smallest positive E4M3 value), and E2M1
+    // codes of y / scale, two per byte
+    float am = fabsf(y);
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, o));
+    uint32_t sc = am > 0.f ? (uint32_t)__nv_cvt_float_to_fp8(am / 6.f, __NV_SATFINITE, __NV_E4M3)
+                           : 0x38u;  // E4M3 1.0
+    float scv = __half2float(__half(__nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)sc, __NV_E4M3)));
+    if (scv == 0.f) {
+      sc = 1u;  // 2^-9
+      scv = __half2float(__half(__nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)1, __NV_E4M3)));
+    }
+    const uint32_t q = (uint32_t)__nv_cvt_float_to_fp4(y / scv, __NV_E2M1, cudaRoundNearest) & 0xFu;
+    const uint32_t q1 = __shfl_down_sync(0xFFFFFFFFu, q, 1);
+    uint8_t* out = reinterpret_cast<uint8_t*>(a.out) + (int64_t)b * (a.out_bstride / 2) + j * (D / 2);
+    if ((c & 1) == 0) out[c >> 1] = static_cast<uint8_t>(q | (q1 << 4));
+    if ((c & 15) == 0)
+      reinterpret_cast<uint8_t*>(a.out_scale)[((int64_t)b * a.scale_bstride + j) * (D / 16) +
+                                              (c >> 4)] = static_cast<uint8_t>(sc);
+    return;
+  }
   if (!a.fp8) {
     bf16* out = reinterpret_cast<bf16*>(a.out) + (int64_t)b * a.out_bstride + j * D;
     out[c] = __float2bfloat16_rn(y);

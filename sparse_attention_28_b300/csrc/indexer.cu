@@ -41,6 +41,7 @@ constexpr int kThreads = 256;     // score kernel
 constexpr int kChunk = 2048;      // entries per score CTA
 constexpr int kUnrollBf16 = 4;    // 16-entry groups in flight per warp (bf16 keys)
 constexpr int kUnrollFp8 = 8;     // (E4M3 keys: half the bytes per row)
+constexpr int kUnrollFp4 = 8;     // (FP4 keys)
 constexpr int kQueryChunk = 256;  // queries per launch (bounds the workspace)
 constexpr int kSelThreads = 1024;  // select CTA size for few queries (512 for many)
 constexpr int kMaxCluster = 16;  // select CTAs per query
@@ -139,16 +140,32 @@ __device__ void bin_from_top(const int (&bins)[PER], int first_bin, int need, in
 //         [64+16c, 64+16c+16); k-step s takes word s of each vector.
 //   E4M3 (m16n8k32, products exact in fp32): thread (g, c) holds row bytes
 //         [16c, 16c+16); k-step s takes words 2s and 2s+1.
+//   FP4 (E2M1 codes, one E4M3 scale per 16 channels; m16n8k16 f16): as
+//         bf16, with each byte of codes expanded to an f16 pair and
+//         multiplied by its block's scale (exact: at most 6 significant
+//         bits, within the f16 range), so products are exact in fp32.
 // Scores of entries [e0, e1) of query qid into scores[e]: each warp takes
-// 16-entry groups, kUnroll groups in flight.
-template <bool FP8>
+// 16-entry groups, kUnroll groups in flight.  FMT: 0 bf16, 1 E4M3, 2 FP4.
+template <int FMT>
 __device__ __forceinline__ void score_range(const IndexerArgs& a, int qid, int64_t e0, int64_t e1,
                                             float* scores, int warp, int g, int c) {
+  constexpr bool FP8 = FMT == 1, FP4 = FMT == 2;
   // query fragments (heads g < 4) and head weights (heads 2c, 2c+1 for c < 2)
   uint32_t qb0[4] = {0, 0, 0, 0}, qb1[4] = {0, 0, 0, 0};
   float w0 = 0.f, w1 = 0.f;
   if (g < kHI) {
-    if (FP8) {
+    if (FP4) {
+      const uint8_t* qr = reinterpret_cast<const uint8_t*>(a.q) + ((int64_t)qid * kHI + g) * (kDI / 2);
+      const uint8_t* qs = reinterpret_cast<const uint8_t*>(a.q_scale) + ((int64_t)qid * kHI + g) * (kDI / 16);
+      const uint32_t v0 = __ldg(reinterpret_cast<const uint32_t*>(qr + 4 * c));
+      const uint32_t v1 = __ldg(reinterpret_cast<const uint32_t*>(qr + 16 + 4 * c));
+      const __half2 s0 = e4m3_half2(__ldg(qs + (c >> 1))), s1 = e4m3_half2(__ldg(qs + 2 + (c >> 1)));
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        qb0[t] = fp4x2_scaled(v0 >> (8 * t), s0);
+        qb1[t] = fp4x2_scaled(v1 >> (8 * t), s1);
+      }
+    } else if (FP8) {
       const uint8_t* qr = reinterpret_cast<const uint8_t*>(a.q) + ((int64_t)qid * kHI + g) * kDI;
       const uint4 v = __ldg(reinterpret_cast<const uint4*>(qr + 16 * c));
       qb0[0] = v.x; qb0[1] = v.y; qb0[2] = v.z; qb0[3] = v.w;
@@ -170,7 +187,7 @@ __device__ __forceinline__ void score_range(const IndexerArgs& a, int qid, int64
   }
 
   const int b = qid / a.T;
-  constexpr int kUnroll = FP8 ? kUnrollFp8 : kUnrollBf16;
+  constexpr int kUnroll = FMT == 0 ? kUnrollBf16 : FMT == 1 ? kUnrollFp8 : kUnrollFp4;
   const int n_groups = (int)((e1 - e0 + 15) / 16);
   for (int gb = warp * kUnroll; gb < n_groups; gb += (kThreads / 32) * kUnroll) {
     uint4 ra[kUnroll][2], rb[kUnroll][2];  // rows g and g+8 of each group
@@ -178,7 +195,24 @@ __device__ __forceinline__ void score_range(const IndexerArgs& a, int qid, int64
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const int64_t ea = e0 + (int64_t)(gb + u) * 16 + g, eb = ea + 8;
-      if (FP8) {
+      if (FP4) {
+        // codes (two 4-byte chunks per row) and the row's 4 block scales
+        const uint8_t* kb = reinterpret_cast<const uint8_t*>(a.keys) + (int64_t)b * (a.k_bstride / 2);
+        const uint32_t* sb = reinterpret_cast<const uint32_t*>(a.k_scale) + (int64_t)b * a.ks_bstride;
+        const uint4 z = make_uint4(0, 0, 0, 0);
+        ra[u][0] = z;
+        rb[u][0] = z;
+        if (ea < e1) {
+          ra[u][0].x = __ldg(reinterpret_cast<const uint32_t*>(kb + ea * (kDI / 2) + 4 * c));
+          ra[u][0].y = __ldg(reinterpret_cast<const uint32_t*>(kb + ea * (kDI / 2) + 16 + 4 * c));
+          ra[u][0].z = __ldg(sb + ea);
+        }
+        if (eb < e1) {
+          rb[u][0].x = __ldg(reinterpret_cast<const uint32_t*>(kb + eb * (kDI / 2) + 4 * c));
+          rb[u][0].y = __ldg(reinterpret_cast<const uint32_t*>(kb + eb * (kDI / 2) + 16 + 4 * c));
+          rb[u][0].z = __ldg(sb + eb);
+        }
+      } else if (FP8) {
         const int64_t es = c == 1 ? eb : ea;
         ks[u] = (c < 2 && es < e1) ? __ldg(a.k_scale + (int64_t)b * a.ks_bstride + es) : 0.f;
         const uint8_t* kb = reinterpret_cast<const uint8_t*>(a.keys) + (int64_t)b * a.k_bstride;
@@ -199,7 +233,20 @@ __device__ __forceinline__ void score_range(const IndexerArgs& a, int qid, int64
     for (int u = 0; u < kUnroll; ++u) {
       if (gb + u >= n_groups) break;
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      if (FP8) {
+      if (FP4) {
+        // this thread's blocks: c >> 1 (channels 8c..) and 2 + (c >> 1) (32 + 8c..)
+        const int sh0 = 8 * (c >> 1), sh1 = 8 * (2 + (c >> 1));
+        const __half2 sa0 = e4m3_half2(ra[u][0].z >> sh0), sa1 = e4m3_half2(ra[u][0].z >> sh1);
+        const __half2 sb0 = e4m3_half2(rb[u][0].z >> sh0), sb1 = e4m3_half2(rb[u][0].z >> sh1);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const uint32_t af[4] = {fp4x2_scaled(ra[u][0].x >> (8 * t), sa0),
+                                  fp4x2_scaled(rb[u][0].x >> (8 * t), sb0),
+                                  fp4x2_scaled(ra[u][0].y >> (8 * t), sa1),
+                                  fp4x2_scaled(rb[u][0].y >> (8 * t), sb1)};
+          mma_f16_16816(acc, af, qb0[t], qb1[t]);
+        }
+      } else if (FP8) {
         const uint32_t a0[4] = {ra[u][0].x, rb[u][0].x, ra[u][0].y, rb[u][0].y};
         const uint32_t a1[4] = {ra[u][0].z, rb[u][0].z, ra[u][0].w, rb[u][0].w};
         mma_e4m3_16832(acc, a0, qb0[0], qb0[1]);
@@ -235,8 +282,11 @@ __device__ __forceinline__ void score_range(const IndexerArgs& a, int qid, int64
 // per CTA.  A CTA walks its range query by query (loading that query's
 // fragments and weights), so that every CTA streams the same number of key
 // bytes whatever the queries' visible counts.
-template <bool FP8>
-__global__ void __launch_bounds__(kThreads) indexer_score_kernel(IndexerArgs a, int q0, int qc,
+// CTAs per SM (a third FP4 CTA within 85 registers spilled and was slower).
+constexpr int score_ctas_per_sm(int) { return 2; }
+
+template <int FMT>
+__global__ void __launch_bounds__(kThreads, score_ctas_per_sm(FMT)) indexer_score_kernel(IndexerArgs a, int q0, int qc,
                                                                 WsLayout L) {
   pdl_trigger();
   pdl_wait();
@@ -269,7 +319,7 @@ __global__ void __launch_bounds__(kThreads) indexer_score_kernel(IndexerArgs a, 
     if (s_hi <= s_lo) continue;
     const int64_t e0 = (int64_t)s_lo * 16;
     const int64_t e1 = min((int64_t)s_hi * 16, (int64_t)nvs[lq]);
-    score_range<FP8>(a, qid, e0, e1, L.scores + (int64_t)lq * L.stride, warp, g, c);
+    score_range<FMT>(a, qid, e0, e1, L.scores + (int64_t)lq * L.stride, warp, g, c);
   }
 }
 
@@ -500,14 +550,16 @@ cudaError_t launch_scores(const IndexerArgs& a, int q0, int qc, const WsLayout& 
                           cudaStream_t st) {
   if (a.T > 8 && indexer_gemm_applies(a))
     return launch_indexer_gemm(a, q0, qc, L.scores, L.stride, st);
-  // one wave (two CTAs per SM), fewer when there is little work: at least
-  // kChunk entries' worth of groups per CTA on average
+  // one wave (the CTAs per SM the format fits), fewer when there is little
+  // work: at least kChunk entries' worth of groups per CTA on average
   const int64_t groups = (int64_t)qc * ((a.N_cap + 15) / 16);
   int64_t n_cta = (groups * 16 + kChunk - 1) / kChunk;
-  if (n_cta > 2 * kNumSMs) n_cta = 2 * kNumSMs;
+  const int per_sm = score_ctas_per_sm(a.fp4 ? 2 : a.fp8 ? 1 : 0);
+  if (n_cta > per_sm * kNumSMs) n_cta = per_sm * kNumSMs;
   const dim3 g1((unsigned)(n_cta > 0 ? n_cta : 1));
-  if (a.fp8) return launch_pdl(indexer_score_kernel<true>, g1, dim3(kThreads), 0, st, a, q0, qc, L);
-  return launch_pdl(indexer_score_kernel<false>, g1, dim3(kThreads), 0, st, a, q0, qc, L);
+  if (a.fp4) return launch_pdl(indexer_score_kernel<2>, g1, dim3(kThreads), 0, st, a, q0, qc, L);
+  if (a.fp8) return launch_pdl(indexer_score_kernel<1>, g1, dim3(kThreads), 0, st, a, q0, qc, L);
+  return launch_pdl(indexer_score_kernel<0>, g1, dim3(kThreads), 0, st, a, q0, qc, L);
 }
 
 }  // namespace

@@ -210,7 +210,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
 }  // namespace
 
 bool indexer_gemm_applies(const IndexerArgs& a) {
-  return !a.fp8 && a.T % kGQ == 0 && a.T >= kGQ && a.k_bstride % 64 == 0;
+  return !a.fp8 && !a.fp4 && a.T % kGQ == 0 && a.T >= kGQ && a.k_bstride % 64 == 0;
 }
 
 // Scores of queries [q0, q0 + qc) (qc a multiple of 64, whole blocks of one

@@ -71,6 +71,7 @@ struct IndexerArgs {
   const float* k_scale;
   int64_t ks_bstride;
   int fp8;
+  int fp4;  // E2M1 codes with E4M3 block scales (one per 16 channels)
   const int32_t* q_pos;
   const int32_t* n_cmp;
   int T;
@@ -106,6 +107,7 @@ struct CompressArgs {
   void* out;
   int64_t out_bstride;
   int fp8;
+  int fp4;  // E2M1 codes with E4M3 block scales (one per 16 channels)
   float* out_scale;
   int64_t scale_bstride;
 };

@@ -128,7 +128,10 @@ class CsaDecodeStep(_Step):
                 j = n // m - 1
                 self.k_cmp[b, j] = float("nan")
                 self.v_cmp[b, j] = float("nan")
-                if self.k_scale is not None:
+                if self.k_scale is not None and self.k_scale.dtype == torch.uint8:
+                    self.k_idx[b, j] = 0x77      # FP4 codes 6.0 ...
+                    self.k_scale[b, j] = 0x7F    # ... times an E4M3 NaN scale
+                elif self.k_scale is not None:
                     self.k_idx[b, j] = 0x7F
                     self.k_scale[b, j] = float("nan")
                 else:

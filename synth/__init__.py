@@ -49,6 +49,7 @@ class Workload:
     k: int = 0               # top-k (CSA)
     T: int = 1               # query tokens per sequence
     idx_fp8: bool = False    # FP8 E4M3 indexer keys / queries
+    idx_fp4: bool = False    # FP4 E2M1 indexer keys / queries (E4M3 scale per 16 channels)
     stream_compress: bool = False  # decode step compresses the newest block first
     D: int = D_HEAD
     W: int = WINDOW
@@ -87,6 +88,9 @@ WORKLOADS = {
                                k=2048, T=4096),
     "csa_decode_1m_fp8": Workload("csa_decode_1m_fp8", "csa_decode", B=8, L=1048576, m=4,
                                   H=64, k=2048, idx_fp8=True, stream_compress=True),
+    # the same with the FP4 indexer path
+    "csa_decode_1m_fp4": Workload("csa_decode_1m_fp4", "csa_decode", B=8, L=1048576, m=4,
+                                  H=64, k=2048, idx_fp4=True, stream_compress=True),
     # the 128K decode with batch-invariant attention (fixed 320-key splits)
     "csa_decode_128k_bi": Workload("csa_decode_128k_bi", "csa_decode", B=32, L=131072, m=4,
                                    H=64, k=1024, batch_invariant=320),
@@ -120,6 +124,20 @@ def randn_fp8_rows(shape, seed: int, tid: int, device="cpu"):
     s = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
     codes = (x / s.unsqueeze(-1)).to(torch.float8_e4m3fn).view(torch.uint8)
     return codes, s.contiguous()
+
+
+def rand_fp4_rows(shape, seed: int, tid: int, device="cpu"):
+    """Random FP4-stored vectors of shape[-1] channels: uniformly drawn E2M1
+    codes (two per byte, uint8 [..., d/2]) and E4M3 block-scale codes, one per
+    16 channels (uint8 [..., d/16]), drawn from 0x28 .. 0x47 (scales 2^-2 ..
+    2^1.9): random bytes, no arithmetic of the method."""
+    *lead, d = shape
+    g = _gen(seed, tid, device)
+    codes = torch.randint(0, 256, (*lead, d // 2), generator=g, device=device,
+                          dtype=torch.int32).to(torch.uint8)
+    scales = torch.randint(0x28, 0x48, (*lead, d // 16), generator=g, device=device,
+                           dtype=torch.int32).to(torch.uint8)
+    return codes, scales
 
 
 def make_inputs(wl: Workload, seed: int = 0, device="cpu") -> dict:
@@ -163,7 +181,11 @@ def make_inputs(wl: Workload, seed: int = 0, device="cpu") -> dict:
         out["v_win"] = randn((B, W, D), seed, 6, dev)
         if wl.kind == "csa_decode":
             out["w"] = randn((B, 1, wl.H_I), seed, 7, dev, dtype=torch.float32)
-            if wl.idx_fp8:
+            if wl.idx_fp4:
+                out["q_idx"], out["q_scale"] = rand_fp4_rows((B, 1, wl.H_I, wl.d_I), seed, 8,
+                                                             dev)
+                out["k_idx"], out["k_scale"] = rand_fp4_rows((B, N_cap, wl.d_I), seed, 9, dev)
+            elif wl.idx_fp8:
                 out["q_idx"], out["q_scale"] = randn_fp8_rows((B, 1, wl.H_I, wl.d_I), seed, 8,
                                                               dev)
                 out["k_idx"], out["k_scale"] = randn_fp8_rows((B, N_cap, wl.d_I), seed, 9, dev)

@@ -72,6 +72,10 @@ def test_kernel_algorithmic_bytes():
     wl8 = synth.WORKLOADS["csa_decode_1m_fp8"]
     assert bench.kernel_algorithmic(wl8, "indexer_score") == {
         "bytes": 8 * 262144 * (68 + 4) + 8 * 4 * (68 + 4)}
+    # FP4 keys: 32 code bytes + 4 E4M3 block scales per row
+    wl4 = synth.WORKLOADS["csa_decode_1m_fp4"]
+    assert bench.kernel_algorithmic(wl4, "indexer_score") == {
+        "bytes": 8 * 262144 * (36 + 4) + 8 * 4 * (36 + 4)}
     hca = synth.WORKLOADS["hca_decode_1m"]
     assert bench.kernel_algorithmic(hca, "attention") == bench.algorithmic(hca)["attention"]
 

@@ -105,7 +105,71 @@ def test_compress_overlap_parity(cuda_device, d, m, span, fp8, ring):
     assert np.all(np.abs(dec - exact_v) <= e4m3_half_step(exact_v) * (1 + 1e-5) + 1e-12)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_compress_fp4_parity(cuda_device, d):
+    # FP4 output: E4M3 scale per 16 channels near amax / 6, E2M1 codes of
+    # y / scale; checked against the oracle's fp64 entries: scales within
+    # E4M3 rounding of amax / 6, values within the FP4 step of the GPU's
+    # scale, codes equal to the oracle's (on the oracle's scale) almost always
+    B, bb, nb, m = 3, 1, 6, 4
+    N_cap = bb + nb + 1
+    raw = rnd((B, N_cap * m, d), 21)
+    W = rnd((d, d), 22, 1 / math.sqrt(d))
+    pb = rnd((m, d), 23, dtype=torch.float32)
+    out = torch.full((B, N_cap, d // 2), 0x77, dtype=torch.uint8, device=DEV)
+    sc = torch.full((B, N_cap, d // 16), 0xFF, dtype=torch.uint8, device=DEV)
+    csa.compress_kv(raw.to(DEV), W.to(DEV), pb.to(DEV), m, bb, nb, out, sc)
+    torch.cuda.synchronize()
+    y = oracle.compress(u16(raw), u16(W), pb.numpy(), m, bb, nb)
+    codes, scales = u8(out[:, bb:bb + nb]), u8(sc[:, bb:bb + nb])
+    gs = oracle.e4m3_decode(scales)
+    amax = np.abs(y.reshape(B, nb, d // 16, 16)).max(axis=3)
+    assert np.all(np.abs(gs - amax / 6) <= amax / 6 * 2.0 ** -4 * (1 + 1e-6))
+    dec = oracle.fp4_dequantize(codes, scales)
+    r = np.abs(y) / np.repeat(gs, 16, axis=2)
+    half = np.where(r < 2, 0.25, np.where(r < 4, 0.5, 1.0)) * np.repeat(gs, 16, axis=2)
+    over = np.maximum(np.abs(y) - 6 * np.repeat(gs, 16, axis=2), 0)
+    assert np.all(np.abs(dec - y) <= np.maximum(half, over) * (1 + 1e-5) + 1e-12)
+    ref_codes, ref_scales = oracle.quantize_fp4_rows(y)
+    assert np.mean(scales == ref_scales) > 0.97
+    assert np.mean(codes == ref_codes) > 0.95
+    assert (u8(out[:, :bb]) == 0x77).all() and (u8(out[:, bb + nb:]) == 0x77).all()
+
+
 # ---------------------------------------------------------------- a2 + a3 indexer top-k
+
+@pytest.mark.parametrize("T", [1, 5, 12])
+def test_indexer_fp4_parity(cuda_device, T):
+    # FP4 indexer vectors (E2M1 codes + E4M3 scale per 16 channels): scores
+    # element by element and the top-k set against the oracle
+    B, N_cap, m, k = 3, 3000, 4, 200
+    n_cmp = [3000, 2100, 150]
+    q_pos = [[(4 * n_cmp[b] + 3) - 37 * (T - 1 - t) for t in range(T)] for b in range(B)]
+    qc, qs = synth.rand_fp4_rows((B, T, 4, 64), 31, 1)
+    kc, ks = synth.rand_fp4_rows((B, N_cap, 64), 31, 2)
+    for b in range(B):  # entries beyond n_cmp are never read: poison them
+        kc[b, n_cmp[b]:] = 0x77
+        ks[b, n_cmp[b]:] = 0x7F
+    w = synth.randn((B, T, 4), 31, 3, dtype=torch.float32)
+    qp = torch.tensor(q_pos, dtype=torch.int32)
+    nc = torch.tensor(n_cmp, dtype=torch.int32)
+    args = (qc.to(DEV), w.to(DEV), kc.to(DEV), qp.to(DEV), nc.to(DEV), m)
+    got = csa.indexer_scores(*args, q_scale=qs.to(DEV), k_scale=ks.to(DEV))
+    idx, sc = csa.indexer_topk(*args, k, q_scale=qs.to(DEV), k_scale=ks.to(DEV),
+                               return_scores=True)
+    torch.cuda.synchronize()
+    want, nv = oracle.indexer_scores(u8(qc), w.numpy(), u8(kc), qp.numpy(), nc.numpy(), m,
+                                     oracle.FP4_E2M1, u8(qs), u8(ks))
+    got = got.cpu().numpy().astype(np.float64)
+    for b in range(B):
+        for t in range(T):
+            n = int(nv[b, t])
+            np.testing.assert_allclose(got[b, t, :n], want[b, t, :n], rtol=2e-5, atol=2e-4)
+    ref = oracle.topk(want, nv, k)
+    check_topk(idx.cpu().numpy(), ref, want, nv, k, "indexer fp4")
+
+
+
 
 def _indexer_case(B, T, N_cap, n_cmp, q_pos, fp8, seed=5):
     if fp8:
