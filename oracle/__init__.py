@@ -91,6 +91,8 @@ def _load():
             lib.orc_compress.restype = I
             lib.orc_compress_span.argtypes = [P, L, I, I, I, I, I, I, P, P, P]
             lib.orc_compress_span.restype = I
+            lib.orc_grouped_out_proj.argtypes = [P, P, L, I, I, I, I, P]
+            lib.orc_grouped_out_proj.restype = I
             lib.orc_indexer_scores.argtypes = [P, P, P, P, L, P, L, I, P, P, I, I, I, I, I, L,
                                                P, P]
             lib.orc_indexer_scores.restype = I
@@ -373,3 +375,28 @@ def csa_prefill(q, k_cmp, v_cmp, topk_idx, k_raw, v_raw, q_pos, window, sink, sc
                       np.asarray(topk_idx).reshape(B * T, -1), k_raw, v_raw, window, sink,
                       scale, raw_base)
     return out.reshape(B, T, H, D), lse.reshape(B, T, H)
+
+
+# --------------------------------------------------------------------------
+# grouped output projection
+# --------------------------------------------------------------------------
+
+def grouped_out_proj(o, W) -> np.ndarray:
+    """y[q][g*d_g + r] = sum_j W[g][r][j] * o[q][g*K + j] in fp64, K = (H/G)*D.
+
+    o: uint16 bf16 bits [n, H, D] (or [n, H*D]); W: uint16 [G, d_g, K].
+    Returns fp64 [n, G*d_g].
+    """
+    o = _c(o, np.uint16)
+    W = _c(W, np.uint16)
+    G, d_g, K = W.shape
+    n = o.shape[0]
+    HD = o.size // n
+    assert HD == G * K
+    D = o.shape[-1] if o.ndim == 3 else K
+    H = HD // D
+    y = np.empty((n, G * d_g), np.float64)
+    rc = _load().orc_grouped_out_proj(_ptr(o), _ptr(W), n, H, D, G, d_g, _ptr(y))
+    _check(rc, "grouped_out_proj")
+    return y
+

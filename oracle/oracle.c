@@ -583,3 +583,47 @@ int orc_attend(const uint16_t* q, const int32_t* qb, const int32_t* qt, int64_t 
   }
   return err;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Grouped output projection after the MQA core attention                   */
+/* ------------------------------------------------------------------------ */
+
+/* The hyper.ai DeepSeek-V4 page (Method, CSA paragraph) follows the MQA core
+ * attention with "a grouped output projection".  Reading: the H heads of a
+ * query's attention output are split into G groups of H/G consecutive heads;
+ * group g's K = (H/G)*D values o_g (heads in order, D channels each) are
+ * projected by its own matrix W_g (d_g rows of K):
+ *     y[q][g*d_g + r] = sum_{j < K} W[g][r][j] * o[q][g*K + j]
+ * o: bf16 [n][H*D]; W: bf16 [G][d_g][K]; y: fp64 [n][G*d_g]. */
+int orc_grouped_out_proj(const uint16_t* o, const uint16_t* W, int64_t n, int H, int D, int G,
+                         int d_g, double* y) {
+  if (!o || !W || !y || n < 0 || H <= 0 || D <= 0 || G <= 0 || d_g <= 0 || H % G != 0)
+    return ORC_ERR_ARG;
+  const int K = (H / G) * D;
+  int err = ORC_OK;
+#pragma omp parallel
+  {
+    double* ov = (double*)malloc(sizeof(double) * (size_t)K);
+    double* wv = (double*)malloc(sizeof(double) * (size_t)K);
+#pragma omp for collapse(2) schedule(dynamic)
+    for (int64_t q = 0; q < n; ++q) {
+      for (int g = 0; g < G; ++g) {
+        if (!ov || !wv) {
+#pragma omp atomic write
+          err = ORC_ERR_NOMEM;
+          continue;
+        }
+        orc_bf16_decode_array(o + q * (int64_t)H * D + (int64_t)g * K, ov, K);
+        for (int r = 0; r < d_g; ++r) {
+          orc_bf16_decode_array(W + ((int64_t)g * d_g + r) * K, wv, K);
+          double s = 0.0;
+          for (int j = 0; j < K; ++j) s += wv[j] * ov[j];
+          y[q * (int64_t)G * d_g + (int64_t)g * d_g + r] = s;
+        }
+      }
+    }
+    free(ov);
+    free(wv);
+  }
+  return err;
+}

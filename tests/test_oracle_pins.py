@@ -583,3 +583,35 @@ def test_attention_rejects_out_of_range_indices():
     with pytest.raises(ValueError):  # window reaches rows the raw buffer does not hold
         oracle.csa_decode(q, K, K, np.array([[0]], np.int32), K, K, np.array([16]), 4, None,
                           1.0)
+
+
+# ---------------------------------------------------------------- grouped output projection
+
+def test_out_proj_hand_example():
+    g = _golden("out_proj_hand.txt")
+    o = bf16_bits(g["o"]).reshape(1, 2, 2)
+    W = bf16_bits(np.stack([g["W0"], g["W1"]]))
+    np.testing.assert_array_equal(oracle.grouped_out_proj(o, W)[0], g["y"])
+
+
+def test_out_proj_one_group_is_a_matmul():
+    n, H, D, d = 5, 4, 8, 12
+    o = _rand_bf16((n, H, D))
+    W = _rand_bf16((1, d, H * D))
+    want = bits_to_f64(o).reshape(n, H * D) @ bits_to_f64(W)[0].T
+    np.testing.assert_allclose(oracle.grouped_out_proj(o, W), want, rtol=1e-13, atol=1e-13)
+
+
+def test_out_proj_is_block_diagonal():
+    # group g's outputs depend on group g's heads only: a block-diagonal
+    # matrix (numpy) over all heads gives the same result
+    n, H, D, G, d_g = 3, 8, 4, 4, 5
+    K = (H // G) * D
+    o = _rand_bf16((n, H, D))
+    W = _rand_bf16((G, d_g, K))
+    big = np.zeros((G * d_g, H * D))
+    for g in range(G):
+        big[g * d_g:(g + 1) * d_g, g * K:(g + 1) * K] = bits_to_f64(W)[g]
+    want = bits_to_f64(o).reshape(n, H * D) @ big.T
+    np.testing.assert_allclose(oracle.grouped_out_proj(o, W), want, rtol=1e-13, atol=1e-13)
+
