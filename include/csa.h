@@ -212,6 +212,26 @@ CSA_API int csa_sparse_attn_batch_invariant(const void* q, const void* k_cmp, co
                                             int keys_per_split, int32_t* err_word, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Grouped output projection after the MQA core attention.  The hyper.ai
+ * DeepSeek-V4 page (Method, CSA paragraph) follows the core attention with
+ * "a grouped output projection"; read as: the H heads of a query's output are
+ * split into G groups of H/G consecutive heads, and group g's K = (H/G) * D
+ * values are projected by its own matrix W_g:
+ *     y[q][g*d_g + r] = sum_{j < K} W[g][r][j] * o[q][g*K + j]
+ * fp32 accumulation, bf16 output (nearest even).
+ *
+ *   o    bf16 [n][H][D] (the attention output, contiguous);
+ *   W    bf16 [G][d_g][K] (row = output channel), caller-owned weights;
+ *   y    bf16 [n][G * d_g] out.
+ *   H % G == 0; K a multiple of 64; d_g a multiple of 128; all three
+ *   pointers 16-byte aligned.  Status as the other calls (1 invalid
+ *   argument, 2 unsupported shape, 4 CUDA); timeouts of the kernel's bounded
+ *   waits set CSA_EW_TIMEOUT in err_word.
+ * ---------------------------------------------------------------------- */
+CSA_API int csa_grouped_out_proj(const void* o, const void* W, void* y, int n, int H, int D,
+                                 int G, int d_g, int32_t* err_word, void* stream);
+
+/* ------------------------------------------------------------------------
  * a3, without caller scratch.  An integration variant: the DeepSeek-V4 pages
  * have no counterpart to it; it computes exactly what csa_indexer_topk does.
  *

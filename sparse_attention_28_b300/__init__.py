@@ -15,6 +15,7 @@ Calls (same names as the C ABI, without the prefix where it reads better):
 * :func:`sparse_attn_prefill`    -- csa_sparse_attn_prefill
 * :func:`sparse_attn_batch_invariant` -- csa_sparse_attn_batch_invariant
 * :func:`hca_dense_attn_decode`  -- hca_dense_attn_decode
+* :func:`grouped_out_proj`       -- csa_grouped_out_proj
 """
 from __future__ import annotations
 
@@ -39,6 +40,7 @@ ABI_SYMBOLS = (
     "csa_indexer_topk", "csa_attn_workspace", "csa_sparse_attn_decode",
     "csa_sparse_attn_prefill", "hca_dense_attn_decode", "csa_indexer_topk_static",
     "csa_indexer_scores", "csa_compress_kv_span", "csa_sparse_attn_batch_invariant",
+    "csa_grouped_out_proj",
 )
 
 # capacity of the library-owned scratch behind indexer_topk_static (bytes)
@@ -97,6 +99,8 @@ def lib() -> ctypes.CDLL:
             L.csa_sparse_attn_batch_invariant.argtypes = [P, P, P, I64, I, P, I, P, P, I64, I64,
                                                           P, I, P, F, I, I, I, I, P, P, I, P, P]
             L.csa_sparse_attn_batch_invariant.restype = I
+            L.csa_grouped_out_proj.argtypes = [P, P, P, I, I, I, I, I, P, P]
+            L.csa_grouped_out_proj.restype = I
             L.hca_dense_attn_decode.argtypes = [P, P, P, I64, I, P, I, P, P, I64, I64, P, I, P, F,
                                                 I, I, I, P, P, P, SZ, P, P]
             L.hca_dense_attn_decode.restype = I
@@ -424,3 +428,26 @@ def hca_dense_attn_decode(q, k_cmp, v_cmp, n_cmp, m_prime: int, k_raw, v_raw, se
         softmax_scale, B, H, D, _p(o), _p(lse), _p(wsb), wsn, _p(err_word), _stream(dev))
     _check(st, "hca_dense_attn_decode")
     return (o, lse) if return_lse else o
+
+
+# ---------------------------------------------------------------- output projection
+
+def grouped_out_proj(o, W, out=None, err_word=None):
+    """Grouped output projection: o bf16 [n, H, D] (the attention output), W
+    bf16 [G, d_g, (H/G)*D] (group g's rows); returns bf16 [n, G*d_g] with
+    y[q, g*d_g + r] = sum_j W[g, r, j] * o[q, heads of group g flattened][j]."""
+    _cuda(o, "o", torch.bfloat16)
+    _cuda(W, "W", torch.bfloat16)
+    _need(o.is_contiguous() and W.is_contiguous(), "o, W must be contiguous")
+    n, H, D = o.shape
+    G, d_g, K = W.shape
+    _need(K * G == H * D, "W must be [G, d_g, (H/G)*D]")
+    y = out if out is not None else torch.empty((n, G * d_g), dtype=torch.bfloat16,
+                                               device=o.device)
+    _need(y.dtype == torch.bfloat16 and y.is_contiguous() and tuple(y.shape) == (n, G * d_g),
+          "out: contiguous bf16 [n, G*d_g]")
+    st = lib().csa_grouped_out_proj(_p(o), _p(W), _p(y), n, H, D, G, d_g, _p(err_word),
+                                    _stream(o.device))
+    _check(st, "csa_grouped_out_proj")
+    return y
+

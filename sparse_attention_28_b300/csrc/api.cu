@@ -415,4 +415,26 @@ int hca_dense_attn_decode(const void* q, const void* k_cmp, const void* v_cmp,
   return run_attention(a, ws, ws_bytes, stream);
 }
 
+// ---------------------------------------------------------------- output projection
+int csa_grouped_out_proj(const void* o, const void* W, void* y, int n, int H, int D, int G,
+                         int d_g, int32_t* err_word, void* stream) {
+  if (n < 0 || H <= 0 || D <= 0 || G <= 0 || d_g <= 0 || H % G != 0) return CSA_ERR_INVALID_ARG;
+  const int64_t K = (int64_t)(H / G) * D;
+  if (K % 64 != 0 || d_g % 128 != 0 || (int64_t)H * D > (1 << 20)) return CSA_ERR_UNSUPPORTED;
+  if (n == 0) return CSA_OK;
+  if (!o || !W || !y) return CSA_ERR_INVALID_ARG;
+  if (!aligned16(o) || !aligned16(W) || !aligned16(y)) return CSA_ERR_INVALID_ARG;
+  OutProjArgs a;
+  a.o = reinterpret_cast<const bf16*>(o);
+  a.W = reinterpret_cast<const bf16*>(W);
+  a.y = reinterpret_cast<bf16*>(y);
+  a.n = n;
+  a.H = H;
+  a.D = D;
+  a.G = G;
+  a.d_g = d_g;
+  a.err = err_word;
+  return cuda_status(launch_out_proj(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

@@ -54,6 +54,16 @@ struct AttnArgs {
   int32_t* err;
 };
 
+// ---------------------------------------------------------------- output projection
+struct OutProjArgs {
+  const __nv_bfloat16* o;  // [n][H * D]
+  const __nv_bfloat16* W;  // [G][d_g][(H / G) * D]
+  __nv_bfloat16* y;        // [n][G * d_g]
+  int n, H, D, G, d_g;
+  int32_t* err;
+};
+cudaError_t launch_out_proj(const OutProjArgs& a, cudaStream_t st);
+
 void attn_plan(int n_query, int n_keys_max, int max_cluster, int* n_split, int* keys_per_split);
 size_t attn_workspace_bytes(int n_query, int H, int n_keys_max);  // 0: splits merge on chip
 cudaError_t launch_attention(AttnArgs a, void* ws, cudaStream_t st);

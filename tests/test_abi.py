@@ -145,6 +145,21 @@ def test_batch_invariant_rejects():
     assert call(B=0, q=None) == 0
 
 
+def test_grouped_out_proj_rejects():
+    L = csa.lib()
+
+    def call(**over):
+        a = dict(o=FAKE, W=FAKE, y=FAKE, n=32, H=64, D=128, G=8, d_g=512, err=None, st=None)
+        a.update(over)
+        return L.csa_grouped_out_proj(*a.values())
+
+    assert call(G=7) == 1           # heads do not split into 7 groups
+    assert call(d_g=100) == 2       # output channels per group: a multiple of 128
+    assert call(D=40, G=64) == 2    # K = 40: not a multiple of 64
+    assert call(y=None) == 1
+    assert call(n=0, o=None) == 0
+
+
 def test_attention_workspace_only_for_split_queries():
     # partial rows + lse (129 fp32 per head) for every split of every query
     # when a query can get several splits (fewer queries than SMs / 2); none

@@ -589,6 +589,24 @@ def test_batch_invariant_attention_is_bitwise_independent_of_the_batch(cuda_devi
     assert (lse_a.cpu() - lse_b).abs().max().item() < 1e-3
 
 
+@pytest.mark.parametrize("n,G,d_g", [(1, 8, 128), (32, 8, 512), (300, 4, 256), (77, 16, 128)])
+def test_grouped_out_proj_parity(cuda_device, n, G, d_g):
+    # 300 queries: two tiles (256 + a ragged 44); K = (64 / G) * 128
+    H, D = 64, 128
+    K = (H // G) * D
+    o = synth.randn((n, H, D), 81, 1)
+    W = synth.randn((G, d_g, K), 81, 2, scale=1 / math.sqrt(K))
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    y = csa.grouped_out_proj(o.to(DEV), W.to(DEV), err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ref = oracle.grouped_out_proj(u16(o), u16(W))
+    g = f64(y)
+    # bf16 rounding of the result plus fp32 accumulation over K products
+    mag = np.abs(oracle.grouped_out_proj(u16(o.abs()), u16(W.abs())))
+    assert np.all(np.abs(g - ref) <= bf16_bound(ref) + K * 2.0 ** -23 * mag)
+
+
 def test_softmax_scale_is_applied(cuda_device):
     B, H, N_cap, k = 2, 32, 64, 16
     lens = [256, 256]
