@@ -87,6 +87,11 @@ def algorithmic(wl) -> dict:
             wl.H_I * qrow + wl.H_I * 4 + wl.k * 4)
         att_b = sum((min(wl.k, n // wl.m) + min(W, n)) * 2 * D * 2 for n in wl.lens) + wl.B * qo
         st = {"indexer_topk": {"bytes": idx_b}, "attention": {"bytes": att_b}}
+        if wl.proj_groups:
+            # the weights once, the attention output in, the projection out
+            K = (H // wl.proj_groups) * D
+            st["out_proj"] = {"bytes": wl.proj_groups * wl.proj_dim * K * 2 + wl.B * H * D * 2
+                              + wl.B * wl.proj_groups * wl.proj_dim * 2}
         if wl.stream_compress:
             per_seq = wl.m * (2 * D * 2 + wl.d_I * 2) + 2 * D * 2 + idx_row_bytes(wl)
             weights = (2 * D * D + wl.d_I * wl.d_I) * 2 + wl.m * (2 * D + wl.d_I) * 4
@@ -264,8 +269,10 @@ class OracleRunner:
                                       wl.m, self.idx_dtype,
                                       a.get("q_scale"), a.get("k_scale"))
             idx = o.topk(sc, nv, wl.k)
-            o.csa_decode(a["q"], a["k_cmp"], a["v_cmp"], idx[:, 0, :], a["k_win"], a["v_win"],
-                         a["seq_len"], wl.W, a["sink"], 1.0, a["raw_base"])
+            ro, _ = o.csa_decode(a["q"], a["k_cmp"], a["v_cmp"], idx[:, 0, :], a["k_win"],
+                                 a["v_win"], a["seq_len"], wl.W, a["sink"], 1.0, a["raw_base"])
+            if wl.proj_groups:
+                o.grouped_out_proj(o.quantize_bf16(ro), a["W_o"])
             return
         # prefill sample: the sampled tokens' blocks, scores, top-k, attention
         for s in ("k", "v", "idx"):
@@ -316,6 +323,8 @@ def main():
     wl = synth.WORKLOADS[args.workload]
     cfg = {"workload": wl.name, "kind": wl.kind, "B": wl.B, "L": wl.L, "T": wl.T, "m": wl.m,
            "span": wl.cspan, "batch_invariant_keys_per_split": wl.batch_invariant,
+           "out_proj": ({"groups": wl.proj_groups, "d_g": wl.proj_dim} if wl.proj_groups
+                        else None),
            "H": wl.H, "D": wl.D, "k": wl.k, "window": wl.W, "H_I": wl.H_I, "d_I": wl.d_I,
            "indexer_dtype": "e2m1" if wl.idx_fp4 else "e4m3" if wl.idx_fp8 else "bf16",
            "stream_compress": wl.stream_compress, "parallelism": f"replicas{world}"}

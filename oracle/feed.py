@@ -73,6 +73,8 @@ def oracle_inputs(wl, inp: dict, n_units: int, seqs=None, tokens=None) -> dict:
                 a["q_scale"], a["k_scale"] = f32(inp["q_scale"][ix]), f32(inp["k_scale"][ix])
             else:
                 a["q_idx"], a["k_idx"] = u16(inp["q_idx"][ix]), u16(inp["k_idx"][ix])
+        if getattr(wl, "proj_groups", 0):
+            a["W_o"] = u16(inp["W_o"])
         if wl.stream_compress:
             m = wl.m
             a["raw_new_k"] = u16(inp["k_win"][ix][:, wl.W - m:])

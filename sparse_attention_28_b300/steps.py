@@ -20,7 +20,7 @@ from __future__ import annotations
 
 import torch
 
-from . import (attn_workspace, compress_kv, hca_dense_attn_decode, indexer_scores,
+from . import (attn_workspace, compress_kv, grouped_out_proj, hca_dense_attn_decode, indexer_scores,
                indexer_topk, indexer_topk_workspace, sparse_attn_batch_invariant,
                sparse_attn_decode, sparse_attn_prefill)
 
@@ -140,6 +140,13 @@ class CsaDecodeStep(_Step):
             self.new_block = lens[0] // m - 1
         self.idx = torch.empty((B, 1, wl.k), dtype=torch.int32, device=dev)
         self.out = torch.empty_like(self.q)
+        if wl.proj_groups:
+            # the attention output feeds the grouped output projection, whose
+            # output is the step's
+            self.W_o = g("W_o")
+            self.attn_out = self.out
+            self.out = torch.empty((B, wl.proj_groups * wl.proj_dim), dtype=torch.bfloat16,
+                                   device=dev)
         self.ws_idx = torch.empty(max(1, indexer_topk_workspace(B, 1, wl.N_cap, wl.k)),
                                   dtype=torch.uint8, device=dev)
         self.ws_attn = torch.empty(max(1, attn_workspace(B, 1, wl.H, wl.k + W)),
@@ -164,7 +171,12 @@ class CsaDecodeStep(_Step):
         # the K/V entries are first needed by the attention: compress them on
         # a side stream while the indexer runs
         return _overlapped(self, self._compress_kv, [self._compress_idx, self._index],
-                           self._attend)
+                           self._finish)
+
+    def _finish(self):
+        self._attend()
+        if self.wl.proj_groups:
+            self._project()
 
     def _index(self):
         wl = self.wl
@@ -179,16 +191,22 @@ class CsaDecodeStep(_Step):
             sparse_attn_batch_invariant(self.q.view(B, 1, H, D), self.k_cmp, self.v_cmp, self.idx,
                                         self.k_raw, self.v_raw, self.q_pos, wl.W, self.sink,
                                         keys_per_split=wl.batch_invariant,
-                                        out=self.out.view(B, 1, H, D))
+                                        out=getattr(self, "attn_out", self.out).view(B, 1, H, D))
             return
         sparse_attn_decode(self.q, self.k_cmp, self.v_cmp, self.idx.view(wl.B, wl.k),
                            self.k_raw, self.v_raw, self.seq_len, wl.W, self.sink,
-                           out=self.out, ws=self.ws_attn)
+                           out=getattr(self, "attn_out", self.out), ws=self.ws_attn)
+
+    def _project(self):
+        grouped_out_proj(self.attn_out, self.W_o, out=self.out)
 
     def stages(self):
         """(name, callable) per stage, in order."""
         st = [("compress", self._compress)] if self.compress else []
-        return st + [("indexer_topk", self._index), ("attention", self._attend)]
+        st += [("indexer_topk", self._index), ("attention", self._attend)]
+        if self.wl.proj_groups:
+            st.append(("out_proj", self._project))
+        return st
 
     def kernel_probe(self):
         """The step's dominant kernel launched alone on the step's buffers:

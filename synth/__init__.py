@@ -59,6 +59,8 @@ class Workload:
     seq_lens: Optional[tuple] = None  # ragged decode lengths (default: all L)
     span: int = 0            # raw tokens per compressed block (0: m, no overlap)
     batch_invariant: int = 0  # > 0: decode attention with fixed key splits of this size
+    proj_groups: int = 0     # > 0: grouped output projection after the attention (G groups)
+    proj_dim: int = 0        # output channels per projection group (d_g)
 
     @property
     def cspan(self) -> int:
@@ -91,6 +93,10 @@ WORKLOADS = {
     # the same with the FP4 indexer path
     "csa_decode_1m_fp4": Workload("csa_decode_1m_fp4", "csa_decode", B=8, L=1048576, m=4,
                                   H=64, k=2048, idx_fp4=True, stream_compress=True),
+    # the 128K decode followed by the grouped output projection (8 groups of 8
+    # heads, 512 output channels each: a 4096-wide output)
+    "csa_decode_128k_proj": Workload("csa_decode_128k_proj", "csa_decode", B=32, L=131072, m=4,
+                                     H=64, k=1024, proj_groups=8, proj_dim=512),
     # the 128K decode with batch-invariant attention (fixed 320-key splits)
     "csa_decode_128k_bi": Workload("csa_decode_128k_bi", "csa_decode", B=32, L=131072, m=4,
                                    H=64, k=1024, batch_invariant=320),
@@ -193,6 +199,10 @@ def make_inputs(wl: Workload, seed: int = 0, device="cpu") -> dict:
                 out["q_idx"] = randn((B, 1, wl.H_I, wl.d_I), seed, 8, dev)
                 out["k_idx"] = randn((B, N_cap, wl.d_I), seed, 9, dev)
                 out["q_scale"] = out["k_scale"] = None
+        if wl.proj_groups:
+            K = (H // wl.proj_groups) * D
+            out["W_o"] = randn((wl.proj_groups, wl.proj_dim, K), seed, 30, dev,
+                               scale=1.0 / math.sqrt(K))
         if wl.stream_compress:
             assert wl.cspan == m, "streaming compression: non-overlapping blocks"
             # the newest block's raw K/V rows are the last m window rows;

@@ -71,7 +71,14 @@ def _check_decode(name, seqs):
     same = [i for i, b in enumerate(seqs)
             if set(gidx[i, 0].tolist()) == set(ref[i, 0].tolist())]
     assert len(same) >= len(seqs) - 1
-    check_attention(out[[seqs[i] for i in same]], ro[same], what=name + " step")
+    att = getattr(step, "attn_out", out)
+    check_attention(att[[seqs[i] for i in same]], ro[same], what=name + " step")
+    if wl.proj_groups:
+        # the projection of the step's own attention output
+        K = (wl.H // wl.proj_groups) * wl.D
+        yr = oracle.grouped_out_proj(u16(att[seqs]), a["W_o"])
+        mag = np.abs(oracle.grouped_out_proj(u16(att[seqs].abs()), u16(step.W_o.abs())))
+        assert np.all(np.abs(f64(out[seqs]) - yr) <= bf16_bound(yr) + K * 2.0 ** -23 * mag)
 
 
 def test_csa_decode_tiny(cuda_device):
@@ -120,6 +127,10 @@ def test_csa_decode_128k_batch_invariant(cuda_device):
 
 def test_csa_decode_1m_fp4_streaming(cuda_device):
     _check_decode("csa_decode_1m_fp4", [0, 7])
+
+
+def test_csa_decode_128k_with_grouped_out_proj(cuda_device):
+    _check_decode("csa_decode_128k_proj", [0, 13, 31])
 
 
 def test_decode_step_is_deterministic(cuda_device):
