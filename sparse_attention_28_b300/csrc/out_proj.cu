@@ -9,7 +9,11 @@
 // fp32 accumulation, bf16 output (nearest even).
 //
 // One tcgen05 product per (128 output channels, group, tile of up to 256
-// queries): M = 128 rows of W_g, N = the queries, K in 64-wide slabs.
+// queries): M = 128 rows of W_g, N = the queries, K in 64-wide slabs.  When
+// that leaves SMs idle (decode: few queries), the K slabs are split over a
+// cluster of ks CTAs; each writes its fp32 partial to its shared memory and,
+// after a cluster barrier, CTA s sums rows [s*128/ks, (s+1)*128/ks) of all
+// ks partials through distributed shared memory.
 //   warp 0     TMA: each slab's W rows (128 x 128 B) and query rows (N x 128 B)
 //              into a four-stage ring, 128-byte swizzled
 //   warp 1     one thread issues 4 tcgen05.mma (M128 N K16) per slab into one
@@ -49,7 +53,8 @@ struct ProjMaps {
 };
 
 __global__ void __launch_bounds__(kPThreads, 1)
-    out_proj_kernel(OutProjArgs a, int n_tile, const __grid_constant__ ProjMaps maps) {
+    out_proj_kernel(OutProjArgs a, int n_tile, int ks, int slabs_per,
+                    const __grid_constant__ ProjMaps maps) {
   pdl_trigger();
   pdl_wait();
   extern __shared__ uint8_t psm_raw[];
@@ -57,9 +62,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
   const uint32_t sbase = smem_u32(sm);
   PBars* bars = reinterpret_cast<PBars*>(sm + kPBarOff);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int m0 = blockIdx.x * kPM, g = blockIdx.y, n0 = blockIdx.z * n_tile;
+  const int kspl = blockIdx.x % ks;  // this CTA's share of the K slabs
+  const int m0 = (blockIdx.x / ks) * kPM, g = blockIdx.y, n0 = blockIdx.z * n_tile;
   const int K = (a.H / a.G) * a.D;
-  const int n_slabs = K / 64;
+  const int s_beg = kspl * slabs_per;
+  const int n_slabs = min(K / 64 - s_beg, slabs_per);  // may be <= 0 for the last split
   const int nq = min(n_tile, a.n - n0);  // queries of this tile
 
   if (warp == 0) {
@@ -91,8 +98,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
         }
         const uint32_t st = sbase + s * kPStageBytes;
         tma::expect_tx(&bars->full[s], tx);
-        tma::load_box(st, &maps.w, i * 64, g * a.d_g + m0, &bars->full[s]);
-        tma::load_box(st + kPABytes, &maps.o, g * K + i * 64, n0, &bars->full[s]);
+        tma::load_box(st, &maps.w, (s_beg + i) * 64, g * a.d_g + m0, &bars->full[s]);
+        tma::load_box(st + kPABytes, &maps.o, g * K + (s_beg + i) * 64, n0, &bars->full[s]);
       }
     }
     __syncwarp();
@@ -130,18 +137,41 @@ __global__ void __launch_bounds__(kPThreads, 1)
       if (lane == 0) flag_error(a.err, CSA_EW_TIMEOUT);
     } else {
       tc::fence_after_sync();
-      const int r = m0 + qd * 32 + lane;  // output channel within the group
-      bf16* y = a.y + (int64_t)g * a.d_g + r;
+      const int rl = qd * 32 + lane;  // output channel within the tile
+      bf16* y = a.y + (int64_t)g * a.d_g + m0 + rl;
       const int64_t ystride = (int64_t)a.G * a.d_g;
+      float* part = reinterpret_cast<float*>(sm);  // [n_tile][128] (stages are done)
       for (int c0 = 0; c0 < n_tile; c0 += 32) {
         uint32_t v[32];
         tc::tmem_ld32(tmem + lanef + c0, v);
         tc::tmem_ld_wait();
+        if (n_slabs <= 0)  // a split left without slabs contributes zeros
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (c0 + j < nq) y[(int64_t)(n0 + c0 + j) * ystride] = __float2bfloat16_rn(__uint_as_float(v[j]));
+          for (int j = 0; j < 32; ++j) v[j] = 0u;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          if (c0 + j >= nq) continue;
+          if (ks == 1)
+            y[(int64_t)(n0 + c0 + j) * ystride] = __float2bfloat16_rn(__uint_as_float(v[j]));
+          else
+            part[(c0 + j) * kPM + rl] = __uint_as_float(v[j]);
+        }
       }
     }
+  }
+  if (ks > 1) {
+    // every CTA's partial is complete; CTA kspl sums its rows of all of them
+    tc::cluster_sync();
+    const int rs = kPM / ks;
+    const int64_t ystride = (int64_t)a.G * a.d_g;
+    for (int it = tid; it < nq * rs; it += kPThreads) {
+      const int q = it / rs, rl = kspl * rs + it % rs;
+      const uint32_t la = sbase + (uint32_t)(q * kPM + rl) * 4u;
+      float acc = 0.f;
+      for (int p = 0; p < ks; ++p) acc += __uint_as_float(tc::ld_cluster_u32(tc::map_shared(la, p)));
+      a.y[(int64_t)(n0 + q) * ystride + (int64_t)g * a.d_g + m0 + rl] = __float2bfloat16_rn(acc);
+    }
+    tc::cluster_sync();  // no CTA leaves while another still reads its partial
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -163,17 +193,36 @@ cudaError_t launch_out_proj(const OutProjArgs& a, cudaStream_t st) {
   cudaError_t e = ensure_smem_attr((const void*)out_proj_kernel, kPSmem);
   if (e != cudaSuccess) return e;
   const int K = (a.H / a.G) * a.D;
+  const int n_slabs = K / 64;
   // queries per CTA: all of them up to 256 (a multiple of 16: the MMA's N)
   int n_tile = a.n < kPMaxN ? a.n : kPMaxN;
   n_tile = (n_tile + 15) / 16 * 16;
+  // K split: the largest power of two up to 8 that keeps the CTAs within the
+  // SMs, every split at least one slab
+  const int64_t base = (int64_t)(a.d_g / kPM) * a.G * ((a.n + n_tile - 1) / n_tile);
+  int ks = 1;
+  while (ks < 8 && base * ks * 2 <= kNumSMs && ks * 2 <= n_slabs) ks *= 2;
+  const int slabs_per = (n_slabs + ks - 1) / ks;
   ProjMaps maps;
   e = tma::encode_rows(&maps.w, a.W, (uint32_t)K, (uint64_t)a.G * a.d_g, kPM);
   if (e != cudaSuccess) return e;
   e = tma::encode_rows(&maps.o, a.o, (uint32_t)(a.H * a.D), (uint64_t)a.n, (uint32_t)n_tile);
   if (e != cudaSuccess) return e;
-  const dim3 grid((unsigned)(a.d_g / kPM), (unsigned)a.G,
-                  (unsigned)((a.n + n_tile - 1) / n_tile));
-  return launch_pdl(out_proj_kernel, grid, dim3(kPThreads), kPSmem, st, a, n_tile, maps);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(a.d_g / kPM * ks), (unsigned)a.G,
+                     (unsigned)((a.n + n_tile - 1) / n_tile));
+  cfg.blockDim = dim3(kPThreads);
+  cfg.dynamicSmemBytes = kPSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)ks;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  set_pdl(attr[1]);
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, out_proj_kernel, a, n_tile, ks, slabs_per, maps);
 }
 
 }  // namespace csa

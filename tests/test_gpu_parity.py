@@ -589,9 +589,12 @@ def test_batch_invariant_attention_is_bitwise_independent_of_the_batch(cuda_devi
     assert (lse_a.cpu() - lse_b).abs().max().item() < 1e-3
 
 
-@pytest.mark.parametrize("n,G,d_g", [(1, 8, 128), (32, 8, 512), (300, 4, 256), (77, 16, 128)])
+@pytest.mark.parametrize("n,G,d_g", [(1, 8, 128), (32, 8, 512), (300, 4, 256), (77, 16, 128),
+                                     (5, 32, 128), (600, 8, 512)])
 def test_grouped_out_proj_parity(cuda_device, n, G, d_g):
-    # 300 queries: two tiles (256 + a ragged 44); K = (64 / G) * 128
+    # 300 queries: two tiles (256 + a ragged 44); K = (64 / G) * 128; few
+    # queries split K over a cluster (G = 32: K = 256, 4 slabs, 4 splits of
+    # one); 600 queries: three tiles, no split
     H, D = 64, 128
     K = (H // G) * D
     o = synth.randn((n, H, D), 81, 1)
