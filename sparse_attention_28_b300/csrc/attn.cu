@@ -707,7 +707,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Split merge through global memory (a6), for splits run without a cluster:
 // grid (queries, ceil(H / 4)), warp w of CTA (q, y) merges head 4y + w.  The
 // same combination as the cluster merge: weights exp(lse_s - M) / Z over the
-// splits, the sink's exp(sink - M) in Z only.
+// splits, the sink's exp(sink - M) in Z only.  The lanes read the splits'
+// lse values in parallel, and the partial rows are loaded eight splits at a
+// time, so that the loads overlap.
 __global__ void __launch_bounds__(128) attn_merge_kernel(AttnArgs a) {
   pdl_trigger();
   pdl_wait();
@@ -716,6 +718,9 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(AttnArgs a) {
   const int ns = a.n_split, H = a.H;
   if (h >= H) return;
   const float* lse_p = a.part_lse + (int64_t)qid * ns * H + h;  // split s at s * H
+  const float4* row = reinterpret_cast<const float4*>(a.part_o + ((int64_t)qid * ns * H + h) * kD);
+  const int64_t rstride = (int64_t)H * kD / 4;  // float4s between splits
+  // the splits' lse values, all lanes at once (lane j holds splits j, j + 32, ..)
   float Mx = a.sink ? __ldg(a.sink + h) : -INFINITY;
   for (int s = lane; s < ns; s += 32) Mx = fmaxf(Mx, lse_p[(int64_t)s * H]);
 #pragma unroll
@@ -723,23 +728,35 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(AttnArgs a) {
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float lse = -INFINITY;
   if (Mx != -INFINITY) {
-    float Z = a.sink ? expf(__ldg(a.sink + h) - Mx) : 0.f;
-    for (int s = 0; s < ns; ++s) {
+    float zl = 0.f;  // this lane's share of Z
+    for (int s = lane; s < ns; s += 32) {
       const float ls = lse_p[(int64_t)s * H];
-      const float w = ls == -INFINITY ? 0.f : expf(ls - Mx);
-      Z += w;
-      const float4 v = reinterpret_cast<const float4*>(
-          a.part_o + (((int64_t)qid * ns + s) * H + h) * kD)[lane];
-      acc.x += w * v.x;
-      acc.y += w * v.y;
-      acc.z += w * v.z;
-      acc.w += w * v.w;
+      zl += ls == -INFINITY ? 0.f : expf(ls - Mx);
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) zl += __shfl_xor_sync(0xFFFFFFFFu, zl, o);
+    const float Z = zl + (a.sink ? expf(__ldg(a.sink + h) - Mx) : 0.f);
     const float inv = 1.f / Z;
-    acc.x *= inv;
-    acc.y *= inv;
-    acc.z *= inv;
-    acc.w *= inv;
+    // the partial rows, eight splits' loads in flight at a time
+    constexpr int kBatch = 8;
+    for (int s0 = 0; s0 < ns; s0 += kBatch) {
+      float4 v[kBatch];
+      float w[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int s = s0 + j;
+        const float ls = s < ns ? lse_p[(int64_t)s * H] : -INFINITY;
+        w[j] = ls == -INFINITY ? 0.f : expf(ls - Mx) * inv;
+        v[j] = s < ns ? row[s * rstride + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        acc.x += w[j] * v[j].x;
+        acc.y += w[j] * v[j].y;
+        acc.z += w[j] * v[j].z;
+        acc.w += w[j] * v[j].w;
+      }
+    }
     lse = Mx + logf(Z);
   }
   reinterpret_cast<uint2*>(a.out + ((int64_t)qid * H + h) * kD)[lane] =
