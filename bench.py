@@ -494,22 +494,15 @@ def launches_per_step(wl, csa) -> int:
 
 
 def run_e2e(args, wl, step, dev, flush, world, dist):
-    """Per step: pinned host -> device copy of the step's inputs, the step via
-    the public API, device -> pinned host copy of its output, all three in one
-    CUDA graph (as a serving loop submits a step), replayed once per step."""
-    names = {"csa_decode": ["q", "q_idx", "w", "q_scale", "seq_len"],
-             "hca_decode": ["q", "seq_len"],
-             "csa_prefill": ["q", "q_idx", "w", "q_pos"]}[wl.kind]
-    pairs = []
-    for n in names:
-        d = getattr(step, n, None)
-        if d is None:
-            continue
-        h = torch.empty(d.shape, dtype=d.dtype, pin_memory=True)
-        h.copy_(d)
-        pairs.append((h, d))
+    """Per step: pinned host -> device copy of the step's inputs (one buffer:
+    queries, positions, lengths, indexer queries and weights), the step via
+    the public API, device -> pinned host copy of its output, all in one CUDA
+    graph (as a serving loop submits a step), replayed once per step."""
+    host_in = torch.empty(step.inputs.shape, dtype=torch.uint8, pin_memory=True)
+    host_in.copy_(step.inputs)
+    pairs = [(host_in, step.inputs)]
     out_h = torch.empty(step.out.shape, dtype=step.out.dtype, pin_memory=True)
-    h2d = sum(h.numel() * h.element_size() for h, _ in pairs)
+    h2d = host_in.numel()
     d2h = out_h.numel() * out_h.element_size()
     stream = torch.cuda.current_stream(dev)
     run = step.graphed(h2d=pairs, d2h=out_h)

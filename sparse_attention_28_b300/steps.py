@@ -57,7 +57,30 @@ def _overlapped(step, side_fn, main_fns, join_fn):
 
 class _Step:
     """Shared by the step classes: ``stages()`` lists (name, callable) in
-    order and ``out`` is the output tensor."""
+    order and ``out`` is the output tensor.  ``inputs`` is one device buffer
+    that holds every tensor the host provides anew each step (the queries,
+    positions, lengths, indexer queries and weights), so that a serving loop
+    uploads a step's inputs with a single copy."""
+
+    INPUTS = ()  # attribute names of the per-step inputs
+
+    def _pack_inputs(self):
+        """Re-home the per-step input tensors as views of one device buffer
+        (each at a 256-byte aligned offset)."""
+        names = [n for n in self.INPUTS if getattr(self, n, None) is not None]
+        offs, total = [], 0
+        for n in names:
+            t = getattr(self, n)
+            offs.append(total)
+            total += (t.numel() * t.element_size() + 255) // 256 * 256
+        buf = torch.empty(max(total, 256), dtype=torch.uint8, device=self.out.device)
+        for n, o in zip(names, offs):
+            t = getattr(self, n).contiguous()
+            nb = t.numel() * t.element_size()
+            view = buf[o:o + nb].view(t.dtype).view(t.shape)
+            view.copy_(t)
+            setattr(self, n, view)
+        self.inputs = buf
 
     def __call__(self):
         for _, fn in self.stages():
@@ -95,6 +118,8 @@ class _Step:
 
 
 class CsaDecodeStep(_Step):
+    INPUTS = ("q", "q_idx", "w", "q_scale", "seq_len", "q_pos")
+
     def __init__(self, inp: dict, device="cuda"):
         wl = inp["workload"]
         self.wl = wl
@@ -151,6 +176,7 @@ class CsaDecodeStep(_Step):
                                   dtype=torch.uint8, device=dev)
         self.ws_attn = torch.empty(max(1, attn_workspace(B, 1, wl.H, wl.k + W)),
                                    dtype=torch.uint8, device=dev)
+        self._pack_inputs()
 
     def _compress_kv(self):
         wl, j = self.wl, self.new_block
@@ -223,6 +249,8 @@ class CsaDecodeStep(_Step):
 
 
 class HcaDecodeStep(_Step):
+    INPUTS = ("q", "seq_len")
+
     def __init__(self, inp: dict, device="cuda"):
         wl = inp["workload"]
         self.wl = wl
@@ -243,6 +271,7 @@ class HcaDecodeStep(_Step):
         self.out = torch.empty_like(self.q)
         self.ws_attn = torch.empty(max(1, attn_workspace(B, 1, wl.H, wl.N_cap + W)),
                                    dtype=torch.uint8, device=dev)
+        self._pack_inputs()
 
     def _attend(self):
         wl = self.wl
@@ -259,6 +288,8 @@ class HcaDecodeStep(_Step):
 
 
 class CsaPrefillStep(_Step):
+    INPUTS = ("q", "q_idx", "w", "q_pos")
+
     def __init__(self, inp: dict, device="cuda"):
         wl = inp["workload"]
         self.wl = wl
@@ -294,6 +325,7 @@ class CsaPrefillStep(_Step):
                                   dtype=torch.uint8, device=dev)
         self.ws_attn = torch.empty(max(1, attn_workspace(B, T, wl.H, wl.k + W)),
                                    dtype=torch.uint8, device=dev)
+        self._pack_inputs()
 
     def _compress_kv(self):
         wl = self.wl
