@@ -150,10 +150,20 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def src_hash() -> str:
+# the source file of each kernel whose DRAM traffic the bench reports
+KERNEL_SOURCE = {"indexer_score": "indexer.cu", "indexer_gemm": "indexer_gemm.cu",
+                 "attention": "attn.cu", "compress": "compress.cu", "out_proj": "out_proj.cu"}
+
+
+def src_hash(kernel: str = None) -> str:
+    """Hash of a kernel's source file and every shared header (all of csrc
+    when no kernel is named)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "sparse_attention_28_b300", "csrc")
+    mine = KERNEL_SOURCE.get(kernel)
     for n in sorted(os.listdir(csrc)):
+        if mine and n.endswith(".cu") and n != mine:
+            continue
         with open(os.path.join(csrc, n), "rb") as f:
             h.update(n.encode() + f.read())
     return h.hexdigest()[:16]
@@ -161,14 +171,14 @@ def src_hash() -> str:
 
 def traffic_record(wl_name: str, kernel: str):
     """DRAM bytes per launch of the kernel from the committed ncu summary, or
-    None if absent or taken on other kernel sources."""
+    None if absent or taken on other sources of that kernel."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
     rec = d.get(wl_name, {}).get(kernel)
-    if not rec or rec.get("src_hash") != src_hash():
+    if not rec or rec.get("src_hash") != src_hash(kernel):
         return None
     return rec.get("dram_bytes")
 
