@@ -16,6 +16,8 @@ Technical Principles):
 * :func:`topk`             -- a3, exact top-k with the lower-index tie rule
 * :func:`attend`           -- a4 / a5, attention over the selected compressed
   entries plus the raw sliding window plus the sink logit
+* :func:`kv8_dequantize`   -- decoded values of FP8-stored compressed K / V
+  entries (E4M3 non-RoPE channels with a per-entry scale, bf16 RoPE channels)
 * :func:`csa_decode`, :func:`hca_decode`, :func:`csa_prefill` -- the steps
   chained per call of the CUDA library's boundary.
 """
@@ -101,6 +103,10 @@ def _load():
             lib.orc_attend.argtypes = [P, P, P, L, I, I, P, P, L, L, P, L, I, P, P, L, L, L, I,
                                        P, D, P, P]
             lib.orc_attend.restype = I
+            lib.orc_attend_f64cmp.argtypes = lib.orc_attend.argtypes
+            lib.orc_attend_f64cmp.restype = I
+            lib.orc_kv8_dequantize.argtypes = [P, P, P, L, I, I, P]
+            lib.orc_kv8_dequantize.restype = I
             _lib = lib
     return _lib
 
@@ -291,26 +297,52 @@ def topk(scores, n_vis, k: int) -> np.ndarray:
 # a4 / a5: attention
 # --------------------------------------------------------------------------
 
+def kv8_dequantize(codes, scale, rope=None) -> np.ndarray:
+    """Decoded fp64 values of FP8-stored compressed entries.
+
+    codes: uint8 E4M3 [..., d - n_rope] (the non-RoPE channels); scale: f32
+    [...] (one per entry); rope: uint16 bf16 bits [..., n_rope] or None (V
+    entries have no RoPE channels).  Returns fp64 [..., d]: code * scale, then
+    the RoPE channels' bf16 values.
+    """
+    codes = _c(codes, np.uint8)
+    scale = _c(scale, np.float32)
+    dn = codes.shape[-1]
+    n_rope = 0 if rope is None else np.asarray(rope).shape[-1]
+    rope = _c(rope, np.uint16)
+    rows = codes.size // dn
+    assert scale.size == rows and (rope is None or rope.size == rows * n_rope)
+    out = np.empty(codes.shape[:-1] + (dn + n_rope,), np.float64)
+    rc = _load().orc_kv8_dequantize(_ptr(codes), _ptr(scale), _ptr(rope), rows, dn + n_rope,
+                                    n_rope, _ptr(out))
+    _check(rc, "kv8_dequantize")
+    return out
+
+
 def attend(q, qb, qt, k_cmp, v_cmp, sel, k_raw, v_raw, window: int, sink, scale: float,
            raw_base: int = 0):
     """a4 / a5 in fp64.
 
     q: uint16 [Q, H, D]; qb, qt: int32 [Q] (sequence, absolute position);
-    k_cmp, v_cmp: uint16 [B, N, D]; sel: int32 [Q, n_sel] compressed rows (-1 =
-    none) or None; k_raw, v_raw: uint16 [B, R, D] holding absolute positions
-    raw_base .. raw_base+R-1 (or None when window == 0); sink: f32 [H] or None.
+    k_cmp, v_cmp: uint16 bf16 bits [B, N, D], or fp64 [B, N, D] decoded values
+    of FP8-stored entries (:func:`kv8_dequantize`); sel: int32 [Q, n_sel]
+    compressed rows (-1 = none) or None; k_raw, v_raw: uint16 [B, R, D]
+    holding absolute positions raw_base .. raw_base+R-1 (or None when
+    window == 0); sink: f32 [H] or None.
     Returns (out fp64 [Q, H, D], lse fp64 [Q, H]).
     """
     q = _c(q, np.uint16)
     Q, H, D = q.shape
     qb = _c(qb, np.int32)
     qt = _c(qt, np.int32)
+    f64 = k_cmp is not None and np.asarray(k_cmp).dtype == np.float64
     if sel is None or k_cmp is None:
         sel_a, n_sel, kc, vc, cmp_bstride, n_rows = None, 0, None, None, 0, 0
     else:
         sel_a = _c(sel, np.int32)
         n_sel = sel_a.shape[-1]
-        kc, vc = _c(k_cmp, np.uint16), _c(v_cmp, np.uint16)
+        ct = np.float64 if f64 else np.uint16
+        kc, vc = _c(k_cmp, ct), _c(v_cmp, ct)
         cmp_bstride, n_rows = kc.shape[1] * D, kc.shape[1]
     if window > 0:
         kr, vr = _c(k_raw, np.uint16), _c(v_raw, np.uint16)
@@ -321,7 +353,8 @@ def attend(q, qb, qt, k_cmp, v_cmp, sel, k_raw, v_raw, window: int, sink, scale:
     sink = _c(sink, np.float32)
     out = np.empty((Q, H, D), np.float64)
     lse = np.empty((Q, H), np.float64)
-    rc = _load().orc_attend(_ptr(q), _ptr(qb), _ptr(qt), Q, H, D, _ptr(kc), _ptr(vc),
+    fn = _load().orc_attend_f64cmp if f64 else _load().orc_attend
+    rc = fn(_ptr(q), _ptr(qb), _ptr(qt), Q, H, D, _ptr(kc), _ptr(vc),
                             cmp_bstride, n_rows, _ptr(sel_a), n_sel, n_sel, _ptr(kr), _ptr(vr),
                             raw_bstride, raw_base, raw_rows, window, _ptr(sink), scale,
                             _ptr(out), _ptr(lse))

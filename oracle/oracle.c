@@ -489,12 +489,25 @@ int orc_topk(const double* scores, int64_t stride, const int32_t* n_vis, int64_t
  * n_cmp_rows valid rows per sequence.  k_raw/v_raw: bf16 [B][raw_bstride]
  * rows of D, row r holding absolute position raw_base + r, raw_rows rows.
  * out: fp64 [Q][H][D]; lse: fp64 [Q][H]. */
-int orc_attend(const uint16_t* q, const int32_t* qb, const int32_t* qt, int64_t Q, int H, int D,
-               const uint16_t* k_cmp, const uint16_t* v_cmp, int64_t cmp_bstride,
-               int64_t n_cmp_rows, const int32_t* sel, int64_t sel_stride, int n_sel,
-               const uint16_t* k_raw, const uint16_t* v_raw, int64_t raw_bstride,
-               int64_t raw_base, int64_t raw_rows, int window, const float* sink, double scale,
-               double* out, double* lse) {
+/* One stored K or V element: bf16 bits (raw rows, bf16 compressed rows) or an
+ * already-decoded fp64 value (FP8-stored compressed rows, see
+ * orc_kv8_dequantize). */
+typedef struct {
+  const void* row;
+  int f64;
+} orc_row;
+
+static double orc_elem(orc_row r, int e) {
+  return r.f64 ? ((const double*)r.row)[e] : orc_bf16_to_f64(((const uint16_t*)r.row)[e]);
+}
+
+static int attend_rows(const uint16_t* q, const int32_t* qb, const int32_t* qt, int64_t Q, int H,
+                       int D, const void* k_cmp, const void* v_cmp, int cmp_f64,
+                       int64_t cmp_bstride, int64_t n_cmp_rows, const int32_t* sel,
+                       int64_t sel_stride, int n_sel, const uint16_t* k_raw,
+                       const uint16_t* v_raw, int64_t raw_bstride, int64_t raw_base,
+                       int64_t raw_rows, int window, const float* sink, double scale,
+                       double* out, double* lse) {
   if (!q || !qb || !qt || !out || !lse || Q < 0 || H <= 0 || D <= 0 || n_sel < 0 ||
       window < 0)
     return ORC_ERR_ARG;
@@ -505,8 +518,8 @@ int orc_attend(const uint16_t* q, const int32_t* qb, const int32_t* qt, int64_t 
 #pragma omp parallel
   {
     double* qv = (double*)malloc(sizeof(double) * (size_t)D);
-    const uint16_t** kr = (const uint16_t**)malloc(sizeof(void*) * (size_t)(max_keys + 1));
-    const uint16_t** vr = (const uint16_t**)malloc(sizeof(void*) * (size_t)(max_keys + 1));
+    orc_row* kr = (orc_row*)malloc(sizeof(orc_row) * (size_t)(max_keys + 1));
+    orc_row* vr = (orc_row*)malloc(sizeof(orc_row) * (size_t)(max_keys + 1));
     double* l = (double*)malloc(sizeof(double) * (size_t)(max_keys + 1));
     double* acc = (double*)malloc(sizeof(double) * (size_t)D);
 #pragma omp for schedule(dynamic)
@@ -526,8 +539,12 @@ int orc_attend(const uint16_t* q, const int32_t* qb, const int32_t* qt, int64_t 
           bad = 1;
           break;
         }
-        kr[n] = k_cmp + b * cmp_bstride + j * D;
-        vr[n] = v_cmp + b * cmp_bstride + j * D;
+        const int64_t off = b * cmp_bstride + j * D;
+        kr[n].f64 = vr[n].f64 = cmp_f64;
+        kr[n].row = cmp_f64 ? (const void*)((const double*)k_cmp + off)
+                            : (const void*)((const uint16_t*)k_cmp + off);
+        vr[n].row = cmp_f64 ? (const void*)((const double*)v_cmp + off)
+                            : (const void*)((const uint16_t*)v_cmp + off);
         ++n;
       }
       int64_t p0 = t - window + 1;
@@ -538,8 +555,9 @@ int orc_attend(const uint16_t* q, const int32_t* qb, const int32_t* qt, int64_t 
           bad = 1;
           break;
         }
-        kr[n] = k_raw + b * raw_bstride + r * D;
-        vr[n] = v_raw + b * raw_bstride + r * D;
+        kr[n].f64 = vr[n].f64 = 0;
+        kr[n].row = k_raw + b * raw_bstride + r * D;
+        vr[n].row = v_raw + b * raw_bstride + r * D;
         ++n;
       }
       if (bad) {
@@ -552,7 +570,7 @@ int orc_attend(const uint16_t* q, const int32_t* qb, const int32_t* qt, int64_t 
         double M = -INFINITY;
         for (int64_t j = 0; j < n; ++j) {
           double s = 0.0;
-          for (int e = 0; e < D; ++e) s += qv[e] * orc_bf16_to_f64(kr[j][e]);
+          for (int e = 0; e < D; ++e) s += qv[e] * orc_elem(kr[j], e);
           l[j] = scale * s;
           if (l[j] > M) M = l[j];
         }
@@ -569,7 +587,7 @@ int orc_attend(const uint16_t* q, const int32_t* qb, const int32_t* qt, int64_t 
         for (int64_t j = 0; j < n; ++j) {
           double p = exp(l[j] - M);
           Z += p;
-          for (int e = 0; e < D; ++e) acc[e] += p * orc_bf16_to_f64(vr[j][e]);
+          for (int e = 0; e < D; ++e) acc[e] += p * orc_elem(vr[j], e);
         }
         for (int e = 0; e < D; ++e) o[e] = acc[e] / Z;
         lse[qq * H + h] = M + log(Z);
@@ -582,6 +600,58 @@ int orc_attend(const uint16_t* q, const int32_t* qb, const int32_t* qt, int64_t 
     free(acc);
   }
   return err;
+}
+
+int orc_attend(const uint16_t* q, const int32_t* qb, const int32_t* qt, int64_t Q, int H, int D,
+               const uint16_t* k_cmp, const uint16_t* v_cmp, int64_t cmp_bstride,
+               int64_t n_cmp_rows, const int32_t* sel, int64_t sel_stride, int n_sel,
+               const uint16_t* k_raw, const uint16_t* v_raw, int64_t raw_bstride,
+               int64_t raw_base, int64_t raw_rows, int window, const float* sink, double scale,
+               double* out, double* lse) {
+  return attend_rows(q, qb, qt, Q, H, D, k_cmp, v_cmp, 0, cmp_bstride, n_cmp_rows, sel,
+                     sel_stride, n_sel, k_raw, v_raw, raw_bstride, raw_base, raw_rows, window,
+                     sink, scale, out, lse);
+}
+
+/* The same with the compressed rows given as fp64 values (FP8-stored entries
+ * decoded by orc_kv8_dequantize); the raw window rows stay bf16. */
+int orc_attend_f64cmp(const uint16_t* q, const int32_t* qb, const int32_t* qt, int64_t Q, int H,
+                      int D, const double* k_cmp, const double* v_cmp, int64_t cmp_bstride,
+                      int64_t n_cmp_rows, const int32_t* sel, int64_t sel_stride, int n_sel,
+                      const uint16_t* k_raw, const uint16_t* v_raw, int64_t raw_bstride,
+                      int64_t raw_base, int64_t raw_rows, int window, const float* sink,
+                      double scale, double* out, double* lse) {
+  return attend_rows(q, qb, qt, Q, H, D, k_cmp, v_cmp, 1, cmp_bstride, n_cmp_rows, sel,
+                     sel_stride, n_sel, k_raw, v_raw, raw_bstride, raw_base, raw_rows, window,
+                     sink, scale, out, lse);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Mixed-precision storage of the compressed KV cache                       */
+/* ------------------------------------------------------------------------ */
+
+/* The hyper.ai DeepSeek-V4 page (Method) keeps the RoPE dimensions of the KV
+ * entries in BF16 and stores the rest in FP8.  Reading: of a compressed
+ * entry's d channels, the last n_rope are the RoPE channels (bf16); the first
+ * d - n_rope are E4M3 codes with one fp32 scale per entry (the FP8 rule of
+ * the indexer keys: scale = amax / 448 over those channels).  A V entry has no
+ * RoPE channels (n_rope = 0).  Decoded value of channel c:
+ *     c <  d - n_rope:  e4m3(codes[r][c]) * scale[r]
+ *     c >= d - n_rope:  bf16(rope[r][c - (d - n_rope)])
+ * codes: uint8 [rows][d - n_rope]; scale: fp32 [rows]; rope: bf16 bits
+ * [rows][n_rope] (NULL when n_rope = 0); out: fp64 [rows][d]. */
+int orc_kv8_dequantize(const uint8_t* codes, const float* scale, const uint16_t* rope,
+                       int64_t rows, int d, int n_rope, double* out) {
+  if (!codes || !scale || !out || rows < 0 || d <= 0 || n_rope < 0 || n_rope > d ||
+      (n_rope > 0 && !rope))
+    return ORC_ERR_ARG;
+  const int dn = d - n_rope;
+  for (int64_t r = 0; r < rows; ++r) {
+    for (int c = 0; c < dn; ++c)
+      out[r * d + c] = orc_e4m3_to_f64(codes[r * dn + c]) * (double)scale[r];
+    for (int c = 0; c < n_rope; ++c) out[r * d + dn + c] = orc_bf16_to_f64(rope[r * n_rope + c]);
+  }
+  return ORC_OK;
 }
 
 /* ------------------------------------------------------------------------ */

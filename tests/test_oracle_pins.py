@@ -615,3 +615,69 @@ def test_out_proj_is_block_diagonal():
     want = bits_to_f64(o).reshape(n, H * D) @ big.T
     np.testing.assert_allclose(oracle.grouped_out_proj(o, W), want, rtol=1e-13, atol=1e-13)
 
+
+
+# ---------------------------------------------------------------- FP8 KV storage
+
+def test_kv8_dequantize_hand_example():
+    g = _golden("kv8_hand.txt")
+    codes = g["deq_codes"].astype(np.uint8)[None]
+    out = oracle.kv8_dequantize(codes, np.array([g["deq_scale"]], np.float32),
+                                bf16_bits(g["deq_rope"])[None])
+    np.testing.assert_array_equal(out[0], g["deq_out"])
+
+
+def test_kv8_dequantize_matches_torch_float8_times_scale():
+    rows, dn, nr = 37, 64, 64
+    codes = RNG.integers(0, 256, (rows, dn)).astype(np.uint8)
+    codes[codes == 0x7F] = 0x7E  # leave out the NaN codes
+    codes[codes == 0xFF] = 0xFE
+    scale = (RNG.random(rows) * 0.02 + 1e-3).astype(np.float32)
+    rope = bf16_bits(RNG.standard_normal((rows, nr)))
+    out = oracle.kv8_dequantize(codes, scale, rope)
+    dec = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    np.testing.assert_array_equal(out[:, :dn], dec * scale.astype(np.float64)[:, None])
+    np.testing.assert_array_equal(out[:, dn:], bits_to_f64(rope))
+    v = oracle.kv8_dequantize(codes, scale)  # V entries: no RoPE channels
+    np.testing.assert_array_equal(v, out[:, :dn])
+
+
+def test_attention_over_fp8_entries_hand_example():
+    g = _golden("kv8_hand.txt")
+    K = oracle.kv8_dequantize(g["k_codes"].astype(np.uint8).reshape(2, 1),
+                              g["k_scale"].astype(np.float32),
+                              bf16_bits(g["k_rope"]).reshape(2, 1))
+    V = oracle.kv8_dequantize(g["v_codes"].astype(np.uint8), g["v_scale"].astype(np.float32))
+    q = bf16_bits(g["q"])[None, None]
+    o, lse = oracle.attend(q, [0], [10], K[None], V[None], np.array([[0, 1]], np.int32), None,
+                           None, 0, None, float(g["scale"]))
+    np.testing.assert_allclose(o[0, 0], g["o"], rtol=1e-14)
+    np.testing.assert_allclose(lse[0, 0], g["lse"], rtol=1e-14)
+
+
+def test_attention_fp64_rows_equal_bf16_rows_on_shared_values():
+    # FP8 codes with power-of-two scales decode to values that bf16 holds
+    # exactly, so attention over the decoded rows must equal attention over
+    # the same values stored as bf16 (the bf16 path is pinned above by SDPA)
+    B, N, H, D, W = 2, 40, 4, 16, 8
+    codes_k = RNG.integers(0, 0x7E, (B, N, D // 2)).astype(np.uint8)
+    codes_k |= (RNG.integers(0, 2, codes_k.shape) << 7).astype(np.uint8)
+    codes_v = RNG.integers(0, 0x7E, (B, N, D)).astype(np.uint8)
+    sk = np.exp2(RNG.integers(-6, 3, (B, N))).astype(np.float32)
+    sv = np.exp2(RNG.integers(-6, 3, (B, N))).astype(np.float32)
+    rope = bf16_bits(RNG.standard_normal((B, N, D // 2)))
+    K = oracle.kv8_dequantize(codes_k, sk, rope)
+    V = oracle.kv8_dequantize(codes_v, sv)
+    Kb, Vb = bf16_bits(K), bf16_bits(V)
+    np.testing.assert_array_equal(bits_to_f64(Kb), K)
+    np.testing.assert_array_equal(bits_to_f64(Vb), V)
+    q = bf16_bits(RNG.standard_normal((B, H, D)) * 0.25)
+    sel = np.stack([RNG.permutation(30)[:12] for _ in range(B)]).astype(np.int32)
+    sel[1, 3] = -1
+    kr, vr = bf16_bits(RNG.standard_normal((B, W, D))), bf16_bits(RNG.standard_normal((B, W, D)))
+    sink = RNG.standard_normal(H).astype(np.float32)
+    seq_len = np.array([128, 128], np.int32)
+    a = oracle.csa_decode(q, K, V, sel, kr, vr, seq_len, W, sink, 0.3, raw_base=120)
+    b = oracle.csa_decode(q, Kb, Vb, sel, kr, vr, seq_len, W, sink, 0.3, raw_base=120)
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
