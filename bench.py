@@ -73,19 +73,30 @@ def idx_row_bytes(wl) -> int:
     return wl.d_I * 2
 
 
+def cmp_row_bytes(wl) -> int:
+    """Bytes of one compressed K/V entry pair: bf16 K and V rows, or FP8
+    storage (K: 64 E4M3 codes + fp32 scale + 64 bf16 RoPE channels; V: 128
+    E4M3 codes + fp32 scale)."""
+    if getattr(wl, "kv_fp8", False):
+        return (64 + 4 + 64 * 2) + (wl.D + 4)
+    return 2 * wl.D * 2
+
+
 def algorithmic(wl) -> dict:
     """Algorithmic bytes (HBM) or FLOPs per stage per step, from the method's
     own data movement: every byte a stage must read or write at least once."""
     D, H, W = wl.D, wl.H, wl.W
     qo = 2 * H * D * 2  # q in + out, bf16
+    crow = cmp_row_bytes(wl)
     if wl.kind == "hca_decode":
-        nb = sum((min(n // wl.m, n // wl.m) + min(W, n)) * 2 * D * 2 for n in wl.lens)
+        nb = sum(n // wl.m * crow + min(W, n) * 2 * D * 2 for n in wl.lens)
         return {"attention": {"bytes": nb + wl.B * qo}}
     if wl.kind == "csa_decode":
         row, qrow = idx_row_bytes(wl), idx_row_bytes(wl)
         idx_b = sum(nv * row for nv in n_vis_decode(wl)) + wl.B * (
             wl.H_I * qrow + wl.H_I * 4 + wl.k * 4)
-        att_b = sum((min(wl.k, n // wl.m) + min(W, n)) * 2 * D * 2 for n in wl.lens) + wl.B * qo
+        att_b = sum(min(wl.k, n // wl.m) * crow + min(W, n) * 2 * D * 2
+                    for n in wl.lens) + wl.B * qo
         st = {"indexer_topk": {"bytes": idx_b}, "attention": {"bytes": att_b}}
         if wl.proj_groups:
             # the weights once, the attention output in, the projection out
@@ -337,6 +348,7 @@ def main():
                         else None),
            "H": wl.H, "D": wl.D, "k": wl.k, "window": wl.W, "H_I": wl.H_I, "d_I": wl.d_I,
            "indexer_dtype": "e2m1" if wl.idx_fp4 else "e4m3" if wl.idx_fp8 else "bf16",
+           "kv_dtype": "e4m3 (RoPE channels bf16)" if wl.kv_fp8 else "bf16",
            "stream_compress": wl.stream_compress, "parallelism": f"replicas{world}"}
 
     if args.impl == "reference":

@@ -132,6 +132,33 @@ CSA_API int csa_compress_kv_span(const void* raw, int64_t raw_bstride, int64_t r
                                  int64_t scale_bstride, int32_t* err_word, void* stream);
 
 /* ------------------------------------------------------------------------
+ * a1 into mixed-precision storage.  The hyper.ai DeepSeek-V4 page (Method)
+ * stores the KV entries in FP8 except their RoPE dimensions, which stay
+ * BF16.  Reading: the last n_rope channels of an entry are its RoPE
+ * channels.  The operator is that of csa_compress_kv_span; its output y is
+ * stored as
+ *     channels [0, d - n_rope):  E4M3 codes, row j of d - n_rope bytes in
+ *                                out_codes [B][codes_bstride], with
+ *                                out_scale fp32 [B][scale_bstride]: scale =
+ *                                max |y| over these channels / 448 (1 when
+ *                                all zero), code = nearest-even E4M3 of
+ *                                y / scale, saturating;
+ *     channels [d - n_rope, d):  bf16 (nearest even), row j of n_rope in
+ *                                out_rope [B][rope_bstride].
+ * Other arguments as csa_compress_kv_span.  0 < n_rope < d, n_rope a
+ * multiple of 8, d - n_rope a multiple of 16; codes_bstride counts bytes,
+ * rope_bstride bf16 elements.  A K stream with RoPE channels uses this call;
+ * a V stream (no RoPE channels) uses csa_compress_kv_span with
+ * CSA_FP8_E4M3.  Status: as csa_compress_kv_span.
+ * ---------------------------------------------------------------------- */
+CSA_API int csa_compress_kv_mixed(const void* raw, int64_t raw_bstride, int64_t raw_cap, int B,
+                                  int d, int m, int span, int block_begin, int n_blocks,
+                                  const void* W, const float* pos_bias, void* out_codes,
+                                  int64_t codes_bstride, float* out_scale, int64_t scale_bstride,
+                                  void* out_rope, int64_t rope_bstride, int n_rope,
+                                  int32_t* err_word, void* stream);
+
+/* ------------------------------------------------------------------------
  * a2 + a3. Lightning-Indexer scores and exact top-k.
  *
  * Sources: hyper.ai DeepSeek-V4 page, Method ("A Lightning Indexer then
@@ -210,6 +237,40 @@ CSA_API int csa_sparse_attn_batch_invariant(const void* q, const void* k_cmp, co
                                             const float* sink, float softmax_scale, int B, int T,
                                             int H, int D, void* out, float* lse,
                                             int keys_per_split, int32_t* err_word, void* stream);
+
+/* ------------------------------------------------------------------------
+ * a4 / a5 over FP8-stored compressed entries.  The hyper.ai DeepSeek-V4 page
+ * (Method) keeps the KV cache in FP8 apart from the RoPE dimensions, which
+ * stay BF16.  Reading (D = 128): K's channels 0-63 are its non-RoPE channels,
+ * stored as E4M3 codes with one fp32 scale per entry, channels 64-127 its
+ * RoPE channels in bf16; V has no RoPE channels: 128 E4M3 codes with its own
+ * per-entry scale.  The attention is that of csa_sparse_attn_prefill (or
+ * hca_dense_attn_decode) over the decoded entries, code * scale; on the GPU
+ * each decoded value is rounded to bf16 (nearest even) before the tensor
+ * cores use it.  The raw window rows stay bf16.
+ *
+ *   q        bf16 [B][T][H][128]; q_pos int32 [B][T] absolute positions
+ *            (T = 1, q_pos = seq_len - 1 for decode).
+ *   k_nope   E4M3 bytes [B][N_cap][64];  k_scale fp32 [B][N_cap];
+ *   k_rope   bf16 [B][N_cap][64];
+ *   v        E4M3 bytes [B][N_cap][128]; v_scale fp32 [B][N_cap]
+ *            (all contiguous: entry e of sequence b is row b * N_cap + e).
+ *   topk_idx int32 [B][T][k]: CSA, the selected entries (-1 = none).
+ *            NULL: HCA, every visible entry 0 .. n_vis - 1 with
+ *            n_vis = min(n_cmp[b], floor((q_pos + 1) / m_prime)).
+ *   k_raw, v_raw, raw_bstride, raw_cap, window, sink, softmax_scale, out,
+ *   lse, ws, ws_bytes: as csa_sparse_attn_prefill (workspace sized by
+ *   csa_attn_workspace(B, T, H, k + window), or N_cap + window for HCA).
+ *   H <= 64, D == 128, else CSA_ERR_UNSUPPORTED; other statuses as the
+ *   bf16 calls.
+ * ---------------------------------------------------------------------- */
+CSA_API int csa_attn_fp8kv(const void* q, const void* k_nope, const float* k_scale,
+                           const void* k_rope, const void* v, const float* v_scale, int N_cap,
+                           const int32_t* topk_idx, int k, const int32_t* n_cmp, int m_prime,
+                           const void* k_raw, const void* v_raw, int64_t raw_bstride,
+                           int64_t raw_cap, const int32_t* q_pos, int window, const float* sink,
+                           float softmax_scale, int B, int T, int H, int D, void* out, float* lse,
+                           void* ws, size_t ws_bytes, int32_t* err_word, void* stream);
 
 /* ------------------------------------------------------------------------
  * Grouped output projection after the MQA core attention.  The hyper.ai

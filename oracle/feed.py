@@ -10,8 +10,8 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from . import (BF16, FP4_E2M1, FP8_E4M3, compress, quantize_bf16, quantize_e4m3_rows,
-               quantize_fp4_rows)
+from . import (BF16, FP4_E2M1, FP8_E4M3, compress, kv8_dequantize, quantize_bf16,
+               quantize_e4m3_rows, quantize_fp4_rows)
 
 
 def u16(t: torch.Tensor) -> np.ndarray:
@@ -58,8 +58,15 @@ def oracle_inputs(wl, inp: dict, n_units: int, seqs=None, tokens=None) -> dict:
         a["seq_len"] = np.array(lens, np.int32)
         a["n_cmp"] = np.array([n // wl.m for n in lens], np.int32)
         a["q"] = u16(inp["q"][ix])
-        a["k_cmp"] = u16(inp["k_cmp"][ix])
-        a["v_cmp"] = u16(inp["v_cmp"][ix])
+        if getattr(wl, "kv_fp8", False):
+            # FP8-stored entries: the oracle attends over their decoded values
+            kn, ks, kr, v8, vs = (inp[k][ix] for k in ("kc_nope", "kc_scale", "kc_rope", "vc8",
+                                                       "vc_scale"))
+            a["k_cmp"] = kv8_dequantize(u8(kn), f32(ks), u16(kr))
+            a["v_cmp"] = kv8_dequantize(u8(v8), f32(vs))
+        else:
+            a["k_cmp"] = u16(inp["k_cmp"][ix])
+            a["v_cmp"] = u16(inp["v_cmp"][ix])
         a["k_win"], a["raw_base"] = window_arrays(inp["k_win"][ix].cpu(), lens)
         a["v_win"], _ = window_arrays(inp["v_win"][ix].cpu(), lens)
         if wl.kind == "csa_decode":

@@ -40,7 +40,7 @@ ABI_SYMBOLS = (
     "csa_indexer_topk", "csa_attn_workspace", "csa_sparse_attn_decode",
     "csa_sparse_attn_prefill", "hca_dense_attn_decode", "csa_indexer_topk_static",
     "csa_indexer_scores", "csa_compress_kv_span", "csa_sparse_attn_batch_invariant",
-    "csa_grouped_out_proj",
+    "csa_grouped_out_proj", "csa_compress_kv_mixed", "csa_attn_fp8kv",
 )
 
 # capacity of the library-owned scratch behind indexer_topk_static (bytes)
@@ -104,6 +104,12 @@ def lib() -> ctypes.CDLL:
             L.hca_dense_attn_decode.argtypes = [P, P, P, I64, I, P, I, P, P, I64, I64, P, I, P, F,
                                                 I, I, I, P, P, P, SZ, P, P]
             L.hca_dense_attn_decode.restype = I
+            L.csa_compress_kv_mixed.argtypes = [P, I64, I64, I, I, I, I, I, I, P, P, P, I64, P,
+                                                I64, P, I64, I, P, P]
+            L.csa_compress_kv_mixed.restype = I
+            L.csa_attn_fp8kv.argtypes = [P, P, P, P, P, P, I, P, I, P, I, P, P, I64, I64, P, I,
+                                         P, F, I, I, I, I, P, P, P, SZ, P, P]
+            L.csa_attn_fp8kv.restype = I
             _lib = L
     return _lib
 
@@ -200,6 +206,35 @@ def compress_kv(raw, W, pos_bias, m: int, block_begin: int, n_blocks: int, out,
                                         block_begin, n_blocks, *common)
         _check(st, "csa_compress_kv_span")
     return out
+
+
+def compress_kv_mixed(raw, W, pos_bias, m: int, block_begin: int, n_blocks: int, out_codes,
+                      out_scale, out_rope, err_word=None):
+    """Compress blocks into mixed-precision storage: the first d - n_rope
+    channels as E4M3 codes (out_codes uint8 [B, N_cap, d - n_rope]) with a
+    per-entry fp32 scale over them (out_scale [B, N_cap]), the last n_rope
+    (RoPE) channels as bf16 (out_rope [B, N_cap, n_rope]).  Other arguments as
+    :func:`compress_kv`.  Writes in place; returns (out_codes, out_scale,
+    out_rope)."""
+    _cuda(raw, "raw", torch.bfloat16)
+    _cuda(W, "W", torch.bfloat16)
+    _cuda(pos_bias, "pos_bias", torch.float32)
+    _cuda(out_codes, "out_codes", torch.uint8)
+    _cuda(out_scale, "out_scale", torch.float32)
+    _cuda(out_rope, "out_rope", torch.bfloat16)
+    B, _, d = raw.shape
+    n_rope = out_rope.shape[-1]
+    _need(out_codes.shape[-1] + n_rope == d, "codes and RoPE channels must add up to d")
+    _need(W.is_contiguous() and pos_bias.is_contiguous(), "W, pos_bias must be contiguous")
+    _need(out_scale.dim() == 2 and out_scale.stride(1) == 1, "out_scale [B, N_cap]")
+    _need(pos_bias.dim() == 2 and pos_bias.shape[1] == d, "pos_bias [span, d]")
+    st = lib().csa_compress_kv_mixed(
+        _p(raw), _bstride(raw), raw.shape[1], B, d, m, pos_bias.shape[0], block_begin, n_blocks,
+        _p(W), _p(pos_bias), _p(out_codes), _bstride(out_codes), _p(out_scale),
+        out_scale.stride(0), _p(out_rope), _bstride(out_rope), n_rope, _p(err_word),
+        _stream(raw.device))
+    _check(st, "csa_compress_kv_mixed")
+    return out_codes, out_scale, out_rope
 
 
 # ---------------------------------------------------------------- a2 + a3
@@ -427,6 +462,58 @@ def hca_dense_attn_decode(q, k_cmp, v_cmp, n_cmp, m_prime: int, k_raw, v_raw, se
         k_raw.shape[1] if k_raw is not None else 0, _p(seq_len), window, _p(sink),
         softmax_scale, B, H, D, _p(o), _p(lse), _p(wsb), wsn, _p(err_word), _stream(dev))
     _check(st, "hca_dense_attn_decode")
+    return (o, lse) if return_lse else o
+
+
+def attn_fp8kv(q, k_nope, k_scale, k_rope, v, v_scale, topk_idx, k_raw, v_raw, q_pos,
+               window: int, sink, n_cmp=None, m_prime: int = 1, softmax_scale: float = 1.0,
+               return_lse: bool = False, out=None, ws=None, err_word=None):
+    """Attention over FP8-stored compressed entries (K: 64 E4M3 non-RoPE
+    channels + k_scale, 64 bf16 RoPE channels; V: 128 E4M3 channels +
+    v_scale).  q: bf16 [B, T, H, 128]; k_nope uint8 [B, N_cap, 64]; k_scale,
+    v_scale fp32 [B, N_cap]; k_rope bf16 [B, N_cap, 64]; v uint8
+    [B, N_cap, 128]; q_pos int32 [B, T].  topk_idx int32 [B, T, k] (CSA) or
+    None (HCA: every visible entry, n_cmp int32 [B] and m_prime required).
+    Returns bf16 [B, T, H, 128] [, lse fp32 [B, T, H]]."""
+    _cuda(q, "q", torch.bfloat16)
+    _need(q.is_contiguous() and q.dim() == 4, "q: contiguous [B, T, H, 128]")
+    B, T, H, D = q.shape
+    N_cap = k_nope.shape[1]
+    for t, n, dt, w in ((k_nope, "k_nope", torch.uint8, 64), (k_rope, "k_rope", torch.bfloat16, 64),
+                        (v, "v", torch.uint8, 128)):
+        _cuda(t, n, dt)
+        _need(t.is_contiguous() and tuple(t.shape) == (B, N_cap, w), f"{n}: [B, N_cap, {w}]")
+    for t, n in ((k_scale, "k_scale"), (v_scale, "v_scale")):
+        _cuda(t, n, torch.float32)
+        _need(t.is_contiguous() and tuple(t.shape) == (B, N_cap), f"{n}: [B, N_cap]")
+    if k_raw is not None:
+        _cuda(k_raw, "k_raw", torch.bfloat16)
+        _cuda(v_raw, "v_raw", torch.bfloat16)
+        _need(k_raw.stride() == v_raw.stride() and k_raw.shape == v_raw.shape,
+              "k_raw and v_raw must share shape and strides")
+    if sink is not None:
+        _cuda(sink, "sink", torch.float32)
+    _cuda(q_pos, "q_pos", torch.int32)
+    _need(q_pos.is_contiguous(), "q_pos must be contiguous")
+    if topk_idx is not None:
+        _cuda(topk_idx, "topk_idx", torch.int32)
+        _need(topk_idx.is_contiguous(), "topk_idx must be contiguous")
+        k = topk_idx.shape[-1]
+        n_keys = k + window
+    else:
+        _cuda(n_cmp, "n_cmp", torch.int32)
+        k = 0
+        n_keys = N_cap + window
+    dev = q.device
+    o = out if out is not None else torch.empty_like(q)
+    lse = torch.empty((B, T, H), dtype=torch.float32, device=dev) if return_lse else None
+    wsb, wsn = _ws(attn_workspace(B, T, H, n_keys), dev, ws)
+    st = lib().csa_attn_fp8kv(
+        _p(q), _p(k_nope), _p(k_scale), _p(k_rope), _p(v), _p(v_scale), N_cap, _p(topk_idx), k,
+        _p(n_cmp), m_prime, _p(k_raw), _p(v_raw), _bstride(k_raw) if k_raw is not None else 0,
+        k_raw.shape[1] if k_raw is not None else 0, _p(q_pos), window, _p(sink), softmax_scale,
+        B, T, H, D, _p(o), _p(lse), _p(wsb), wsn, _p(err_word), _stream(dev))
+    _check(st, "csa_attn_fp8kv")
     return (o, lse) if return_lse else o
 
 

@@ -113,7 +113,7 @@ int csa_compress_kv_span(const void* raw, int64_t raw_bstride, int64_t raw_cap, 
     if (!out_scale || !aligned4(out_scale) || end_block > scale_bstride) return CSA_ERR_INVALID_ARG;
   }
   if (out_dtype == CSA_FP4_E2M1 && out_bstride % 32 != 0) return CSA_ERR_INVALID_ARG;
-  CompressArgs a;
+  CompressArgs a = {};
   a.raw = reinterpret_cast<const bf16*>(raw);
   a.raw_bstride = raw_bstride;
   a.raw_cap = raw_cap;
@@ -141,6 +141,50 @@ int csa_compress_kv(const void* raw, int64_t raw_bstride, int64_t raw_cap, int B
   return csa_compress_kv_span(raw, raw_bstride, raw_cap, B, d, m, m, block_begin, n_blocks, W,
                               pos_bias, out, out_bstride, out_dtype, out_scale, scale_bstride,
                               err_word, stream);
+}
+
+int csa_compress_kv_mixed(const void* raw, int64_t raw_bstride, int64_t raw_cap, int B, int d,
+                          int m, int span, int block_begin, int n_blocks, const void* W,
+                          const float* pos_bias, void* out_codes, int64_t codes_bstride,
+                          float* out_scale, int64_t scale_bstride, void* out_rope,
+                          int64_t rope_bstride, int n_rope, int32_t* err_word, void* stream) {
+  (void)err_word;
+  if (B < 0 || d <= 0 || m <= 0 || span < m || block_begin < 0 || n_blocks < 0)
+    return CSA_ERR_INVALID_ARG;
+  if ((d != 64 && d != 128) || span > 256) return CSA_ERR_UNSUPPORTED;
+  if (n_rope <= 0 || n_rope >= d || n_rope % 8 != 0 || (d - n_rope) % 16 != 0)
+    return CSA_ERR_INVALID_ARG;
+  if (B == 0 || n_blocks == 0) return CSA_OK;
+  if (!raw || !W || !pos_bias || !out_codes || !out_scale || !out_rope) return CSA_ERR_INVALID_ARG;
+  if (!aligned16(raw) || !aligned16(W) || !aligned4(pos_bias) || !aligned4(out_scale))
+    return CSA_ERR_INVALID_ARG;
+  const int64_t end_block = (int64_t)block_begin + n_blocks;
+  if (raw_cap < span || raw_bstride % 8 != 0 || raw_cap * d > raw_bstride)
+    return CSA_ERR_INVALID_ARG;
+  if (end_block * (d - n_rope) > codes_bstride || end_block * n_rope > rope_bstride ||
+      end_block > scale_bstride)
+    return CSA_ERR_INVALID_ARG;
+  CompressArgs a = {};
+  a.raw = reinterpret_cast<const bf16*>(raw);
+  a.raw_bstride = raw_bstride;
+  a.raw_cap = raw_cap;
+  a.B = B;
+  a.d = d;
+  a.m = m;
+  a.span = span;
+  a.block_begin = block_begin;
+  a.n_blocks = n_blocks;
+  a.W = reinterpret_cast<const bf16*>(W);
+  a.pos_bias = pos_bias;
+  a.out = out_codes;
+  a.out_bstride = codes_bstride;
+  a.fp8 = 1;
+  a.out_scale = out_scale;
+  a.scale_bstride = scale_bstride;
+  a.fp8_dims = d - n_rope;
+  a.out_hi = reinterpret_cast<bf16*>(out_rope);
+  a.out_hi_bstride = rope_bstride;
+  return cuda_status(launch_compress(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 // ---------------------------------------------------------------- a2 + a3
@@ -269,6 +313,7 @@ static void fill_common(AttnArgs& a, const void* q, const void* k_cmp, const voi
                         int64_t cmp_bstride, int N_cap, const void* k_raw, const void* v_raw,
                         int64_t raw_bstride, int64_t raw_cap, int window, const float* sink,
                         float softmax_scale, int H, void* out, float* lse, int32_t* err_word) {
+  a = AttnArgs();
   a.q = reinterpret_cast<const bf16*>(q);
   a.k_cmp = reinterpret_cast<const bf16*>(k_cmp);
   a.v_cmp = reinterpret_cast<const bf16*>(v_cmp);
@@ -412,6 +457,56 @@ int hca_dense_attn_decode(const void* q, const void* k_cmp, const void* v_cmp,
   a.n_batch = B;
   a.n_query = B;
   a.n_keys_max = N_cap + window;
+  return run_attention(a, ws, ws_bytes, stream);
+}
+
+int csa_attn_fp8kv(const void* q, const void* k_nope, const float* k_scale, const void* k_rope,
+                   const void* v, const float* v_scale, int N_cap, const int32_t* topk_idx, int k,
+                   const int32_t* n_cmp, int m_prime, const void* k_raw, const void* v_raw,
+                   int64_t raw_bstride, int64_t raw_cap, const int32_t* q_pos, int window,
+                   const float* sink, float softmax_scale, int B, int T, int H, int D, void* out,
+                   float* lse, void* ws, size_t ws_bytes, int32_t* err_word, void* stream) {
+  int st = check_attention_common(q, k_nope, v, (int64_t)N_cap * kD, N_cap, k_raw, v_raw,
+                                  raw_bstride, raw_cap, window, sink, B, T, H, D, out, lse);
+  if (st != CSA_OK || B == 0 || T == 0) return st;
+  if (H > 64) return CSA_ERR_UNSUPPORTED;
+  if (!q_pos || !aligned4(q_pos)) return CSA_ERR_INVALID_ARG;
+  if ((int64_t)B * T > (1 << 30)) return CSA_ERR_UNSUPPORTED;
+  if (N_cap > 0 && (!k_scale || !v_scale || !k_rope || !aligned4(k_scale) ||
+                    !aligned4(v_scale) || !aligned16(k_rope)))
+    return CSA_ERR_INVALID_ARG;
+  const bool dense = topk_idx == nullptr;
+  if (dense) {
+    if (m_prime <= 0 || (N_cap > 0 && (!n_cmp || !aligned4(n_cmp)))) return CSA_ERR_INVALID_ARG;
+    if (N_cap + window <= 0) return CSA_ERR_INVALID_ARG;
+  } else {
+    if (k <= 0 || N_cap <= 0 || !aligned4(topk_idx)) return CSA_ERR_INVALID_ARG;
+  }
+  AttnArgs a;
+  fill_common(a, q, k_nope, v, (int64_t)N_cap * kD, N_cap, k_raw, v_raw, raw_bstride, raw_cap,
+              window, sink, softmax_scale, H, out, lse, err_word);
+  a.kv8 = 1;
+  a.k8 = reinterpret_cast<const uint8_t*>(k_nope);
+  a.k8_scale = k_scale;
+  a.k_rope = reinterpret_cast<const bf16*>(k_rope);
+  a.v8 = reinterpret_cast<const uint8_t*>(v);
+  a.v8_scale = v_scale;
+  if (dense) {
+    a.dense = 1;
+    a.n_cmp = n_cmp;
+    a.m_prime = m_prime;
+    a.n_keys_max = N_cap + window;
+  } else {
+    a.sel = topk_idx;
+    a.sel_count = k;
+    a.sel_stride = k;
+    a.n_keys_max = k + window;
+  }
+  a.pos = q_pos;
+  a.pos_is_len = 0;
+  a.T = T;
+  a.n_batch = B;
+  a.n_query = B * T;
   return run_attention(a, ws, ws_bytes, stream);
 }
 

@@ -65,9 +65,20 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSCol = 0;    // S buffer b at column 128 * b
 constexpr uint32_t kOCol = 256;  // O accumulator
 
-template <int M>
+// FP8-stored compressed entries (KV8): per entry 64 E4M3 codes of K's
+// non-RoPE channels, 128 of V, one fp32 scale each; the staging slot of a
+// stage holds them for its 64 slots until they are decoded into the ring.
+constexpr int kS8K = 0;                  // [64 rows][64 B]
+constexpr int kS8V = kS8K + 64 * 64;     // [64 rows][128 B]
+constexpr int kS8KS = kS8V + 64 * 128;   // fp32 [64]
+constexpr int kS8VS = kS8KS + 64 * 4;    // fp32 [64]
+constexpr int kS8Bytes = kS8VS + 64 * 4;
+constexpr int kS8Slots = 3;  // a stage's codes are decoded kS8Lag stages after their copies
+constexpr int kS8Lag = 2;
+
+template <int M, bool KV8 = false>
 struct Cfg {
-  static constexpr int kStages = M == 64 ? 6 : 4;  // 64-key stages, even
+  static constexpr int kStages = KV8 ? 4 : M == 64 ? 6 : 4;  // 64-key stages, even
   static constexpr int kPairs = kStages / 2;
   static constexpr int kRegion = kStages * kBlk;
   static constexpr int kQBytes = M * 256;  // 2 K-blocks x [M x 128 B]
@@ -79,7 +90,8 @@ struct Cfg {
   static constexpr int kV1 = kV0 + kRegion;
   static constexpr int kPOff = kV1 + kRegion;
   static constexpr int kMetaOff = kPOff + kPBytes;  // stages x 64 row codes
-  static constexpr int kBarOff = kMetaOff + kStages * kStageKeys * 4;
+  static constexpr int kS8Off = kMetaOff + kStages * kStageKeys * 4;
+  static constexpr int kBarOff = kS8Off + (KV8 ? kS8Slots * kS8Bytes : 0);
   static constexpr int kSmemBytes = kBarOff + 512 + 1024;  // + alignment slack
   // after the main loop: own partial O rows (fp32) over the K regions, rows
   // received from the cluster over the V regions (and P); lse values and
@@ -109,12 +121,14 @@ struct Bars {
   int timed_out;
   uint32_t valid[6][2];
   uint32_t dense[6][2];  // per loader warp 0/1: its 32 rows continue its lane 0's row
+  uint64_t s8_full[kS8Slots];  // KV8: a staging slot's bulk copies landed (one arrival a stage)
 };
 
 // Tensor maps: the query block, and boxes of 64 rows that load a whole stage
 // of contiguous compressed entries.
 struct Maps {
   CUtensorMap q, kc, vc;
+  CUtensorMap kr;  // KV8: K's RoPE channels, rows of 64 bf16
 };
 
 // Slot -> row code: r >= 0 is row r of the 2-D row view of the compressed
@@ -180,6 +194,19 @@ __device__ __forceinline__ void loaders_sync() {
   asm volatile("bar.sync 1, %0;\n" ::"n"(kLoadThreads) : "memory");
 }
 
+// Eight E4M3 codes (c.x low byte first) times the entry's scale, as eight
+// bf16 (nearest even): one 16-byte row chunk of the decoded entry.
+__device__ __forceinline__ uint4 dequant8(uint2 c, float sc) {
+  uint32_t w[4];
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    const uint32_t hv = e4m3x2_to_f16x2((uint16_t)(((h < 2) ? c.x : c.y) >> (16 * (h & 1))));
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hv));
+    w[h] = pack_bf16x2(f.x * sc, f.y * sc);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 template <int M>
 struct RowMap {  // softmax-thread view of the 16-lane TMEM layout
   static constexpr int NG = M / 64;  // 16-lane groups per warp quadrant
@@ -191,10 +218,10 @@ struct RowMap {  // softmax-thread view of the 16-lane TMEM layout
   }
 };
 
-template <int M>
+template <int M, bool KV8>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(AttnArgs a, const __grid_constant__ Maps maps) {
-  using C = Cfg<M>;
+  using C = Cfg<M, KV8>;
   constexpr int kStages = C::kStages;
   constexpr int kPairs = C::kPairs;
   constexpr int NL = kLoadThreads;
@@ -258,6 +285,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::mbar_init(&bars->p_full, kSoftThreads / 32);
     tc::mbar_init(&bars->p_free, 1);
     tc::mbar_init(&bars->q_full, 1);
+    if (KV8)
+      for (int i = 0; i < kS8Slots; ++i) tc::mbar_init(&bars->s8_full[i], 1);
     bars->timed_out = 0;
     tc::fence_mbar_init();
     if (n_tiles > 0) {  // H rows of 256 bytes as two K-blocks
@@ -356,6 +385,105 @@ __global__ void __launch_bounds__(kThreads, 1)
     // for a gathered stage once its own copies have landed (cp.async
     // mbarrier tracking, the loader does not block), for a TMA stage at issue
     // (thread 0's arrival carries the transaction count).
+    // KV8: a stage's compressed rows go as E4M3 codes and scales to a staging
+    // slot (bulk copies when its 64 rows are contiguous, else 16-byte
+    // cp.async gathers), RoPE channels (bf16) and raw window rows straight to
+    // the ring; kS8Lag stages later every loader decodes its share of the
+    // codes into the ring's bf16 rows (code * scale) and gives the stage's
+    // kv_full arrival.
+    auto kv8_issue = [&](int j, bool dense) {
+      const int st = j % kStages;
+      const uint32_t stg = sbase + C::kS8Off + (j % kS8Slots) * kS8Bytes;
+      const uint32_t off = st * kBlk;
+      uint64_t* full = &bars->s8_full[j % kS8Slots];
+      if (dense) {
+        // 64 contiguous entries: their codes as two bulk copies, their RoPE
+        // channels as one TMA box into the ring (thread 0); the scales below
+        if (lt == 0) {
+          const int32_t row0 = codes[st * kStageKeys];
+          tma::expect_tx(full, kStageKeys * (64 + 128 + 128));
+          tma::bulk_load(stg + kS8K, a.k8 + (int64_t)row0 * 64, kStageKeys * 64, full);
+          tma::bulk_load(stg + kS8V, a.v8 + (int64_t)row0 * 128, kStageKeys * 128, full);
+          tma::load_box(sbase + C::kK1 + off, &maps.kr, 0, row0, full);
+        }
+      } else if (lt == 0) {
+        tc::mbar_arrive(full);
+      }
+      constexpr int kIss = (kStageKeys * 16 + NL - 1) / NL;
+      int32_t cds[kIss];
+#pragma unroll
+      for (int i = 0; i < kIss; ++i) {
+        const int ci = lt + i * NL;
+        cds[i] = ci < kStageKeys * 16 ? codes[st * kStageKeys + (ci >> 4)] : -1;
+      }
+#pragma unroll
+      for (int i = 0; i < kIss; ++i) {
+        const int ci = lt + i * NL;
+        if (dense || ci >= kStageKeys * 16) break;
+        const int r = ci >> 4, c16 = ci & 15;
+        const int32_t cd = cds[i];
+        const uint32_t so = off + ((c16 >> 3) ? C::kRegion : 0) + tc::sw128_offset(r, c16 & 7);
+        if (cd >= 0) {
+          if (c16 < 4)
+            cp_async16(stg + kS8K + r * 64 + c16 * 16, a.k8 + (int64_t)cd * 64 + c16 * 16, 16);
+          if (c16 < 8)
+            cp_async16(stg + kS8V + r * 128 + c16 * 16, a.v8 + (int64_t)cd * 128 + c16 * 16, 16);
+          else
+            cp_async16(sbase + C::kK0 + so, a.k_rope + (int64_t)cd * 64 + (c16 - 8) * 8, 16);
+        } else {
+          const bool ok = cd != -1;
+          const int64_t goff = (int64_t)(-(cd + 2)) * kD + c16 * 8;
+          cp_async16(sbase + C::kK0 + so, ok ? (const void*)(kr + goff) : (const void*)a.q,
+                     ok ? 16 : 0);
+          cp_async16(sbase + C::kV0 + so, ok ? (const void*)(vr + goff) : (const void*)a.q,
+                     ok ? 16 : 0);
+        }
+      }
+      if (lt < kStageKeys) {
+        const int32_t cd = codes[st * kStageKeys + lt];
+        if (cd >= 0) {
+          cp_async4(stg + kS8KS + lt * 4, a.k8_scale + cd, 4);
+          cp_async4(stg + kS8VS + lt * 4, a.v8_scale + cd, 4);
+        }
+      }
+      cp_async_commit();
+    };
+    auto kv8_decode = [&](int s8) {
+      loaders_sync();  // every loader's copies of stage s8 have landed
+      wait_or_flag(&bars->s8_full[s8 % kS8Slots], (s8 / kS8Slots) & 1, bars, a.err);  // and bulk
+      const int st = s8 % kStages, pr = (s8 >> 1) % kPairs;
+      const uint8_t* stg = sm + C::kS8Off + (s8 % kS8Slots) * kS8Bytes;
+      const float* ksc = reinterpret_cast<const float*>(stg + kS8KS);
+      const float* vsc = reinterpret_cast<const float*>(stg + kS8VS);
+      const uint32_t off = st * kBlk;
+      // 24 output chunks per row: 8 of K's non-RoPE channels, 16 of V; each
+      // thread loads all of its chunks' codes first, then converts and stores
+      // them (independent work for the few loader warps of each scheduler)
+      constexpr int kPer = kStageKeys * 24 / NL;
+      static_assert(kStageKeys * 24 % NL == 0, "decode chunks per loader thread");
+      uint2 c8[kPer];
+      float scv[kPer];
+      uint32_t dst[kPer];
+      bool use[kPer];
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const int oc = lt + i * NL;
+        const int r = oc / 24, part = oc - r * 24;
+        const int v = part - 8;
+        const bool isk = part < 8;
+        use[i] = codes[st * kStageKeys + r] >= 0;  // rows of other kinds are in place
+        c8[i] = *reinterpret_cast<const uint2*>(stg + (isk ? kS8K + r * 64 + part * 8
+                                                           : kS8V + r * 128 + v * 8));
+        scv[i] = isk ? ksc[r] : vsc[r];
+        dst[i] = isk ? C::kK0 + off + tc::sw128_offset(r, part)
+                     : C::kV0 + off + (v >> 3) * C::kRegion + tc::sw128_offset(r, v & 7);
+      }
+#pragma unroll
+      for (int i = 0; i < kPer; ++i)
+        if (use[i]) *reinterpret_cast<uint4*>(sm + dst[i]) = dequant8(c8[i], scv[i]);
+      tc::fence_proxy_async_smem();
+      tc::mbar_arrive(&bars->kv_full[pr]);
+    };
     int issued = 0;
     for (int j = 0; j < n_stages; ++j) {
       const int st = j % kStages, pr = (j >> 1) % kPairs;
@@ -383,11 +511,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         pf[kPrefetch - 1] = ks.fetch(k_begin + (j + kPrefetch) * kStageKeys + lt);
       loaders_sync();
       const int32_t base = codes[st * kStageKeys];
-      const bool dense = (bars->dense[st][0] & bars->dense[st][1]) == 0xFFFFFFFFu &&
-                         codes[st * kStageKeys + 32] == base + 32;
+      const bool dense_rows = (bars->dense[st][0] & bars->dense[st][1]) == 0xFFFFFFFFu &&
+                              codes[st * kStageKeys + 32] == base + 32;
+      const bool dense = !KV8 && dense_rows;
       if (lt == 0 && (j & 1)) tc::mbar_arrive(&bars->meta_full[pr]);  // both stages' bits
       const uint32_t off = st * kBlk;
-      if (dense) {
+      if constexpr (KV8) {
+        kv8_issue(j, dense_rows);
+        if (j >= kS8Lag) {
+          cp_async_wait<kS8Lag>();
+          kv8_decode(j - kS8Lag);
+        }
+      } else if (dense) {
         if (lt == 0) {
           tma::expect_tx(&bars->kv_full[pr], 4 * kBlk);
           tma::load_box(sbase + C::kK0 + off, &maps.kc, 0, (int)base, &bars->kv_full[pr]);
@@ -414,8 +549,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       issued = j + 1;
     }
+    if constexpr (KV8) {
+      // the last stages' codes (only when every stage was issued)
+      if (issued == n_stages)
+        for (int s8 = n_stages > kS8Lag ? n_stages - kS8Lag : 0; s8 < n_stages; ++s8) {
+          if (n_stages - 1 - s8 >= 1)
+            cp_async_wait<1>();
+          else
+            cp_async_wait<0>();
+          kv8_decode(s8);
+        }
+    }
     asm volatile("cp.async.wait_all;\n" ::: "memory");
-    if (lt == 0) {
+    if (KV8 && lt == 0) {
+      // bulk copies still in flight after a timeout land before the CTA exits
+      tc::mbar_wait(&bars->q_full, 0, kWaitLimit);
+      for (int i = issued > kS8Slots ? issued - kS8Slots : 0; i < issued; ++i)
+        tc::mbar_wait(&bars->s8_full[i % kS8Slots], (i / kS8Slots) & 1, kWaitLimit);
+    } else if (lt == 0) {
       // bulk copies still in flight after a timeout land before the CTA exits
       tc::mbar_wait(&bars->q_full, 0, kWaitLimit);
       for (int i = issued > kStages ? issued - kStages : 0; i < issued; i += 2)
@@ -765,13 +916,13 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(AttnArgs a) {
 }
 
 // attr: room for two attributes (cluster shape; programmatic launch if pdl)
-template <int M>
+template <int M, bool KV8>
 cudaLaunchConfig_t launch_cfg(int n_split, int n_query, cudaStream_t st,
                               cudaLaunchAttribute* attr, bool pdl, bool cluster = true) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)n_split * (unsigned)n_query);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = Cfg<M>::kSmemBytes;
+  cfg.dynamicSmemBytes = Cfg<M, KV8>::kSmemBytes;
   cfg.stream = st;
   unsigned n = 0;
   if (n_split > 1 && cluster) {
@@ -788,7 +939,7 @@ cudaLaunchConfig_t launch_cfg(int n_split, int n_query, cudaStream_t st,
 }
 
 // Clusters of size n the device keeps resident at once (cached per device).
-template <int M>
+template <int M, bool KV8>
 int active_clusters(int n) {
   static std::mutex mu;  // callers may be on several host threads
   static int cache[16][kMaxCluster + 1];
@@ -804,11 +955,11 @@ int active_clusters(int n) {
   }
   int& c = cache[dev][n];
   if (c < 0) {
-    ensure_smem_attr((const void*)attn_tc_kernel<M>, Cfg<M>::kSmemBytes, true);
+    ensure_smem_attr((const void*)attn_tc_kernel<M, KV8>, Cfg<M, KV8>::kSmemBytes, true);
     cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = launch_cfg<M>(n, 1, nullptr, attr, false);
+    cudaLaunchConfig_t cfg = launch_cfg<M, KV8>(n, 1, nullptr, attr, false);
     int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, attn_tc_kernel<M>, &cfg) != cudaSuccess)
+    if (cudaOccupancyMaxActiveClusters(&clusters, attn_tc_kernel<M, KV8>, &cfg) != cudaSuccess)
       clusters = 0;
     cudaGetLastError();
     c = clusters;
@@ -816,9 +967,10 @@ int active_clusters(int n) {
   return c;
 }
 
-template <int M>
+template <int M, bool KV8>
 cudaError_t launch_tc(AttnArgs a, const Maps& maps, void* ws, cudaStream_t st) {
-  cudaError_t e = ensure_smem_attr((const void*)attn_tc_kernel<M>, Cfg<M>::kSmemBytes, true);
+  cudaError_t e =
+      ensure_smem_attr((const void*)attn_tc_kernel<M, KV8>, Cfg<M, KV8>::kSmemBytes, true);
   if (e != cudaSuccess) return e;
   // Pick the split count: at most one cluster of splits per query, every
   // cluster resident at once (one wave), about one CTA per SM in total.
@@ -833,7 +985,7 @@ cudaError_t launch_tc(AttnArgs a, const Maps& maps, void* ws, cudaStream_t st) {
   } else {
     for (int cap = kMaxCluster; cap >= 1; --cap) {
       attn_plan(a.n_query, a.n_keys_max, cap, &ns, &kps);
-      if (ns <= 1 || (long)active_clusters<M>(ns) >= (long)a.n_query) break;
+      if (ns <= 1 || (long)active_clusters<M, KV8>(ns) >= (long)a.n_query) break;
     }
   }
   // Where clusters that large cannot all be resident and a workspace is
@@ -856,8 +1008,8 @@ cudaError_t launch_tc(AttnArgs a, const Maps& maps, void* ws, cudaStream_t st) {
     a.part_lse = a.part_o + (int64_t)a.n_query * ns * a.H * kD;
   }
   cudaLaunchAttribute attr[2];
-  cudaLaunchConfig_t cfg = launch_cfg<M>(ns, a.n_query, st, attr, true, !free_splits);
-  e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<M>, a, maps);
+  cudaLaunchConfig_t cfg = launch_cfg<M, KV8>(ns, a.n_query, st, attr, true, !free_splits);
+  e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<M, KV8>, a, maps);
   if (e != cudaSuccess || !free_splits) return e;
   return launch_pdl(attn_merge_kernel, dim3((unsigned)a.n_query, (unsigned)((a.H + 3) / 4)),
                     dim3(128), 0, st, a);
@@ -900,13 +1052,21 @@ cudaError_t launch_attention(AttnArgs a, void* ws, cudaStream_t st) {
   const void* dummy = a.q;
   cudaError_t e = tma::encode_rows128(&maps.q, a.q, (uint64_t)a.n_query * a.H, (uint32_t)a.H);
   if (e != cudaSuccess) return e;
-  const bool has_c = a.k_cmp && a.N_cap > 0;
+  const bool has_c = a.k_cmp && a.N_cap > 0 && !a.kv8;
   const uint64_t crow = has_c ? (uint64_t)(a.n_batch - 1) * (a.cmp_bstride / kD) + a.N_cap : 1;
   e = tma::encode_rows128(&maps.kc, has_c ? a.k_cmp : dummy, crow, kStageKeys);
   if (e == cudaSuccess) e = tma::encode_rows128(&maps.vc, has_c ? a.v_cmp : dummy, crow, kStageKeys);
   if (e != cudaSuccess) return e;
-  if (a.H <= 64) return launch_tc<64>(a, maps, ws, st);
-  return launch_tc<128>(a, maps, ws, st);
+  if (a.kv8) {
+    if (a.H > 64) return cudaErrorInvalidValue;  // checked on the host first
+    const uint64_t rrow = a.N_cap > 0 ? (uint64_t)a.n_batch * a.N_cap : 1;
+    e = tma::encode_rows(&maps.kr, a.N_cap > 0 ? (const void*)a.k_rope : dummy, 64, rrow,
+                         kStageKeys);
+    if (e != cudaSuccess) return e;
+    return launch_tc<64, true>(a, maps, ws, st);
+  }
+  if (a.H <= 64) return launch_tc<64, false>(a, maps, ws, st);
+  return launch_tc<128, false>(a, maps, ws, st);
 }
 
 }  // namespace csa

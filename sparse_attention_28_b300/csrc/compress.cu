@@ -11,7 +11,10 @@
 //     y[j][c] = sum_i softmax_i(g[.][c])[i] * x[p_i][c]
 // span = m is the non-overlapping operator.  Output: bf16 (nearest even), or
 // E4M3 with one fp32 scale per entry, scale = max_c |y| / 448 (1 if all
-// zero), code = nearest-even E4M3 of y / scale, saturating.
+// zero), code = nearest-even E4M3 of y / scale, saturating.  Mixed storage
+// (the same page keeps the RoPE channels of the KV entries in BF16 and the
+// rest in FP8): channels below fp8_dims as E4M3 with the scale taken over
+// them alone, the others bf16 into a second array.
 //
 // One CTA per (block, sequence), one thread per output channel.  The
 // block's span raw rows (fp32) are staged in shared memory; each thread
@@ -131,8 +134,9 @@ __global__ void __launch_bounds__(D) compress_kernel(CompressArgs a) {
     out[c] = __float2bfloat16_rn(y);
     return;
   }
-  // E4M3 with a per-entry scale
-  float am = fabsf(y);
+  // E4M3 with a per-entry scale (channels below dl; mixed storage: the rest bf16)
+  const int dl = (a.fp8_dims > 0 && a.fp8_dims < D) ? a.fp8_dims : D;
+  float am = c < dl ? fabsf(y) : 0.f;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, o));
   if ((c & 31) == 0) red[c >> 5] = am;
@@ -141,8 +145,13 @@ __global__ void __launch_bounds__(D) compress_kernel(CompressArgs a) {
 #pragma unroll
   for (int w = 0; w < D / 32; ++w) amax = fmaxf(amax, red[w]);
   const float scale = amax > 0.f ? amax / 448.f : 1.f;
-  uint8_t* out = reinterpret_cast<uint8_t*>(a.out) + (int64_t)b * a.out_bstride + j * D;
-  out[c] = static_cast<uint8_t>(__nv_cvt_float_to_fp8(y / scale, __NV_SATFINITE, __NV_E4M3));
+  if (c < dl) {
+    uint8_t* out = reinterpret_cast<uint8_t*>(a.out) + (int64_t)b * a.out_bstride + j * dl;
+    out[c] = static_cast<uint8_t>(__nv_cvt_float_to_fp8(y / scale, __NV_SATFINITE, __NV_E4M3));
+  } else {
+    bf16* hi = a.out_hi + (int64_t)b * a.out_hi_bstride + j * (D - dl);
+    hi[c - dl] = __float2bfloat16_rn(y);
+  }
   if (c == 0) a.out_scale[(int64_t)b * a.scale_bstride + j] = scale;
 }
 

@@ -43,6 +43,16 @@ struct AttnArgs {
   int n_query;
   int n_keys_max;
   int fixed_kps;  // > 0: every query's keys split into ranges of this many slots
+  // FP8-stored compressed entries (kv8 != 0; k_cmp / v_cmp unused): K's 64
+  // non-RoPE channels as E4M3 codes [rows][64] with fp32 scales [rows], its 64
+  // RoPE channels bf16 [rows][64]; V as E4M3 codes [rows][128] with scales.
+  // Row = b * N_cap + entry.  H <= 64.
+  int kv8;
+  const uint8_t* k8;
+  const float* k8_scale;
+  const __nv_bfloat16* k_rope;
+  const uint8_t* v8;
+  const float* v8_scale;
   // filled by launch_attention
   int n_split;
   int keys_per_split;
@@ -120,6 +130,12 @@ struct CompressArgs {
   int fp4;  // E2M1 codes with E4M3 block scales (one per 16 channels)
   float* out_scale;
   int64_t scale_bstride;
+  // mixed storage (fp8 != 0, 0 < fp8_dims < d): channels [0, fp8_dims) as
+  // E4M3 rows of fp8_dims bytes in out, the rest bf16 rows of d - fp8_dims in
+  // out_hi (batch stride out_hi_bstride elements)
+  int fp8_dims;
+  __nv_bfloat16* out_hi;
+  int64_t out_hi_bstride;
 };
 
 cudaError_t launch_compress(const CompressArgs& a, cudaStream_t st);

@@ -20,9 +20,11 @@ from __future__ import annotations
 
 import torch
 
-from . import (attn_workspace, compress_kv, grouped_out_proj, hca_dense_attn_decode, indexer_scores,
-               indexer_topk, indexer_topk_workspace, sparse_attn_batch_invariant,
-               sparse_attn_decode, sparse_attn_prefill)
+from . import (attn_fp8kv, attn_workspace, compress_kv, grouped_out_proj, hca_dense_attn_decode,
+               indexer_scores, indexer_topk, indexer_topk_workspace,
+               sparse_attn_batch_invariant, sparse_attn_decode, sparse_attn_prefill)
+
+KV8_KEYS = ("kc_nope", "kc_scale", "kc_rope", "vc8", "vc_scale")
 
 
 def _ring_put(cache, b, positions, rows):
@@ -130,6 +132,7 @@ class CsaDecodeStep(_Step):
         self.q, self.sink = g("q"), g("sink")
         self.seq_len, self.n_cmp = g("seq_len"), g("n_cmp")
         self.k_cmp, self.v_cmp = g("k_cmp"), g("v_cmp")
+        self.kv8 = tuple(g(k) for k in KV8_KEYS) if wl.kv_fp8 else None
         self.q_idx, self.w, self.k_idx = g("q_idx"), g("w"), g("k_idx")
         self.q_scale, self.k_scale = g("q_scale"), g("k_scale")
         self.q_pos = (self.seq_len - 1).view(B, 1).contiguous()
@@ -211,6 +214,12 @@ class CsaDecodeStep(_Step):
 
     def _attend(self):
         wl = self.wl
+        if wl.kv_fp8:
+            B, H, D = self.q.shape
+            attn_fp8kv(self.q.view(B, 1, H, D), *self.kv8, self.idx, self.k_raw, self.v_raw,
+                       self.q_pos, wl.W, self.sink,
+                       out=getattr(self, "attn_out", self.out).view(B, 1, H, D), ws=self.ws_attn)
+            return
         if wl.batch_invariant:
             # fixed key splits: each sequence's result is independent of the batch
             B, H, D = self.q.shape
@@ -249,7 +258,7 @@ class CsaDecodeStep(_Step):
 
 
 class HcaDecodeStep(_Step):
-    INPUTS = ("q", "seq_len")
+    INPUTS = ("q", "seq_len", "q_pos")
 
     def __init__(self, inp: dict, device="cuda"):
         wl = inp["workload"]
@@ -261,6 +270,8 @@ class HcaDecodeStep(_Step):
         self.q, self.sink = g("q"), g("sink")
         self.seq_len, self.n_cmp = g("seq_len"), g("n_cmp")
         self.k_cmp, self.v_cmp = g("k_cmp"), g("v_cmp")
+        self.kv8 = tuple(g(k) for k in KV8_KEYS) if wl.kv_fp8 else None
+        self.q_pos = (self.seq_len - 1).view(B, 1).contiguous() if wl.kv_fp8 else None
         self.k_raw = _nan((B, W, D), torch.bfloat16, dev)
         self.v_raw = _nan((B, W, D), torch.bfloat16, dev)
         kw, vw = g("k_win"), g("v_win")
@@ -275,6 +286,12 @@ class HcaDecodeStep(_Step):
 
     def _attend(self):
         wl = self.wl
+        if wl.kv_fp8:
+            B, H, D = self.q.shape
+            attn_fp8kv(self.q.view(B, 1, H, D), *self.kv8, None, self.k_raw, self.v_raw,
+                       self.q_pos, wl.W, self.sink, n_cmp=self.n_cmp, m_prime=wl.m,
+                       out=self.out.view(B, 1, H, D), ws=self.ws_attn)
+            return
         hca_dense_attn_decode(self.q, self.k_cmp, self.v_cmp, self.n_cmp, wl.m, self.k_raw,
                               self.v_raw, self.seq_len, wl.W, self.sink, out=self.out,
                               ws=self.ws_attn)

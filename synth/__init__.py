@@ -16,6 +16,9 @@ Recipe (the same for every workload):
 * FP8 indexer keys / queries: N(0, 1) fp32 values x, a per-row fp32 scale
   s = max|x| / 448, codes = torch's float8_e4m3fn cast of x / s (torch's
   library cast, not the oracle's codec nor the kernels' conversion);
+* FP8-stored compressed K/V (mixed precision): K's 64 non-RoPE channels and
+  V's 128 channels drawn as the FP8 indexer keys are (own scale per entry and
+  stream), K's 64 RoPE channels N(0, 1) bf16;
 * compressed caches of decode workloads are drawn directly (they are inputs
   of the decode calls); raw caches hold only the rows a step may read (the
   sliding window, plus the newest block where a step compresses one).
@@ -61,6 +64,7 @@ class Workload:
     batch_invariant: int = 0  # > 0: decode attention with fixed key splits of this size
     proj_groups: int = 0     # > 0: grouped output projection after the attention (G groups)
     proj_dim: int = 0        # output channels per projection group (d_g)
+    kv_fp8: bool = False     # compressed K/V stored in FP8 (E4M3 + scale; K's RoPE half bf16)
 
     @property
     def cspan(self) -> int:
@@ -100,6 +104,13 @@ WORKLOADS = {
     # the 128K decode with batch-invariant attention (fixed 320-key splits)
     "csa_decode_128k_bi": Workload("csa_decode_128k_bi", "csa_decode", B=32, L=131072, m=4,
                                    H=64, k=1024, batch_invariant=320),
+    # the 128K CSA decode and the 1M HCA decode over an FP8-stored compressed
+    # KV cache (K: 64 E4M3 non-RoPE channels + scale, 64 bf16 RoPE channels;
+    # V: 128 E4M3 channels + scale)
+    "csa_decode_128k_fp8kv": Workload("csa_decode_128k_fp8kv", "csa_decode", B=32, L=131072,
+                                      m=4, H=64, k=1024, kv_fp8=True),
+    "hca_decode_1m_fp8kv": Workload("hca_decode_1m_fp8kv", "hca_decode", B=16, L=1048576,
+                                    m=128, H=64, kv_fp8=True),
     # overlapping compression: each block formed from 2m tokens (its own and
     # the previous block's)
     "csa_prefill_4k_overlap": Workload("csa_prefill_4k_overlap", "csa_prefill", B=1, L=262144,
@@ -132,6 +143,19 @@ def randn_fp8_rows(shape, seed: int, tid: int, device="cpu"):
     return codes, s.contiguous()
 
 
+def randn_kv8(B: int, N: int, seed: int, tid: int, device="cpu", n_rope: int = 64):
+    """An FP8-stored compressed K/V cache of N(0,1) values: K's first
+    D_HEAD - n_rope channels as E4M3 codes with per-entry scales
+    (:func:`randn_fp8_rows`), its last n_rope channels bf16, V's D_HEAD
+    channels as E4M3 codes with per-entry scales.
+    Returns (k_nope u8 [B,N,D-n_rope], k_scale f32 [B,N], k_rope bf16
+    [B,N,n_rope], v u8 [B,N,D], v_scale f32 [B,N])."""
+    k_nope, k_scale = randn_fp8_rows((B, N, D_HEAD - n_rope), seed, tid, device)
+    k_rope = randn((B, N, n_rope), seed, tid + 1, device)
+    v, v_scale = randn_fp8_rows((B, N, D_HEAD), seed, tid + 2, device)
+    return k_nope, k_scale, k_rope, v, v_scale
+
+
 def rand_fp4_rows(shape, seed: int, tid: int, device="cpu"):
     """Random FP4-stored vectors of shape[-1] channels: uniformly drawn E2M1
     codes (two per byte, uint8 [..., d/2]) and E4M3 block-scale codes, one per
@@ -149,7 +173,8 @@ def rand_fp4_rows(shape, seed: int, tid: int, device="cpu"):
 def make_inputs(wl: Workload, seed: int = 0, device="cpu") -> dict:
     """All inputs of one step of workload ``wl`` (see the module docstring).
 
-    Decode keys: q [B,H,D]; k_cmp, v_cmp [B,N_cap,D]; q_idx [B,1,H_I,d_I];
+    Decode keys: q [B,H,D]; k_cmp, v_cmp [B,N_cap,D] (FP8-stored KV instead:
+    kc_nope, kc_scale, kc_rope, vc8, vc_scale, see :func:`randn_kv8`); q_idx [B,1,H_I,d_I];
     w [B,1,H_I]; k_idx [B,N_cap,d_I] (+ q_scale, k_scale for FP8); sink [H];
     seq_len, n_cmp [B]; k_win, v_win [B,W,D] = raw rows L_b-W .. L_b-1.
     Streaming compression adds raw_new_idx [B,m,d_I] (raw indexer-key rows of
@@ -181,8 +206,14 @@ def make_inputs(wl: Workload, seed: int = 0, device="cpu") -> dict:
         out["seq_len"] = lens.to(dev)
         out["n_cmp"] = (lens // m).to(dev)
         out["q"] = randn((B, H, D), seed, 2, dev, scale=qs)
-        out["k_cmp"] = randn((B, N_cap, D), seed, 3, dev)
-        out["v_cmp"] = randn((B, N_cap, D), seed, 4, dev)
+        if wl.kv_fp8:
+            assert not wl.stream_compress, "FP8 KV workloads read a cache filled beforehand"
+            out["k_cmp"] = out["v_cmp"] = None
+            (out["kc_nope"], out["kc_scale"], out["kc_rope"], out["vc8"],
+             out["vc_scale"]) = randn_kv8(B, N_cap, seed, 40, dev)
+        else:
+            out["k_cmp"] = randn((B, N_cap, D), seed, 3, dev)
+            out["v_cmp"] = randn((B, N_cap, D), seed, 4, dev)
         out["k_win"] = randn((B, W, D), seed, 5, dev)
         out["v_win"] = randn((B, W, D), seed, 6, dev)
         if wl.kind == "csa_decode":

@@ -70,8 +70,9 @@ def window_arrays(win: torch.Tensor, lens):
     return arr, base
 
 
-def check_attention(out_gpu, out_ref, lse_gpu=None, lse_ref=None, what=""):
-    """Attention parity: max-abs <= 2e-2, relative L2 <= 5e-3, lse within 1e-3."""
+def check_attention(out_gpu, out_ref, lse_gpu=None, lse_ref=None, what="", lse_tol=None):
+    """Attention parity: max-abs <= 2e-2, relative L2 <= 5e-3, lse within 1e-3
+    (or lse_tol: a scalar or an array shaped like lse)."""
     o = f64(out_gpu).reshape(-1)
     r = np.asarray(out_ref, np.float64).reshape(-1)
     assert np.all(np.isfinite(o)), f"{what}: non-finite output (stray read?)"
@@ -85,9 +86,31 @@ def check_attention(out_gpu, out_ref, lse_gpu=None, lse_ref=None, what=""):
         fin = np.isfinite(lr)
         np.testing.assert_array_equal(np.isfinite(lg), fin, err_msg=f"{what}: lse finiteness")
         if fin.any():
-            d = np.max(np.abs(lg[fin] - lr[fin]))
-            assert d <= LSE_ABS, f"{what}: lse max-abs {d:.3e}"
+            tol = np.asarray(LSE_ABS if lse_tol is None else lse_tol, np.float64).reshape(-1)
+            tol = (tol if tol.size == lr.size else np.full(lr.shape, tol.max()))[fin]
+            d = np.abs(lg[fin] - lr[fin])
+            assert np.all(d <= tol), f"{what}: lse max-abs {d.max():.3e} (worst excess " \
+                f"{(d - tol).max():.3e})"
     return max_abs, rel_l2
+
+
+def lse_tol(q, K, n_vis, scale=1.0):
+    """lse tolerance for FP8-stored keys.  The kernel rounds each decoded key
+    value to bf16 (relative error <= 2^-9) before the tensor cores use it, so
+    a logit moves by at most 2^-9 * scale * sum_d |q_d| |k_d|, and the lse by
+    at most the largest such move over the keys; on top of that the 1e-3 of
+    the bf16 path.  q: bf16 [B, T, H, D] (torch) or fp64 values; K: decoded
+    fp64 [B, N, D]; the max runs over each sequence's first n_vis[b] entries
+    (a superset of its keys; the raw window rows are bf16 and exact).
+    Returns [B, T, H]."""
+    qa = np.abs(f64(q) if isinstance(q, torch.Tensor) else np.asarray(q, np.float64))
+    B, T, H, _ = qa.shape
+    tol = np.full((B, T, H), 1e-3)
+    for b in range(B):
+        if n_vis[b] > 0:
+            m = np.einsum("thd,nd->thn", qa[b], np.abs(K[b, :n_vis[b]])).max(-1)
+            tol[b] += 2.0 ** -9 * scale * m
+    return tol
 
 
 def check_topk(idx_gpu, idx_ref, scores_ref, n_vis, k: int, what=""):

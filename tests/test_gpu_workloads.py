@@ -8,7 +8,7 @@ import torch
 import oracle
 import sparse_attention_28_b300 as csa
 import synth
-from _util import bf16_bound, check_attention, check_topk, f64, u8, u16
+from _util import bf16_bound, check_attention, check_topk, f64, lse_tol, u8, u16
 from oracle.feed import fill_new_entries, idx_dtype, oracle_inputs
 from sparse_attention_28_b300.steps import make_step
 
@@ -63,10 +63,20 @@ def _check_decode(name, seqs):
     # the same attention call as the step, fed the oracle's top-k
     full_ref = step.idx[:, 0].clone()
     full_ref[seqs] = torch.from_numpy(ref[:, 0]).to(DEV)
-    o2, l2 = csa.sparse_attn_decode(step.q, step.k_cmp, step.v_cmp, full_ref, step.k_raw,
-                                    step.v_raw, step.seq_len, wl.W, step.sink, return_lse=True)
+    if wl.kv_fp8:
+        B, H, D = step.q.shape
+        o2, l2 = csa.attn_fp8kv(step.q.view(B, 1, H, D), *step.kv8, full_ref.view(B, 1, -1),
+                                step.k_raw, step.v_raw, step.q_pos, wl.W, step.sink,
+                                return_lse=True)
+        o2, l2 = o2[:, 0], l2[:, 0]
+        tol = lse_tol(oracle.bf16_decode(a["q"])[:, None], a["k_cmp"], list(a["n_cmp"]))[:, 0]
+    else:
+        o2, l2 = csa.sparse_attn_decode(step.q, step.k_cmp, step.v_cmp, full_ref, step.k_raw,
+                                        step.v_raw, step.seq_len, wl.W, step.sink,
+                                        return_lse=True)
+        tol = None
     torch.cuda.synchronize()
-    check_attention(o2[seqs], ro, l2[seqs], rl, name + " attention")
+    check_attention(o2[seqs], ro, l2[seqs], rl, name + " attention", tol)
     # the step's own output wherever its top-k set is the oracle's
     same = [i for i, b in enumerate(seqs)
             if set(gidx[i, 0].tolist()) == set(ref[i, 0].tolist())]
@@ -95,6 +105,14 @@ def test_hca_decode_1m(cuda_device):
 
 def test_csa_decode_1m_fp8_streaming(cuda_device):
     _check_decode("csa_decode_1m_fp8", [0, 7])
+
+
+def test_csa_decode_128k_fp8kv(cuda_device):
+    _check_decode("csa_decode_128k_fp8kv", [0, 13, 31])
+
+
+def test_hca_decode_1m_fp8kv(cuda_device):
+    _check_decode("hca_decode_1m_fp8kv", [0, 9, 15])
 
 
 @pytest.mark.parametrize("name", ["csa_prefill_4k", "csa_prefill_4k_overlap"])
