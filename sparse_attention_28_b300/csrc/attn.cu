@@ -67,12 +67,16 @@ constexpr uint32_t kOCol = 256;  // O accumulator
 
 // FP8-stored compressed entries (KV8): per entry 64 E4M3 codes of K's
 // non-RoPE channels, 128 of V, one fp32 scale each; the staging slot of a
-// stage holds them for its 64 slots until they are decoded into the ring.
-constexpr int kS8K = 0;                  // [64 rows][64 B]
+// stage holds them (and K's bf16 RoPE channels) for its 64 slots until they
+// are decoded into the ring.  Only the decode writes a stage's compressed rows
+// into the ring, so the copies of a stage need no free ring slot and run
+// ahead of the tensor cores by kS8Lag stages.
+constexpr int kS8R = 0;                  // RoPE channels, [64 rows][128 B], 128-byte swizzled
+constexpr int kS8K = kS8R + 64 * 128;    // [64 rows][64 B]
 constexpr int kS8V = kS8K + 64 * 64;     // [64 rows][128 B]
 constexpr int kS8KS = kS8V + 64 * 128;   // fp32 [64]
 constexpr int kS8VS = kS8KS + 64 * 4;    // fp32 [64]
-constexpr int kS8Bytes = kS8VS + 64 * 4;
+constexpr int kS8Bytes = (kS8VS + 64 * 4 + 1023) / 1024 * 1024;  // slots stay 1024-aligned
 constexpr int kS8Slots = 3;  // a stage's codes are decoded kS8Lag stages after their copies
 constexpr int kS8Lag = 2;
 
@@ -111,7 +115,7 @@ struct Bars {
   uint64_t kv_full[3];     // per stage pair: both stages landed (one arrival per loader thread
                            // per stage, plus the TMA bytes)
   uint64_t pair_empty[3];  // per stage pair: the P V that read it has completed
-  uint64_t meta_full[3];   // per stage pair: validity bits published
+  uint64_t meta_full[4];   // per tile t % 4: its stages' validity bits published
   uint64_t s_full[2];
   uint64_t s_free[2];
   uint64_t p_full;
@@ -119,8 +123,11 @@ struct Bars {
   uint64_t q_full;
   uint32_t tmem_slot;
   int timed_out;
-  uint32_t valid[6][2];
-  uint32_t dense[6][2];  // per loader warp 0/1: its 32 rows continue its lane 0's row
+  // per stage j % 8 and loader warp 0/1 (a stage's bits outlive its ring slot:
+  // with KV8 the copies of stage j + 4 may start before tile j / 2 is done)
+  uint32_t valid[8][2];
+  uint32_t dense[8][2];  // its 32 rows continue its lane 0's row
+  uint32_t cmp[8][2];    // its 32 rows are all compressed entries
   uint64_t s8_full[kS8Slots];  // KV8: a staging slot's bulk copies landed (one arrival a stage)
 };
 
@@ -276,8 +283,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int p = 0; p < kPairs; ++p) {
       tc::mbar_init(&bars->kv_full[p], 2 * kLoadThreads);
       tc::mbar_init(&bars->pair_empty[p], 1);
-      tc::mbar_init(&bars->meta_full[p], 1);
     }
+    for (int i = 0; i < 4; ++i) tc::mbar_init(&bars->meta_full[i], 1);
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&bars->s_full[i], 1);
       tc::mbar_init(&bars->s_free[i], kSoftThreads / 32);  // one arrival per softmax warp
@@ -391,20 +398,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the ring; kS8Lag stages later every loader decodes its share of the
     // codes into the ring's bf16 rows (code * scale) and gives the stage's
     // kv_full arrival.
-    auto kv8_issue = [&](int j, bool dense) {
+    auto kv8_issue = [&](int j, bool dense, bool all_cmp) {
       const int st = j % kStages;
       const uint32_t stg = sbase + C::kS8Off + (j % kS8Slots) * kS8Bytes;
       const uint32_t off = st * kBlk;
       uint64_t* full = &bars->s8_full[j % kS8Slots];
+      if (!all_cmp && j >= kStages) {
+        // raw window rows and skipped slots go straight to the ring slot
+        if (lt == 0)
+          wait_or_flag(&bars->pair_empty[(j >> 1) % kPairs], ((j >> 1) / kPairs - 1) & 1, bars,
+                       a.err);
+        loaders_sync();
+      }
       if (dense) {
         // 64 contiguous entries: their codes as two bulk copies, their RoPE
-        // channels as one TMA box into the ring (thread 0); the scales below
+        // channels as one TMA box (thread 0); the scales below
         if (lt == 0) {
           const int32_t row0 = codes[st * kStageKeys];
           tma::expect_tx(full, kStageKeys * (64 + 128 + 128));
           tma::bulk_load(stg + kS8K, a.k8 + (int64_t)row0 * 64, kStageKeys * 64, full);
           tma::bulk_load(stg + kS8V, a.v8 + (int64_t)row0 * 128, kStageKeys * 128, full);
-          tma::load_box(sbase + C::kK1 + off, &maps.kr, 0, row0, full);
+          tma::load_box(stg + kS8R, &maps.kr, 0, row0, full);
         }
       } else if (lt == 0) {
         tc::mbar_arrive(full);
@@ -429,7 +443,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (c16 < 8)
             cp_async16(stg + kS8V + r * 128 + c16 * 16, a.v8 + (int64_t)cd * 128 + c16 * 16, 16);
           else
-            cp_async16(sbase + C::kK0 + so, a.k_rope + (int64_t)cd * 64 + (c16 - 8) * 8, 16);
+            cp_async16(stg + kS8R + tc::sw128_offset(r, c16 & 7),
+                       a.k_rope + (int64_t)cd * 64 + (c16 - 8) * 8, 16);
         } else {
           const bool ok = cd != -1;
           const int64_t goff = (int64_t)(-(cd + 2)) * kD + c16 * 8;
@@ -449,6 +464,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       cp_async_commit();
     };
     auto kv8_decode = [&](int s8) {
+      if (lt == 0 && s8 >= kStages)  // the ring slot's previous tile is done
+        wait_or_flag(&bars->pair_empty[(s8 >> 1) % kPairs], ((s8 >> 1) / kPairs - 1) & 1, bars,
+                     a.err);
       loaders_sync();  // every loader's copies of stage s8 have landed
       wait_or_flag(&bars->s8_full[s8 % kS8Slots], (s8 / kS8Slots) & 1, bars, a.err);  // and bulk
       const int st = s8 % kStages, pr = (s8 >> 1) % kPairs;
@@ -481,6 +499,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < kPer; ++i)
         if (use[i]) *reinterpret_cast<uint4*>(sm + dst[i]) = dequant8(c8[i], scv[i]);
+      // K's RoPE channels of the compressed rows: same swizzled offsets
+#pragma unroll
+      for (int i = 0; i < (kStageKeys * 8 + NL - 1) / NL; ++i) {
+        const int ci = lt + i * NL;
+        if (ci < kStageKeys * 8 && codes[st * kStageKeys + (ci >> 3)] >= 0) {
+          const uint32_t o = tc::sw128_offset(ci >> 3, ci & 7);
+          *reinterpret_cast<uint4*>(sm + C::kK1 + off + o) =
+              *reinterpret_cast<const uint4*>(stg + kS8R + o);
+        }
+      }
       tc::fence_proxy_async_smem();
       tc::mbar_arrive(&bars->kv_full[pr]);
     };
@@ -488,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < n_stages; ++j) {
       const int st = j % kStages, pr = (j >> 1) % kPairs;
       bool go = true;
-      if (lt == 0 && j >= kStages && (j & 1) == 0)
+      if (!KV8 && lt == 0 && j >= kStages && (j & 1) == 0)
         go = wait_or_flag(&bars->pair_empty[pr], ((j >> 1) / kPairs - 1) & 1, bars, a.err);
       go = go && !*(volatile int*)&bars->timed_out;
       // every loader thread takes the same branch: named barrier 1 below
@@ -500,9 +528,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int32_t w0 = __shfl_sync(0xFFFFFFFFu, cd, 0);
         const unsigned vb = __ballot_sync(0xFFFFFFFFu, cd != -1);
         const unsigned cb = __ballot_sync(0xFFFFFFFFu, w0 >= 0 && cd == w0 + (lt & 31));
+        const unsigned ab = __ballot_sync(0xFFFFFFFFu, cd >= 0);
         if ((lt & 31) == 0) {
-          bars->valid[st][lt >> 5] = vb;
-          bars->dense[st][lt >> 5] = cb;
+          bars->valid[j & 7][lt >> 5] = vb;
+          bars->dense[j & 7][lt >> 5] = cb;
+          bars->cmp[j & 7][lt >> 5] = ab;
         }
       }
 #pragma unroll
@@ -511,13 +541,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         pf[kPrefetch - 1] = ks.fetch(k_begin + (j + kPrefetch) * kStageKeys + lt);
       loaders_sync();
       const int32_t base = codes[st * kStageKeys];
-      const bool dense_rows = (bars->dense[st][0] & bars->dense[st][1]) == 0xFFFFFFFFu &&
+      const bool dense_rows = (bars->dense[j & 7][0] & bars->dense[j & 7][1]) == 0xFFFFFFFFu &&
                               codes[st * kStageKeys + 32] == base + 32;
+      const bool all_cmp = (bars->cmp[j & 7][0] & bars->cmp[j & 7][1]) == 0xFFFFFFFFu;
       const bool dense = !KV8 && dense_rows;
-      if (lt == 0 && (j & 1)) tc::mbar_arrive(&bars->meta_full[pr]);  // both stages' bits
+      if (lt == 0 && (j & 1)) tc::mbar_arrive(&bars->meta_full[(j >> 1) & 3]);  // both stages
       const uint32_t off = st * kBlk;
       if constexpr (KV8) {
-        kv8_issue(j, dense_rows);
+        kv8_issue(j, dense_rows, all_cmp);
         if (j >= kS8Lag) {
           cp_async_wait<kS8Lag>();
           kv8_decode(j - kS8Lag);
@@ -586,12 +617,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     uint8_t* pbuf = sm + C::kPOff;
     for (int j = 0; j < n_tiles; ++j) {
-      const int sb = j & 1, pr = j % kPairs;
+      const int sb = j & 1;
       // waits are made warp-uniform: tcgen05.ld/st below are warp-collective
-      if (!__all_sync(0xFFFFFFFFu,
-                      wait_or_flag(&bars->meta_full[pr], (j / kPairs) & 1, bars, a.err)))
+      if (!__all_sync(0xFFFFFFFFu, wait_or_flag(&bars->meta_full[j & 3], (j >> 2) & 1, bars, a.err)))
         break;
-      const int st0 = (2 * j) % kStages;
+      const int st0 = (2 * j) & 7;
       const uint32_t vm[4] = {bars->valid[st0][0], bars->valid[st0][1], bars->valid[st0 + 1][0],
                               bars->valid[st0 + 1][1]};
       if (!__all_sync(0xFFFFFFFFu, wait_or_flag(&bars->s_full[sb], (j >> 1) & 1, bars, a.err)))
