@@ -43,6 +43,9 @@ constexpr int kUnrollBf16 = 4;    // 16-entry groups in flight per warp (bf16 ke
 constexpr int kUnrollFp8 = 8;     // (E4M3 keys: half the bytes per row)
 constexpr int kUnrollFp4 = 8;     // (FP4 keys)
 constexpr int kQueryChunk = 256;  // queries per launch (bounds the workspace)
+// from this many queries in a launch, one streaming CTA per query
+// (topk_stream_kernel) instead of a cluster per query
+constexpr int kStreamQueries = 128;
 constexpr int kSelThreads = 1024;  // select CTA size for few queries (512 for many)
 constexpr int kMaxCluster = 16;  // select CTAs per query
 static_assert(kMaxNcap <= kMaxCluster * kSelThreads * 32, "select cluster");
@@ -535,6 +538,181 @@ __global__ void __launch_bounds__(NT, 1024 / NT) topk_select_kernel(IndexerArgs 
   }
 }
 
+// One CTA per query, no cluster, for calls with many queries (chunked
+// prefill): the query's scores stay in L2 and are streamed rather than held
+// in registers.  Pass 1: histogram of key bits 31..20 (4096 bins) and the bin
+// B* holding the k-th key.  Pass 2: the keys of B* (at most kCand; else two
+// more streamed passes) resolve bits 19..10 and 9..0 to the exact k-th key k*
+// and the count of entries equal to it to take.  Pass 3: tiles of NT*16
+// entries in index order, one block scan per tile, write the entries above
+// k* and the lowest-index ties.  Same selection as topk_select_kernel.
+constexpr int kCand = 2048;
+struct StreamShared {
+  uint32_t hist[kHistBins];
+  uint32_t cand[kCand];
+  int scratch[32];
+  int res[3];
+  int ncand;
+};
+
+template <int NT>
+__global__ void __launch_bounds__(NT, 2) topk_stream_kernel(IndexerArgs a, int q0, WsLayout L) {
+  constexpr int PER1 = kHistBins / NT;
+  constexpr int PER2 = 1024 / NT;
+  constexpr int kE = 16;  // entries per thread per output tile
+  __shared__ StreamShared sh;
+  pdl_trigger();
+  pdl_wait();
+  const int tid = threadIdx.x;
+  const int lq = blockIdx.x, qid = q0 + lq;
+  const int64_t nv = visible_entries(a, qid, nullptr, false);
+  int32_t* out = a.topk_idx + (int64_t)qid * a.k;
+  float* out_s = a.topk_score ? a.topk_score + (int64_t)qid * a.k : nullptr;
+  const float* scores = L.scores + (int64_t)lq * L.stride;
+  if (nv <= a.k) {  // every visible entry is selected
+    for (int i = tid; i < a.k; i += NT) {
+      out[i] = i < nv ? (int32_t)i : -1;
+      if (out_s) out_s[i] = i < nv ? scores[i] : -INFINITY;
+    }
+    return;
+  }
+  const int n = (int)nv;
+  const int n4 = n >> 2;
+  const float4* s4 = reinterpret_cast<const float4*>(scores);  // rows are 128-byte aligned
+  // stream every visible key through f(key) (4 vectors in flight per thread)
+  auto sweep = [&](auto&& f) {
+    int i = tid;
+    for (; i + 3 * NT < n4; i += 4 * NT) {
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) v[u] = s4[i + u * NT];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        f(score_key(v[u].x));
+        f(score_key(v[u].y));
+        f(score_key(v[u].z));
+        f(score_key(v[u].w));
+      }
+    }
+    for (; i < n4; i += NT) {
+      const float4 v = s4[i];
+      f(score_key(v.x));
+      f(score_key(v.y));
+      f(score_key(v.z));
+      f(score_key(v.w));
+    }
+    for (int e = 4 * n4 + tid; e < n; e += NT) f(score_key(scores[e]));
+  };
+
+  // ---- pass 1: bits 31..20
+  for (int i = tid; i < kHistBins; i += NT) sh.hist[i] = 0u;
+  if (tid == 0) sh.ncand = 0;
+  __syncthreads();
+  sweep([&](uint32_t key) { atomicAdd(&sh.hist[key >> 20], 1u); });
+  __syncthreads();
+  {
+    int bins[PER1];
+#pragma unroll
+    for (int i = 0; i < PER1; ++i) bins[i] = (int)sh.hist[kHistBins - 1 - PER1 * tid - i];
+    bin_from_top<NT, PER1>(bins, kHistBins - 1 - PER1 * tid, a.k, sh.scratch, sh.res);
+  }
+  const uint32_t bstar = (uint32_t)sh.res[0];
+  int need = a.k - sh.res[1];
+  const bool in_smem = sh.hist[bstar] <= (uint32_t)kCand;
+  __syncthreads();
+
+  // ---- pass 2: the keys of B*; levels 2 and 3 over them
+  if (in_smem)
+    sweep([&](uint32_t key) {
+      if ((key >> 20) == bstar) sh.cand[atomicAdd(&sh.ncand, 1)] = key;
+    });
+  for (int i = tid; i < 1024; i += NT) sh.hist[i] = 0u;
+  __syncthreads();
+  const int nc = sh.ncand;
+  if (in_smem) {
+    for (int c = tid; c < nc; c += NT) atomicAdd(&sh.hist[(sh.cand[c] >> 10) & 1023], 1u);
+  } else {
+    sweep([&](uint32_t key) {
+      if ((key >> 20) == bstar) atomicAdd(&sh.hist[(key >> 10) & 1023], 1u);
+    });
+  }
+  __syncthreads();
+  {
+    int bins[PER2];
+#pragma unroll
+    for (int i = 0; i < PER2; ++i) bins[i] = (int)sh.hist[1023 - PER2 * tid - i];
+    bin_from_top<NT, PER2>(bins, 1023 - PER2 * tid, need, sh.scratch, sh.res);
+  }
+  const uint32_t p2 = (bstar << 10) | (uint32_t)sh.res[0];
+  need -= sh.res[1];
+  for (int i = tid; i < 1024; i += NT) sh.hist[i] = 0u;
+  __syncthreads();
+  if (in_smem) {
+    for (int c = tid; c < nc; c += NT)
+      if ((sh.cand[c] >> 10) == p2) atomicAdd(&sh.hist[sh.cand[c] & 1023], 1u);
+  } else {
+    sweep([&](uint32_t key) {
+      if ((key >> 10) == p2) atomicAdd(&sh.hist[key & 1023], 1u);
+    });
+  }
+  __syncthreads();
+  {
+    int bins[PER2];
+#pragma unroll
+    for (int i = 0; i < PER2; ++i) bins[i] = (int)sh.hist[1023 - PER2 * tid - i];
+    bin_from_top<NT, PER2>(bins, 1023 - PER2 * tid, need, sh.scratch, sh.res);
+  }
+  const uint32_t kstar = (p2 << 10) | (uint32_t)sh.res[0];
+  const int need_eq = need - sh.res[1];  // entries equal to k* to take, lowest index first
+
+  // ---- pass 3: the selection in index order
+  int run_above = 0, run_eq = 0;
+  for (int base = 0; base < n; base += NT * kE) {
+    const int i0 = base + tid * kE;
+    uint32_t above = 0u, eq = 0u;
+#pragma unroll
+    for (int q = 0; q < kE / 4; ++q) {
+      const int e = i0 + 4 * q;
+      float f[4];
+      if (e + 3 < n) {
+        const float4 v = s4[e >> 2];
+        f[0] = v.x, f[1] = v.y, f[2] = v.z, f[3] = v.w;
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) f[c] = e + c < n ? scores[e + c] : 0.f;
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint32_t key = e + c < n ? score_key(f[c]) : 0u;
+        above |= (uint32_t)(key > kstar) << (4 * q + c);
+        eq |= (uint32_t)(key == kstar) << (4 * q + c);
+      }
+    }
+    int tot;
+    const int before =
+        block_excl_scan<NT>(__popc(above) | (__popc(eq) << 16), sh.scratch, &tot);
+    const int a_before = before & 0xFFFF, e_before = before >> 16;
+    int e_rank = run_eq + e_before;
+    int pos = run_above + a_before + min(e_rank, need_eq);
+    for (uint32_t m = above | eq; m; m &= m - 1) {
+      const int b = __ffs(m) - 1;
+      bool take = (above >> b) & 1u;
+      if (!take) take = e_rank++ < need_eq;
+      if (take) {
+        if (pos < a.k) {
+          out[pos] = i0 + b;
+          if (out_s) out_s[pos] = scores[i0 + b];
+        }
+        ++pos;
+      }
+    }
+    run_above += tot & 0xFFFF;
+    run_eq += tot >> 16;
+  }
+  if (tid == 0 && run_above + min(run_eq, need_eq) != a.k)
+    flag_error(a.err, CSA_EW_BAD_INDEX);  // internal invariant
+}
+
 }  // namespace
 
 size_t indexer_topk_workspace_bytes(int n_query, int N_cap) {
@@ -620,6 +798,11 @@ cudaError_t launch_indexer_topk(const IndexerArgs& a, void* ws, cudaStream_t st)
     const int qc = (a.n_query - q0 < kQueryChunk) ? a.n_query - q0 : kQueryChunk;
     cudaError_t e = launch_scores(a, q0, qc, L, st);
     if (e != cudaSuccess) return e;
+    if (qc >= kStreamQueries) {  // one CTA per query, streamed from L2
+      e = launch_pdl(topk_stream_kernel<512>, dim3((unsigned)qc), dim3(512), 0, st, a, q0, L);
+      if (e != cudaSuccess) return e;
+      continue;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.cs, (unsigned)qc);
     cfg.blockDim = dim3((unsigned)p.nt);

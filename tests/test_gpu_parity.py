@@ -329,6 +329,29 @@ def test_topk_dense_threshold_bin_slow_path(cuda_device):
     np.testing.assert_array_equal(idx, ref)  # exact: ties resolved by index
 
 
+@pytest.mark.parametrize("n_levels", [16, 128])
+def test_topk_dense_threshold_bin_many_queries(cuda_device, n_levels):
+    # 160 queries in one call (the one-CTA-per-query select), scores drawn
+    # from n_levels bf16 values 1 + j/128: with 16 every entry falls in one
+    # level-1 bin (12000 keys: levels 2 and 3 streamed from the scores
+    # again); with 128 eight bins of about 1500 tied keys each (levels 2 and 3
+    # on the candidate list in shared memory)
+    T, N_cap, m, k = 160, 12000, 4, 777
+    qi = torch.zeros((1, T, 4, 64), dtype=torch.bfloat16)
+    qi[:, :, 0, 0] = 1.0
+    g = torch.Generator().manual_seed(10)
+    ki = synth.randn((1, N_cap, 64), 4, 3)
+    ki[:, :, 0] = (1.0 + torch.randint(0, n_levels, (1, N_cap), generator=g) / 128.0
+                   ).to(torch.bfloat16)
+    w = torch.tensor([1.0, 0.0, 0.0, 0.0]).repeat(1, T, 1)
+    qp = torch.tensor([[N_cap * m - 1 - 61 * (T - 1 - t) for t in range(T)]], dtype=torch.int32)
+    nc = torch.tensor([N_cap], dtype=torch.int32)
+    case = (qi, None, ki, None, w, qp, nc)
+    idx, _ = _run_indexer(*case, m, k)
+    s, nv, ref = _oracle_indexer(*case, m, k, False)
+    np.testing.assert_array_equal(idx, ref)  # exact: ties resolved by index
+
+
 def test_topk_zero_scores_and_short_lists(cuda_device):
     # n_vis below k (every visible entry, -1 padded), n_vis == 0, and a query
     # whose scores are mostly exactly zero (negative dot products)
