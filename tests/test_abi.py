@@ -195,3 +195,45 @@ def test_static_indexer_refuses_beyond_its_scratch():
     st = L.csa_indexer_topk_static(FAKE, None, FAKE, FAKE, (1 << 19) * 64, None, 0, 0, FAKE, FAKE,
                                    256, 1, 4, 64, 1 << 19, 4, 64, FAKE, None, None, None)
     assert st == 3
+
+
+def test_compress_mixed_rejects():
+    L = csa.lib()
+
+    def call(**over):
+        a = dict(raw=FAKE, rbs=64 * 128, rcap=64, B=2, d=128, m=4, span=4, b0=0, nb=16, W=FAKE,
+                 pb=FAKE, codes=FAKE, cbs=16 * 64, sc=FAKE, sbs=16, rope=FAKE, ropebs=16 * 64,
+                 n_rope=64, err=None, st=None)
+        a.update(over)
+        return L.csa_compress_kv_mixed(*a.values())
+
+    assert call(n_rope=0) == 1 and call(n_rope=128) == 1
+    assert call(n_rope=60) == 1       # RoPE channels in whole 16-byte bf16 chunks
+    assert call(n_rope=56) == 1       # E4M3 part in whole 16-byte chunks
+    assert call(d=96) == 2
+    assert call(cbs=15 * 64) == 1     # codes rows beyond the sequence stride
+    assert call(ropebs=15 * 64) == 1
+    assert call(sbs=15) == 1
+    assert call(sc=None) == 1 and call(rope=None) == 1
+    assert call(B=0, raw=None) == 0
+
+
+def test_attn_fp8kv_rejects():
+    L = csa.lib()
+
+    def call(**over):
+        a = dict(q=FAKE, kn=FAKE, ks=FAKE, kr=FAKE, v=FAKE, vs=FAKE, N=1024, idx=FAKE, k=512,
+                 nc=None, mp=1, kraw=FAKE, vraw=FAKE, rbs=4096 * 128, rcap=4096, pos=FAKE, W=128,
+                 sink=None, scale=1.0, B=2, T=1, H=64, D=128, out=FAKE, lse=None, ws=None,
+                 wsb=0, err=None, st=None)
+        a.update(over)
+        return L.csa_attn_fp8kv(*a.values())
+
+    assert call(H=128) == 2                # FP8 entries: at most 64 heads
+    assert call(D=64) == 2
+    assert call(pos=None) == 1
+    assert call(ks=None) == 1 and call(vs=None) == 1 and call(kr=None) == 1
+    assert call(idx=None) == 1             # HCA needs n_cmp
+    assert call(idx=None, nc=FAKE, mp=0) == 1
+    assert call(k=0) == 1
+    assert call(B=0, q=None) == 0

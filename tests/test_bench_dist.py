@@ -110,3 +110,21 @@ def test_reference_arm_under_torchrun_prints_once_from_rank_0():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_fp8kv_algorithmic_bytes():
+    sys.path.insert(0, ROOT)
+    import bench
+    import synth
+    # FP8-stored entries: K 64 E4M3 codes + fp32 scale + 64 bf16 RoPE channels,
+    # V 128 E4M3 codes + fp32 scale (328 B a pair instead of 512); window rows
+    # stay bf16
+    wl8, wl = synth.WORKLOADS["hca_decode_1m_fp8kv"], synth.WORKLOADS["hca_decode_1m"]
+    assert bench.cmp_row_bytes(wl8) == 328 and bench.cmp_row_bytes(wl) == 512
+    n = 8192 * 16
+    d = bench.algorithmic(wl)["attention"]["bytes"] - bench.algorithmic(wl8)["attention"]["bytes"]
+    assert d == n * (512 - 328)
+    c8 = bench.algorithmic(synth.WORKLOADS["csa_decode_128k_fp8kv"])
+    c = bench.algorithmic(synth.WORKLOADS["csa_decode_128k"])
+    assert c["attention"]["bytes"] - c8["attention"]["bytes"] == 32 * 1024 * (512 - 328)
+    assert c["indexer_topk"] == c8["indexer_topk"]
