@@ -33,6 +33,10 @@
 //                running max grows by more than 2^8); P (bf16) to shared
 //                memory.  The exponentials of tile t are computed while the
 //                P V of tile t-1 still runs.
+// FP8-stored entries (KV8 = true, csa_attn_fp8kv): the loaders copy each
+// stage's E4M3 codes, scales and bf16 RoPE channels to a staging slot and,
+// two stages later, decode them into the ring's bf16 rows (code * scale,
+// nearest even); the rest of the kernel is the same.
 // Separate S and P V issuers keep the tensor pipe fed while either one waits
 // on a barrier.  Every mbarrier wait is bounded; on timeout the CTA records
 // CSA_EW_TIMEOUT in the error word, still reaches every barrier, and frees its
