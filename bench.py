@@ -123,12 +123,14 @@ def algorithmic(wl) -> dict:
 def kernel_algorithmic(wl, name: str) -> dict:
     """Algorithmic bytes or FLOPs of one launch of the kernel that
     ``kernel_probe`` runs alone: the indexer's scoring reads each visible key
-    row once plus the query and weights and writes one fp32 score per visible
-    entry; the attention kernels are their whole stage."""
+    row once plus the query rows and head weights (the method's bytes); the
+    fp32 score it writes per visible entry is workspace traffic, not the
+    method's, and is reported beside them ("overhead_bytes"), not counted in
+    the roofline.  The attention kernels are their whole stage."""
     if name == "indexer_score":
         row, qrow = idx_row_bytes(wl), idx_row_bytes(wl)
         nv = sum(n_vis_decode(wl))
-        return {"bytes": nv * (row + 4) + wl.B * wl.H_I * (qrow + 4)}
+        return {"bytes": nv * row + wl.B * wl.H_I * (qrow + 4), "overhead_bytes": nv * 4}
     return algorithmic(wl)[name]
 
 
@@ -337,8 +339,17 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.gpus < 1:
+        ap.error("--gpus must be >= 1")
 
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        # one process per GPU: start them under torchrun and pass its status on
+        sys.exit(relaunch_under_torchrun(args.gpus))
     world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world != args.gpus:
+        print(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world}; launch one rank per GPU "
+              f"(torchrun --nproc-per-node {args.gpus}) or drop --gpus", file=sys.stderr)
+        sys.exit(2)
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     wl = synth.WORKLOADS[args.workload]
@@ -426,7 +437,8 @@ def main():
                                       for i in range(args.steps))
                 for s, (name, _) in enumerate(graphs)}
     total_ms = max_over_ranks(sum(step_ms), world, dist, dev)
-    ms_per_step = total_ms / args.steps
+    ms_per_step = total_ms / args.steps  # mean over the K timed steps
+    median_ms = max_over_ranks(statistics.median(step_ms), world, dist, dev)
     value = job_value(units(wl), world, args.steps, total_ms)
 
     # e2e: public API, inputs from pinned host memory, result back to host
@@ -451,7 +463,8 @@ def main():
         kg.replay()
         kev[i][1].record(stream)
     torch.cuda.synchronize()
-    k_ms = statistics.mean(a.elapsed_time(b) for a, b in kev)
+    k_times = [a.elapsed_time(b) for a, b in kev]
+    k_ms = statistics.mean(k_times)
     kalg = kernel_algorithmic(wl, kname)
     if "bytes" in kalg:
         achieved = kalg["bytes"] / (k_ms / 1e3) / 1e9
@@ -463,7 +476,8 @@ def main():
         roof = {"bound": "tensor", "unit": "TFLOP/s"}
     roof.update({"achieved": round(achieved, 2), "peak": peak, "frac": round(achieved / peak, 4),
                  "traffic": traffic_record(wl.name, kname), "kernel": kname,
-                 "kernel_ms": round(k_ms, 5), "algorithmic": kalg,
+                 "kernel_ms": round(k_ms, 5),
+                 "kernel_ms_median": round(statistics.median(k_times), 5), "algorithmic": kalg,
                  "peak_source": peaks_src + " (burst)"})
 
     stage_report = {}
@@ -487,11 +501,15 @@ def main():
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": unit_name(wl), "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "ms_per_step_median": round(median_ms, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": ("e2m1-indexer+bf16" if wl.idx_fp4 else "e4m3-indexer+bf16" if wl.idx_fp8
                   else "bf16"), "data": "synthetic",
         "config": dict(cfg, l2="flushed before every step (2x L2 write + 2x L2 read, untimed)",
-                       timing="whole step as one CUDA graph, CUDA events; stages timed separately"),
+                       timing="whole step as one CUDA graph, CUDA events per step; "
+                              "ms_per_step and value use the mean of the K timed steps "
+                              "(their total / K), ms_per_step_median beside it; stages and "
+                              "the roofline kernel timed separately (means)"),
         "roofline": roof, "stages": stage_report, "cpu_baseline": cpu, "e2e": e2e,
         "clocks": clocks, "gpu_launches": launches,
     }
@@ -499,6 +517,19 @@ def main():
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def relaunch_under_torchrun(n: int) -> int:
+    """Run this same command as n ranks (one per GPU) under torchrun on this
+    node, rendezvous on 127.0.0.1; returns torchrun's exit status."""
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={n}", "--master-addr", "127.0.0.1", "--master-port", str(port),
+           os.path.abspath(__file__)] + sys.argv[1:]
+    return subprocess.call(cmd)
 
 
 def launches_per_step(wl, csa) -> int:

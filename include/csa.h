@@ -311,11 +311,16 @@ CSA_API int csa_grouped_out_proj(const void* o, const void* W, void* y, int n, i
  *   score per compressed entry for up to 256 queries at a time, so this covers
  *   any number of queries over 16384 entries, 32 queries over 131072, or 8 over
  *   524288; a larger problem returns CSA_ERR_WORKSPACE before anything runs.
+ *   Statuses: the argument checks of csa_indexer_topk come first and give
+ *   its statuses; the capacity check follows; both before any CUDA call.
  *   Set-up: the first call on a device (the device current on the calling
  *   thread) looks up the array's device address (cudaGetSymbolAddress) and
- *   caches it; that lookup can load the library's kernels, so make the first
- *   call per device before any stream capture.  A failed lookup returns
- *   CSA_ERR_CUDA.
+ *   caches it with the id of the current context; that lookup can load the
+ *   library's kernels, so make the first call per device before any stream
+ *   capture.  A device reset (cudaDeviceReset) creates a new context in which
+ *   the array may sit elsewhere: the next call sees the new context id and
+ *   looks the address up again (again outside any capture, then).  A failed
+ *   lookup returns CSA_ERR_CUDA.
  *   Zeroing: nothing in the array has to start at zero; each call writes
  *   every score it later reads, before reading it, on `stream`.
  *   Overlap: all calls on one device share the one array.  Calls ordered on
@@ -330,6 +335,31 @@ CSA_API int csa_indexer_topk_static(const void* q_idx, const float* q_scale, con
                                     const int32_t* n_cmp, int B, int T, int H_I, int d_I,
                                     int N_cap, int m, int k, int32_t* topk_idx,
                                     float* topk_score, int32_t* err_word, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Self-test of the bounded device waits.  Not part of the method (the pages
+ * have no counterpart): every pipelined kernel of this library waits on its
+ * mbarriers with an iteration limit and, when a wait gives up, sets
+ * CSA_EW_TIMEOUT in err_word and returns instead of hanging.  This call runs
+ * that same wait on a barrier in a one-thread kernel with nothing else in
+ * flight (no bulk copy, MMA or tensor memory), so a caller can check the
+ * give-up path on its GPU without faulting or hanging it.
+ *
+ *   arrive    0: nobody arrives at the barrier, the wait gives up after
+ *             `limit` polls and CSA_EW_TIMEOUT is ORed into *err_word;
+ *             nonzero: the one expected arrival comes first, the wait returns
+ *             at once and *err_word is left as it was.
+ *   limit     polls before giving up, 1 .. 2^20 (each poll blocks for a
+ *             bounded, hardware-defined time, so the kernel ends within
+ *             milliseconds).
+ *   err_word  device int32, 4-byte aligned, required; read it after the
+ *             stream has reached the call.
+ * Status: 0 launched, 1 bad argument (nothing launched), 4 launch failed.
+ * The kernel leaves the device usable: later calls of the library run
+ * normally.
+ * ---------------------------------------------------------------------- */
+CSA_API int csa_selftest_bounded_wait(int arrive, uint32_t limit, int32_t* err_word,
+                                      void* stream);
 
 /* ------------------------------------------------------------------------
  * a4 / a5 / a6. Attention over compressed entries + window + sink.

@@ -33,6 +33,7 @@ CSA_FP8_E4M3 = 1
 CSA_FP4_E2M1 = 2
 EW_BAD_INDEX = 1
 EW_BAD_POSITION = 2
+EW_TIMEOUT = 4
 
 # exported symbols of the C ABI (include/csa.h)
 ABI_SYMBOLS = (
@@ -41,6 +42,7 @@ ABI_SYMBOLS = (
     "csa_sparse_attn_prefill", "hca_dense_attn_decode", "csa_indexer_topk_static",
     "csa_indexer_scores", "csa_compress_kv_span", "csa_sparse_attn_batch_invariant",
     "csa_grouped_out_proj", "csa_compress_kv_mixed", "csa_attn_fp8kv",
+    "csa_selftest_bounded_wait",
 )
 
 # capacity of the library-owned scratch behind indexer_topk_static (bytes)
@@ -110,6 +112,8 @@ def lib() -> ctypes.CDLL:
             L.csa_attn_fp8kv.argtypes = [P, P, P, P, P, P, I, P, I, P, I, P, P, I64, I64, P, I,
                                          P, F, I, I, I, I, P, P, P, SZ, P, P]
             L.csa_attn_fp8kv.restype = I
+            L.csa_selftest_bounded_wait.argtypes = [I, ctypes.c_uint32, P, P]
+            L.csa_selftest_bounded_wait.restype = I
             _lib = L
     return _lib
 
@@ -326,16 +330,21 @@ def indexer_topk(q_idx, w, k_idx, q_pos, n_cmp, m: int, k: int, q_scale=None, k_
 
 
 def indexer_topk_static(q_idx, w, k_idx, q_pos, n_cmp, m: int, k: int, q_scale=None,
-                        k_scale=None, return_scores: bool = False, out=None, err_word=None):
+                        k_scale=None, return_scores: bool = False, out=None, err_word=None,
+                        scores_out=None):
     """indexer_topk with the library's fixed scratch instead of a caller
     workspace: the C call allocates no device memory (the output tensors here
-    are still allocated by torch unless `out` is given).  Problems whose
-    workspace would exceed INDEXER_STATIC_SCRATCH_BYTES are refused.  Calls
-    that may run at the same time share the scratch and race."""
+    are still allocated by torch unless `out` and, with return_scores,
+    `scores_out` are given).  Problems whose workspace would exceed
+    INDEXER_STATIC_SCRATCH_BYTES are refused.  Calls that may run at the same
+    time share the scratch and race."""
     args, (B, T, N_cap) = _indexer_common(q_idx, w, k_idx, q_pos, n_cmp, m, q_scale, k_scale)
     dev = q_idx.device
     idx = out if out is not None else torch.empty((B, T, k), dtype=torch.int32, device=dev)
-    scores = torch.empty((B, T, k), dtype=torch.float32, device=dev) if return_scores else None
+    scores = None
+    if return_scores:
+        scores = scores_out if scores_out is not None else torch.empty(
+            (B, T, k), dtype=torch.float32, device=dev)
     st = lib().csa_indexer_topk_static(*args, k, _p(idx), _p(scores), _p(err_word), _stream(dev))
     _check(st, "csa_indexer_topk_static")
     return (idx, scores) if return_scores else idx
@@ -518,6 +527,17 @@ def attn_fp8kv(q, k_nope, k_scale, k_rope, v, v_scale, topk_idx, k_raw, v_raw, q
 
 
 # ---------------------------------------------------------------- output projection
+
+def selftest_bounded_wait(err_word, arrive: bool = False, limit: int = 1000):
+    """Run the library's bounded mbarrier wait on a barrier in a one-thread
+    kernel: without `arrive` nobody completes it, so the wait gives up after
+    `limit` polls and ORs CSA_EW_TIMEOUT into err_word (an int32 CUDA
+    tensor); with `arrive` the wait succeeds and err_word is untouched."""
+    _cuda(err_word, "err_word", torch.int32)
+    st = lib().csa_selftest_bounded_wait(int(bool(arrive)), int(limit), _p(err_word),
+                                         _stream(err_word.device))
+    _check(st, "csa_selftest_bounded_wait")
+
 
 def grouped_out_proj(o, W, out=None, err_word=None):
     """Grouped output projection: o bf16 [n, H, D] (the attention output), W

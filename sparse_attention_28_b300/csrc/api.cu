@@ -257,6 +257,32 @@ IndexerArgs indexer_args(const void* q_idx, const float* q_scale, const float* w
 
 }  // namespace
 
+}  // extern "C"
+
+namespace csa {
+
+// Every argument check of csa_indexer_topk except the workspace: a status to
+// return, or -1 when the call may go on (shared with the static-scratch
+// entry point, so that both give the same status for the same arguments).
+int indexer_topk_arg_status(const void* q_idx, const float* q_scale, const float* w,
+                            const void* k_idx, int64_t k_bstride, const float* k_scale,
+                            int64_t ks_bstride, int idx_dtype, const int32_t* q_pos,
+                            const int32_t* n_cmp, int B, int T, int H_I, int d_I, int N_cap,
+                            int m, int k, const int32_t* topk_idx, const float* topk_score) {
+  if (k <= 0) return CSA_ERR_INVALID_ARG;
+  const int c = indexer_checks(q_idx, q_scale, w, k_idx, k_bstride, k_scale, ks_bstride, idx_dtype,
+                               q_pos, n_cmp, B, T, H_I, d_I, N_cap, m);
+  if (c >= 0) return c;
+  if (k > N_cap) return CSA_ERR_INVALID_ARG;
+  if (!topk_idx || !aligned4(topk_idx)) return CSA_ERR_INVALID_ARG;
+  if (topk_score && !aligned4(topk_score)) return CSA_ERR_INVALID_ARG;
+  return -1;
+}
+
+}  // namespace csa
+
+extern "C" {
+
 int csa_indexer_scores(const void* q_idx, const float* q_scale, const float* w, const void* k_idx,
                        int64_t k_bstride, const float* k_scale, int64_t ks_bstride, int idx_dtype,
                        const int32_t* q_pos, const int32_t* n_cmp, int B, int T, int H_I, int d_I,
@@ -277,13 +303,10 @@ int csa_indexer_topk(const void* q_idx, const float* q_scale, const float* w, co
                      const int32_t* q_pos, const int32_t* n_cmp, int B, int T, int H_I, int d_I,
                      int N_cap, int m, int k, int32_t* topk_idx, float* topk_score, void* ws,
                      size_t ws_bytes, int32_t* err_word, void* stream) {
-  if (k <= 0) return CSA_ERR_INVALID_ARG;
-  const int c = indexer_checks(q_idx, q_scale, w, k_idx, k_bstride, k_scale, ks_bstride, idx_dtype,
-                               q_pos, n_cmp, B, T, H_I, d_I, N_cap, m);
+  const int c = indexer_topk_arg_status(q_idx, q_scale, w, k_idx, k_bstride, k_scale, ks_bstride,
+                                        idx_dtype, q_pos, n_cmp, B, T, H_I, d_I, N_cap, m, k,
+                                        topk_idx, topk_score);
   if (c >= 0) return c;
-  if (k > N_cap) return CSA_ERR_INVALID_ARG;
-  if (!topk_idx || !aligned4(topk_idx)) return CSA_ERR_INVALID_ARG;
-  if (topk_score && !aligned4(topk_score)) return CSA_ERR_INVALID_ARG;
   const size_t need = indexer_topk_workspace_bytes(B * T, N_cap);
   if (!ws || ws_bytes < need || !aligned16(ws)) return CSA_ERR_WORKSPACE;
   IndexerArgs a = indexer_args(q_idx, q_scale, w, k_idx, k_bstride, k_scale, ks_bstride, idx_dtype,

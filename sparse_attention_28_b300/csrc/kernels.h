@@ -106,6 +106,13 @@ struct IndexerArgs {
 };
 
 size_t indexer_topk_workspace_bytes(int n_query, int N_cap);
+// Host checks of csa_indexer_topk's arguments other than the workspace: a
+// CSA_* status to return, or -1 when the call may go on.
+int indexer_topk_arg_status(const void* q_idx, const float* q_scale, const float* w,
+                            const void* k_idx, int64_t k_bstride, const float* k_scale,
+                            int64_t ks_bstride, int idx_dtype, const int32_t* q_pos,
+                            const int32_t* n_cmp, int B, int T, int H_I, int d_I, int N_cap,
+                            int m, int k, const int32_t* topk_idx, const float* topk_score);
 cudaError_t launch_indexer_topk(const IndexerArgs& a, void* ws, cudaStream_t st);
 // the scores alone: query q's row at scores + q * ld (entries < n_vis)
 cudaError_t launch_indexer_scores(const IndexerArgs& a, float* scores, int ld, cudaStream_t st);

@@ -26,6 +26,76 @@ def bf16_bound(y):
     return ulp + COMPRESS_ABS
 
 
+# Quantised entries.  The GPU forms a compressed value y in fp32, the oracle
+# in fp64; their difference stays below about 1e-6 of the entry's (or
+# block's) largest magnitude, the agreement the fp32 scale amax/448 shows
+# against the oracle's at rtol 1e-6.  A rounding decision may therefore
+# differ only where the exact value lies that close to a rounding midpoint of
+# the format; everywhere else the GPU's code must be the oracle's.
+QUANT_REL = 1e-6
+
+
+def _format_midpoints(decode, n_codes):
+    v = decode(np.arange(n_codes, dtype=np.uint8))
+    v = np.unique(np.abs(v[np.isfinite(v)]))
+    return (v[1:] + v[:-1]) / 2
+
+
+def _near(x, mids, window):
+    """|x| within `window` (broadcast against x) of one of `mids`."""
+    a = np.abs(np.asarray(x, np.float64))
+    d = np.abs(a[..., None] - mids).min(axis=-1)
+    return d <= window
+
+
+def check_e4m3_rows(codes_gpu, scale_gpu, y, what=""):
+    """FP8 storage of compressed entries (one fp32 scale per row, E4M3 codes):
+    the scale equals the oracle's amax/448 within rtol 1e-6, and every code is
+    the nearest E4M3 value of y / scale (the GPU's stored scale), except where
+    that quotient lies within 1e-6 of the row's range (448) of an E4M3
+    rounding midpoint."""
+    import oracle
+    y = np.asarray(y, np.float64)
+    _, sc_ref = oracle.quantize_e4m3_rows(y)
+    gs = np.asarray(scale_gpu, np.float64)
+    np.testing.assert_allclose(gs, sc_ref, rtol=QUANT_REL, err_msg=f"{what}: scales")
+    r = y / gs[..., None]
+    want = oracle.e4m3_encode(r)
+    mids = _format_midpoints(oracle.e4m3_decode, 256)
+    tie = _near(r, mids, QUANT_REL * 448.0)
+    bad = (np.asarray(codes_gpu) != want) & ~tie
+    assert not bad.any(), f"{what}: {int(bad.sum())} E4M3 codes differ away from a midpoint"
+
+
+def check_fp4_rows(codes_gpu, scales_gpu, y, what=""):
+    """FP4 storage (E2M1 codes two per byte, one E4M3 scale per 16 channels):
+    every scale byte equals the oracle's (nearest E4M3 of amax/6) unless
+    amax/6 lies within 1e-6 relative of an E4M3 midpoint; every code is the
+    nearest E2M1 value of y / scale on the GPU's scale (the oracle's, except at
+    such a scale tie) unless the quotient lies within 1e-6 of the block's
+    range (6) of an E2M1 midpoint.  Signs of zero count: -0 is its own code."""
+    import oracle
+    y = np.asarray(y, np.float64)
+    codes_gpu = np.asarray(codes_gpu, np.uint8)
+    scales_gpu = np.asarray(scales_gpu, np.uint8)
+    d = y.shape[-1]
+    _, ref_scales = oracle.quantize_fp4_rows(y)
+    blk = y.reshape(y.shape[:-1] + (d // 16, 16))
+    x = np.abs(blk).max(axis=-1) / 6.0
+    scale_tie = _near(x, _format_midpoints(oracle.e4m3_decode, 256), QUANT_REL * x)
+    bad_s = (scales_gpu != ref_scales) & ~scale_tie
+    assert not bad_s.any(), f"{what}: {int(bad_s.sum())} E4M3 block scales differ"
+    s = np.repeat(oracle.e4m3_decode(scales_gpu), 16, axis=-1)
+    r = y / s
+    want = oracle.e2m1_encode(r)
+    got = np.empty(y.shape, np.uint8)
+    got[..., 0::2] = codes_gpu & 0x0F
+    got[..., 1::2] = codes_gpu >> 4
+    tie = _near(r, _format_midpoints(oracle.e2m1_decode, 16), QUANT_REL * 6.0)
+    bad = (got != want) & ~tie
+    assert not bad.any(), f"{what}: {int(bad.sum())} E2M1 codes differ away from a midpoint"
+
+
 def u16(t: torch.Tensor) -> np.ndarray:
     """bf16 tensor -> numpy uint16 bit patterns (CPU copy)."""
     return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)

@@ -197,6 +197,48 @@ def test_static_indexer_refuses_beyond_its_scratch():
     assert st == 3
 
 
+def _static(**over):
+    a = dict(q=FAKE, qs=None, w=FAKE, kk=FAKE, kbs=16416 * 64, ks=None, ksbs=0, dt=0, pos=FAKE,
+             ncmp=FAKE, B=256, T=1, HI=4, dI=64, N=16385, m=4, k=64, idx=FAKE, sc=None, err=None,
+             st=None)
+    a.update(over)
+    return csa.lib().csa_indexer_topk_static(*a.values())
+
+
+def test_static_indexer_capacity_boundary():
+    # any number of queries over 16384 entries fits exactly (the scores are
+    # taken 256 queries at a time); one entry more (rows rounded up to 32
+    # entries) no longer does
+    L = csa.lib()
+    cap = csa.INDEXER_STATIC_SCRATCH_BYTES
+    assert L.csa_indexer_topk_workspace(256, 1, 16384, 64) == cap
+    assert L.csa_indexer_topk_workspace(8, 1, 1 << 19, 64) == cap
+    assert L.csa_indexer_topk_workspace(256, 1, 16385, 64) > cap
+    assert L.csa_indexer_topk_workspace(9, 1, 1 << 19, 64) > cap
+    assert _static() == 3
+    assert _static(B=9, N=1 << 19, kbs=(1 << 19) * 64) == 3
+
+
+def test_static_indexer_gives_the_workspace_entrys_statuses():
+    # a call that is both oversized and invalid reports what csa_indexer_topk
+    # reports for the invalid argument, not the capacity
+    assert _static(k=0) == 1
+    assert _static(q=None) == 1
+    assert _static(idx=None) == 1
+    assert _static(HI=8) == 2
+    assert _static(dt=7) == 2
+    assert _static(N=(1 << 19) + 1, kbs=((1 << 19) + 32) * 64) == 2
+    assert _static(B=0) == 0  # nothing to do, no CUDA call
+
+
+def test_selftest_bounded_wait_rejects():
+    L = csa.lib()
+    assert L.csa_selftest_bounded_wait(0, 100, None, None) == 1
+    assert L.csa_selftest_bounded_wait(0, 100, ctypes.c_void_p(0x10002), None) == 1
+    assert L.csa_selftest_bounded_wait(0, 0, FAKE, None) == 1
+    assert L.csa_selftest_bounded_wait(0, (1 << 20) + 1, FAKE, None) == 1
+
+
 def test_compress_mixed_rejects():
     L = csa.lib()
 

@@ -66,16 +66,17 @@ def test_kernel_algorithmic_bytes():
     import bench
     import synth
     wl = synth.WORKLOADS["csa_decode_128k"]
+    # the fp32 score written per entry is workspace overhead, reported apart
     assert bench.kernel_algorithmic(wl, "indexer_score") == {
-        "bytes": 32 * 32768 * (128 + 4) + 32 * 4 * (128 + 4)}
+        "bytes": 32 * 32768 * 128 + 32 * 4 * (128 + 4), "overhead_bytes": 32 * 32768 * 4}
     # E4M3 keys: 64 code bytes + a 4-byte scale per row
     wl8 = synth.WORKLOADS["csa_decode_1m_fp8"]
     assert bench.kernel_algorithmic(wl8, "indexer_score") == {
-        "bytes": 8 * 262144 * (68 + 4) + 8 * 4 * (68 + 4)}
+        "bytes": 8 * 262144 * 68 + 8 * 4 * (68 + 4), "overhead_bytes": 8 * 262144 * 4}
     # FP4 keys: 32 code bytes + 4 E4M3 block scales per row
     wl4 = synth.WORKLOADS["csa_decode_1m_fp4"]
     assert bench.kernel_algorithmic(wl4, "indexer_score") == {
-        "bytes": 8 * 262144 * (36 + 4) + 8 * 4 * (36 + 4)}
+        "bytes": 8 * 262144 * 36 + 8 * 4 * (36 + 4), "overhead_bytes": 8 * 262144 * 4}
     hca = synth.WORKLOADS["hca_decode_1m"]
     assert bench.kernel_algorithmic(hca, "attention") == bench.algorithmic(hca)["attention"]
 
@@ -110,6 +111,30 @@ def test_reference_arm_under_torchrun_prints_once_from_rank_0():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_gpus_flag_without_torchrun_starts_the_ranks():
+    # --gpus 2 run as a plain process: bench.py starts two ranks itself and
+    # the one line it prints says n_gpus 2
+    cmd = [sys.executable, "bench.py", "--impl", "reference", "--gpus", "2", "--steps", "1",
+           "--warmup", "3", "--workload", "csa_decode_tiny"]
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600,
+                       env={k: v for k, v in dict(os.environ, OMP_NUM_THREADS="2").items()
+                            if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")})
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    assert json.loads(lines[0])["n_gpus"] == 2
+
+
+def test_gpus_flag_that_contradicts_the_launch_fails():
+    cmd = [sys.executable, "bench.py", "--impl", "reference", "--gpus", "4", "--steps", "1",
+           "--warmup", "3", "--workload", "csa_decode_tiny"]
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=300,
+                       env=dict(os.environ, WORLD_SIZE="2", RANK="0", LOCAL_RANK="0"))
+    assert r.returncode != 0
+    assert "WORLD_SIZE=2" in r.stderr
+    assert not [l for l in r.stdout.splitlines() if l.startswith("{")]
 
 
 def test_fp8kv_algorithmic_bytes():

@@ -11,17 +11,11 @@ import torch
 import oracle
 import sparse_attention_28_b300 as csa
 import synth
-from _util import (bf16_bound, check_attention, f64, lse_tol, place_window, u8, u16,
-                   window_arrays)
+from _util import (bf16_bound, check_attention, check_e4m3_rows, f64, lse_tol, place_window, u8,
+                   u16, window_arrays)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
-
-
-def e4m3_half_step(v):
-    a = np.abs(v)
-    e = np.floor(np.log2(np.maximum(a, 2.0 ** -6)))
-    return 2.0 ** (e - 4)
 
 
 # ---------------------------------------------------------------- compression
@@ -42,13 +36,8 @@ def test_compress_mixed_parity(cuda_device, d, n_rope, m, span):
     csa.compress_kv_mixed(raw.to(DEV), W.to(DEV), pb.to(DEV), m, bb, nb, codes, sc, rope)
     torch.cuda.synchronize()
     y = oracle.compress(u16(raw), u16(W), pb.numpy(), m, bb, nb)
-    codes_ref, sc_ref = oracle.quantize_e4m3_rows(y[..., :dn])
-    gs = sc[:, bb:bb + nb].cpu().numpy().astype(np.float64)
-    np.testing.assert_allclose(gs, sc_ref, rtol=1e-6)
-    dec = oracle.e4m3_decode(u8(codes[:, bb:bb + nb]))
-    exact_v = y[..., :dn] / gs[..., None]
-    assert np.all(np.abs(dec - exact_v) <= e4m3_half_step(exact_v) * (1 + 1e-5) + 1e-12)
-    assert np.mean(u8(codes[:, bb:bb + nb]) == codes_ref) > 0.99
+    check_e4m3_rows(u8(codes[:, bb:bb + nb]), sc[:, bb:bb + nb].cpu().numpy(), y[..., :dn],
+                    "mixed compression")
     g = f64(rope[:, bb:bb + nb])
     assert np.all(np.abs(g - y[..., dn:]) <= bf16_bound(y[..., dn:])), "RoPE channels"
     # nothing outside the written blocks

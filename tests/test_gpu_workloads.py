@@ -8,7 +8,8 @@ import torch
 import oracle
 import sparse_attention_28_b300 as csa
 import synth
-from _util import bf16_bound, check_attention, check_topk, f64, lse_tol, u8, u16
+from _util import (bf16_bound, check_attention, check_e4m3_rows, check_fp4_rows, check_topk, f64,
+                   lse_tol, u8, u16)
 from oracle.feed import fill_new_entries, idx_dtype, oracle_inputs
 from sparse_attention_28_b300.steps import make_step
 
@@ -40,14 +41,11 @@ def _check_decode(name, seqs):
         _check_bf16_entries(step.k_cmp[ix, j], y["k"][:, 0], "compressed K")
         _check_bf16_entries(step.v_cmp[ix, j], y["v"][:, 0], "compressed V")
         if wl.idx_fp4:
-            codes, scales = oracle.quantize_fp4_rows(y["idx"])
-            assert np.mean(u8(step.k_scale[ix, j]) == scales[:, 0]) > 0.9
-            assert np.mean(u8(step.k_idx[ix, j]) == codes[:, 0]) > 0.9
+            check_fp4_rows(u8(step.k_idx[ix, j]), u8(step.k_scale[ix, j]), y["idx"][:, 0],
+                           "streamed FP4 index key")
         else:
-            codes, scales = oracle.quantize_e4m3_rows(y["idx"])
-            np.testing.assert_allclose(step.k_scale[ix, j].cpu().numpy(), scales[:, 0],
-                                       rtol=1e-6)
-            assert np.mean(u8(step.k_idx[ix, j]) == codes[:, 0]) > 0.95
+            check_e4m3_rows(u8(step.k_idx[ix, j]), step.k_scale[ix, j].cpu().numpy(),
+                            y["idx"][:, 0], "streamed FP8 index key")
     if wl.kind == "hca_decode":
         ro, rl = oracle.hca_decode(a["q"], a["k_cmp"], a["v_cmp"], a["n_cmp"], wl.m, a["k_win"],
                                    a["v_win"], a["seq_len"], wl.W, a["sink"], 1.0, a["raw_base"])
