@@ -109,10 +109,11 @@ struct Cfg {
   static constexpr int kPartLseOff = kQOff;         // [H]
   static constexpr int kRecvLseOff = kQOff + 1024;  // [ns][hp]
   static constexpr int kWgtOff = kQOff + 2048;      // [hp][ns]
+  static constexpr int kSinkOff = kQOff + 3072;     // [H]
   static_assert(kSmemBytes <= 232448, "shared memory");
   static_assert(2 * kRegion >= M * 512, "partial O fits over the K regions");
   static_assert(2 * kRegion + kPBytes >= (M + kMaxCluster) * 512, "received rows fit");
-  static_assert(kQBytes >= 3072, "merge scratch fits over Q");
+  static_assert(kQBytes >= 3072 + 4 * 128, "merge scratch and sink logits fit over Q");
 };
 
 struct Bars {
@@ -236,8 +237,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kStages = C::kStages;
   constexpr int kPairs = C::kPairs;
   constexpr int NL = kLoadThreads;
+  // Everything up to griddepcontrol.wait below reads only what no kernel of
+  // this library writes (the queries, positions, entry counts, sink logits)
+  // and sets up shared and tensor memory, so it overlaps the end of the
+  // previous kernel (the top-k select) under programmatic dependent launch.
   pdl_trigger();
-  pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* sm = smem_raw + ((1024 - (raw_addr & 1023)) & 1023);
@@ -254,14 +258,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- the query's key set and this split's range
   const int64_t t = a.pos_is_len ? (int64_t)__ldg(a.pos + b) - 1 : (int64_t)__ldg(a.pos + qid);
-  if (tid == 0 && split == 0 && t < 0) flag_error(a.err, CSA_EW_BAD_POSITION);
+  bool bad_pos = t < 0;  // flagged after the wait (the error word may be the previous kernel's)
   int n_c;
   if (!a.dense) {
     n_c = a.sel_count;
   } else {
     int64_t present = a.n_cmp ? (int64_t)__ldg(a.n_cmp + b) : 0;
     if (present < 0 || present > a.N_cap) {
-      if (tid == 0 && split == 0) flag_error(a.err, CSA_EW_BAD_POSITION);
+      bad_pos = true;
       present = present < 0 ? 0 : a.N_cap;
     }
     const int64_t nv = t >= 0 ? (t + 1) / a.m_prime : 0;
@@ -311,11 +315,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     *reinterpret_cast<uint4*>(sm + C::kQOff + (c16 >> 3) * (M * 128) +
                               tc::sw128_offset(r, c16 & 7)) = make_uint4(0, 0, 0, 0);
   }
+  // sink logits: one per thread for the split merge (tid < H), and the
+  // softmax threads' own rows for a single split's epilogue
+  const float sink_mine = (a.sink && tid < H) ? __ldg(a.sink + tid) : -INFINITY;
+  float sink_rows[2][2];
+  if (warp >= kSoftWarp0 && warp < kSoftWarp0 + 4) {
+#pragma unroll
+    for (int g = 0; g < RowMap<M>::NG; ++g)
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const int h = RowMap<M>::row(warp & 3, g, lane >> 2) + 8 * h2;
+        sink_rows[g][h2] = (a.sink && h < H) ? __ldg(a.sink + h) * kLog2e : -INFINITY;
+      }
+  }
   tc::fence_proxy_async_smem();
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = bars->tmem_slot;
+  pdl_wait();  // the previous kernel's results (top-k lists, new entries) are visible now
+  if (bad_pos && tid == 0 && split == 0) flag_error(a.err, CSA_EW_BAD_POSITION);
 
   if (n_tiles > 0 && warp == 0) {
     // ------------------------------------------------------------ S issuer
@@ -755,7 +774,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           fac[h2] = any ? 1.f / l_sum[g][h2] : 0.f;
           lse_r[h2] = any ? (m_ref[g][h2] + log2f(l_sum[g][h2])) * kLn2 : -INFINITY;
         } else {
-          const float sk = (a.sink && h < H) ? __ldg(a.sink + h) * kLog2e : -INFINITY;
+          const float sk = sink_rows[g][h2];
           float Mx = any ? m_ref[g][h2] : -INFINITY;
           if (a.sink) Mx = fmaxf(Mx, sk);
           fac[h2] = 0.f;
@@ -829,6 +848,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // its stages again, so every CTA pushes its partial rows and lse values for
   // those heads into the owner's shared memory (remote stores, no round
   // trips); after the second barrier each CTA combines its heads locally.
+  if (tid < H) reinterpret_cast<float*>(sm + C::kSinkOff)[tid] = sink_mine;
   tc::cluster_sync();
   const int hp = (H + ns - 1) / ns;
   {
@@ -851,13 +871,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const float* rlse = reinterpret_cast<const float*>(sm + C::kRecvLseOff);  // [ns][hp]
   const float* rrow = reinterpret_cast<const float*>(sm + C::kRecvOff);     // [ns][hp][128]
   float* wgt = reinterpret_cast<float*>(sm + C::kWgtOff);                  // [nh][ns]
+  const float* sink_s = reinterpret_cast<const float*>(sm + C::kSinkOff);
   for (int hl = tid; hl < nh; hl += kThreads) {
     const int h = h0 + hl;
-    float Mx = a.sink ? __ldg(a.sink + h) : -INFINITY;
+    float Mx = sink_s[h];
     for (int s = 0; s < ns; ++s) Mx = fmaxf(Mx, rlse[s * hp + hl]);
     float lse = -INFINITY;
     if (Mx != -INFINITY) {
-      float Z = a.sink ? expf(__ldg(a.sink + h) - Mx) : 0.f;
+      float Z = a.sink ? expf(sink_s[h] - Mx) : 0.f;
       for (int s = 0; s < ns; ++s) {
         const float ls = rlse[s * hp + hl];
         const float w = ls == -INFINITY ? 0.f : expf(ls - Mx);
@@ -897,16 +918,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 // time, so that the loads overlap.
 __global__ void __launch_bounds__(128) attn_merge_kernel(AttnArgs a) {
   pdl_trigger();
-  pdl_wait();
   const int qid = blockIdx.x, lane = threadIdx.x & 31;
   const int h = blockIdx.y * 4 + (threadIdx.x >> 5);
   const int ns = a.n_split, H = a.H;
   if (h >= H) return;
+  const float sink_h = a.sink ? __ldg(a.sink + h) : -INFINITY;  // an input: before the wait
+  pdl_wait();
   const float* lse_p = a.part_lse + (int64_t)qid * ns * H + h;  // split s at s * H
   const float4* row = reinterpret_cast<const float4*>(a.part_o + ((int64_t)qid * ns * H + h) * kD);
   const int64_t rstride = (int64_t)H * kD / 4;  // float4s between splits
   // the splits' lse values, all lanes at once (lane j holds splits j, j + 32, ..)
-  float Mx = a.sink ? __ldg(a.sink + h) : -INFINITY;
+  float Mx = sink_h;
   for (int s = lane; s < ns; s += 32) Mx = fmaxf(Mx, lse_p[(int64_t)s * H]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) Mx = fmaxf(Mx, __shfl_xor_sync(0xFFFFFFFFu, Mx, o));
@@ -920,7 +942,7 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(AttnArgs a) {
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) zl += __shfl_xor_sync(0xFFFFFFFFu, zl, o);
-    const float Z = zl + (a.sink ? expf(__ldg(a.sink + h) - Mx) : 0.f);
+    const float Z = zl + (a.sink ? expf(sink_h - Mx) : 0.f);
     const float inv = 1.f / Z;
     // the partial rows, eight splits' loads in flight at a time
     constexpr int kBatch = 8;
