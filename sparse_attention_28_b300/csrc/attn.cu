@@ -230,6 +230,69 @@ struct RowMap {  // softmax-thread view of the 16-lane TMEM layout
   }
 };
 
+// Split merge of one query whose splits form a cluster and left their
+// normalised partial rows and lse values in part_o / part_lse (global
+// memory): one cluster barrier (release / acquire at cluster scope) makes
+// every split's rows visible, then CTA `split` combines heads
+// [split*hp, split*hp + hp) reading them from L2 (ld.global.cg), with the
+// weights exp(lse_s - M) / Z of the cluster merge (the sink's term in Z
+// only).  wgt: ns*hp floats of scratch; sink_s: H floats.
+__device__ __forceinline__ void merge_from_global(const AttnArgs& a, int qid, int split, int ns,
+                                                  float* wgt, float* sink_s, float sink_mine) {
+  const int tid = threadIdx.x, H = a.H;
+  if (tid < H) sink_s[tid] = sink_mine;
+  tc::cluster_sync();
+  const int hp = (H + ns - 1) / ns;
+  const int h0 = split * hp;
+  const int nh = H - h0 < hp ? (H - h0 > 0 ? H - h0 : 0) : hp;
+  const float* plse = a.part_lse + (int64_t)qid * ns * H;  // split s, head h at s * H + h
+  for (int hl = tid; hl < nh; hl += kThreads) {
+    const int h = h0 + hl;
+    float Mx = a.sink ? sink_s[h] : -INFINITY;
+    for (int s = 0; s < ns; ++s) Mx = fmaxf(Mx, __ldcg(plse + s * H + h));
+    float lse = -INFINITY;
+    if (Mx != -INFINITY) {
+      float Z = a.sink ? ex2_approx((sink_s[h] - Mx) * kLog2e) : 0.f;
+      for (int s = 0; s < ns; ++s) {
+        const float ls = __ldcg(plse + s * H + h);
+        const float w = ls == -INFINITY ? 0.f : ex2_approx((ls - Mx) * kLog2e);
+        wgt[hl * ns + s] = w;
+        Z += w;
+      }
+      const float inv = 1.f / Z;
+      for (int s = 0; s < ns; ++s) wgt[hl * ns + s] *= inv;
+      lse = Mx + logf(Z);
+    } else {
+      for (int s = 0; s < ns; ++s) wgt[hl * ns + s] = 0.f;
+    }
+    if (a.lse) a.lse[(int64_t)qid * H + h] = lse;
+  }
+  __syncthreads();
+  const float4* rows = reinterpret_cast<const float4*>(a.part_o + (int64_t)qid * ns * H * kD);
+  const int64_t sstride = (int64_t)H * kD / 4;  // float4s between splits
+  for (int it = tid; it < nh * 32; it += kThreads) {
+    const int hl = it >> 5, d4 = it & 31, h = h0 + hl;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < ns; s0 += 4) {  // four splits' rows in flight at a time
+      float4 v[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        v[j] = s0 + j < ns ? __ldcg(rows + (s0 + j) * sstride + h * 32 + d4)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float w = s0 + j < ns ? wgt[hl * ns + s0 + j] : 0.f;
+        acc.x += w * v[j].x;
+        acc.y += w * v[j].y;
+        acc.z += w * v[j].z;
+        acc.w += w * v[j].w;
+      }
+    }
+    reinterpret_cast<uint2*>(a.out + ((int64_t)qid * H + h) * kD)[d4] =
+        make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+  }
+}
+
 template <int M, bool KV8>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(AttnArgs a, const __grid_constant__ Maps maps) {
@@ -317,15 +380,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   // sink logits: one per thread for the split merge (tid < H), and the
   // softmax threads' own rows for a single split's epilogue
-  const float sink_mine = (a.sink && tid < H) ? __ldg(a.sink + tid) : -INFINITY;
-  float sink_rows[2][2];
-  if (warp >= kSoftWarp0 && warp < kSoftWarp0 + 4) {
+  // (loaded here, first used after the main loop: the loads do not hold up
+  // the set-up)
+  float sink_mine = -INFINITY;
+  if (a.sink && tid < H) sink_mine = __ldg(a.sink + tid);
+  float sink_rows[2][2] = {{-INFINITY, -INFINITY}, {-INFINITY, -INFINITY}};
+  if (a.sink && warp >= kSoftWarp0 && warp < kSoftWarp0 + 4) {
 #pragma unroll
     for (int g = 0; g < RowMap<M>::NG; ++g)
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2) {
         const int h = RowMap<M>::row(warp & 3, g, lane >> 2) + 8 * h2;
-        sink_rows[g][h2] = (a.sink && h < H) ? __ldg(a.sink + h) * kLog2e : -INFINITY;
+        if (h < H) sink_rows[g][h2] = __ldg(a.sink + h);
       }
   }
   tc::fence_proxy_async_smem();
@@ -774,7 +840,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           fac[h2] = any ? 1.f / l_sum[g][h2] : 0.f;
           lse_r[h2] = any ? (m_ref[g][h2] + log2f(l_sum[g][h2])) * kLn2 : -INFINITY;
         } else {
-          const float sk = sink_rows[g][h2];
+          const float sk = sink_rows[g][h2] * kLog2e;
           float Mx = any ? m_ref[g][h2] : -INFINITY;
           if (a.sink) Mx = fmaxf(Mx, sk);
           fac[h2] = 0.f;
@@ -841,7 +907,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, kTmemCols);
   }
-  if (ns <= 1 || a.part_o) return;  // one split, or partials merged by attn_merge_kernel
+  if (ns <= 1 || (a.part_o && !a.xch)) return;  // one split, or merged by attn_merge_kernel
+  if (a.xch) {
+    merge_from_global(a, qid, split, ns, reinterpret_cast<float*>(sm + C::kWgtOff),
+                      reinterpret_cast<float*>(sm + C::kSinkOff), sink_mine);
+    return;
+  }
 
   // ---- split merge inside the cluster.  CTA `split` combines heads
   // [split*hp, split*hp + hp).  After the first cluster barrier no CTA uses
@@ -1059,9 +1130,13 @@ cudaError_t launch_tc(AttnArgs a, const Maps& maps, void* ws, cudaStream_t st) {
   }
   a.n_split = ns;
   a.keys_per_split = kps;
-  if (free_splits) {
+  a.xch = 0;
+  if (ns > 1 && ws) {
+    // partial rows through the workspace: merged by a second kernel (free
+    // splits) or by the cluster itself after one barrier
     a.part_o = reinterpret_cast<float*>(ws);
     a.part_lse = a.part_o + (int64_t)a.n_query * ns * a.H * kD;
+    a.xch = free_splits ? 0 : 1;
   }
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = launch_cfg<M, KV8>(ns, a.n_query, st, attr, true, !free_splits);

@@ -58,7 +58,11 @@ struct AttnArgs {
   int keys_per_split;
   float* part_o;
   float* part_lse;
-  int* counters;  // [n_query] split arrivals (zeroed per call)
+  // 1: the splits of a query are one cluster and exchange their partial rows
+  // through part_o / part_lse (global memory, L2) instead of distributed
+  // shared memory; 0 with part_o set: splits without a cluster, merged by a
+  // second kernel
+  int xch;
   __nv_bfloat16* out;
   float* lse;
   int32_t* err;
