@@ -471,12 +471,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bf16* kr = a.k_raw;
     const bf16* vr = a.v_raw;
     int32_t* codes = reinterpret_cast<int32_t*>(sm + C::kMetaOff);
+    // Leading stages whose 64 slots are all compressed entries of a dense key
+    // set (HCA) are four TMA boxes each: one thread issues them -- waiting for
+    // the ring slot, publishing the stage's slot bits, arriving for the whole
+    // loader group -- without the per-slot lookups and loader barriers; the
+    // group joins at the first stage that needs them (the window).
+    int j_fast = 0;
+    if (!KV8 && a.dense) {
+      const int full = (n_c < k_end ? n_c : k_end) - k_begin;
+      j_fast = full > 0 ? full / kStageKeys : 0;
+      if (j_fast > n_stages) j_fast = n_stages;
+    }
+    int issued = 0;
+    bool fast_ok = true;
+    if (j_fast > 0 && lt == 0) {
+      for (int j = 0; j < j_fast; ++j) {
+        const int st = j % kStages, pr = (j >> 1) % kPairs;
+        if (j >= kStages && (j & 1) == 0)
+          fast_ok = wait_or_flag(&bars->pair_empty[pr], ((j >> 1) / kPairs - 1) & 1, bars, a.err);
+        fast_ok = fast_ok && !*(volatile int*)&bars->timed_out;
+        if (!fast_ok) break;
+        bars->valid[j & 7][0] = 0xFFFFFFFFu;
+        bars->valid[j & 7][1] = 0xFFFFFFFFu;
+        if (j & 1) tc::mbar_arrive(&bars->meta_full[(j >> 1) & 3]);  // both stages' bits
+        const int row = (int)(ks.cmp_row0 + k_begin + (int64_t)j * kStageKeys);
+        const uint32_t off = st * kBlk;
+        tma::expect_tx(&bars->kv_full[pr], 4 * kBlk);
+        tma::load_box(sbase + C::kK0 + off, &maps.kc, 0, row, &bars->kv_full[pr]);
+        tma::load_box(sbase + C::kK1 + off, &maps.kc, 64, row, &bars->kv_full[pr]);
+        tma::load_box(sbase + C::kV0 + off, &maps.vc, 0, row, &bars->kv_full[pr]);
+        tma::load_box(sbase + C::kV1 + off, &maps.vc, 64, row, &bars->kv_full[pr]);
+        tc::mbar_arrive_count(&bars->kv_full[pr], kLoadThreads - 1);
+        issued = j + 1;
+      }
+    }
     // top-k entries of this thread's slot (lt < 64) for the next kPrefetch
     // stages: pf[i] belongs to stage j + i
     int32_t pf[kPrefetch];
 #pragma unroll
     for (int i = 0; i < kPrefetch; ++i)
-      pf[i] = lt < kStageKeys ? ks.fetch(k_begin + i * kStageKeys + lt) : 0;
+      pf[i] = lt < kStageKeys ? ks.fetch(k_begin + (j_fast + i) * kStageKeys + lt) : 0;
     // Every loader thread gives one arrival per stage on its pair's kv_full:
     // for a gathered stage once its own copies have landed (cp.async
     // mbarrier tracking, the loader does not block), for a TMA stage at issue
@@ -601,10 +635,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::fence_proxy_async_smem();
       tc::mbar_arrive(&bars->kv_full[pr]);
     };
-    int issued = 0;
-    for (int j = 0; j < n_stages; ++j) {
+    for (int j = j_fast; j < n_stages; ++j) {
       const int st = j % kStages, pr = (j >> 1) % kPairs;
-      bool go = true;
+      bool go = fast_ok;
       if (!KV8 && lt == 0 && j >= kStages && (j & 1) == 0)
         go = wait_or_flag(&bars->pair_empty[pr], ((j >> 1) / kPairs - 1) & 1, bars, a.err);
       go = go && !*(volatile int*)&bars->timed_out;

@@ -45,6 +45,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar)) : "memory");
 }
+// `count` arrivals at once (one thread standing in for a group).
+__device__ __forceinline__ void mbar_arrive_count(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
 // The mbarrier tracks completion of the calling thread's prior cp.async ops
 // (one pending arrival per thread, without incrementing the expected count).
 __device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
