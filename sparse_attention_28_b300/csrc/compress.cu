@@ -19,7 +19,7 @@
 // One CTA per (block, sequence), one thread per output channel.  The
 // block's span raw rows (fp32) are staged in shared memory; each thread
 // reads its own W row straight from global memory (all of it in flight at
-// once: no other thread uses it) and forms its channel's gate logits 16
+// once: no other thread uses it) and forms its channel's gate logits 4
 // positions at a time (x rows as shared-memory broadcasts), folded into an
 // online softmax.
 #include "common.cuh"
@@ -29,12 +29,15 @@ namespace csa {
 
 namespace {
 
-constexpr int kPosChunk = 16;
+constexpr int kPosChunk = 4;  // positions whose gate logits are formed together
 
 template <int D>
 __global__ void __launch_bounds__(D) compress_kernel(CompressArgs a) {
+  // The reads below (raw rows, W, position biases) touch only what no kernel
+  // of this library writes, so they are issued before griddepcontrol.wait and
+  // all at once (one memory latency for the kernel, not one per position);
+  // the output is written after the wait.
   pdl_trigger();
-  pdl_wait();
   extern __shared__ __align__(16) float xs[];  // [span][D]
   __shared__ float red[D / 32];
   const int c = threadIdx.x;
@@ -53,17 +56,35 @@ __global__ void __launch_bounds__(D) compress_kernel(CompressArgs a) {
   const int i_off = p0 < 0 ? (int)(-p0) : 0;
   const int np = a.span - i_off;
   const int64_t r0 = (p0 + i_off) % a.raw_cap;  // ring row of the first token
-  for (int k = 0; k < np; ++k) {
-    int64_t r = r0 + k;
-    if (r >= a.raw_cap) r -= a.raw_cap;
-    xs[k * D + c] = __bfloat162float(xb[r * D + c]);
+  const float* bias = a.pos_bias + (int64_t)i_off * D;
+  float bnext[kPosChunk];  // position biases of this channel for the next chunk
+#pragma unroll
+  for (int ii = 0; ii < kPosChunk; ++ii) bnext[ii] = ii < np ? __ldg(bias + (int64_t)ii * D + c) : 0.f;
+  constexpr int kRowBatch = 8;  // raw rows in flight per thread
+  for (int k0 = 0; k0 < np; k0 += kRowBatch) {
+    bf16 xr[kRowBatch];
+#pragma unroll
+    for (int kk = 0; kk < kRowBatch; ++kk) {
+      int64_t r = r0 + k0 + kk;
+      if (r >= a.raw_cap) r -= a.raw_cap;
+      if (k0 + kk < np) xr[kk] = xb[r * D + c];
+    }
+#pragma unroll
+    for (int kk = 0; kk < kRowBatch; ++kk)
+      if (k0 + kk < np) xs[(k0 + kk) * D + c] = __bfloat162float(xr[kk]);
   }
   __syncthreads();
-  const float* bias = a.pos_bias + (int64_t)i_off * D;
 
   float mx = -INFINITY, den = 0.f, num = 0.f;
   for (int i0 = 0; i0 < np; i0 += kPosChunk) {
     const int n = (np - i0 < kPosChunk) ? np - i0 : kPosChunk;
+    float bv[kPosChunk];
+#pragma unroll
+    for (int ii = 0; ii < kPosChunk; ++ii) {  // this chunk's biases; the next chunk's requested
+      bv[ii] = bnext[ii];
+      const int in = i0 + kPosChunk + ii;
+      bnext[ii] = in < np ? __ldg(bias + (int64_t)in * D + c) : 0.f;
+    }
     float gl[kPosChunk];
 #pragma unroll
     for (int ii = 0; ii < kPosChunk; ++ii) gl[ii] = 0.f;
@@ -89,7 +110,7 @@ __global__ void __launch_bounds__(D) compress_kernel(CompressArgs a) {
 #pragma unroll
     for (int ii = 0; ii < kPosChunk; ++ii) {
       if (ii < n) {
-        const float gi = gl[ii] + __ldg(bias + (int64_t)(i0 + ii) * D + c);
+        const float gi = gl[ii] + bv[ii];
         const float xv = xs[(i0 + ii) * D + c];
         if (gi > mx) {
           const float r = expf(mx - gi);
@@ -105,6 +126,7 @@ __global__ void __launch_bounds__(D) compress_kernel(CompressArgs a) {
     }
   }
   const float y = num / den;
+  pdl_wait();  // outputs only from here on
 
   if (a.fp4) {
     // FP4: per 16 channels one E4M3 scale, the nearest to amax / 6 (1 if the
