@@ -541,14 +541,22 @@ __global__ void __launch_bounds__(NT, 1024 / NT) topk_select_kernel(IndexerArgs 
 // One CTA per query, no cluster, for calls with many queries (chunked
 // prefill): the query's scores stay in L2 and are streamed rather than held
 // in registers.  Pass 1: histogram of key bits 31..20 (4096 bins) and the bin
-// B* holding the k-th key.  Pass 2: the keys of B* (at most kCand; else two
-// more streamed passes) resolve bits 19..10 and 9..0 to the exact k-th key k*
-// and the count of entries equal to it to take.  Pass 3: tiles of NT*16
-// entries in index order, one block scan per tile, write the entries above
-// k* and the lowest-index ties.  Same selection as topk_select_kernel.
+// B* holding the k-th key.  When the entries above B* and in it number at
+// most kList (the usual case: fewer than k above, a few hundred in B*),
+// pass 2 walks the scores in index order, one block scan per tile of NT*16
+// entries, and writes those entries (index and key) into a list in shared
+// memory, in index order; bits 19..10 and 9..0 of the list's B* keys give
+// the exact k-th key k* and how many entries equal to it to take, and one
+// block scan over the list writes the entries above k* and the lowest-index
+// ties.  Otherwise (heavy ties) pass 2 keeps B*'s keys (at most kCand; else
+// two more streamed passes) to find k*, and pass 3 walks the scores in index
+// order once more.  Same selection as topk_select_kernel.
 constexpr int kCand = 2048;
+constexpr int kList = 4096;
 struct StreamShared {
   uint32_t hist[kHistBins];
+  uint32_t lkey[kList];  // the list: keys and entry indices, in index order
+  int32_t lidx[kList];
   uint32_t cand[kCand];
   int scratch[32];
   int res[3];
@@ -560,7 +568,8 @@ __global__ void __launch_bounds__(NT, 2) topk_stream_kernel(IndexerArgs a, int q
   constexpr int PER1 = kHistBins / NT;
   constexpr int PER2 = 1024 / NT;
   constexpr int kE = 16;  // entries per thread per output tile
-  __shared__ StreamShared sh;
+  extern __shared__ __align__(16) uint8_t stream_smem[];
+  StreamShared& sh = *reinterpret_cast<StreamShared*>(stream_smem);
   pdl_trigger();
   pdl_wait();
   const int tid = threadIdx.x;
@@ -619,7 +628,95 @@ __global__ void __launch_bounds__(NT, 2) topk_stream_kernel(IndexerArgs a, int q
   const uint32_t bstar = (uint32_t)sh.res[0];
   int need = a.k - sh.res[1];
   const bool in_smem = sh.hist[bstar] <= (uint32_t)kCand;
+  const int nlist = sh.res[1] + (int)sh.hist[bstar];  // entries in B* or above it
   __syncthreads();
+
+  if (nlist <= kList) {
+    // ---- pass 2: those entries, in index order, into the list
+    int run = 0;
+    for (int base = 0; base < n; base += NT * kE) {
+      const int i0 = base + tid * kE;
+      uint32_t keys[kE];
+      uint32_t take = 0u;
+#pragma unroll
+      for (int q = 0; q < kE / 4; ++q) {
+        const int e = i0 + 4 * q;
+        float f[4];
+        if (e + 3 < n) {
+          const float4 v = s4[e >> 2];
+          f[0] = v.x, f[1] = v.y, f[2] = v.z, f[3] = v.w;
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) f[c] = e + c < n ? scores[e + c] : 0.f;
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint32_t key = e + c < n ? score_key(f[c]) : 0u;
+          keys[4 * q + c] = key;
+          take |= (uint32_t)(key && (key >> 20) >= bstar) << (4 * q + c);
+        }
+      }
+      int tot;
+      int pos = run + block_excl_scan<NT>(__popc(take), sh.scratch, &tot);
+#pragma unroll
+      for (int i = 0; i < kE; ++i)
+        if ((take >> i) & 1u) {
+          sh.lkey[pos] = keys[i];
+          sh.lidx[pos] = i0 + i;
+          ++pos;
+        }
+      run += tot;
+    }
+    for (int i = tid; i < 1024; i += NT) sh.hist[i] = 0u;
+    __syncthreads();
+    // ---- k* from the list's B* keys: bits 19..10, then 9..0
+    for (int c = tid; c < nlist; c += NT)
+      if ((sh.lkey[c] >> 20) == bstar) atomicAdd(&sh.hist[(sh.lkey[c] >> 10) & 1023], 1u);
+    __syncthreads();
+    {
+      int bins[PER2];
+#pragma unroll
+      for (int i = 0; i < PER2; ++i) bins[i] = (int)sh.hist[1023 - PER2 * tid - i];
+      bin_from_top<NT, PER2>(bins, 1023 - PER2 * tid, need, sh.scratch, sh.res);
+    }
+    const uint32_t p2 = (bstar << 10) | (uint32_t)sh.res[0];
+    need -= sh.res[1];
+    for (int i = tid; i < 1024; i += NT) sh.hist[i] = 0u;
+    __syncthreads();
+    for (int c = tid; c < nlist; c += NT)
+      if ((sh.lkey[c] >> 10) == p2) atomicAdd(&sh.hist[sh.lkey[c] & 1023], 1u);
+    __syncthreads();
+    {
+      int bins[PER2];
+#pragma unroll
+      for (int i = 0; i < PER2; ++i) bins[i] = (int)sh.hist[1023 - PER2 * tid - i];
+      bin_from_top<NT, PER2>(bins, 1023 - PER2 * tid, need, sh.scratch, sh.res);
+    }
+    const uint32_t kstar = (p2 << 10) | (uint32_t)sh.res[0];
+    const int need_eq = need - sh.res[1];
+    // ---- the selection in list (= index) order: above k*, then the lowest ties
+    int run_above = 0, run_eq = 0;
+    for (int c0 = 0; c0 < nlist; c0 += NT) {
+      const int c = c0 + tid;
+      const uint32_t key = c < nlist ? sh.lkey[c] : 0u;
+      const int above = key > kstar ? 1 : 0, eq = (c < nlist && key == kstar) ? 1 : 0;
+      int tot;
+      const int before = block_excl_scan<NT>(above | (eq << 16), sh.scratch, &tot);
+      const int e_rank = run_eq + (before >> 16);
+      if (above || (eq && e_rank < need_eq)) {
+        const int pos = run_above + (before & 0xFFFF) + min(e_rank, need_eq);
+        if (pos < a.k) {
+          out[pos] = sh.lidx[c];
+          if (out_s) out_s[pos] = scores[sh.lidx[c]];
+        }
+      }
+      run_above += tot & 0xFFFF;
+      run_eq += tot >> 16;
+    }
+    if (tid == 0 && run_above + min(run_eq, need_eq) != a.k)
+      flag_error(a.err, CSA_EW_BAD_INDEX);  // internal invariant
+    return;
+  }
 
   // ---- pass 2: the keys of B*; levels 2 and 3 over them
   if (in_smem)
@@ -791,7 +888,9 @@ cudaError_t launch_indexer_topk(const IndexerArgs& a, void* ws, cudaStream_t st)
   WsLayout L = carve(ws, a.N_cap);
   const SelPlan p = select_plan(a.n_query, a.N_cap);
   {
-    const cudaError_t e = ensure_smem_attr(p.fn, sel_smem_bytes(p.nt, p.per), true);
+    cudaError_t e = ensure_smem_attr(p.fn, sel_smem_bytes(p.nt, p.per), true);
+    if (e == cudaSuccess)
+      e = ensure_smem_attr((const void*)topk_stream_kernel<512>, (int)sizeof(StreamShared));
     if (e != cudaSuccess) return e;
   }
   for (int q0 = 0; q0 < a.n_query; q0 += kQueryChunk) {
@@ -799,7 +898,8 @@ cudaError_t launch_indexer_topk(const IndexerArgs& a, void* ws, cudaStream_t st)
     cudaError_t e = launch_scores(a, q0, qc, L, st);
     if (e != cudaSuccess) return e;
     if (qc >= kStreamQueries) {  // one CTA per query, streamed from L2
-      e = launch_pdl(topk_stream_kernel<512>, dim3((unsigned)qc), dim3(512), 0, st, a, q0, L);
+      e = launch_pdl(topk_stream_kernel<512>, dim3((unsigned)qc), dim3(512),
+                     sizeof(StreamShared), st, a, q0, L);
       if (e != cudaSuccess) return e;
       continue;
     }
