@@ -26,6 +26,8 @@
 //      writes the indices of its consecutive entries in order.
 // Bins, keys and the tie rule give the same set as a full sort on
 // (-score, index).
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "tc.cuh"
@@ -539,29 +541,43 @@ __global__ void __launch_bounds__(NT, 1024 / NT) topk_select_kernel(IndexerArgs 
 }
 
 // One CTA per query, no cluster, for calls with many queries (chunked
-// prefill): the query's scores stay in L2 and are streamed rather than held
-// in registers.  Pass 1: histogram of key bits 31..20 (4096 bins) and the bin
-// B* holding the k-th key.  When the entries above B* and in it number at
-// most kList (the usual case: fewer than k above, a few hundred in B*),
-// pass 2 walks the scores in index order, one block scan per tile of NT*16
-// entries, and writes those entries (index and key) into a list in shared
-// memory, in index order; bits 19..10 and 9..0 of the list's B* keys give
-// the exact k-th key k* and how many entries equal to it to take, and one
-// block scan over the list writes the entries above k* and the lowest-index
-// ties.  Otherwise (heavy ties) pass 2 keeps B*'s keys (at most kCand; else
-// two more streamed passes) to find k*, and pass 3 walks the scores in index
-// order once more.  Same selection as topk_select_kernel.
+// prefill): the query's scores are streamed from the workspace rather than
+// held in registers.  The usual case reads them once: an evenly spaced
+// sample of the row gives a key bound lo (its key at the rank that
+// corresponds to about (k + kList) / 2 entries of the row); one streamed
+// pass lists, in index order, the entries above lo and the first k equal to
+// it (per-warp segments and buckets, no block barrier per tile); when the
+// list holds at least k and at most kList entries, key bits 31..20, 19..10
+// and 9..0 of the listed keys give the exact k-th key k* and how many
+// entries equal to it to take, and one block scan over the list writes the
+// entries above k* and the lowest-index ties.  Otherwise (a skewed sample,
+// k > kList / 2) the histogram passes do it: pass 1, a histogram of key bits
+// 31..20 (4096 bins) and the bin B* holding the k-th key; when B* and the
+// bins above it hold at most kList entries, one more streamed pass lists
+// them and the selection is made from the list as above; else pass 2 keeps
+// B*'s keys (at most kCand; else two more streamed passes) to find k*, and
+// pass 3 walks the scores in index order once more.  Same selection as
+// topk_select_kernel.
 constexpr int kCand = 2048;
 constexpr int kList = 4096;
+constexpr int kSampleVec = 1024;  // 16-byte score vectors sampled for the list's bound
+static_assert(kList >= 4 * kSampleVec, "a row longer than the list holds a whole sample");
+constexpr int kStreamWarps = 16;  // warps of a select CTA (512 threads)
+constexpr int kBucket = 512;      // entries a warp may take in one streamed pass
 struct StreamShared {
   uint32_t hist[kHistBins];
   uint32_t lkey[kList];  // the list: keys and entry indices, in index order
   int32_t lidx[kList];
-  uint32_t cand[kCand];
+  // per-warp buckets of a streamed pass: keys [warp][kBucket], then indices;
+  // the histogram passes keep threshold-bin keys (at most kCand) at the front
+  uint32_t buckets[2 * kStreamWarps * kBucket];
+  int wcnt[kStreamWarps];    // entries a warp took (above lo or equal to it)
+  int wcnt_e[kStreamWarps];  // of those, equal to lo
   int scratch[32];
   int res[3];
   int ncand;
 };
+static_assert(kCand <= 2 * kStreamWarps * kBucket, "threshold-bin keys fit the buckets");
 
 template <int NT>
 __global__ void __launch_bounds__(NT, 2) topk_stream_kernel(IndexerArgs a, int q0, WsLayout L) {
@@ -570,11 +586,14 @@ __global__ void __launch_bounds__(NT, 2) topk_stream_kernel(IndexerArgs a, int q
   constexpr int kE = 16;  // entries per thread per output tile
   extern __shared__ __align__(16) uint8_t stream_smem[];
   StreamShared& sh = *reinterpret_cast<StreamShared*>(stream_smem);
+  uint32_t* const cand = sh.buckets;
   pdl_trigger();
-  pdl_wait();
   const int tid = threadIdx.x;
   const int lq = blockIdx.x, qid = q0 + lq;
+  // positions and entry counts: inputs that no kernel of this library
+  // writes, read while the scoring kernel finishes
   const int64_t nv = visible_entries(a, qid, nullptr, false);
+  pdl_wait();
   int32_t* out = a.topk_idx + (int64_t)qid * a.k;
   float* out_s = a.topk_score ? a.topk_score + (int64_t)qid * a.k : nullptr;
   const float* scores = L.scores + (int64_t)lq * L.stride;
@@ -613,63 +632,26 @@ __global__ void __launch_bounds__(NT, 2) topk_stream_kernel(IndexerArgs a, int q
     for (int e = 4 * n4 + tid; e < n; e += NT) f(score_key(scores[e]));
   };
 
-  // ---- pass 1: bits 31..20
-  for (int i = tid; i < kHistBins; i += NT) sh.hist[i] = 0u;
-  if (tid == 0) sh.ncand = 0;
-  __syncthreads();
-  sweep([&](uint32_t key) { atomicAdd(&sh.hist[key >> 20], 1u); });
-  __syncthreads();
-  {
-    int bins[PER1];
+  // ---- the exact selection among a list of entries (index order) that holds
+  // every entry whose key is at or above some bound, and at least k of them
+  // (so the k-th key k* is in the list): k* from key bits 31..20, 19..10 and
+  // 9..0 of the listed keys, then one block scan per NT listed entries writes
+  // the entries above k* and the lowest-index ties, in index order
+  auto select_list = [&](int nlist) {
+    for (int i = tid; i < kHistBins; i += NT) sh.hist[i] = 0u;
+    __syncthreads();
+    for (int c = tid; c < nlist; c += NT) atomicAdd(&sh.hist[sh.lkey[c] >> 20], 1u);
+    __syncthreads();
+    {
+      int bins[PER1];
 #pragma unroll
-    for (int i = 0; i < PER1; ++i) bins[i] = (int)sh.hist[kHistBins - 1 - PER1 * tid - i];
-    bin_from_top<NT, PER1>(bins, kHistBins - 1 - PER1 * tid, a.k, sh.scratch, sh.res);
-  }
-  const uint32_t bstar = (uint32_t)sh.res[0];
-  int need = a.k - sh.res[1];
-  const bool in_smem = sh.hist[bstar] <= (uint32_t)kCand;
-  const int nlist = sh.res[1] + (int)sh.hist[bstar];  // entries in B* or above it
-  __syncthreads();
-
-  if (nlist <= kList) {
-    // ---- pass 2: those entries, in index order, into the list
-    int run = 0;
-    for (int base = 0; base < n; base += NT * kE) {
-      const int i0 = base + tid * kE;
-      uint32_t keys[kE];
-      uint32_t take = 0u;
-#pragma unroll
-      for (int q = 0; q < kE / 4; ++q) {
-        const int e = i0 + 4 * q;
-        float f[4];
-        if (e + 3 < n) {
-          const float4 v = s4[e >> 2];
-          f[0] = v.x, f[1] = v.y, f[2] = v.z, f[3] = v.w;
-        } else {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) f[c] = e + c < n ? scores[e + c] : 0.f;
-        }
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint32_t key = e + c < n ? score_key(f[c]) : 0u;
-          keys[4 * q + c] = key;
-          take |= (uint32_t)(key && (key >> 20) >= bstar) << (4 * q + c);
-        }
-      }
-      int tot;
-      int pos = run + block_excl_scan<NT>(__popc(take), sh.scratch, &tot);
-#pragma unroll
-      for (int i = 0; i < kE; ++i)
-        if ((take >> i) & 1u) {
-          sh.lkey[pos] = keys[i];
-          sh.lidx[pos] = i0 + i;
-          ++pos;
-        }
-      run += tot;
+      for (int i = 0; i < PER1; ++i) bins[i] = (int)sh.hist[kHistBins - 1 - PER1 * tid - i];
+      bin_from_top<NT, PER1>(bins, kHistBins - 1 - PER1 * tid, a.k, sh.scratch, sh.res);
     }
+    const uint32_t bstar = (uint32_t)sh.res[0];
+    int need = a.k - sh.res[1];
     for (int i = tid; i < 1024; i += NT) sh.hist[i] = 0u;
     __syncthreads();
-    // ---- k* from the list's B* keys: bits 19..10, then 9..0
     for (int c = tid; c < nlist; c += NT)
       if ((sh.lkey[c] >> 20) == bstar) atomicAdd(&sh.hist[(sh.lkey[c] >> 10) & 1023], 1u);
     __syncthreads();
@@ -694,7 +676,6 @@ __global__ void __launch_bounds__(NT, 2) topk_stream_kernel(IndexerArgs a, int q
     }
     const uint32_t kstar = (p2 << 10) | (uint32_t)sh.res[0];
     const int need_eq = need - sh.res[1];
-    // ---- the selection in list (= index) order: above k*, then the lowest ties
     int run_above = 0, run_eq = 0;
     for (int c0 = 0; c0 < nlist; c0 += NT) {
       const int c = c0 + tid;
@@ -715,19 +696,250 @@ __global__ void __launch_bounds__(NT, 2) topk_stream_kernel(IndexerArgs a, int q
     }
     if (tid == 0 && run_above + min(run_eq, need_eq) != a.k)
       flag_error(a.err, CSA_EW_BAD_INDEX);  // internal invariant
-    return;
-  }
+  };
 
+  // ---- one streamed pass: the entries at or above lo, in index order, into
+  // the list.  Each warp streams its own contiguous segment of the row (whole
+  // 256-entry steps: lane l holds entries 4 l .. 4 l + 3 of each half, three
+  // steps of loads in flight) and appends to its own bucket, in order, every
+  // entry that a float compare with lo's value does not rule out (NaN scores
+  // included); no barrier until the segment ends.  The exact key test comes
+  // at the copy to the list: every warp counts the keys of its bucket above
+  // lo and equal to it, and copies them to the list at the offsets the lower
+  // warps' counts give.  Strict: the entries above lo all go in, and of
+  // those equal to lo only the first k of the row (no more can be selected:
+  // if k* == lo they are the lowest-index ties), so a bound that many
+  // entries share still gives a short list.  Returns the list's length (at
+  // most kList entries are written), or -1 when a bucket overflowed.
+  constexpr int kWarps = NT / 32;
+  constexpr int kStep = 256;
+  constexpr int kAhead = 3;
+  static_assert(kWarps == kStreamWarps, "one bucket per warp");
+  auto warp_gather = [&](auto strict_tag, uint32_t lo) -> int {
+    constexpr bool strict = decltype(strict_tag)::value;
+    const int warp = tid >> 5, lane = tid & 31;
+    const unsigned lt_mask = (1u << lane) - 1u;
+    // lo's score (the inverse of score_key); !(f < lo_f) holds for every f
+    // whose key is at least lo, and for NaN
+    const uint32_t lo_bits = (lo & 0x80000000u) ? (lo & 0x7FFFFFFFu) : ~lo;
+    const float lo_f = __uint_as_float(lo_bits);
+    const int seg = (n + kWarps * kStep - 1) / (kWarps * kStep) * kStep;
+    const int s_begin = min(n, warp * seg), s_end = min(n, s_begin + seg);
+    uint32_t* bk = sh.buckets + warp * kBucket;
+    int32_t* bi = reinterpret_cast<int32_t*>(sh.buckets + kStreamWarps * kBucket) + warp * kBucket;
+    const uint64_t drop = l2_evict_first_policy();  // each score is read once here
+    float4 v[kAhead][2];
+    auto ld = [&](float4 (&w)[2], int base) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int e = base + 128 * j + 4 * lane;  // the row holds whole 16-byte vectors
+        w[j] = e < s_end ? ld_f32x4_policy(s4 + (e >> 2), drop)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    };
+#pragma unroll
+    for (int i = 0; i < kAhead; ++i) ld(v[i], s_begin + i * kStep);
+    int run = 0;
+    for (int base = s_begin; base < s_end; base += kAhead * kStep) {
+#pragma unroll
+      for (int i = 0; i < kAhead; ++i) {
+        const int b = base + i * kStep;
+        if (b < s_end) {  // warp-uniform
+          const float f[8] = {v[i][0].x, v[i][0].y, v[i][0].z, v[i][0].w,
+                              v[i][1].x, v[i][1].y, v[i][1].z, v[i][1].w};
+          unsigned m = 0u;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) m |= (unsigned)!(f[c] < lo_f) << c;
+          if (b + kStep > s_end) {  // the segment's last step: entries past its end
+            const int r0 = s_end - (b + 4 * lane), r1 = r0 - 128;
+            m &= (r0 >= 4 ? 0xFu : (1u << max(r0, 0)) - 1u) |
+                 ((r1 >= 4 ? 0xFu : (1u << max(r1, 0)) - 1u) << 4);
+          }
+          // takes before this lane, both halves at once (8 bits each)
+          const int own = __popc(m & 0xFu) | (__popc(m >> 4) << 8);
+          int inc = own;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+            if (lane >= o) inc += y;
+          }
+          const int tot = __shfl_sync(0xFFFFFFFFu, inc, 31);
+          const int excl = inc - own;
+          int pos0 = run + (excl & 0xFF), pos1 = run + (tot & 0xFF) + (excl >> 8);
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            if ((m >> c) & 1u) {
+              int& p = c < 4 ? pos0 : pos1;
+              if (p < kBucket) {
+                bk[p] = score_key(f[c]);
+                bi[p] = b + (c < 4 ? 0 : 128) + 4 * lane + (c & 3);
+              }
+              ++p;
+            }
+          run += (tot & 0xFF) + (tot >> 8);
+        }
+        if (b + kAhead * kStep < s_end) ld(v[i], b + kAhead * kStep);
+      }
+    }
+    // exact keys: above lo (at or above it when not strict), equal to it
+    int cnt_a = 0, cnt_e = 0;
+    if (run <= kBucket)
+      for (int c0 = 0; c0 < run; c0 += 32) {
+        const int c = c0 + lane;
+        const uint32_t key = c < run ? bk[c] : 0u;
+        const bool is_a = c < run && (strict ? key > lo : key >= lo);
+        const bool is_e = c < run && strict && key == lo;
+        cnt_a += __popc(__ballot_sync(0xFFFFFFFFu, is_a));
+        cnt_e += __popc(__ballot_sync(0xFFFFFFFFu, is_e));
+      }
+    if (lane == 0) {
+      sh.wcnt[warp] = run > kBucket ? -1 : cnt_a;
+      sh.wcnt_e[warp] = cnt_e;
+    }
+    __syncthreads();
+    bool over = false;
+    int tot_a = 0, tot_e = 0, a_before = 0, e_before = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const int ca = sh.wcnt[w], ce = sh.wcnt_e[w];
+      over |= ca < 0;
+      if (w < warp) {
+        a_before += ca;
+        e_before += ce;
+      }
+      tot_a += ca;
+      tot_e += ce;
+    }
+    const int len = tot_a + min(tot_e, a.k);
+    if (over) return -1;
+    if (len < a.k || len > kList) return len;
+    for (int c0 = 0; c0 < run; c0 += 32) {
+      const int c = c0 + lane;
+      const uint32_t key = c < run ? bk[c] : 0u;
+      const bool is_a = c < run && (strict ? key > lo : key >= lo);
+      const bool is_e = c < run && strict && key == lo;
+      const unsigned be = __ballot_sync(0xFFFFFFFFu, is_e), ba = __ballot_sync(0xFFFFFFFFu, is_a);
+      const int e_r = e_before + __popc(be & lt_mask);
+      const int a_r = a_before + __popc(ba & lt_mask);
+      int p = kList;
+      if (is_a) p = a_r + min(e_r, a.k);
+      else if (is_e && e_r < a.k) p = a_r + e_r;
+      if (p < kList) {
+        sh.lkey[p] = key;
+        sh.lidx[p] = bi[c];
+      }
+      a_before += __popc(ba);
+      e_before += __popc(be);
+    }
+    __syncthreads();
+    return len;
+  };
+
+  // ---- the usual case: a bound from a sample.  kSampleVec evenly spaced
+  // 16-byte vectors of the scores (4 * kSampleVec keys) give lo, the
+  // sample's key of the rank that corresponds to (k + kList) / 2 entries of
+  // the whole row; when at
+  // least k entries are at or above lo and the list holds them, one streamed
+  // pass lists them and the selection is made from the list.  Otherwise (a
+  // skewed sample) the histogram passes below do it.  With n <= kList every
+  // entry is listed.
+  if (2 * a.k <= kList) {
+    uint32_t lo = 1u;
+    bool strict = false;
+    if (n > kList) {
+      constexpr int kSV = kSampleVec / NT;
+      const int stride = n4 / kSampleVec;  // >= 1: n > kList >= 4 * kSampleVec
+      // the sample's keys wait in the list's key array (thread t's at 4 t + ...)
+      uint32_t* sk = sh.lkey;
+#pragma unroll
+      for (int u = 0; u < kSV; ++u) {
+        const float4 f = s4[(int64_t)(tid + u * NT) * stride];
+        *reinterpret_cast<uint4*>(sk + 4 * (tid + u * NT)) =
+            make_uint4(score_key(f.x), score_key(f.y), score_key(f.z), score_key(f.w));
+      }
+      for (int i = tid; i < kHistBins; i += NT) sh.hist[i] = 0u;
+      __syncthreads();
+      for (int i = tid; i < 4 * kSampleVec; i += NT) atomicAdd(&sh.hist[sk[i] >> 20], 1u);
+      __syncthreads();
+      int r = (int)((int64_t)((a.k + kList) / 2) * (4 * kSampleVec) / n);
+      r = r < 1 ? 1 : r;  // < 4 * kSampleVec, since n > kList
+      {
+        int bins[PER1];
+#pragma unroll
+        for (int i = 0; i < PER1; ++i) bins[i] = (int)sh.hist[kHistBins - 1 - PER1 * tid - i];
+        bin_from_top<NT, PER1>(bins, kHistBins - 1 - PER1 * tid, r, sh.scratch, sh.res);
+      }
+      const uint32_t b1 = (uint32_t)sh.res[0];
+      r -= sh.res[1];
+      for (int i = tid; i < 1024; i += NT) sh.hist[i] = 0u;
+      __syncthreads();
+      for (int i = tid; i < 4 * kSampleVec; i += NT)
+        if ((sk[i] >> 20) == b1) atomicAdd(&sh.hist[(sk[i] >> 10) & 1023], 1u);
+      __syncthreads();
+      {
+        int bins[PER2];
+#pragma unroll
+        for (int i = 0; i < PER2; ++i) bins[i] = (int)sh.hist[1023 - PER2 * tid - i];
+        bin_from_top<NT, PER2>(bins, 1023 - PER2 * tid, r, sh.scratch, sh.res);
+      }
+      const uint32_t b2 = (b1 << 10) | (uint32_t)sh.res[0];
+      r -= sh.res[1];
+      for (int i = tid; i < 1024; i += NT) sh.hist[i] = 0u;
+      __syncthreads();
+      for (int i = tid; i < 4 * kSampleVec; i += NT)
+        if ((sk[i] >> 10) == b2) atomicAdd(&sh.hist[sk[i] & 1023], 1u);
+      __syncthreads();
+      {
+        int bins[PER2];
+#pragma unroll
+        for (int i = 0; i < PER2; ++i) bins[i] = (int)sh.hist[1023 - PER2 * tid - i];
+        bin_from_top<NT, PER2>(bins, 1023 - PER2 * tid, r, sh.scratch, sh.res);
+      }
+      lo = (b2 << 10) | (uint32_t)sh.res[0];  // a sample key: never 0
+      strict = true;
+    }
+    const int nlist =
+        strict ? warp_gather(std::true_type{}, lo) : warp_gather(std::false_type{}, lo);
+    if (nlist >= a.k && nlist <= kList) {
+      select_list(nlist);
+      return;
+    }
+  }
+  // ---- pass 1: bits 31..20
+  for (int i = tid; i < kHistBins; i += NT) sh.hist[i] = 0u;
+  if (tid == 0) sh.ncand = 0;
+  __syncthreads();
+  sweep([&](uint32_t key) { atomicAdd(&sh.hist[key >> 20], 1u); });
+  __syncthreads();
+  {
+    int bins[PER1];
+#pragma unroll
+    for (int i = 0; i < PER1; ++i) bins[i] = (int)sh.hist[kHistBins - 1 - PER1 * tid - i];
+    bin_from_top<NT, PER1>(bins, kHistBins - 1 - PER1 * tid, a.k, sh.scratch, sh.res);
+  }
+  const uint32_t bstar = (uint32_t)sh.res[0];
+  int need = a.k - sh.res[1];
+  const bool in_smem = sh.hist[bstar] <= (uint32_t)kCand;
+  const int nlist = sh.res[1] + (int)sh.hist[bstar];  // entries in B* or above it
+  __syncthreads();
+
+  if (nlist <= kList) {
+    // ---- pass 2: those entries into the list
+    if (warp_gather(std::false_type{}, bstar << 20) == nlist) {
+      select_list(nlist);
+      return;
+    }
+  }
   // ---- pass 2: the keys of B*; levels 2 and 3 over them
   if (in_smem)
     sweep([&](uint32_t key) {
-      if ((key >> 20) == bstar) sh.cand[atomicAdd(&sh.ncand, 1)] = key;
+      if ((key >> 20) == bstar) cand[atomicAdd(&sh.ncand, 1)] = key;
     });
   for (int i = tid; i < 1024; i += NT) sh.hist[i] = 0u;
   __syncthreads();
   const int nc = sh.ncand;
   if (in_smem) {
-    for (int c = tid; c < nc; c += NT) atomicAdd(&sh.hist[(sh.cand[c] >> 10) & 1023], 1u);
+    for (int c = tid; c < nc; c += NT) atomicAdd(&sh.hist[(cand[c] >> 10) & 1023], 1u);
   } else {
     sweep([&](uint32_t key) {
       if ((key >> 20) == bstar) atomicAdd(&sh.hist[(key >> 10) & 1023], 1u);
@@ -746,7 +958,7 @@ __global__ void __launch_bounds__(NT, 2) topk_stream_kernel(IndexerArgs a, int q
   __syncthreads();
   if (in_smem) {
     for (int c = tid; c < nc; c += NT)
-      if ((sh.cand[c] >> 10) == p2) atomicAdd(&sh.hist[sh.cand[c] & 1023], 1u);
+      if ((cand[c] >> 10) == p2) atomicAdd(&sh.hist[cand[c] & 1023], 1u);
   } else {
     sweep([&](uint32_t key) {
       if ((key >> 10) == p2) atomicAdd(&sh.hist[key & 1023], 1u);

@@ -163,6 +163,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
     const int qd = warp & 3;      // TMEM lane quarter
     const int half = e8 >> 2;     // columns [128 half, 128 half + 128): tokens 32 half ..
     const uint32_t lanef = (uint32_t)(qd * 32) << 16;
+    const uint64_t keep = l2_evict_last_policy();  // read back by the select
     for (int i = 0; i < n_tiles; ++i) {
       const int buf = i & 1;
       if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&bars->tfull[buf], (i >> 1) & 1, kGWait))) {
@@ -184,7 +185,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
                            wq[1] * fmaxf(__uint_as_float(v[4 * j + 1]), 0.f) +
                            wq[2] * fmaxf(__uint_as_float(v[4 * j + 2]), 0.f) +
                            wq[3] * fmaxf(__uint_as_float(v[4 * j + 3]), 0.f);
-          if (e < a.N_cap) scores[(int64_t)(qb * kGQ + tq) * stride + e] = sc;
+          if (e < a.N_cap) st_f32_policy(scores + (int64_t)(qb * kGQ + tq) * stride + e, sc, keep);
         }
       }
       tc::fence_before_sync();

@@ -326,6 +326,34 @@ def test_topk_dense_threshold_bin_many_queries(cuda_device, n_levels):
     np.testing.assert_array_equal(idx, ref)  # exact: ties resolved by index
 
 
+@pytest.mark.parametrize("sampled", ["low", "high"])
+def test_topk_stream_skewed_sample(cuda_device, sampled):
+    # the one-CTA-per-query select first bounds the list from an evenly spaced
+    # sample of 16-byte score vectors (entries 16 i .. 16 i + 3 at 20000
+    # visible entries).  Scores that give the sampled entries the smallest
+    # ("low": far more than the list holds lie above the sample's bound) or
+    # the largest values ("high": fewer than k lie above it) send every query
+    # to the histogram passes; the selection stays exact
+    T, N_cap, m, k = 160, 20000, 4, 1500
+    qi = torch.zeros((1, T, 4, 64), dtype=torch.bfloat16)
+    qi[:, :, 0, 0] = 1.0
+    g = torch.Generator().manual_seed(21)
+    ki = synth.randn((1, N_cap, 64), 6, 3)
+    val = 1.0 + torch.rand((1, N_cap), generator=g)
+    in_sample = (torch.arange(N_cap) % 16) < 4  # 5000 entries, about 4100 of them sampled
+    low = 0.25 + torch.rand((1, N_cap), generator=g) / 8
+    high = 3.0 + torch.rand((1, N_cap), generator=g)
+    val[:, in_sample] = (low if sampled == "low" else high)[:, in_sample]
+    ki[:, :, 0] = val.to(torch.bfloat16)
+    w = torch.tensor([1.0, 0.0, 0.0, 0.0]).repeat(1, T, 1)
+    qp = torch.tensor([[N_cap * m - 1 - 3 * (T - 1 - t) for t in range(T)]], dtype=torch.int32)
+    nc = torch.tensor([N_cap], dtype=torch.int32)
+    case = (qi, None, ki, None, w, qp, nc)
+    idx, _ = _run_indexer(*case, m, k)
+    s, nv, ref = _oracle_indexer(*case, m, k, False)
+    np.testing.assert_array_equal(idx, ref)  # exact: ties resolved by index
+
+
 def test_topk_zero_scores_and_short_lists(cuda_device):
     # n_vis below k (every visible entry, -1 padded), n_vis == 0, and a query
     # whose scores are mostly exactly zero (negative dot products)
