@@ -248,14 +248,20 @@ __device__ __forceinline__ void merge_from_global(const AttnArgs& a, int qid, in
   const float* plse = a.part_lse + (int64_t)qid * ns * H;  // split s, head h at s * H + h
   for (int hl = tid; hl < nh; hl += kThreads) {
     const int h = h0 + hl;
+    // every split's lse at once (one round trip to L2)
+    float ls[kMaxCluster];
+#pragma unroll
+    for (int s = 0; s < kMaxCluster; ++s) ls[s] = s < ns ? __ldcg(plse + s * H + h) : -INFINITY;
     float Mx = a.sink ? sink_s[h] : -INFINITY;
-    for (int s = 0; s < ns; ++s) Mx = fmaxf(Mx, __ldcg(plse + s * H + h));
+#pragma unroll
+    for (int s = 0; s < kMaxCluster; ++s) Mx = fmaxf(Mx, ls[s]);
     float lse = -INFINITY;
     if (Mx != -INFINITY) {
       float Z = a.sink ? ex2_approx((sink_s[h] - Mx) * kLog2e) : 0.f;
-      for (int s = 0; s < ns; ++s) {
-        const float ls = __ldcg(plse + s * H + h);
-        const float w = ls == -INFINITY ? 0.f : ex2_approx((ls - Mx) * kLog2e);
+#pragma unroll
+      for (int s = 0; s < kMaxCluster; ++s) {
+        if (s >= ns) break;
+        const float w = ls[s] == -INFINITY ? 0.f : ex2_approx((ls[s] - Mx) * kLog2e);
         wgt[hl * ns + s] = w;
         Z += w;
       }
@@ -1031,13 +1037,56 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(AttnArgs a) {
   const float* lse_p = a.part_lse + (int64_t)qid * ns * H + h;  // split s at s * H
   const float4* row = reinterpret_cast<const float4*>(a.part_o + ((int64_t)qid * ns * H + h) * kD);
   const int64_t rstride = (int64_t)H * kD / 4;  // float4s between splits
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float lse = -INFINITY;
+  if (ns <= 32) {
+    // lane j holds split j's lse; the first kRows splits' rows are loaded at
+    // the same time (one round trip for both), the rest kRows at a time
+    constexpr int kRows = 16;
+    const float ls = lane < ns ? lse_p[(int64_t)lane * H] : -INFINITY;
+    float4 v[kRows];
+#pragma unroll
+    for (int j = 0; j < kRows; ++j)
+      v[j] = j < ns ? row[j * rstride + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+    float Mx = fmaxf(sink_h, ls);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) Mx = fmaxf(Mx, __shfl_xor_sync(0xFFFFFFFFu, Mx, o));
+    if (Mx != -INFINITY) {
+      const float wl = ls == -INFINITY ? 0.f : expf(ls - Mx);
+      float zl = wl;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) zl += __shfl_xor_sync(0xFFFFFFFFu, zl, o);
+      const float Z = zl + (a.sink ? expf(sink_h - Mx) : 0.f);
+      const float inv = 1.f / Z;
+      for (int s0 = 0; s0 < ns; s0 += kRows) {
+        if (s0 > 0) {
+#pragma unroll
+          for (int j = 0; j < kRows; ++j)
+            v[j] = s0 + j < ns ? row[(s0 + j) * rstride + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int j = 0; j < kRows; ++j) {
+          const float w = __shfl_sync(0xFFFFFFFFu, wl, (s0 + j) & 31) * inv;
+          if (s0 + j < ns) {
+            acc.x += w * v[j].x;
+            acc.y += w * v[j].y;
+            acc.z += w * v[j].z;
+            acc.w += w * v[j].w;
+          }
+        }
+      }
+      lse = Mx + logf(Z);
+    }
+    reinterpret_cast<uint2*>(a.out + ((int64_t)qid * H + h) * kD)[lane] =
+        make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+    if (lane == 0 && a.lse) a.lse[(int64_t)qid * H + h] = lse;
+    return;
+  }
   // the splits' lse values, all lanes at once (lane j holds splits j, j + 32, ..)
   float Mx = sink_h;
   for (int s = lane; s < ns; s += 32) Mx = fmaxf(Mx, lse_p[(int64_t)s * H]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) Mx = fmaxf(Mx, __shfl_xor_sync(0xFFFFFFFFu, Mx, o));
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float lse = -INFINITY;
   if (Mx != -INFINITY) {
     float zl = 0.f;  // this lane's share of Z
     for (int s = lane; s < ns; s += 32) {

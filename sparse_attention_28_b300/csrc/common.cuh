@@ -45,6 +45,20 @@ __device__ __forceinline__ void st_f32_policy(float* addr, float v, uint64_t pol
   asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;\n" ::"l"(addr), "f"(v), "l"(pol)
                : "memory");
 }
+// Read-only loads of data streamed once (the indexer keys) with an L2
+// eviction policy.
+__device__ __forceinline__ uint4 ldg_u32x4_policy(const void* addr, uint64_t pol) {
+  uint4 r;
+  asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;\n"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(addr), "l"(pol));
+  return r;
+}
+__device__ __forceinline__ uint32_t ldg_u32_policy(const void* addr, uint64_t pol) {
+  uint32_t r;
+  asm volatile("ld.global.nc.L2::cache_hint.u32 %0, [%1], %2;\n" : "=r"(r) : "l"(addr), "l"(pol));
+  return r;
+}
 __device__ __forceinline__ float4 ld_f32x4_policy(const float4* addr, uint64_t pol) {
   float4 r;
   asm volatile("ld.global.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;\n"

@@ -194,6 +194,8 @@ __device__ __forceinline__ void score_range(const IndexerArgs& a, int qid, int64
   const int b = qid / a.T;
   constexpr int kUnroll = FMT == 0 ? kUnrollBf16 : FMT == 1 ? kUnrollFp8 : kUnrollFp4;
   const int n_groups = (int)((e1 - e0 + 15) / 16);
+  // the keys are read once; the scores are read back by the select
+  const uint64_t once = l2_evict_first_policy(), keep = l2_evict_last_policy();
   for (int gb = warp * kUnroll; gb < n_groups; gb += (kThreads / 32) * kUnroll) {
     uint4 ra[kUnroll][2], rb[kUnroll][2];  // rows g and g+8 of each group
     float ks[kUnroll];                      // E4M3: scale of the entry this thread scores
@@ -208,30 +210,28 @@ __device__ __forceinline__ void score_range(const IndexerArgs& a, int qid, int64
         ra[u][0] = z;
         rb[u][0] = z;
         if (ea < e1) {
-          ra[u][0].x = __ldg(reinterpret_cast<const uint32_t*>(kb + ea * (kDI / 2) + 4 * c));
-          ra[u][0].y = __ldg(reinterpret_cast<const uint32_t*>(kb + ea * (kDI / 2) + 16 + 4 * c));
+          ra[u][0].x = ldg_u32_policy(kb + ea * (kDI / 2) + 4 * c, once);
+          ra[u][0].y = ldg_u32_policy(kb + ea * (kDI / 2) + 16 + 4 * c, once);
           ra[u][0].z = __ldg(sb + ea);
         }
         if (eb < e1) {
-          rb[u][0].x = __ldg(reinterpret_cast<const uint32_t*>(kb + eb * (kDI / 2) + 4 * c));
-          rb[u][0].y = __ldg(reinterpret_cast<const uint32_t*>(kb + eb * (kDI / 2) + 16 + 4 * c));
+          rb[u][0].x = ldg_u32_policy(kb + eb * (kDI / 2) + 4 * c, once);
+          rb[u][0].y = ldg_u32_policy(kb + eb * (kDI / 2) + 16 + 4 * c, once);
           rb[u][0].z = __ldg(sb + eb);
         }
       } else if (FP8) {
         const int64_t es = c == 1 ? eb : ea;
         ks[u] = (c < 2 && es < e1) ? __ldg(a.k_scale + (int64_t)b * a.ks_bstride + es) : 0.f;
         const uint8_t* kb = reinterpret_cast<const uint8_t*>(a.keys) + (int64_t)b * a.k_bstride;
-        ra[u][0] = ea < e1 ? __ldg(reinterpret_cast<const uint4*>(kb + ea * kDI + 16 * c))
-                           : make_uint4(0, 0, 0, 0);
-        rb[u][0] = eb < e1 ? __ldg(reinterpret_cast<const uint4*>(kb + eb * kDI + 16 * c))
-                           : make_uint4(0, 0, 0, 0);
+        ra[u][0] = ea < e1 ? ldg_u32x4_policy(kb + ea * kDI + 16 * c, once) : make_uint4(0, 0, 0, 0);
+        rb[u][0] = eb < e1 ? ldg_u32x4_policy(kb + eb * kDI + 16 * c, once) : make_uint4(0, 0, 0, 0);
       } else {
         const bf16* kb = reinterpret_cast<const bf16*>(a.keys) + (int64_t)b * a.k_bstride;
         const uint4 z = make_uint4(0, 0, 0, 0);
-        ra[u][0] = ea < e1 ? __ldg(reinterpret_cast<const uint4*>(kb + ea * kDI + 8 * c)) : z;
-        ra[u][1] = ea < e1 ? __ldg(reinterpret_cast<const uint4*>(kb + ea * kDI + 32 + 8 * c)) : z;
-        rb[u][0] = eb < e1 ? __ldg(reinterpret_cast<const uint4*>(kb + eb * kDI + 8 * c)) : z;
-        rb[u][1] = eb < e1 ? __ldg(reinterpret_cast<const uint4*>(kb + eb * kDI + 32 + 8 * c)) : z;
+        ra[u][0] = ea < e1 ? ldg_u32x4_policy(kb + ea * kDI + 8 * c, once) : z;
+        ra[u][1] = ea < e1 ? ldg_u32x4_policy(kb + ea * kDI + 32 + 8 * c, once) : z;
+        rb[u][0] = eb < e1 ? ldg_u32x4_policy(kb + eb * kDI + 8 * c, once) : z;
+        rb[u][1] = eb < e1 ? ldg_u32x4_policy(kb + eb * kDI + 32 + 8 * c, once) : z;
       }
     }
 #pragma unroll
@@ -276,7 +276,7 @@ __device__ __forceinline__ void score_range(const IndexerArgs& a, int qid, int64
       float sc = c == 1 ? sb : sa;
       if (c < 2 && e < e1) {
         if (FP8) sc *= ks[u];
-        scores[e] = sc;
+        st_f32_policy(scores + e, sc, keep);
       }
     }
   }
