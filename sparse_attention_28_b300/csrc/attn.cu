@@ -35,8 +35,11 @@
 //                P V of tile t-1 still runs.
 // FP8-stored entries (KV8 = true, csa_attn_fp8kv): the loaders copy each
 // stage's E4M3 codes, scales and bf16 RoPE channels to a staging slot and,
-// two stages later, decode them into the ring's bf16 rows (code * scale,
-// nearest even); the rest of the kernel is the same.
+// two stages later, decode them into the ring: K's rows as bf16 (code *
+// scale, nearest even), V's rows as their exact f16 codes, unscaled.  The
+// softmax adds log2 of each key's V scale to its logit, so P (f16 here)
+// carries the scale into P V, and divides it out of the row sums; the raw
+// window rows' V is converted to f16 in place (scale 1).
 // Separate S and P V issuers keep the tensor pipe fed while either one waits
 // on a barrier.  Every mbarrier wait is bounded; on timeout the CTA records
 // CSA_EW_TIMEOUT in the error word, still reaches every barrier, and frees its
@@ -99,7 +102,10 @@ struct Cfg {
   static constexpr int kPOff = kV1 + kRegion;
   static constexpr int kMetaOff = kPOff + kPBytes;  // stages x 64 row codes
   static constexpr int kS8Off = kMetaOff + kStages * kStageKeys * 4;
-  static constexpr int kBarOff = kS8Off + (KV8 ? kS8Slots * kS8Bytes : 0);
+  // KV8: log2 of each key's V scale, per ring stage (the softmax folds the
+  // scale into P; V enters the tensor cores as its exact f16 codes)
+  static constexpr int kSvOff = kS8Off + (KV8 ? kS8Slots * kS8Bytes : 0);
+  static constexpr int kBarOff = kSvOff + (KV8 ? kStages * kStageKeys * 4 : 0);
   static constexpr int kSmemBytes = kBarOff + 512 + 1024;  // + alignment slack
   // after the main loop: own partial O rows (fp32) over the K regions, rows
   // received from the cluster over the V regions (and P); lse values and
@@ -217,6 +223,20 @@ __device__ __forceinline__ uint4 dequant8(uint2 c, float sc) {
     w[h] = pack_bf16x2(f.x * sc, f.y * sc);
   }
   return make_uint4(w[0], w[1], w[2], w[3]);
+}
+// Eight E4M3 codes (c.x low byte first) as eight f16, exact (no scale).
+__device__ __forceinline__ uint4 e4m3x8_to_f16x8(uint2 c) {
+  return make_uint4(e4m3x2_to_f16x2((uint16_t)c.x), e4m3x2_to_f16x2((uint16_t)(c.x >> 16)),
+                    e4m3x2_to_f16x2((uint16_t)c.y), e4m3x2_to_f16x2((uint16_t)(c.y >> 16)));
+}
+// Eight bf16 as eight f16 (nearest even).
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int h = 0; h < 4; ++h)
+    o[h] = pack_f16x2(__uint_as_float(w[h] << 16), __uint_as_float(w[h] & 0xFFFF0000u));
+  return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 template <int M>
@@ -361,7 +381,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_init(&bars->kv_full[p], 2 * kLoadThreads);
       tc::mbar_init(&bars->pair_empty[p], 1);
     }
-    for (int i = 0; i < 4; ++i) tc::mbar_init(&bars->meta_full[i], 1);
+    // KV8: every code thread arrives once per stage, after its key's V scale
+    for (int i = 0; i < 4; ++i) tc::mbar_init(&bars->meta_full[i], KV8 ? 2 * kStageKeys : 1);
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&bars->s_full[i], 1);
       tc::mbar_init(&bars->s_free[i], kSoftThreads / 32);  // one arrival per softmax warp
@@ -435,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (n_tiles > 0 && warp == 1) {
     // ------------------------------------------------------------ P V issuer
     if (lane == 0) {
-      const uint32_t id_o = tc::idesc_bf16(M, kD, false, true);
+      const uint32_t id_o = KV8 ? tc::idesc_f16(M, kD, false, true) : tc::idesc_bf16(M, kD, false, true);
       bool ok = true;
       for (int j = 0; j < n_tiles && ok; ++j) {
         const int pr = j % kPairs;
@@ -603,31 +624,52 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* ksc = reinterpret_cast<const float*>(stg + kS8KS);
       const float* vsc = reinterpret_cast<const float*>(stg + kS8VS);
       const uint32_t off = st * kBlk;
-      // 24 output chunks per row: 8 of K's non-RoPE channels, 16 of V; each
-      // thread loads all of its chunks' codes first, then converts and stores
-      // them (independent work for the few loader warps of each scheduler)
-      constexpr int kPer = kStageKeys * 24 / NL;
-      static_assert(kStageKeys * 24 % NL == 0, "decode chunks per loader thread");
-      uint2 c8[kPer];
-      float scv[kPer];
-      uint32_t dst[kPer];
-      bool use[kPer];
+      // Output chunks of 8 channels: 8 per row of K's non-RoPE channels
+      // (code * scale -> bf16), 16 per row of V (code -> f16, or a raw row's
+      // bf16 -> f16 in place).  The K chunks and the V chunks are separate
+      // loops, so that a warp's lanes take the same path; each thread loads
+      // all of a loop's codes first, then converts and stores them.
+      constexpr int kPerK = (kStageKeys * 8 + NL - 1) / NL;
+      constexpr int kPerV = (kStageKeys * 16 + NL - 1) / NL;
+      {
+        uint2 c8[kPerK];
+        float scv[kPerK];
 #pragma unroll
-      for (int i = 0; i < kPer; ++i) {
-        const int oc = lt + i * NL;
-        const int r = oc / 24, part = oc - r * 24;
-        const int v = part - 8;
-        const bool isk = part < 8;
-        use[i] = codes[st * kStageKeys + r] >= 0;  // rows of other kinds are in place
-        c8[i] = *reinterpret_cast<const uint2*>(stg + (isk ? kS8K + r * 64 + part * 8
-                                                           : kS8V + r * 128 + v * 8));
-        scv[i] = isk ? ksc[r] : vsc[r];
-        dst[i] = isk ? C::kK0 + off + tc::sw128_offset(r, part)
-                     : C::kV0 + off + (v >> 3) * C::kRegion + tc::sw128_offset(r, v & 7);
+        for (int i = 0; i < kPerK; ++i) {
+          const int oc = lt + i * NL;
+          const int r = (oc >> 3) & (kStageKeys - 1), part = oc & 7;
+          c8[i] = *reinterpret_cast<const uint2*>(stg + kS8K + r * 64 + part * 8);
+          scv[i] = ksc[r];
+        }
+#pragma unroll
+        for (int i = 0; i < kPerK; ++i) {
+          const int oc = lt + i * NL;
+          const int r = oc >> 3, part = oc & 7;
+          if (oc < kStageKeys * 8 && codes[st * kStageKeys + r] >= 0)
+            *reinterpret_cast<uint4*>(sm + C::kK0 + off + tc::sw128_offset(r, part)) =
+                dequant8(c8[i], scv[i]);
+        }
       }
+      {
+        uint2 c8[kPerV];
 #pragma unroll
-      for (int i = 0; i < kPer; ++i)
-        if (use[i]) *reinterpret_cast<uint4*>(sm + dst[i]) = dequant8(c8[i], scv[i]);
+        for (int i = 0; i < kPerV; ++i) {
+          const int oc = lt + i * NL;
+          const int r = (oc >> 4) & (kStageKeys - 1), v = oc & 15;
+          c8[i] = *reinterpret_cast<const uint2*>(stg + kS8V + r * 128 + v * 8);
+        }
+#pragma unroll
+        for (int i = 0; i < kPerV; ++i) {
+          const int oc = lt + i * NL;
+          const int r = oc >> 4, v = oc & 15;
+          if (oc >= kStageKeys * 16) break;
+          const int32_t cd = codes[st * kStageKeys + r];
+          uint4* d = reinterpret_cast<uint4*>(sm + C::kV0 + off + (v >> 3) * C::kRegion +
+                                              tc::sw128_offset(r, v & 7));
+          if (cd >= 0) *d = e4m3x8_to_f16x8(c8[i]);
+          else if (cd < -1) *d = bf16x8_to_f16x8(*d);
+        }
+      }
       // K's RoPE channels of the compressed rows: same swizzled offsets
 #pragma unroll
       for (int i = 0; i < (kStageKeys * 8 + NL - 1) / NL; ++i) {
@@ -638,8 +680,16 @@ __global__ void __launch_bounds__(kThreads, 1)
               *reinterpret_cast<const uint4*>(stg + kS8R + o);
         }
       }
+      // log2 of the key's V scale (0 for raw rows, skipped slots and zero scales)
+      if (lt < kStageKeys) {
+        const float sv = codes[st * kStageKeys + lt] >= 0 ? vsc[lt] : 1.f;
+        reinterpret_cast<float*>(sm + C::kSvOff)[st * kStageKeys + lt] =
+            sv > 0.f ? __log2f(sv) : 0.f;
+      }
       tc::fence_proxy_async_smem();
       tc::mbar_arrive(&bars->kv_full[pr]);
+      // the stage's validity bits and V scales are published for the softmax
+      if (lt < kStageKeys) tc::mbar_arrive(&bars->meta_full[(s8 >> 1) & 3]);
     };
     for (int j = j_fast; j < n_stages; ++j) {
       const int st = j % kStages, pr = (j >> 1) % kPairs;
@@ -673,7 +723,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                               codes[st * kStageKeys + 32] == base + 32;
       const bool all_cmp = (bars->cmp[j & 7][0] & bars->cmp[j & 7][1]) == 0xFFFFFFFFu;
       const bool dense = !KV8 && dense_rows;
-      if (lt == 0 && (j & 1)) tc::mbar_arrive(&bars->meta_full[(j >> 1) & 3]);  // both stages
+      if (!KV8 && lt == 0 && (j & 1)) tc::mbar_arrive(&bars->meta_full[(j >> 1) & 3]);  // both stages
       const uint32_t off = st * kBlk;
       if constexpr (KV8) {
         kv8_issue(j, dense_rows, all_cmp);
@@ -744,6 +794,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       l_sum[g][0] = l_sum[g][1] = 0.f;
     }
     uint8_t* pbuf = sm + C::kPOff;
+    // KV8: log2 V scale of key 32q + 8u + 2c4 of tile j (stage 2j + q/2)
+    const float* svp = reinterpret_cast<const float*>(sm + C::kSvOff);
+    auto sv_col = [&](int j, int q, int u) {
+      return ((2 * j + (q >> 1)) % kStages) * kStageKeys + 32 * (q & 1) + 8 * u + 2 * c4;
+    };
     for (int j = 0; j < n_tiles; ++j) {
       const int sb = j & 1;
       // waits are made warp-uniform: tcgen05.ld/st below are warp-collective
@@ -775,16 +830,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int q = 0; q < 4; ++q)
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
+          for (int u = 0; u < 4; ++u) {
+            // KV8: log2 of the V scales of keys 32q + 8u + 2c4 (+1), added to
+            // their logits so that P carries them (V is the raw codes)
+            float2 lv = make_float2(0.f, 0.f);
+            if constexpr (KV8) lv = *reinterpret_cast<const float2*>(svp + sv_col(j, q, u));
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               const int bit = 8 * u + 2 * c4 + (k & 1);
               const int i = q * 16 + u * 4 + k;
-              const float x =
-                  ((vm[q] >> bit) & 1u) ? __uint_as_float(sr[i]) * a.scale_log2 : -INFINITY;
+              const float x = ((vm[q] >> bit) & 1u)
+                                  ? __uint_as_float(sr[i]) * a.scale_log2 + ((k & 1) ? lv.y : lv.x)
+                                  : -INFINITY;
               sr[i] = __float_as_uint(x);
               mt[k >> 1] = fmaxf(mt[k >> 1], x);
             }
+          }
         // lazy rescaling: a row's reference max moves only when the tile max
         // exceeds it by more than 2^8 (or on its first finite tile)
         float f[2];
@@ -810,10 +871,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float p1 = ex2_approx(__uint_as_float(sr[4 * i + 1]) - mA);
           const float p2 = ex2_approx(__uint_as_float(sr[4 * i + 2]) - mB);
           const float p3 = ex2_approx(__uint_as_float(sr[4 * i + 3]) - mB);
-          l_sum[g][0] += p0 + p1;
-          l_sum[g][1] += p2 + p3;
-          pk[2 * i] = pack_bf16x2(p0, p1);
-          pk[2 * i + 1] = pack_bf16x2(p2, p3);
+          if constexpr (KV8) {
+            // the row sums exclude the V scales: weights p / scale
+            const float2 lv = *reinterpret_cast<const float2*>(svp + sv_col(j, i >> 2, i & 3));
+            const float i0 = ex2_approx(-lv.x), i1 = ex2_approx(-lv.y);
+            l_sum[g][0] += p0 * i0 + p1 * i1;
+            l_sum[g][1] += p2 * i0 + p3 * i1;
+            pk[2 * i] = pack_f16x2(p0, p1);
+            pk[2 * i + 1] = pack_f16x2(p2, p3);
+          } else {
+            l_sum[g][0] += p0 + p1;
+            l_sum[g][1] += p2 + p3;
+            pk[2 * i] = pack_bf16x2(p0, p1);
+            pk[2 * i + 1] = pack_bf16x2(p2, p3);
+          }
         }
         // the P buffer and O are free once P V of tile j-1 has completed
         if (g == 0 && j >= 1) {
