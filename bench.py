@@ -324,6 +324,58 @@ def time_oracle(runner, budget_s: float):
             return reps * runner.n / el, reps, el
 
 
+# ---------------------------------------------------------------- feed probes
+
+def run_probes(dev, l2_bytes: int):
+    """`--probe`: the read rates behind the kernels' rooflines, one JSON line
+    each (mean of 10 timed launches after 3 warm-up ones, L2 flushed clean
+    before each).  (1) a contiguous stream read once, the size of the
+    csa_decode_128k indexer keys (134 MB), for several CTAs per SM and loads
+    in flight; (2) 512-byte row gathers into shared memory from an L2-resident
+    table of the csa_prefill_4k caches' size (43 MB: 88,000 rows), 4096 CTAs x
+    34 stages x 64 rows like the prefill attention, for ring depths of 2, 4
+    and 6 stages (3, 1 and 1 CTAs per SM by shared memory)."""
+    import sparse_attention_28_b300 as csa
+    flush = L2Flush(l2_bytes, dev)
+    sink = torch.zeros(1, dtype=torch.float32, device=dev)
+
+    def timed(fn, flush_each=True):
+        for _ in range(3):
+            fn()
+        ms = []
+        for _ in range(10):
+            if flush_each:
+                flush()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize(dev)
+            ms.append(a.elapsed_time(b))
+        return sum(ms) / len(ms)
+
+    keys = torch.zeros(32 * 32768 * 128, dtype=torch.uint8, device=dev)
+    for cps in (1, 2, 3):
+        for k in (1, 4, 8):
+            ms = timed(lambda: csa.probe_stream_read(keys, sink, cps, k))
+            print(json.dumps({"probe": "stream_read", "bytes": keys.numel(), "ctas_per_sm": cps,
+                              "in_flight": k, "us": round(ms * 1e3, 2),
+                              "GB/s": round(keys.numel() / ms / 1e6, 1)}), flush=True)
+    del keys
+    n_rows, ctas, stages = 88000, 4096, 34
+    table = torch.zeros((n_rows, 512), dtype=torch.uint8, device=dev)
+    g = torch.Generator(device="cpu").manual_seed(1)
+    idx = torch.randint(0, n_rows, (ctas * stages * 64,), generator=g, dtype=torch.int32).to(dev)
+    moved = ctas * stages * 64 * 512
+    for ring in (2, 4, 6):
+        # the table stays in L2 between launches: no flush
+        ms = timed(lambda: csa.probe_row_gather(table, idx, ctas, stages, ring, sink),
+                   flush_each=False)
+        print(json.dumps({"probe": "row_gather", "rows": n_rows, "row_bytes": 512, "ctas": ctas,
+                          "stages": stages, "ring": ring, "us": round(ms * 1e3, 1),
+                          "GB/s": round(moved / ms / 1e6, 1)}), flush=True)
+
+
 # ---------------------------------------------------------------- main
 
 def main():
@@ -336,6 +388,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--probe", action="store_true",
+                    help="time the feed probes (stream read, row gathers) instead of a step")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -374,6 +428,9 @@ def main():
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
     csa.lib()  # fail loudly now if the library is missing
+    if args.probe:
+        run_probes(dev, torch.cuda.get_device_properties(dev).L2_cache_size)
+        return
 
     inp = synth.make_inputs(wl, seed=args.seed + 7919 * rank, device=dev)
     step = make_step(inp, dev)

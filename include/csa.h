@@ -362,6 +362,33 @@ CSA_API int csa_selftest_bounded_wait(int arrive, uint32_t limit, int32_t* err_w
                                       void* stream);
 
 /* ------------------------------------------------------------------------
+ * Feed probes (measurement only: nothing of the method).  They time the two
+ * ways the hot path reads memory, for the rooflines the kernels are judged
+ * against: a contiguous stream read once (the indexer keys) and 512-byte row
+ * gathers into shared memory (the attention's top-k K/V rows).
+ *
+ * csa_probe_stream_read: 148 * ctas_per_sm CTAs (1..4) of 512 threads each
+ *   read an equal contiguous share of src with 16-byte loads, in_flight
+ *   (1, 4 or 8) loads per thread issued before any is used.  src: device,
+ *   16-byte aligned, `bytes` readable (the remainder below one vector per
+ *   CTA is not read).  sink: device float, written only if the XOR of all
+ *   data read equals a fixed constant (it is there so that the loads stay).
+ * csa_probe_row_gather: n_ctas CTAs of 256 threads; CTA c reads `stages`
+ *   stages of 64 rows of 512 bytes, row r of stage s at index
+ *   idx[(c * stages + s) * 64 + r] of the table (n_rows rows; indices are
+ *   clamped into [0, n_rows)), with 16-byte cp.async copies into a ring of
+ *   `ring` (2, 4 or 6) stages of 32 KB of shared memory and a block barrier
+ *   per stage.  table: device, 16-byte aligned; idx: device int32, n_ctas *
+ *   stages * 64 entries; sink as above.
+ * Both return CSA_OK, CSA_ERR_INVALID_ARG (checked before any launch) or
+ * CSA_ERR_CUDA; they are asynchronous on `stream`.
+ * ---------------------------------------------------------------------- */
+CSA_API int csa_probe_stream_read(const void* src, int64_t bytes, int ctas_per_sm, int in_flight,
+                                  float* sink, void* stream);
+CSA_API int csa_probe_row_gather(const void* table, int64_t n_rows, const int32_t* idx, int n_ctas,
+                                 int stages, int ring, float* sink, void* stream);
+
+/* ------------------------------------------------------------------------
  * a4 / a5 / a6. Attention over compressed entries + window + sink.
  *
  * Sources: hyper.ai DeepSeek-V4 page, Method (MQA core attention with shared

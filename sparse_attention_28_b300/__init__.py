@@ -42,7 +42,7 @@ ABI_SYMBOLS = (
     "csa_sparse_attn_prefill", "hca_dense_attn_decode", "csa_indexer_topk_static",
     "csa_indexer_scores", "csa_compress_kv_span", "csa_sparse_attn_batch_invariant",
     "csa_grouped_out_proj", "csa_compress_kv_mixed", "csa_attn_fp8kv",
-    "csa_selftest_bounded_wait",
+    "csa_selftest_bounded_wait", "csa_probe_stream_read", "csa_probe_row_gather",
 )
 
 # capacity of the library-owned scratch behind indexer_topk_static (bytes)
@@ -114,6 +114,10 @@ def lib() -> ctypes.CDLL:
             L.csa_attn_fp8kv.restype = I
             L.csa_selftest_bounded_wait.argtypes = [I, ctypes.c_uint32, P, P]
             L.csa_selftest_bounded_wait.restype = I
+            L.csa_probe_stream_read.argtypes = [P, I64, I, I, P, P]
+            L.csa_probe_stream_read.restype = I
+            L.csa_probe_row_gather.argtypes = [P, I64, P, I, I, I, P, P]
+            L.csa_probe_row_gather.restype = I
             _lib = L
     return _lib
 
@@ -558,3 +562,30 @@ def grouped_out_proj(o, W, out=None, err_word=None):
     _check(st, "csa_grouped_out_proj")
     return y
 
+
+
+# ---------------------------------------------------------------- feed probes
+
+def probe_stream_read(src, sink, ctas_per_sm: int = 2, in_flight: int = 4):
+    """Stream-read every byte of the CUDA tensor src (16-byte loads, in_flight
+    per thread before any is used, 148 * ctas_per_sm CTAs).  sink: a float32
+    CUDA tensor of one element.  Asynchronous on the current stream."""
+    _need(src.is_cuda and src.is_contiguous(), "src: contiguous CUDA tensor")
+    _cuda(sink, "sink", torch.float32)
+    st = lib().csa_probe_stream_read(_p(src), src.numel() * src.element_size(), int(ctas_per_sm),
+                                     int(in_flight), _p(sink), _stream(src.device))
+    _check(st, "csa_probe_stream_read")
+
+
+def probe_row_gather(table, idx, n_ctas: int, stages: int, ring: int, sink):
+    """Gather 512-byte rows of table (uint8 CUDA tensor [n_rows, 512]) into
+    shared memory: CTA c reads idx[c * stages * 64: (c + 1) * stages * 64]
+    (int32, 64 rows per stage) through a ring of `ring` 32 KB stages."""
+    _need(table.is_cuda and table.is_contiguous() and table.dim() == 2 and table.shape[1] == 512,
+          "table: contiguous CUDA [n_rows, 512]")
+    _cuda(idx, "idx", torch.int32)
+    _need(idx.is_contiguous() and idx.numel() >= n_ctas * stages * 64, "idx: n_ctas * stages * 64")
+    _cuda(sink, "sink", torch.float32)
+    st = lib().csa_probe_row_gather(_p(table), table.shape[0], _p(idx), int(n_ctas), int(stages),
+                                    int(ring), _p(sink), _stream(table.device))
+    _check(st, "csa_probe_row_gather")

@@ -239,6 +239,28 @@ def test_selftest_bounded_wait_rejects():
     assert L.csa_selftest_bounded_wait(0, (1 << 20) + 1, FAKE, None) == 1
 
 
+def test_probe_rejects():
+    # invalid arguments are refused on the host, before any CUDA call
+    L = csa.lib()
+    odd = ctypes.c_void_p(0x10008)  # not 16-byte aligned
+    assert L.csa_probe_stream_read(None, 1 << 20, 2, 4, FAKE, None) == 1
+    assert L.csa_probe_stream_read(FAKE, 1 << 20, 2, 4, None, None) == 1
+    assert L.csa_probe_stream_read(odd, 1 << 20, 2, 4, FAKE, None) == 1
+    assert L.csa_probe_stream_read(FAKE, 0, 2, 4, FAKE, None) == 1
+    assert L.csa_probe_stream_read(FAKE, 1 << 20, 0, 4, FAKE, None) == 1
+    assert L.csa_probe_stream_read(FAKE, 1 << 20, 5, 4, FAKE, None) == 1
+    assert L.csa_probe_stream_read(FAKE, 1 << 20, 2, 3, FAKE, None) == 1
+    assert L.csa_probe_stream_read(FAKE, 16, 2, 4, FAKE, None) == 1  # under one vector per CTA
+    assert L.csa_probe_row_gather(None, 100, FAKE, 1, 1, 2, FAKE, None) == 1
+    assert L.csa_probe_row_gather(FAKE, 100, None, 1, 1, 2, FAKE, None) == 1
+    assert L.csa_probe_row_gather(FAKE, 100, FAKE, 1, 1, 2, None, None) == 1
+    assert L.csa_probe_row_gather(odd, 100, FAKE, 1, 1, 2, FAKE, None) == 1
+    assert L.csa_probe_row_gather(FAKE, 0, FAKE, 1, 1, 2, FAKE, None) == 1
+    assert L.csa_probe_row_gather(FAKE, 100, FAKE, 0, 1, 2, FAKE, None) == 1
+    assert L.csa_probe_row_gather(FAKE, 100, FAKE, 1, 0, 2, FAKE, None) == 1
+    assert L.csa_probe_row_gather(FAKE, 100, FAKE, 1, 1, 3, FAKE, None) == 1
+
+
 def test_compress_mixed_rejects():
     L = csa.lib()
 
