@@ -334,7 +334,8 @@ def run_probes(dev, l2_bytes: int):
     in flight; (2) 512-byte row gathers into shared memory from an L2-resident
     table of the csa_prefill_4k caches' size (43 MB: 88,000 rows), 4096 CTAs x
     34 stages x 64 rows like the prefill attention, for ring depths of 2, 4
-    and 6 stages (3, 1 and 1 CTAs per SM by shared memory)."""
+    and 6 stages (3, 1 and 1 CTAs per SM by shared memory), with 16-byte
+    cp.async copies and with TMA tile::gather4."""
     import sparse_attention_28_b300 as csa
     flush = L2Flush(l2_bytes, dev)
     sink = torch.zeros(1, dtype=torch.float32, device=dev)
@@ -367,13 +368,18 @@ def run_probes(dev, l2_bytes: int):
     g = torch.Generator(device="cpu").manual_seed(1)
     idx = torch.randint(0, n_rows, (ctas * stages * 64,), generator=g, dtype=torch.int32).to(dev)
     moved = ctas * stages * 64 * 512
-    for ring in (2, 4, 6):
-        # the table stays in L2 between launches: no flush
-        ms = timed(lambda: csa.probe_row_gather(table, idx, ctas, stages, ring, sink),
-                   flush_each=False)
-        print(json.dumps({"probe": "row_gather", "rows": n_rows, "row_bytes": 512, "ctas": ctas,
-                          "stages": stages, "ring": ring, "us": round(ms * 1e3, 1),
-                          "GB/s": round(moved / ms / 1e6, 1)}), flush=True)
+    for tma in (False, True):
+        for ring in (2, 4, 6):
+            # the table stays in L2 between launches: no flush
+            ms = timed(lambda: csa.probe_row_gather(table, idx, ctas, stages, ring, sink, tma),
+                       flush_each=False)
+            print(json.dumps({"probe": "row_gather", "copies": "tma_gather4" if tma else "cp.async",
+                              "rows": n_rows, "row_bytes": 512, "ctas": ctas, "stages": stages,
+                              "ring": ring, "us": round(ms * 1e3, 1),
+                              "GB/s": round(moved / ms / 1e6, 1)}), flush=True)
+    torch.cuda.synchronize(dev)
+    if sink.item() == 2.0:
+        print(json.dumps({"probe": "row_gather", "error": "a bounded wait gave up"}), flush=True)
 
 
 # ---------------------------------------------------------------- main

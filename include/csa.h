@@ -375,18 +375,22 @@ CSA_API int csa_selftest_bounded_wait(int arrive, uint32_t limit, int32_t* err_w
  *   data read equals a fixed constant (it is there so that the loads stay).
  * csa_probe_row_gather: n_ctas CTAs of 256 threads; CTA c reads `stages`
  *   stages of 64 rows of 512 bytes, row r of stage s at index
- *   idx[(c * stages + s) * 64 + r] of the table (n_rows rows; indices are
- *   clamped into [0, n_rows)), with 16-byte cp.async copies into a ring of
- *   `ring` (2, 4 or 6) stages of 32 KB of shared memory and a block barrier
- *   per stage.  table: device, 16-byte aligned; idx: device int32, n_ctas *
- *   stages * 64 entries; sink as above.
+ *   idx[(c * stages + s) * 64 + r] of the table (n_rows < 2^31 rows;
+ *   indices are clamped into [0, n_rows)), into a ring of `ring` (2, 4 or
+ *   6) stages of 32 KB of shared memory.  mode 0: 16-byte cp.async copies
+ *   by every thread and a block barrier per stage; mode 1: TMA
+ *   tile::gather4 (four 128-byte pieces of four rows per instruction, 128-
+ *   byte swizzled; each 512-byte row read as 4 x 128 bytes) issued by one
+ *   warp, with a full and an empty mbarrier per ring slot (bounded waits:
+ *   sink = 2 if one gave up).  table: device, 16-byte aligned; idx: device
+ *   int32, n_ctas * stages * 64 entries; sink as above.
  * Both return CSA_OK, CSA_ERR_INVALID_ARG (checked before any launch) or
  * CSA_ERR_CUDA; they are asynchronous on `stream`.
  * ---------------------------------------------------------------------- */
 CSA_API int csa_probe_stream_read(const void* src, int64_t bytes, int ctas_per_sm, int in_flight,
                                   float* sink, void* stream);
 CSA_API int csa_probe_row_gather(const void* table, int64_t n_rows, const int32_t* idx, int n_ctas,
-                                 int stages, int ring, float* sink, void* stream);
+                                 int stages, int ring, int mode, float* sink, void* stream);
 
 /* ------------------------------------------------------------------------
  * a4 / a5 / a6. Attention over compressed entries + window + sink.

@@ -116,7 +116,7 @@ def lib() -> ctypes.CDLL:
             L.csa_selftest_bounded_wait.restype = I
             L.csa_probe_stream_read.argtypes = [P, I64, I, I, P, P]
             L.csa_probe_stream_read.restype = I
-            L.csa_probe_row_gather.argtypes = [P, I64, P, I, I, I, P, P]
+            L.csa_probe_row_gather.argtypes = [P, I64, P, I, I, I, I, P, P]
             L.csa_probe_row_gather.restype = I
             _lib = L
     return _lib
@@ -577,15 +577,16 @@ def probe_stream_read(src, sink, ctas_per_sm: int = 2, in_flight: int = 4):
     _check(st, "csa_probe_stream_read")
 
 
-def probe_row_gather(table, idx, n_ctas: int, stages: int, ring: int, sink):
+def probe_row_gather(table, idx, n_ctas: int, stages: int, ring: int, sink, tma: bool = False):
     """Gather 512-byte rows of table (uint8 CUDA tensor [n_rows, 512]) into
     shared memory: CTA c reads idx[c * stages * 64: (c + 1) * stages * 64]
-    (int32, 64 rows per stage) through a ring of `ring` 32 KB stages."""
+    (int32, 64 rows per stage) through a ring of `ring` 32 KB stages, with
+    16-byte cp.async copies, or TMA tile::gather4 when `tma`."""
     _need(table.is_cuda and table.is_contiguous() and table.dim() == 2 and table.shape[1] == 512,
           "table: contiguous CUDA [n_rows, 512]")
     _cuda(idx, "idx", torch.int32)
     _need(idx.is_contiguous() and idx.numel() >= n_ctas * stages * 64, "idx: n_ctas * stages * 64")
     _cuda(sink, "sink", torch.float32)
     st = lib().csa_probe_row_gather(_p(table), table.shape[0], _p(idx), int(n_ctas), int(stages),
-                                    int(ring), _p(sink), _stream(table.device))
+                                    int(ring), int(bool(tma)), _p(sink), _stream(table.device))
     _check(st, "csa_probe_row_gather")

@@ -11,8 +11,14 @@
 //   memory, a block barrier per stage; the rows are summed as they are
 //   consumed (the sparse attention's loader situation without the tensor
 //   cores).  The ring depth sets the shared memory and so the CTAs per SM.
+//   Mode 1 moves the same rows with TMA `tile::gather4` (four 128-byte row
+//   pieces per instruction, 128-byte swizzled, issued by 16 lanes of one warp)
+//   into the attention's layout (K and V halves as four 8 KB regions per
+//   stage), with a full and an empty mbarrier per ring slot.
 #include "common.cuh"
 #include "kernels.h"
+#include "tc.cuh"
+#include "tma.cuh"
 
 namespace csa {
 namespace {
@@ -72,6 +78,59 @@ __global__ void __launch_bounds__(kGatherThreads)
   if (acc == 0x9E3779B9u) sink[0] = 1.f;
 }
 
+template <int RING>
+__global__ void __launch_bounds__(kGatherThreads)
+    row_gather4_kernel(const __grid_constant__ CUtensorMap map, int64_t n_rows,
+                       const int32_t* __restrict__ idx, int stages, float* sink) {
+  extern __shared__ uint8_t g4_raw[];
+  __shared__ __align__(8) uint64_t full[RING], empty[RING];
+  uint8_t* base = g4_raw + ((1024 - (smem_u32(g4_raw) & 1023)) & 1023);
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int32_t* my = idx + (int64_t)blockIdx.x * stages * 64;
+  constexpr uint32_t kLimit = 1u << 22;
+  if (t == 0) {
+    for (int d = 0; d < RING; ++d) {
+      tc::mbar_init(&full[d], 1);
+      tc::mbar_init(&empty[d], kGatherThreads / 32 - 1);  // one arrival per consumer warp
+    }
+    tc::fence_mbar_init();
+  }
+  __syncthreads();
+  bool ok = true;
+  uint32_t acc = 0u;
+  if (warp == 0) {
+    for (int s = 0; s < stages; ++s) {
+      const int d = s % RING;
+      if (s >= RING) ok &= tc::mbar_wait(&empty[d], ((s / RING) - 1) & 1, kLimit);
+      int r[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        int64_t row = lane < 16 ? __ldg(my + s * 64 + 4 * lane + q) : 0;
+        r[q] = (int)(row < 0 ? 0 : (row >= n_rows ? n_rows - 1 : row));
+      }
+      if (lane == 0) tma::expect_tx(&full[d], kGatherStageBytes);
+      __syncwarp();
+      if (lane < 16) {
+        const uint32_t st = smem_u32(base + d * kGatherStageBytes) + lane * 512;
+#pragma unroll
+        for (int h = 0; h < 4; ++h)  // K 0-63, K 64-127, V 0-63, V 64-127
+          tma::gather4(st + h * 8192, &map, 64 * h, r[0], r[1], r[2], r[3], &full[d]);
+      }
+    }
+  } else {
+    for (int s = 0; s < stages; ++s) {
+      const int d = s % RING;
+      ok &= tc::mbar_wait(&full[d], (s / RING) & 1, kLimit);
+      const uint4* v = reinterpret_cast<const uint4*>(base + d * kGatherStageBytes);
+      for (int c = t - 32; c < 2048; c += kGatherThreads - 32) acc ^= v[c].x;
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&empty[d]);
+    }
+  }
+  if (!ok) sink[0] = 2.f;  // a wait gave up
+  if (acc == 0x9E3779B9u) sink[0] = 1.f;
+}
+
 }  // namespace
 }  // namespace csa
 
@@ -97,26 +156,48 @@ CSA_API int csa_probe_stream_read(const void* src, int64_t bytes, int ctas_per_s
 }
 
 CSA_API int csa_probe_row_gather(const void* table, int64_t n_rows, const int32_t* idx, int n_ctas,
-                                 int stages, int ring, float* sink, void* stream) {
-  if (!table || !idx || !sink || n_rows <= 0 || n_ctas <= 0 || stages <= 0 ||
-      (ring != 2 && ring != 4 && ring != 6) || (reinterpret_cast<uintptr_t>(table) & 15))
+                                 int stages, int ring, int mode, float* sink, void* stream) {
+  if (!table || !idx || !sink || n_rows <= 0 || n_rows >= (int64_t)1 << 31 || n_ctas <= 0 ||
+      stages <= 0 || (ring != 2 && ring != 4 && ring != 6) || (mode != 0 && mode != 1) ||
+      (reinterpret_cast<uintptr_t>(table) & 15))
     return CSA_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const uint4* tb = static_cast<const uint4*>(table);
-  const int smem = ring * kGatherStageBytes;
   cudaError_t e;
-  if (ring == 2) {
-    e = ensure_smem_attr((const void*)row_gather_kernel<2>, smem);
-    if (e == cudaSuccess)
-      row_gather_kernel<2><<<n_ctas, kGatherThreads, smem, st>>>(tb, n_rows, idx, stages, sink);
-  } else if (ring == 4) {
-    e = ensure_smem_attr((const void*)row_gather_kernel<4>, smem);
-    if (e == cudaSuccess)
-      row_gather_kernel<4><<<n_ctas, kGatherThreads, smem, st>>>(tb, n_rows, idx, stages, sink);
+  if (mode == 0) {
+    const int smem = ring * kGatherStageBytes;
+    if (ring == 2) {
+      e = ensure_smem_attr((const void*)row_gather_kernel<2>, smem);
+      if (e == cudaSuccess)
+        row_gather_kernel<2><<<n_ctas, kGatherThreads, smem, st>>>(tb, n_rows, idx, stages, sink);
+    } else if (ring == 4) {
+      e = ensure_smem_attr((const void*)row_gather_kernel<4>, smem);
+      if (e == cudaSuccess)
+        row_gather_kernel<4><<<n_ctas, kGatherThreads, smem, st>>>(tb, n_rows, idx, stages, sink);
+    } else {
+      e = ensure_smem_attr((const void*)row_gather_kernel<6>, smem);
+      if (e == cudaSuccess)
+        row_gather_kernel<6><<<n_ctas, kGatherThreads, smem, st>>>(tb, n_rows, idx, stages, sink);
+    }
   } else {
-    e = ensure_smem_attr((const void*)row_gather_kernel<6>, smem);
-    if (e == cudaSuccess)
-      row_gather_kernel<6><<<n_ctas, kGatherThreads, smem, st>>>(tb, n_rows, idx, stages, sink);
+    // rows of 256 bf16 (a K row and a V row), boxes of 64 columns x 1 row
+    CUtensorMap map;
+    e = tma::encode_rows(&map, table, 256, (uint64_t)n_rows, 1);
+    if (e != cudaSuccess) return CSA_ERR_CUDA;
+    const int smem = ring * kGatherStageBytes + 1024;  // + room to align the ring to 1024
+    if (ring == 2) {
+      e = ensure_smem_attr((const void*)row_gather4_kernel<2>, smem);
+      if (e == cudaSuccess)
+        row_gather4_kernel<2><<<n_ctas, kGatherThreads, smem, st>>>(map, n_rows, idx, stages, sink);
+    } else if (ring == 4) {
+      e = ensure_smem_attr((const void*)row_gather4_kernel<4>, smem);
+      if (e == cudaSuccess)
+        row_gather4_kernel<4><<<n_ctas, kGatherThreads, smem, st>>>(map, n_rows, idx, stages, sink);
+    } else {
+      e = ensure_smem_attr((const void*)row_gather4_kernel<6>, smem);
+      if (e == cudaSuccess)
+        row_gather4_kernel<6><<<n_ctas, kGatherThreads, smem, st>>>(map, n_rows, idx, stages, sink);
+    }
   }
   if (e != cudaSuccess) return CSA_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? CSA_OK : CSA_ERR_CUDA;

@@ -251,14 +251,16 @@ def test_probe_rejects():
     assert L.csa_probe_stream_read(FAKE, 1 << 20, 5, 4, FAKE, None) == 1
     assert L.csa_probe_stream_read(FAKE, 1 << 20, 2, 3, FAKE, None) == 1
     assert L.csa_probe_stream_read(FAKE, 16, 2, 4, FAKE, None) == 1  # under one vector per CTA
-    assert L.csa_probe_row_gather(None, 100, FAKE, 1, 1, 2, FAKE, None) == 1
-    assert L.csa_probe_row_gather(FAKE, 100, None, 1, 1, 2, FAKE, None) == 1
-    assert L.csa_probe_row_gather(FAKE, 100, FAKE, 1, 1, 2, None, None) == 1
-    assert L.csa_probe_row_gather(odd, 100, FAKE, 1, 1, 2, FAKE, None) == 1
-    assert L.csa_probe_row_gather(FAKE, 0, FAKE, 1, 1, 2, FAKE, None) == 1
-    assert L.csa_probe_row_gather(FAKE, 100, FAKE, 0, 1, 2, FAKE, None) == 1
-    assert L.csa_probe_row_gather(FAKE, 100, FAKE, 1, 0, 2, FAKE, None) == 1
-    assert L.csa_probe_row_gather(FAKE, 100, FAKE, 1, 1, 3, FAKE, None) == 1
+    assert L.csa_probe_row_gather(None, 100, FAKE, 1, 1, 2, 0, FAKE, None) == 1
+    assert L.csa_probe_row_gather(FAKE, 100, None, 1, 1, 2, 0, FAKE, None) == 1
+    assert L.csa_probe_row_gather(FAKE, 100, FAKE, 1, 1, 2, 0, None, None) == 1
+    assert L.csa_probe_row_gather(odd, 100, FAKE, 1, 1, 2, 0, FAKE, None) == 1
+    assert L.csa_probe_row_gather(FAKE, 0, FAKE, 1, 1, 2, 0, FAKE, None) == 1
+    assert L.csa_probe_row_gather(FAKE, 100, FAKE, 0, 1, 2, 0, FAKE, None) == 1
+    assert L.csa_probe_row_gather(FAKE, 100, FAKE, 1, 0, 2, 0, FAKE, None) == 1
+    assert L.csa_probe_row_gather(FAKE, 100, FAKE, 1, 1, 3, 0, FAKE, None) == 1
+    assert L.csa_probe_row_gather(FAKE, 100, FAKE, 1, 1, 2, 2, FAKE, None) == 1
+    assert L.csa_probe_row_gather(FAKE, 1 << 31, FAKE, 1, 1, 2, 1, FAKE, None) == 1
 
 
 def test_compress_mixed_rejects():
