@@ -371,6 +371,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_tiles = k_end > k_begin ? (k_end - k_begin + kTileKeys - 1) / kTileKeys : 0;
   const int n_stages = 2 * n_tiles;
 
+  // Leading stages whose 64 slots are all compressed entries of a dense key
+  // set (HCA) are four TMA boxes each, issued by one thread without per-slot
+  // lookups: the thread publishes the stage's slot bits and arrives for the
+  // whole loader group.  The first kStages of them (no ring slot to wait
+  // for) are issued during the set-up, once the barriers exist.
+  int j_fast = 0;
+  if (!KV8 && a.dense) {
+    const int full = (n_c < k_end ? n_c : k_end) - k_begin;
+    j_fast = full > 0 ? full / kStageKeys : 0;
+    if (j_fast > n_stages) j_fast = n_stages;
+  }
+  const int j_pre = j_fast < kStages ? j_fast : kStages;
+  auto issue_dense_stage = [&](int j) {
+    const int st = j % kStages, pr = (j >> 1) % kPairs;
+    bars->valid[j & 7][0] = 0xFFFFFFFFu;
+    bars->valid[j & 7][1] = 0xFFFFFFFFu;
+    if (j & 1) tc::mbar_arrive(&bars->meta_full[(j >> 1) & 3]);  // both stages' bits
+    const int row = (int)((int64_t)b * (a.cmp_bstride / kD) + k_begin + (int64_t)j * kStageKeys);
+    const uint32_t off = st * kBlk;
+    tma::expect_tx(&bars->kv_full[pr], 4 * kBlk);
+    tma::load_box(sbase + C::kK0 + off, &maps.kc, 0, row, &bars->kv_full[pr]);
+    tma::load_box(sbase + C::kK1 + off, &maps.kc, 64, row, &bars->kv_full[pr]);
+    tma::load_box(sbase + C::kV0 + off, &maps.vc, 0, row, &bars->kv_full[pr]);
+    tma::load_box(sbase + C::kV1 + off, &maps.vc, 64, row, &bars->kv_full[pr]);
+    tc::mbar_arrive_count(&bars->kv_full[pr], kLoadThreads - 1);
+  };
+
   // ---- set-up: barriers, TMEM, the query block, zero Q rows >= H
   if (warp == 0) {
     tc::tmem_alloc(&bars->tmem_slot, kTmemCols);
@@ -398,6 +425,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma::expect_tx(&bars->q_full, 2 * H * 128);
       tma::load_box(sbase + C::kQOff, &maps.q, 0, qid * H, &bars->q_full);
       tma::load_box(sbase + C::kQOff + M * 128, &maps.q, 64, qid * H, &bars->q_full);
+    }
+    if (j_pre > 0) {
+      pdl_wait();  // the entries may be the previous kernel's output
+      for (int j = 0; j < j_pre; ++j) issue_dense_stage(j);
     }
   }
   for (int idx = tid; idx < (M - H) * 16; idx += kThreads) {
@@ -498,37 +529,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bf16* kr = a.k_raw;
     const bf16* vr = a.v_raw;
     int32_t* codes = reinterpret_cast<int32_t*>(sm + C::kMetaOff);
-    // Leading stages whose 64 slots are all compressed entries of a dense key
-    // set (HCA) are four TMA boxes each: one thread issues them -- waiting for
-    // the ring slot, publishing the stage's slot bits, arriving for the whole
-    // loader group -- without the per-slot lookups and loader barriers; the
-    // group joins at the first stage that needs them (the window).
-    int j_fast = 0;
-    if (!KV8 && a.dense) {
-      const int full = (n_c < k_end ? n_c : k_end) - k_begin;
-      j_fast = full > 0 ? full / kStageKeys : 0;
-      if (j_fast > n_stages) j_fast = n_stages;
-    }
-    int issued = 0;
+    // The dense key set's remaining whole-entry stages (the set-up issued the
+    // first j_pre): one thread waits for each ring slot and issues them; the
+    // group joins at the first stage that needs per-slot lookups (the window).
+    int issued = lt == 0 ? j_pre : 0;
     bool fast_ok = true;
     if (j_fast > 0 && lt == 0) {
-      for (int j = 0; j < j_fast; ++j) {
-        const int st = j % kStages, pr = (j >> 1) % kPairs;
+      for (int j = j_pre; j < j_fast; ++j) {
+        const int pr = (j >> 1) % kPairs;
         if (j >= kStages && (j & 1) == 0)
           fast_ok = wait_or_flag(&bars->pair_empty[pr], ((j >> 1) / kPairs - 1) & 1, bars, a.err);
         fast_ok = fast_ok && !*(volatile int*)&bars->timed_out;
         if (!fast_ok) break;
-        bars->valid[j & 7][0] = 0xFFFFFFFFu;
-        bars->valid[j & 7][1] = 0xFFFFFFFFu;
-        if (j & 1) tc::mbar_arrive(&bars->meta_full[(j >> 1) & 3]);  // both stages' bits
-        const int row = (int)(ks.cmp_row0 + k_begin + (int64_t)j * kStageKeys);
-        const uint32_t off = st * kBlk;
-        tma::expect_tx(&bars->kv_full[pr], 4 * kBlk);
-        tma::load_box(sbase + C::kK0 + off, &maps.kc, 0, row, &bars->kv_full[pr]);
-        tma::load_box(sbase + C::kK1 + off, &maps.kc, 64, row, &bars->kv_full[pr]);
-        tma::load_box(sbase + C::kV0 + off, &maps.vc, 0, row, &bars->kv_full[pr]);
-        tma::load_box(sbase + C::kV1 + off, &maps.vc, 64, row, &bars->kv_full[pr]);
-        tc::mbar_arrive_count(&bars->kv_full[pr], kLoadThreads - 1);
+        issue_dense_stage(j);
         issued = j + 1;
       }
     }
