@@ -354,6 +354,23 @@ def test_topk_stream_skewed_sample(cuda_device, sampled):
     np.testing.assert_array_equal(idx, ref)  # exact: ties resolved by index
 
 
+def test_topk_stream_large_k_histogram_path(cuda_device):
+    # 2k above the 4096-entry list: the one-CTA-per-query select skips the
+    # sampled bound and runs the histogram passes (pass 1, then the list of
+    # the threshold bin and above through the per-warp buckets, or the
+    # candidate passes when that list would not fit)
+    T, N_cap, m, k = 160, 24000, 4, 2100
+    qi = synth.randn((1, T, 4, 64), 8, 1)
+    ki = synth.randn((1, N_cap, 64), 8, 2)
+    w = synth.randn((1, T, 4), 8, 3, dtype=torch.float32)
+    qp = torch.tensor([[N_cap * m - 1 - 50 * (T - 1 - t) for t in range(T)]], dtype=torch.int32)
+    nc = torch.tensor([N_cap], dtype=torch.int32)
+    case = (qi, None, ki, None, w, qp, nc)
+    idx, _ = _run_indexer(*case, m, k)
+    s, nv, ref = _oracle_indexer(*case, m, k, False)
+    check_topk(idx, ref, s, nv, k, "stream select, k = 2100")
+
+
 def test_topk_zero_scores_and_short_lists(cuda_device):
     # n_vis below k (every visible entry, -1 padded), n_vis == 0, and a query
     # whose scores are mostly exactly zero (negative dot products)
