@@ -60,8 +60,12 @@ struct GemmMaps {
 __global__ void __launch_bounds__(kGThreads, 1)
     indexer_gemm_kernel(IndexerArgs a, int q0, float* scores, int stride,
                         const __grid_constant__ GemmMaps maps) {
+  // Until the producer's griddepcontrol.wait below the kernel reads only
+  // inputs that no kernel of this library writes (positions, entry counts,
+  // the chunk's queries and head weights) and sets up shared and tensor
+  // memory, so that part overlaps the previous kernel (the select of the
+  // previous chunk, which still reads the score workspace).
   pdl_trigger();
-  pdl_wait();
   extern __shared__ uint8_t gsm_raw[];
   uint8_t* sm = gsm_raw + ((1024 - (smem_u32(gsm_raw) & 1023)) & 1023);
   const uint32_t sbase = smem_u32(sm);
@@ -74,11 +78,11 @@ __global__ void __launch_bounds__(kGThreads, 1)
 
   // entries any token of the block can see: tiles [0, n_tiles)
   int nv_max = 0;
+  bool bad = false;  // flagged after the wait (the error word may be the previous kernel's)
   for (int i = lane; i < kGQ; i += 32) {
     const int64_t t = __ldg(a.q_pos + tok0 + i);
     int64_t present = __ldg(a.n_cmp + b);
-    if (blockIdx.x == 0 && (t < 0 || present < 0 || present > a.N_cap))
-      flag_error(a.err, CSA_EW_BAD_POSITION);
+    if (blockIdx.x == 0 && (t < 0 || present < 0 || present > a.N_cap)) bad = true;
     present = present < 0 ? 0 : (present > a.N_cap ? a.N_cap : present);
     int64_t nv = t >= 0 ? (t + 1) / a.m : 0;
     nv = nv < present ? nv : present;
@@ -119,6 +123,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
     if (lane == 0) {
       tma::expect_tx(&bars->qfull, kGQBytes);
       tma::load_box(sbase + kGQOff, &maps.q, 0, tok0 * 4, &bars->qfull);
+      pdl_wait();  // the keys may be the compression's output
       const int krow0 = (int)((int64_t)b * (a.k_bstride / 64));
       for (int i = 0; i < n_tiles; ++i) {
         const int s = i % kGStages;
@@ -164,6 +169,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
     const int half = e8 >> 2;     // columns [128 half, 128 half + 128): tokens 32 half ..
     const uint32_t lanef = (uint32_t)(qd * 32) << 16;
     const uint64_t keep = l2_evict_last_policy();  // read back by the select
+    pdl_wait();  // the previous select has finished reading the score workspace
     for (int i = 0; i < n_tiles; ++i) {
       const int buf = i & 1;
       if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&bars->tfull[buf], (i >> 1) & 1, kGWait))) {
@@ -195,6 +201,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
   }
   tc::fence_before_sync();
   __syncthreads();
+  pdl_wait();
+  if (bad) flag_error(a.err, CSA_EW_BAD_POSITION);
   if (warp == 0) {
     // copies still in flight (after a timeout) land before TMEM and smem go
     if (lane == 0 && n_tiles > 0) {
