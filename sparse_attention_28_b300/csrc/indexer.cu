@@ -293,8 +293,9 @@ constexpr int score_ctas_per_sm(int) { return 2; }
 template <int FMT>
 __global__ void __launch_bounds__(kThreads, score_ctas_per_sm(FMT)) indexer_score_kernel(IndexerArgs a, int q0, int qc,
                                                                 WsLayout L) {
+  // the visible counts and their prefix come from inputs no kernel of this
+  // library writes: computed while the previous kernel finishes
   pdl_trigger();
-  pdl_wait();
   __shared__ int gp[kQueryChunk + 1];  // group prefix over the chunk's queries
   __shared__ int nvs[kQueryChunk];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -302,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, score_ctas_per_sm(FMT)) indexer_scor
   {
     int nv = 0;
     if (tid < qc) {
-      nv = (int)visible_entries(a, q0 + tid, a.err, blockIdx.x == 0);
+      nv = (int)visible_entries(a, q0 + tid, nullptr, false);
       nvs[tid] = nv;
     }
     int tot;
@@ -313,6 +314,8 @@ __global__ void __launch_bounds__(kThreads, score_ctas_per_sm(FMT)) indexer_scor
     if (tid == 0) gp[qc] = tot;
     __syncthreads();
   }
+  pdl_wait();
+  if (tid < qc && blockIdx.x == 0) visible_entries(a, q0 + tid, a.err, true);  // flags bad input
   const int G = gp[qc];
   const int g_lo = (int)((int64_t)blockIdx.x * G / gridDim.x);
   const int g_hi = (int)((int64_t)(blockIdx.x + 1) * G / gridDim.x);
@@ -370,12 +373,18 @@ __global__ void __launch_bounds__(NT, 1024 / NT) topk_select_kernel(IndexerArgs 
   extern __shared__ __align__(128) uint8_t sel_smem[];
   SelShared* sh = reinterpret_cast<SelShared*>(sel_smem);
   pdl_trigger();
-  pdl_wait();
   float* sc = reinterpret_cast<float*>(sel_smem + (sizeof(SelShared) + 127) / 128 * 128);
   const int tid = threadIdx.x;
   const int cs = gridDim.x, r = blockIdx.x;
   const int lq = blockIdx.y, qid = q0 + lq;
+  // positions and entry counts: inputs that no kernel of this library
+  // writes, read while the scoring kernel finishes; the slice's barrier too
   const int64_t nv = visible_entries(a, qid, nullptr, false);
+  if (tid == 0) {
+    tc::mbar_init(&sh->bar, 1);
+    tc::fence_mbar_init();
+  }
+  pdl_wait();
   int32_t* out = a.topk_idx + (int64_t)qid * a.k;
   float* out_s = a.topk_score ? a.topk_score + (int64_t)qid * a.k : nullptr;
   const float* scores = L.scores + (int64_t)lq * L.stride;
@@ -392,8 +401,6 @@ __global__ void __launch_bounds__(NT, 1024 / NT) topk_select_kernel(IndexerArgs 
   // the slice's scores: one bulk copy of whole 16-byte chunks, the tail below
   const int bulk = (n_slice * 4) & ~15;
   if (tid == 0) {
-    tc::mbar_init(&sh->bar, 1);
-    tc::fence_mbar_init();
     if (bulk > 0)
       tma::expect_tx(&sh->bar, (uint32_t)bulk);
     else
