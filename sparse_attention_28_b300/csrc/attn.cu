@@ -256,9 +256,13 @@ struct RowMap {  // softmax-thread view of the 16-lane TMEM layout
 // every split's rows visible, then CTA `split` combines heads
 // [split*hp, split*hp + hp) reading them from L2 (ld.global.cg), with the
 // weights exp(lse_s - M) / Z of the cluster merge (the sink's term in Z
-// only).  wgt: ns*hp floats of scratch; sink_s: H floats.
+// only).  Each thread owns four channels of one head: it loads the head's
+// lse values and its pieces of the first eight splits' rows together (one
+// round trip to L2; a second for splits 8-15), and forms the weights itself.
+// sink_s: H floats.
 __device__ __forceinline__ void merge_from_global(const AttnArgs& a, int qid, int split, int ns,
-                                                  float* wgt, float* sink_s, float sink_mine) {
+                                                  float* sink_s, float sink_mine) {
+  constexpr int kRows = 8;  // splits' rows in flight at a time
   const int tid = threadIdx.x, H = a.H;
   if (tid < H) sink_s[tid] = sink_mine;
   tc::cluster_sync();
@@ -266,54 +270,56 @@ __device__ __forceinline__ void merge_from_global(const AttnArgs& a, int qid, in
   const int h0 = split * hp;
   const int nh = H - h0 < hp ? (H - h0 > 0 ? H - h0 : 0) : hp;
   const float* plse = a.part_lse + (int64_t)qid * ns * H;  // split s, head h at s * H + h
-  for (int hl = tid; hl < nh; hl += kThreads) {
-    const int h = h0 + hl;
-    // every split's lse at once (one round trip to L2)
-    float ls[kMaxCluster];
-#pragma unroll
-    for (int s = 0; s < kMaxCluster; ++s) ls[s] = s < ns ? __ldcg(plse + s * H + h) : -INFINITY;
-    float Mx = a.sink ? sink_s[h] : -INFINITY;
-#pragma unroll
-    for (int s = 0; s < kMaxCluster; ++s) Mx = fmaxf(Mx, ls[s]);
-    float lse = -INFINITY;
-    if (Mx != -INFINITY) {
-      float Z = a.sink ? ex2_approx((sink_s[h] - Mx) * kLog2e) : 0.f;
-#pragma unroll
-      for (int s = 0; s < kMaxCluster; ++s) {
-        if (s >= ns) break;
-        const float w = ls[s] == -INFINITY ? 0.f : ex2_approx((ls[s] - Mx) * kLog2e);
-        wgt[hl * ns + s] = w;
-        Z += w;
-      }
-      const float inv = 1.f / Z;
-      for (int s = 0; s < ns; ++s) wgt[hl * ns + s] *= inv;
-      lse = Mx + logf(Z);
-    } else {
-      for (int s = 0; s < ns; ++s) wgt[hl * ns + s] = 0.f;
-    }
-    if (a.lse) a.lse[(int64_t)qid * H + h] = lse;
-  }
-  __syncthreads();
   const float4* rows = reinterpret_cast<const float4*>(a.part_o + (int64_t)qid * ns * H * kD);
   const int64_t sstride = (int64_t)H * kD / 4;  // float4s between splits
   for (int it = tid; it < nh * 32; it += kThreads) {
     const int hl = it >> 5, d4 = it & 31, h = h0 + hl;
+    float ls[kMaxCluster];
+    float4 v[kRows];
+#pragma unroll
+    for (int s = 0; s < kMaxCluster; ++s) ls[s] = s < ns ? __ldcg(plse + s * H + h) : -INFINITY;
+#pragma unroll
+    for (int s = 0; s < kRows; ++s)
+      v[s] = s < ns ? __ldcg(rows + s * sstride + h * 32 + d4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    float Mx = a.sink ? sink_s[h] : -INFINITY;
+#pragma unroll
+    for (int s = 0; s < kMaxCluster; ++s) Mx = fmaxf(Mx, ls[s]);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s0 = 0; s0 < ns; s0 += 4) {  // four splits' rows in flight at a time
-      float4 v[4];
+    float lse = -INFINITY;
+    if (Mx != -INFINITY) {
+      float w[kMaxCluster];
+      float Z = a.sink ? ex2_approx((sink_s[h] - Mx) * kLog2e) : 0.f;
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        v[j] = s0 + j < ns ? __ldcg(rows + (s0 + j) * sstride + h * 32 + d4)
-                           : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float w = s0 + j < ns ? wgt[hl * ns + s0 + j] : 0.f;
-        acc.x += w * v[j].x;
-        acc.y += w * v[j].y;
-        acc.z += w * v[j].z;
-        acc.w += w * v[j].w;
+      for (int s = 0; s < kMaxCluster; ++s) {
+        w[s] = ls[s] == -INFINITY ? 0.f : ex2_approx((ls[s] - Mx) * kLog2e);
+        Z += w[s];
       }
+      const float inv = 1.f / Z;
+#pragma unroll
+      for (int s = 0; s < kRows; ++s) {
+        const float ws = w[s] * inv;
+        acc.x += ws * v[s].x;
+        acc.y += ws * v[s].y;
+        acc.z += ws * v[s].z;
+        acc.w += ws * v[s].w;
+      }
+      if (ns > kRows) {
+#pragma unroll
+        for (int s = 0; s < kMaxCluster - kRows; ++s)
+          v[s] = kRows + s < ns ? __ldcg(rows + (kRows + s) * sstride + h * 32 + d4)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int s = 0; s < kMaxCluster - kRows; ++s) {
+          const float ws = w[kRows + s] * inv;
+          acc.x += ws * v[s].x;
+          acc.y += ws * v[s].y;
+          acc.z += ws * v[s].z;
+          acc.w += ws * v[s].w;
+        }
+      }
+      lse = Mx + logf(Z);
     }
+    if (d4 == 0 && a.lse) a.lse[(int64_t)qid * H + h] = lse;
     reinterpret_cast<uint2*>(a.out + ((int64_t)qid * H + h) * kD)[d4] =
         make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
   }
@@ -755,9 +761,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::mbar_arrive(&bars->kv_full[pr]);
         }
       } else {
-        for (int ci = lt; ci < kStageKeys * 16; ci += NL) {
+        // the row codes of all of this thread's chunks first, then the copies
+        // back to back (no shared-memory load between two copies)
+        constexpr int kIt = (kStageKeys * 16 + NL - 1) / NL;
+        int32_t cds[kIt];
+#pragma unroll
+        for (int i = 0; i < kIt; ++i) {
+          const int ci = lt + i * NL;
+          cds[i] = ci < kStageKeys * 16 ? codes[st * kStageKeys + (ci >> 4)] : -1;
+        }
+#pragma unroll
+        for (int i = 0; i < kIt; ++i) {
+          const int ci = lt + i * NL;
+          if (ci >= kStageKeys * 16) break;
           const int r = ci >> 4, c16 = ci & 15;
-          const int32_t cd = codes[st * kStageKeys + r];
+          const int32_t cd = cds[i];
           const bool ok = cd != -1;
           const bool raw = cd < -1;
           const int64_t goff = (int64_t)(raw ? -(cd + 2) : cd) * kD + c16 * 8;
@@ -957,7 +975,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       float fac[2], lse_r[2];
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2) {
-        const int h = rowA + 8 * h2;
         const bool any = have_o && l_sum[g][h2] > 0.f;
         if (ns > 1) {
           fac[h2] = any ? 1.f / l_sum[g][h2] : 0.f;
@@ -1032,8 +1049,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (ns <= 1 || (a.part_o && !a.xch)) return;  // one split, or merged by attn_merge_kernel
   if (a.xch) {
-    merge_from_global(a, qid, split, ns, reinterpret_cast<float*>(sm + C::kWgtOff),
-                      reinterpret_cast<float*>(sm + C::kSinkOff), sink_mine);
+    merge_from_global(a, qid, split, ns, reinterpret_cast<float*>(sm + C::kSinkOff), sink_mine);
     return;
   }
 
