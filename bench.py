@@ -331,11 +331,14 @@ def run_probes(dev, l2_bytes: int):
     each (mean of 10 timed launches after 3 warm-up ones, L2 flushed clean
     before each).  (1) a contiguous stream read once, the size of the
     csa_decode_128k indexer keys (134 MB), for several CTAs per SM and loads
-    in flight; (2) 512-byte row gathers into shared memory from an L2-resident
-    table of the csa_prefill_4k caches' size (43 MB: 88,000 rows), 4096 CTAs x
-    34 stages x 64 rows like the prefill attention, for ring depths of 2, 4
-    and 6 stages (3, 1 and 1 CTAs per SM by shared memory), with 16-byte
-    cp.async copies and with TMA tile::gather4."""
+    in flight; (2) 512-byte row gathers into shared memory, 34 stages x 64
+    rows per CTA like the prefill attention: 4096 CTAs from an L2-resident
+    table of the csa_prefill_4k caches' size (43 MB: 88,000 rows), and 888
+    CTAs reading distinct rows of a 1 GB table (every row from DRAM); for
+    ring depths of 2, 4 and 6 stages (3, 1 and 1 CTAs per SM by shared
+    memory), with 16-byte cp.async copies by 256 or 512 threads and with TMA
+    tile::gather4 issued by one, four or eight warps; each CTA's row indices
+    are staged in shared memory first."""
     import sparse_attention_28_b300 as csa
     flush = L2Flush(l2_bytes, dev)
     sink = torch.zeros(1, dtype=torch.float32, device=dev)
@@ -363,20 +366,37 @@ def run_probes(dev, l2_bytes: int):
                               "in_flight": k, "us": round(ms * 1e3, 2),
                               "GB/s": round(keys.numel() / ms / 1e6, 1)}), flush=True)
     del keys
-    n_rows, ctas, stages = 88000, 4096, 34
-    table = torch.zeros((n_rows, 512), dtype=torch.uint8, device=dev)
+    stages = 34
     g = torch.Generator(device="cpu").manual_seed(1)
-    idx = torch.randint(0, n_rows, (ctas * stages * 64,), generator=g, dtype=torch.int32).to(dev)
-    moved = ctas * stages * 64 * 512
-    for tma in (False, True):
-        for ring in (2, 4, 6):
-            # the table stays in L2 between launches: no flush
-            ms = timed(lambda: csa.probe_row_gather(table, idx, ctas, stages, ring, sink, tma),
-                       flush_each=False)
-            print(json.dumps({"probe": "row_gather", "copies": "tma_gather4" if tma else "cp.async",
-                              "rows": n_rows, "row_bytes": 512, "ctas": ctas, "stages": stages,
-                              "ring": ring, "us": round(ms * 1e3, 1),
-                              "GB/s": round(moved / ms / 1e6, 1)}), flush=True)
+    # an L2-resident table (the csa_prefill_4k caches' size), indices drawn
+    # with repeats, 4096 CTAs; and a 1 GB table read without repeats (every
+    # row from DRAM), 888 CTAs
+    for where, n_rows, ctas in (("l2", 88000, 4096), ("dram", 1 << 21, 888)):
+        n_idx = ctas * stages * 64
+        table = torch.zeros((n_rows, 512), dtype=torch.uint8, device=dev)
+        if where == "l2":
+            idx = torch.randint(0, n_rows, (n_idx,), generator=g, dtype=torch.int32)
+        else:
+            idx = torch.randperm(n_rows, generator=g, dtype=torch.int32)[:n_idx]
+        idx = idx.to(dev)
+        moved = n_idx * 512
+        for tma, wide, issuers, who in ((False, False, 0, "256 threads"),
+                                        (False, True, 0, "512 threads"),
+                                        (True, False, 1, "1 warp"), (True, False, 4, "4 warps"),
+                                        (True, False, 8, "8 warps")):
+            for ring in (2, 4, 6):
+                # the L2 case keeps the table in L2 between launches; the
+                # DRAM case flushes L2 before each launch
+                ms = timed(lambda: csa.probe_row_gather(table, idx, ctas, stages, ring, sink,
+                                                        tma, wide, issuers),
+                           flush_each=where == "dram")
+                print(json.dumps({
+                    "probe": "row_gather", "copies": "tma_gather4" if tma else "cp.async",
+                    "issuers": who,
+                    "table": where, "rows": n_rows, "row_bytes": 512, "ctas": ctas,
+                    "stages": stages, "ring": ring, "us": round(ms * 1e3, 1),
+                    "GB/s": round(moved / ms / 1e6, 1)}), flush=True)
+        del table, idx
     torch.cuda.synchronize(dev)
     if sink.item() == 2.0:
         print(json.dumps({"probe": "row_gather", "error": "a bounded wait gave up"}), flush=True)

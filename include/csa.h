@@ -373,17 +373,21 @@ CSA_API int csa_selftest_bounded_wait(int arrive, uint32_t limit, int32_t* err_w
  *   16-byte aligned, `bytes` readable (the remainder below one vector per
  *   CTA is not read).  sink: device float, written only if the XOR of all
  *   data read equals a fixed constant (it is there so that the loads stay).
- * csa_probe_row_gather: n_ctas CTAs of 256 threads; CTA c reads `stages`
- *   stages of 64 rows of 512 bytes, row r of stage s at index
+ * csa_probe_row_gather: n_ctas CTAs; CTA c reads `stages` (1..64) stages
+ *   of 64 rows of 512 bytes, row r of stage s at index
  *   idx[(c * stages + s) * 64 + r] of the table (n_rows < 2^31 rows;
  *   indices are clamped into [0, n_rows)), into a ring of `ring` (2, 4 or
- *   6) stages of 32 KB of shared memory.  mode 0: 16-byte cp.async copies
- *   by every thread and a block barrier per stage; mode 1: TMA
+ *   6) stages of 32 KB of shared memory.  Each CTA first copies its
+ *   stages * 64 indices into shared memory, so no copy waits on an index
+ *   load.  mode 0: 16-byte cp.async copies by each of 256 threads and a
+ *   block barrier per stage; mode 2: the same with 512 threads; mode 1: TMA
  *   tile::gather4 (four 128-byte pieces of four rows per instruction, 128-
  *   byte swizzled; each 512-byte row read as 4 x 128 bytes) issued by one
- *   warp, with a full and an empty mbarrier per ring slot (bounded waits:
- *   sink = 2 if one gave up).  table: device, 16-byte aligned; idx: device
- *   int32, n_ctas * stages * 64 entries; sink as above.
+ *   warp of 256 threads, with a full and an empty mbarrier per ring slot
+ *   (bounded waits: sink = 2 if one gave up); mode 3: the same issued by
+ *   four warps; mode 4: by eight warps (384 threads).  table: device,
+ *   16-byte aligned; idx: device int32,
+ *   n_ctas * stages * 64 entries; sink as above.
  * Both return CSA_OK, CSA_ERR_INVALID_ARG (checked before any launch) or
  * CSA_ERR_CUDA; they are asynchronous on `stream`.
  * ---------------------------------------------------------------------- */

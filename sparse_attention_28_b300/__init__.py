@@ -577,16 +577,29 @@ def probe_stream_read(src, sink, ctas_per_sm: int = 2, in_flight: int = 4):
     _check(st, "csa_probe_stream_read")
 
 
-def probe_row_gather(table, idx, n_ctas: int, stages: int, ring: int, sink, tma: bool = False):
+def _gather_mode(tma: bool, wide: bool, issuers: int) -> int:
+    if not tma:
+        _need(issuers == 0, "issuers: TMA gathers only")
+        return 2 if wide else 0
+    n = issuers if issuers else (4 if wide else 1)
+    _need(n in (1, 4, 8), "issuers: 1, 4 or 8")
+    return {1: 1, 4: 3, 8: 4}[n]
+
+
+def probe_row_gather(table, idx, n_ctas: int, stages: int, ring: int, sink, tma: bool = False,
+                     wide: bool = False, issuers: int = 0):
     """Gather 512-byte rows of table (uint8 CUDA tensor [n_rows, 512]) into
     shared memory: CTA c reads idx[c * stages * 64: (c + 1) * stages * 64]
     (int32, 64 rows per stage) through a ring of `ring` 32 KB stages, with
-    16-byte cp.async copies, or TMA tile::gather4 when `tma`."""
+    16-byte cp.async copies by 256 threads (512 when `wide`), or TMA
+    tile::gather4 when `tma`, issued by `issuers` warps (1, 4 or 8; when 0:
+    four if `wide`, else one)."""
     _need(table.is_cuda and table.is_contiguous() and table.dim() == 2 and table.shape[1] == 512,
           "table: contiguous CUDA [n_rows, 512]")
     _cuda(idx, "idx", torch.int32)
     _need(idx.is_contiguous() and idx.numel() >= n_ctas * stages * 64, "idx: n_ctas * stages * 64")
     _cuda(sink, "sink", torch.float32)
     st = lib().csa_probe_row_gather(_p(table), table.shape[0], _p(idx), int(n_ctas), int(stages),
-                                    int(ring), int(bool(tma)), _p(sink), _stream(table.device))
+                                    int(ring), _gather_mode(tma, wide, issuers), _p(sink),
+                                    _stream(table.device))
     _check(st, "csa_probe_row_gather")

@@ -258,8 +258,10 @@ def test_probe_rejects():
     assert L.csa_probe_row_gather(FAKE, 0, FAKE, 1, 1, 2, 0, FAKE, None) == 1
     assert L.csa_probe_row_gather(FAKE, 100, FAKE, 0, 1, 2, 0, FAKE, None) == 1
     assert L.csa_probe_row_gather(FAKE, 100, FAKE, 1, 0, 2, 0, FAKE, None) == 1
+    assert L.csa_probe_row_gather(FAKE, 100, FAKE, 1, 65, 2, 0, FAKE, None) == 1  # index list cap
     assert L.csa_probe_row_gather(FAKE, 100, FAKE, 1, 1, 3, 0, FAKE, None) == 1
-    assert L.csa_probe_row_gather(FAKE, 100, FAKE, 1, 1, 2, 2, FAKE, None) == 1
+    assert L.csa_probe_row_gather(FAKE, 100, FAKE, 1, 1, 2, 5, FAKE, None) == 1
+    assert L.csa_probe_row_gather(FAKE, 100, FAKE, 1, 1, 2, -1, FAKE, None) == 1
     assert L.csa_probe_row_gather(FAKE, 1 << 31, FAKE, 1, 1, 2, 1, FAKE, None) == 1
 
 

@@ -26,19 +26,20 @@ def test_probe_stream_read_reads_every_vector(cuda_device):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("tma", [False, True])
+@pytest.mark.parametrize("tma,wide,issuers", [(False, False, 0), (False, True, 0), (True, False, 1),
+                                              (True, True, 4), (True, False, 8)])
 @pytest.mark.parametrize("ring", [2, 4, 6])
-def test_probe_row_gather_reads_the_indexed_rows(cuda_device, ring, tma):
+def test_probe_row_gather_reads_the_indexed_rows(cuda_device, ring, tma, wide, issuers):
     n_rows, ctas, stages = 1000, 3, 5
     table = torch.zeros((n_rows, 512), dtype=torch.uint8, device=DEV)
     idx = torch.randint(0, n_rows - 1, (ctas * stages * 64,), dtype=torch.int32, device=DEV)
     sink = torch.zeros(1, dtype=torch.float32, device=DEV)
-    csa.probe_row_gather(table, idx, ctas, stages, ring, sink, tma)
+    csa.probe_row_gather(table, idx, ctas, stages, ring, sink, tma, wide, issuers)
     torch.cuda.synchronize()
     assert sink.item() == 0.0
     # row n_rows-1 is read once (by CTA 1's first stage); it holds the constant
     idx[64 * stages] = n_rows - 1
     table[n_rows - 1, :4] = torch.tensor([0xB9, 0x79, 0x37, 0x9E], dtype=torch.uint8)
-    csa.probe_row_gather(table, idx, ctas, stages, ring, sink, tma)
+    csa.probe_row_gather(table, idx, ctas, stages, ring, sink, tma, wide, issuers)
     torch.cuda.synchronize()
     assert sink.item() == 1.0
