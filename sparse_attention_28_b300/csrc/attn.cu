@@ -644,60 +644,52 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* vsc = reinterpret_cast<const float*>(stg + kS8VS);
       const uint32_t off = st * kBlk;
       // Output chunks of 8 channels: 8 per row of K's non-RoPE channels
-      // (code * scale -> bf16), 16 per row of V (code -> f16, or a raw row's
-      // bf16 -> f16 in place).  The K chunks and the V chunks are separate
-      // loops, so that a warp's lanes take the same path; each thread loads
-      // all of a loop's codes first, then converts and stores them.
+      // (code * scale -> bf16) and of its RoPE channels (copied), 16 per row
+      // of V (code -> f16, or a raw row's bf16 -> f16 in place).  Each thread
+      // first loads every row code, scale and source chunk of its outputs,
+      // then converts and stores them (no shared-memory load between two
+      // stores); the K and V chunks are separate loops, so that a warp's
+      // lanes take the same path.
       constexpr int kPerK = (kStageKeys * 8 + NL - 1) / NL;
       constexpr int kPerV = (kStageKeys * 16 + NL - 1) / NL;
-      {
-        uint2 c8[kPerK];
-        float scv[kPerK];
+      int32_t cdk[kPerK], cdv[kPerV];
+      uint2 ck[kPerK], cv[kPerV];
+      float scv[kPerK];
+      uint4 rope[kPerK];
 #pragma unroll
-        for (int i = 0; i < kPerK; ++i) {
-          const int oc = lt + i * NL;
-          const int r = (oc >> 3) & (kStageKeys - 1), part = oc & 7;
-          c8[i] = *reinterpret_cast<const uint2*>(stg + kS8K + r * 64 + part * 8);
-          scv[i] = ksc[r];
-        }
+      for (int i = 0; i < kPerK; ++i) {
+        const int oc = lt + i * NL;
+        const int r = (oc >> 3) & (kStageKeys - 1), part = oc & 7;
+        cdk[i] = oc < kStageKeys * 8 ? codes[st * kStageKeys + r] : -1;
+        ck[i] = *reinterpret_cast<const uint2*>(stg + kS8K + r * 64 + part * 8);
+        scv[i] = ksc[r];
+        rope[i] = *reinterpret_cast<const uint4*>(stg + kS8R + tc::sw128_offset(r, part));
+      }
 #pragma unroll
-        for (int i = 0; i < kPerK; ++i) {
-          const int oc = lt + i * NL;
-          const int r = oc >> 3, part = oc & 7;
-          if (oc < kStageKeys * 8 && codes[st * kStageKeys + r] >= 0)
-            *reinterpret_cast<uint4*>(sm + C::kK0 + off + tc::sw128_offset(r, part)) =
-                dequant8(c8[i], scv[i]);
+      for (int i = 0; i < kPerV; ++i) {
+        const int oc = lt + i * NL;
+        const int r = (oc >> 4) & (kStageKeys - 1), v = oc & 15;
+        cdv[i] = oc < kStageKeys * 16 ? codes[st * kStageKeys + r] : -1;
+        cv[i] = *reinterpret_cast<const uint2*>(stg + kS8V + r * 128 + v * 8);
+      }
+#pragma unroll
+      for (int i = 0; i < kPerK; ++i) {
+        const int oc = lt + i * NL;
+        if (cdk[i] >= 0) {
+          const uint32_t o = off + tc::sw128_offset(oc >> 3, oc & 7);
+          *reinterpret_cast<uint4*>(sm + C::kK0 + o) = dequant8(ck[i], scv[i]);
+          *reinterpret_cast<uint4*>(sm + C::kK1 + o) = rope[i];  // same swizzled offsets
         }
       }
-      {
-        uint2 c8[kPerV];
 #pragma unroll
-        for (int i = 0; i < kPerV; ++i) {
-          const int oc = lt + i * NL;
-          const int r = (oc >> 4) & (kStageKeys - 1), v = oc & 15;
-          c8[i] = *reinterpret_cast<const uint2*>(stg + kS8V + r * 128 + v * 8);
-        }
-#pragma unroll
-        for (int i = 0; i < kPerV; ++i) {
-          const int oc = lt + i * NL;
-          const int r = oc >> 4, v = oc & 15;
-          if (oc >= kStageKeys * 16) break;
-          const int32_t cd = codes[st * kStageKeys + r];
-          uint4* d = reinterpret_cast<uint4*>(sm + C::kV0 + off + (v >> 3) * C::kRegion +
-                                              tc::sw128_offset(r, v & 7));
-          if (cd >= 0) *d = e4m3x8_to_f16x8(c8[i]);
-          else if (cd < -1) *d = bf16x8_to_f16x8(*d);
-        }
-      }
-      // K's RoPE channels of the compressed rows: same swizzled offsets
-#pragma unroll
-      for (int i = 0; i < (kStageKeys * 8 + NL - 1) / NL; ++i) {
-        const int ci = lt + i * NL;
-        if (ci < kStageKeys * 8 && codes[st * kStageKeys + (ci >> 3)] >= 0) {
-          const uint32_t o = tc::sw128_offset(ci >> 3, ci & 7);
-          *reinterpret_cast<uint4*>(sm + C::kK1 + off + o) =
-              *reinterpret_cast<const uint4*>(stg + kS8R + o);
-        }
+      for (int i = 0; i < kPerV; ++i) {
+        const int oc = lt + i * NL;
+        const int r = oc >> 4, v = oc & 15;
+        if (cdv[i] == -1) continue;  // skipped slot or past the stage
+        uint4* d = reinterpret_cast<uint4*>(sm + C::kV0 + off + (v >> 3) * C::kRegion +
+                                            tc::sw128_offset(r, v & 7));
+        if (cdv[i] >= 0) *d = e4m3x8_to_f16x8(cv[i]);
+        else *d = bf16x8_to_f16x8(*d);
       }
       // log2 of the key's V scale (0 for raw rows, skipped slots and zero scales)
       if (lt < kStageKeys) {
